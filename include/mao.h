@@ -1,0 +1,166 @@
+/*
+ * mao.h — C ABI of the GB300 (sm_103a) Muon / Sign-Muon optimizer step.
+ *
+ * One optimizer step, for one weight matrix or a batch of them, is
+ *
+ *   momentum      M <- mu*M + G                                  muon_momentum_update
+ *   polar factor  U ~ polar(M) by Newton–Schulz                   ns_orthogonalize
+ *   sign + pack   S = sign(U), one bit per entry                  sign_pack_bits (or fused
+ *                                                                 into ns_orthogonalize)
+ *   vote          S_bar = sign(sum_m S^(m)) over W_n workers      majority_vote_packed
+ *   update        W <- W - eta*S_bar  (Sign-Muon)                 apply_update
+ *                 W <- W - eta*U      (Muon)
+ *
+ * Sources, cited by page title and section:
+ *   [SignMuon] "Resumo Técnico: SignMuon: Otimização Distribuída de Muon com Eficiência de
+ *              Comunicação" (gist.science, paper 2605.16311), §2 "Metodologia: Sign-Muon".
+ *   [Megatron] "NVIDIA MegatronによるLLM学習高速化へ向けた新世代オプティマイザの高度化"
+ *              (news.ainew.jp), sections "分散ニュートン・シュルツ" and "SYRK と融合された all-reduce".
+ *   [Dion]     "대규모 AI 모델 학습을 10배 빠르게: Dion 옵티마이저를 사용한 분산 학습"
+ *              (dsdanielpark.github.io), ablation section (heavy-ball momentum form).
+ *
+ * Conventions shared by every call
+ *   - Matrices are row-major: element (i, j) of a mao_mat lives at data + (i*ld + j)*elem_size.
+ *     data is a DEVICE pointer, aligned to the element size (16-byte alignment with ld a
+ *     multiple of 8 selects the vectorised paths; other layouts take element-wise paths).
+ *   - Descriptor arrays (const mao_mat*, pointer arrays) are HOST arrays of `batch` entries,
+ *     read during the call only. The caller owns all memory; the library allocates none.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream). Every call only enqueues
+ *     work on it and returns; results are ready when the stream reaches that point.
+ *   - Argument errors are reported synchronously and enqueue nothing. A failed launch
+ *     returns MAO_ERR_CUDA. A device-side wait that ran out of time (MAO_ERR_TIMEOUT) is
+ *     reported by mao_sync_status().
+ *   - No C++ exception crosses this boundary. Calls are thread-safe per stream.
+ *   - Packed sign buffers: entry k of the row-major R x C matrix (k = i*C + j, original
+ *     orientation) is bit k%32 of uint32 word k/32, least significant bit first; bit 1
+ *     encodes +1 and bit 0 encodes -1 (u < 0). ceil(R*C/32) words; padding bits are 0.
+ */
+#ifndef MAO_H
+#define MAO_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum mao_status {
+  MAO_OK = 0,
+  MAO_ERR_INVALID_ARG = 1,  /* null pointer, bad size, bad enum */
+  MAO_ERR_UNSUPPORTED = 2,  /* valid request this build cannot serve (device, limits) */
+  MAO_ERR_MISALIGNED = 3,   /* pointer not aligned to its element size / workspace to 256 B */
+  MAO_ERR_WORKSPACE = 4,    /* workspace smaller than ns_workspace_bytes() */
+  MAO_ERR_CUDA = 5,         /* a CUDA runtime call or launch failed */
+  MAO_ERR_TIMEOUT = 6       /* a device-side wait gave up (reported by mao_sync_status) */
+} mao_status;
+
+typedef enum mao_dtype { MAO_F32 = 0, MAO_BF16 = 1 } mao_dtype;
+
+typedef struct mao_mat {
+  void* data;     /* device pointer, row-major */
+  int64_t rows;   /* R >= 1 */
+  int64_t cols;   /* C >= 1 */
+  int64_t ld;     /* elements between consecutive row starts, ld >= cols */
+  int32_t dtype;  /* mao_dtype */
+  int32_t reserved; /* must be 0 */
+} mao_mat;
+
+/* Version of this ABI (bumped on any incompatible change). */
+int32_t mao_abi_version(void);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* mao_status_string(mao_status status);
+
+/*
+ * Momentum of each worker / matrix ([SignMuon] §2 "Fluxo Algorítmico", step 1: each worker
+ * updates its local momentum; the form M <- mu*M + G is the heavy-ball form of the [Dion]
+ * ablation section).
+ *   M[b]  in/out, f32 or bf16; G[b] in, f32 or bf16, same rows/cols as M[b].
+ *   Per element: m = fmaf(mu, m, g) in fp32, then round-to-nearest-even to M's dtype.
+ *   batch >= 1 matrices of any shapes. M and G must not overlap.
+ */
+mao_status muon_momentum_update(const mao_mat* M, const mao_mat* G, int32_t batch, float mu,
+                                void* stream);
+
+/*
+ * Bytes of device workspace ns_orthogonalize needs for this batch (its descriptors' shapes
+ * and the compute dtype; pointers are not read). Returns 0 for invalid arguments.
+ */
+size_t ns_workspace_bytes(const mao_mat* X, int32_t batch, int32_t compute_dtype);
+
+/*
+ * Newton–Schulz orthogonalisation toward the polar factor ([SignMuon] §2 "Mecanismo Central"
+ * item 1; three matrix products per iteration as [Megatron] "分散ニュートン・シュルツ" counts them;
+ * the first two are symmetric rank-k products as in [Megatron] "SYRK と融合された all-reduce").
+ *
+ * For each matrix (m = min(R,C), X taken as in[b] or its transpose so that X is m x n):
+ *   X_0 = X / (||X||_F + eps)
+ *   for k in 0..steps-1:  A = X X^T;  B = b_k A + c_k A A;  X = a_k X + B X
+ *   U = X (transposed back when R > C; no transposed copy is ever materialised).
+ *
+ *   in[b]        f32 or bf16 input (the momentum); read only.
+ *   out[b]       f32 or bf16 output U, same rows/cols as in[b]; out[b].data may be NULL when
+ *                sign_bits is given (signs only). out may alias in (in-place).
+ *   steps        1..64 iterations.
+ *   coeffs       HOST array of (a, b, c) triples: 3 floats when coeff_stride == 0 (same
+ *                triple every iteration) or steps*3 floats when coeff_stride == 3.
+ *   eps          added to the Frobenius norm (1e-7 is the usual value).
+ *   compute      MAO_BF16: operands stored in bf16, products on tcgen05 tensor cores with
+ *                fp32 accumulation and fp32 epilogue arithmetic;
+ *                MAO_F32: fp32 storage and fp32 FFMA products (accuracy path).
+ *   sign_bits    NULL, or HOST array of `batch` device pointers (each may be NULL): the
+ *                packed signs of the final U (layout in the header comment), written by the
+ *                last product's epilogue from the fp32 value before any output rounding.
+ *   workspace    device buffer of >= ns_workspace_bytes(in, batch, compute) bytes, 256-byte
+ *                aligned; clobbered. Calls sharing a workspace must be stream-ordered.
+ */
+mao_status ns_orthogonalize(const mao_mat* in, const mao_mat* out, int32_t batch, int32_t steps,
+                            const float* coeffs, int32_t coeff_stride, float eps,
+                            int32_t compute, uint32_t* const* sign_bits, void* workspace,
+                            size_t workspace_bytes, void* stream);
+
+/*
+ * Entrywise sign and 1-bit packing ([SignMuon] §2 step 2 "Extração de Sinal" and step 3,
+ * all-gather variant: one bit per entry).
+ *   U     f32 or bf16 matrix (read). bits: device array of ceil(R*C/32) words (written).
+ *   sign(u) = -1 (bit 0) if u < 0, else +1 (bit 1): +0, -0 and NaN give +1.
+ */
+mao_status sign_pack_bits(const mao_mat* U, uint32_t* bits, void* stream);
+
+/*
+ * Majority vote over W_n workers' packed sign buffers ([SignMuon] §2 step 4: the vote
+ * S_bar = sign(sum_m S^(m)) computed locally after the all-gather of packed buffers).
+ *   bits           device, worker m's words start at bits + m*worker_stride_words
+ *                  (the all-gather result layout; worker_stride_words >= ceil(nbits/32)).
+ *   n_workers      1..65535.   nbits  entries per worker (>= 1).
+ *   vote           device, ceil(nbits/32) words written: bit = 1 where the number of +1
+ *                  signs is >= the number of -1 signs (a tie gives +1); padding bits 0.
+ */
+mao_status majority_vote_packed(const uint32_t* bits, int32_t n_workers,
+                                int64_t worker_stride_words, int64_t nbits, uint32_t* vote,
+                                void* stream);
+
+/*
+ * Parameter update ([SignMuon] §2 step 4: W_{t+1} = W_t - eta_t * S_bar_t).
+ *   W[b]     in/out, f32 or bf16.
+ *   Exactly one of:
+ *     vote   HOST array of `batch` device pointers to packed signs of W[b]'s shape
+ *            (Sign-Muon: D = +1 for bit 1, -1 for bit 0);
+ *     U      HOST array of `batch` matrices of W[b]'s shape, f32 or bf16 (Muon: D = U).
+ *   Per element: w = fmaf(-lr, d, w) in fp32, then round-to-nearest-even to W's dtype.
+ */
+mao_status apply_update(const mao_mat* W, const uint32_t* const* vote, const mao_mat* U,
+                        int32_t batch, float lr, void* stream);
+
+/*
+ * Synchronise `stream`, then read and clear the device-side error word that kernels set
+ * when a bounded wait gives up. Returns MAO_OK, MAO_ERR_TIMEOUT or MAO_ERR_CUDA.
+ */
+mao_status mao_sync_status(void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MAO_H */

@@ -1,0 +1,165 @@
+"""GB300 (sm_103a) Muon / Sign-Muon optimizer step behind a C ABI (libmao.so).
+
+This module only marshals PyTorch CUDA tensors into the C ABI of include/mao.h;
+every stage of the step runs in the library's CUDA kernels. There is no CPU or
+PyTorch fallback: if libmao.so is missing, the calls raise.
+
+Functions (same names as the C ABI):
+  muon_momentum_update(M, G, mu)                     M <- mu*M + G
+  ns_workspace_bytes(X, compute)                     workspace size for ns_orthogonalize
+  ns_orthogonalize(inp, out, steps, coeffs, ...)     Newton–Schulz polar factor (+ packed signs)
+  sign_pack_bits(U, bits)                            sign + 1-bit pack
+  majority_vote_packed(bits, nbits, vote)            vote over workers' packed signs
+  apply_update(W, lr, vote=..., U=...)               W <- W - lr*D
+  sync_status()                                      stream sync + device error word
+"""
+
+import ctypes
+
+import torch
+
+from . import _abi
+from ._abi import MaoError  # noqa: F401
+
+# Default Newton–Schulz coefficients (a, b, c): the quintic used by Muon.
+QUINTIC = (3.4445, -4.7750, 2.0315)
+
+_DT = {torch.float32: _abi.MAO_F32, torch.bfloat16: _abi.MAO_BF16}
+_COMPUTE = {"f32": _abi.MAO_F32, "bf16": _abi.MAO_BF16,
+            torch.float32: _abi.MAO_F32, torch.bfloat16: _abi.MAO_BF16}
+
+
+def lib():
+    return _abi.load()
+
+
+def _as_list(x):
+    if x is None:
+        return None
+    return list(x) if isinstance(x, (list, tuple)) else [x]
+
+
+def _mat(t, allow_none=False, like=None):
+    if t is None:
+        if not allow_none:
+            raise ValueError("tensor required")
+        return _abi.MaoMat(None, like.shape[0], like.shape[1], like.shape[1], _abi.MAO_F32, 0)
+    if not t.is_cuda:
+        raise ValueError("expected a CUDA tensor")
+    if t.dim() != 2 or t.stride(1) != 1:
+        raise ValueError("expected a 2-D tensor with unit column stride")
+    if t.dtype not in _DT:
+        raise ValueError("dtype must be float32 or bfloat16")
+    return _abi.MaoMat(t.data_ptr(), t.shape[0], t.shape[1], max(t.stride(0), t.shape[1]),
+                       _DT[t.dtype], 0)
+
+
+def _mats(ts, allow_none=False, like=None):
+    arr = (_abi.MaoMat * len(ts))()
+    for i, t in enumerate(ts):
+        arr[i] = _mat(t, allow_none, like[i] if like is not None else None)
+    return arr
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def muon_momentum_update(M, G, mu, stream=None):
+    """M <- mu*M + G for each (M, G) pair (one fp32 FMA per element, rounded to M's dtype)."""
+    Ms, Gs = _as_list(M), _as_list(G)
+    st = lib().muon_momentum_update(_mats(Ms), _mats(Gs), len(Ms), float(mu), _stream(stream))
+    _abi.check("muon_momentum_update", st)
+
+
+def ns_workspace_bytes(X, compute="bf16"):
+    Xs = _as_list(X)
+    arr = (_abi.MaoMat * len(Xs))()
+    for i, x in enumerate(Xs):
+        shape = x.shape if hasattr(x, "shape") else x
+        arr[i] = _abi.MaoMat(None, shape[0], shape[1], shape[1], _abi.MAO_F32, 0)
+    n = lib().ns_workspace_bytes(arr, len(Xs), _COMPUTE[compute])
+    if n == 0:
+        raise ValueError("invalid shapes for ns_workspace_bytes")
+    return int(n)
+
+
+def workspace(X, compute="bf16", device=None):
+    """A device buffer of ns_workspace_bytes(X) bytes (256-byte aligned by the allocator)."""
+    n = ns_workspace_bytes(X, compute)
+    dev = device if device is not None else torch.device("cuda")
+    return torch.empty(n, dtype=torch.uint8, device=dev)
+
+
+def ns_orthogonalize(inp, out, steps=5, coeffs=QUINTIC, eps=1e-7, compute="bf16",
+                     sign_bits=None, ws=None, stream=None):
+    """Newton–Schulz orthogonalisation of each input into out (and/or packed signs).
+
+    coeffs: one (a, b, c) triple for every step, or a list of `steps` triples.
+    out entries may be None when sign_bits (int32 tensors of ceil(R*C/32) words) are given.
+    """
+    ins = _as_list(inp)
+    outs = _as_list(out) if out is not None else [None] * len(ins)
+    co = list(coeffs)
+    if len(co) == 3 and not isinstance(co[0], (list, tuple)):
+        flat, stride = [float(c) for c in co], 0
+    else:
+        if len(co) != steps:
+            raise ValueError("need one coefficient triple per step")
+        flat, stride = [float(c) for t in co for c in t], 3
+    carr = (ctypes.c_float * len(flat))(*flat)
+    bits = _as_list(sign_bits)
+    barr = None
+    if bits is not None:
+        barr = (ctypes.c_void_p * len(bits))(*[b.data_ptr() if b is not None else None for b in bits])
+    if ws is None:
+        ws = workspace(ins, compute, ins[0].device)
+    st = lib().ns_orthogonalize(
+        _mats(ins), _mats(outs, allow_none=True, like=ins), len(ins), int(steps), carr, stride,
+        float(eps), _COMPUTE[compute], barr, ctypes.c_void_p(ws.data_ptr()), ws.numel(),
+        _stream(stream))
+    _abi.check("ns_orthogonalize", st)
+
+
+def packed_words(rows, cols):
+    return (rows * cols + 31) // 32
+
+
+def sign_pack_bits(U, bits=None, stream=None):
+    if bits is None:
+        bits = torch.empty(packed_words(*U.shape), dtype=torch.int32, device=U.device)
+    st = lib().sign_pack_bits(ctypes.byref(_mat(U)), ctypes.c_void_p(bits.data_ptr()), _stream(stream))
+    _abi.check("sign_pack_bits", st)
+    return bits
+
+
+def majority_vote_packed(bits, nbits, vote=None, stream=None):
+    """bits: int32 tensor [W_n][stride] of packed worker signs; returns the packed vote."""
+    if bits.dim() != 2 or bits.stride(1) != 1:
+        raise ValueError("bits must be [n_workers][stride] with unit stride")
+    if vote is None:
+        vote = torch.empty((nbits + 31) // 32, dtype=torch.int32, device=bits.device)
+    st = lib().majority_vote_packed(ctypes.c_void_p(bits.data_ptr()), bits.shape[0], bits.stride(0),
+                                    int(nbits), ctypes.c_void_p(vote.data_ptr()), _stream(stream))
+    _abi.check("majority_vote_packed", st)
+    return vote
+
+
+def apply_update(W, lr, vote=None, U=None, stream=None):
+    """W <- W - lr*D with D the packed vote (+1/-1) or the matrix U."""
+    Ws = _as_list(W)
+    varr = None
+    uarr = None
+    if vote is not None:
+        vs = _as_list(vote)
+        varr = (ctypes.c_void_p * len(vs))(*[v.data_ptr() for v in vs])
+    if U is not None:
+        uarr = _mats(_as_list(U))
+    st = lib().apply_update(_mats(Ws), varr, uarr, len(Ws), float(lr), _stream(stream))
+    _abi.check("apply_update", st)
+
+
+def sync_status(stream=None):
+    st = lib().mao_sync_status(_stream(stream))
+    _abi.check("mao_sync_status", st)

@@ -1,0 +1,158 @@
+// C ABI entry points: argument validation (synchronous, nothing enqueued on error) and
+// dispatch to the launchers. No exception crosses this boundary.
+#include <cmath>
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace mao {
+
+namespace {
+constexpr int kMaxDevices = 64;
+int g_sms[kMaxDevices];
+int g_cc[kMaxDevices];
+std::once_flag g_dev_once[kMaxDevices];
+
+void query_device(int dev) {
+  std::call_once(g_dev_once[dev], [dev] {
+    int sms = 0, major = 0, minor = 0;
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    g_sms[dev] = sms > 0 ? sms : 1;
+    g_cc[dev] = major * 10 + minor;
+  });
+}
+
+int current_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+  return dev;
+}
+}  // namespace
+
+int num_sms() {
+  const int d = current_device();
+  query_device(d);
+  return g_sms[d];
+}
+
+int device_cc() {
+  const int d = current_device();
+  query_device(d);
+  return g_cc[d];
+}
+
+}  // namespace mao
+
+using namespace mao;
+
+extern "C" {
+
+int32_t mao_abi_version(void) { return 1; }
+
+const char* mao_status_string(mao_status s) {
+  switch (s) {
+    case MAO_OK: return "MAO_OK";
+    case MAO_ERR_INVALID_ARG: return "MAO_ERR_INVALID_ARG";
+    case MAO_ERR_UNSUPPORTED: return "MAO_ERR_UNSUPPORTED";
+    case MAO_ERR_MISALIGNED: return "MAO_ERR_MISALIGNED";
+    case MAO_ERR_WORKSPACE: return "MAO_ERR_WORKSPACE";
+    case MAO_ERR_CUDA: return "MAO_ERR_CUDA";
+    case MAO_ERR_TIMEOUT: return "MAO_ERR_TIMEOUT";
+  }
+  return "MAO_ERR_UNKNOWN";
+}
+
+mao_status muon_momentum_update(const mao_mat* M, const mao_mat* G, int32_t batch, float mu,
+                                void* stream) {
+  if (!M || !G || batch < 1 || !std::isfinite(mu)) return MAO_ERR_INVALID_ARG;
+  for (int b = 0; b < batch; ++b) {
+    mao_status st = check_mat(M[b]);
+    if (st == MAO_OK) st = check_mat(G[b]);
+    if (st != MAO_OK) return st;
+    if (M[b].rows != G[b].rows || M[b].cols != G[b].cols) return MAO_ERR_INVALID_ARG;
+  }
+  return momentum_launch(M, G, batch, mu, static_cast<cudaStream_t>(stream));
+}
+
+size_t ns_workspace_bytes(const mao_mat* X, int32_t batch, int32_t compute) {
+  if (!X || batch < 1 || !valid_dtype(compute)) return 0;
+  for (int b = 0; b < batch; ++b) {
+    if (X[b].rows < 1 || X[b].cols < 1 || X[b].rows > (int64_t(1) << 31) ||
+        X[b].cols > (int64_t(1) << 31))
+      return 0;
+  }
+  return ns_workspace_size(X, batch, compute);
+}
+
+mao_status ns_orthogonalize(const mao_mat* in, const mao_mat* out, int32_t batch, int32_t steps,
+                            const float* coeffs, int32_t coeff_stride, float eps,
+                            int32_t compute, uint32_t* const* sign_bits, void* workspace,
+                            size_t workspace_bytes, void* stream) {
+  if (!in || !out || batch < 1 || steps < 1 || steps > 64 || !coeffs) return MAO_ERR_INVALID_ARG;
+  if (coeff_stride != 0 && coeff_stride != 3) return MAO_ERR_INVALID_ARG;
+  if (!valid_dtype(compute) || !std::isfinite(eps) || eps < 0.0f) return MAO_ERR_INVALID_ARG;
+  for (int i = 0; i < (coeff_stride ? 3 * steps : 3); ++i)
+    if (!std::isfinite(coeffs[i])) return MAO_ERR_INVALID_ARG;
+  for (int b = 0; b < batch; ++b) {
+    mao_status st = check_mat(in[b]);
+    if (st != MAO_OK) return st;
+    const bool bits = sign_bits && sign_bits[b];
+    st = check_mat(out[b], bits);
+    if (st != MAO_OK) return st;
+    if (out[b].rows != in[b].rows || out[b].cols != in[b].cols) return MAO_ERR_INVALID_ARG;
+    if (bits && (reinterpret_cast<uintptr_t>(sign_bits[b]) % 4 != 0)) return MAO_ERR_MISALIGNED;
+  }
+  if (!workspace) return MAO_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0) return MAO_ERR_MISALIGNED;
+  if (compute == MAO_BF16 && device_cc() / 10 != 10) return MAO_ERR_UNSUPPORTED;
+  if (workspace_bytes < ns_workspace_size(in, batch, compute)) return MAO_ERR_WORKSPACE;
+  return ns_run(in, out, batch, steps, coeffs, coeff_stride, eps, compute, sign_bits, workspace,
+                workspace_bytes, static_cast<cudaStream_t>(stream));
+}
+
+mao_status sign_pack_bits(const mao_mat* U, uint32_t* bits, void* stream) {
+  if (!U || !bits) return MAO_ERR_INVALID_ARG;
+  const mao_status st = check_mat(*U);
+  if (st != MAO_OK) return st;
+  if (reinterpret_cast<uintptr_t>(bits) % 4 != 0) return MAO_ERR_MISALIGNED;
+  return sign_pack_launch(*U, bits, static_cast<cudaStream_t>(stream));
+}
+
+mao_status majority_vote_packed(const uint32_t* bits, int32_t n_workers,
+                                int64_t worker_stride_words, int64_t nbits, uint32_t* vote,
+                                void* stream) {
+  if (!bits || !vote || n_workers < 1 || n_workers > 65535 || nbits < 1) return MAO_ERR_INVALID_ARG;
+  if (worker_stride_words < ceil_div(nbits, 32)) return MAO_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(bits) % 4 != 0 || reinterpret_cast<uintptr_t>(vote) % 4 != 0)
+    return MAO_ERR_MISALIGNED;
+  return vote_launch(bits, n_workers, worker_stride_words, nbits, vote,
+                     static_cast<cudaStream_t>(stream));
+}
+
+mao_status apply_update(const mao_mat* W, const uint32_t* const* vote, const mao_mat* U,
+                        int32_t batch, float lr, void* stream) {
+  if (!W || batch < 1 || !std::isfinite(lr)) return MAO_ERR_INVALID_ARG;
+  if ((vote == nullptr) == (U == nullptr)) return MAO_ERR_INVALID_ARG;
+  for (int b = 0; b < batch; ++b) {
+    mao_status st = check_mat(W[b]);
+    if (st != MAO_OK) return st;
+    if (vote) {
+      if (!vote[b]) return MAO_ERR_INVALID_ARG;
+      if (reinterpret_cast<uintptr_t>(vote[b]) % 4 != 0) return MAO_ERR_MISALIGNED;
+    } else {
+      st = check_mat(U[b]);
+      if (st != MAO_OK) return st;
+      if (U[b].rows != W[b].rows || U[b].cols != W[b].cols) return MAO_ERR_INVALID_ARG;
+    }
+  }
+  return update_launch(W, vote, U, batch, lr, static_cast<cudaStream_t>(stream));
+}
+
+mao_status mao_sync_status(void* stream) {
+  return tc_read_and_clear_error(static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,327 @@
+// HBM-bound stages of the optimizer step: momentum, sign + 1-bit pack, majority vote and
+// parameter update. All are grouped (one launch covers a batch of matrices of any shapes)
+// and move 16 bytes per access where the layout allows it.
+#include <algorithm>
+#include <vector>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace mao {
+namespace {
+
+constexpr int kEwThreads = 256;
+constexpr int kEwUnitsPerThread = 4;  // 8 elements per unit
+constexpr int kEwUnitsPerBlock = kEwThreads * kEwUnitsPerThread;
+constexpr int kEwMax = 96;            // matrices per launch (kernel-parameter table)
+
+enum EwMode : int32_t { EW_MOMENTUM = 0, EW_UPDATE_U = 1, EW_UPDATE_VOTE = 2 };
+
+struct EwEntry {
+  void* a;            // in/out: M (momentum) or W (update)
+  const void* b;      // G, U, or packed vote words
+  int64_t rows, cols, lda, ldb;
+  int64_t units;      // 8-element work units
+  int64_t units_per_row;
+  int64_t block_begin;
+  int32_t dta, dtb;
+  int32_t vec;        // 16-byte accesses allowed on a and b
+  int32_t flat;       // both contiguous: treated as one row of rows*cols elements
+};
+
+struct EwParams {
+  EwEntry e[kEwMax];
+  int32_t n;
+  int32_t mode;
+  float scalar;       // mu (momentum) or lr (update)
+};
+
+__device__ __forceinline__ int find_entry(const EwParams& p, int64_t block) {
+  int lo = 0, hi = p.n - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (p.e[mid].block_begin <= block) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+// The per-element arithmetic of each mode, in fp32 with one fused multiply-add.
+__device__ __forceinline__ float ew_op(int32_t mode, float s, float a, float b) {
+  // momentum: fmaf(mu, m, g); update: fmaf(-lr, d, w)
+  return mode == EW_MOMENTUM ? __fmaf_rn(s, a, b) : __fmaf_rn(-s, b, a);
+}
+
+__global__ void __launch_bounds__(kEwThreads) ew_kernel(const __grid_constant__ EwParams p) {
+  const int ei = find_entry(p, blockIdx.x);
+  const EwEntry& e = p.e[ei];
+  const int64_t u_begin = (int64_t(blockIdx.x) - e.block_begin) * kEwUnitsPerBlock;
+  const uint32_t* vote = reinterpret_cast<const uint32_t*>(e.b);
+#pragma unroll 1
+  for (int t = 0; t < kEwUnitsPerThread; ++t) {
+    const int64_t u = u_begin + t * kEwThreads + threadIdx.x;
+    if (u >= e.units) break;
+    int64_t row, col0, ncols_row;
+    if (e.flat) { row = 0; col0 = u * 8; ncols_row = e.rows * e.cols; }
+    else { row = u / e.units_per_row; col0 = (u - row * e.units_per_row) * 8; ncols_row = e.cols; }
+    const int valid = int(ncols_row - col0 < 8 ? ncols_row - col0 : 8);
+    const int64_t ia = e.flat ? col0 : row * e.lda + col0;
+    const int64_t ib = e.flat ? col0 : row * e.ldb + col0;
+    const int64_t k0 = e.flat ? col0 : row * e.cols + col0;  // row-major bit index
+    float va[8], vb[8];
+    if (e.vec && valid == 8) {
+      load8(e.a, ia, e.dta, va);
+      if (p.mode == EW_UPDATE_VOTE) {
+        if ((k0 & 7) == 0) {
+          const uint32_t w = vote[k0 >> 5] >> (k0 & 31);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) vb[i] = ((w >> i) & 1u) ? 1.0f : -1.0f;
+        } else {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int64_t k = k0 + i;
+            vb[i] = ((vote[k >> 5] >> (k & 31)) & 1u) ? 1.0f : -1.0f;
+          }
+        }
+      } else {
+        load8(e.b, ib, e.dtb, vb);
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) va[i] = ew_op(p.mode, p.scalar, va[i], vb[i]);
+      store8(e.a, ia, e.dta, va);
+    } else {
+      for (int i = 0; i < valid; ++i) {
+        const float x = load_elem(e.a, ia + i, e.dta);
+        float y;
+        if (p.mode == EW_UPDATE_VOTE) {
+          const int64_t k = k0 + i;
+          y = ((vote[k >> 5] >> (k & 31)) & 1u) ? 1.0f : -1.0f;
+        } else {
+          y = load_elem(e.b, ib + i, e.dtb);
+        }
+        store_elem(e.a, ia + i, e.dta, ew_op(p.mode, p.scalar, x, y));
+      }
+    }
+  }
+}
+
+// Fills one entry of the grouped table; returns its number of blocks.
+int64_t make_entry(EwEntry& e, const mao_mat& A, const mao_mat* B, const void* bptr,
+                   int32_t dtb, int64_t ldb) {
+  e.a = A.data;
+  e.b = bptr;
+  e.rows = A.rows;
+  e.cols = A.cols;
+  e.lda = A.ld;
+  e.ldb = ldb;
+  e.dta = A.dtype;
+  e.dtb = dtb;
+  const bool contig_a = A.ld == A.cols || A.rows == 1;
+  const bool contig_b = B ? (B->ld == B->cols || B->rows == 1) : true;
+  e.flat = (contig_a && contig_b) ? 1 : 0;
+  bool vec = (reinterpret_cast<uintptr_t>(A.data) % 16 == 0);
+  if (B) vec = vec && (reinterpret_cast<uintptr_t>(B->data) % 16 == 0);
+  if (!e.flat) {
+    vec = vec && (A.cols % 8 == 0) && ((A.ld * elem_size(A.dtype)) % 16 == 0);
+    if (B) vec = vec && ((B->ld * elem_size(B->dtype)) % 16 == 0);
+  }
+  e.vec = vec ? 1 : 0;
+  if (e.flat) {
+    e.units_per_row = ceil_div(A.rows * A.cols, 8);
+    e.units = e.units_per_row;
+  } else {
+    e.units_per_row = ceil_div(A.cols, 8);
+    e.units = e.units_per_row * A.rows;
+  }
+  return ceil_div(e.units, kEwUnitsPerBlock);
+}
+
+mao_status launch_grouped(std::vector<EwEntry>& entries, int32_t mode, float scalar,
+                          cudaStream_t stream) {
+  size_t pos = 0;
+  while (pos < entries.size()) {
+    EwParams p;
+    p.mode = mode;
+    p.scalar = scalar;
+    p.n = 0;
+    int64_t blocks = 0;
+    while (pos < entries.size() && p.n < kEwMax) {
+      EwEntry e = entries[pos++];
+      if (e.units == 0) continue;
+      e.block_begin = blocks;
+      blocks += ceil_div(e.units, kEwUnitsPerBlock);
+      p.e[p.n++] = e;
+    }
+    if (p.n == 0) continue;
+    if (blocks > 0x7FFFFFFF) return MAO_ERR_UNSUPPORTED;
+    ew_kernel<<<unsigned(blocks), kEwThreads, 0, stream>>>(p);
+    if (cudaGetLastError() != cudaSuccess) return MAO_ERR_CUDA;
+  }
+  return MAO_OK;
+}
+
+// ----------------------------------------------------------------- sign + pack
+
+// One thread per 32-bit word: entries k = 32w .. 32w+31 of the row-major matrix.
+__global__ void __launch_bounds__(256) sign_pack_kernel(const void* u, int64_t rows, int64_t cols,
+                                                        int64_t ld, int32_t dt, int32_t vec,
+                                                        uint32_t* bits, int64_t nwords) {
+  const int64_t w = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (w >= nwords) return;
+  const int64_t k0 = w * 32;
+  uint32_t word = 0;
+  if (vec) {  // cols % 32 == 0: the word lies inside one row, 16-byte aligned
+    const int64_t row = k0 / cols, col0 = k0 - row * cols;
+    const int64_t base = row * ld + col0;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      float v[8];
+      load8(u, base + 8 * q, dt, v);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) word |= (v[i] < 0.0f ? 0u : 1u) << (8 * q + i);
+    }
+  } else {
+    const int64_t n = rows * cols;
+    for (int i = 0; i < 32; ++i) {
+      const int64_t k = k0 + i;
+      if (k >= n) break;
+      const int64_t row = k / cols, col = k - row * cols;
+      const float v = load_elem(u, row * ld + col, dt);
+      word |= (v < 0.0f ? 0u : 1u) << i;
+    }
+  }
+  bits[w] = word;
+}
+
+// --------------------------------------------------------------- majority vote
+
+constexpr int kMaxPlanes = 16;  // counts up to 65535 workers
+
+// Adds one 32-lane word of bits into a bit-sliced binary counter (plane p holds bit p of
+// every lane's count): a ripple of half adders, three logic ops per plane.
+__device__ __forceinline__ void counter_add(uint32_t (&plane)[kMaxPlanes], int P, uint32_t x) {
+  uint32_t carry = x;
+#pragma unroll
+  for (int p = 0; p < kMaxPlanes; ++p) {
+    if (p < P) {
+      const uint32_t t = plane[p] & carry;
+      plane[p] ^= carry;
+      carry = t;
+    }
+  }
+}
+
+// Lanes whose count is >= T, by comparing the bit-sliced count with T from the top bit.
+__device__ __forceinline__ uint32_t counter_ge(const uint32_t (&plane)[kMaxPlanes], int P,
+                                               uint32_t T) {
+  uint32_t gt = 0, eq = 0xFFFFFFFFu;
+#pragma unroll
+  for (int p = kMaxPlanes - 1; p >= 0; --p) {
+    if (p < P) {
+      if ((T >> p) & 1u) {
+        eq &= plane[p];
+      } else {
+        gt |= eq & plane[p];
+        eq &= ~plane[p];
+      }
+    }
+  }
+  return gt | eq;
+}
+
+template <int V>
+__global__ void __launch_bounds__(256) vote_kernel(const uint32_t* __restrict__ bits, int32_t nw,
+                                                   int64_t stride, int64_t nwords, int64_t nbits,
+                                                   int64_t total_words, uint32_t* __restrict__ vote,
+                                                   int P, uint32_t T) {
+  const int64_t w0 = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) * V;
+  if (w0 >= nwords) return;
+  uint32_t plane[V][kMaxPlanes];
+#pragma unroll
+  for (int v = 0; v < V; ++v)
+#pragma unroll
+    for (int p = 0; p < kMaxPlanes; ++p) plane[v][p] = 0;
+  for (int m = 0; m < nw; ++m) {
+    const uint32_t* src = bits + int64_t(m) * stride + w0;
+    if (V == 4) {
+      const uint4 x = __ldg(reinterpret_cast<const uint4*>(src));
+      counter_add(plane[0], P, x.x);
+      counter_add(plane[V > 1 ? 1 : 0], P, x.y);
+      counter_add(plane[V > 2 ? 2 : 0], P, x.z);
+      counter_add(plane[V > 3 ? 3 : 0], P, x.w);
+    } else {
+      counter_add(plane[0], P, __ldg(src));
+    }
+  }
+  uint32_t out[V];
+#pragma unroll
+  for (int v = 0; v < V; ++v) {
+    out[v] = counter_ge(plane[v], P, T);
+    const int64_t w = w0 + v;
+    if (w == total_words - 1 && (nbits & 31)) out[v] &= (1u << (nbits & 31)) - 1u;
+  }
+  if (V == 4) {
+    *reinterpret_cast<uint4*>(vote + w0) = make_uint4(out[0], out[V > 1 ? 1 : 0],
+                                                      out[V > 2 ? 2 : 0], out[V > 3 ? 3 : 0]);
+  } else {
+    vote[w0] = out[0];
+  }
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------- entry points
+
+mao_status momentum_launch(const mao_mat* M, const mao_mat* G, int32_t batch, float mu,
+                           cudaStream_t stream) {
+  std::vector<EwEntry> entries(batch);
+  for (int i = 0; i < batch; ++i) make_entry(entries[i], M[i], &G[i], G[i].data, G[i].dtype, G[i].ld);
+  return launch_grouped(entries, EW_MOMENTUM, mu, stream);
+}
+
+mao_status update_launch(const mao_mat* W, const uint32_t* const* vote, const mao_mat* U,
+                         int32_t batch, float lr, cudaStream_t stream) {
+  std::vector<EwEntry> entries(batch);
+  for (int i = 0; i < batch; ++i) {
+    if (vote) make_entry(entries[i], W[i], nullptr, vote[i], MAO_F32, W[i].cols);
+    else make_entry(entries[i], W[i], &U[i], U[i].data, U[i].dtype, U[i].ld);
+  }
+  return launch_grouped(entries, vote ? EW_UPDATE_VOTE : EW_UPDATE_U, lr, stream);
+}
+
+mao_status sign_pack_launch(const mao_mat& U, uint32_t* bits, cudaStream_t stream) {
+  const int64_t n = U.rows * U.cols;
+  const int64_t nwords = ceil_div(n, 32);
+  const bool vec = (U.cols % 32 == 0) && vec8_ok(U);
+  const int64_t blocks = ceil_div(nwords, 256);
+  if (blocks > 0x7FFFFFFF) return MAO_ERR_UNSUPPORTED;
+  sign_pack_kernel<<<unsigned(blocks), 256, 0, stream>>>(U.data, U.rows, U.cols, U.ld, U.dtype,
+                                                         vec ? 1 : 0, bits, nwords);
+  return cuda_status(cudaGetLastError());
+}
+
+mao_status vote_launch(const uint32_t* bits, int32_t n_workers, int64_t stride, int64_t nbits,
+                       uint32_t* vote, cudaStream_t stream) {
+  const int64_t nwords = ceil_div(nbits, 32);
+  int P = 0;
+  while ((int64_t(1) << P) <= n_workers) ++P;  // n_workers < 2^P
+  const uint32_t T = uint32_t((n_workers + 1) / 2);  // count of +1 needed: 2*cnt >= W_n
+  // 16-byte path over the first floor(nwords/4)*4 words, one word per thread for the rest
+  const bool v4 = (stride % 4 == 0) && (reinterpret_cast<uintptr_t>(bits) % 16 == 0) &&
+                  (reinterpret_cast<uintptr_t>(vote) % 16 == 0);
+  const int64_t bulk = v4 ? (nwords / 4) * 4 : 0;
+  if (bulk > 0) {
+    const int64_t blocks = ceil_div(bulk / 4, 256);
+    vote_kernel<4><<<unsigned(blocks), 256, 0, stream>>>(bits, n_workers, stride, bulk, nbits,
+                                                         nwords, vote, P, T);
+  }
+  if (nwords > bulk) {
+    const int64_t rest = nwords - bulk;
+    const int64_t blocks = ceil_div(rest, 256);
+    vote_kernel<1><<<unsigned(blocks), 256, 0, stream>>>(bits + bulk, n_workers, stride, rest,
+                                                         nbits - bulk * 32, nwords - bulk,
+                                                         vote + bulk, P, T);
+  }
+  return cuda_status(cudaGetLastError());
+}
+
+}  // namespace mao

@@ -1,0 +1,40 @@
+// Internal launchers behind the C ABI (arguments already validated by abi.cu).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "mao.h"
+
+namespace mao {
+
+mao_status momentum_launch(const mao_mat* M, const mao_mat* G, int32_t batch, float mu,
+                           cudaStream_t stream);
+mao_status update_launch(const mao_mat* W, const uint32_t* const* vote, const mao_mat* U,
+                         int32_t batch, float lr, cudaStream_t stream);
+mao_status sign_pack_launch(const mao_mat& U, uint32_t* bits, cudaStream_t stream);
+mao_status vote_launch(const uint32_t* bits, int32_t n_workers, int64_t stride, int64_t nbits,
+                       uint32_t* vote, cudaStream_t stream);
+
+size_t ns_workspace_size(const mao_mat* X, int32_t batch, int32_t compute);
+mao_status ns_run(const mao_mat* in, const mao_mat* out, int32_t batch, int32_t steps,
+                  const float* coeffs, int32_t coeff_stride, float eps, int32_t compute,
+                  uint32_t* const* sign_bits, void* workspace, size_t workspace_bytes,
+                  cudaStream_t stream);
+
+// Reads and clears the device error word of the tensor-core kernels (after a stream sync).
+mao_status tc_read_and_clear_error(cudaStream_t stream);
+
+// Entry in the workspace table of final outputs, one per matrix slot.
+struct OutEntry {
+  void* out;        // U destination (may be null)
+  uint32_t* bits;   // packed signs destination (may be null)
+  int64_t ld;       // U row stride (elements)
+  int32_t dtype;    // U dtype
+  int32_t flags;    // bit 0: 16-byte vector stores allowed; bit 1: one sign word per 32 columns
+};
+
+enum OutFlags : int32_t { OUT_VEC = 1, OUT_WORDS = 2 };
+
+}  // namespace mao

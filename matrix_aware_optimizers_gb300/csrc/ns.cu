@@ -1,0 +1,593 @@
+// Newton–Schulz orchestration: shape grouping, workspace layout, staging with the
+// Frobenius norm, the per-iteration chain of three grouped products, and the fp32 FFMA
+// product kernel of the accuracy path.
+//
+// Per iteration ("分散ニュートン・シュルツ" of the Megatron Muon article counts three matrix
+// products per Newton–Schulz iteration; its "SYRK" section maps the first two onto
+// symmetric rank-k updates that still produce the full matrix):
+//   A = X X^T ; B = b A + c A A ; X <- a X + B X
+// The first iteration reads the staged, unnormalised input and applies s = 1/(||X||_F+eps)
+// as s^2 in the first product's epilogue and s in the third's, so the normalisation costs
+// no pass of its own.
+#include <algorithm>
+#include <cmath>
+#include <map>
+#include <utility>
+
+#include "common.cuh"
+#include "ns_plan.h"
+
+namespace mao {
+
+// ------------------------------------------------------------------- planning
+
+bool make_ns_plan(const mao_mat* X, int32_t batch, int32_t compute, NsPlan& plan) {
+  plan = NsPlan();
+  plan.es = compute == MAO_BF16 ? 2 : 4;
+  std::map<std::pair<int64_t, int64_t>, int> gid;
+  std::vector<std::vector<int>> members;
+  for (int b = 0; b < batch; ++b) {
+    const auto key = std::make_pair(X[b].rows, X[b].cols);
+    auto it = gid.find(key);
+    if (it == gid.end()) {
+      gid.emplace(key, int(members.size()));
+      members.emplace_back();
+      members.back().push_back(b);
+    } else {
+      members[it->second].push_back(b);
+    }
+  }
+  // groups in decreasing per-matrix work (4 m^2 n + 2 m^3), ties in order of appearance
+  std::vector<int> order(members.size());
+  for (size_t g = 0; g < order.size(); ++g) order[g] = int(g);
+  auto work = [&](int g) {
+    const double R = double(X[members[g][0]].rows), C = double(X[members[g][0]].cols);
+    const double m = std::min(R, C), n = std::max(R, C);
+    return 4.0 * m * m * n + 2.0 * m * m * m;
+  };
+  std::stable_sort(order.begin(), order.end(), [&](int x, int y) { return work(x) > work(y); });
+
+  plan.slot_of.assign(batch, -1);
+  plan.partial_begin.assign(batch + 1, 0);
+  int slot = 0;
+  for (int g : order) {
+    NsGroupPlan gp;
+    gp.R = X[members[g][0]].rows;
+    gp.C = X[members[g][0]].cols;
+    gp.m = std::min(gp.R, gp.C);
+    gp.n = std::max(gp.R, gp.C);
+    gp.tall = gp.R > gp.C;
+    gp.count = int32_t(members[g].size());
+    gp.slot0 = slot;
+    gp.ldx = round_up(gp.C, 8);
+    gp.lda = round_up(gp.m, 8);
+    for (int b : members[g]) {
+      plan.slot_of[b] = slot;
+      plan.input_of.push_back(b);
+      ++slot;
+    }
+    plan.groups.push_back(gp);
+  }
+  int64_t np = 0;
+  for (int s = 0; s < batch; ++s) {
+    const mao_mat& x = X[plan.input_of[s]];
+    plan.partial_begin[s] = np;
+    np += ceil_div(x.rows * ceil_div(x.cols, 8), kStageUnitsPerBlock);
+  }
+  plan.partial_begin[batch] = np;
+  plan.n_partials = np;
+
+  size_t off = 0;
+  plan.off_out_table = off;
+  off = size_t(round_up(int64_t(off + sizeof(OutEntry) * batch), 256));
+  plan.off_scale = off;
+  off = size_t(round_up(int64_t(off + sizeof(float) * batch), 256));
+  plan.off_prange = off;
+  off = size_t(round_up(int64_t(off + 2 * sizeof(int64_t) * batch), 256));
+  plan.off_partials = off;
+  off = size_t(round_up(int64_t(off + sizeof(float) * np), 1024));
+  for (auto& gp : plan.groups) {
+    const size_t xb = size_t(gp.count) * size_t(gp.R) * size_t(gp.ldx) * plan.es;
+    const size_t ab = size_t(gp.count) * size_t(gp.m) * size_t(gp.lda) * plan.es;
+    gp.off_x[0] = off;
+    off = size_t(round_up(int64_t(off + xb), 1024));
+    gp.off_x[1] = off;
+    off = size_t(round_up(int64_t(off + xb), 1024));
+    gp.off_a = off;
+    off = size_t(round_up(int64_t(off + ab), 1024));
+    gp.off_b = off;
+    off = size_t(round_up(int64_t(off + ab), 1024));
+  }
+  plan.total = off;
+  return true;
+}
+
+size_t ns_workspace_size(const mao_mat* X, int32_t batch, int32_t compute) {
+  NsPlan plan;
+  make_ns_plan(X, batch, compute, plan);
+  return plan.total;
+}
+
+namespace {
+
+// ------------------------------------------------------------ stage-in + norm
+
+constexpr int kStageMax = 48;
+
+struct StageEntry {
+  const void* src;
+  void* dst;
+  int64_t src_ld, dst_ld, rows, cols, units_per_row, units;
+  int64_t block_begin;  // first block of this entry in the launch
+  int64_t partial0;     // partial-sum index of that block
+  int64_t nblocks;      // blocks (= partial sums) of this entry
+  OutEntry out;
+  int32_t src_dt, vec_src, slot, pad;
+};
+
+struct StageParams {
+  StageEntry e[kStageMax];
+  int32_t n, ws_dt;
+  OutEntry* table;
+  int64_t* prange;      // per slot: first partial, number of partials
+  float* partials;
+};
+
+// Copies each input into its workspace slot (converting to the compute type) and writes
+// one fp32 partial sum of squares per block; records the slot's output entry.
+__global__ void __launch_bounds__(kStageThreads) stage_in_kernel(const __grid_constant__ StageParams p) {
+  int lo = 0, hi = p.n - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (p.e[mid].block_begin <= int64_t(blockIdx.x)) lo = mid; else hi = mid - 1;
+  }
+  const StageEntry& e = p.e[lo];
+  const int64_t blk = int64_t(blockIdx.x) - e.block_begin;
+  if (blk == 0 && threadIdx.x == 0) {
+    p.table[e.slot] = e.out;
+    p.prange[2 * e.slot] = e.partial0;
+    p.prange[2 * e.slot + 1] = e.nblocks;
+  }
+  float sq = 0.0f;
+  const int64_t u0 = blk * kStageUnitsPerBlock;
+#pragma unroll 1
+  for (int t = 0; t < kStageUnitsPerBlock / kStageThreads; ++t) {
+    const int64_t u = u0 + t * kStageThreads + threadIdx.x;
+    if (u >= e.units) break;
+    const int64_t row = u / e.units_per_row;
+    const int64_t col0 = (u - row * e.units_per_row) * 8;
+    const int valid = int(e.cols - col0 < 8 ? e.cols - col0 : 8);
+    float v[8];
+    if (e.vec_src && valid == 8) {
+      load8(e.src, row * e.src_ld + col0, e.src_dt, v);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] = i < valid ? load_elem(e.src, row * e.src_ld + col0 + i, e.src_dt) : 0.0f;
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) sq = __fmaf_rn(v[i], v[i], sq);
+    if (valid == 8) {
+      store8(e.dst, row * e.dst_ld + col0, p.ws_dt, v);
+    } else {
+      for (int i = 0; i < valid; ++i) store_elem(e.dst, row * e.dst_ld + col0 + i, p.ws_dt, v[i]);
+    }
+  }
+  // fixed-order block reduction: warp tree, then warp 0 over the warp sums
+  __shared__ float wsum[kStageThreads / 32];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sq += __shfl_xor_sync(0xFFFFFFFFu, sq, o);
+  if ((threadIdx.x & 31) == 0) wsum[threadIdx.x >> 5] = sq;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    float x = threadIdx.x < kStageThreads / 32 ? wsum[threadIdx.x] : 0.0f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xFFFFFFFFu, x, o);
+    if (threadIdx.x == 0) p.partials[e.partial0 + blk] = x;
+  }
+}
+
+// One warp per slot: fp64 sum of the slot's partials in a fixed order, then
+// s = 1 / (sqrt(sum) + eps).
+__global__ void __launch_bounds__(32) finalize_scale_kernel(const float* partials,
+                                                            const int64_t* prange, float* scale,
+                                                            float eps) {
+  const int slot = blockIdx.x;
+  const int64_t b0 = prange[2 * slot], nb = prange[2 * slot + 1];
+  double acc = 0.0;
+  for (int64_t i = threadIdx.x; i < nb; i += 32) acc += double(partials[b0 + i]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
+  if (threadIdx.x == 0) scale[slot] = float(1.0 / (sqrt(acc) + double(eps)));
+}
+
+// ------------------------------------------------------- fp32 FFMA product path
+
+constexpr int kSimtMaxGroups = 8;
+constexpr int kSimtTile = 64;
+constexpr int kSimtK = 16;
+
+struct SimtGroup {
+  const float* a;
+  const float* b;
+  float* out;
+  const float* res;
+  int64_t a_ms, a_si, a_sk;     // operand A(i, k) = a[z*a_ms + i*a_si + k*a_sk]
+  int64_t b_ms, b_sj, b_sk;     // operand B(j, k) = b[z*b_ms + j*b_sj + k*b_sk]
+  int64_t out_ms, out_ld, res_ms, res_ld;
+  int64_t block_begin;
+  int32_t M, N, K, count, slot0, syrk, tiles_m, tiles_n, final_out, orig_cols;
+};
+
+struct SimtParams {
+  SimtGroup g[kSimtMaxGroups];
+  int32_t ngroups, stage;
+  float a, b, c;
+  const float* scale;
+  const OutEntry* out_table;
+};
+
+// D(i, j) = sum_k A(i, k) B(j, k) on a 64x64 tile, 4x4 outputs per thread, fp32 FFMA.
+__global__ void __launch_bounds__(256) ns_simt_kernel(const __grid_constant__ SimtParams p) {
+  int gi = 0;
+  while (gi + 1 < p.ngroups && p.g[gi + 1].block_begin <= int64_t(blockIdx.x)) ++gi;
+  const SimtGroup& G = p.g[gi];
+  const int64_t local = int64_t(blockIdx.x) - G.block_begin;
+  const int tiles = G.tiles_m * G.tiles_n;
+  const int z = int(local / tiles);
+  const int r = int(local - int64_t(z) * tiles);
+  const int tm = r / G.tiles_n, tn = r - tm * G.tiles_n;
+  if (G.syrk && tm > tn) return;  // lower tiles come from the mirror of upper ones
+  const int row0 = tm * kSimtTile, col0 = tn * kSimtTile;
+  const float* A = G.a + int64_t(z) * G.a_ms;
+  const float* B = G.b + int64_t(z) * G.b_ms;
+
+  __shared__ float As[kSimtK][kSimtTile + 4];
+  __shared__ float Bs[kSimtK][kSimtTile + 4];
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  float acc[4][4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[i][j] = 0.0f;
+
+  for (int k0 = 0; k0 < G.K; k0 += kSimtK) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int idx = threadIdx.x + 256 * q;
+      const int ii = idx & 63, kk = idx >> 6;
+      const int gi_ = row0 + ii, gj = col0 + ii, gk = k0 + kk;
+      As[kk][ii] = (gi_ < G.M && gk < G.K) ? A[int64_t(gi_) * G.a_si + int64_t(gk) * G.a_sk] : 0.0f;
+      Bs[kk][ii] = (gj < G.N && gk < G.K) ? B[int64_t(gj) * G.b_sj + int64_t(gk) * G.b_sk] : 0.0f;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int kk = 0; kk < kSimtK; ++kk) {
+      float av[4], bv[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) av[i] = As[kk][ty * 4 + i];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) bv[j] = Bs[kk][tx * 4 + j];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = __fmaf_rn(av[i], bv[j], acc[i][j]);
+    }
+    __syncthreads();
+  }
+
+  const int slot = G.slot0 + z;
+  const float s = p.scale ? p.scale[slot] : 1.0f;
+  float* out = G.out + int64_t(z) * G.out_ms;
+  const float* res = G.res + int64_t(z) * G.res_ms;
+#pragma unroll
+  for (int ii = 0; ii < 4; ++ii) {
+    const int i = row0 + ty * 4 + ii;
+    if (i >= G.M) continue;
+#pragma unroll
+    for (int jj = 0; jj < 4; ++jj) {
+      const int j = col0 + tx * 4 + jj;
+      if (j >= G.N) continue;
+      const float v = acc[ii][jj];
+      if (p.stage == NS_GRAM || p.stage == NS_POLY) {
+        if (j < i) continue;
+        const float w = p.stage == NS_GRAM ? (s * s) * v
+                                           : __fmaf_rn(p.c, v, p.b * res[int64_t(i) * G.res_ld + j]);
+        out[int64_t(i) * G.out_ld + j] = w;
+        if (j > i) out[int64_t(j) * G.out_ld + i] = w;
+      } else {
+        const float w = s * __fmaf_rn(p.a, res[int64_t(i) * G.res_ld + j], v);
+        if (G.final_out) {
+          const OutEntry e = p.out_table[slot];
+          if (e.out) store_elem(e.out, int64_t(i) * e.ld + j, e.dtype, w);
+          if (e.bits && !(w < 0.0f)) {
+            const int64_t k = int64_t(i) * G.orig_cols + j;
+            atomicOr(e.bits + (k >> 5), 1u << (k & 31));
+          }
+        } else {
+          out[int64_t(i) * G.out_ld + j] = w;
+        }
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------------- driver
+
+struct Buffers {
+  uint8_t* ws;
+  const NsPlan* plan;
+  void* x(const NsGroupPlan& g, int which) const { return ws + g.off_x[which]; }
+  void* a(const NsGroupPlan& g) const { return ws + g.off_a; }
+  void* b(const NsGroupPlan& g) const { return ws + g.off_b; }
+};
+
+int syrk_tiles(int64_t m) {
+  int t = 0;
+  for (int64_t ib = 0; tc::BM * ib < m; ++ib) t += int(ceil_div(m - tc::BM * ib, tc::BN));
+  return t;
+}
+
+mao_status run_tc_stage(const Buffers& buf, const std::vector<const NsGroupPlan*>& round,
+                        int stage, int cur, bool first, bool last, const float* co,
+                        const float* scale, const OutEntry* table, cudaStream_t stream) {
+  TcParams p;
+  memset(&p, 0, sizeof(p));
+  p.ngroups = int32_t(round.size());
+  p.stage = stage;
+  p.a = co[0];
+  p.b = co[1];
+  p.c = co[2];
+  p.scale = first ? scale : nullptr;
+  p.out_table = table;
+  p.timeout_ns = 4000000000ull;
+  int tiles = 0;
+  for (size_t gi = 0; gi < round.size(); ++gi) {
+    const NsGroupPlan& g = *round[gi];
+    TcGroup& G = p.g[gi];
+    G.count = g.count;
+    G.slot0 = g.slot0;
+    G.orig_cols = int32_t(g.C);
+    const void* X = buf.x(g, cur);
+    const int64_t xs = g.R * g.ldx, as = g.m * g.lda;
+    mao_status st = MAO_OK;
+    if (stage == NS_GRAM) {
+      st = tc_encode_map(&G.tmA, X, g.C, g.R, g.ldx, g.count);
+      G.tmB = G.tmA;
+      G.a_mn = G.b_mn = g.tall ? 1 : 0;
+      G.M = G.N = int32_t(g.m);
+      G.K = int32_t(g.n);
+      G.out = buf.a(g);
+      G.out_ld = g.lda;
+      G.out_mstride = as;
+      G.res = nullptr;
+      G.syrk = 1;
+    } else if (stage == NS_POLY) {
+      st = tc_encode_map(&G.tmA, buf.a(g), g.m, g.m, g.lda, g.count);
+      G.tmB = G.tmA;
+      G.a_mn = G.b_mn = 0;
+      G.M = G.N = G.K = int32_t(g.m);
+      G.out = buf.b(g);
+      G.out_ld = g.lda;
+      G.out_mstride = as;
+      G.res = buf.a(g);
+      G.res_ld = g.lda;
+      G.res_mstride = as;
+      G.syrk = 1;
+    } else {
+      if (!g.tall) {  // X' = a X + B X : A-operand B (K-major), B-operand X (MN-major)
+        st = tc_encode_map(&G.tmA, buf.b(g), g.m, g.m, g.lda, g.count);
+        if (st == MAO_OK) st = tc_encode_map(&G.tmB, X, g.C, g.R, g.ldx, g.count);
+        G.a_mn = 0;
+        G.b_mn = 1;
+      } else {        // X' = a X + X B : A-operand X (K-major), B-operand B (K-major)
+        st = tc_encode_map(&G.tmA, X, g.C, g.R, g.ldx, g.count);
+        if (st == MAO_OK) st = tc_encode_map(&G.tmB, buf.b(g), g.m, g.m, g.lda, g.count);
+        G.a_mn = 0;
+        G.b_mn = 0;
+      }
+      G.M = int32_t(g.R);
+      G.N = int32_t(g.C);
+      G.K = int32_t(g.m);
+      G.out = last ? nullptr : buf.x(g, 1 - cur);
+      G.out_ld = g.ldx;
+      G.out_mstride = xs;
+      G.res = X;
+      G.res_ld = g.ldx;
+      G.res_mstride = xs;
+      G.syrk = 0;
+      G.final_out = last ? 1 : 0;
+    }
+    if (st != MAO_OK) return st;
+    G.tiles_m = int32_t(ceil_div(G.M, tc::BM));
+    G.tiles_n = int32_t(ceil_div(G.N, tc::BN));
+    G.tiles_per_mat = G.syrk ? syrk_tiles(G.M) : G.tiles_m * G.tiles_n;
+    G.tile_begin = tiles;
+    const int64_t t64 = int64_t(tiles) + int64_t(G.tiles_per_mat) * G.count;
+    if (t64 > 0x7FFFFFFF) return MAO_ERR_UNSUPPORTED;
+    tiles = int(t64);
+  }
+  p.total_tiles = tiles;
+  return tc_gemm_launch(p, stream);
+}
+
+mao_status run_simt_stage(const Buffers& buf, const std::vector<const NsGroupPlan*>& round,
+                          int stage, int cur, bool first, bool last, const float* co,
+                          const float* scale, const OutEntry* table, cudaStream_t stream) {
+  SimtParams p;
+  memset(&p, 0, sizeof(p));
+  p.ngroups = int32_t(round.size());
+  p.stage = stage;
+  p.a = co[0];
+  p.b = co[1];
+  p.c = co[2];
+  p.scale = first ? scale : nullptr;
+  p.out_table = table;
+  int64_t blocks = 0;
+  for (size_t gi = 0; gi < round.size(); ++gi) {
+    const NsGroupPlan& g = *round[gi];
+    SimtGroup& G = p.g[gi];
+    G.count = g.count;
+    G.slot0 = g.slot0;
+    G.orig_cols = int32_t(g.C);
+    const float* X = reinterpret_cast<const float*>(buf.x(g, cur));
+    const float* Ab = reinterpret_cast<const float*>(buf.a(g));
+    const float* Bb = reinterpret_cast<const float*>(buf.b(g));
+    const int64_t xs = g.R * g.ldx, as = g.m * g.lda;
+    if (stage == NS_GRAM) {
+      G.a = G.b = X;
+      G.a_ms = G.b_ms = xs;
+      if (!g.tall) { G.a_si = G.b_sj = g.ldx; G.a_sk = G.b_sk = 1; }
+      else { G.a_si = G.b_sj = 1; G.a_sk = G.b_sk = g.ldx; }
+      G.M = G.N = int32_t(g.m);
+      G.K = int32_t(g.n);
+      G.out = reinterpret_cast<float*>(buf.a(g));
+      G.out_ld = g.lda;
+      G.out_ms = as;
+      G.res = Ab;
+      G.syrk = 1;
+    } else if (stage == NS_POLY) {
+      G.a = G.b = Ab;
+      G.a_ms = G.b_ms = as;
+      G.a_si = G.b_sj = g.lda;
+      G.a_sk = G.b_sk = 1;
+      G.M = G.N = G.K = int32_t(g.m);
+      G.out = reinterpret_cast<float*>(buf.b(g));
+      G.out_ld = g.lda;
+      G.out_ms = as;
+      G.res = Ab;
+      G.res_ld = g.lda;
+      G.res_ms = as;
+      G.syrk = 1;
+    } else {
+      if (!g.tall) {
+        G.a = Bb; G.a_ms = as; G.a_si = g.lda; G.a_sk = 1;
+        G.b = X;  G.b_ms = xs; G.b_sj = 1;     G.b_sk = g.ldx;
+      } else {
+        G.a = X;  G.a_ms = xs; G.a_si = g.ldx; G.a_sk = 1;
+        G.b = Bb; G.b_ms = as; G.b_sj = g.lda; G.b_sk = 1;
+      }
+      G.M = int32_t(g.R);
+      G.N = int32_t(g.C);
+      G.K = int32_t(g.m);
+      G.out = last ? nullptr : reinterpret_cast<float*>(buf.x(g, 1 - cur));
+      G.out_ld = g.ldx;
+      G.out_ms = xs;
+      G.res = X;
+      G.res_ld = g.ldx;
+      G.res_ms = xs;
+      G.syrk = 0;
+      G.final_out = last ? 1 : 0;
+    }
+    G.tiles_m = int32_t(ceil_div(G.M, kSimtTile));
+    G.tiles_n = int32_t(ceil_div(G.N, kSimtTile));
+    G.block_begin = blocks;
+    blocks += int64_t(G.tiles_m) * G.tiles_n * G.count;
+  }
+  if (blocks > 0x7FFFFFFF) return MAO_ERR_UNSUPPORTED;
+  ns_simt_kernel<<<unsigned(blocks), 256, 0, stream>>>(p);
+  return cuda_status(cudaGetLastError());
+}
+
+}  // namespace
+
+mao_status ns_run(const mao_mat* in, const mao_mat* out, int32_t batch, int32_t steps,
+                  const float* coeffs, int32_t coeff_stride, float eps, int32_t compute,
+                  uint32_t* const* sign_bits, void* workspace, size_t workspace_bytes,
+                  cudaStream_t stream) {
+  NsPlan plan;
+  make_ns_plan(in, batch, compute, plan);
+  if (workspace_bytes < plan.total) return MAO_ERR_WORKSPACE;
+  uint8_t* ws = reinterpret_cast<uint8_t*>(workspace);
+  OutEntry* table = reinterpret_cast<OutEntry*>(ws + plan.off_out_table);
+  float* scale = reinterpret_cast<float*>(ws + plan.off_scale);
+  float* partials = reinterpret_cast<float*>(ws + plan.off_partials);
+  int64_t* prange = reinterpret_cast<int64_t*>(ws + plan.off_prange);
+  const bool tcpath = compute == MAO_BF16;
+  const int32_t ws_dt = tcpath ? MAO_BF16 : MAO_F32;
+
+  // ---- output entries; sign buffers filled by atomics start from zero
+  std::vector<OutEntry> entries(batch);
+  for (int b = 0; b < batch; ++b) {
+    OutEntry& e = entries[b];
+    e.out = out[b].data;
+    e.bits = sign_bits ? sign_bits[b] : nullptr;
+    e.ld = out[b].ld;
+    e.dtype = out[b].dtype;
+    e.flags = 0;
+    if (e.out && (reinterpret_cast<uintptr_t>(e.out) % 16 == 0) &&
+        ((out[b].ld * elem_size(out[b].dtype)) % 16 == 0))
+      e.flags |= OUT_VEC;
+    if (tcpath && in[b].cols % 32 == 0) e.flags |= OUT_WORDS;
+    if (e.bits && !(e.flags & OUT_WORDS)) {
+      const int64_t words = ceil_div(in[b].rows * in[b].cols, 32);
+      if (cudaMemsetAsync(e.bits, 0, size_t(words) * 4, stream) != cudaSuccess) return MAO_ERR_CUDA;
+    }
+  }
+
+  // ---- stage-in (copy to the workspace, partial sums of squares), in launches of kStageMax
+  {
+    int s = 0;
+    while (s < batch) {
+      StageParams p;
+      memset(&p, 0, sizeof(p));
+      p.ws_dt = ws_dt;
+      p.table = table;
+      p.prange = prange;
+      p.partials = partials;
+      int64_t blocks = 0;
+      while (s < batch && p.n < kStageMax) {
+        const int b = plan.input_of[s];
+        const NsGroupPlan* gp = nullptr;
+        for (const auto& g : plan.groups)
+          if (s >= g.slot0 && s < g.slot0 + g.count) gp = &g;
+        StageEntry& e = p.e[p.n++];
+        e.src = in[b].data;
+        e.src_ld = in[b].ld;
+        e.src_dt = in[b].dtype;
+        e.vec_src = vec8_ok(in[b]) ? 1 : 0;
+        e.dst = ws + gp->off_x[0] + size_t(s - gp->slot0) * size_t(gp->R * gp->ldx) * plan.es;
+        e.dst_ld = gp->ldx;
+        e.rows = in[b].rows;
+        e.cols = in[b].cols;
+        e.units_per_row = ceil_div(in[b].cols, 8);
+        e.units = e.units_per_row * in[b].rows;
+        e.block_begin = blocks;
+        e.partial0 = plan.partial_begin[s];
+        e.nblocks = ceil_div(e.units, kStageUnitsPerBlock);
+        e.out = entries[b];
+        e.slot = s;
+        blocks += ceil_div(e.units, kStageUnitsPerBlock);
+        ++s;
+      }
+      if (blocks > 0x7FFFFFFF) return MAO_ERR_UNSUPPORTED;
+      stage_in_kernel<<<unsigned(blocks), kStageThreads, 0, stream>>>(p);
+      if (cudaGetLastError() != cudaSuccess) return MAO_ERR_CUDA;
+    }
+  }
+  // ---- per-slot scale s = 1 / (||X||_F + eps)
+  finalize_scale_kernel<<<unsigned(batch), 32, 0, stream>>>(partials, prange, scale, eps);
+  if (cudaGetLastError() != cudaSuccess) return MAO_ERR_CUDA;
+
+  // ---- the iterations, for rounds of up to eight shape groups
+  const Buffers buf{ws, &plan};
+  const int max_groups = tcpath ? tc::MAX_GROUPS : kSimtMaxGroups;
+  for (size_t g0 = 0; g0 < plan.groups.size(); g0 += max_groups) {
+    std::vector<const NsGroupPlan*> round;
+    for (size_t g = g0; g < plan.groups.size() && round.size() < size_t(max_groups); ++g)
+      round.push_back(&plan.groups[g]);
+    for (int it = 0; it < steps; ++it) {
+      const float* co = coeffs + (coeff_stride ? 3 * it : 0);
+      const int cur = it & 1;
+      const bool first = it == 0, last = it == steps - 1;
+      for (int stage = NS_GRAM; stage <= NS_APPLY; ++stage) {
+        const mao_status st =
+            tcpath ? run_tc_stage(buf, round, stage, cur, first, last, co, scale, table, stream)
+                   : run_simt_stage(buf, round, stage, cur, first, last, co, scale, table, stream);
+        if (st != MAO_OK) return st;
+      }
+    }
+  }
+  return MAO_OK;
+}
+
+}  // namespace mao

@@ -1,0 +1,97 @@
+// Newton–Schulz execution plan: shape groups, workspace layout and the launch parameters
+// of the grouped product kernels (tensor-core bf16 path and fp32 FFMA path).
+#pragma once
+
+#include <cuda.h>  // CUtensorMap
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <vector>
+
+#include "internal.h"
+#include "mao.h"
+
+namespace mao {
+
+// Matrices of one original shape R x C. The iteration runs on X (m x n, m <= n): X is the
+// matrix itself when R <= C ("wide") and its transpose when R > C ("tall"); in both cases
+// the workspace holds the matrix in its original row-major R x C orientation.
+struct NsGroupPlan {
+  int64_t R, C, m, n;
+  bool tall;
+  int32_t count;       // matrices in the group
+  int32_t slot0;       // first slot (slots are numbered group by group)
+  int64_t ldx;         // workspace row stride of X (elements, multiple of 8)
+  int64_t lda;         // workspace row stride of A and B (elements, multiple of 8)
+  size_t off_x[2];     // ping/pong X buffers [count][R][ldx]
+  size_t off_a, off_b; // [count][m][lda]
+};
+
+struct NsPlan {
+  int es = 2;                          // workspace element size (2: bf16, 4: fp32)
+  std::vector<NsGroupPlan> groups;
+  std::vector<int32_t> slot_of;        // input index -> slot
+  std::vector<int32_t> input_of;       // slot -> input index
+  std::vector<int64_t> partial_begin;  // slot -> first partial-sum index
+  int64_t n_partials = 0;
+  size_t off_out_table = 0, off_scale = 0, off_prange = 0, off_partials = 0;
+  size_t total = 0;
+};
+
+// Stage-in work decomposition (shared by the plan and the stage-in launch).
+constexpr int kStageThreads = 256;
+constexpr int kStageUnitsPerBlock = kStageThreads * 4;  // 8 elements per unit
+
+bool make_ns_plan(const mao_mat* X, int32_t batch, int32_t compute, NsPlan& plan);
+
+// --------------------------------------------------------- tensor-core product kernel
+
+namespace tc {
+constexpr int BM = 128;          // output rows per tile (UMMA M)
+constexpr int BN = 256;          // output columns per tile (UMMA N, up to)
+constexpr int BK = 64;           // reduction depth per pipeline stage (one 128-byte swizzle row)
+constexpr int STAGES = 4;
+constexpr int BOX_BYTES = 64 * 64 * 2;         // every TMA box is 64 x 64 bf16
+constexpr int A_STAGE_BYTES = 2 * BOX_BYTES;   // 128 x 64
+constexpr int B_STAGE_BYTES = 4 * BOX_BYTES;   // 256 x 64
+constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
+constexpr int THREADS = 192;     // warp 0 TMA producer, warp 1 MMA issuer, warps 2-5 epilogue
+constexpr int TMEM_COLS = 512;   // two 256-column fp32 accumulators
+constexpr int TPAD = 40;         // epilogue transpose tile pitch (bf16 elements)
+constexpr int MAX_GROUPS = 8;
+constexpr size_t SMEM_BYTES = 1024 /*align*/ + size_t(STAGES) * STAGE_BYTES +
+                              4 * 32 * TPAD * 2 /*transpose*/ + 256 /*barriers*/;
+}  // namespace tc
+
+enum NsStage : int32_t { NS_GRAM = 1, NS_POLY = 2, NS_APPLY = 3 };
+
+struct alignas(64) TcGroup {
+  CUtensorMap tmA;          // operand A source (3-D: cols, rows, matrix)
+  CUtensorMap tmB;          // operand B source
+  void* out;                // product output buffer base (workspace), bf16
+  const void* res;          // residual buffer base (A for NS_POLY, X for NS_APPLY), bf16
+  int64_t out_mstride, res_mstride;  // elements between matrices
+  int64_t out_ld, res_ld;            // elements between rows
+  int32_t M, N, K;          // product shape: (M x K) . (K x N)
+  int32_t count, slot0;
+  int32_t a_mn, b_mn;       // operand stored MN-major (1) or K-major (0)
+  int32_t syrk;             // symmetric result: upper tiles computed, mirrored on store
+  int32_t tiles_m, tiles_n, tiles_per_mat, tile_begin;
+  int32_t final_out;        // last NS_APPLY: write U / signs through the slot's OutEntry
+  int32_t orig_cols;        // C of the original matrix (sign-bit indexing)
+};
+
+struct TcParams {
+  TcGroup g[tc::MAX_GROUPS];
+  int32_t ngroups, total_tiles, stage;
+  float a, b, c;                 // this iteration's coefficients
+  const float* scale;            // first iteration: per-slot 1/(||X||_F + eps); else null
+  const OutEntry* out_table;     // per-slot final outputs
+  unsigned long long timeout_ns; // bound of every barrier wait
+};
+
+mao_status tc_encode_map(CUtensorMap* map, const void* base, int64_t cols, int64_t rows,
+                         int64_t ld, int64_t count);
+mao_status tc_gemm_launch(const TcParams& p, cudaStream_t stream);
+
+}  // namespace mao
