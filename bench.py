@@ -1,0 +1,504 @@
+#!/usr/bin/env python
+"""Throughput of one Muon / Sign-Muon optimizer step on GB300, as one JSON line.
+
+A step is the whole hot path over one batch of synthetic input resident in HBM:
+  Muon:       momentum -> Newton–Schulz (bf16 tensor cores) -> W <- W - lr*U
+  Sign-Muon:  momentum (per worker) -> Newton–Schulz with fused sign packing
+              -> majority vote -> W <- W - lr*S_bar
+every stage through the C ABI of libmao.so.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config C] [--impl reference]
+
+Default workload: the 12-layer d=768 transformer-shaped Muon step (48 bf16 matrices).
+`--impl reference` times the fp64 CPU oracle on the same workload and metric (each
+step a bounded sample: one matrix of the workload, cycling), on rank 0 only.
+"""
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+DEFAULT_STEPS = {1: 2000, 2: 400, 3: 60, 4: 4, 5: 100}
+DEFAULT_WARMUP = {1: 20, 2: 10, 3: 5, 4: 3, 5: 5}
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=None)
+    ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--impl", default="mao", choices=["mao", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="CPU work budget of the oracle baseline sample")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ------------------------------------------------------------------ work model
+
+def alg_flops(shapes, steps):
+    """Newton–Schulz flops the method needs given symmetric A and B:
+    m(m+1)n (A = X X^T) + m^2(m+1) (A A) + 2 m^2 n (B X) per iteration."""
+    tot = 0
+    for R, C in shapes:
+        m, n = min(R, C), max(R, C)
+        tot += steps * (m * (m + 1) * n + m * m * (m + 1) + 2 * m * m * n)
+    return tot
+
+
+def dense_flops(shapes, steps):
+    """(4 m^2 n + 2 m^3) per iteration (dense count)."""
+    tot = 0
+    for R, C in shapes:
+        m, n = min(R, C), max(R, C)
+        tot += steps * (4 * m * m * n + 2 * m ** 3)
+    return tot
+
+
+def esize(dt):
+    import torch
+    return 2 if dt == torch.bfloat16 else 4
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi samples (200 ms) while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.proc = None
+        self.gpu = gpu_index
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------ the step
+
+class Step:
+    """Device buffers and the sequence of C-ABI calls of one optimizer step."""
+
+    def __init__(self, wl, inputs, device):
+        import torch
+        import matrix_aware_optimizers_gb300 as mao
+        self.mao = mao
+        self.wl = wl
+        self.W, self.M, self.G = inputs["W"], inputs["M"], inputs["G"]
+        self.dev = device
+        if wl.kind == "sign":
+            R, C = self.W[0].shape
+            self.nbits = R * C
+            nw = mao.packed_words(R, C)
+            stride = (nw + 3) // 4 * 4
+            self.words = torch.zeros((wl.workers, stride), dtype=torch.int32, device=device)
+            self.vote = torch.zeros(stride, dtype=torch.int32, device=device)
+            self.bits = [self.words[m, :nw] for m in range(wl.workers)]
+            self.U = [None] * wl.workers
+        else:
+            self.U = [torch.empty_like(w) for w in self.W]
+        self.ws = mao.workspace(self.M, wl.compute, device)
+
+    def momentum(self):
+        self.mao.muon_momentum_update(self.M, self.G, self.wl.mu)
+
+    def ns(self):
+        wl = self.wl
+        if wl.kind == "sign":
+            self.mao.ns_orthogonalize(self.M, self.U, wl.steps, wl.coeffs, wl.eps, wl.compute,
+                                      sign_bits=self.bits, ws=self.ws)
+        else:
+            self.mao.ns_orthogonalize(self.M, self.U, wl.steps, wl.coeffs, wl.eps, wl.compute,
+                                      ws=self.ws)
+
+    def update(self):
+        if self.wl.kind == "sign":
+            self.mao.majority_vote_packed(self.words, self.nbits, self.vote)
+            self.mao.apply_update(self.W, self.wl.lr, vote=self.vote)
+        else:
+            self.mao.apply_update(self.W, self.wl.lr, U=self.U)
+
+    def __call__(self):
+        self.momentum()
+        self.ns()
+        self.update()
+
+
+def stage_bytes(wl, step):
+    """Algorithmic HBM bytes of the elementwise stages per step."""
+    mom = sum(m.numel() * (2 * esize(m.dtype) + esize(g.dtype)) for m, g in zip(step.M, step.G))
+    if wl.kind == "sign":
+        n = step.nbits
+        upd = sum(w.numel() * 2 * esize(w.dtype) for w in step.W) + n // 8 + wl.workers * n // 8
+    else:
+        upd = sum(w.numel() * (2 * esize(w.dtype) + esize(u.dtype)) for w, u in zip(step.W, step.U))
+    return mom, upd
+
+
+# ------------------------------------------------------------------ oracle arm
+
+def oracle_sample(wl, host, budget_s, max_items=None):
+    """Time the fp64 oracle on whole matrices of the workload (cycling) for ~budget_s.
+
+    Returns (fraction of one step processed, seconds, description)."""
+    import numpy as np
+
+    import oracle
+    shapes = [tuple(x.shape) for x in host["M"]] if wl.kind == "muon" else [tuple(host["W"][0].shape)]
+    total = dense_flops(shapes, wl.steps) * (wl.workers if wl.kind == "sign" else 1)
+    store = "bf16" if wl.m_dtype.itemsize == 2 else "f32"
+    wstore = "bf16" if wl.w_dtype.itemsize == 2 else "f32"
+    done_flops, t_used, items = 0, 0.0, 0
+    n_items = len(host["M"])
+    words = {}
+    i = 0
+    while True:
+        t0 = time.perf_counter()
+        if wl.kind == "muon":
+            oracle.muon_step([host["W"][i]], [host["M"][i]], [host["G"][i]], wl.mu, wl.lr,
+                             wl.steps, wl.coeffs, wl.eps, m_store=store)
+            done_flops += dense_flops([shapes[i]], wl.steps)
+        else:
+            # one worker's momentum + NS + sign/pack; the vote and update run with the last
+            M = oracle.momentum(host["M"][i], host["G"][i], wl.mu, store)
+            U = oracle.newton_schulz(M, wl.steps, wl.coeffs, wl.eps)
+            words[i] = oracle.pack_signs(oracle.sign_of(U))
+            done_flops += dense_flops(shapes, wl.steps)
+            if i == n_items - 1 and len(words) == n_items:
+                vote = oracle.majority_vote(np.stack([words[m] for m in range(n_items)]), U.size)
+                S = oracle.unpack_signs(vote, U.size).reshape(U.shape)
+                oracle.apply_update(host["W"][0], S, wl.lr, wstore)
+        t_used += time.perf_counter() - t0
+        items += 1
+        i = (i + 1) % n_items
+        if t_used >= budget_s or (max_items is not None and items >= max_items):
+            break
+    frac = done_flops / total
+    desc = "%d matrix step(s) of the workload (%.3f of one step), fp64 numpy" % (items, frac)
+    return frac, t_used, desc
+
+
+def blas_threads():
+    try:
+        import threadpoolctl
+        info = threadpoolctl.threadpool_info()
+        n = [d.get("num_threads") for d in info if d.get("user_api") == "blas"]
+        if n:
+            return int(n[0])
+    except Exception:
+        pass
+    return os.cpu_count()
+
+
+def host_copy(inputs):
+    return {k: [t.float().cpu().numpy() for t in v] for k, v in inputs.items()}
+
+
+def run_reference(args, wl):
+    import torch
+    from matrix_aware_optimizers_gb300 import workloads
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    K = args.steps if args.steps is not None else DEFAULT_STEPS[wl.index]
+    Wu = args.warmup if args.warmup is not None else DEFAULT_WARMUP[wl.index]
+    shapes = wl.shapes if wl.kind == "muon" else wl.shapes
+    # one matrix of the workload per reference step
+    if wl.index == 4:
+        shapes = [(4096, 4096)] * 4 + [(4096, 14336), (14336, 4096), (4096, 14336)]
+    inputs = workloads.generate(wl, "cpu", shapes=shapes if wl.index == 4 else None)
+    host = host_copy(inputs)
+    for _ in range(Wu):
+        oracle_sample(wl, host, 0.0, max_items=1)
+    frac, secs = 0.0, 0.0
+    for _ in range(K):
+        f, s, _ = oracle_sample(wl, host, 0.0, max_items=1)
+        frac += f
+        secs += s
+    value = frac / secs
+    line = {
+        "impl": "reference", "metric": metric_name(wl), "value": value, "unit": "steps/s",
+        "n_gpus": args.gpus, "steps": K, "warmup": Wu, "ms_per_step": 1000.0 / value,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic", "config": config_block(wl, None),
+        "cpu_baseline": {"value": value, "unit": "steps/s", "cores": blas_threads(),
+                         "kind": "oracle",
+                         "sample": "each step: one matrix of the workload (cycling), fp64 numpy "
+                                   "momentum + Newton-Schulz + update; value = work fraction / time"},
+        "e2e": {"value": value, "unit": "steps/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+def metric_name(wl):
+    return ("Sign-Muon steps/s" if wl.kind == "sign" else "Muon steps/s") + \
+        " (%s); NS TFLOP/s; elementwise GB/s" % wl.name
+
+
+def config_block(wl, step_bytes):
+    c = {"workload": wl.name, "kind": wl.kind, "matrices": len(wl.shapes),
+         "elements": wl.elements, "workers": wl.workers, "ns_steps": wl.steps,
+         "coeffs": list(wl.coeffs), "mu": wl.mu, "lr": wl.lr, "compute": wl.compute,
+         "parallelism": "replicas: each rank steps its own copy of the workload"}
+    if step_bytes is not None:
+        c["l2"] = ("inputs larger than L2: %.0f MB of matrices touched per step vs 129 MB L2"
+                   % (step_bytes / 1e6))
+    return c
+
+
+# ------------------------------------------------------------------ main arm
+
+def main():
+    args = parse_args()
+    from matrix_aware_optimizers_gb300 import workloads
+    wl = workloads.workload(args.config)
+    if args.impl == "reference":
+        run_reference(args, wl)
+        return
+
+    import torch
+    import torch.distributed as dist
+    import matrix_aware_optimizers_gb300 as mao
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    mao.lib()
+
+    K = args.steps if args.steps is not None else DEFAULT_STEPS[wl.index]
+    Wu = max(3, args.warmup if args.warmup is not None else DEFAULT_WARMUP[wl.index])
+    inputs = workloads.generate(wl, dev, seed=(wl.index - 1) + 1000 * rank)
+    step = Step(wl, inputs, dev)
+    stream = torch.cuda.current_stream()
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    def max_over_ranks(x):
+        if world == 1:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    for _ in range(Wu):
+        step()
+    mao.sync_status()
+
+    # ---------------- timed region: K whole steps, inputs resident in HBM
+    n_tc_per_step = 3 * wl.steps * ((len(set(wl.shapes)) + 7) // 8)
+    mao.profile_begin(K * n_tc_per_step)
+    launches0 = mao.launch_count()
+    clocks = ClockSampler(local)
+    barrier()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(K):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clk = clocks.stop()
+    launches = mao.launch_count() - launches0
+    tc_ms = mao.profile_end()
+    mao.sync_status()
+    ms_total = max_over_ranks(e0.elapsed_time(e1))
+    ms_step = ms_total / K
+    value = world * K / (ms_total / 1000.0)
+
+    # ---------------- per-stage times (separate pass, same stream)
+    reps = max(3, min(K, 50))
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(reps)]
+    for r in range(reps):
+        ev[r][0].record(stream)
+        step.momentum()
+        ev[r][1].record(stream)
+        step.ns()
+        ev[r][2].record(stream)
+        step.update()
+        ev[r][3].record(stream)
+    torch.cuda.synchronize()
+    st_mom = statistics.median(e[0].elapsed_time(e[1]) for e in ev)
+    st_ns = statistics.median(e[1].elapsed_time(e[2]) for e in ev)
+    st_upd = statistics.median(e[2].elapsed_time(e[3]) for e in ev)
+
+    # ---------------- roofline of the dominant kernel (tensor-core NS product kernel)
+    peaks, peak_src = load_peaks()
+    shapes = [tuple(m.shape) for m in step.M]
+    alg = alg_flops(shapes, wl.steps)
+    dense = dense_flops(shapes, wl.steps)
+    tc_total_ms = sum(tc_ms)
+    if wl.compute == "bf16" and tc_ms:
+        tflops = alg * K / (tc_total_ms / 1000.0) / 1e12
+        peak = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
+        roof = {"kernel": "ns_tc_kernel", "bound": "tensor", "achieved": tflops, "peak": peak,
+                "unit": "TFLOP/s", "frac": tflops / peak, "traffic": None,
+                "peak_source": "%s bf16_tflops_sustained (kernel inside a long step loop)" % peak_src,
+                "work": "symmetric-minimum flops m(m+1)n + m^2(m+1) + 2m^2n per iteration",
+                "launches": len(tc_ms), "avg_launch_ms": tc_total_ms / len(tc_ms),
+                "share_of_step": tc_total_ms / ms_total}
+        traffic = read_traffic(wl)
+        if traffic is not None:
+            roof["traffic"] = traffic
+    else:
+        hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+        mom_b, upd_b = stage_bytes(wl, step)
+        gbs = (mom_b + upd_b) / ((st_mom + st_upd) / 1000.0) / 1e9
+        roof = {"kernel": "elementwise stages", "bound": "hbm", "achieved": gbs, "peak": hbm,
+                "unit": "GB/s", "frac": gbs / hbm, "traffic": None,
+                "peak_source": "%s hbm_gbs" % peak_src}
+    mom_b, upd_b = stage_bytes(wl, step)
+    hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+    touched = sum(m.numel() * esize(m.dtype) for m in step.M) * 2 + \
+        sum(w.numel() * esize(w.dtype) for w in step.W) * 2
+
+    line = {
+        "metric": metric_name(wl), "value": value, "unit": "steps/s", "n_gpus": world,
+        "steps": K, "warmup": Wu, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": wl.compute, "data": "synthetic",
+        "config": config_block(wl, touched),
+        "ns_tflops_dense": dense / (st_ns / 1000.0) / 1e12,
+        "ns_tflops_alg": alg / (st_ns / 1000.0) / 1e12,
+        "stages_ms": {"momentum": st_mom, "ns": st_ns, "update": st_upd},
+        "elementwise_gbs": {"momentum": mom_b / (st_mom / 1000.0) / 1e9,
+                            "update": upd_b / (st_upd / 1000.0) / 1e9, "peak": hbm},
+        "roofline": roof,
+        "gpu_launches": launches,
+        "clocks": clk,
+    }
+
+    # ---------------- end to end: host gradients in, host weights out, every step
+    if not args.no_e2e:
+        line["e2e"] = run_e2e(step, K if wl.index != 4 else min(K, 2), world, dev, barrier,
+                              max_over_ranks)
+
+    # ---------------- CPU baseline: the oracle on a bounded sample (rank 0, N = 1)
+    if world == 1 and rank == 0 and not args.no_cpu_baseline:
+        host = host_copy(workloads.generate(
+            wl, "cpu", shapes=None if wl.index != 4 else
+            [(4096, 4096)] * 4 + [(4096, 14336), (14336, 4096), (4096, 14336)]))
+        frac, secs, desc = oracle_sample(wl, host, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": frac / secs, "unit": "steps/s", "cores": blas_threads(),
+                                "kind": "oracle", "sample": desc + ", %.1f s" % secs}
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def run_e2e(step, K, world, dev, barrier, max_over_ranks):
+    import torch
+    stream = torch.cuda.current_stream()
+    G_host = [g.cpu().pin_memory() for g in step.G]
+    W_host = [w.cpu().pin_memory() for w in step.W]
+    h2d = sum(g.numel() * g.element_size() for g in G_host)
+    d2h = sum(w.numel() * w.element_size() for w in W_host)
+    barrier()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(K):
+        for gd, gh in zip(step.G, G_host):
+            gd.copy_(gh, non_blocking=True)
+        step()
+        for wh, wd in zip(W_host, step.W):
+            wh.copy_(wd, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    ms = max_over_ranks(e0.elapsed_time(e1))
+    return {"value": world * K / (ms / 1000.0), "unit": "steps/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": K}
+
+
+def read_traffic(wl):
+    """DRAM bytes per launch of the tensor-core kernel from the committed ncu summary of this
+    workload, or None when that summary was taken on a different kernel source."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "ns_tc_kernel_%s.md" % wl.name)
+    src = os.path.join(ROOT, "matrix_aware_optimizers_gb300", "csrc", "ns_tc.cu")
+    try:
+        with open(src, "rb") as f:
+            digest = hashlib.sha256(f.read()).hexdigest()[:16]
+        traffic, srchash = None, None
+        with open(path) as f:
+            for line in f:
+                if line.startswith("traffic_bytes_per_launch:"):
+                    traffic = float(line.split(":", 1)[1])
+                if line.startswith("kernel_source_sha256_16:"):
+                    srchash = line.split(":", 1)[1].strip()
+        if traffic is not None and srchash == digest:
+            return traffic
+    except OSError:
+        pass
+    return None
+
+
+if __name__ == "__main__":
+    main()

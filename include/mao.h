@@ -98,6 +98,8 @@ size_t ns_workspace_bytes(const mao_mat* X, int32_t batch, int32_t compute_dtype
  *   X_0 = X / (||X||_F + eps)
  *   for k in 0..steps-1:  A = X X^T;  B = b_k A + c_k A A;  X = a_k X + B X
  *   U = X (transposed back when R > C; no transposed copy is ever materialised).
+ *   The last two products are evaluated as B' = a_k I + b_k A + c_k A A, X = B' X (the same
+ *   polynomial; the bf16 operand B' then rounds a + ... instead of the smaller-margin B).
  *
  *   in[b]        f32 or bf16 input (the momentum); read only.
  *   out[b]       f32 or bf16 output U, same rows/cols as in[b]; out[b].data may be NULL when
@@ -158,6 +160,26 @@ mao_status apply_update(const mao_mat* W, const uint32_t* const* vote, const mao
  * when a bounded wait gives up. Returns MAO_OK, MAO_ERR_TIMEOUT or MAO_ERR_CUDA.
  */
 mao_status mao_sync_status(void* stream);
+
+/*
+ * Measurement support (no counterpart on the pages; used by benchmarks).
+ *
+ * mao_launch_count: number of kernels this library has launched in this process.
+ *
+ * mao_profile_begin: from now on, every launch of the Newton–Schulz tensor-core product
+ *   kernel (three per iteration) is bracketed by a pair of CUDA events recorded on the
+ *   launch's stream, for up to max_launches launches (1..1<<20). Creates the events
+ *   (host-side driver objects, no device memory). Not thread-safe: one profiling session
+ *   per process. Returns MAO_ERR_INVALID_ARG for a bad count, MAO_ERR_CUDA on failure.
+ *
+ * mao_profile_end: stops recording, synchronises the recorded events, writes the elapsed
+ *   milliseconds of up to max_out recorded launches into ms_out (host array, may be NULL
+ *   when max_out is 0), destroys the events and returns the number of launches recorded
+ *   (negative on a CUDA error).
+ */
+int64_t mao_launch_count(void);
+mao_status mao_profile_begin(int32_t max_launches);
+int32_t mao_profile_end(float* ms_out, int32_t max_out);
 
 #ifdef __cplusplus
 }

@@ -163,3 +163,22 @@ def apply_update(W, lr, vote=None, U=None, stream=None):
 def sync_status(stream=None):
     st = lib().mao_sync_status(_stream(stream))
     _abi.check("mao_sync_status", st)
+
+
+def launch_count():
+    """Kernels libmao has launched in this process."""
+    return int(lib().mao_launch_count())
+
+
+def profile_begin(max_launches):
+    """Record CUDA events around each tensor-core product launch (benchmarking)."""
+    _abi.check("mao_profile_begin", lib().mao_profile_begin(int(max_launches)))
+
+
+def profile_end(max_out=1 << 20):
+    """Stop recording; returns the per-launch durations in milliseconds."""
+    buf = (ctypes.c_float * max_out)()
+    n = lib().mao_profile_end(buf, max_out)
+    if n < 0:
+        raise MaoError("mao_profile_end", _abi.MAO_ERR_CUDA)
+    return [buf[i] for i in range(min(n, max_out))]

@@ -27,6 +27,9 @@ EXPORTS = (
     "majority_vote_packed",
     "apply_update",
     "mao_sync_status",
+    "mao_launch_count",
+    "mao_profile_begin",
+    "mao_profile_end",
 )
 
 
@@ -89,6 +92,12 @@ def load():
                                  ctypes.c_float, vp]
     lib.mao_sync_status.restype = ctypes.c_int
     lib.mao_sync_status.argtypes = [vp]
+    lib.mao_launch_count.restype = ctypes.c_int64
+    lib.mao_launch_count.argtypes = []
+    lib.mao_profile_begin.restype = ctypes.c_int
+    lib.mao_profile_begin.argtypes = [ctypes.c_int32]
+    lib.mao_profile_end.restype = ctypes.c_int32
+    lib.mao_profile_end.argtypes = [P(ctypes.c_float), ctypes.c_int32]
     _LIB = lib
     return lib
 

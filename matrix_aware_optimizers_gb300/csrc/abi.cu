@@ -1,7 +1,9 @@
 // C ABI entry points: argument validation (synchronous, nothing enqueued on error) and
 // dispatch to the launchers. No exception crosses this boundary.
+#include <atomic>
 #include <cmath>
 #include <mutex>
+#include <vector>
 
 #include "common.cuh"
 #include "internal.h"
@@ -42,6 +44,31 @@ int device_cc() {
   const int d = current_device();
   query_device(d);
   return g_cc[d];
+}
+
+namespace {
+std::atomic<long long> g_launches{0};
+
+struct Profile {
+  bool on = false;
+  int32_t cap = 0;
+  int32_t used = 0;
+  std::vector<cudaEvent_t> ev;  // 2 per launch
+};
+Profile g_prof;
+}  // namespace
+
+void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+void profile_before_launch(cudaStream_t stream) {
+  if (g_prof.on && g_prof.used < g_prof.cap) cudaEventRecord(g_prof.ev[2 * g_prof.used], stream);
+}
+
+void profile_after_launch(cudaStream_t stream) {
+  if (g_prof.on && g_prof.used < g_prof.cap) {
+    cudaEventRecord(g_prof.ev[2 * g_prof.used + 1], stream);
+    ++g_prof.used;
+  }
 }
 
 }  // namespace mao
@@ -153,6 +180,43 @@ mao_status apply_update(const mao_mat* W, const uint32_t* const* vote, const mao
 
 mao_status mao_sync_status(void* stream) {
   return tc_read_and_clear_error(static_cast<cudaStream_t>(stream));
+}
+
+int64_t mao_launch_count(void) { return g_launches.load(); }
+
+mao_status mao_profile_begin(int32_t max_launches) {
+  if (max_launches < 1 || max_launches > (1 << 20) || g_prof.on) return MAO_ERR_INVALID_ARG;
+  g_prof.ev.assign(size_t(2) * max_launches, nullptr);
+  for (auto& e : g_prof.ev) {
+    if (cudaEventCreate(&e) != cudaSuccess) {
+      for (auto& x : g_prof.ev)
+        if (x) cudaEventDestroy(x);
+      g_prof.ev.clear();
+      return MAO_ERR_CUDA;
+    }
+  }
+  g_prof.cap = max_launches;
+  g_prof.used = 0;
+  g_prof.on = true;
+  return MAO_OK;
+}
+
+int32_t mao_profile_end(float* ms_out, int32_t max_out) {
+  if (!g_prof.on) return 0;
+  g_prof.on = false;
+  int32_t n = g_prof.used;
+  bool ok = true;
+  for (int32_t i = 0; i < n; ++i) {
+    float ms = 0.0f;
+    if (cudaEventSynchronize(g_prof.ev[2 * i + 1]) != cudaSuccess ||
+        cudaEventElapsedTime(&ms, g_prof.ev[2 * i], g_prof.ev[2 * i + 1]) != cudaSuccess)
+      ok = false;
+    if (ms_out && i < max_out) ms_out[i] = ms;
+  }
+  for (auto& e : g_prof.ev) cudaEventDestroy(e);
+  g_prof.ev.clear();
+  g_prof.used = 0;
+  return ok ? n : -1;
 }
 
 }  // extern "C"

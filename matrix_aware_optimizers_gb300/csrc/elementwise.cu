@@ -154,6 +154,7 @@ mao_status launch_grouped(std::vector<EwEntry>& entries, int32_t mode, float sca
     if (p.n == 0) continue;
     if (blocks > 0x7FFFFFFF) return MAO_ERR_UNSUPPORTED;
     ew_kernel<<<unsigned(blocks), kEwThreads, 0, stream>>>(p);
+    count_launch();
     if (cudaGetLastError() != cudaSuccess) return MAO_ERR_CUDA;
   }
   return MAO_OK;
@@ -296,6 +297,7 @@ mao_status sign_pack_launch(const mao_mat& U, uint32_t* bits, cudaStream_t strea
   if (blocks > 0x7FFFFFFF) return MAO_ERR_UNSUPPORTED;
   sign_pack_kernel<<<unsigned(blocks), 256, 0, stream>>>(U.data, U.rows, U.cols, U.ld, U.dtype,
                                                          vec ? 1 : 0, bits, nwords);
+  count_launch();
   return cuda_status(cudaGetLastError());
 }
 
@@ -313,6 +315,7 @@ mao_status vote_launch(const uint32_t* bits, int32_t n_workers, int64_t stride, 
     const int64_t blocks = ceil_div(bulk / 4, 256);
     vote_kernel<4><<<unsigned(blocks), 256, 0, stream>>>(bits, n_workers, stride, bulk, nbits,
                                                          nwords, vote, P, T);
+    count_launch();
   }
   if (nwords > bulk) {
     const int64_t rest = nwords - bulk;
@@ -320,6 +323,7 @@ mao_status vote_launch(const uint32_t* bits, int32_t n_workers, int64_t stride, 
     vote_kernel<1><<<unsigned(blocks), 256, 0, stream>>>(bits + bulk, n_workers, stride, rest,
                                                          nbits - bulk * 32, nwords - bulk,
                                                          vote + bulk, P, T);
+    count_launch();
   }
   return cuda_status(cudaGetLastError());
 }

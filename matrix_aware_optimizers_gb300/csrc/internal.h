@@ -23,6 +23,12 @@ mao_status ns_run(const mao_mat* in, const mao_mat* out, int32_t batch, int32_t 
                   uint32_t* const* sign_bits, void* workspace, size_t workspace_bytes,
                   cudaStream_t stream);
 
+// Launch accounting (every kernel launch of the library calls this once).
+void count_launch();
+// Optional timing of the tensor-core product launches (see mao_profile_begin).
+void profile_before_launch(cudaStream_t stream);
+void profile_after_launch(cudaStream_t stream);
+
 // Reads and clears the device error word of the tensor-core kernels (after a stream sync).
 mao_status tc_read_and_clear_error(cudaStream_t stream);
 

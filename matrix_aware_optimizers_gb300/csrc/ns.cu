@@ -6,6 +6,7 @@
 // products per Newton–Schulz iteration; its "SYRK" section maps the first two onto
 // symmetric rank-k updates that still produce the full matrix):
 //   A = X X^T ; B = b A + c A A ; X <- a X + B X
+// evaluated as X <- (a I + B) X, with a I added on the diagonal by the second product.
 // The first iteration reads the staged, unnormalised input and applies s = 1/(||X||_F+eps)
 // as s^2 in the first product's epilogue and s in the third's, so the normalisation costs
 // no pass of its own.
@@ -290,12 +291,13 @@ __global__ void __launch_bounds__(256) ns_simt_kernel(const __grid_constant__ Si
       const float v = acc[ii][jj];
       if (p.stage == NS_GRAM || p.stage == NS_POLY) {
         if (j < i) continue;
-        const float w = p.stage == NS_GRAM ? (s * s) * v
-                                           : __fmaf_rn(p.c, v, p.b * res[int64_t(i) * G.res_ld + j]);
+        const float w = p.stage == NS_GRAM
+                            ? (s * s) * v
+                            : __fmaf_rn(p.c, v, p.b * res[int64_t(i) * G.res_ld + j]) + (i == j ? p.a : 0.0f);
         out[int64_t(i) * G.out_ld + j] = w;
         if (j > i) out[int64_t(j) * G.out_ld + i] = w;
       } else {
-        const float w = s * __fmaf_rn(p.a, res[int64_t(i) * G.res_ld + j], v);
+        const float w = s * v;
         if (G.final_out) {
           const OutEntry e = p.out_table[slot];
           if (e.out) store_elem(e.out, int64_t(i) * e.ld + j, e.dtype, w);
@@ -485,6 +487,7 @@ mao_status run_simt_stage(const Buffers& buf, const std::vector<const NsGroupPla
   }
   if (blocks > 0x7FFFFFFF) return MAO_ERR_UNSUPPORTED;
   ns_simt_kernel<<<unsigned(blocks), 256, 0, stream>>>(p);
+  count_launch();
   return cuda_status(cudaGetLastError());
 }
 
@@ -561,11 +564,13 @@ mao_status ns_run(const mao_mat* in, const mao_mat* out, int32_t batch, int32_t 
       }
       if (blocks > 0x7FFFFFFF) return MAO_ERR_UNSUPPORTED;
       stage_in_kernel<<<unsigned(blocks), kStageThreads, 0, stream>>>(p);
+      count_launch();
       if (cudaGetLastError() != cudaSuccess) return MAO_ERR_CUDA;
     }
   }
   // ---- per-slot scale s = 1 / (||X||_F + eps)
   finalize_scale_kernel<<<unsigned(batch), 32, 0, stream>>>(partials, prange, scale, eps);
+  count_launch();
   if (cudaGetLastError() != cudaSuccess) return MAO_ERR_CUDA;
 
   // ---- the iterations, for rounds of up to eight shape groups

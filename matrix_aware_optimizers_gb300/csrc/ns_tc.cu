@@ -3,8 +3,11 @@
 // One persistent kernel serves all three products of an iteration (the stage is a launch
 // parameter):
 //   NS_GRAM   A = alpha * X X^T            (symmetric: upper tiles + mirrored store)
-//   NS_POLY   B = b A + c A A              (symmetric; A A = A A^T by symmetry)
-//   NS_APPLY  X' = beta * (a X + B X)      (X . B in the tall orientation; B symmetric)
+//   NS_POLY   B = a I + b A + c A A        (symmetric; A A = A A^T by symmetry)
+//   NS_APPLY  X' = beta * B X              (X . B in the tall orientation; B symmetric)
+// a X + (b A + c A^2) X is evaluated as (a I + b A + c A^2) X: the identity term is added
+// on the diagonal in the second product's epilogue, so the bf16 operand B rounds a + (...)
+// rather than (...) alone, and the third product needs no residual read.
 // over every matrix of up to eight shape groups. Each CTA owns one SM and walks a static
 // stride of the flattened tile list.
 //
@@ -508,15 +511,14 @@ __global__ void __launch_bounds__(THREADS, 1) ns_tc_kernel(const __grid_constant
             for (int c = 0; c < 32; ++c) r[c] = 0.0f;
             if (row_ok) load32_bf16(res + int64_t(i) * G.res_ld + j0, nvalid == 32, nvalid, r);
 #pragma unroll
-            for (int c = 0; c < 32; ++c) w[c] = __fmaf_rn(p.c, v[c], p.b * r[c]);
+            for (int c = 0; c < 32; ++c)
+              w[c] = __fmaf_rn(p.c, v[c], p.b * r[c]) + (j0 + c == i ? p.a : 0.0f);
           }
           store_sym_chunk(out, G.out_ld, G.M, i0, j0, lane, w, tp);
         } else if (row_ok) {
-          float r[32];
-          load32_bf16(res + int64_t(i) * G.res_ld + j0, nvalid == 32, nvalid, r);
           float w[32];
 #pragma unroll
-          for (int c = 0; c < 32; ++c) w[c] = s * __fmaf_rn(p.a, r[c], v[c]);
+          for (int c = 0; c < 32; ++c) w[c] = s * v[c];
           if (G.final_out) {
             store_final(oe, i, j0, nvalid, G.orig_cols, w);
           } else {
@@ -592,7 +594,10 @@ mao_status tc_gemm_launch(const TcParams& p, cudaStream_t stream) {
   });
   if (attr_err != cudaSuccess) return MAO_ERR_CUDA;
   const int grid = p.total_tiles < num_sms() ? p.total_tiles : num_sms();
+  profile_before_launch(stream);
   ns_tc_kernel<<<grid, THREADS, SMEM_BYTES, stream>>>(p);
+  count_launch();
+  profile_after_launch(stream);
   return cuda_status(cudaGetLastError());
 }
 
