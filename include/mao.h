@@ -122,6 +122,35 @@ mao_status ns_orthogonalize(const mao_mat* in, const mao_mat* out, int32_t batch
                             int32_t compute, uint32_t* const* sign_bits, void* workspace,
                             size_t workspace_bytes, void* stream);
 
+/* Size of the scratch area ns_orthogonalize_noalloc uses (16 MiB per device). */
+#define MAO_NOALLOC_WORKSPACE_BYTES (16u * 1024u * 1024u)
+
+/*
+ * ns_orthogonalize without a workspace argument. The pages have no counterpart of this
+ * call: it exists for callers that cannot call cudaMalloc, such as code inside a host
+ * framework that owns all device memory through its own pool, or a latency-critical loop
+ * that must not pay cudaMalloc's implicit device synchronisation. Such a caller passes only
+ * inputs and outputs; the scratch is one static 16 MiB device array inside this library.
+ *
+ *   Arguments, results and errors are those of ns_orthogonalize (same kernels, same math).
+ *   Limit: the batch must satisfy ns_workspace_bytes(in, batch, compute) <=
+ *     MAO_NOALLOC_WORKSPACE_BYTES (for example one 1024 x 1024 or one 768 x 3072 matrix in
+ *     bf16); larger requests return MAO_ERR_WORKSPACE before any device work.
+ *   Memory: allocates nothing. Every GPU that loads this library holds the 16 MiB array
+ *     until the process exits, whether or not the call is used.
+ *   Set-up: the first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call before any
+ *     stream capture on the device.
+ *   Sharing: all calls on a device use the same array, which keeps the last call's
+ *     contents (nothing in it needs to start at zero). Calls whose work overlaps on the GPU
+ *     (other streams, other host threads) race on it: order them on one stream or with
+ *     events.
+ */
+mao_status ns_orthogonalize_noalloc(const mao_mat* in, const mao_mat* out, int32_t batch,
+                                    int32_t steps, const float* coeffs, int32_t coeff_stride,
+                                    float eps, int32_t compute, uint32_t* const* sign_bits,
+                                    void* stream);
+
 /*
  * Entrywise sign and 1-bit packing ([SignMuon] §2 step 2 "Extração de Sinal" and step 3,
  * all-gather variant: one bit per entry).

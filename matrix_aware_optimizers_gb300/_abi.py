@@ -16,6 +16,9 @@ MAO_ERR_TIMEOUT = 6
 MAO_F32 = 0
 MAO_BF16 = 1
 
+# scratch size of ns_orthogonalize_noalloc (MAO_NOALLOC_WORKSPACE_BYTES in mao.h)
+NOALLOC_WORKSPACE_BYTES = 16 * 1024 * 1024
+
 # every symbol include/mao.h declares
 EXPORTS = (
     "mao_abi_version",
@@ -23,6 +26,7 @@ EXPORTS = (
     "muon_momentum_update",
     "ns_workspace_bytes",
     "ns_orthogonalize",
+    "ns_orthogonalize_noalloc",
     "sign_pack_bits",
     "majority_vote_packed",
     "apply_update",
@@ -83,6 +87,10 @@ def load():
     lib.ns_orthogonalize.argtypes = [
         P(MaoMat), P(MaoMat), ctypes.c_int32, ctypes.c_int32, P(ctypes.c_float), ctypes.c_int32,
         ctypes.c_float, ctypes.c_int32, P(ctypes.c_void_p), vp, ctypes.c_size_t, vp]
+    lib.ns_orthogonalize_noalloc.restype = ctypes.c_int
+    lib.ns_orthogonalize_noalloc.argtypes = [
+        P(MaoMat), P(MaoMat), ctypes.c_int32, ctypes.c_int32, P(ctypes.c_float), ctypes.c_int32,
+        ctypes.c_float, ctypes.c_int32, P(ctypes.c_void_p), vp]
     lib.sign_pack_bits.restype = ctypes.c_int
     lib.sign_pack_bits.argtypes = [P(MaoMat), vp, vp]
     lib.majority_vote_packed.restype = ctypes.c_int
