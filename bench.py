@@ -401,6 +401,8 @@ def main():
                 "peak_source": "%s bf16_tflops_sustained (kernel inside a long step loop)" % peak_src,
                 "work": "symmetric-minimum flops m(m+1)n + m^2(m+1) + 2m^2n per iteration",
                 "launches": len(tc_ms), "avg_launch_ms": tc_total_ms / len(tc_ms),
+                "stage_avg_ms": {name: statistics.mean(tc_ms[i::3]) for i, name in
+                                 enumerate(("gram", "poly", "apply"))},
                 "share_of_step": tc_total_ms / ms_total}
         traffic = read_traffic(wl)
         if traffic is not None:

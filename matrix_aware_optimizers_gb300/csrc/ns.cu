@@ -352,9 +352,13 @@ mao_status run_tc_stage(const Buffers& buf, const std::vector<const NsGroupPlan*
     const void* X = buf.x(g, cur);
     const int64_t xs = g.R * g.ldx, as = g.m * g.lda;
     mao_status st = MAO_OK;
+    const void *srcA, *srcB;
+    int64_t colsA, rowsA, ldA, colsB, rowsB, ldB;
     if (stage == NS_GRAM) {
-      st = tc_encode_map(&G.tmA, X, g.C, g.R, g.ldx, g.count);
-      G.tmB = G.tmA;
+      srcA = srcB = X;
+      colsA = colsB = g.C;
+      rowsA = rowsB = g.R;
+      ldA = ldB = g.ldx;
       G.a_mn = G.b_mn = g.tall ? 1 : 0;
       G.M = G.N = int32_t(g.m);
       G.K = int32_t(g.n);
@@ -364,8 +368,9 @@ mao_status run_tc_stage(const Buffers& buf, const std::vector<const NsGroupPlan*
       G.res = nullptr;
       G.syrk = 1;
     } else if (stage == NS_POLY) {
-      st = tc_encode_map(&G.tmA, buf.a(g), g.m, g.m, g.lda, g.count);
-      G.tmB = G.tmA;
+      srcA = srcB = buf.a(g);
+      colsA = colsB = rowsA = rowsB = g.m;
+      ldA = ldB = g.lda;
       G.a_mn = G.b_mn = 0;
       G.M = G.N = G.K = int32_t(g.m);
       G.out = buf.b(g);
@@ -376,14 +381,14 @@ mao_status run_tc_stage(const Buffers& buf, const std::vector<const NsGroupPlan*
       G.res_mstride = as;
       G.syrk = 1;
     } else {
-      if (!g.tall) {  // X' = a X + B X : A-operand B (K-major), B-operand X (MN-major)
-        st = tc_encode_map(&G.tmA, buf.b(g), g.m, g.m, g.lda, g.count);
-        if (st == MAO_OK) st = tc_encode_map(&G.tmB, X, g.C, g.R, g.ldx, g.count);
+      if (!g.tall) {  // X' = B X : A-operand B (K-major), B-operand X (MN-major)
+        srcA = buf.b(g); colsA = rowsA = g.m; ldA = g.lda;
+        srcB = X; colsB = g.C; rowsB = g.R; ldB = g.ldx;
         G.a_mn = 0;
         G.b_mn = 1;
-      } else {        // X' = a X + X B : A-operand X (K-major), B-operand B (K-major)
-        st = tc_encode_map(&G.tmA, X, g.C, g.R, g.ldx, g.count);
-        if (st == MAO_OK) st = tc_encode_map(&G.tmB, buf.b(g), g.m, g.m, g.lda, g.count);
+      } else {        // X' = X B : A-operand X (K-major), B-operand B (K-major)
+        srcA = X; colsA = g.C; rowsA = g.R; ldA = g.ldx;
+        srcB = buf.b(g); colsB = rowsB = g.m; ldB = g.lda;
         G.a_mn = 0;
         G.b_mn = 0;
       }
@@ -393,12 +398,16 @@ mao_status run_tc_stage(const Buffers& buf, const std::vector<const NsGroupPlan*
       G.out = last ? nullptr : buf.x(g, 1 - cur);
       G.out_ld = g.ldx;
       G.out_mstride = xs;
-      G.res = X;
-      G.res_ld = g.ldx;
-      G.res_mstride = xs;
+      G.res = nullptr;
       G.syrk = 0;
       G.final_out = last ? 1 : 0;
     }
+    // K-major operands load 64 x KBOX_ROWS boxes; MN-major ones 64 x 64 (the 128-byte
+    // swizzle span limits the contiguous dimension to 64 elements)
+    G.a_box_rows = G.a_mn ? 64 : tc::KBOX_ROWS;
+    G.b_box_rows = G.b_mn ? 64 : tc::KBOX_ROWS;
+    st = tc_encode_map(&G.tmA, srcA, colsA, rowsA, ldA, g.count, G.a_box_rows);
+    if (st == MAO_OK) st = tc_encode_map(&G.tmB, srcB, colsB, rowsB, ldB, g.count, G.b_box_rows);
     if (st != MAO_OK) return st;
     G.tiles_m = int32_t(ceil_div(G.M, tc::BM));
     G.tiles_n = int32_t(ceil_div(G.N, tc::BN));

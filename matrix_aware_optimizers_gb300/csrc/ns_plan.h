@@ -50,8 +50,12 @@ namespace tc {
 constexpr int BM = 128;          // output rows per tile (UMMA M)
 constexpr int BN = 256;          // output columns per tile (UMMA N, up to)
 constexpr int BK = 64;           // reduction depth per pipeline stage (one 128-byte swizzle row)
+#ifndef MAO_TC_KBOX
+#define MAO_TC_KBOX 128
+#endif
 constexpr int STAGES = 4;
-constexpr int BOX_BYTES = 64 * 64 * 2;         // every TMA box is 64 x 64 bf16
+constexpr int KBOX_ROWS = MAO_TC_KBOX;   // rows per TMA box of a K-major operand (64 or 128)
+constexpr int BOX_BYTES = 64 * 64 * 2;         // a 64 x 64 bf16 box (MN-major operands)
 constexpr int A_STAGE_BYTES = 2 * BOX_BYTES;   // 128 x 64
 constexpr int B_STAGE_BYTES = 4 * BOX_BYTES;   // 256 x 64
 constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
@@ -68,6 +72,7 @@ enum NsStage : int32_t { NS_GRAM = 1, NS_POLY = 2, NS_APPLY = 3 };
 struct alignas(64) TcGroup {
   CUtensorMap tmA;          // operand A source (3-D: cols, rows, matrix)
   CUtensorMap tmB;          // operand B source
+  int32_t a_box_rows, b_box_rows;  // rows of one TMA box (64 x rows bf16)
   void* out;                // product output buffer base (workspace), bf16
   const void* res;          // residual buffer base (A for NS_POLY, X for NS_APPLY), bf16
   int64_t out_mstride, res_mstride;  // elements between matrices
@@ -91,7 +96,7 @@ struct TcParams {
 };
 
 mao_status tc_encode_map(CUtensorMap* map, const void* base, int64_t cols, int64_t rows,
-                         int64_t ld, int64_t count);
+                         int64_t ld, int64_t count, int box_rows);
 mao_status tc_gemm_launch(const TcParams& p, cudaStream_t stream);
 
 }  // namespace mao

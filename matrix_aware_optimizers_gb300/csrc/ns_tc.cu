@@ -31,6 +31,19 @@ namespace mao {
 
 __device__ unsigned int g_tc_error;  // bit 0: a barrier wait timed out
 
+#ifdef MAO_TC_TRACE
+// Debug builds only: cycles each role spends waiting, summed over CTAs.
+// [0] producer waiting for a free stage, [1] MMA waiting for data, [2] MMA waiting for a
+// free accumulator, [3] epilogue waiting for an accumulator, [4] epilogue busy cycles,
+// [5] MMA k-blocks, [6] tiles, [7] total CTA cycles
+__device__ unsigned long long g_tc_trace[16];
+#define TRACE_T0() const long long _t0 = clock64()
+#define TRACE_ADD(i, t0) atomicAdd(&g_tc_trace[i], (unsigned long long)(clock64() - (t0)))
+#else
+#define TRACE_T0()
+#define TRACE_ADD(i, t0)
+#endif
+
 namespace {
 
 using namespace tc;
@@ -332,6 +345,9 @@ __global__ void __launch_bounds__(THREADS, 1) ns_tc_kernel(const __grid_constant
   uint64_t* drain_bar = tempty_bar + 2;      // [1]       MMA drain after an abort
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+#ifdef MAO_TC_TRACE
+  __shared__ volatile long long arm_time[STAGES];
+#endif
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -362,52 +378,93 @@ __global__ void __launch_bounds__(THREADS, 1) ns_tc_kernel(const __grid_constant
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
   const uint64_t limit = p.timeout_ns;
+#ifdef MAO_TC_TRACE
+  const long long t_cta = clock64();
+#endif
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
+    // Lane 0 waits for a free stage and arms its barrier; then lane q issues box q of the
+    // stage (A boxes first, then B boxes), so the boxes of one stage are issued in parallel.
+#ifndef MAO_TC_NO_DESC_PREFETCH
     if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
-      int armed_parity[STAGES];
+      for (int g = 0; g < p.ngroups; ++g) {
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.g[g].tmA)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.g[g].tmB)) : "memory");
+      }
+    }
+#endif
+    int stage = 0;
+    uint32_t phase = 0;
+    int armed_parity[STAGES];
 #pragma unroll
-      for (int s = 0; s < STAGES; ++s) armed_parity[s] = -1;
-      bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < p.total_tiles; tile += gridDim.x) {
-        Tile t;
-        decode_tile(p, tile, t);
-        const TcGroup& G = p.g[t.g];
-        const int nbox_b = (t.n_valid + 63) / 64;
-        const uint32_t bytes = uint32_t(2 + nbox_b) * BOX_BYTES;
-        for (int kb = 0; kb < t.nkb; ++kb) {
+    for (int s = 0; s < STAGES; ++s) armed_parity[s] = -1;
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < p.total_tiles; tile += gridDim.x) {
+      Tile t;
+      decode_tile(p, tile, t);
+      const TcGroup& G = p.g[t.g];
+      const int abox = G.a_box_rows, bbox = G.b_box_rows;
+      const int nbox_a = BM / abox;
+      const int nbox_b = (t.n_valid + bbox - 1) / bbox;
+      const uint32_t bytes = uint32_t(nbox_a * abox + nbox_b * bbox) * 128u;
+      // this lane's box: operand, tensor map, destination offset and tile coordinate
+      const bool is_a = lane < nbox_a;
+      const bool active = lane < nbox_a + nbox_b;
+      const int q = is_a ? lane : lane - nbox_a;
+      const CUtensorMap* map = is_a ? &G.tmA : &G.tmB;
+      const int mn = is_a ? G.a_mn : G.b_mn;
+      const int box = is_a ? abox : bbox;
+      const uint32_t off = (is_a ? 0u : uint32_t(A_STAGE_BYTES)) + uint32_t(q * box) * 128u;
+      const int rc = (is_a ? t.row0 : t.col0) + box * q;
+      for (int kb = 0; kb < t.nkb; ++kb) {
+        int okw = 1;
+        if (lane == 0) {
+#ifdef MAO_TC_TRACE
+          const long long tw = clock64();
+#endif
           if (!mbar_wait(smem_u32(&empty_bar[stage]), phase ^ 1u, abort_flag, limit)) {
-            ok = false;
-            break;
-          }
-          const uint32_t fb = smem_u32(&full_bar[stage]);
-          mbar_expect_tx(fb, bytes);
-          armed_parity[stage] = int(phase);
-          const uint32_t a_dst = smem_u32(ring + stage * STAGE_BYTES);
-          const uint32_t b_dst = a_dst + A_STAGE_BYTES;
-          const int k0 = kb * BK;
-#pragma unroll
-          for (int q = 0; q < 2; ++q) {
-            if (G.a_mn) tma_load_3d(a_dst + q * BOX_BYTES, &G.tmA, fb, t.row0 + 64 * q, k0, t.z);
-            else tma_load_3d(a_dst + q * BOX_BYTES, &G.tmA, fb, k0, t.row0 + 64 * q, t.z);
-          }
-          for (int q = 0; q < nbox_b; ++q) {
-            if (G.b_mn) tma_load_3d(b_dst + q * BOX_BYTES, &G.tmB, fb, t.col0 + 64 * q, k0, t.z);
-            else tma_load_3d(b_dst + q * BOX_BYTES, &G.tmB, fb, k0, t.col0 + 64 * q, t.z);
-          }
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1u;
+            okw = 0;
+          } else {
+            TRACE_ADD(0, tw);
+            mbar_expect_tx(smem_u32(&full_bar[stage]), bytes);
+            armed_parity[stage] = int(phase);
+#ifdef MAO_TC_TRACE
+            arm_time[stage] = clock64();
+#endif
           }
         }
+        okw = __shfl_sync(0xFFFFFFFFu, okw, 0);
+        if (!okw) {
+          ok = false;
+          break;
+        }
+#ifdef MAO_TC_TRACE
+        const long long t_tma = clock64();
+#endif
+        if (active) {
+          const uint32_t fb = smem_u32(&full_bar[stage]);
+          const uint32_t dst = smem_u32(ring + stage * STAGE_BYTES) + off;
+          const int k0 = kb * BK;
+          if (mn) tma_load_3d(dst, map, fb, rc, k0, t.z);
+          else tma_load_3d(dst, map, fb, k0, rc, t.z);
+        }
+#ifdef MAO_TC_TRACE
+        __syncwarp();
+        if (lane == 0) {
+          atomicAdd(&g_tc_trace[10], (unsigned long long)(clock64() - t_tma));
+          atomicAdd(&g_tc_trace[11], (unsigned long long)(nbox_a + nbox_b));
+        }
+#endif
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
       }
-      if (!ok) {  // let every copy in flight land before the CTA exits
-        for (int s = 0; s < STAGES; ++s)
-          if (armed_parity[s] >= 0) mbar_drain(smem_u32(&full_bar[s]), uint32_t(armed_parity[s]), 1000000000ull);
-      }
+    }
+    if (!ok && lane == 0) {  // let every copy in flight land before the CTA exits
+      for (int s = 0; s < STAGES; ++s)
+        if (armed_parity[s] >= 0) mbar_drain(smem_u32(&full_bar[s]), uint32_t(armed_parity[s]), 1000000000ull);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -424,20 +481,35 @@ __global__ void __launch_bounds__(THREADS, 1) ns_tc_kernel(const __grid_constant
         const TcGroup& G = p.g[t.g];
         const int acc = local & 1;
         const uint32_t acc_phase = uint32_t(local >> 1) & 1u;
+#ifdef MAO_TC_TRACE
+        const long long tw0 = clock64();
+#endif
         if (!mbar_wait(smem_u32(&tempty_bar[acc]), acc_phase ^ 1u, abort_flag, limit)) {
           ok = false;
           break;
         }
+        TRACE_ADD(2, tw0);
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + uint32_t(acc * BN);
         const int n_mma = (t.n_valid + 15) & ~15;
         const uint32_t idesc = instr_desc(n_mma, G.a_mn, G.b_mn);
         for (int kb = 0; kb < t.nkb; ++kb) {
+#ifdef MAO_TC_TRACE
+          const long long tw1 = clock64();
+#endif
           if (!mbar_wait(smem_u32(&full_bar[stage]), phase, abort_flag, limit)) {
             ok = false;
             break;
           }
+          TRACE_ADD(1, tw1);
+#ifdef MAO_TC_TRACE
+          atomicAdd(&g_tc_trace[5], 1ull);
+          const long long t_issue = clock64();
+          atomicAdd(&g_tc_trace[9], (unsigned long long)(t_issue - arm_time[stage]));
+#endif
+#ifndef MAO_TC_NO_FULL_FENCE
           tc_fence_after();
+#endif
           const uint32_t a_base = smem_u32(ring + stage * STAGE_BYTES);
           const uint32_t b_base = a_base + A_STAGE_BYTES;
 #pragma unroll
@@ -452,6 +524,9 @@ __global__ void __launch_bounds__(THREADS, 1) ns_tc_kernel(const __grid_constant
             issued = true;
           }
           umma_commit(smem_u32(&empty_bar[stage]));
+#ifdef MAO_TC_TRACE
+          atomicAdd(&g_tc_trace[8], (unsigned long long)(clock64() - t_issue));
+#endif
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -477,8 +552,15 @@ __global__ void __launch_bounds__(THREADS, 1) ns_tc_kernel(const __grid_constant
       const TcGroup& G = p.g[t.g];
       const int acc = local & 1;
       const uint32_t acc_phase = uint32_t(local >> 1) & 1u;
+#ifdef MAO_TC_TRACE
+      const long long tw2 = clock64();
+#endif
       if (!mbar_wait(smem_u32(&tfull_bar[acc]), acc_phase, abort_flag, limit)) break;
       tc_fence_after();
+#ifdef MAO_TC_TRACE
+      if (lane == 0) TRACE_ADD(3, tw2);
+      const long long tb = clock64();
+#endif
       const int slot = G.slot0 + t.z;
       const float s = p.scale ? p.scale[slot] : 1.0f;
       const int rl = 32 * quad + lane;
@@ -536,12 +618,21 @@ __global__ void __launch_bounds__(THREADS, 1) ns_tc_kernel(const __grid_constant
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&tempty_bar[acc]));
+#ifdef MAO_TC_TRACE
+      if (lane == 0) {
+        TRACE_ADD(4, tb);
+        if (warp == 2) atomicAdd(&g_tc_trace[6], 1ull);
+      }
+#endif
     }
   }
 
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+#ifdef MAO_TC_TRACE
+  if (threadIdx.x == 0) TRACE_ADD(7, t_cta);
+#endif
   if (warp == 1) {
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
                  "r"(TMEM_COLS)
@@ -568,12 +659,12 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }  // namespace
 
 mao_status tc_encode_map(CUtensorMap* map, const void* base, int64_t cols, int64_t rows,
-                         int64_t ld, int64_t count) {
+                         int64_t ld, int64_t count, int box_rows) {
   auto fn = encode_fn();
   if (!fn) return MAO_ERR_CUDA;
   const cuuint64_t dims[3] = {cuuint64_t(cols), cuuint64_t(rows), cuuint64_t(count)};
   const cuuint64_t strides[2] = {cuuint64_t(ld) * 2, cuuint64_t(rows) * cuuint64_t(ld) * 2};
-  const cuuint32_t box[3] = {64, 64, 1};
+  const cuuint32_t box[3] = {64, cuuint32_t(box_rows), 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -600,6 +691,18 @@ mao_status tc_gemm_launch(const TcParams& p, cudaStream_t stream) {
   profile_after_launch(stream);
   return cuda_status(cudaGetLastError());
 }
+
+#ifdef MAO_TC_TRACE
+extern "C" int mao_debug_tc_trace(unsigned long long* out, int reset) {
+  if (cudaDeviceSynchronize() != cudaSuccess) return -1;
+  if (cudaMemcpyFromSymbol(out, g_tc_trace, sizeof(unsigned long long) * 16) != cudaSuccess) return -1;
+  if (reset) {
+    unsigned long long z[16] = {0};
+    if (cudaMemcpyToSymbol(g_tc_trace, z, sizeof(z)) != cudaSuccess) return -1;
+  }
+  return 0;
+}
+#endif
 
 mao_status tc_read_and_clear_error(cudaStream_t stream) {
   unsigned int v = 0;
