@@ -288,6 +288,23 @@ def run_reference(args, wl):
     print(json.dumps(line))
 
 
+def reduce_max(x, device, world):
+    """Max of a scalar over all ranks (identity at world size 1)."""
+    if world == 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(ms_max, steps, world):
+    """Whole-job steps/s: every rank steps its own copy of the workload (weak scaling), so
+    the job completes world * steps steps in the slowest rank's time."""
+    return world * steps / (ms_max / 1000.0)
+
+
 def metric_name(wl):
     return ("Sign-Muon steps/s" if wl.kind == "sign" else "Muon steps/s") + \
         " (%s); NS TFLOP/s; elementwise GB/s" % wl.name
@@ -338,11 +355,7 @@ def main():
             dist.barrier()
 
     def max_over_ranks(x):
-        if world == 1:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+        return reduce_max(x, dev, world)
 
     for _ in range(Wu):
         step()
@@ -369,7 +382,7 @@ def main():
     mao.sync_status()
     ms_total = max_over_ranks(e0.elapsed_time(e1))
     ms_step = ms_total / K
-    value = world * K / (ms_total / 1000.0)
+    value = job_throughput(ms_total, K, world)
 
     # ---------------- per-stage times (separate pass, same stream)
     reps = max(3, min(K, 50))
@@ -475,7 +488,7 @@ def run_e2e(step, K, world, dev, barrier, max_over_ranks):
     torch.cuda.synchronize()
     barrier()
     ms = max_over_ranks(e0.elapsed_time(e1))
-    return {"value": world * K / (ms / 1000.0), "unit": "steps/s", "h2d_bytes_per_step": h2d,
+    return {"value": job_throughput(ms, K, world), "unit": "steps/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": K}
 
 

@@ -1,0 +1,144 @@
+"""End-to-end parity of whole optimizer steps at the full workload sizes.
+
+The step runs on the GPU exactly as bench.py launches it (bench.Step). The fp64 oracle
+then checks sampled outputs one by one:
+  * momentum: bit-exact (sampled matrices);
+  * Newton–Schulz U: relative Frobenius error <= 1e-4 (fp32 path) / 2e-2 (bf16 path);
+  * signs: every disagreement with the oracle's U is explained by the value error at that
+    entry, and (fp32) lies where |U| < 1e-3 rms(U); agreement >= 99.9% (fp32) / 99% (bf16,
+    the bound implied by the 2e-2 value tolerance);
+  * vote and update: bit-exact on the GPU's own inputs (packed words, stored U).
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import bench
+import oracle
+from helpers import bits_of, check_sign_agreement, rel_fro, to_np, words_np
+from matrix_aware_optimizers_gb300 import workloads
+import matrix_aware_optimizers_gb300 as mao
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"f32": 1e-4, "bf16": 2e-2}
+AGREE = {"f32": 0.999, "bf16": 0.99}
+
+
+def _store(dt):
+    return "bf16" if dt == torch.bfloat16 else "f32"
+
+
+def _run_step(wl, dev, keep_u=False):
+    """One step through bench.Step; returns the step object and host copies of the inputs."""
+    inp = workloads.generate(wl, dev)
+    host_in = {k: [to_np(t) for t in v] for k, v in inp.items()}
+    step = bench.Step(wl, inp, dev)
+    step.momentum()
+    M_after = [m.clone() for m in step.M]
+    U_vals = None
+    if keep_u:
+        # the same NS call with U written as fp32 next to the fused sign bits
+        U_vals = [torch.empty(m.shape, dtype=torch.float32, device=dev) for m in step.M]
+        bits2 = [torch.zeros_like(b) for b in step.bits] if wl.kind == "sign" else None
+        mao.ns_orthogonalize(step.M, U_vals, wl.steps, wl.coeffs, wl.eps, wl.compute,
+                             sign_bits=bits2, ws=step.ws)
+    step.ns()
+    W_before = [w.clone() for w in step.W]
+    step.update()
+    mao.sync_status()
+    if keep_u and wl.kind == "sign":
+        for b1, b2 in zip(step.bits, bits2):
+            assert torch.equal(b1, b2), "sign-only and value+sign calls disagree"
+    return step, host_in, M_after, U_vals, W_before
+
+
+def test_config1_sign_muon_64x128_f32(cuda):
+    wl = workloads.workload(1)
+    step, host, M_after, U, W_before = _run_step(wl, cuda, keep_u=True)
+    R, C = wl.shapes[0]
+    ref = oracle.sign_muon_step(host["W"][0], host["M"], host["G"], wl.mu, wl.lr, wl.steps,
+                                wl.coeffs, wl.eps, m_store="f32", w_store="f32")
+    for m in range(wl.workers):
+        assert np.array_equal(to_np(M_after[m]), ref["M"][m])
+        u = to_np(U[m])
+        assert rel_fro(u, ref["U"][m]) <= TOL["f32"]
+        got = bits_of(words_np(step.bits[m]), R * C)
+        frac = check_sign_agreement(u, ref["U"][m], got, strict_rms=1e-3)
+        assert frac >= AGREE["f32"]
+    words = words_np(step.words)[:, : (R * C + 31) // 32]
+    assert np.array_equal(words_np(step.vote)[: words.shape[1]], oracle.majority_vote(words, R * C))
+    S_bar = oracle.unpack_signs(words_np(step.vote), R * C).reshape(R, C)
+    assert np.array_equal(to_np(step.W[0]), oracle.apply_update(host["W"][0], S_bar, wl.lr, "f32"))
+
+
+def _check_muon(wl, step, host, M_after, W_before, sample):
+    for i in sample:
+        mstore = _store(wl.m_dtype)
+        assert np.array_equal(to_np(M_after[i]), oracle.momentum(host["M"][i], host["G"][i], wl.mu, mstore)), i
+        u_gpu = to_np(step.U[i])
+        u_ref = oracle.newton_schulz(to_np(M_after[i]), wl.steps, wl.coeffs, wl.eps)
+        err = rel_fro(u_gpu, u_ref)
+        assert err <= TOL[wl.compute], (i, err)
+        want_w = oracle.apply_update(to_np(W_before[i]), u_gpu, wl.lr, _store(wl.w_dtype))
+        assert np.array_equal(to_np(step.W[i]), want_w), i
+
+
+def test_config2_muon_gpt12_d768_full(cuda):
+    wl = workloads.workload(2)
+    step, host, M_after, _, W_before = _run_step(wl, cuda)
+    # one matrix of each shape (layer 0), plus one from the last layer
+    _check_muon(wl, step, host, M_after, W_before, [0, 1, 2, 3, 46])
+
+
+def test_config3_sign_muon_4096_w8_full(cuda):
+    wl = workloads.workload(3)
+    step, host, M_after, U, W_before = _run_step(wl, cuda, keep_u=True)
+    R, C = wl.shapes[0]
+    n = R * C
+    m = 0  # sampled worker: oracle momentum and Newton–Schulz in fp64
+    assert np.array_equal(to_np(M_after[m]), oracle.momentum(host["M"][m], host["G"][m], wl.mu, "bf16"))
+    u_ref = oracle.newton_schulz(to_np(M_after[m]), wl.steps, wl.coeffs, wl.eps)
+    u_gpu = to_np(U[m])
+    assert rel_fro(u_gpu, u_ref) <= TOL["bf16"]
+    frac = check_sign_agreement(u_gpu, u_ref, bits_of(words_np(step.bits[m]), n))
+    assert frac >= AGREE["bf16"], frac
+    # fused signs equal the signs of the fp32 values the same epilogue produced
+    for w in range(wl.workers):
+        uw = to_np(U[w]).reshape(-1)
+        assert np.array_equal(bits_of(words_np(step.bits[w]), n), (~(uw < 0)).astype(np.uint8))
+    nw = (n + 31) // 32
+    words = words_np(step.words)[:, :nw]
+    vote = words_np(step.vote)[:nw]
+    assert vote.nbytes == 2 * 1024 * 1024  # 1 bit per entry: 2 MiB for 4096 x 4096
+    assert np.array_equal(vote, oracle.majority_vote(words, n))
+    S_bar = oracle.unpack_signs(vote, n).reshape(R, C)
+    assert np.array_equal(to_np(step.W[0]), oracle.apply_update(to_np(W_before[0]), S_bar, wl.lr, "bf16"))
+
+
+def test_config5_moe_grouped_full(cuda):
+    wl = workloads.workload(5)
+    step, host, M_after, _, W_before = _run_step(wl, cuda)
+    # two experts (three matrices each, different gradient scales) and the dense block
+    _check_muon(wl, step, host, M_after, W_before, [0, 1, 2, 192, 193, 194, 384])
+
+
+def test_config4_dense32_full(cuda):
+    wl = workloads.workload(4)
+    free, _ = torch.cuda.mem_get_info()
+    if free < 160 * 2 ** 30:
+        pytest.skip("needs about 130 GB of free device memory")
+    step, host, M_after, _, W_before = _run_step(wl, cuda)
+    # one attention matrix (4096 x 4096) and the tall MLP matrix of layer 31 (sampled
+    # entries of the momentum; the 14336 x 4096 NS is checked through its properties)
+    _check_muon(wl, step, host, M_after, W_before, [0])
+    i = 7 * 31 + 5  # 14336 x 4096
+    u = step.U[i].float()
+    # polar-factor property at any size: the Gram matrix of U has eigenvalues in the
+    # quintic's output band (singular values of U in [0.68, 1.21] for sigma >= 1.5e-3,
+    # smaller sigma map below the band)
+    gram = (u.t() @ u).double()
+    ev = torch.linalg.eigvalsh(gram).clamp_min(0).sqrt().cpu().numpy()
+    assert ev.max() <= 1.2024 * 1.02
+    assert np.mean(ev >= 0.6798 * 0.98) >= 0.95
