@@ -325,7 +325,7 @@ struct Buffers {
 
 int syrk_tiles(int64_t m) {
   int t = 0;
-  for (int64_t ib = 0; tc::BM * ib < m; ++ib) t += int(ceil_div(m - tc::BM * ib, tc::BN));
+  for (int64_t ib = 0; tc::TILE_M * ib < m; ++ib) t += int(ceil_div(m - tc::TILE_M * ib, tc::BN));
   return t;
 }
 
@@ -409,7 +409,7 @@ mao_status run_tc_stage(const Buffers& buf, const std::vector<const NsGroupPlan*
     st = tc_encode_map(&G.tmA, srcA, colsA, rowsA, ldA, g.count, G.a_box_rows);
     if (st == MAO_OK) st = tc_encode_map(&G.tmB, srcB, colsB, rowsB, ldB, g.count, G.b_box_rows);
     if (st != MAO_OK) return st;
-    G.tiles_m = int32_t(ceil_div(G.M, tc::BM));
+    G.tiles_m = int32_t(ceil_div(G.M, tc::TILE_M));
     G.tiles_n = int32_t(ceil_div(G.N, tc::BN));
     G.tiles_per_mat = G.syrk ? syrk_tiles(G.M) : G.tiles_m * G.tiles_n;
     G.tile_begin = tiles;

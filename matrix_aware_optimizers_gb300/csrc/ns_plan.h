@@ -65,11 +65,22 @@ constexpr int TPAD = 40;         // epilogue transpose tile pitch (bf16 elements
 constexpr int MAX_GROUPS = 8;
 constexpr size_t SMEM_BYTES = 1024 /*align*/ + size_t(STAGES) * STAGE_BYTES +
                               4 * 32 * TPAD * 2 /*transpose*/ + 256 /*barriers*/;
+// CTA-pair kernel (cluster of two, cta_group::2): 256-row tiles, 6 stages of 32 KB per CTA
+#ifndef MAO_TC_PAIR
+#define MAO_TC_PAIR 1
+#endif
+constexpr bool PAIR = MAO_TC_PAIR != 0;
+constexpr int TILE_M = PAIR ? 256 : BM;   // output rows per tile as the host enumerates them
+#ifndef MAO_TC_EPI_WARPS
+#define MAO_TC_EPI_WARPS 4
+#endif
+constexpr size_t PAIR_SMEM_BYTES = 1024 + size_t(6) * (2 * 128 * 64 * 2) +
+                                   MAO_TC_EPI_WARPS * 32 * TPAD * 2 + 256;
 }  // namespace tc
 
 enum NsStage : int32_t { NS_GRAM = 1, NS_POLY = 2, NS_APPLY = 3 };
 
-struct alignas(64) TcGroup {
+struct TcGroup {
   CUtensorMap tmA;          // operand A source (3-D: cols, rows, matrix)
   CUtensorMap tmB;          // operand B source
   int32_t a_box_rows, b_box_rows;  // rows of one TMA box (64 x rows bf16)
