@@ -47,35 +47,34 @@ bool make_ns_plan(const mao_mat* X, int32_t batch, int32_t compute, NsPlan& plan
 // --------------------------------------------------------- tensor-core product kernel
 
 namespace tc {
-constexpr int BM = 128;          // output rows per tile (UMMA M)
-constexpr int BN = 256;          // output columns per tile (UMMA N, up to)
+// Tiles of TILE_M x BN outputs are computed by a pair of CTAs (a cluster of two on two SMs,
+// tcgen05 cta_group::2): each CTA holds 128 rows of the A operand tile and 128 columns of
+// the B operand tile per pipeline stage and receives 128 output rows in its TMEM.
+constexpr int TILE_M = 256;      // output rows per tile
+constexpr int BN = 256;          // output columns per tile
 constexpr int BK = 64;           // reduction depth per pipeline stage (one 128-byte swizzle row)
+constexpr int HALF = 128;        // rows (A) / columns (B) of the operand tile held per CTA
 #ifndef MAO_TC_KBOX
 #define MAO_TC_KBOX 128
 #endif
-constexpr int STAGES = 4;
+#ifndef MAO_TC_STAGES
+#define MAO_TC_STAGES 6
+#endif
 constexpr int KBOX_ROWS = MAO_TC_KBOX;   // rows per TMA box of a K-major operand (64 or 128)
-constexpr int BOX_BYTES = 64 * 64 * 2;         // a 64 x 64 bf16 box (MN-major operands)
-constexpr int A_STAGE_BYTES = 2 * BOX_BYTES;   // 128 x 64
-constexpr int B_STAGE_BYTES = 4 * BOX_BYTES;   // 256 x 64
-constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
-constexpr int THREADS = 192;     // warp 0 TMA producer, warp 1 MMA issuer, warps 2-5 epilogue
+constexpr int STAGES = MAO_TC_STAGES;
+constexpr int BOX_BYTES = 64 * 64 * 2;            // a 64 x 64 bf16 box (MN-major operands)
+constexpr int A_HALF_BYTES = HALF * BK * 2;       // 16 KB
+constexpr int B_HALF_BYTES = HALF * BK * 2;       // 16 KB
+constexpr int STAGE_BYTES = A_HALF_BYTES + B_HALF_BYTES;
+constexpr int EPI_WARPS = 4;     // one epilogue warp per 32-lane TMEM quadrant
+constexpr int THREADS = 64 + 32 * EPI_WARPS;  // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
 constexpr int TMEM_COLS = 512;   // two 256-column fp32 accumulators
-constexpr int TPAD = 40;         // epilogue transpose tile pitch (bf16 elements)
+constexpr int EP_ROW = 72;       // staging pitch (bf16) of a 32 x 64 row-major block: 144 B
+constexpr int EP_COL = 40;       // staging pitch (bf16) of the 64 x 32 transposed block: 80 B
+constexpr int EP_ELEMS = 64 * EP_COL;  // per-warp staging buffer (>= 32 * EP_ROW)
 constexpr int MAX_GROUPS = 8;
 constexpr size_t SMEM_BYTES = 1024 /*align*/ + size_t(STAGES) * STAGE_BYTES +
-                              4 * 32 * TPAD * 2 /*transpose*/ + 256 /*barriers*/;
-// CTA-pair kernel (cluster of two, cta_group::2): 256-row tiles, 6 stages of 32 KB per CTA
-#ifndef MAO_TC_PAIR
-#define MAO_TC_PAIR 1
-#endif
-constexpr bool PAIR = MAO_TC_PAIR != 0;
-constexpr int TILE_M = PAIR ? 256 : BM;   // output rows per tile as the host enumerates them
-#ifndef MAO_TC_EPI_WARPS
-#define MAO_TC_EPI_WARPS 4
-#endif
-constexpr size_t PAIR_SMEM_BYTES = 1024 + size_t(6) * (2 * 128 * 64 * 2) +
-                                   MAO_TC_EPI_WARPS * 32 * TPAD * 2 + 256;
+                              size_t(EPI_WARPS) * EP_ELEMS * 2 + 256 /*barriers*/;
 }  // namespace tc
 
 enum NsStage : int32_t { NS_GRAM = 1, NS_POLY = 2, NS_APPLY = 3 };
