@@ -58,7 +58,7 @@ constexpr int HALF = 128;        // rows (A) / columns (B) of the operand tile h
 #define MAO_TC_KBOX 128
 #endif
 #ifndef MAO_TC_STAGES
-#define MAO_TC_STAGES 6
+#define MAO_TC_STAGES 5
 #endif
 constexpr int KBOX_ROWS = MAO_TC_KBOX;   // rows per TMA box of a K-major operand (64 or 128)
 constexpr int STAGES = MAO_TC_STAGES;
@@ -71,10 +71,11 @@ constexpr int THREADS = 64 + 32 * EPI_WARPS;  // warp 0 TMA, warp 1 MMA, warps 2
 constexpr int TMEM_COLS = 512;   // two 256-column fp32 accumulators
 constexpr int EP_ROW = 72;       // staging pitch (bf16) of a 32 x 64 row-major block: 144 B
 constexpr int EP_COL = 40;       // staging pitch (bf16) of the 64 x 32 transposed block: 80 B
-constexpr int EP_ELEMS = 64 * EP_COL;  // per-warp staging buffer (>= 32 * EP_ROW)
+constexpr int EP_ELEMS = 64 * EP_COL;  // one staging buffer (>= 32 * EP_ROW)
+constexpr int EP_BUFS = 2;             // per epilogue warp: residual prefetch double buffer
 constexpr int MAX_GROUPS = 8;
 constexpr size_t SMEM_BYTES = 1024 /*align*/ + size_t(STAGES) * STAGE_BYTES +
-                              size_t(EPI_WARPS) * EP_ELEMS * 2 + 256 /*barriers*/;
+                              size_t(EPI_WARPS) * EP_BUFS * EP_ELEMS * 2 + 256 /*barriers*/;
 }  // namespace tc
 
 enum NsStage : int32_t { NS_GRAM = 1, NS_POLY = 2, NS_APPLY = 3 };

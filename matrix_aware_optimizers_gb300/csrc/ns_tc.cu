@@ -338,34 +338,41 @@ __device__ __forceinline__ void store_cols(const __nv_bfloat16* S, __nv_bfloat16
   }
 }
 
-// Reads the 32 x 64 residual block (rows i0.., columns jb..) with coalesced loads and
-// returns this lane's row in r[64] (zeros outside the matrix).
-__device__ __forceinline__ void load_rows(__nv_bfloat16* S, const __nv_bfloat16* src, int64_t ld,
-                                          int i0, int jb, int M, int N, int lane, float* r) {
+// Starts copying the 32 x 64 residual block (rows i0.., columns jb..) into the row-major
+// staging layout of R with asynchronous 16-byte copies (cp.async, zero fill outside the
+// matrix) and commits them as one group.
+__device__ __forceinline__ void prefetch_rows(__nv_bfloat16* R, const __nv_bfloat16* src,
+                                              int64_t ld, int i0, int jb, int M, int N,
+                                              int lane) {
   const int sg = lane & 7;
-  uint4 v[8];
 #pragma unroll
   for (int q = 0; q < 8; ++q) {
-    const int gi = i0 + (lane >> 3) + 4 * q;
+    const int r = (lane >> 3) + 4 * q;
+    const int gi = i0 + r;
     const int gj = jb + 8 * sg;
-    v[q] = make_uint4(0, 0, 0, 0);
-    if (gi < M) {
-      const __nv_bfloat16* g = src + int64_t(gi) * ld + gj;
-      if (gj + 8 <= N) {
-        v[q] = *reinterpret_cast<const uint4*>(g);
-      } else {
-        __nv_bfloat16* e = reinterpret_cast<__nv_bfloat16*>(&v[q]);
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-          if (gj + k < N) e[k] = g[k];
-      }
+    int bytes = 0;
+    const __nv_bfloat16* g = src;
+    if (gi < M && gj < N) {
+      g = src + int64_t(gi) * ld + gj;
+      bytes = 2 * min(8, N - gj);
     }
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(
+                     smem_u32(R + r * EP_ROW + 8 * sg)),
+                 "l"(g), "r"(bytes)
+                 : "memory");
   }
-#pragma unroll
-  for (int q = 0; q < 8; ++q)
-    *reinterpret_cast<uint4*>(S + ((lane >> 3) + 4 * q) * EP_ROW + 8 * sg) = v[q];
-  __syncwarp();
-  const uint4* row = reinterpret_cast<const uint4*>(S + lane * EP_ROW);
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+// Waits until at most `pending` committed copy groups of this thread are outstanding.
+template <int PENDING>
+__device__ __forceinline__ void prefetch_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(PENDING) : "memory");
+}
+
+// This lane's row (64 values) of a staged 32 x 64 block.
+__device__ __forceinline__ void read_row(const __nv_bfloat16* R, int lane, float* r) {
+  const uint4* row = reinterpret_cast<const uint4*>(R + lane * EP_ROW);
 #pragma unroll
   for (int k = 0; k < 8; ++k) {
     const uint4 u = row[k];
@@ -377,7 +384,6 @@ __device__ __forceinline__ void load_rows(__nv_bfloat16* S, const __nv_bfloat16*
       r[8 * k + 2 * e + 1] = f.y;
     }
   }
-  __syncwarp();
 }
 
 // Final output of the last product for this lane's row, columns jb..jb+63: U (through the
@@ -463,8 +469,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* ring = smem;
   __nv_bfloat16* staging = reinterpret_cast<__nv_bfloat16*>(smem + STAGES * STAGE_BYTES);
-  uint64_t* bars =
-      reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES + EPI_WARPS * EP_ELEMS * 2);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES +
+                                               EPI_WARPS * EP_BUFS * EP_ELEMS * 2);
   uint64_t* full_bar = bars;                // [STAGES]  (used in the even CTA)
   uint64_t* empty_bar = bars + STAGES;      // [STAGES]
   uint64_t* tfull_bar = bars + 2 * STAGES;  // [2]
@@ -635,7 +641,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   } else {
     // ------------------------------------------------------------ epilogue (both CTAs)
     const int quad = warp & 3;  // TMEM lanes 32*quad .. 32*quad+31 = this warp's rows
-    __nv_bfloat16* S = staging + (warp - 2) * EP_ELEMS;
+    __nv_bfloat16* buf[2] = {staging + (warp - 2) * EP_BUFS * EP_ELEMS,
+                             staging + ((warp - 2) * EP_BUFS + 1) * EP_ELEMS};
     const uint32_t tempty_leader[2] = {mapa_shared(smem_u32(&tempty_bar[0]), 0),
                                        mapa_shared(smem_u32(&tempty_bar[1]), 0)};
     int local = 0;
@@ -649,6 +656,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       const float s = p.scale ? p.scale[slot] : 1.0f;
       OutEntry oe;
       if (G.final_out) oe = p.out_table[slot];
+      const int i0 = t.row0 + HALF * int(cta) + 32 * quad;
+      const int i = i0 + lane;
+      const bool sym = p.stage != NS_APPLY;
+      const bool poly = p.stage == NS_POLY;
+      const __nv_bfloat16* res =
+          reinterpret_cast<const __nv_bfloat16*>(G.res) + int64_t(t.z) * G.res_mstride;
+      // blocks of 64 columns this warp processes: b_first .. nb-1 (earlier blocks of a
+      // symmetric tile lie strictly below the diagonal and are mirrored elsewhere)
+      const int nb = min(BN / 64, (G.N - t.col0 + 63) / 64);
+      int b_first = 0;
+      if (sym)
+        while (b_first < nb && t.col0 + 64 * b_first + 63 < i0) ++b_first;
+      // the first residual block is fetched while the accumulator is still being produced
+      if (poly && b_first < nb)
+        prefetch_rows(buf[b_first & 1], res, G.res_ld, i0, t.col0 + 64 * b_first, G.M, G.N, lane);
 #ifdef MAO_TC_TRACE
       const long long tw2 = clock64();
 #endif
@@ -658,17 +680,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       if (lane == 0 && leader) TRACE_ADD(3, tw2);
       const long long tb = clock64();
 #endif
-      const int i0 = t.row0 + HALF * int(cta) + 32 * quad;
-      const int i = i0 + lane;
-      const bool sym = p.stage != NS_APPLY;
       __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(G.out) + int64_t(t.z) * G.out_mstride;
-      const __nv_bfloat16* res =
-          reinterpret_cast<const __nv_bfloat16*>(G.res) + int64_t(t.z) * G.res_mstride;
       const uint32_t trow = tmem_base + (uint32_t(32 * quad) << 16) + uint32_t(acc * BN);
-      for (int b = 0; b < BN / 64; ++b) {
+      for (int b = b_first; b < nb; ++b) {
         const int jb = t.col0 + 64 * b;
-        if (jb >= G.N) break;
-        if (sym && jb + 63 < i0) continue;  // strictly below the diagonal: mirrored elsewhere
+        __nv_bfloat16* S = buf[b & 1];
         const bool above = jb >= i0 + 32;   // every element strictly above the diagonal
         float w[64];
         tmem_ld32(trow + uint32_t(64 * b), w);
@@ -677,9 +693,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           const float alpha = s * s;
 #pragma unroll
           for (int c = 0; c < 64; ++c) w[c] *= alpha;
-        } else if (p.stage == NS_POLY) {
+        } else if (poly) {
+          // next block's residual in flight while this one is used
+          if (b + 1 < nb) {
+            prefetch_rows(buf[(b + 1) & 1], res, G.res_ld, i0, jb + 64, G.M, G.N, lane);
+            prefetch_wait<1>();
+          } else {
+            prefetch_wait<0>();
+          }
+          __syncwarp();
           float r[64];
-          load_rows(S, res, G.res_ld, i0, jb, G.M, G.N, lane, r);
+          read_row(S, lane, r);
+          __syncwarp();
 #pragma unroll
           for (int c = 0; c < 64; ++c)
             w[c] = __fmaf_rn(p.c, w[c], p.b * r[c]) + (jb + c == i ? p.a : 0.0f);
@@ -712,6 +737,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       }
 #endif
     }
+    prefetch_wait<0>();  // no copy into shared memory may outlive the loop (timeout path)
   }
 
   tc_fence_before();
