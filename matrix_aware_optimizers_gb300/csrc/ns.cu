@@ -60,8 +60,8 @@ bool make_ns_plan(const mao_mat* X, int32_t batch, int32_t compute, NsPlan& plan
     gp.tall = gp.R > gp.C;
     gp.count = int32_t(members[g].size());
     gp.slot0 = slot;
-    gp.ldx = round_up(gp.C, 8);
-    gp.lda = round_up(gp.m, 8);
+    gp.ldx = round_up(gp.C, tc::LD_ALIGN);
+    gp.lda = round_up(gp.m, tc::LD_ALIGN);
     for (int b : members[g]) {
       plan.slot_of[b] = slot;
       plan.input_of.push_back(b);
@@ -70,10 +70,11 @@ bool make_ns_plan(const mao_mat* X, int32_t batch, int32_t compute, NsPlan& plan
     plan.groups.push_back(gp);
   }
   int64_t np = 0;
-  for (int s = 0; s < batch; ++s) {
-    const mao_mat& x = X[plan.input_of[s]];
-    plan.partial_begin[s] = np;
-    np += ceil_div(x.rows * ceil_div(x.cols, 8), kStageUnitsPerBlock);
+  for (const auto& gp : plan.groups) {
+    for (int j = 0; j < gp.count; ++j) {
+      plan.partial_begin[gp.slot0 + j] = np;
+      np += ceil_div(gp.R * (gp.ldx / 8), kStageUnitsPerBlock);
+    }
   }
   plan.partial_begin[batch] = np;
   plan.n_partials = np;
@@ -155,9 +156,11 @@ __global__ void __launch_bounds__(kStageThreads) stage_in_kernel(const __grid_co
   for (int t = 0; t < kStageUnitsPerBlock / kStageThreads; ++t) {
     const int64_t u = u0 + t * kStageThreads + threadIdx.x;
     if (u >= e.units) break;
+    // units cover the padded workspace row: columns >= cols are written as zeros
     const int64_t row = u / e.units_per_row;
     const int64_t col0 = (u - row * e.units_per_row) * 8;
-    const int valid = int(e.cols - col0 < 8 ? e.cols - col0 : 8);
+    const int64_t left = e.cols - col0;
+    const int valid = int(left >= 8 ? 8 : (left > 0 ? left : 0));
     float v[8];
     if (e.vec_src && valid == 8) {
       load8(e.src, row * e.src_ld + col0, e.src_dt, v);
@@ -167,11 +170,7 @@ __global__ void __launch_bounds__(kStageThreads) stage_in_kernel(const __grid_co
     }
 #pragma unroll
     for (int i = 0; i < 8; ++i) sq = __fmaf_rn(v[i], v[i], sq);
-    if (valid == 8) {
-      store8(e.dst, row * e.dst_ld + col0, p.ws_dt, v);
-    } else {
-      for (int i = 0; i < valid; ++i) store_elem(e.dst, row * e.dst_ld + col0 + i, p.ws_dt, v[i]);
-    }
+    store8(e.dst, row * e.dst_ld + col0, p.ws_dt, v);
   }
   // fixed-order block reduction: warp tree, then warp 0 over the warp sums
   __shared__ float wsum[kStageThreads / 32];
@@ -353,10 +352,9 @@ mao_status run_tc_stage(const Buffers& buf, const std::vector<const NsGroupPlan*
     const int64_t xs = g.R * g.ldx, as = g.m * g.lda;
     mao_status st = MAO_OK;
     const void *srcA, *srcB;
-    int64_t colsA, rowsA, ldA, colsB, rowsB, ldB;
+    int64_t rowsA, ldA, rowsB, ldB;
     if (stage == NS_GRAM) {
       srcA = srcB = X;
-      colsA = colsB = g.C;
       rowsA = rowsB = g.R;
       ldA = ldB = g.ldx;
       G.a_mn = G.b_mn = g.tall ? 1 : 0;
@@ -369,7 +367,7 @@ mao_status run_tc_stage(const Buffers& buf, const std::vector<const NsGroupPlan*
       G.syrk = 1;
     } else if (stage == NS_POLY) {
       srcA = srcB = buf.a(g);
-      colsA = colsB = rowsA = rowsB = g.m;
+      rowsA = rowsB = g.m;
       ldA = ldB = g.lda;
       G.a_mn = G.b_mn = 0;
       G.M = G.N = G.K = int32_t(g.m);
@@ -381,14 +379,14 @@ mao_status run_tc_stage(const Buffers& buf, const std::vector<const NsGroupPlan*
       G.res_mstride = as;
       G.syrk = 1;
     } else {
-      if (!g.tall) {  // X' = B X : A-operand B (K-major), B-operand X (MN-major)
-        srcA = buf.b(g); colsA = rowsA = g.m; ldA = g.lda;
-        srcB = X; colsB = g.C; rowsB = g.R; ldB = g.ldx;
+      if (!g.tall) {  // X' = B' X : A-operand B' (K-major), B-operand X (MN-major)
+        srcA = buf.b(g); rowsA = g.m; ldA = g.lda;
+        srcB = X; rowsB = g.R; ldB = g.ldx;
         G.a_mn = 0;
         G.b_mn = 1;
-      } else {        // X' = X B : A-operand X (K-major), B-operand B (K-major)
-        srcA = X; colsA = g.C; rowsA = g.R; ldA = g.ldx;
-        srcB = buf.b(g); colsB = rowsB = g.m; ldB = g.lda;
+      } else {        // X' = X B' : A-operand X (K-major), B-operand B' (K-major)
+        srcA = X; rowsA = g.R; ldA = g.ldx;
+        srcB = buf.b(g); rowsB = g.m; ldB = g.lda;
         G.a_mn = 0;
         G.b_mn = 0;
       }
@@ -402,12 +400,10 @@ mao_status run_tc_stage(const Buffers& buf, const std::vector<const NsGroupPlan*
       G.syrk = 0;
       G.final_out = last ? 1 : 0;
     }
-    // K-major operands load 64 x KBOX_ROWS boxes; MN-major ones 64 x 64 (the 128-byte
-    // swizzle span limits the contiguous dimension to 64 elements)
-    G.a_box_rows = G.a_mn ? 64 : tc::KBOX_ROWS;
-    G.b_box_rows = G.b_mn ? 64 : tc::KBOX_ROWS;
-    st = tc_encode_map(&G.tmA, srcA, colsA, rowsA, ldA, g.count, G.a_box_rows);
-    if (st == MAO_OK) st = tc_encode_map(&G.tmB, srcB, colsB, rowsB, ldB, g.count, G.b_box_rows);
+    // One 4-D map per buffer serves both operand orientations: box = 64 columns x 128 rows
+    // x 2 column chunks; K-major operands step the chunk along K, MN-major ones along M/N.
+    st = tc_encode_map(&G.tmA, srcA, rowsA, ldA, g.count);
+    if (st == MAO_OK) st = tc_encode_map(&G.tmB, srcB, rowsB, ldB, g.count);
     if (st != MAO_OK) return st;
     G.tiles_m = int32_t(ceil_div(G.M, tc::TILE_M));
     G.tiles_n = int32_t(ceil_div(G.N, tc::BN));
@@ -561,7 +557,7 @@ mao_status ns_run(const mao_mat* in, const mao_mat* out, int32_t batch, int32_t 
         e.dst_ld = gp->ldx;
         e.rows = in[b].rows;
         e.cols = in[b].cols;
-        e.units_per_row = ceil_div(in[b].cols, 8);
+        e.units_per_row = gp->ldx / 8;
         e.units = e.units_per_row * in[b].rows;
         e.block_begin = blocks;
         e.partial0 = plan.partial_begin[s];

@@ -52,38 +52,37 @@ namespace tc {
 // the B operand tile per pipeline stage and receives 128 output rows in its TMEM.
 constexpr int TILE_M = 256;      // output rows per tile
 constexpr int BN = 256;          // output columns per tile
-constexpr int BK = 64;           // reduction depth per pipeline stage (one 128-byte swizzle row)
+constexpr int BK = 128;          // reduction depth per pipeline stage
 constexpr int HALF = 128;        // rows (A) / columns (B) of the operand tile held per CTA
-#ifndef MAO_TC_KBOX
-#define MAO_TC_KBOX 128
-#endif
+constexpr int CHUNK = 64;        // columns of one 128-byte swizzle row (bf16)
+constexpr int LD_ALIGN = 64;     // workspace rows are padded (with zeros) to CHUNK columns
 #ifndef MAO_TC_STAGES
-#define MAO_TC_STAGES 5
+#define MAO_TC_STAGES 3
 #endif
-constexpr int KBOX_ROWS = MAO_TC_KBOX;   // rows per TMA box of a K-major operand (64 or 128)
 constexpr int STAGES = MAO_TC_STAGES;
-constexpr int BOX_BYTES = 64 * 64 * 2;            // a 64 x 64 bf16 box (MN-major operands)
-constexpr int A_HALF_BYTES = HALF * BK * 2;       // 16 KB
-constexpr int B_HALF_BYTES = HALF * BK * 2;       // 16 KB
-constexpr int STAGE_BYTES = A_HALF_BYTES + B_HALF_BYTES;
+// Every operand half is one TMA box of 64 x 128 x 2 (two 64-column chunks of 128 rows,
+// chunk c at byte offset c * CHUNK_BYTES): 32 KB.
+constexpr int CHUNK_BYTES = HALF * CHUNK * 2;     // 16 KB
+constexpr int HALF_BYTES = 2 * CHUNK_BYTES;       // 32 KB
+constexpr int STAGE_BYTES = 2 * HALF_BYTES;       // A half + B half
 constexpr int EPI_WARPS = 4;     // one epilogue warp per 32-lane TMEM quadrant
 constexpr int THREADS = 64 + 32 * EPI_WARPS;  // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
 constexpr int TMEM_COLS = 512;   // two 256-column fp32 accumulators
-constexpr int EP_ROW = 72;       // staging pitch (bf16) of a 32 x 64 row-major block: 144 B
-constexpr int EP_COL = 40;       // staging pitch (bf16) of the 64 x 32 transposed block: 80 B
-constexpr int EP_ELEMS = 64 * EP_COL;  // one staging buffer (>= 32 * EP_ROW)
-constexpr int EP_BUFS = 2;             // per epilogue warp: residual prefetch double buffer
+// Epilogue staging: 32 x 64 bf16 row-major blocks (128-byte rows, 16-byte chunks XOR-
+// swizzled by row) and their 64 x 32 transposes (64-byte rows); two buffers per warp.
+constexpr int EP_BYTES = 32 * 64 * 2;             // 4 KB
+constexpr int EP_BUFS = 2;
 constexpr int MAX_GROUPS = 8;
 constexpr size_t SMEM_BYTES = 1024 /*align*/ + size_t(STAGES) * STAGE_BYTES +
-                              size_t(EPI_WARPS) * EP_BUFS * EP_ELEMS * 2 + 256 /*barriers*/;
+                              size_t(EPI_WARPS) * EP_BUFS * EP_BYTES + 256 /*barriers*/;
+static_assert(SMEM_BYTES <= 232448, "shared memory budget of one CTA");
 }  // namespace tc
 
 enum NsStage : int32_t { NS_GRAM = 1, NS_POLY = 2, NS_APPLY = 3 };
 
 struct TcGroup {
-  CUtensorMap tmA;          // operand A source (3-D: cols, rows, matrix)
+  CUtensorMap tmA;          // operand A source (4-D: 64 columns, rows, column chunk, matrix)
   CUtensorMap tmB;          // operand B source
-  int32_t a_box_rows, b_box_rows;  // rows of one TMA box (64 x rows bf16)
   void* out;                // product output buffer base (workspace), bf16
   const void* res;          // residual buffer base (A for NS_POLY, X for NS_APPLY), bf16
   int64_t out_mstride, res_mstride;  // elements between matrices
@@ -106,8 +105,8 @@ struct TcParams {
   unsigned long long timeout_ns; // bound of every barrier wait
 };
 
-mao_status tc_encode_map(CUtensorMap* map, const void* base, int64_t cols, int64_t rows,
-                         int64_t ld, int64_t count, int box_rows);
+mao_status tc_encode_map(CUtensorMap* map, const void* base, int64_t rows, int64_t ld,
+                         int64_t count);
 mao_status tc_gemm_launch(const TcParams& p, cudaStream_t stream);
 
 }  // namespace mao

@@ -12,13 +12,14 @@
 // Tiles of 256 x 256 outputs are computed by a pair of CTAs (thread-block cluster of two,
 // tcgen05 cta_group::2). CTA r of the pair loads rows [128 r, 128 r + 128) of the A
 // operand tile and columns [128 r, 128 r + 128) of the B operand tile into its own shared
-// memory (64x64 or 64x128 bf16 TMA boxes, 128-byte swizzle, 6-stage ring of 32 KB); the
-// even CTA issues M=256, N=256, K=16 products that read both halves; each CTA's TMEM
-// receives its 128 output rows (two 256-column fp32 accumulators, double-buffered).
+// memory: per 128-deep k-block one 32 KB TMA box per operand half (64 columns x 128 rows x
+// two 64-column chunks, 128-byte swizzle), a 3-stage ring of 64 KB; the even CTA issues
+// M=256, N=256, K=16 products that read both halves; each CTA's TMEM receives its 128
+// output rows (two 256-column fp32 accumulators, double-buffered).
 //
 // Roles per CTA (192 threads):
 //   warp 0       TMA producer: lane 0 waits for a free stage (and in the even CTA arms the
-//                pair's full barrier); lane q then issues box q of the stage
+//                pair's full barrier); lanes 0 and 1 then issue the A and B boxes
 //   warp 1       TMEM allocation (both CTAs); in the even CTA one thread issues tcgen05.mma
 //                and multicasts tcgen05.commit to both CTAs' barriers
 //   warps 2..5   epilogue: tcgen05.ld of their 32-lane quadrant, fp32 arithmetic, then
@@ -157,13 +158,13 @@ __device__ __noinline__ void mbar_drain(uint32_t bar, uint32_t parity, uint64_t 
 
 // TMA load into this CTA's shared memory, completing its bytes on a barrier that may live
 // in the peer CTA (cta_group::2 form).
-__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap* map,
+__device__ __forceinline__ void tma_load_4d_pair(uint32_t dst, const CUtensorMap* map,
                                                  uint32_t bar_cluster, int32_t x, int32_t y,
-                                                 int32_t z) {
+                                                 int32_t z, int32_t w) {
   asm volatile(
-      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar_cluster)
+      "cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar_cluster)
       : "memory");
 }
 
@@ -266,33 +267,39 @@ __device__ __forceinline__ void decode_tile(const TcParams& p, int tile, Tile& t
 // Each epilogue warp owns 32 output rows i0..i0+31 (lane = row) and walks its tile's
 // columns in blocks of 64. A block's values pass through a per-warp staging buffer so that
 // every global store instruction writes whole 128-byte rows:
-//   row-major staging   S[r * EP_ROW + c]  (32 x 64 bf16, 144-byte pitch)
-//   transposed staging  S[c * EP_COL + r]  (64 x 32 bf16,  80-byte pitch) for the mirror
+//   row-major staging   32 rows of 128 bytes; 16-byte chunk k of row r sits at chunk
+//                       position k ^ (r & 7), so row-wise and column-wise accesses of the
+//                       warp hit distinct banks
+//   transposed staging  64 rows of 64 bytes (the mirror of a block)
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
   const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
   return *reinterpret_cast<const uint32_t*>(&h);
 }
 
+// Byte offset of 16-byte chunk k of row r in the row-major staging layout.
+__device__ __forceinline__ int srow(int r, int k) { return r * 128 + ((k ^ (r & 7)) << 4); }
+
 // Thread `lane` writes its row's 64 values (bf16) into the row-major staging buffer.
-__device__ __forceinline__ void stage_rows(__nv_bfloat16* S, int lane, const float* w) {
-  uint4* dst = reinterpret_cast<uint4*>(S + lane * EP_ROW);
+__device__ __forceinline__ void stage_rows(uint8_t* S, int lane, const float* w) {
 #pragma unroll
   for (int k = 0; k < 8; ++k)
-    dst[k] = make_uint4(pack_bf16x2(w[8 * k], w[8 * k + 1]), pack_bf16x2(w[8 * k + 2], w[8 * k + 3]),
-                        pack_bf16x2(w[8 * k + 4], w[8 * k + 5]), pack_bf16x2(w[8 * k + 6], w[8 * k + 7]));
+    *reinterpret_cast<uint4*>(S + srow(lane, k)) =
+        make_uint4(pack_bf16x2(w[8 * k], w[8 * k + 1]), pack_bf16x2(w[8 * k + 2], w[8 * k + 3]),
+                   pack_bf16x2(w[8 * k + 4], w[8 * k + 5]), pack_bf16x2(w[8 * k + 6], w[8 * k + 7]));
 }
 
 // Thread `lane` writes its row's 64 values (bf16) as column `lane` of the transposed buffer.
-__device__ __forceinline__ void stage_cols(__nv_bfloat16* S, int lane, const float* w) {
+__device__ __forceinline__ void stage_cols(uint8_t* S, int lane, const float* w) {
+  __nv_bfloat16* T = reinterpret_cast<__nv_bfloat16*>(S);
 #pragma unroll
-  for (int c = 0; c < 64; ++c) S[c * EP_COL + lane] = __float2bfloat16_rn(w[c]);
+  for (int c = 0; c < 64; ++c) T[c * 32 + lane] = __float2bfloat16_rn(w[c]);
 }
 
 // Writes the staged 32 x 64 block to dst rows i0.., columns jb.. (row stride ld). Element
-// (i, j) is written when i < M, j < N and, for a symmetric product, j >= i.
-__device__ __forceinline__ void store_rows(const __nv_bfloat16* S, __nv_bfloat16* dst, int64_t ld,
-                                           int i0, int jb, int M, int N, bool sym, bool above,
+// (i, j) is written when i < M, j < ncols and, for a symmetric product, j >= i.
+__device__ __forceinline__ void store_rows(const uint8_t* S, __nv_bfloat16* dst, int64_t ld,
+                                           int i0, int jb, int M, int ncols, bool sym, bool above,
                                            int lane) {
   const int sg = lane & 7;
 #pragma unroll
@@ -301,23 +308,24 @@ __device__ __forceinline__ void store_rows(const __nv_bfloat16* S, __nv_bfloat16
     const int gi = i0 + r;
     const int gj = jb + 8 * sg;
     if (gi >= M) continue;
-    const uint4 val = *reinterpret_cast<const uint4*>(S + r * EP_ROW + 8 * sg);
+    const uint4 val = *reinterpret_cast<const uint4*>(S + srow(r, sg));
     __nv_bfloat16* g = dst + int64_t(gi) * ld + gj;
-    if (gj + 8 <= N && (!sym || above)) {
+    if (gj + 8 <= ncols && (!sym || above)) {
       *reinterpret_cast<uint4*>(g) = val;
     } else {
       const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&val);
 #pragma unroll
       for (int k = 0; k < 8; ++k)
-        if (gj + k < N && (!sym || gj + k >= gi)) g[k] = e[k];
+        if (gj + k < ncols && (!sym || gj + k >= gi)) g[k] = e[k];
     }
   }
 }
 
 // Writes the transposed staging buffer (the mirror of the block) to dst rows jb..,
-// columns i0..: element (j, i) is written when j < M, i < M and j > i.
-__device__ __forceinline__ void store_cols(const __nv_bfloat16* S, __nv_bfloat16* dst, int64_t ld,
-                                           int i0, int jb, int M, bool above, int lane) {
+// columns i0..: element (j, i) is written when j < M, i < ncols and j > i.
+__device__ __forceinline__ void store_cols(const uint8_t* S, __nv_bfloat16* dst, int64_t ld,
+                                           int i0, int jb, int M, int ncols, bool above,
+                                           int lane) {
   const int sg = lane & 3;
 #pragma unroll
   for (int q = 0; q < 8; ++q) {
@@ -325,15 +333,15 @@ __device__ __forceinline__ void store_cols(const __nv_bfloat16* S, __nv_bfloat16
     const int gj = jb + c;
     const int gi = i0 + 8 * sg;
     if (gj >= M) continue;
-    const uint4 val = *reinterpret_cast<const uint4*>(S + c * EP_COL + 8 * sg);
+    const uint4 val = *reinterpret_cast<const uint4*>(S + c * 64 + 16 * sg);
     __nv_bfloat16* g = dst + int64_t(gj) * ld + gi;
-    if (above && gi + 8 <= M) {
+    if (above && gi + 8 <= ncols) {
       *reinterpret_cast<uint4*>(g) = val;
     } else {
       const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&val);
 #pragma unroll
       for (int k = 0; k < 8; ++k)
-        if (gi + k < M && gj > gi + k) g[k] = e[k];
+        if (gi + k < ncols && gj > gi + k) g[k] = e[k];
     }
   }
 }
@@ -341,9 +349,8 @@ __device__ __forceinline__ void store_cols(const __nv_bfloat16* S, __nv_bfloat16
 // Starts copying the 32 x 64 residual block (rows i0.., columns jb..) into the row-major
 // staging layout of R with asynchronous 16-byte copies (cp.async, zero fill outside the
 // matrix) and commits them as one group.
-__device__ __forceinline__ void prefetch_rows(__nv_bfloat16* R, const __nv_bfloat16* src,
-                                              int64_t ld, int i0, int jb, int M, int N,
-                                              int lane) {
+__device__ __forceinline__ void prefetch_rows(uint8_t* R, const __nv_bfloat16* src, int64_t ld,
+                                              int i0, int jb, int M, int N, int lane) {
   const int sg = lane & 7;
 #pragma unroll
   for (int q = 0; q < 8; ++q) {
@@ -356,8 +363,7 @@ __device__ __forceinline__ void prefetch_rows(__nv_bfloat16* R, const __nv_bfloa
       g = src + int64_t(gi) * ld + gj;
       bytes = 2 * min(8, N - gj);
     }
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(
-                     smem_u32(R + r * EP_ROW + 8 * sg)),
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(R + srow(r, sg))),
                  "l"(g), "r"(bytes)
                  : "memory");
   }
@@ -370,12 +376,11 @@ __device__ __forceinline__ void prefetch_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(PENDING) : "memory");
 }
 
-// This lane's row (64 values) of a staged 32 x 64 block.
-__device__ __forceinline__ void read_row(const __nv_bfloat16* R, int lane, float* r) {
-  const uint4* row = reinterpret_cast<const uint4*>(R + lane * EP_ROW);
+// This lane's row (64 values) of a staged row-major block.
+__device__ __forceinline__ void read_row(const uint8_t* R, int lane, float* r) {
 #pragma unroll
   for (int k = 0; k < 8; ++k) {
-    const uint4 u = row[k];
+    const uint4 u = *reinterpret_cast<const uint4*>(R + srow(lane, k));
     const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
@@ -388,9 +393,8 @@ __device__ __forceinline__ void read_row(const __nv_bfloat16* R, int lane, float
 
 // Final output of the last product for this lane's row, columns jb..jb+63: U (through the
 // slot's output entry) and/or its packed signs, taken from the fp32 values.
-__device__ __forceinline__ void store_final(const OutEntry& e, __nv_bfloat16* S, int i0, int jb,
-                                            int M, int N, int orig_cols, int lane,
-                                            const float* w) {
+__device__ __forceinline__ void store_final(const OutEntry& e, uint8_t* S, int i0, int jb, int M,
+                                            int N, int orig_cols, int lane, const float* w) {
   const int i = i0 + lane;
   if (e.out) {
     if ((e.flags & OUT_VEC) && e.dtype == MAO_BF16) {
@@ -401,15 +405,13 @@ __device__ __forceinline__ void store_final(const OutEntry& e, __nv_bfloat16* S,
       __syncwarp();
     } else if (e.flags & OUT_VEC) {
       // fp32: two 32-column halves, each a 32 x 32 fp32 block of 128-byte rows
-      float* Sf = reinterpret_cast<float*>(S);
-      constexpr int FP = EP_ROW / 2;  // 36 floats = 144 bytes
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        float4* d = reinterpret_cast<float4*>(Sf + lane * FP);
 #pragma unroll
         for (int k = 0; k < 8; ++k)
-          d[k] = make_float4(w[32 * h + 4 * k], w[32 * h + 4 * k + 1], w[32 * h + 4 * k + 2],
-                             w[32 * h + 4 * k + 3]);
+          *reinterpret_cast<float4*>(S + srow(lane, k)) =
+              make_float4(w[32 * h + 4 * k], w[32 * h + 4 * k + 1], w[32 * h + 4 * k + 2],
+                          w[32 * h + 4 * k + 3]);
         __syncwarp();
         const int sg = lane & 7;
 #pragma unroll
@@ -418,7 +420,7 @@ __device__ __forceinline__ void store_final(const OutEntry& e, __nv_bfloat16* S,
           const int gi = i0 + r;
           const int gj = jb + 32 * h + 4 * sg;
           if (gi >= M) continue;
-          const float4 val = *reinterpret_cast<const float4*>(Sf + r * FP + 4 * sg);
+          const float4 val = *reinterpret_cast<const float4*>(S + srow(r, sg));
           float* g = reinterpret_cast<float*>(e.out) + int64_t(gi) * e.ld + gj;
           if (gj + 4 <= N) {
             *reinterpret_cast<float4*>(g) = val;
@@ -468,9 +470,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* ring = smem;
-  __nv_bfloat16* staging = reinterpret_cast<__nv_bfloat16*>(smem + STAGES * STAGE_BYTES);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES +
-                                               EPI_WARPS * EP_BUFS * EP_ELEMS * 2);
+  uint8_t* staging = smem + STAGES * STAGE_BYTES;
+  uint64_t* bars =
+      reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES + EPI_WARPS * EP_BUFS * EP_BYTES);
   uint64_t* full_bar = bars;                // [STAGES]  (used in the even CTA)
   uint64_t* empty_bar = bars + STAGES;      // [STAGES]
   uint64_t* tfull_bar = bars + 2 * STAGES;  // [2]
@@ -526,17 +528,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       Tile t;
       decode_tile(p, tile, t);
       const TcGroup& G = p.g[t.g];
-      const int abox = G.a_box_rows, bbox = G.b_box_rows;
-      const int nbox_a = HALF / abox, nbox_b = HALF / bbox;
-      // this lane's box: operand, tensor map, destination offset and tile coordinate
-      const bool is_a = lane < nbox_a;
-      const bool active = lane < nbox_a + nbox_b;
-      const int q = is_a ? lane : lane - nbox_a;
+      // lane 0 loads this CTA's A half, lane 1 its B half: one 64 x 128 x 2 box each
+      // (K-major: 128 rows, two 64-deep k chunks; MN-major: 128 k rows, two 64-wide chunks)
+      const bool is_a = lane == 0;
+      const bool active = lane < 2;
       const CUtensorMap* map = is_a ? &G.tmA : &G.tmB;
       const int mn = is_a ? G.a_mn : G.b_mn;
-      const int box = is_a ? abox : bbox;
-      const uint32_t off = (is_a ? 0u : uint32_t(A_HALF_BYTES)) + uint32_t(q * box) * 128u;
-      const int rc = (is_a ? t.row0 : t.col0) + HALF * int(cta) + box * q;
+      const uint32_t off = is_a ? 0u : uint32_t(HALF_BYTES);
+      const int rc = (is_a ? t.row0 : t.col0) + HALF * int(cta);  // this CTA's M/N range
       for (int kb = 0; kb < t.nkb; ++kb) {
         int okw = 1;
         if (lane == 0) {
@@ -558,8 +557,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           const uint32_t fb = mapa_shared(smem_u32(&full_bar[stage]), 0);
           const uint32_t dst = smem_u32(ring + stage * STAGE_BYTES) + off;
           const int k0 = kb * BK;
-          if (mn) tma_load_3d_pair(dst, map, fb, rc, k0, t.z);
-          else tma_load_3d_pair(dst, map, fb, k0, rc, t.z);
+          if (mn) tma_load_4d_pair(dst, map, fb, 0, k0, rc / CHUNK, t.z);
+          else tma_load_4d_pair(dst, map, fb, 0, rc, k0 / CHUNK, t.z);
         }
         if (++stage == STAGES) {
           stage = 0;
@@ -608,15 +607,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 #endif
           tc_fence_after();
           const uint32_t a_base = smem_u32(ring + stage * STAGE_BYTES);
-          const uint32_t b_base = a_base + A_HALF_BYTES;
+          const uint32_t b_base = a_base + HALF_BYTES;
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
-            // K-major: 16 k-elements are 32 bytes along the swizzled row.
-            // MN-major: 16 k-rows are two 1024-byte swizzle atoms; 64-wide chunks 8 KB apart.
-            const uint64_t ad = G.a_mn ? smem_desc(a_base + kk * 2048, BOX_BYTES, 1024)
-                                       : smem_desc(a_base + kk * 32, 16, 1024);
-            const uint64_t bd = G.b_mn ? smem_desc(b_base + kk * 2048, BOX_BYTES, 1024)
-                                       : smem_desc(b_base + kk * 32, 16, 1024);
+            // K-major: chunk kk/4 holds k 64*(kk/4).., 16 k-elements are 32 bytes along the
+            //          swizzled row.
+            // MN-major: 16 k-rows are two 1024-byte swizzle atoms; the two 64-wide M/N
+            //          chunks are CHUNK_BYTES apart.
+            const uint32_t koff = uint32_t(kk >> 2) * CHUNK_BYTES + uint32_t(kk & 3) * 32u;
+            const uint64_t ad = G.a_mn ? smem_desc(a_base + kk * 2048, CHUNK_BYTES, 1024)
+                                       : smem_desc(a_base + koff, 16, 1024);
+            const uint64_t bd = G.b_mn ? smem_desc(b_base + kk * 2048, CHUNK_BYTES, 1024)
+                                       : smem_desc(b_base + koff, 16, 1024);
             umma_bf16_pair(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
             issued = true;
           }
@@ -641,8 +643,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   } else {
     // ------------------------------------------------------------ epilogue (both CTAs)
     const int quad = warp & 3;  // TMEM lanes 32*quad .. 32*quad+31 = this warp's rows
-    __nv_bfloat16* buf[2] = {staging + (warp - 2) * EP_BUFS * EP_ELEMS,
-                             staging + ((warp - 2) * EP_BUFS + 1) * EP_ELEMS};
+    uint8_t* buf[2] = {staging + (warp - 2) * EP_BUFS * EP_BYTES,
+                       staging + ((warp - 2) * EP_BUFS + 1) * EP_BYTES};
     const uint32_t tempty_leader[2] = {mapa_shared(smem_u32(&tempty_bar[0]), 0),
                                        mapa_shared(smem_u32(&tempty_bar[1]), 0)};
     int local = 0;
@@ -684,7 +686,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       const uint32_t trow = tmem_base + (uint32_t(32 * quad) << 16) + uint32_t(acc * BN);
       for (int b = b_first; b < nb; ++b) {
         const int jb = t.col0 + 64 * b;
-        __nv_bfloat16* S = buf[b & 1];
+        uint8_t* S = buf[b & 1];
         const bool above = jb >= i0 + 32;   // every element strictly above the diagonal
         float w[64];
         tmem_ld32(trow + uint32_t(64 * b), w);
@@ -715,14 +717,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         if (G.final_out) {
           store_final(oe, S, i0, jb, G.M, G.N, G.orig_cols, lane, w);
         } else {
+          // workspace outputs cover the zero-padded row (columns up to out_ld)
+          const int ncols = int(G.out_ld);
           stage_rows(S, lane, w);
           __syncwarp();
-          store_rows(S, out, G.out_ld, i0, jb, G.M, G.N, sym, above, lane);
+          store_rows(S, out, G.out_ld, i0, jb, G.M, ncols, sym, above, lane);
           __syncwarp();
           if (sym) {
             stage_cols(S, lane, w);
             __syncwarp();
-            store_cols(S, out, G.out_ld, i0, jb, G.M, above, lane);
+            store_cols(S, out, G.out_ld, i0, jb, G.M, ncols, above, lane);
             __syncwarp();
           }
         }
@@ -772,15 +776,18 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 }  // namespace
 
-mao_status tc_encode_map(CUtensorMap* map, const void* base, int64_t cols, int64_t rows,
-                         int64_t ld, int64_t count, int box_rows) {
+mao_status tc_encode_map(CUtensorMap* map, const void* base, int64_t rows, int64_t ld,
+                         int64_t count) {
   auto fn = encode_fn();
-  if (!fn) return MAO_ERR_CUDA;
-  const cuuint64_t dims[3] = {cuuint64_t(cols), cuuint64_t(rows), cuuint64_t(count)};
-  const cuuint64_t strides[2] = {cuuint64_t(ld) * 2, cuuint64_t(rows) * cuuint64_t(ld) * 2};
-  const cuuint32_t box[3] = {64, cuuint32_t(box_rows), 1};
-  const cuuint32_t estr[3] = {1, 1, 1};
-  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+  if (!fn || ld % CHUNK != 0) return MAO_ERR_UNSUPPORTED;
+  // dims: 64 columns of a chunk, rows, column chunks (128 bytes apart), matrices
+  const cuuint64_t dims[4] = {cuuint64_t(CHUNK), cuuint64_t(rows), cuuint64_t(ld / CHUNK),
+                              cuuint64_t(count)};
+  const cuuint64_t strides[3] = {cuuint64_t(ld) * 2, cuuint64_t(CHUNK) * 2,
+                                 cuuint64_t(rows) * cuuint64_t(ld) * 2};
+  const cuuint32_t box[4] = {CHUNK, HALF, 2, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims,
                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
