@@ -370,6 +370,7 @@ mao_status run_tc_stage(const Buffers& buf, const std::vector<const NsGroupPlan*
       rowsA = rowsB = g.m;
       ldA = ldB = g.lda;
       G.a_mn = G.b_mn = 0;
+      G.a_sym = G.b_sym = 1;
       G.M = G.N = G.K = int32_t(g.m);
       G.out = buf.b(g);
       G.out_ld = g.lda;
@@ -384,11 +385,13 @@ mao_status run_tc_stage(const Buffers& buf, const std::vector<const NsGroupPlan*
         srcB = X; rowsB = g.R; ldB = g.ldx;
         G.a_mn = 0;
         G.b_mn = 1;
+        G.a_sym = 1;
       } else {        // X' = X B' : A-operand X (K-major), B-operand B' (K-major)
         srcA = X; rowsA = g.R; ldA = g.ldx;
         srcB = buf.b(g); rowsB = g.m; ldB = g.lda;
         G.a_mn = 0;
         G.b_mn = 0;
+        G.b_sym = 1;
       }
       G.M = int32_t(g.R);
       G.N = int32_t(g.C);
@@ -404,6 +407,8 @@ mao_status run_tc_stage(const Buffers& buf, const std::vector<const NsGroupPlan*
     // x 2 column chunks; K-major operands step the chunk along K, MN-major ones along M/N.
     st = tc_encode_map(&G.tmA, srcA, rowsA, ldA, g.count);
     if (st == MAO_OK) st = tc_encode_map(&G.tmB, srcB, rowsB, ldB, g.count);
+    if (st == MAO_OK && G.out)
+      st = tc_encode_store_map(&G.tmOR, G.out, G.M, G.out_ld, g.count);
     if (st != MAO_OK) return st;
     G.tiles_m = int32_t(ceil_div(G.M, tc::TILE_M));
     G.tiles_n = int32_t(ceil_div(G.N, tc::BN));

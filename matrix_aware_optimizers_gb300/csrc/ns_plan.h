@@ -83,6 +83,7 @@ enum NsStage : int32_t { NS_GRAM = 1, NS_POLY = 2, NS_APPLY = 3 };
 struct TcGroup {
   CUtensorMap tmA;          // operand A source (4-D: 64 columns, rows, column chunk, matrix)
   CUtensorMap tmB;          // operand B source
+  CUtensorMap tmOR;         // workspace output, 64 x 32 blocks, 128-byte swizzle (bulk stores)
   void* out;                // product output buffer base (workspace), bf16
   const void* res;          // residual buffer base (A for NS_POLY, X for NS_APPLY), bf16
   int64_t out_mstride, res_mstride;  // elements between matrices
@@ -90,7 +91,10 @@ struct TcGroup {
   int32_t M, N, K;          // product shape: (M x K) . (K x N)
   int32_t count, slot0;
   int32_t a_mn, b_mn;       // operand stored MN-major (1) or K-major (0)
-  int32_t syrk;             // symmetric result: upper tiles computed, mirrored on store
+  int32_t a_sym, b_sym;     // operand is a symmetric product stored as its upper and
+                            // diagonal 256-tiles: blocks below the diagonal are read
+                            // through the transposed (MN-major) view of the upper block
+  int32_t syrk;             // symmetric result: only upper and diagonal tiles computed
   int32_t tiles_m, tiles_n, tiles_per_mat, tile_begin;
   int32_t final_out;        // last NS_APPLY: write U / signs through the slot's OutEntry
   int32_t orig_cols;        // C of the original matrix (sign-bit indexing)
@@ -107,6 +111,9 @@ struct TcParams {
 
 mao_status tc_encode_map(CUtensorMap* map, const void* base, int64_t rows, int64_t ld,
                          int64_t count);
+// Bulk-store map of a workspace output buffer [count][rows][ld] bf16 (64 x 32 blocks).
+mao_status tc_encode_store_map(CUtensorMap* map, const void* base, int64_t rows, int64_t ld,
+                               int64_t count);
 mao_status tc_gemm_launch(const TcParams& p, cudaStream_t stream);
 
 }  // namespace mao

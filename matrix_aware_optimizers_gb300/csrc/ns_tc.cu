@@ -2,9 +2,12 @@
 //
 // One persistent kernel serves all three products of an iteration (the stage is a launch
 // parameter), over every matrix of up to eight shape groups:
-//   NS_GRAM   A  = alpha * X X^T              (symmetric: upper tiles, mirrored on store)
+//   NS_GRAM   A  = alpha * X X^T              (symmetric: upper and diagonal tiles only)
 //   NS_POLY   B' = a I + b A + c A A          (symmetric; A A = A A^T by symmetry)
 //   NS_APPLY  X' = beta * B' X                (X B' in the tall orientation; B' symmetric)
+// A symmetric result is stored as its upper and diagonal 256 x 256 tiles. A product that
+// reads it takes each 128-deep k-block below the diagonal from the transposed view of the
+// stored upper block (an MN-major load of the same buffer), so no tile is ever mirrored.
 // a X + (b A + c A^2) X is evaluated as (a I + b A + c A^2) X: the identity term is added
 // on the diagonal in the second product's epilogue, so the bf16 operand rounds a + (...)
 // rather than the cancelling (...) alone, and the third product reads no residual.
@@ -23,9 +26,8 @@
 //   warp 1       TMEM allocation (both CTAs); in the even CTA one thread issues tcgen05.mma
 //                and multicasts tcgen05.commit to both CTAs' barriers
 //   warps 2..5   epilogue: tcgen05.ld of their 32-lane quadrant, fp32 arithmetic, then
-//                32 x 64 blocks staged in shared memory and written with coalesced 16-byte
-//                stores (whole 128-byte rows), the mirror of symmetric tiles through a
-//                transposed staging layout
+//                32 x 64 blocks staged in shared memory (128-byte swizzle) and written by
+//                bulk tensor stores
 // Barriers: full[s] (even CTA; both CTAs' loads complete on it), empty[s] (both CTAs),
 // tfull[a] (both), tempty[a] (even CTA; the pair's eight epilogue warps arrive on it).
 // Every wait is bounded by %globaltimer: a wait that gives up sets the device error word
@@ -168,6 +170,31 @@ __device__ __forceinline__ void tma_load_4d_pair(uint32_t dst, const CUtensorMap
       : "memory");
 }
 
+// Bulk tensor store of a staged block (shared -> global) and its group bookkeeping.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int32_t x,
+                                             int32_t y, int32_t z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(x), "r"(y), "r"(z), "r"(src)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// Waits until every committed bulk store of this thread has read its shared-memory source.
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// Waits until every committed bulk store of this thread is complete.
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+// Orders this thread's shared-memory writes before later async-proxy reads of them.
+__device__ __forceinline__ void fence_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
@@ -265,12 +292,10 @@ __device__ __forceinline__ void decode_tile(const TcParams& p, int tile, Tile& t
 // ------------------------------------------------------------------ epilogue
 //
 // Each epilogue warp owns 32 output rows i0..i0+31 (lane = row) and walks its tile's
-// columns in blocks of 64. A block's values pass through a per-warp staging buffer so that
-// every global store instruction writes whole 128-byte rows:
-//   row-major staging   32 rows of 128 bytes; 16-byte chunk k of row r sits at chunk
-//                       position k ^ (r & 7), so row-wise and column-wise accesses of the
-//                       warp hit distinct banks
-//   transposed staging  64 rows of 64 bytes (the mirror of a block)
+// columns in blocks of 64. A block's values pass through a per-warp staging buffer:
+//   32 rows of 128 bytes; 16-byte chunk k of row r sits at chunk position k ^ (r & 7) (the
+//   128-byte swizzle of the output's bulk-store map), so row-wise and column-wise accesses
+//   of the warp hit distinct banks
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
   const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
@@ -289,18 +314,10 @@ __device__ __forceinline__ void stage_rows(uint8_t* S, int lane, const float* w)
                    pack_bf16x2(w[8 * k + 4], w[8 * k + 5]), pack_bf16x2(w[8 * k + 6], w[8 * k + 7]));
 }
 
-// Thread `lane` writes its row's 64 values (bf16) as column `lane` of the transposed buffer.
-__device__ __forceinline__ void stage_cols(uint8_t* S, int lane, const float* w) {
-  __nv_bfloat16* T = reinterpret_cast<__nv_bfloat16*>(S);
-#pragma unroll
-  for (int c = 0; c < 64; ++c) T[c * 32 + lane] = __float2bfloat16_rn(w[c]);
-}
-
-// Writes the staged 32 x 64 block to dst rows i0.., columns jb.. (row stride ld). Element
-// (i, j) is written when i < M, j < ncols and, for a symmetric product, j >= i.
+// Writes the staged 32 x 64 block to dst rows i0.., columns jb.. (row stride ld) with
+// coalesced 16-byte stores; element (i, j) is written when i < M and j < ncols.
 __device__ __forceinline__ void store_rows(const uint8_t* S, __nv_bfloat16* dst, int64_t ld,
-                                           int i0, int jb, int M, int ncols, bool sym, bool above,
-                                           int lane) {
+                                           int i0, int jb, int M, int ncols, int lane) {
   const int sg = lane & 7;
 #pragma unroll
   for (int q = 0; q < 8; ++q) {
@@ -310,38 +327,13 @@ __device__ __forceinline__ void store_rows(const uint8_t* S, __nv_bfloat16* dst,
     if (gi >= M) continue;
     const uint4 val = *reinterpret_cast<const uint4*>(S + srow(r, sg));
     __nv_bfloat16* g = dst + int64_t(gi) * ld + gj;
-    if (gj + 8 <= ncols && (!sym || above)) {
+    if (gj + 8 <= ncols) {
       *reinterpret_cast<uint4*>(g) = val;
     } else {
       const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&val);
 #pragma unroll
       for (int k = 0; k < 8; ++k)
-        if (gj + k < ncols && (!sym || gj + k >= gi)) g[k] = e[k];
-    }
-  }
-}
-
-// Writes the transposed staging buffer (the mirror of the block) to dst rows jb..,
-// columns i0..: element (j, i) is written when j < M, i < ncols and j > i.
-__device__ __forceinline__ void store_cols(const uint8_t* S, __nv_bfloat16* dst, int64_t ld,
-                                           int i0, int jb, int M, int ncols, bool above,
-                                           int lane) {
-  const int sg = lane & 3;
-#pragma unroll
-  for (int q = 0; q < 8; ++q) {
-    const int c = (lane >> 2) + 8 * q;
-    const int gj = jb + c;
-    const int gi = i0 + 8 * sg;
-    if (gj >= M) continue;
-    const uint4 val = *reinterpret_cast<const uint4*>(S + c * 64 + 16 * sg);
-    __nv_bfloat16* g = dst + int64_t(gj) * ld + gi;
-    if (above && gi + 8 <= ncols) {
-      *reinterpret_cast<uint4*>(g) = val;
-    } else {
-      const __nv_bfloat16* e = reinterpret_cast<const __nv_bfloat16*>(&val);
-#pragma unroll
-      for (int k = 0; k < 8; ++k)
-        if (gi + k < ncols && gj > gi + k) g[k] = e[k];
+        if (gj + k < ncols) g[k] = e[k];
     }
   }
 }
@@ -400,8 +392,7 @@ __device__ __forceinline__ void store_final(const OutEntry& e, uint8_t* S, int i
     if ((e.flags & OUT_VEC) && e.dtype == MAO_BF16) {
       stage_rows(S, lane, w);
       __syncwarp();
-      store_rows(S, reinterpret_cast<__nv_bfloat16*>(e.out), e.ld, i0, jb, M, N, false, true,
-                 lane);
+      store_rows(S, reinterpret_cast<__nv_bfloat16*>(e.out), e.ld, i0, jb, M, N, lane);
       __syncwarp();
     } else if (e.flags & OUT_VEC) {
       // fp32: two 32-column halves, each a 32 x 32 fp32 block of 128-byte rows
@@ -533,7 +524,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       const bool is_a = lane == 0;
       const bool active = lane < 2;
       const CUtensorMap* map = is_a ? &G.tmA : &G.tmB;
-      const int mn = is_a ? G.a_mn : G.b_mn;
+      const int mn_cfg = is_a ? G.a_mn : G.b_mn;
+      const int sym_op = is_a ? G.a_sym : G.b_sym;
+      const int op_tile = (is_a ? t.row0 : t.col0) / BN;           // 256-tile of the operand rows
       const uint32_t off = is_a ? 0u : uint32_t(HALF_BYTES);
       const int rc = (is_a ? t.row0 : t.col0) + HALF * int(cta);  // this CTA's M/N range
       for (int kb = 0; kb < t.nkb; ++kb) {
@@ -557,6 +550,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           const uint32_t fb = mapa_shared(smem_u32(&full_bar[stage]), 0);
           const uint32_t dst = smem_u32(ring + stage * STAGE_BYTES) + off;
           const int k0 = kb * BK;
+          // below the diagonal of a symmetric operand: transposed view of the upper block
+          const bool mn = mn_cfg || (sym_op && op_tile > k0 / BN);
           if (mn) tma_load_4d_pair(dst, map, fb, 0, k0, rc / CHUNK, t.z);
           else tma_load_4d_pair(dst, map, fb, 0, rc, k0 / CHUNK, t.z);
         }
@@ -591,8 +586,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         TRACE_ADD(2, tw0);
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + uint32_t(acc * BN);
-        const uint32_t idesc = instr_desc(G.a_mn, G.b_mn);
+        const int a_tile = t.row0 / BN, b_tile = t.col0 / BN;
         for (int kb = 0; kb < t.nkb; ++kb) {
+          const int k_tile = (kb * BK) / BN;
+          const int a_mn = G.a_mn || (G.a_sym && a_tile > k_tile);
+          const int b_mn = G.b_mn || (G.b_sym && b_tile > k_tile);
+          const uint32_t idesc = instr_desc(a_mn, b_mn);
 #ifdef MAO_TC_TRACE
           const long long tw1 = clock64();
 #endif
@@ -615,10 +614,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
             // MN-major: 16 k-rows are two 1024-byte swizzle atoms; the two 64-wide M/N
             //          chunks are CHUNK_BYTES apart.
             const uint32_t koff = uint32_t(kk >> 2) * CHUNK_BYTES + uint32_t(kk & 3) * 32u;
-            const uint64_t ad = G.a_mn ? smem_desc(a_base + kk * 2048, CHUNK_BYTES, 1024)
-                                       : smem_desc(a_base + koff, 16, 1024);
-            const uint64_t bd = G.b_mn ? smem_desc(b_base + kk * 2048, CHUNK_BYTES, 1024)
-                                       : smem_desc(b_base + koff, 16, 1024);
+            const uint64_t ad = a_mn ? smem_desc(a_base + kk * 2048, CHUNK_BYTES, 1024)
+                                     : smem_desc(a_base + koff, 16, 1024);
+            const uint64_t bd = b_mn ? smem_desc(b_base + kk * 2048, CHUNK_BYTES, 1024)
+                                     : smem_desc(b_base + koff, 16, 1024);
             umma_bf16_pair(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
             issued = true;
           }
@@ -660,19 +659,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       if (G.final_out) oe = p.out_table[slot];
       const int i0 = t.row0 + HALF * int(cta) + 32 * quad;
       const int i = i0 + lane;
-      const bool sym = p.stage != NS_APPLY;
       const bool poly = p.stage == NS_POLY;
       const __nv_bfloat16* res =
           reinterpret_cast<const __nv_bfloat16*>(G.res) + int64_t(t.z) * G.res_mstride;
-      // blocks of 64 columns this warp processes: b_first .. nb-1 (earlier blocks of a
-      // symmetric tile lie strictly below the diagonal and are mirrored elsewhere)
+      // blocks of 64 columns of the tile (the last one reaches into the zero padding)
       const int nb = min(BN / 64, (G.N - t.col0 + 63) / 64);
-      int b_first = 0;
-      if (sym)
-        while (b_first < nb && t.col0 + 64 * b_first + 63 < i0) ++b_first;
       // the first residual block is fetched while the accumulator is still being produced
-      if (poly && b_first < nb)
-        prefetch_rows(buf[b_first & 1], res, G.res_ld, i0, t.col0 + 64 * b_first, G.M, G.N, lane);
+      // (into a buffer the previous tile's bulk stores must have finished reading)
+      if (poly && nb > 0) {
+        if (lane == 0) bulk_wait_read();
+        __syncwarp();
+        prefetch_rows(buf[0], res, G.res_ld, i0, t.col0, G.M, G.N, lane);
+      }
 #ifdef MAO_TC_TRACE
       const long long tw2 = clock64();
 #endif
@@ -684,20 +682,32 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 #endif
       __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(G.out) + int64_t(t.z) * G.out_mstride;
       const uint32_t trow = tmem_base + (uint32_t(32 * quad) << 16) + uint32_t(acc * BN);
-      for (int b = b_first; b < nb; ++b) {
+      for (int b = 0; b < nb; ++b) {
         const int jb = t.col0 + 64 * b;
         uint8_t* S = buf[b & 1];
-        const bool above = jb >= i0 + 32;   // every element strictly above the diagonal
+        if (!poly) {  // S was the source of the bulk stores two blocks ago
+          if (lane == 0) bulk_wait_read();
+          __syncwarp();
+        }
         float w[64];
+#ifdef MAO_TC_TRACE
+        long long te = clock64();
+#endif
         tmem_ld32(trow + uint32_t(64 * b), w);
         tmem_ld32(trow + uint32_t(64 * b + 32), w + 32);
+#ifdef MAO_TC_TRACE
+        if (lane == 0 && leader) { TRACE_ADD(9, te); te = clock64(); }
+#endif
         if (p.stage == NS_GRAM) {
           const float alpha = s * s;
 #pragma unroll
           for (int c = 0; c < 64; ++c) w[c] *= alpha;
         } else if (poly) {
-          // next block's residual in flight while this one is used
+          // next block's residual in flight while this one is used (its buffer was the
+          // source of the previous block's bulk stores: those must have read it)
           if (b + 1 < nb) {
+            if (lane == 0) bulk_wait_read();
+            __syncwarp();
             prefetch_rows(buf[(b + 1) & 1], res, G.res_ld, i0, jb + 64, G.M, G.N, lane);
             prefetch_wait<1>();
           } else {
@@ -707,6 +717,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           float r[64];
           read_row(S, lane, r);
           __syncwarp();
+#ifdef MAO_TC_TRACE
+          if (lane == 0 && leader) { TRACE_ADD(12, te); te = clock64(); }
+#endif
 #pragma unroll
           for (int c = 0; c < 64; ++c)
             w[c] = __fmaf_rn(p.c, w[c], p.b * r[c]) + (jb + c == i ? p.a : 0.0f);
@@ -717,18 +730,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         if (G.final_out) {
           store_final(oe, S, i0, jb, G.M, G.N, G.orig_cols, lane, w);
         } else {
-          // workspace outputs cover the zero-padded row (columns up to out_ld)
-          const int ncols = int(G.out_ld);
+          // workspace outputs cover the zero-padded row: the bulk store writes the whole
+          // 64-column block (its padding columns hold zeros)
+#ifdef MAO_TC_TRACE
+          if (lane == 0 && leader) te = clock64();
+#endif
           stage_rows(S, lane, w);
+          fence_async_smem();
           __syncwarp();
-          store_rows(S, out, G.out_ld, i0, jb, G.M, ncols, sym, above, lane);
+          if (lane == 0) tma_store_3d(&G.tmOR, smem_u32(S), jb, i0, t.z);
+#ifdef MAO_TC_TRACE
+          if (lane == 0 && leader) { TRACE_ADD(10, te); te = clock64(); }
+#endif
+          if (lane == 0) bulk_commit();
           __syncwarp();
-          if (sym) {
-            stage_cols(S, lane, w);
-            __syncwarp();
-            store_cols(S, out, G.out_ld, i0, jb, G.M, ncols, above, lane);
-            __syncwarp();
-          }
         }
       }
       tc_fence_before();
@@ -742,6 +757,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 #endif
     }
     prefetch_wait<0>();  // no copy into shared memory may outlive the loop (timeout path)
+    if (lane == 0) bulk_wait_all();  // stores complete before the CTA leaves
+    __syncwarp();
   }
 
   tc_fence_before();
@@ -790,6 +807,21 @@ mao_status tc_encode_map(CUtensorMap* map, const void* base, int64_t rows, int64
   const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims,
                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MAO_OK : MAO_ERR_UNSUPPORTED;
+}
+
+mao_status tc_encode_store_map(CUtensorMap* map, const void* base, int64_t rows, int64_t ld,
+                               int64_t count) {
+  auto fn = encode_fn();
+  if (!fn) return MAO_ERR_UNSUPPORTED;
+  const cuuint64_t dims[3] = {cuuint64_t(ld), cuuint64_t(rows), cuuint64_t(count)};
+  const cuuint64_t strides[2] = {cuuint64_t(ld) * 2, cuuint64_t(rows) * cuuint64_t(ld) * 2};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const cuuint32_t box[3] = {64, 32, 1};  // 32 rows of 128 bytes, 128-byte swizzle
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? MAO_OK : MAO_ERR_UNSUPPORTED;
 }
