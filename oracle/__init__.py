@@ -33,6 +33,8 @@ against something other than itself):
                            cubic convergence to scipy's polar factor, invariants
   muon.sign_of/pack_signs  hand-computed words (tests/golden/pack_signs.txt)
   muon.majority_vote       exhaustive brute force over all sign patterns (W_n <= 8)
+  muon.int8_sum_vote       brute-force integer sums; equals the packed-bit vote on all patterns
+  muon.post_vote_polar     Newton-Schulz pins (it is newton_schulz on the +-1 matrix)
   muon.apply_update        hand-computed rounding table (tests/golden/update_rounding.txt)
   muon.sign_muon_step      composition checked against an SVD-route recomputation
 
@@ -51,6 +53,8 @@ from .muon import (
     pack_signs_loop,
     unpack_signs,
     majority_vote,
+    int8_sum_vote,
+    post_vote_polar,
     apply_update,
     apply_update_f64,
     sign_muon_step,
@@ -61,6 +65,7 @@ from .muon import (
 __all__ = [
     "bf16_rne", "fma_f32", "to_f32", "QUINTIC", "CUBIC", "momentum",
     "frobenius_normalise", "newton_schulz", "sign_of", "pack_signs",
-    "pack_signs_loop", "unpack_signs", "majority_vote", "apply_update",
+    "pack_signs_loop", "unpack_signs", "majority_vote", "int8_sum_vote", "post_vote_polar",
+    "apply_update",
     "apply_update_f64", "sign_muon_step", "muon_step", "ns_dense_flops",
 ]

@@ -144,6 +144,22 @@ def majority_vote(worker_words, nbits):
     return pack_signs(vote)
 
 
+def int8_sum_vote(S_workers):
+    """All-reduce variant of the vote ([SignMuon] §2 step 3 "Variante All-Reduce"):
+    signs travel as int8 +-1, an integer SUM over the workers gives sum_m S^(m), and the
+    local threshold sign(.) with ties -> +1 gives S_bar. Returns (sums, S_bar)."""
+    total = np.zeros(np.asarray(S_workers[0]).shape, dtype=np.int64)
+    for S in S_workers:
+        total += np.asarray(S, dtype=np.int64)
+    return total, np.where(total >= 0, 1, -1).astype(np.int8)
+
+
+def post_vote_polar(S_bar, steps=5, coeffs=QUINTIC, eps=1e-7):
+    """Optional local polar step on the aggregated sign matrix ([SignMuon] §2 step 5):
+    Newton-Schulz applied to S_bar (+-1 entries) before the update."""
+    return newton_schulz(np.asarray(S_bar, dtype=np.float64), steps, coeffs, eps)
+
+
 def apply_update(W, D, lr, store="f32"):
     """W <- W - eta * D as one fp32 fused multiply-add, rounded to ``store``.
 
@@ -159,23 +175,40 @@ def apply_update_f64(W, D, lr):
 
 
 def sign_muon_step(W, Ms, Gs, mu, lr, steps=5, coeffs=QUINTIC, eps=1e-7,
-                   m_store="f32", w_store="f32"):
-    """One Sign-Muon step over W_n simulated workers ([SignMuon] §2, 1-bit all-gather variant).
+                   m_store="f32", w_store="f32", variant="bits", post_polar=False):
+    """One Sign-Muon step over W_n simulated workers ([SignMuon] §2).
 
-    Returns a dict with every intermediate: per-worker momentum, polar factor U,
-    signs, packed words, the packed vote and the updated W.
+    variant "bits": the 1-bit all-gather variant (packed words, vote on the words);
+    variant "int8": the integer SUM all-reduce variant (int8 sums, then the threshold).
+    post_polar: the optional local polar step of [SignMuon] §2 step 5; the update is then
+    W - eta * polar(S_bar) in fp64 (Newton–Schulz with the same steps and coefficients).
+
+    Returns a dict with every intermediate: per-worker momentum, polar factor U, signs,
+    the aggregation's buffers, S_bar, (U_bar) and the updated W.
     """
+    if variant not in ("bits", "int8"):
+        raise ValueError(variant)
     Wn = len(Ms)
     nbits = int(np.asarray(W).size)
     M_new = [momentum(Ms[m], Gs[m], mu, m_store) for m in range(Wn)]
     U = [newton_schulz(M_new[m], steps, coeffs, eps) for m in range(Wn)]
     S = [sign_of(u) for u in U]
-    words = np.stack([pack_signs(s) for s in S])
-    vote = majority_vote(words, nbits)
-    S_bar = unpack_signs(vote, nbits).reshape(np.asarray(W).shape)
-    W_new = apply_update(W, S_bar, lr, w_store)
-    return {"M": M_new, "U": U, "S": S, "words": words, "vote": vote,
-            "S_bar": S_bar, "W": W_new}
+    out = {"M": M_new, "U": U, "S": S}
+    if variant == "bits":
+        words = np.stack([pack_signs(s) for s in S])
+        vote = majority_vote(words, nbits)
+        S_bar = unpack_signs(vote, nbits).reshape(np.asarray(W).shape)
+        out.update(words=words, vote=vote)
+    else:
+        sums, S_bar = int8_sum_vote(S)
+        out.update(sums=sums)
+    out["S_bar"] = S_bar
+    if post_polar:
+        out["U_bar"] = post_vote_polar(S_bar, steps, coeffs, eps)
+        out["W"] = apply_update_f64(W, out["U_bar"], lr)
+    else:
+        out["W"] = apply_update(W, S_bar, lr, w_store)
+    return out
 
 
 def muon_step(Ws, Ms, Gs, mu, lr, steps=5, coeffs=QUINTIC, eps=1e-7,

@@ -307,3 +307,62 @@ def test_sign_muon_step_composition():
 def test_dense_flop_count():
     # (4 m^2 n + 2 m^3) per iteration: 64 x 128, 5 steps
     assert oracle.ns_dense_flops(64, 128, 5) == 5 * (4 * 64 * 64 * 128 + 2 * 64 ** 3) == 13_107_200
+
+
+# --------------------------------------------- int8 all-reduce variant, post-vote polar
+
+@pytest.mark.parametrize("Wn", [1, 2, 3, 4, 7, 8])
+def test_int8_sum_vote_brute_force_and_bit_vote(Wn):
+    patterns = np.array(list(itertools.product([-1, 1], repeat=Wn)), np.int8)  # [2^Wn][Wn]
+    S = [patterns[:, m] for m in range(Wn)]
+    sums, vote = oracle.int8_sum_vote(S)
+    for i, p in enumerate(patterns):
+        assert sums[i] == int(sum(int(x) for x in p))
+        assert vote[i] == (1 if list(p).count(1) >= list(p).count(-1) else -1)
+    # the int8 all-reduce variant and the 1-bit all-gather variant decide identically
+    words = np.stack([oracle.pack_signs(s) for s in S])
+    bits_vote = oracle.unpack_signs(oracle.majority_vote(words, len(patterns)), len(patterns))
+    assert np.array_equal(vote, bits_vote)
+
+
+def test_post_vote_polar_is_ns_of_sign_matrix():
+    rng = np.random.default_rng(11)
+    S_bar = rng.choice(np.array([-1, 1], np.int8), (12, 20))
+    got = oracle.post_vote_polar(S_bar, 5, QUINTIC)
+    assert np.linalg.norm(got - _ns_by_svd(S_bar.astype(np.float64), 5, QUINTIC)) <= 1e-10 * np.linalg.norm(got)
+
+
+@pytest.mark.parametrize("Wn", [2, 3, 5])
+def test_sign_muon_step_variants_agree(Wn):
+    # the all-reduce (int8) and all-gather (1-bit) variants are two encodings of one vote
+    rng = np.random.default_rng(20 + Wn)
+    R, C = 7, 9
+    W = rng.standard_normal((R, C)).astype(np.float32) * 0.02
+    Ms = [rng.standard_normal((R, C)).astype(np.float32) for _ in range(Wn)]
+    Gs = [rng.standard_normal((R, C)).astype(np.float32) for _ in range(Wn)]
+    a = oracle.sign_muon_step(W, Ms, Gs, 0.9, 1e-3, 3, QUINTIC, variant="bits")
+    b = oracle.sign_muon_step(W, Ms, Gs, 0.9, 1e-3, 3, QUINTIC, variant="int8")
+    assert np.array_equal(a["S_bar"], b["S_bar"]) and np.array_equal(a["W"], b["W"])
+    # the int8 sums are the counts: (#plus - #minus), odd worker counts never tie
+    tot = sum(np.where(u < 0, -1, 1) for u in a["U"])
+    assert np.array_equal(b["sums"], tot)
+    if Wn % 2:
+        assert np.all(b["sums"] != 0)
+
+
+def test_sign_muon_step_post_polar_reaches_polar_of_vote():
+    # with the cubic iteration run long enough, the post-vote direction is the polar factor
+    # of S_bar (scipy), and the update moves W by exactly -eta times it
+    scipy_linalg = pytest.importorskip("scipy.linalg")
+    rng = np.random.default_rng(31)
+    R, C, Wn = 6, 11, 3
+    W = rng.standard_normal((R, C)).astype(np.float32)
+    Ms = [rng.standard_normal((R, C)).astype(np.float32) for _ in range(Wn)]
+    Gs = [rng.standard_normal((R, C)).astype(np.float32) for _ in range(Wn)]
+    out = oracle.sign_muon_step(W, Ms, Gs, 0.9, 0.5, 60, (1.5, -0.5, 0.0), variant="int8",
+                                post_polar=True)
+    Q, _ = scipy_linalg.polar(out["S_bar"].astype(np.float64).T)  # C x R, orthonormal columns
+    assert np.allclose(out["U_bar"], Q.T, atol=1e-9)
+    assert np.allclose(out["W"], W.astype(np.float64) - 0.5 * Q.T, atol=1e-9)
+    # rows of the polar factor of a full-row-rank matrix are orthonormal
+    assert np.allclose(out["U_bar"] @ out["U_bar"].T, np.eye(R), atol=1e-9)
