@@ -41,6 +41,10 @@ def parse_args():
     ap.add_argument("--impl", default="mao", choices=["mao", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="CPU work budget of the oracle baseline sample")
+    ap.add_argument("--variant", default="bits", choices=["bits", "int8"],
+                    help="Sign-Muon aggregation: 1-bit all-gather (bits) or int8 SUM all-reduce")
+    ap.add_argument("--post-polar", action="store_true",
+                    help="Sign-Muon: Newton-Schulz on the aggregated signs before the update")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
@@ -136,11 +140,18 @@ class ClockSampler:
 class Step:
     """Device buffers and the sequence of C-ABI calls of one optimizer step."""
 
-    def __init__(self, wl, inputs, device):
+    def __init__(self, wl, inputs, device, variant="bits", post_polar=False):
+        """variant: "bits" (1-bit all-gather) or "int8" (integer SUM all-reduce) aggregation
+        of a Sign-Muon workload; post_polar: the optional Newton–Schulz step on S_bar."""
         import torch
         import matrix_aware_optimizers_gb300 as mao
+        if wl.kind != "sign" and (variant != "bits" or post_polar):
+            raise ValueError("the aggregation variants apply to Sign-Muon workloads only")
+        if variant not in ("bits", "int8"):
+            raise ValueError(variant)
         self.mao = mao
         self.wl = wl
+        self.variant, self.post_polar = variant, post_polar
         self.W, self.M, self.G = inputs["W"], inputs["M"], inputs["G"]
         self.dev = device
         if wl.kind == "sign":
@@ -148,10 +159,19 @@ class Step:
             self.nbits = R * C
             nw = mao.packed_words(R, C)
             stride = (nw + 3) // 4 * 4
-            self.words = torch.zeros((wl.workers, stride), dtype=torch.int32, device=device)
             self.vote = torch.zeros(stride, dtype=torch.int32, device=device)
-            self.bits = [self.words[m, :nw] for m in range(wl.workers)]
-            self.U = [None] * wl.workers
+            if variant == "bits":
+                self.words = torch.zeros((wl.workers, stride), dtype=torch.int32, device=device)
+                self.bits = [self.words[m, :nw] for m in range(wl.workers)]
+                self.U = [None] * wl.workers
+            else:
+                # U of each worker, then its int8 signs in the all-reduce buffer layout
+                self.U = [torch.empty_like(m) for m in self.M]
+                s_stride = (self.nbits + 15) // 16 * 16
+                self.s8 = torch.zeros((wl.workers, s_stride), dtype=torch.int8, device=device)
+                self.sbar = torch.zeros(self.nbits, dtype=torch.int8, device=device)
+            if post_polar:
+                self.U_bar = torch.empty_like(self.W[0])
         else:
             self.U = [torch.empty_like(w) for w in self.W]
         self.ws = mao.workspace(self.M, wl.compute, device)
@@ -161,19 +181,34 @@ class Step:
 
     def ns(self):
         wl = self.wl
-        if wl.kind == "sign":
+        if wl.kind == "sign" and self.variant == "bits":
             self.mao.ns_orthogonalize(self.M, self.U, wl.steps, wl.coeffs, wl.eps, wl.compute,
                                       sign_bits=self.bits, ws=self.ws)
         else:
             self.mao.ns_orthogonalize(self.M, self.U, wl.steps, wl.coeffs, wl.eps, wl.compute,
                                       ws=self.ws)
+            if wl.kind == "sign":
+                for m in range(wl.workers):
+                    self.mao.sign_int8(self.U[m], self.s8[m, : self.nbits].view(self.U[m].shape))
 
     def update(self):
-        if self.wl.kind == "sign":
+        wl = self.wl
+        if wl.kind != "sign":
+            self.mao.apply_update(self.W, wl.lr, U=self.U)
+            return
+        if self.variant == "bits":
             self.mao.majority_vote_packed(self.words, self.nbits, self.vote)
-            self.mao.apply_update(self.W, self.wl.lr, vote=self.vote)
+            s_bar = self.mao.PackedSigns(self.vote, *self.W[0].shape)
         else:
-            self.mao.apply_update(self.W, self.wl.lr, U=self.U)
+            self.mao.majority_vote_int8(self.s8, self.nbits, s_bar=self.sbar if self.post_polar else None,
+                                        vote=None if self.post_polar else self.vote)
+            s_bar = self.sbar.view(self.W[0].shape)
+        if self.post_polar:
+            self.mao.ns_orthogonalize(s_bar, self.U_bar, wl.steps, wl.coeffs, wl.eps, wl.compute,
+                                      ws=self.ws)
+            self.mao.apply_update(self.W, wl.lr, U=self.U_bar)
+        else:
+            self.mao.apply_update(self.W, wl.lr, vote=self.vote)
 
     def __call__(self):
         self.momentum()
@@ -182,9 +217,15 @@ class Step:
 
 
 def stage_bytes(wl, step):
-    """Algorithmic HBM bytes of the elementwise stages per step."""
+    """Algorithmic HBM bytes of the elementwise stages per step (the update stage's figure is
+    None when it holds the post-vote Newton–Schulz, which is not elementwise)."""
     mom = sum(m.numel() * (2 * esize(m.dtype) + esize(g.dtype)) for m, g in zip(step.M, step.G))
-    if wl.kind == "sign":
+    if wl.kind == "sign" and step.post_polar:
+        upd = None
+    elif wl.kind == "sign" and step.variant == "int8":
+        n = step.nbits  # W_n int8 signs read, packed vote written and read, W read + written
+        upd = sum(w.numel() * 2 * esize(w.dtype) for w in step.W) + 2 * (n // 8) + wl.workers * n
+    elif wl.kind == "sign":
         n = step.nbits
         upd = sum(w.numel() * 2 * esize(w.dtype) for w in step.W) + n // 8 + wl.workers * n // 8
     else:
@@ -194,7 +235,7 @@ def stage_bytes(wl, step):
 
 # ------------------------------------------------------------------ oracle arm
 
-def oracle_sample(wl, host, budget_s, max_items=None):
+def oracle_sample(wl, host, budget_s, max_items=None, variant="bits", post_polar=False):
     """Time the fp64 oracle on whole matrices of the workload (cycling) for ~budget_s.
 
     Returns (fraction of one step processed, seconds, description)."""
@@ -202,7 +243,8 @@ def oracle_sample(wl, host, budget_s, max_items=None):
 
     import oracle
     shapes = [tuple(x.shape) for x in host["M"]] if wl.kind == "muon" else [tuple(host["W"][0].shape)]
-    total = dense_flops(shapes, wl.steps) * (wl.workers if wl.kind == "sign" else 1)
+    total = dense_flops(shapes, wl.steps) * (wl.workers + (1 if post_polar else 0)
+                                             if wl.kind == "sign" else 1)
     store = "bf16" if wl.m_dtype.itemsize == 2 else "f32"
     wstore = "bf16" if wl.w_dtype.itemsize == 2 else "f32"
     done_flops, t_used, items = 0, 0.0, 0
@@ -219,12 +261,20 @@ def oracle_sample(wl, host, budget_s, max_items=None):
             # one worker's momentum + NS + sign/pack; the vote and update run with the last
             M = oracle.momentum(host["M"][i], host["G"][i], wl.mu, store)
             U = oracle.newton_schulz(M, wl.steps, wl.coeffs, wl.eps)
-            words[i] = oracle.pack_signs(oracle.sign_of(U))
+            S_m = oracle.sign_of(U)
+            words[i] = oracle.pack_signs(S_m) if variant == "bits" else S_m
             done_flops += dense_flops(shapes, wl.steps)
             if i == n_items - 1 and len(words) == n_items:
-                vote = oracle.majority_vote(np.stack([words[m] for m in range(n_items)]), U.size)
-                S = oracle.unpack_signs(vote, U.size).reshape(U.shape)
-                oracle.apply_update(host["W"][0], S, wl.lr, wstore)
+                if variant == "bits":
+                    vote = oracle.majority_vote(np.stack([words[m] for m in range(n_items)]), U.size)
+                    S = oracle.unpack_signs(vote, U.size).reshape(U.shape)
+                else:
+                    S = oracle.int8_sum_vote([words[m] for m in range(n_items)])[1]
+                if post_polar:
+                    U_bar = oracle.post_vote_polar(S, wl.steps, wl.coeffs, wl.eps)
+                    oracle.apply_update_f64(host["W"][0], U_bar, wl.lr)
+                else:
+                    oracle.apply_update(host["W"][0], S, wl.lr, wstore)
         t_used += time.perf_counter() - t0
         items += 1
         i = (i + 1) % n_items
@@ -265,11 +315,12 @@ def run_reference(args, wl):
         shapes = [(4096, 4096)] * 4 + [(4096, 14336), (14336, 4096), (4096, 14336)]
     inputs = workloads.generate(wl, "cpu", shapes=shapes if wl.index == 4 else None)
     host = host_copy(inputs)
+    var = dict(variant=args.variant, post_polar=args.post_polar)
     for _ in range(Wu):
-        oracle_sample(wl, host, 0.0, max_items=1)
+        oracle_sample(wl, host, 0.0, max_items=1, **var)
     frac, secs = 0.0, 0.0
     for _ in range(K):
-        f, s, _ = oracle_sample(wl, host, 0.0, max_items=1)
+        f, s, _ = oracle_sample(wl, host, 0.0, max_items=1, **var)
         frac += f
         secs += s
     value = frac / secs
@@ -277,7 +328,8 @@ def run_reference(args, wl):
         "impl": "reference", "metric": metric_name(wl), "value": value, "unit": "steps/s",
         "n_gpus": args.gpus, "steps": K, "warmup": Wu, "ms_per_step": 1000.0 / value,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "f64", "data": "synthetic", "config": config_block(wl, None),
+        "dtype": "f64", "data": "synthetic",
+        "config": config_block(wl, None, args.variant, args.post_polar),
         "cpu_baseline": {"value": value, "unit": "steps/s", "cores": blas_threads(),
                          "kind": "oracle",
                          "sample": "each step: one matrix of the workload (cycling), fp64 numpy "
@@ -310,11 +362,15 @@ def metric_name(wl):
         " (%s); NS TFLOP/s; elementwise GB/s" % wl.name
 
 
-def config_block(wl, step_bytes):
+def config_block(wl, step_bytes, variant="bits", post_polar=False):
     c = {"workload": wl.name, "kind": wl.kind, "matrices": len(wl.shapes),
          "elements": wl.elements, "workers": wl.workers, "ns_steps": wl.steps,
          "coeffs": list(wl.coeffs), "mu": wl.mu, "lr": wl.lr, "compute": wl.compute,
          "parallelism": "replicas: each rank steps its own copy of the workload"}
+    if wl.kind == "sign":
+        c["aggregation"] = ("1-bit packed all-gather + local vote" if variant == "bits" else
+                            "int8 SUM all-reduce + local threshold")
+        c["post_vote_polar"] = bool(post_polar)
     if step_bytes is not None:
         c["l2"] = ("inputs larger than L2: %.0f MB of matrices touched per step vs 129 MB L2"
                    % (step_bytes / 1e6))
@@ -327,6 +383,8 @@ def main():
     args = parse_args()
     from matrix_aware_optimizers_gb300 import workloads
     wl = workloads.workload(args.config)
+    if wl.kind != "sign" and (args.variant != "bits" or args.post_polar):
+        sys.exit("--variant / --post-polar apply to the Sign-Muon workloads (--config 1 or 3)")
     if args.impl == "reference":
         run_reference(args, wl)
         return
@@ -347,7 +405,7 @@ def main():
     K = args.steps if args.steps is not None else DEFAULT_STEPS[wl.index]
     Wu = max(3, args.warmup if args.warmup is not None else DEFAULT_WARMUP[wl.index])
     inputs = workloads.generate(wl, dev, seed=(wl.index - 1) + 1000 * rank)
-    step = Step(wl, inputs, dev)
+    step = Step(wl, inputs, dev, args.variant, args.post_polar)
     stream = torch.cuda.current_stream()
 
     def barrier():
@@ -362,7 +420,7 @@ def main():
     mao.sync_status()
 
     # ---------------- timed region: K whole steps, inputs resident in HBM
-    n_tc_per_step = 3 * wl.steps * ((len(set(wl.shapes)) + 7) // 8)
+    n_tc_per_step = 3 * wl.steps * ((len(set(wl.shapes)) + 7) // 8 + (1 if args.post_polar else 0))
     mao.profile_begin(K * n_tc_per_step)
     launches0 = mao.launch_count()
     clocks = ClockSampler(local)
@@ -405,9 +463,11 @@ def main():
     shapes = [tuple(m.shape) for m in step.M]
     alg = alg_flops(shapes, wl.steps)
     dense = dense_flops(shapes, wl.steps)
+    # the post-vote polar step is one more Newton–Schulz on a matrix of W's shape
+    alg_tc = alg + (alg_flops([tuple(step.W[0].shape)], wl.steps) if args.post_polar else 0)
     tc_total_ms = sum(tc_ms)
     if wl.compute == "bf16" and tc_ms:
-        tflops = alg * K / (tc_total_ms / 1000.0) / 1e12
+        tflops = alg_tc * K / (tc_total_ms / 1000.0) / 1e12
         peak = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
         roof = {"kernel": "ns_tc_kernel", "bound": "tensor", "achieved": tflops, "peak": peak,
                 "unit": "TFLOP/s", "frac": tflops / peak, "traffic": None,
@@ -423,7 +483,7 @@ def main():
     else:
         hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
         mom_b, upd_b = stage_bytes(wl, step)
-        gbs = (mom_b + upd_b) / ((st_mom + st_upd) / 1000.0) / 1e9
+        gbs = (mom_b + (upd_b or 0)) / ((st_mom + (st_upd if upd_b else 0)) / 1000.0) / 1e9
         roof = {"kernel": "elementwise stages", "bound": "hbm", "achieved": gbs, "peak": hbm,
                 "unit": "GB/s", "frac": gbs / hbm, "traffic": None,
                 "peak_source": "%s hbm_gbs" % peak_src}
@@ -436,12 +496,13 @@ def main():
         "metric": metric_name(wl), "value": value, "unit": "steps/s", "n_gpus": world,
         "steps": K, "warmup": Wu, "ms_per_step": ms_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": wl.compute, "data": "synthetic",
-        "config": config_block(wl, touched),
+        "config": config_block(wl, touched, args.variant, args.post_polar),
         "ns_tflops_dense": dense / (st_ns / 1000.0) / 1e12,
         "ns_tflops_alg": alg / (st_ns / 1000.0) / 1e12,
         "stages_ms": {"momentum": st_mom, "ns": st_ns, "update": st_upd},
         "elementwise_gbs": {"momentum": mom_b / (st_mom / 1000.0) / 1e9,
-                            "update": upd_b / (st_upd / 1000.0) / 1e9, "peak": hbm},
+                            "update": upd_b / (st_upd / 1000.0) / 1e9 if upd_b else None,
+                            "peak": hbm},
         "roofline": roof,
         "gpu_launches": launches,
         "clocks": clk,
@@ -457,7 +518,8 @@ def main():
         host = host_copy(workloads.generate(
             wl, "cpu", shapes=None if wl.index != 4 else
             [(4096, 4096)] * 4 + [(4096, 14336), (14336, 4096), (4096, 14336)]))
-        frac, secs, desc = oracle_sample(wl, host, args.cpu_seconds)
+        frac, secs, desc = oracle_sample(wl, host, args.cpu_seconds, variant=args.variant,
+                                         post_polar=args.post_polar)
         line["cpu_baseline"] = {"value": frac / secs, "unit": "steps/s", "cores": blas_threads(),
                                 "kind": "oracle", "sample": desc + ", %.1f s" % secs}
     if rank == 0:

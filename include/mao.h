@@ -11,6 +11,14 @@
  *   update        W <- W - eta*S_bar  (Sign-Muon)                 apply_update
  *                 W <- W - eta*U      (Muon)
  *
+ * and the two variants the Sign-Muon page describes beside that path:
+ *
+ *   int8 signs    S = sign(U) as int8 +-1                         sign_int8
+ *   SUM + vote    sum_m S^(m) in int8, then S_bar = sign(sum)     majority_vote_int8
+ *   polar step    U_bar ~ polar(S_bar) (optional, local)          ns_orthogonalize with an
+ *                                                                 MAO_I8 / MAO_SIGN1 input
+ *   update        W <- W - eta*U_bar                              apply_update (U form)
+ *
  * Sources, cited by page title and section:
  *   [SignMuon] "Resumo Técnico: SignMuon: Otimização Distribuída de Muon com Eficiência de
  *              Comunicação" (gist.science, paper 2605.16311), §2 "Metodologia: Sign-Muon".
@@ -55,7 +63,16 @@ typedef enum mao_status {
   MAO_ERR_TIMEOUT = 6       /* a device-side wait gave up (reported by mao_sync_status) */
 } mao_status;
 
-typedef enum mao_dtype { MAO_F32 = 0, MAO_BF16 = 1 } mao_dtype;
+/*
+ * MAO_F32 and MAO_BF16 are storage types of every matrix argument. MAO_I8 and MAO_SIGN1 are
+ * accepted only as the INPUT of ns_orthogonalize / ns_orthogonalize_noalloc (the optional
+ * polar step on an aggregated sign matrix):
+ *   MAO_I8     int8 values, element (i, j) at (int8_t*)data + i*ld + j (any int8 value is
+ *              taken as its integer; a sign matrix holds -1 / +1);
+ *   MAO_SIGN1  packed signs in the layout of the header comment (uint32 words, 4-byte
+ *              aligned data); ld must equal cols; bit 1 -> +1.0, bit 0 -> -1.0.
+ */
+typedef enum mao_dtype { MAO_F32 = 0, MAO_BF16 = 1, MAO_I8 = 2, MAO_SIGN1 = 3 } mao_dtype;
 
 typedef struct mao_mat {
   void* data;     /* device pointer, row-major */
@@ -101,7 +118,9 @@ size_t ns_workspace_bytes(const mao_mat* X, int32_t batch, int32_t compute_dtype
  *   The last two products are evaluated as B' = a_k I + b_k A + c_k A A, X = B' X (the same
  *   polynomial; the bf16 operand B' then rounds a + ... instead of the smaller-margin B).
  *
- *   in[b]        f32 or bf16 input (the momentum); read only.
+ *   in[b]        f32 or bf16 input (the momentum); read only. For the optional polar step
+ *                on an aggregated sign matrix ([SignMuon] §2 step 5) the input may also be
+ *                MAO_I8 or MAO_SIGN1 (see mao_dtype); it is converted exactly on staging.
  *   out[b]       f32 or bf16 output U, same rows/cols as in[b]; out[b].data may be NULL when
  *                sign_bits is given (signs only). out may alias in (in-place).
  *   steps        1..64 iterations.
@@ -171,6 +190,36 @@ mao_status sign_pack_bits(const mao_mat* U, uint32_t* bits, void* stream);
 mao_status majority_vote_packed(const uint32_t* bits, int32_t n_workers,
                                 int64_t worker_stride_words, int64_t nbits, uint32_t* vote,
                                 void* stream);
+
+/*
+ * Entrywise sign as int8 ([SignMuon] §2 step 2, for the all-reduce variant of step 3 and the
+ * "8 bits with int8" payload of "Eficiência de Comunicação").
+ *   U     f32 or bf16 matrix (read).
+ *   s     device array of R*C int8 (written), row-major packed: s[i*C + j] = -1 if
+ *         U(i, j) < 0, else +1 (+0, -0 and NaN give +1).
+ */
+mao_status sign_int8(const mao_mat* U, int8_t* s, void* stream);
+
+/*
+ * Integer SUM of W_n workers' int8 sign buffers followed by the local threshold
+ * ([SignMuon] §2 step 3, all-reduce variant, and step 4: S_bar = sign(sum_m S^(m))).
+ * On one GPU the workers' buffers sit side by side and the SUM all-reduce is the reduction
+ * over them; its result is the int8 buffer an int8 SUM all-reduce would leave on every
+ * worker.
+ *   s              device, worker m's n entries start at s + m*worker_stride (bytes,
+ *                  worker_stride >= n). Entries are expected in {-1, +1}; any int8 values
+ *                  are summed as integers.
+ *   n_workers      1..127 (the int8 sum of +-1 signs is then exact).
+ *   n              entries per worker (>= 1).
+ *   sum            NULL or device array of n int8: sum_m S^(m) (wraps modulo 256 only if
+ *                  the entries are not +-1).
+ *   s_bar          NULL or device array of n int8: +1 where sum >= 0 (a tie gives +1), else -1.
+ *   vote           NULL or device array of ceil(n/32) words: S_bar packed (header layout).
+ *   At least one of sum, s_bar, vote must be non-NULL. Outputs must not overlap s.
+ */
+mao_status majority_vote_int8(const int8_t* s, int32_t n_workers, int64_t worker_stride,
+                              int64_t n, int8_t* sum, int8_t* s_bar, uint32_t* vote,
+                              void* stream);
 
 /*
  * Parameter update ([SignMuon] §2 step 4: W_{t+1} = W_t - eta_t * S_bar_t).

@@ -10,6 +10,8 @@ Functions (same names as the C ABI):
   ns_orthogonalize(inp, out, steps, coeffs, ...)     Newton–Schulz polar factor (+ packed signs)
   sign_pack_bits(U, bits)                            sign + 1-bit pack
   majority_vote_packed(bits, nbits, vote)            vote over workers' packed signs
+  sign_int8(U, s)                                    sign as int8 +-1 (all-reduce variant)
+  majority_vote_int8(s, n, sum, s_bar, vote)         int8 SUM over workers + threshold
   apply_update(W, lr, vote=..., U=...)               W <- W - lr*D
   sync_status()                                      stream sync + device error word
 """
@@ -24,7 +26,7 @@ from ._abi import MaoError  # noqa: F401
 # Default Newton–Schulz coefficients (a, b, c): the quintic used by Muon.
 QUINTIC = (3.4445, -4.7750, 2.0315)
 
-_DT = {torch.float32: _abi.MAO_F32, torch.bfloat16: _abi.MAO_BF16}
+_DT = {torch.float32: _abi.MAO_F32, torch.bfloat16: _abi.MAO_BF16, torch.int8: _abi.MAO_I8}
 _COMPUTE = {"f32": _abi.MAO_F32, "bf16": _abi.MAO_BF16,
             torch.float32: _abi.MAO_F32, torch.bfloat16: _abi.MAO_BF16}
 
@@ -39,7 +41,23 @@ def _as_list(x):
     return list(x) if isinstance(x, (list, tuple)) else [x]
 
 
+class PackedSigns:
+    """A rows x cols sign matrix held as packed words (int32 tensor of ceil(rows*cols/32)
+    words, header layout), usable as an ns_orthogonalize input."""
+
+    def __init__(self, words, rows, cols):
+        if not words.is_cuda or words.dtype != torch.int32 or not words.is_contiguous():
+            raise ValueError("words must be a contiguous int32 CUDA tensor")
+        if words.numel() < packed_words(rows, cols):
+            raise ValueError("too few words for a %d x %d sign matrix" % (rows, cols))
+        self.words, self.shape = words, (int(rows), int(cols))
+        self.device = words.device
+
+
 def _mat(t, allow_none=False, like=None):
+    if isinstance(t, PackedSigns):
+        R, C = t.shape
+        return _abi.MaoMat(t.words.data_ptr(), R, C, C, _abi.MAO_SIGN1, 0)
     if t is None:
         if not allow_none:
             raise ValueError("tensor required")
@@ -49,7 +67,7 @@ def _mat(t, allow_none=False, like=None):
     if t.dim() != 2 or t.stride(1) != 1:
         raise ValueError("expected a 2-D tensor with unit column stride")
     if t.dtype not in _DT:
-        raise ValueError("dtype must be float32 or bfloat16")
+        raise ValueError("dtype must be float32, bfloat16 or int8")
     return _abi.MaoMat(t.data_ptr(), t.shape[0], t.shape[1], max(t.stride(0), t.shape[1]),
                        _DT[t.dtype], 0)
 
@@ -144,6 +162,40 @@ def majority_vote_packed(bits, nbits, vote=None, stream=None):
                                     int(nbits), ctypes.c_void_p(vote.data_ptr()), _stream(stream))
     _abi.check("majority_vote_packed", st)
     return vote
+
+
+def sign_int8(U, s=None, stream=None):
+    """int8 signs of U (-1 where U < 0, else +1), row-major R x C."""
+    if s is None:
+        s = torch.empty(U.shape, dtype=torch.int8, device=U.device)
+    st = lib().sign_int8(ctypes.byref(_mat(U)), ctypes.c_void_p(s.data_ptr()), _stream(stream))
+    _abi.check("sign_int8", st)
+    return s
+
+
+def majority_vote_int8(s, n, sum=None, s_bar=None, vote=None, stream=None):
+    """Integer SUM of workers' int8 signs, then the threshold vote.
+
+    s: int8 tensor [W_n][stride] (stride >= n, unit inner stride). Each of sum / s_bar
+    (int8, n entries) and vote (int32, ceil(n/32) words) is a tensor to fill, True to
+    allocate, or None to skip. Returns (sum, s_bar, vote).
+    """
+    if s.dim() != 2 or s.stride(1) != 1 or s.dtype != torch.int8:
+        raise ValueError("s must be an int8 [n_workers][stride] tensor with unit stride")
+
+    def alloc(x, count, dt):
+        if x is True:
+            return torch.empty(count, dtype=dt, device=s.device)
+        return x if x is not None and x is not False else None
+
+    sum = alloc(sum, n, torch.int8)
+    s_bar = alloc(s_bar, n, torch.int8)
+    vote = alloc(vote, packed_words(1, n), torch.int32)
+    ptr = lambda x: ctypes.c_void_p(x.data_ptr() if x is not None else None)  # noqa: E731
+    st = lib().majority_vote_int8(ptr(s), s.shape[0], s.stride(0), int(n), ptr(sum), ptr(s_bar),
+                                  ptr(vote), _stream(stream))
+    _abi.check("majority_vote_int8", st)
+    return sum, s_bar, vote
 
 
 def apply_update(W, lr, vote=None, U=None, stream=None):

@@ -15,6 +15,8 @@ MAO_ERR_TIMEOUT = 6
 
 MAO_F32 = 0
 MAO_BF16 = 1
+MAO_I8 = 2      # ns_orthogonalize input only
+MAO_SIGN1 = 3   # ns_orthogonalize input only (packed signs, ld == cols)
 
 # scratch size of ns_orthogonalize_noalloc (MAO_NOALLOC_WORKSPACE_BYTES in mao.h)
 NOALLOC_WORKSPACE_BYTES = 16 * 1024 * 1024
@@ -29,6 +31,8 @@ EXPORTS = (
     "ns_orthogonalize_noalloc",
     "sign_pack_bits",
     "majority_vote_packed",
+    "sign_int8",
+    "majority_vote_int8",
     "apply_update",
     "mao_sync_status",
     "mao_launch_count",
@@ -95,6 +99,11 @@ def load():
     lib.sign_pack_bits.argtypes = [P(MaoMat), vp, vp]
     lib.majority_vote_packed.restype = ctypes.c_int
     lib.majority_vote_packed.argtypes = [vp, ctypes.c_int32, ctypes.c_int64, ctypes.c_int64, vp, vp]
+    lib.sign_int8.restype = ctypes.c_int
+    lib.sign_int8.argtypes = [P(MaoMat), vp, vp]
+    lib.majority_vote_int8.restype = ctypes.c_int
+    lib.majority_vote_int8.argtypes = [vp, ctypes.c_int32, ctypes.c_int64, ctypes.c_int64, vp, vp,
+                                       vp, vp]
     lib.apply_update.restype = ctypes.c_int
     lib.apply_update.argtypes = [P(MaoMat), P(ctypes.c_void_p), P(MaoMat), ctypes.c_int32,
                                  ctypes.c_float, vp]

@@ -124,7 +124,7 @@ mao_status ns_orthogonalize(const mao_mat* in, const mao_mat* out, int32_t batch
   for (int i = 0; i < (coeff_stride ? 3 * steps : 3); ++i)
     if (!std::isfinite(coeffs[i])) return MAO_ERR_INVALID_ARG;
   for (int b = 0; b < batch; ++b) {
-    mao_status st = check_mat(in[b]);
+    mao_status st = check_ns_input(in[b]);
     if (st != MAO_OK) return st;
     const bool bits = sign_bits && sign_bits[b];
     st = check_mat(out[b], bits);
@@ -157,6 +157,23 @@ mao_status majority_vote_packed(const uint32_t* bits, int32_t n_workers,
     return MAO_ERR_MISALIGNED;
   return vote_launch(bits, n_workers, worker_stride_words, nbits, vote,
                      static_cast<cudaStream_t>(stream));
+}
+
+mao_status sign_int8(const mao_mat* U, int8_t* s, void* stream) {
+  if (!U || !s) return MAO_ERR_INVALID_ARG;
+  const mao_status st = check_mat(*U);
+  if (st != MAO_OK) return st;
+  return sign_int8_launch(*U, s, static_cast<cudaStream_t>(stream));
+}
+
+mao_status majority_vote_int8(const int8_t* s, int32_t n_workers, int64_t worker_stride,
+                              int64_t n, int8_t* sum, int8_t* s_bar, uint32_t* vote,
+                              void* stream) {
+  if (!s || n_workers < 1 || n_workers > 127 || n < 1 || worker_stride < n) return MAO_ERR_INVALID_ARG;
+  if (!sum && !s_bar && !vote) return MAO_ERR_INVALID_ARG;
+  if (vote && reinterpret_cast<uintptr_t>(vote) % 4 != 0) return MAO_ERR_MISALIGNED;
+  return vote_int8_launch(s, n_workers, worker_stride, n, sum, s_bar, vote,
+                          static_cast<cudaStream_t>(stream));
 }
 
 mao_status apply_update(const mao_mat* W, const uint32_t* const* vote, const mao_mat* U,

@@ -11,7 +11,8 @@ namespace mao {
 
 // ---------------------------------------------------------------- host helpers
 
-inline int elem_size(int32_t dt) { return dt == MAO_BF16 ? 2 : 4; }
+// Bytes per element (MAO_SIGN1 is addressed by 4-byte words).
+inline int elem_size(int32_t dt) { return dt == MAO_BF16 ? 2 : dt == MAO_I8 ? 1 : 4; }
 inline bool valid_dtype(int32_t dt) { return dt == MAO_F32 || dt == MAO_BF16; }
 
 // Checks a descriptor: non-null data, positive sizes, ld >= cols, element alignment.
@@ -20,6 +21,18 @@ inline mao_status check_mat(const mao_mat& m, bool allow_null_data = false) {
   if (m.rows < 1 || m.cols < 1 || m.ld < m.cols) return MAO_ERR_INVALID_ARG;
   if (m.rows > (int64_t(1) << 31) || m.cols > (int64_t(1) << 31)) return MAO_ERR_UNSUPPORTED;
   if (m.data == nullptr) return allow_null_data ? MAO_OK : MAO_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(m.data) % elem_size(m.dtype) != 0) return MAO_ERR_MISALIGNED;
+  return MAO_OK;
+}
+
+// Checks an ns_orthogonalize input: f32/bf16 as check_mat, or an int8 / packed sign matrix
+// (the optional polar step on an aggregated sign matrix).
+inline mao_status check_ns_input(const mao_mat& m) {
+  if (m.dtype != MAO_I8 && m.dtype != MAO_SIGN1) return check_mat(m);
+  if (m.reserved != 0 || m.rows < 1 || m.cols < 1 || m.ld < m.cols) return MAO_ERR_INVALID_ARG;
+  if (m.rows > (int64_t(1) << 31) || m.cols > (int64_t(1) << 31)) return MAO_ERR_UNSUPPORTED;
+  if (m.dtype == MAO_SIGN1 && m.ld != m.cols) return MAO_ERR_INVALID_ARG;
+  if (m.data == nullptr) return MAO_ERR_INVALID_ARG;
   if (reinterpret_cast<uintptr_t>(m.data) % elem_size(m.dtype) != 0) return MAO_ERR_MISALIGNED;
   return MAO_OK;
 }

@@ -193,6 +193,110 @@ __global__ void __launch_bounds__(256) sign_pack_kernel(const void* u, int64_t r
   bits[w] = word;
 }
 
+// ------------------------------------------------------------------ sign as int8
+
+// One thread per 16 entries k = 16t .. 16t+15 of the row-major matrix: -1 (0xFF) where
+// u < 0, else +1. VEC: cols % 16 == 0 and 16-byte aligned rows, one 16-byte store.
+template <bool VEC>
+__global__ void __launch_bounds__(256) sign_int8_kernel(const void* u, int64_t rows, int64_t cols,
+                                                        int64_t ld, int32_t dt, int8_t* s,
+                                                        int64_t nchunks) {
+  const int64_t t = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (t >= nchunks) return;
+  const int64_t k0 = t * 16;
+  if (VEC) {
+    const int64_t row = k0 / cols, col0 = k0 - row * cols;
+    float v[16];
+    load8(u, row * ld + col0, dt, *reinterpret_cast<float(*)[8]>(&v[0]));
+    load8(u, row * ld + col0 + 8, dt, *reinterpret_cast<float(*)[8]>(&v[8]));
+    uint32_t w[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      w[q] = 0;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) w[q] |= (v[4 * q + i] < 0.0f ? 0xFFu : 0x01u) << (8 * i);
+    }
+    *reinterpret_cast<uint4*>(s + k0) = make_uint4(w[0], w[1], w[2], w[3]);
+  } else {
+    const int64_t n = rows * cols;
+    for (int i = 0; i < 16; ++i) {
+      const int64_t k = k0 + i;
+      if (k >= n) break;
+      const int64_t row = k / cols, col = k - row * cols;
+      s[k] = load_elem(u, row * ld + col, dt) < 0.0f ? int8_t(-1) : int8_t(1);
+    }
+  }
+}
+
+// ------------------------------------------------------- int8 SUM + threshold vote
+
+// One thread per 32 entries k = 32t .. 32t+31 (one vote word). The W_n int8 signs of each
+// entry are summed with per-byte SIMD adds (exact: |sum| <= 127); the sum's sign bit then
+// gives S_bar and the vote bit. VEC: 16-byte aligned buffers, all 32 entries in range.
+template <bool VEC>
+__global__ void __launch_bounds__(256) vote_int8_kernel(const int8_t* __restrict__ s, int32_t nw,
+                                                        int64_t stride, int64_t n,
+                                                        int8_t* __restrict__ sum,
+                                                        int8_t* __restrict__ sbar,
+                                                        uint32_t* __restrict__ vote) {
+  const int64_t t = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t k0 = t * 32;
+  if (k0 >= n) return;
+  const int valid = n - k0 < 32 ? int(n - k0) : 32;
+  uint32_t acc[8];
+#pragma unroll
+  for (int q = 0; q < 8; ++q) acc[q] = 0;
+  for (int m = 0; m < nw; ++m) {
+    const int8_t* src = s + int64_t(m) * stride + k0;
+    uint32_t x[8];
+    if (VEC) {
+      const uint4 a = __ldg(reinterpret_cast<const uint4*>(src));
+      const uint4 b = __ldg(reinterpret_cast<const uint4*>(src) + 1);
+      x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+      x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+    } else {
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        x[q] = 0;
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (4 * q + j < valid) x[q] |= uint32_t(uint8_t(src[4 * q + j])) << (8 * j);
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < 8; ++q) acc[q] = __vadd4(acc[q], x[q]);
+  }
+  uint32_t sb[8], word = 0;
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const uint32_t neg = (acc[q] >> 7) & 0x01010101u;  // 1 in each byte whose sum is < 0
+    sb[q] = 0x01010101u | (neg * 0xFEu);                // 0x01 (+1) or 0xFF (-1) per byte
+    // gather the low bit of each byte of pos into 4 adjacent bits (distinct product terms,
+    // no carries): byte i lands on bit 28 + i
+    const uint32_t pos = neg ^ 0x01010101u;
+    word |= ((pos * 0x10204080u) >> 28) << (4 * q);
+  }
+  if (valid < 32) word &= (1u << valid) - 1u;
+  if (vote) vote[t] = word;
+  if (VEC) {
+    if (sum) {
+      uint4* d = reinterpret_cast<uint4*>(sum + k0);
+      d[0] = make_uint4(acc[0], acc[1], acc[2], acc[3]);
+      d[1] = make_uint4(acc[4], acc[5], acc[6], acc[7]);
+    }
+    if (sbar) {
+      uint4* d = reinterpret_cast<uint4*>(sbar + k0);
+      d[0] = make_uint4(sb[0], sb[1], sb[2], sb[3]);
+      d[1] = make_uint4(sb[4], sb[5], sb[6], sb[7]);
+    }
+  } else {
+    for (int j = 0; j < valid; ++j) {
+      if (sum) sum[k0 + j] = int8_t(uint8_t(acc[j >> 2] >> (8 * (j & 3))));
+      if (sbar) sbar[k0 + j] = int8_t(uint8_t(sb[j >> 2] >> (8 * (j & 3))));
+    }
+  }
+}
+
 // --------------------------------------------------------------- majority vote
 
 constexpr int kMaxPlanes = 16;  // counts up to 65535 workers
@@ -298,6 +402,46 @@ mao_status sign_pack_launch(const mao_mat& U, uint32_t* bits, cudaStream_t strea
   sign_pack_kernel<<<unsigned(blocks), 256, 0, stream>>>(U.data, U.rows, U.cols, U.ld, U.dtype,
                                                          vec ? 1 : 0, bits, nwords);
   count_launch();
+  return cuda_status(cudaGetLastError());
+}
+
+mao_status sign_int8_launch(const mao_mat& U, int8_t* s, cudaStream_t stream) {
+  const int64_t n = U.rows * U.cols;
+  const int64_t nchunks = ceil_div(n, 16);
+  const bool vec = (U.cols % 16 == 0) && vec8_ok(U) && (reinterpret_cast<uintptr_t>(s) % 16 == 0);
+  const int64_t blocks = ceil_div(nchunks, 256);
+  if (blocks > 0x7FFFFFFF) return MAO_ERR_UNSUPPORTED;
+  if (vec)
+    sign_int8_kernel<true><<<unsigned(blocks), 256, 0, stream>>>(U.data, U.rows, U.cols, U.ld,
+                                                                 U.dtype, s, nchunks);
+  else
+    sign_int8_kernel<false><<<unsigned(blocks), 256, 0, stream>>>(U.data, U.rows, U.cols, U.ld,
+                                                                  U.dtype, s, nchunks);
+  count_launch();
+  return cuda_status(cudaGetLastError());
+}
+
+mao_status vote_int8_launch(const int8_t* s, int32_t n_workers, int64_t stride, int64_t n,
+                            int8_t* sum, int8_t* sbar, uint32_t* vote, cudaStream_t stream) {
+  auto a16 = [](const void* p) { return reinterpret_cast<uintptr_t>(p) % 16 == 0; };
+  // 16-byte path over the first floor(n/32)*32 entries, byte path for the rest
+  const bool vec = a16(s) && stride % 16 == 0 && (!sum || a16(sum)) && (!sbar || a16(sbar));
+  const int64_t bulk = vec ? (n / 32) * 32 : 0;
+  if (bulk > 0) {
+    const int64_t blocks = ceil_div(bulk / 32, 256);
+    if (blocks > 0x7FFFFFFF) return MAO_ERR_UNSUPPORTED;
+    vote_int8_kernel<true><<<unsigned(blocks), 256, 0, stream>>>(s, n_workers, stride, bulk, sum,
+                                                                 sbar, vote);
+    count_launch();
+  }
+  if (n > bulk) {
+    const int64_t blocks = ceil_div(ceil_div(n - bulk, 32), 256);
+    if (blocks > 0x7FFFFFFF) return MAO_ERR_UNSUPPORTED;
+    vote_int8_kernel<false><<<unsigned(blocks), 256, 0, stream>>>(
+        s + bulk, n_workers, stride, n - bulk, sum ? sum + bulk : nullptr,
+        sbar ? sbar + bulk : nullptr, vote ? vote + bulk / 32 : nullptr);
+    count_launch();
+  }
   return cuda_status(cudaGetLastError());
 }
 

@@ -14,6 +14,9 @@ mao_status momentum_launch(const mao_mat* M, const mao_mat* G, int32_t batch, fl
 mao_status update_launch(const mao_mat* W, const uint32_t* const* vote, const mao_mat* U,
                          int32_t batch, float lr, cudaStream_t stream);
 mao_status sign_pack_launch(const mao_mat& U, uint32_t* bits, cudaStream_t stream);
+mao_status sign_int8_launch(const mao_mat& U, int8_t* s, cudaStream_t stream);
+mao_status vote_int8_launch(const int8_t* s, int32_t n_workers, int64_t stride, int64_t n,
+                            int8_t* sum, int8_t* sbar, uint32_t* vote, cudaStream_t stream);
 mao_status vote_launch(const uint32_t* bits, int32_t n_workers, int64_t stride, int64_t nbits,
                        uint32_t* vote, cudaStream_t stream);
 

@@ -58,7 +58,7 @@ extern "C" mao_status ns_orthogonalize_noalloc(const mao_mat* in, const mao_mat*
   for (int i = 0; i < (coeff_stride ? 3 * steps : 3); ++i)
     if (!std::isfinite(coeffs[i])) return MAO_ERR_INVALID_ARG;
   for (int b = 0; b < batch; ++b) {
-    mao_status st = check_mat(in[b]);
+    mao_status st = check_ns_input(in[b]);
     if (st != MAO_OK) return st;
     const bool bits = sign_bits && sign_bits[b];
     st = check_mat(out[b], bits);

@@ -135,6 +135,46 @@ struct StageParams {
   float* partials;
 };
 
+// Loads the `valid` (<= 8) source elements (row, col0 .. col0+valid-1) of a staged input as
+// fp32, zeros beyond. f32/bf16 take 16-byte loads when `vec`; int8 takes one 8-byte load when
+// `vec`; packed signs read the (at most two) words holding the 8 bits.
+__device__ __forceinline__ void stage_load8(const StageEntry& e, int64_t row, int64_t col0,
+                                            int valid, float (&v)[8]) {
+  if (e.src_dt == MAO_SIGN1) {
+    const uint32_t* w = reinterpret_cast<const uint32_t*>(e.src);
+    const int64_t k = row * e.cols + col0;
+    const int64_t wi = k >> 5;
+    const int sh = int(k & 31);
+    uint64_t x = w[wi];
+    if (sh + valid > 32) x |= uint64_t(w[wi + 1]) << 32;
+    x >>= sh;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = i < valid ? (((x >> i) & 1u) ? 1.0f : -1.0f) : 0.0f;
+    return;
+  }
+  if (e.src_dt == MAO_I8) {
+    const int8_t* p = reinterpret_cast<const int8_t*>(e.src) + row * e.src_ld + col0;
+    if (e.vec_src && valid == 8) {
+      const uint2 raw = *reinterpret_cast<const uint2*>(p);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        v[i] = float(int8_t(raw.x >> (8 * i)));
+        v[4 + i] = float(int8_t(raw.y >> (8 * i)));
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] = i < valid ? float(p[i]) : 0.0f;
+    }
+    return;
+  }
+  if (e.vec_src && valid == 8) {
+    load8(e.src, row * e.src_ld + col0, e.src_dt, v);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = i < valid ? load_elem(e.src, row * e.src_ld + col0 + i, e.src_dt) : 0.0f;
+  }
+}
+
 // Copies each input into its workspace slot (converting to the compute type) and writes
 // one fp32 partial sum of squares per block; records the slot's output entry.
 __global__ void __launch_bounds__(kStageThreads) stage_in_kernel(const __grid_constant__ StageParams p) {
@@ -162,12 +202,7 @@ __global__ void __launch_bounds__(kStageThreads) stage_in_kernel(const __grid_co
     const int64_t left = e.cols - col0;
     const int valid = int(left >= 8 ? 8 : (left > 0 ? left : 0));
     float v[8];
-    if (e.vec_src && valid == 8) {
-      load8(e.src, row * e.src_ld + col0, e.src_dt, v);
-    } else {
-#pragma unroll
-      for (int i = 0; i < 8; ++i) v[i] = i < valid ? load_elem(e.src, row * e.src_ld + col0 + i, e.src_dt) : 0.0f;
-    }
+    stage_load8(e, row, col0, valid, v);
 #pragma unroll
     for (int i = 0; i < 8; ++i) sq = __fmaf_rn(v[i], v[i], sq);
     store8(e.dst, row * e.dst_ld + col0, p.ws_dt, v);
@@ -557,7 +592,13 @@ mao_status ns_run(const mao_mat* in, const mao_mat* out, int32_t batch, int32_t 
         e.src = in[b].data;
         e.src_ld = in[b].ld;
         e.src_dt = in[b].dtype;
-        e.vec_src = vec8_ok(in[b]) ? 1 : 0;
+        if (in[b].dtype == MAO_I8)
+          e.vec_src = (reinterpret_cast<uintptr_t>(in[b].data) % 8 == 0 && in[b].cols % 8 == 0 &&
+                       in[b].ld % 8 == 0) ? 1 : 0;
+        else if (in[b].dtype == MAO_SIGN1)
+          e.vec_src = 0;
+        else
+          e.vec_src = vec8_ok(in[b]) ? 1 : 0;
         e.dst = ws + gp->off_x[0] + size_t(s - gp->slot0) * size_t(gp->R * gp->ldx) * plan.es;
         e.dst_ld = gp->ldx;
         e.rows = in[b].rows;

@@ -87,3 +87,47 @@ def test_invalid_arguments_rejected_before_any_launch(lib):
     assert lib.apply_update(m, None, None, 1, 0.01, None) == 1
     votes = (ctypes.c_void_p * 1)(fake)
     assert lib.apply_update(m, votes, m, 1, 0.01, None) == 1
+
+
+def test_int8_variant_arguments_rejected_before_any_launch(lib):
+    fake = 0x10000
+    p = ctypes.c_void_p(fake)
+    m = _mats((4, 4), data=fake)
+    assert lib.sign_int8(m, None, None) == _abi.MAO_ERR_INVALID_ARG
+    assert lib.sign_int8(None, p, None) == _abi.MAO_ERR_INVALID_ARG
+    i8 = _mats((4, 4), dtype=_abi.MAO_I8, data=fake)
+    assert lib.sign_int8(i8, p, None) == _abi.MAO_ERR_INVALID_ARG  # input must be f32/bf16
+    # workers 1..127, stride >= n, at least one output, word-aligned vote
+    assert lib.majority_vote_int8(p, 0, 64, 64, p, None, None, None) == _abi.MAO_ERR_INVALID_ARG
+    assert lib.majority_vote_int8(p, 128, 64, 64, p, None, None, None) == _abi.MAO_ERR_INVALID_ARG
+    assert lib.majority_vote_int8(p, 3, 63, 64, p, None, None, None) == _abi.MAO_ERR_INVALID_ARG
+    assert lib.majority_vote_int8(p, 3, 64, 0, p, None, None, None) == _abi.MAO_ERR_INVALID_ARG
+    assert lib.majority_vote_int8(None, 3, 64, 64, p, None, None, None) == _abi.MAO_ERR_INVALID_ARG
+    assert lib.majority_vote_int8(p, 3, 64, 64, None, None, None, None) == _abi.MAO_ERR_INVALID_ARG
+    assert lib.majority_vote_int8(p, 3, 64, 64, None, None, ctypes.c_void_p(fake + 2),
+                                  None) == _abi.MAO_ERR_MISALIGNED
+
+
+def test_sign_matrix_inputs_only_where_declared(lib):
+    fake = 0x10000
+    co = (ctypes.c_float * 3)(3.4445, -4.775, 2.0315)
+    ws = ctypes.c_void_p(fake)
+    out = _mats((4, 40), dtype=_abi.MAO_F32, data=fake)
+    # packed signs need ld == cols
+    bad = (_abi.MaoMat * 1)(_abi.MaoMat(fake, 4, 40, 48, _abi.MAO_SIGN1, 0))
+    assert lib.ns_orthogonalize(bad, out, 1, 5, co, 0, 1e-7, 1, None, ws, 1 << 30, None) == 1
+    assert lib.ns_orthogonalize_noalloc(bad, out, 1, 5, co, 0, 1e-7, 1, None, None) == 1
+    # packed words are 4-byte aligned
+    odd = (_abi.MaoMat * 1)(_abi.MaoMat(fake + 2, 4, 40, 40, _abi.MAO_SIGN1, 0))
+    assert lib.ns_orthogonalize(odd, out, 1, 5, co, 0, 1e-7, 1, None, ws, 1 << 30,
+                                None) == _abi.MAO_ERR_MISALIGNED
+    # int8 and packed signs are inputs only: not outputs, not momentum or update operands
+    i8 = _mats((4, 40), dtype=_abi.MAO_I8, data=fake)
+    s1 = _mats((4, 40), dtype=_abi.MAO_SIGN1, data=fake)
+    f32 = _mats((4, 40), dtype=_abi.MAO_F32, data=fake)
+    assert lib.ns_orthogonalize(f32, i8, 1, 5, co, 0, 1e-7, 1, None, ws, 1 << 30, None) == 1
+    assert lib.muon_momentum_update(i8, f32, 1, 0.9, None) == 1
+    assert lib.muon_momentum_update(f32, s1, 1, 0.9, None) == 1
+    assert lib.apply_update(f32, None, i8, 1, 0.01, None) == 1
+    # workspace sizes do not depend on the input encoding
+    assert lib.ns_workspace_bytes(i8, 1, 1) == lib.ns_workspace_bytes(f32, 1, 1) > 0
