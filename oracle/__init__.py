@@ -31,6 +31,9 @@ against something other than itself):
   muon.momentum            follows from fma_f32 / bf16_rne pins + a hand table
   muon.newton_schulz       SVD closed form (odd polynomial acts on singular values),
                            cubic convergence to scipy's polar factor, invariants
+  muon.blockwise_newton_schulz  1 x 1 grid = newton_schulz; block independence; on a
+                           block-diagonal input the cubic iteration reaches scipy's polar
+                           factor of the whole matrix
   muon.sign_of/pack_signs  hand-computed words (tests/golden/pack_signs.txt)
   muon.majority_vote       exhaustive brute force over all sign patterns (W_n <= 8)
   muon.int8_sum_vote       brute-force integer sums; equals the packed-bit vote on all patterns
@@ -48,6 +51,7 @@ from .muon import (
     momentum,
     frobenius_normalise,
     newton_schulz,
+    blockwise_newton_schulz,
     sign_of,
     pack_signs,
     pack_signs_loop,
@@ -64,7 +68,7 @@ from .muon import (
 
 __all__ = [
     "bf16_rne", "fma_f32", "to_f32", "QUINTIC", "CUBIC", "momentum",
-    "frobenius_normalise", "newton_schulz", "sign_of", "pack_signs",
+    "frobenius_normalise", "newton_schulz", "blockwise_newton_schulz", "sign_of", "pack_signs",
     "pack_signs_loop", "unpack_signs", "majority_vote", "int8_sum_vote", "post_vote_polar",
     "apply_update",
     "apply_update_f64", "sign_muon_step", "muon_step", "ns_dense_flops",

@@ -91,6 +91,21 @@ def newton_schulz(M, steps=5, coeffs=QUINTIC, eps=1e-7):
     return X.T if tall else X
 
 
+def blockwise_newton_schulz(M, block_rows, block_cols, steps=5, coeffs=QUINTIC, eps=1e-7):
+    """Blockwise orthogonalisation ([Megatron] §"分散モード", blockwise paragraph): each
+    block of a block_rows x block_cols grid (the last block row / column ragged) is what one
+    rank owns, and is orthogonalised on its own (its own Frobenius norm, its own
+    Newton–Schulz). This is not the orthogonalisation of the whole matrix."""
+    M = np.asarray(M, dtype=np.float64)
+    R, C = M.shape
+    out = np.empty_like(M)
+    for i0 in range(0, R, block_rows):
+        for j0 in range(0, C, block_cols):
+            blk = M[i0:i0 + block_rows, j0:j0 + block_cols]
+            out[i0:i0 + block_rows, j0:j0 + block_cols] = newton_schulz(blk, steps, coeffs, eps)
+    return out
+
+
 def sign_of(U):
     """Entrywise sign in {-1, +1} ([SignMuon] §2 step 2); u < 0 -> -1, else +1."""
     U = np.asarray(U)

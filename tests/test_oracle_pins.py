@@ -366,3 +366,43 @@ def test_sign_muon_step_post_polar_reaches_polar_of_vote():
     assert np.allclose(out["W"], W.astype(np.float64) - 0.5 * Q.T, atol=1e-9)
     # rows of the polar factor of a full-row-rank matrix are orthonormal
     assert np.allclose(out["U_bar"] @ out["U_bar"].T, np.eye(R), atol=1e-9)
+
+
+# ----------------------------------------------------------------- blockwise NS
+
+def test_blockwise_single_block_is_full_ns():
+    rng = np.random.default_rng(50)
+    M = rng.standard_normal((24, 40))
+    assert np.array_equal(oracle.blockwise_newton_schulz(M, 24, 40, 5, QUINTIC),
+                          oracle.newton_schulz(M, 5, QUINTIC))
+    assert np.array_equal(oracle.blockwise_newton_schulz(M, 100, 100, 5, QUINTIC),
+                          oracle.newton_schulz(M, 5, QUINTIC))
+
+
+def test_blockwise_blocks_are_independent():
+    rng = np.random.default_rng(51)
+    M = rng.standard_normal((30, 50))
+    base = oracle.blockwise_newton_schulz(M, 16, 24, 5, QUINTIC)
+    M2 = M.copy()
+    M2[16:, 24:48] *= -3.0  # change one block (rows 16..29, columns 24..47)
+    other = oracle.blockwise_newton_schulz(M2, 16, 24, 5, QUINTIC)
+    changed = np.zeros(M.shape, bool)
+    changed[16:, 24:48] = True
+    assert np.array_equal(base[~changed], other[~changed])
+    # scaling a block by -3: the odd polynomial of the normalised block flips its sign only
+    assert np.allclose(other[changed], -base[changed], atol=1e-12)
+
+
+def test_blockwise_cubic_on_block_diagonal_reaches_full_polar():
+    scipy_linalg = pytest.importorskip("scipy.linalg")
+    rng = np.random.default_rng(52)
+    A, B = rng.standard_normal((8, 12)), rng.standard_normal((6, 9))
+    M = np.zeros((14, 21))
+    M[:8, :12], M[8:, 12:] = A, B
+    got = oracle.blockwise_newton_schulz(M, 8, 12, 60, (1.5, -0.5, 0.0))
+    Q, _ = scipy_linalg.polar(M.T)
+    assert np.allclose(got, Q.T, atol=1e-9)
+    # the whole-matrix quintic result is not blockwise: on a generic input they differ
+    G = rng.standard_normal((14, 21))
+    assert np.linalg.norm(oracle.blockwise_newton_schulz(G, 8, 12, 5, QUINTIC)
+                          - oracle.newton_schulz(G, 5, QUINTIC)) > 0.1
