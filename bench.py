@@ -45,6 +45,9 @@ def parse_args():
                     help="Sign-Muon aggregation: 1-bit all-gather (bits) or int8 SUM all-reduce")
     ap.add_argument("--post-polar", action="store_true",
                     help="Sign-Muon: Newton-Schulz on the aggregated signs before the update")
+    ap.add_argument("--sweep-hbm", action="store_true",
+                    help="time each HBM-bound kernel alone on L2-cold buffers of 256 MB-4 GB "
+                         "and print one JSON line per kernel and size")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
@@ -377,6 +380,86 @@ def config_block(wl, step_bytes, variant="bits", post_polar=False):
     return c
 
 
+# ------------------------------------------------------------------ HBM sweep
+
+def sweep_hbm(dev, reps=20):
+    """GB/s of each HBM-bound kernel alone, on buffers far larger than L2 or rotated across
+    >= 4 x L2 of distinct memory, so that every timed call reads cold lines."""
+    import torch
+    import matrix_aware_optimizers_gb300 as mao
+    stream = torch.cuda.current_stream()
+    peaks, src = load_peaks()
+    hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+    Wn = 8
+    kernels = {
+        # name: (bytes per element, setup(n) -> callable)
+        "momentum bf16 M, bf16 G": 6,
+        "momentum fp32 M, bf16 G": 10,
+        "update Muon bf16 W, bf16 U": 6,
+        "update Sign-Muon bf16 W, packed vote": 4 + 1 / 8,
+        "sign_pack_bits bf16 U": 2 + 1 / 8,
+        "sign_int8 bf16 U": 3,
+        "majority_vote_packed 8 workers": (Wn + 1) / 8,
+        "majority_vote_int8 8 workers": Wn + 1 / 8,
+    }
+
+    def make(name, n):
+        C = 4096
+        R = max(1, n // C)
+        bf, f32 = torch.bfloat16, torch.float32
+        if name.startswith("momentum"):
+            M = torch.zeros((R, C), dtype=f32 if "fp32" in name else bf, device=dev)
+            G = torch.ones((R, C), dtype=bf, device=dev)
+            return lambda: mao.muon_momentum_update(M, G, 0.95)
+        if name.startswith("update Muon"):
+            W = torch.zeros((R, C), dtype=bf, device=dev)
+            U = torch.ones((R, C), dtype=bf, device=dev)
+            return lambda: mao.apply_update(W, 0.02, U=U)
+        if name.startswith("update Sign"):
+            W = torch.zeros((R, C), dtype=bf, device=dev)
+            v = torch.zeros(mao.packed_words(R, C), dtype=torch.int32, device=dev)
+            return lambda: mao.apply_update(W, 0.02, vote=v)
+        if name.startswith("sign_pack"):
+            U = torch.ones((R, C), dtype=bf, device=dev)
+            b = torch.empty(mao.packed_words(R, C), dtype=torch.int32, device=dev)
+            return lambda: mao.sign_pack_bits(U, b)
+        if name.startswith("sign_int8"):
+            U = torch.ones((R, C), dtype=bf, device=dev)
+            s8 = torch.empty((R, C), dtype=torch.int8, device=dev)
+            return lambda: mao.sign_int8(U, s8)
+        if name.startswith("majority_vote_packed"):
+            nw = mao.packed_words(R, C)
+            words = torch.zeros((Wn, nw), dtype=torch.int32, device=dev)
+            vote = torch.empty(nw, dtype=torch.int32, device=dev)
+            return lambda: mao.majority_vote_packed(words, R * C, vote)
+        s8 = torch.ones((Wn, R * C), dtype=torch.int8, device=dev)
+        vote = torch.empty(mao.packed_words(R, C), dtype=torch.int32, device=dev)
+        return lambda: mao.majority_vote_int8(s8, R * C, vote=vote)
+
+    for name, bpe in kernels.items():
+        for total in (256 << 20, 1 << 30, 4 << 30):
+            n = int(total / bpe) // 4096 * 4096
+            copies = max(1, -(-4 * L2_BYTES // total))  # rotate over >= 4 x L2 of memory
+            fns = [make(name, n) for _ in range(copies)]
+            for f in fns:
+                f()
+            torch.cuda.synchronize()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for r in range(reps):
+                fns[r % copies]()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1) / reps
+            gbs = n * bpe / (ms / 1000.0) / 1e9
+            print(json.dumps({"kernel": name, "bytes_per_call": int(n * bpe), "copies": copies,
+                              "elements": n, "ms": ms, "GB/s": gbs, "peak_GB/s": hbm,
+                              "frac": gbs / hbm, "peak_source": "%s hbm_gbs" % src}))
+            del fns
+            torch.cuda.empty_cache()
+
+
 # ------------------------------------------------------------------ main arm
 
 def main():
@@ -401,6 +484,10 @@ def main():
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     mao.lib()
+    if args.sweep_hbm:
+        if rank == 0:
+            sweep_hbm(dev)
+        return
 
     K = args.steps if args.steps is not None else DEFAULT_STEPS[wl.index]
     Wu = max(3, args.warmup if args.warmup is not None else DEFAULT_WARMUP[wl.index])

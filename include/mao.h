@@ -19,6 +19,8 @@
  *                                                                 MAO_I8 / MAO_SIGN1 input
  *   update        W <- W - eta*U_bar                              apply_update (U form)
  *
+ * and the blockwise orthogonalisation of the Megatron page    ns_orthogonalize_blockwise
+ *
  * Sources, cited by page title and section:
  *   [SignMuon] "Resumo Técnico: SignMuon: Otimização Distribuída de Muon com Eficiência de
  *              Comunicação" (gist.science, paper 2605.16311), §2 "Metodologia: Sign-Muon".
@@ -169,6 +171,29 @@ mao_status ns_orthogonalize_noalloc(const mao_mat* in, const mao_mat* out, int32
                                     int32_t steps, const float* coeffs, int32_t coeff_stride,
                                     float eps, int32_t compute, uint32_t* const* sign_bits,
                                     void* stream);
+
+/*
+ * Blockwise Newton–Schulz ([Megatron] "分散モード", blockwise paragraph: each rank
+ * orthogonalises only the block of the momentum it owns; no communication, and not the
+ * orthogonalisation of the whole matrix).
+ *
+ * Each matrix is cut into a grid of block_rows x block_cols blocks (the last block row and
+ * column take what is left); every block is orthogonalised on its own exactly as
+ * ns_orthogonalize would orthogonalise that block alone (its own Frobenius norm, its own
+ * orientation), and written to the same place of out[b]. Blocks of equal shape run as one
+ * group; the blocks are read and written in place through strides (no copies).
+ *   in[b]        f32, bf16 or MAO_I8 (not MAO_SIGN1); out[b] f32 or bf16, same shape.
+ *   block_rows, block_cols   >= 1; at most 2^20 blocks per call (else MAO_ERR_UNSUPPORTED).
+ *   Other arguments as ns_orthogonalize (no sign output); workspace of at least
+ *   ns_blockwise_workspace_bytes(in, batch, block_rows, block_cols, compute) bytes.
+ */
+size_t ns_blockwise_workspace_bytes(const mao_mat* X, int32_t batch, int64_t block_rows,
+                                    int64_t block_cols, int32_t compute_dtype);
+mao_status ns_orthogonalize_blockwise(const mao_mat* in, const mao_mat* out, int32_t batch,
+                                      int64_t block_rows, int64_t block_cols, int32_t steps,
+                                      const float* coeffs, int32_t coeff_stride, float eps,
+                                      int32_t compute, void* workspace, size_t workspace_bytes,
+                                      void* stream);
 
 /*
  * Entrywise sign and 1-bit packing ([SignMuon] §2 step 2 "Extração de Sinal" and step 3,

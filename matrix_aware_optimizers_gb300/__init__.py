@@ -8,6 +8,7 @@ Functions (same names as the C ABI):
   muon_momentum_update(M, G, mu)                     M <- mu*M + G
   ns_workspace_bytes(X, compute)                     workspace size for ns_orthogonalize
   ns_orthogonalize(inp, out, steps, coeffs, ...)     Newton–Schulz polar factor (+ packed signs)
+  ns_orthogonalize_blockwise(inp, out, block, ...)   Newton–Schulz of every block on its own
   sign_pack_bits(U, bits)                            sign + 1-bit pack
   majority_vote_packed(bits, nbits, vote)            vote over workers' packed signs
   sign_int8(U, s)                                    sign as int8 +-1 (all-reduce variant)
@@ -138,6 +139,44 @@ def ns_orthogonalize(inp, out, steps=5, coeffs=QUINTIC, eps=1e-7, compute="bf16"
         float(eps), _COMPUTE[compute], barr, ctypes.c_void_p(ws.data_ptr()), ws.numel(),
         _stream(stream))
     _abi.check("ns_orthogonalize", st)
+
+
+def _coeff_args(coeffs, steps):
+    co = list(coeffs)
+    if len(co) == 3 and not isinstance(co[0], (list, tuple)):
+        flat, stride = [float(c) for c in co], 0
+    else:
+        if len(co) != steps:
+            raise ValueError("need one coefficient triple per step")
+        flat, stride = [float(c) for t in co for c in t], 3
+    return (ctypes.c_float * len(flat))(*flat), stride
+
+
+def ns_blockwise_workspace_bytes(X, block, compute="bf16"):
+    Xs = _as_list(X)
+    arr = (_abi.MaoMat * len(Xs))()
+    for i, x in enumerate(Xs):
+        shape = x.shape if hasattr(x, "shape") else x
+        arr[i] = _abi.MaoMat(None, shape[0], shape[1], shape[1], _abi.MAO_F32, 0)
+    n = lib().ns_blockwise_workspace_bytes(arr, len(Xs), int(block[0]), int(block[1]),
+                                           _COMPUTE[compute])
+    if n == 0:
+        raise ValueError("invalid shapes or block for ns_blockwise_workspace_bytes")
+    return int(n)
+
+
+def ns_orthogonalize_blockwise(inp, out, block, steps=5, coeffs=QUINTIC, eps=1e-7,
+                               compute="bf16", ws=None, stream=None):
+    """Newton–Schulz of every (block[0] x block[1]) block of each input on its own."""
+    ins, outs = _as_list(inp), _as_list(out)
+    carr, stride = _coeff_args(coeffs, steps)
+    if ws is None:
+        n = ns_blockwise_workspace_bytes(ins, block, compute)
+        ws = torch.empty(n, dtype=torch.uint8, device=ins[0].device)
+    st = lib().ns_orthogonalize_blockwise(
+        _mats(ins), _mats(outs), len(ins), int(block[0]), int(block[1]), int(steps), carr, stride,
+        float(eps), _COMPUTE[compute], ctypes.c_void_p(ws.data_ptr()), ws.numel(), _stream(stream))
+    _abi.check("ns_orthogonalize_blockwise", st)
 
 
 def packed_words(rows, cols):

@@ -29,6 +29,8 @@ EXPORTS = (
     "ns_workspace_bytes",
     "ns_orthogonalize",
     "ns_orthogonalize_noalloc",
+    "ns_blockwise_workspace_bytes",
+    "ns_orthogonalize_blockwise",
     "sign_pack_bits",
     "majority_vote_packed",
     "sign_int8",
@@ -95,6 +97,13 @@ def load():
     lib.ns_orthogonalize_noalloc.argtypes = [
         P(MaoMat), P(MaoMat), ctypes.c_int32, ctypes.c_int32, P(ctypes.c_float), ctypes.c_int32,
         ctypes.c_float, ctypes.c_int32, P(ctypes.c_void_p), vp]
+    lib.ns_blockwise_workspace_bytes.restype = ctypes.c_size_t
+    lib.ns_blockwise_workspace_bytes.argtypes = [P(MaoMat), ctypes.c_int32, ctypes.c_int64,
+                                                 ctypes.c_int64, ctypes.c_int32]
+    lib.ns_orthogonalize_blockwise.restype = ctypes.c_int
+    lib.ns_orthogonalize_blockwise.argtypes = [
+        P(MaoMat), P(MaoMat), ctypes.c_int32, ctypes.c_int64, ctypes.c_int64, ctypes.c_int32,
+        P(ctypes.c_float), ctypes.c_int32, ctypes.c_float, ctypes.c_int32, vp, ctypes.c_size_t, vp]
     lib.sign_pack_bits.restype = ctypes.c_int
     lib.sign_pack_bits.argtypes = [P(MaoMat), vp, vp]
     lib.majority_vote_packed.restype = ctypes.c_int

@@ -246,6 +246,7 @@ __global__ void __launch_bounds__(256) vote_int8_kernel(const int8_t* __restrict
   uint32_t acc[8];
 #pragma unroll
   for (int q = 0; q < 8; ++q) acc[q] = 0;
+#pragma unroll 4
   for (int m = 0; m < nw; ++m) {
     const int8_t* src = s + int64_t(m) * stride + k0;
     uint32_t x[8];
@@ -302,11 +303,13 @@ __global__ void __launch_bounds__(256) vote_int8_kernel(const int8_t* __restrict
 constexpr int kMaxPlanes = 16;  // counts up to 65535 workers
 
 // Adds one 32-lane word of bits into a bit-sliced binary counter (plane p holds bit p of
-// every lane's count): a ripple of half adders, three logic ops per plane.
-__device__ __forceinline__ void counter_add(uint32_t (&plane)[kMaxPlanes], int P, uint32_t x) {
+// every lane's count): a ripple of half adders, three logic ops per plane. PL planes are
+// held in registers (PL >= P, the planes the worker count needs).
+template <int PL>
+__device__ __forceinline__ void counter_add(uint32_t (&plane)[PL], int P, uint32_t x) {
   uint32_t carry = x;
 #pragma unroll
-  for (int p = 0; p < kMaxPlanes; ++p) {
+  for (int p = 0; p < PL; ++p) {
     if (p < P) {
       const uint32_t t = plane[p] & carry;
       plane[p] ^= carry;
@@ -316,11 +319,11 @@ __device__ __forceinline__ void counter_add(uint32_t (&plane)[kMaxPlanes], int P
 }
 
 // Lanes whose count is >= T, by comparing the bit-sliced count with T from the top bit.
-__device__ __forceinline__ uint32_t counter_ge(const uint32_t (&plane)[kMaxPlanes], int P,
-                                               uint32_t T) {
+template <int PL>
+__device__ __forceinline__ uint32_t counter_ge(const uint32_t (&plane)[PL], int P, uint32_t T) {
   uint32_t gt = 0, eq = 0xFFFFFFFFu;
 #pragma unroll
-  for (int p = kMaxPlanes - 1; p >= 0; --p) {
+  for (int p = PL - 1; p >= 0; --p) {
     if (p < P) {
       if ((T >> p) & 1u) {
         eq &= plane[p];
@@ -333,34 +336,36 @@ __device__ __forceinline__ uint32_t counter_ge(const uint32_t (&plane)[kMaxPlane
   return gt | eq;
 }
 
-template <int V>
+template <int V, int PL>
 __global__ void __launch_bounds__(256) vote_kernel(const uint32_t* __restrict__ bits, int32_t nw,
                                                    int64_t stride, int64_t nwords, int64_t nbits,
                                                    int64_t total_words, uint32_t* __restrict__ vote,
                                                    int P, uint32_t T) {
   const int64_t w0 = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) * V;
   if (w0 >= nwords) return;
-  uint32_t plane[V][kMaxPlanes];
+  uint32_t plane[V][PL];
 #pragma unroll
   for (int v = 0; v < V; ++v)
 #pragma unroll
-    for (int p = 0; p < kMaxPlanes; ++p) plane[v][p] = 0;
+    for (int p = 0; p < PL; ++p) plane[v][p] = 0;
+  // unrolled so that several workers' loads are in flight before the counter updates
+#pragma unroll 4
   for (int m = 0; m < nw; ++m) {
     const uint32_t* src = bits + int64_t(m) * stride + w0;
     if (V == 4) {
       const uint4 x = __ldg(reinterpret_cast<const uint4*>(src));
-      counter_add(plane[0], P, x.x);
-      counter_add(plane[V > 1 ? 1 : 0], P, x.y);
-      counter_add(plane[V > 2 ? 2 : 0], P, x.z);
-      counter_add(plane[V > 3 ? 3 : 0], P, x.w);
+      counter_add<PL>(plane[0], P, x.x);
+      counter_add<PL>(plane[V > 1 ? 1 : 0], P, x.y);
+      counter_add<PL>(plane[V > 2 ? 2 : 0], P, x.z);
+      counter_add<PL>(plane[V > 3 ? 3 : 0], P, x.w);
     } else {
-      counter_add(plane[0], P, __ldg(src));
+      counter_add<PL>(plane[0], P, __ldg(src));
     }
   }
   uint32_t out[V];
 #pragma unroll
   for (int v = 0; v < V; ++v) {
-    out[v] = counter_ge(plane[v], P, T);
+    out[v] = counter_ge<PL>(plane[v], P, T);
     const int64_t w = w0 + v;
     if (w == total_words - 1 && (nbits & 31)) out[v] &= (1u << (nbits & 31)) - 1u;
   }
@@ -370,6 +375,22 @@ __global__ void __launch_bounds__(256) vote_kernel(const uint32_t* __restrict__ 
   } else {
     vote[w0] = out[0];
   }
+}
+
+template <int V>
+void launch_vote(int64_t blocks, cudaStream_t stream, const uint32_t* bits, int32_t nw,
+                 int64_t stride, int64_t nwords, int64_t nbits, int64_t total_words,
+                 uint32_t* vote, int P, uint32_t T) {
+  if (P <= 4)
+    vote_kernel<V, 4><<<unsigned(blocks), 256, 0, stream>>>(bits, nw, stride, nwords, nbits,
+                                                            total_words, vote, P, T);
+  else if (P <= 8)
+    vote_kernel<V, 8><<<unsigned(blocks), 256, 0, stream>>>(bits, nw, stride, nwords, nbits,
+                                                            total_words, vote, P, T);
+  else
+    vote_kernel<V, kMaxPlanes><<<unsigned(blocks), 256, 0, stream>>>(bits, nw, stride, nwords,
+                                                                     nbits, total_words, vote,
+                                                                     P, T);
 }
 
 }  // namespace
@@ -457,16 +478,14 @@ mao_status vote_launch(const uint32_t* bits, int32_t n_workers, int64_t stride, 
   const int64_t bulk = v4 ? (nwords / 4) * 4 : 0;
   if (bulk > 0) {
     const int64_t blocks = ceil_div(bulk / 4, 256);
-    vote_kernel<4><<<unsigned(blocks), 256, 0, stream>>>(bits, n_workers, stride, bulk, nbits,
-                                                         nwords, vote, P, T);
+    launch_vote<4>(blocks, stream, bits, n_workers, stride, bulk, nbits, nwords, vote, P, T);
     count_launch();
   }
   if (nwords > bulk) {
     const int64_t rest = nwords - bulk;
     const int64_t blocks = ceil_div(rest, 256);
-    vote_kernel<1><<<unsigned(blocks), 256, 0, stream>>>(bits + bulk, n_workers, stride, rest,
-                                                         nbits - bulk * 32, nwords - bulk,
-                                                         vote + bulk, P, T);
+    launch_vote<1>(blocks, stream, bits + bulk, n_workers, stride, rest, nbits - bulk * 32,
+                   nwords - bulk, vote + bulk, P, T);
     count_launch();
   }
   return cuda_status(cudaGetLastError());

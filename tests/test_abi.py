@@ -131,3 +131,27 @@ def test_sign_matrix_inputs_only_where_declared(lib):
     assert lib.apply_update(f32, None, i8, 1, 0.01, None) == 1
     # workspace sizes do not depend on the input encoding
     assert lib.ns_workspace_bytes(i8, 1, 1) == lib.ns_workspace_bytes(f32, 1, 1) > 0
+
+
+def test_blockwise_arguments_and_sizes(lib):
+    fake = 0x10000
+    co = (ctypes.c_float * 3)(3.4445, -4.775, 2.0315)
+    ws = ctypes.c_void_p(fake)
+    X = _mats((300, 1000), dtype=_abi.MAO_BF16, data=fake)
+    # the workspace of a blockwise call is that of its blocks as one batch
+    blocks = _mats(*([(128, 256)] * 6 + [(128, 232)] * 2 + [(44, 256)] * 3 + [(44, 232)]))
+    assert lib.ns_blockwise_workspace_bytes(X, 1, 128, 256, 1) == lib.ns_workspace_bytes(blocks, 12, 1)
+    assert lib.ns_blockwise_workspace_bytes(X, 1, 300, 1000, 1) == lib.ns_workspace_bytes(X, 1, 1)
+    assert lib.ns_blockwise_workspace_bytes(X, 1, 0, 256, 1) == 0
+    big = _mats((2048, 1024), dtype=_abi.MAO_BF16, data=fake)
+    assert lib.ns_blockwise_workspace_bytes(big, 1, 1, 1, 1) == 0  # 2^21 blocks > 2^20
+    out = _mats((300, 1000), dtype=_abi.MAO_F32, data=fake)
+    s1 = (_abi.MaoMat * 1)(_abi.MaoMat(fake, 300, 1000, 1000, _abi.MAO_SIGN1, 0))
+    args = (1, 128, 256, 5, co, 0, 1e-7, 1, ws, 1 << 40, None)
+    assert lib.ns_orthogonalize_blockwise(s1, out, *args) == _abi.MAO_ERR_INVALID_ARG
+    assert lib.ns_orthogonalize_blockwise(X, out, 1, 0, 256, 5, co, 0, 1e-7, 1, ws, 1 << 40,
+                                          None) == _abi.MAO_ERR_INVALID_ARG
+    assert lib.ns_orthogonalize_blockwise(X, out, 1, 128, 256, 5, co, 0, 1e-7, 1, None, 1 << 40,
+                                          None) == _abi.MAO_ERR_INVALID_ARG
+    assert lib.ns_orthogonalize_blockwise(X, X, 1, 128, 256, 5, co, 1, 1e-7, 1, ws, 1 << 40,
+                                          None) == _abi.MAO_ERR_INVALID_ARG

@@ -76,7 +76,7 @@ def test_sign_pack_strided(cuda):
     assert np.array_equal(words_np(bits), oracle.pack_signs(oracle.sign_of(to_np(U))))
 
 
-@pytest.mark.parametrize("Wn", [1, 2, 3, 4, 7, 8, 15, 16, 33])
+@pytest.mark.parametrize("Wn", [1, 2, 3, 4, 7, 8, 15, 16, 33, 255, 256, 300])
 @pytest.mark.parametrize("nbits", [1, 31, 32, 100, 4096, 1000003])
 def test_vote_bit_exact(cuda, Wn, nbits):
     rng = np.random.default_rng(Wn * 1000 + nbits % 1000)
