@@ -1,7 +1,8 @@
 // Grouped Newton–Schulz products on the 5th-generation tensor cores (sm_103a).
 //
-// One persistent kernel serves all three products of an iteration (the stage is a launch
-// parameter), over every matrix of up to eight shape groups:
+// One persistent kernel template serves all three products of an iteration (one
+// instantiation per product, and one more for the last product of the last iteration, which
+// writes the caller's outputs), over every matrix of up to eight shape groups:
 //   NS_GRAM   A  = alpha * X X^T              (symmetric: upper and diagonal tiles only)
 //   NS_POLY   B' = a I + b A + c A A          (symmetric; A A = A A^T by symmetry)
 //   NS_APPLY  X' = beta * B' X                (X B' in the tall orientation; B' symmetric)
@@ -455,6 +456,10 @@ __device__ __forceinline__ void store_final(const OutEntry& e, uint8_t* S, int i
 
 // ------------------------------------------------------------------ the kernel
 
+// STAGE selects the epilogue (NS_GRAM, NS_POLY, NS_APPLY); FINAL (NS_APPLY only) writes
+// the caller's outputs instead of the workspace. Each instantiation holds only its own
+// epilogue code.
+template <int STAGE, bool FINAL>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     ns_tc_kernel(const __grid_constant__ TcParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -656,10 +661,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       const int slot = G.slot0 + t.z;
       const float s = p.scale ? p.scale[slot] : 1.0f;
       OutEntry oe;
-      if (G.final_out) oe = p.out_table[slot];
+      if (FINAL) oe = p.out_table[slot];
       const int i0 = t.row0 + HALF * int(cta) + 32 * quad;
       const int i = i0 + lane;
-      const bool poly = p.stage == NS_POLY;
+      constexpr bool poly = STAGE == NS_POLY;
       const __nv_bfloat16* res =
           reinterpret_cast<const __nv_bfloat16*>(G.res) + int64_t(t.z) * G.res_mstride;
       // blocks of 64 columns of the tile (the last one reaches into the zero padding)
@@ -698,7 +703,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 #ifdef MAO_TC_TRACE
         if (lane == 0 && leader) { TRACE_ADD(9, te); te = clock64(); }
 #endif
-        if (p.stage == NS_GRAM) {
+        if (STAGE == NS_GRAM) {
           const float alpha = s * s;
 #pragma unroll
           for (int c = 0; c < 64; ++c) w[c] *= alpha;
@@ -727,7 +732,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 #pragma unroll
           for (int c = 0; c < 64; ++c) w[c] *= s;
         }
-        if (G.final_out) {
+        if (FINAL) {
           store_final(oe, S, i0, jb, G.M, G.N, G.orig_cols, lane, w);
         } else {
           // workspace outputs cover the zero-padded row: the bulk store writes the whole
@@ -828,18 +833,29 @@ mao_status tc_encode_store_map(CUtensorMap* map, const void* base, int64_t rows,
 
 mao_status tc_gemm_launch(const TcParams& p, cudaStream_t stream) {
   if (p.total_tiles <= 0) return MAO_OK;
+  using Kernel = void (*)(TcParams);
+  const Kernel kernels[4] = {ns_tc_kernel<NS_GRAM, false>, ns_tc_kernel<NS_POLY, false>,
+                             ns_tc_kernel<NS_APPLY, false>, ns_tc_kernel<NS_APPLY, true>};
   static std::once_flag attr_once[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return MAO_ERR_CUDA;
   cudaError_t attr_err = cudaSuccess;
   std::call_once(attr_once[dev & 63], [&] {
-    attr_err = cudaFuncSetAttribute(ns_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    int(SMEM_BYTES));
+    for (Kernel k : kernels) {
+      const cudaError_t e =
+          cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, int(SMEM_BYTES));
+      if (e != cudaSuccess) attr_err = e;
+    }
   });
   if (attr_err != cudaSuccess) return MAO_ERR_CUDA;
+  // every group of one launch is either final or not (the last iteration's product)
+  const bool final_out = p.g[0].final_out != 0;
+  if (p.stage < NS_GRAM || p.stage > NS_APPLY || (final_out && p.stage != NS_APPLY))
+    return MAO_ERR_INVALID_ARG;
+  const Kernel k = kernels[final_out ? 3 : p.stage - NS_GRAM];
   const int pairs = p.total_tiles < num_sms() / 2 ? p.total_tiles : num_sms() / 2;
   profile_before_launch(stream);
-  ns_tc_kernel<<<2 * pairs, THREADS, SMEM_BYTES, stream>>>(p);
+  k<<<2 * pairs, THREADS, SMEM_BYTES, stream>>>(p);
   count_launch();
   profile_after_launch(stream);
   return cuda_status(cudaGetLastError());
