@@ -65,16 +65,23 @@ constexpr int STAGES = MAO_TC_STAGES;
 constexpr int CHUNK_BYTES = HALF * CHUNK * 2;     // 16 KB
 constexpr int HALF_BYTES = 2 * CHUNK_BYTES;       // 32 KB
 constexpr int STAGE_BYTES = 2 * HALF_BYTES;       // A half + B half
-constexpr int EPI_WARPS = 4;     // one epilogue warp per 32-lane TMEM quadrant
-constexpr int THREADS = 64 + 32 * EPI_WARPS;  // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
+// Epilogue warps: the products that write the workspace use two warps per 32-lane TMEM
+// quadrant (eight), each taking every other 64-column block of the tile, with one staging
+// buffer each; the last product, which writes the caller's outputs, uses one warp per
+// quadrant (four) with two staging buffers each. Both layouts stage 32 KB.
+constexpr int EPI_WARPS_WS = 8;
+constexpr int EPI_WARPS_FINAL = 4;
+constexpr int epi_warps(bool final_out) { return final_out ? EPI_WARPS_FINAL : EPI_WARPS_WS; }
+// warp 0 TMA, warp 1 MMA, then the epilogue warps
+constexpr int threads(bool final_out) { return 64 + 32 * epi_warps(final_out); }
 constexpr int TMEM_COLS = 512;   // two 256-column fp32 accumulators
 // Epilogue staging: 32 x 64 bf16 row-major blocks (128-byte rows, 16-byte chunks XOR-
-// swizzled by row) and their 64 x 32 transposes (64-byte rows); two buffers per warp.
+// swizzled by row).
 constexpr int EP_BYTES = 32 * 64 * 2;             // 4 KB
-constexpr int EP_BUFS = 2;
+constexpr int STAGING_BYTES = 8 * EP_BYTES;       // 32 KB
 constexpr int MAX_GROUPS = 8;
 constexpr size_t SMEM_BYTES = 1024 /*align*/ + size_t(STAGES) * STAGE_BYTES +
-                              size_t(EPI_WARPS) * EP_BUFS * EP_BYTES + 256 /*barriers*/;
+                              size_t(STAGING_BYTES) + 256 /*barriers*/;
 static_assert(SMEM_BYTES <= 232448, "shared memory budget of one CTA");
 }  // namespace tc
 

@@ -339,49 +339,27 @@ __device__ __forceinline__ void store_rows(const uint8_t* S, __nv_bfloat16* dst,
   }
 }
 
-// Starts copying the 32 x 64 residual block (rows i0.., columns jb..) into the row-major
-// staging layout of R with asynchronous 16-byte copies (cp.async, zero fill outside the
-// matrix) and commits them as one group.
-__device__ __forceinline__ void prefetch_rows(uint8_t* R, const __nv_bfloat16* src, int64_t ld,
-                                              int i0, int jb, int M, int N, int lane) {
-  const int sg = lane & 7;
+// This lane's residual row: 64 bf16 values (row i, columns jb..jb+63) as eight 16-byte
+// words, loaded straight into registers (zeros for rows at or beyond M). Rows of the
+// workspace are 128-byte aligned and zero-padded to a multiple of 64 columns, so the 64
+// columns of a block are always addressable.
+__device__ __forceinline__ void load_res_row(const __nv_bfloat16* src, int64_t ld, int i, int jb,
+                                             int M, uint4 (&r)[8]) {
+  if (i < M) {
+    const uint4* q = reinterpret_cast<const uint4*>(src + int64_t(i) * ld + jb);
 #pragma unroll
-  for (int q = 0; q < 8; ++q) {
-    const int r = (lane >> 3) + 4 * q;
-    const int gi = i0 + r;
-    const int gj = jb + 8 * sg;
-    int bytes = 0;
-    const __nv_bfloat16* g = src;
-    if (gi < M && gj < N) {
-      g = src + int64_t(gi) * ld + gj;
-      bytes = 2 * min(8, N - gj);
-    }
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(R + srow(r, sg))),
-                 "l"(g), "r"(bytes)
-                 : "memory");
+    for (int k = 0; k < 8; ++k) r[k] = __ldg(q + k);
+  } else {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) r[k] = make_uint4(0u, 0u, 0u, 0u);
   }
-  asm volatile("cp.async.commit_group;" ::: "memory");
 }
 
-// Waits until at most `pending` committed copy groups of this thread are outstanding.
-template <int PENDING>
-__device__ __forceinline__ void prefetch_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(PENDING) : "memory");
-}
-
-// This lane's row (64 values) of a staged row-major block.
-__device__ __forceinline__ void read_row(const uint8_t* R, int lane, float* r) {
-#pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    const uint4 u = *reinterpret_cast<const uint4*>(R + srow(lane, k));
-    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const float2 f = __bfloat1622float2(h[e]);
-      r[8 * k + 2 * e] = f.x;
-      r[8 * k + 2 * e + 1] = f.y;
-    }
-  }
+// Element c (0..63) of a residual row held as eight 16-byte words.
+__device__ __forceinline__ float res_elem(const uint4 (&r)[8], int c) {
+  const uint4& u = r[c >> 3];
+  const uint32_t w = (c & 7) < 2 ? u.x : (c & 7) < 4 ? u.y : (c & 7) < 6 ? u.z : u.w;
+  return __uint_as_float((c & 1) ? (w & 0xFFFF0000u) : (w << 16));
 }
 
 // Final output of the last product for this lane's row, columns jb..jb+63: U (through the
@@ -460,15 +438,17 @@ __device__ __forceinline__ void store_final(const OutEntry& e, uint8_t* S, int i
 // the caller's outputs instead of the workspace. Each instantiation holds only its own
 // epilogue code.
 template <int STAGE, bool FINAL>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads(FINAL), 1)
     ns_tc_kernel(const __grid_constant__ TcParams p) {
+  constexpr int NEPI = epi_warps(FINAL);  // epilogue warps
+  constexpr int SPLIT = NEPI / 4;         // epilogue warps per TMEM quadrant
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* ring = smem;
   uint8_t* staging = smem + STAGES * STAGE_BYTES;
   uint64_t* bars =
-      reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES + EPI_WARPS * EP_BUFS * EP_BYTES);
+      reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES + STAGING_BYTES);
   uint64_t* full_bar = bars;                // [STAGES]  (used in the even CTA)
   uint64_t* empty_bar = bars + STAGES;      // [STAGES]
   uint64_t* tfull_bar = bars + 2 * STAGES;  // [2]
@@ -491,7 +471,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(smem_u32(&tfull_bar[a]), 1);
-      mbar_init(smem_u32(&tempty_bar[a]), 2 * EPI_WARPS);
+      mbar_init(smem_u32(&tempty_bar[a]), 2 * NEPI);
     }
     mbar_init(smem_u32(drain_bar), 1);
     *abort_flag = 0;
@@ -646,9 +626,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue (both CTAs)
-    const int quad = warp & 3;  // TMEM lanes 32*quad .. 32*quad+31 = this warp's rows
-    uint8_t* buf[2] = {staging + (warp - 2) * EP_BUFS * EP_BYTES,
-                       staging + ((warp - 2) * EP_BUFS + 1) * EP_BYTES};
+    const int quad = warp & 3;              // TMEM lanes 32*quad .. 32*quad+31 = this warp's rows
+    const int part = (warp - 2) / 4;        // which of the quadrant's SPLIT warps
+    // staging: FINAL, four warps with two buffers each; otherwise eight warps with one
+    uint8_t* buf[2] = {staging + (warp - 2) * (2 / SPLIT) * EP_BYTES,
+                       staging + ((warp - 2) * (2 / SPLIT) + (SPLIT == 1 ? 1 : 0)) * EP_BYTES};
     const uint32_t tempty_leader[2] = {mapa_shared(smem_u32(&tempty_bar[0]), 0),
                                        mapa_shared(smem_u32(&tempty_bar[1]), 0)};
     int local = 0;
@@ -659,22 +641,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       const int acc = local & 1;
       const uint32_t acc_phase = uint32_t(local >> 1) & 1u;
       const int slot = G.slot0 + t.z;
-      const float s = p.scale ? p.scale[slot] : 1.0f;
+      // the Frobenius scale applies in the first iteration only (p.scale is null after)
+      const bool scaled = p.scale != nullptr;
+      const float s = scaled ? p.scale[slot] : 1.0f;
       OutEntry oe;
       if (FINAL) oe = p.out_table[slot];
       const int i0 = t.row0 + HALF * int(cta) + 32 * quad;
       const int i = i0 + lane;
-      constexpr bool poly = STAGE == NS_POLY;
-      const __nv_bfloat16* res =
-          reinterpret_cast<const __nv_bfloat16*>(G.res) + int64_t(t.z) * G.res_mstride;
-      // blocks of 64 columns of the tile (the last one reaches into the zero padding)
+      // blocks of 64 columns of the tile (the last one reaches into the zero padding);
+      // this warp takes blocks part, part + SPLIT, ...
       const int nb = min(BN / 64, (G.N - t.col0 + 63) / 64);
-      // the first residual block is fetched while the accumulator is still being produced
-      // (into a buffer the previous tile's bulk stores must have finished reading)
-      if (poly && nb > 0) {
-        if (lane == 0) bulk_wait_read();
-        __syncwarp();
-        prefetch_rows(buf[0], res, G.res_ld, i0, t.col0, G.M, G.N, lane);
+      // NS_POLY: this warp's residual rows (A) are fetched while the accumulator is still
+      // being produced (at most two blocks per warp per tile)
+      uint4 res0[8], res1[8];
+      if (STAGE == NS_POLY) {
+        const __nv_bfloat16* res =
+            reinterpret_cast<const __nv_bfloat16*>(G.res) + int64_t(t.z) * G.res_mstride;
+        static_assert(STAGE != NS_POLY || SPLIT == 2, "residual registers cover two blocks");
+        if (part < nb) load_res_row(res, G.res_ld, i, t.col0 + 64 * part, G.M, res0);
+        if (part + SPLIT < nb) load_res_row(res, G.res_ld, i, t.col0 + 64 * (part + SPLIT), G.M, res1);
       }
 #ifdef MAO_TC_TRACE
       const long long tw2 = clock64();
@@ -685,50 +670,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       if (lane == 0 && leader) TRACE_ADD(3, tw2);
       const long long tb = clock64();
 #endif
-      __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(G.out) + int64_t(t.z) * G.out_mstride;
       const uint32_t trow = tmem_base + (uint32_t(32 * quad) << 16) + uint32_t(acc * BN);
-      for (int b = 0; b < nb; ++b) {
+      // unrolled so that the residual registers are selected at compile time
+#pragma unroll
+      for (int nth = 0; nth < 4 / SPLIT; ++nth) {
+        const int b = part + SPLIT * nth;
+        if (b >= nb) break;
         const int jb = t.col0 + 64 * b;
-        uint8_t* S = buf[b & 1];
-        if (!poly) {  // S was the source of the bulk stores two blocks ago
-          if (lane == 0) bulk_wait_read();
-          __syncwarp();
-        }
+        uint8_t* S = buf[nth & 1];
         float w[64];
-#ifdef MAO_TC_TRACE
-        long long te = clock64();
-#endif
         tmem_ld32(trow + uint32_t(64 * b), w);
         tmem_ld32(trow + uint32_t(64 * b + 32), w + 32);
-#ifdef MAO_TC_TRACE
-        if (lane == 0 && leader) { TRACE_ADD(9, te); te = clock64(); }
-#endif
         if (STAGE == NS_GRAM) {
-          const float alpha = s * s;
+          if (scaled) {
+            const float alpha = s * s;
 #pragma unroll
-          for (int c = 0; c < 64; ++c) w[c] *= alpha;
-        } else if (poly) {
-          // next block's residual in flight while this one is used (its buffer was the
-          // source of the previous block's bulk stores: those must have read it)
-          if (b + 1 < nb) {
-            if (lane == 0) bulk_wait_read();
-            __syncwarp();
-            prefetch_rows(buf[(b + 1) & 1], res, G.res_ld, i0, jb + 64, G.M, G.N, lane);
-            prefetch_wait<1>();
-          } else {
-            prefetch_wait<0>();
+            for (int c = 0; c < 64; ++c) w[c] *= alpha;
           }
-          __syncwarp();
-          float r[64];
-          read_row(S, lane, r);
-          __syncwarp();
-#ifdef MAO_TC_TRACE
-          if (lane == 0 && leader) { TRACE_ADD(12, te); te = clock64(); }
-#endif
+        } else if (STAGE == NS_POLY) {
+          // B' = c (A A) + b A, plus a on the diagonal
+          const uint4(&r)[8] = nth == 0 ? res0 : res1;
 #pragma unroll
-          for (int c = 0; c < 64; ++c)
-            w[c] = __fmaf_rn(p.c, w[c], p.b * r[c]) + (jb + c == i ? p.a : 0.0f);
-        } else {
+          for (int c = 0; c < 64; ++c) w[c] = __fmaf_rn(p.c, w[c], p.b * res_elem(r, c));
+          if (i0 < jb + 64 && jb < i0 + 32) {  // the block meets the diagonal
+#pragma unroll
+            for (int c = 0; c < 64; ++c) w[c] += (jb + c == i) ? p.a : 0.0f;
+          }
+        } else if (scaled) {
 #pragma unroll
           for (int c = 0; c < 64; ++c) w[c] *= s;
         }
@@ -736,18 +704,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           store_final(oe, S, i0, jb, G.M, G.N, G.orig_cols, lane, w);
         } else {
           // workspace outputs cover the zero-padded row: the bulk store writes the whole
-          // 64-column block (its padding columns hold zeros)
-#ifdef MAO_TC_TRACE
-          if (lane == 0 && leader) te = clock64();
-#endif
+          // 64-column block (its padding columns hold zeros). The single staging buffer
+          // must have been read by this warp's previous bulk store.
+          if (lane == 0) bulk_wait_read();
+          __syncwarp();
           stage_rows(S, lane, w);
           fence_async_smem();
           __syncwarp();
-          if (lane == 0) tma_store_3d(&G.tmOR, smem_u32(S), jb, i0, t.z);
-#ifdef MAO_TC_TRACE
-          if (lane == 0 && leader) { TRACE_ADD(10, te); te = clock64(); }
-#endif
-          if (lane == 0) bulk_commit();
+          if (lane == 0) {
+            tma_store_3d(&G.tmOR, smem_u32(S), jb, i0, t.z);
+            bulk_commit();
+          }
           __syncwarp();
         }
       }
@@ -761,7 +728,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
       }
 #endif
     }
-    prefetch_wait<0>();  // no copy into shared memory may outlive the loop (timeout path)
     if (lane == 0) bulk_wait_all();  // stores complete before the CTA leaves
     __syncwarp();
   }
@@ -855,7 +821,7 @@ mao_status tc_gemm_launch(const TcParams& p, cudaStream_t stream) {
   const Kernel k = kernels[final_out ? 3 : p.stage - NS_GRAM];
   const int pairs = p.total_tiles < num_sms() / 2 ? p.total_tiles : num_sms() / 2;
   profile_before_launch(stream);
-  k<<<2 * pairs, THREADS, SMEM_BYTES, stream>>>(p);
+  k<<<2 * pairs, threads(final_out), SMEM_BYTES, stream>>>(p);
   count_launch();
   profile_after_launch(stream);
   return cuda_status(cudaGetLastError());
