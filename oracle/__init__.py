@@ -40,11 +40,17 @@ against something other than itself):
   muon.post_vote_polar     Newton-Schulz pins (it is newton_schulz on the +-1 matrix)
   muon.apply_update        hand-computed rounding table (tests/golden/update_rounding.txt)
   muon.sign_muon_step      composition checked against an SVD-route recomputation
+  dion.orthonormalise_columns  classical Gram-Schmidt loop; P = Q R with R upper triangular
+  dion.column_normalize    unit column norms, directions kept, zero columns
+  dion.dion_step           exact rank-r buffer with Q_prev = its right singular vectors gives
+                           the polar factor U V^T; full rank gives M = mu B; error feedback
+                           M + (1 - mu) P R^T = B
 
 No function is "parity unpinned".
 """
 
 from .rounding import bf16_rne, fma_f32, to_f32
+from .dion import column_normalize, dion_step, orthonormalise_columns
 from .muon import (
     QUINTIC,
     CUBIC,
@@ -72,4 +78,5 @@ __all__ = [
     "pack_signs_loop", "unpack_signs", "majority_vote", "int8_sum_vote", "post_vote_polar",
     "apply_update",
     "apply_update_f64", "sign_muon_step", "muon_step", "ns_dense_flops",
+    "orthonormalise_columns", "column_normalize", "dion_step",
 ]
