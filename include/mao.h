@@ -20,6 +20,7 @@
  *   update        W <- W - eta*U_bar                              apply_update (U form)
  *
  * and the blockwise orthogonalisation of the Megatron page    ns_orthogonalize_blockwise
+ * and one step of Dion, the low-rank orthonormal optimizer    dion_step
  *
  * Sources, cited by page title and section:
  *   [SignMuon] "Resumo Técnico: SignMuon: Otimização Distribuída de Muon com Eficiência de
@@ -62,7 +63,8 @@ typedef enum mao_status {
   MAO_ERR_MISALIGNED = 3,   /* pointer not aligned to its element size / workspace to 256 B */
   MAO_ERR_WORKSPACE = 4,    /* workspace smaller than ns_workspace_bytes() */
   MAO_ERR_CUDA = 5,         /* a CUDA runtime call or launch failed */
-  MAO_ERR_TIMEOUT = 6       /* a device-side wait gave up (reported by mao_sync_status) */
+  MAO_ERR_TIMEOUT = 6,      /* a device-side wait gave up (reported by mao_sync_status) */
+  MAO_ERR_NUMERIC = 7       /* a factorisation met a non-positive pivot (mao_sync_status) */
 } mao_status;
 
 /*
@@ -259,8 +261,36 @@ mao_status apply_update(const mao_mat* W, const uint32_t* const* vote, const mao
                         int32_t batch, float lr, void* stream);
 
 /*
- * Synchronise `stream`, then read and clear the device-side error word that kernels set
- * when a bounded wait gives up. Returns MAO_OK, MAO_ERR_TIMEOUT or MAO_ERR_CUDA.
+ * One Dion step ([Dion] "대규모 AI 모델 학습을 10배 빠르게: Dion 옵티마이저를 사용한 분산 학습",
+ * algorithm section) for `batch` parameter matrices of ONE shape m x n and rank r:
+ *
+ *   B = M + G;  P = orthonormalise(B Q);  R = B^T P
+ *   M <- B - (1 - mu) P R^T;  Q <- ColumnNormalize(R);  X <- X - lr P Q^T
+ *
+ * orthonormalise gives the Q factor of the thin QR of B Q with a positive triangular
+ * diagonal (computed as Cholesky QR applied twice, in fp32); ColumnNormalize divides each
+ * column by its Euclidean norm (a zero column stays zero).
+ *   X[b], M[b]  in/out, f32 or bf16, m x n;  G[b] in, f32 or bf16, m x n.
+ *   Q[b]        in/out, f32, n x r (any ld): the previous right factor in, the new one out.
+ *   P_out       NULL, or HOST array of `batch` device pointers (each may be NULL): the
+ *               final P, m x r fp32, row stride r.
+ *   rank        1..256, at most min(m, n).  compute  MAO_BF16 only: B, Q, P and R enter
+ *               the three dense products (B Q, B^T P, P R^T / P Q^T) as bf16 with fp32
+ *               accumulation on tcgen05 tensor cores; everything else is fp32.
+ *   workspace   >= dion_workspace_bytes(X, batch, rank) bytes, 256-byte aligned.
+ *   Errors: MAO_ERR_INVALID_ARG for shapes that differ within the batch or a bad rank;
+ *   B Q without full column rank (a non-positive Cholesky pivot) is reported by
+ *   mao_sync_status() as MAO_ERR_NUMERIC (the pivot is replaced by 1e-30).
+ */
+size_t dion_workspace_bytes(const mao_mat* X, int32_t batch, int32_t rank);
+mao_status dion_step(const mao_mat* X, const mao_mat* M, const mao_mat* G, const mao_mat* Q,
+                     float* const* P_out, int32_t batch, int32_t rank, float mu, float lr,
+                     int32_t compute, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Synchronise `stream`, then read and clear the device-side error words that kernels set
+ * when a bounded wait gives up or a factorisation meets a non-positive pivot. Returns
+ * MAO_OK, MAO_ERR_TIMEOUT, MAO_ERR_NUMERIC or MAO_ERR_CUDA.
  */
 mao_status mao_sync_status(void* stream);
 

@@ -14,6 +14,7 @@ Functions (same names as the C ABI):
   sign_int8(U, s)                                    sign as int8 +-1 (all-reduce variant)
   majority_vote_int8(s, n, sum, s_bar, vote)         int8 SUM over workers + threshold
   apply_update(W, lr, vote=..., U=...)               W <- W - lr*D
+  dion_step(X, M, G, Q, mu, lr, ...)                 one Dion step (low-rank, error feedback)
   sync_status()                                      stream sync + device error word
 """
 
@@ -249,6 +250,50 @@ def apply_update(W, lr, vote=None, U=None, stream=None):
         uarr = _mats(_as_list(U))
     st = lib().apply_update(_mats(Ws), varr, uarr, len(Ws), float(lr), _stream(stream))
     _abi.check("apply_update", st)
+
+
+def dion_workspace_bytes(shape, rank, count=1):
+    arr = (_abi.MaoMat * count)()
+    for i in range(count):
+        arr[i] = _abi.MaoMat(None, shape[0], shape[1], shape[1], _abi.MAO_F32, 0)
+    n = lib().dion_workspace_bytes(arr, count, int(rank))
+    if n == 0:
+        raise ValueError("invalid shape or rank for dion_workspace_bytes")
+    return int(n)
+
+
+def _q_mat(q):
+    if not q.is_cuda or q.dtype != torch.float32 or q.dim() != 2 or q.stride(1) != 1:
+        raise ValueError("Q must be a 2-D float32 CUDA tensor with unit column stride")
+    return _abi.MaoMat(q.data_ptr(), q.shape[0], q.shape[1], max(q.stride(0), q.shape[1]),
+                       _abi.MAO_F32, 0)
+
+
+def dion_step(X, M, G, Q, mu, lr, P_out=None, ws=None, stream=None):
+    """One Dion step for each (X, M, G, Q): X, M updated in place, Q replaced by the new right
+    factor (n x r, float32). Matrices are grouped by shape; each group is one C call.
+    P_out: optional float32 tensors (m x r, contiguous) receiving the final P."""
+    Xs, Ms, Gs, Qs = _as_list(X), _as_list(M), _as_list(G), _as_list(Q)
+    Ps = _as_list(P_out) if P_out is not None else [None] * len(Xs)
+    groups = {}
+    for i, x in enumerate(Xs):
+        groups.setdefault((tuple(x.shape), Qs[i].shape[1]), []).append(i)
+    for (shape, rank), idx in groups.items():
+        need = dion_workspace_bytes(shape, rank, len(idx))
+        w = ws if ws is not None and ws.numel() >= need else \
+            torch.empty(need, dtype=torch.uint8, device=Xs[idx[0]].device)
+        qarr = (_abi.MaoMat * len(idx))()
+        for k, i in enumerate(idx):
+            qarr[k] = _q_mat(Qs[i])
+        parr = None
+        if any(Ps[i] is not None for i in idx):
+            parr = (ctypes.c_void_p * len(idx))(
+                *[Ps[i].data_ptr() if Ps[i] is not None else None for i in idx])
+        st = lib().dion_step(
+            _mats([Xs[i] for i in idx]), _mats([Ms[i] for i in idx]), _mats([Gs[i] for i in idx]),
+            qarr, parr, len(idx), int(rank), float(mu), float(lr), _abi.MAO_BF16,
+            ctypes.c_void_p(w.data_ptr()), w.numel(), _stream(stream))
+        _abi.check("dion_step", st)
 
 
 def sync_status(stream=None):

@@ -12,6 +12,7 @@ MAO_ERR_MISALIGNED = 3
 MAO_ERR_WORKSPACE = 4
 MAO_ERR_CUDA = 5
 MAO_ERR_TIMEOUT = 6
+MAO_ERR_NUMERIC = 7
 
 MAO_F32 = 0
 MAO_BF16 = 1
@@ -36,6 +37,8 @@ EXPORTS = (
     "sign_int8",
     "majority_vote_int8",
     "apply_update",
+    "dion_workspace_bytes",
+    "dion_step",
     "mao_sync_status",
     "mao_launch_count",
     "mao_profile_begin",
@@ -116,6 +119,12 @@ def load():
     lib.apply_update.restype = ctypes.c_int
     lib.apply_update.argtypes = [P(MaoMat), P(ctypes.c_void_p), P(MaoMat), ctypes.c_int32,
                                  ctypes.c_float, vp]
+    lib.dion_workspace_bytes.restype = ctypes.c_size_t
+    lib.dion_workspace_bytes.argtypes = [P(MaoMat), ctypes.c_int32, ctypes.c_int32]
+    lib.dion_step.restype = ctypes.c_int
+    lib.dion_step.argtypes = [P(MaoMat), P(MaoMat), P(MaoMat), P(MaoMat), P(ctypes.c_void_p),
+                              ctypes.c_int32, ctypes.c_int32, ctypes.c_float, ctypes.c_float,
+                              ctypes.c_int32, vp, ctypes.c_size_t, vp]
     lib.mao_sync_status.restype = ctypes.c_int
     lib.mao_sync_status.argtypes = [vp]
     lib.mao_launch_count.restype = ctypes.c_int64

@@ -88,6 +88,7 @@ const char* mao_status_string(mao_status s) {
     case MAO_ERR_WORKSPACE: return "MAO_ERR_WORKSPACE";
     case MAO_ERR_CUDA: return "MAO_ERR_CUDA";
     case MAO_ERR_TIMEOUT: return "MAO_ERR_TIMEOUT";
+    case MAO_ERR_NUMERIC: return "MAO_ERR_NUMERIC";
   }
   return "MAO_ERR_UNKNOWN";
 }
@@ -196,7 +197,10 @@ mao_status apply_update(const mao_mat* W, const uint32_t* const* vote, const mao
 }
 
 mao_status mao_sync_status(void* stream) {
-  return tc_read_and_clear_error(static_cast<cudaStream_t>(stream));
+  const mao_status a = tc_read_and_clear_error(static_cast<cudaStream_t>(stream));
+  const mao_status b = dion_read_and_clear_error(static_cast<cudaStream_t>(stream));
+  if (a == MAO_ERR_CUDA || b == MAO_ERR_CUDA) return MAO_ERR_CUDA;
+  return a != MAO_OK ? a : b;
 }
 
 int64_t mao_launch_count(void) { return g_launches.load(); }

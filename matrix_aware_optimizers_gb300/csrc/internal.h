@@ -34,6 +34,8 @@ void profile_after_launch(cudaStream_t stream);
 
 // Reads and clears the device error word of the tensor-core kernels (after a stream sync).
 mao_status tc_read_and_clear_error(cudaStream_t stream);
+// Reads and clears the Cholesky pivot error word of the Dion kernels.
+mao_status dion_read_and_clear_error(cudaStream_t stream);
 
 // Entry in the workspace table of final outputs, one per matrix slot.
 struct OutEntry {

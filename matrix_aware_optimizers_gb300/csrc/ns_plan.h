@@ -86,6 +86,9 @@ static_assert(SMEM_BYTES <= 232448, "shared memory budget of one CTA");
 }  // namespace tc
 
 enum NsStage : int32_t { NS_GRAM = 1, NS_POLY = 2, NS_APPLY = 3 };
+// Products of the same kernel outside Newton–Schulz: an in-place rank-k update of the
+// caller's matrix, out <- out + a * (A B^T), written through the slot's OutEntry.
+constexpr int32_t TC_UPDATE = 4;
 
 struct TcGroup {
   CUtensorMap tmA;          // operand A source (4-D: 64 columns, rows, column chunk, matrix)

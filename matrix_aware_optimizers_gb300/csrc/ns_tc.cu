@@ -432,6 +432,51 @@ __device__ __forceinline__ void store_final(const OutEntry& e, uint8_t* S, int i
   }
 }
 
+// In-place update of the caller's matrix for this lane's row, columns jb..jb+63:
+// out = fmaf(alpha, acc, out) in fp32, rounded to out's dtype.
+__device__ __forceinline__ void update_final(const OutEntry& e, int i0, int jb, int M, int N,
+                                             int lane, const float* w, float alpha) {
+  const int i = i0 + lane;
+  if (i >= M) return;
+  if ((e.flags & OUT_VEC) && jb + 64 <= N) {
+    if (e.dtype == MAO_BF16) {
+      uint4* g = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(e.out) +
+                                          int64_t(i) * e.ld + jb);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        uint4 u = g[k];
+        uint32_t* h = reinterpret_cast<uint32_t*>(&u);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float lo = __uint_as_float(h[q] << 16), hi = __uint_as_float(h[q] & 0xFFFF0000u);
+          h[q] = pack_bf16x2(__fmaf_rn(alpha, w[8 * k + 2 * q], lo),
+                             __fmaf_rn(alpha, w[8 * k + 2 * q + 1], hi));
+        }
+        g[k] = u;
+      }
+    } else {
+      float4* g = reinterpret_cast<float4*>(reinterpret_cast<float*>(e.out) + int64_t(i) * e.ld + jb);
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        float4 v = g[k];
+        v.x = __fmaf_rn(alpha, w[4 * k], v.x);
+        v.y = __fmaf_rn(alpha, w[4 * k + 1], v.y);
+        v.z = __fmaf_rn(alpha, w[4 * k + 2], v.z);
+        v.w = __fmaf_rn(alpha, w[4 * k + 3], v.w);
+        g[k] = v;
+      }
+    }
+  } else {
+#pragma unroll
+    for (int c = 0; c < 64; ++c) {
+      if (jb + c < N) {
+        const int64_t idx = int64_t(i) * e.ld + jb + c;
+        store_elem(e.out, idx, e.dtype, __fmaf_rn(alpha, w[c], load_elem(e.out, idx, e.dtype)));
+      }
+    }
+  }
+}
+
 // ------------------------------------------------------------------ the kernel
 
 // STAGE selects the epilogue (NS_GRAM, NS_POLY, NS_APPLY); FINAL (NS_APPLY only) writes
@@ -696,11 +741,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads(FINAL), 1)
 #pragma unroll
             for (int c = 0; c < 64; ++c) w[c] += (jb + c == i) ? p.a : 0.0f;
           }
-        } else if (scaled) {
+        } else if (STAGE == NS_APPLY && scaled) {
 #pragma unroll
           for (int c = 0; c < 64; ++c) w[c] *= s;
         }
-        if (FINAL) {
+        if (STAGE == TC_UPDATE) {
+          update_final(oe, i0, jb, G.M, G.N, lane, w, p.a);
+        } else if (FINAL) {
           store_final(oe, S, i0, jb, G.M, G.N, G.orig_cols, lane, w);
         } else {
           // workspace outputs cover the zero-padded row: the bulk store writes the whole
@@ -800,8 +847,9 @@ mao_status tc_encode_store_map(CUtensorMap* map, const void* base, int64_t rows,
 mao_status tc_gemm_launch(const TcParams& p, cudaStream_t stream) {
   if (p.total_tiles <= 0) return MAO_OK;
   using Kernel = void (*)(TcParams);
-  const Kernel kernels[4] = {ns_tc_kernel<NS_GRAM, false>, ns_tc_kernel<NS_POLY, false>,
-                             ns_tc_kernel<NS_APPLY, false>, ns_tc_kernel<NS_APPLY, true>};
+  const Kernel kernels[5] = {ns_tc_kernel<NS_GRAM, false>, ns_tc_kernel<NS_POLY, false>,
+                             ns_tc_kernel<NS_APPLY, false>, ns_tc_kernel<NS_APPLY, true>,
+                             ns_tc_kernel<TC_UPDATE, true>};
   static std::once_flag attr_once[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return MAO_ERR_CUDA;
@@ -814,11 +862,12 @@ mao_status tc_gemm_launch(const TcParams& p, cudaStream_t stream) {
     }
   });
   if (attr_err != cudaSuccess) return MAO_ERR_CUDA;
-  // every group of one launch is either final or not (the last iteration's product)
-  const bool final_out = p.g[0].final_out != 0;
-  if (p.stage < NS_GRAM || p.stage > NS_APPLY || (final_out && p.stage != NS_APPLY))
+  // every group of one launch is either final or not (the last iteration's product); the
+  // rank-k update always writes the caller's matrices
+  const bool final_out = p.g[0].final_out != 0 || p.stage == TC_UPDATE;
+  if (p.stage < NS_GRAM || p.stage > TC_UPDATE || (final_out && p.stage < NS_APPLY))
     return MAO_ERR_INVALID_ARG;
-  const Kernel k = kernels[final_out ? 3 : p.stage - NS_GRAM];
+  const Kernel k = p.stage == TC_UPDATE ? kernels[4] : kernels[final_out ? 3 : p.stage - NS_GRAM];
   const int pairs = p.total_tiles < num_sms() / 2 ? p.total_tiles : num_sms() / 2;
   profile_before_launch(stream);
   k<<<2 * pairs, threads(final_out), SMEM_BYTES, stream>>>(p);
