@@ -5,9 +5,14 @@ A step is the whole hot path over one batch of synthetic input resident in HBM:
   Muon:       momentum -> Newton–Schulz (bf16 tensor cores) -> W <- W - lr*U
   Sign-Muon:  momentum (per worker) -> Newton–Schulz with fused sign packing
               -> majority vote -> W <- W - lr*S_bar
+              (--variant int8: int8 signs, integer sum, threshold; --post-polar:
+              Newton–Schulz on S_bar before the update)
+  Dion:       (--config 6) B = M + G, warm-started power iteration, error feedback,
+              column normalisation, low-rank update
 every stage through the C ABI of libmao.so.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config C] [--impl reference]
+  python bench.py --sweep-hbm      (each HBM-bound kernel alone on L2-cold buffers)
 
 Default workload: the 12-layer d=768 transformer-shaped Muon step (48 bf16 matrices).
 `--impl reference` times the fp64 CPU oracle on the same workload and metric (each
@@ -26,8 +31,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
-DEFAULT_STEPS = {1: 2000, 2: 400, 3: 60, 4: 4, 5: 100}
-DEFAULT_WARMUP = {1: 20, 2: 10, 3: 5, 4: 3, 5: 5}
+DEFAULT_STEPS = {1: 2000, 2: 400, 3: 60, 4: 4, 5: 100, 6: 400}
+DEFAULT_WARMUP = {1: 20, 2: 10, 3: 5, 4: 3, 5: 5, 6: 10}
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
@@ -37,7 +42,7 @@ def parse_args():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=None)
     ap.add_argument("--warmup", type=int, default=None)
-    ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5, 6])
     ap.add_argument("--impl", default="mao", choices=["mao", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="CPU work budget of the oracle baseline sample")
@@ -157,6 +162,13 @@ class Step:
         self.variant, self.post_polar = variant, post_polar
         self.W, self.M, self.G = inputs["W"], inputs["M"], inputs["G"]
         self.dev = device
+        if wl.kind == "dion":
+            # one Dion step per call: the previous right factors Q are updated in place
+            self.Q = inputs["Q"]
+            self.U = []
+            need = mao.dion_workspace_bytes([tuple(w.shape) for w in self.W], wl.rank)
+            self.ws = torch.empty(need, dtype=torch.uint8, device=device)
+            return
         if wl.kind == "sign":
             R, C = self.W[0].shape
             self.nbits = R * C
@@ -180,10 +192,15 @@ class Step:
         self.ws = mao.workspace(self.M, wl.compute, device)
 
     def momentum(self):
+        if self.wl.kind == "dion":  # B = M + G is the first stage of the Dion call
+            return
         self.mao.muon_momentum_update(self.M, self.G, self.wl.mu)
 
     def ns(self):
         wl = self.wl
+        if wl.kind == "dion":
+            self.mao.dion_step(self.W, self.M, self.G, self.Q, wl.mu, wl.lr, ws=self.ws)
+            return
         if wl.kind == "sign" and self.variant == "bits":
             self.mao.ns_orthogonalize(self.M, self.U, wl.steps, wl.coeffs, wl.eps, wl.compute,
                                       sign_bits=self.bits, ws=self.ws)
@@ -196,6 +213,8 @@ class Step:
 
     def update(self):
         wl = self.wl
+        if wl.kind == "dion":  # the updates of M and X are the last stages of the Dion call
+            return
         if wl.kind != "sign":
             self.mao.apply_update(self.W, wl.lr, U=self.U)
             return
@@ -245,9 +264,11 @@ def oracle_sample(wl, host, budget_s, max_items=None, variant="bits", post_polar
     import numpy as np
 
     import oracle
-    shapes = [tuple(x.shape) for x in host["M"]] if wl.kind == "muon" else [tuple(host["W"][0].shape)]
+    shapes = [tuple(x.shape) for x in host["M"]] if wl.kind != "sign" else [tuple(host["W"][0].shape)]
     total = dense_flops(shapes, wl.steps) * (wl.workers + (1 if post_polar else 0)
                                              if wl.kind == "sign" else 1)
+    if wl.kind == "dion":  # work fraction by matrix elements (every element costs 8 r flops)
+        total = sum(r * c for r, c in shapes)
     store = "bf16" if wl.m_dtype.itemsize == 2 else "f32"
     wstore = "bf16" if wl.w_dtype.itemsize == 2 else "f32"
     done_flops, t_used, items = 0, 0.0, 0
@@ -256,7 +277,10 @@ def oracle_sample(wl, host, budget_s, max_items=None, variant="bits", post_polar
     i = 0
     while True:
         t0 = time.perf_counter()
-        if wl.kind == "muon":
+        if wl.kind == "dion":
+            oracle.dion_step(host["W"][i], host["M"][i], host["G"][i], host["Q"][i], wl.mu, wl.lr)
+            done_flops += shapes[i][0] * shapes[i][1]
+        elif wl.kind == "muon":
             oracle.muon_step([host["W"][i]], [host["M"][i]], [host["G"][i]], wl.mu, wl.lr,
                              wl.steps, wl.coeffs, wl.eps, m_store=store)
             done_flops += dense_flops([shapes[i]], wl.steps)
@@ -285,6 +309,8 @@ def oracle_sample(wl, host, budget_s, max_items=None, variant="bits", post_polar
             break
     frac = done_flops / total
     desc = "%d matrix step(s) of the workload (%.3f of one step), fp64 numpy" % (items, frac)
+    if wl.kind == "dion":
+        desc += " (fraction by matrix elements)"
     return frac, t_used, desc
 
 
@@ -361,8 +387,19 @@ def job_throughput(ms_max, steps, world):
 
 
 def metric_name(wl):
+    if wl.kind == "dion":
+        return "Dion steps/s (%s)" % wl.name
     return ("Sign-Muon steps/s" if wl.kind == "sign" else "Muon steps/s") + \
         " (%s); NS TFLOP/s; elementwise GB/s" % wl.name
+
+
+def dion_min_bytes(step):
+    """Bytes a Dion step must move: read X, M, G and Q_prev; write X, M and Q."""
+    tot = 0
+    for x, m, g, q in zip(step.W, step.M, step.G, step.Q):
+        tot += x.numel() * 2 * esize(x.dtype) + m.numel() * 2 * esize(m.dtype)
+        tot += g.numel() * esize(g.dtype) + 2 * q.numel() * 4
+    return tot
 
 
 def config_block(wl, step_bytes, variant="bits", post_polar=False):
@@ -507,7 +544,10 @@ def main():
     mao.sync_status()
 
     # ---------------- timed region: K whole steps, inputs resident in HBM
-    n_tc_per_step = 3 * wl.steps * ((len(set(wl.shapes)) + 7) // 8 + (1 if args.post_polar else 0))
+    if wl.kind == "dion":  # P = B Q, R = B^T P and the two rank-r updates, per shape
+        n_tc_per_step = 4 * ((len(set(wl.shapes)) + 7) // 8)
+    else:
+        n_tc_per_step = 3 * wl.steps * ((len(set(wl.shapes)) + 7) // 8 + (1 if args.post_polar else 0))
     mao.profile_begin(K * n_tc_per_step)
     launches0 = mao.launch_count()
     clocks = ClockSampler(local)
@@ -545,8 +585,14 @@ def main():
     st_ns = statistics.median(e[1].elapsed_time(e[2]) for e in ev)
     st_upd = statistics.median(e[2].elapsed_time(e[3]) for e in ev)
 
-    # ---------------- roofline of the dominant kernel (tensor-core NS product kernel)
     peaks, peak_src = load_peaks()
+    if wl.kind == "dion":
+        line = dion_line(wl, step, K, Wu, world, value, ms_step, ms_total, st_ns, tc_ms,
+                         launches, clk, peaks, peak_src)
+        finish_line(args, line, wl, step, K, world, rank, dev, barrier, max_over_ranks)
+        return
+
+    # ---------------- roofline of the dominant kernel (tensor-core NS product kernel)
     shapes = [tuple(m.shape) for m in step.M]
     alg = alg_flops(shapes, wl.steps)
     dense = dense_flops(shapes, wl.steps)
@@ -595,6 +641,41 @@ def main():
         "clocks": clk,
     }
 
+    finish_line(args, line, wl, step, K, world, rank, dev, barrier, max_over_ranks)
+
+
+def dion_line(wl, step, K, Wu, world, value, ms_step, ms_total, st_step, tc_ms, launches, clk,
+              peaks, peak_src):
+    """Bench line of a Dion workload: the step is HBM-bound (every matrix element is read and
+    written a fixed number of times, 8 m n r flops against about 10 bytes per element)."""
+    hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+    need = dion_min_bytes(step)
+    gbs = need / (st_step / 1000.0) / 1e9
+    flops = sum(8 * w.shape[0] * w.shape[1] * wl.rank for w in step.W)
+    tc_total = sum(tc_ms)
+    roof = {"kernel": "dion_step (all kernels of one call)", "bound": "hbm", "achieved": gbs,
+            "peak": hbm, "unit": "GB/s", "frac": gbs / hbm, "traffic": None,
+            "peak_source": "%s hbm_gbs" % peak_src,
+            "work": "bytes a step must move: X, M, G, Q read; X, M, Q written",
+            "tc_launches": len(tc_ms),
+            "tc_share_of_step": tc_total / ms_total if tc_ms else None,
+            "tc_tflops": flops * K / (tc_total / 1000.0) / 1e12 if tc_ms else None}
+    touched = sum(m.numel() * esize(m.dtype) for m in step.M) * 2 + \
+        sum(w.numel() * esize(w.dtype) for w in step.W) * 2
+    c = config_block(wl, touched)
+    c["rank"] = wl.rank
+    return {
+        "metric": metric_name(wl), "value": value, "unit": "steps/s", "n_gpus": world,
+        "steps": K, "warmup": Wu, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": wl.compute, "data": "synthetic",
+        "config": c, "stages_ms": {"dion_step": st_step}, "roofline": roof,
+        "gpu_launches": launches, "clocks": clk,
+    }
+
+
+def finish_line(args, line, wl, step, K, world, rank, dev, barrier, max_over_ranks):
+    import torch.distributed as dist
+    from matrix_aware_optimizers_gb300 import workloads
     # ---------------- end to end: host gradients in, host weights out, every step
     if not args.no_e2e:
         line["e2e"] = run_e2e(step, K if wl.index != 4 else min(K, 2), world, dev, barrier,

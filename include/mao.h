@@ -262,7 +262,8 @@ mao_status apply_update(const mao_mat* W, const uint32_t* const* vote, const mao
 
 /*
  * One Dion step ([Dion] "대규모 AI 모델 학습을 10배 빠르게: Dion 옵티마이저를 사용한 분산 학습",
- * algorithm section) for `batch` parameter matrices of ONE shape m x n and rank r:
+ * algorithm section) for `batch` parameter matrices of any shapes m x n (grouped by shape
+ * inside the call) and one rank r:
  *
  *   B = M + G;  P = orthonormalise(B Q);  R = B^T P
  *   M <- B - (1 - mu) P R^T;  Q <- ColumnNormalize(R);  X <- X - lr P Q^T
@@ -274,11 +275,12 @@ mao_status apply_update(const mao_mat* W, const uint32_t* const* vote, const mao
  *   Q[b]        in/out, f32, n x r (any ld): the previous right factor in, the new one out.
  *   P_out       NULL, or HOST array of `batch` device pointers (each may be NULL): the
  *               final P, m x r fp32, row stride r.
- *   rank        1..256, at most min(m, n).  compute  MAO_BF16 only: B, Q, P and R enter
+ *   rank        1..256, at most min(m, n) of every matrix; batch <= 65535.
+ *   compute     MAO_BF16 only: B, Q, P and R enter
  *               the three dense products (B Q, B^T P, P R^T / P Q^T) as bf16 with fp32
  *               accumulation on tcgen05 tensor cores; everything else is fp32.
  *   workspace   >= dion_workspace_bytes(X, batch, rank) bytes, 256-byte aligned.
- *   Errors: MAO_ERR_INVALID_ARG for shapes that differ within the batch or a bad rank;
+ *   Errors: MAO_ERR_INVALID_ARG for mismatched shapes of X, M, G, Q or a bad rank;
  *   B Q without full column rank (a non-positive Cholesky pivot) is reported by
  *   mao_sync_status() as MAO_ERR_NUMERIC (the pivot is replaced by 1e-30).
  */

@@ -252,13 +252,14 @@ def apply_update(W, lr, vote=None, U=None, stream=None):
     _abi.check("apply_update", st)
 
 
-def dion_workspace_bytes(shape, rank, count=1):
-    arr = (_abi.MaoMat * count)()
-    for i in range(count):
-        arr[i] = _abi.MaoMat(None, shape[0], shape[1], shape[1], _abi.MAO_F32, 0)
-    n = lib().dion_workspace_bytes(arr, count, int(rank))
+def dion_workspace_bytes(shapes, rank):
+    """Workspace bytes of one dion_step call over matrices of the given (m, n) shapes."""
+    arr = (_abi.MaoMat * len(shapes))()
+    for i, sh in enumerate(shapes):
+        arr[i] = _abi.MaoMat(None, sh[0], sh[1], sh[1], _abi.MAO_F32, 0)
+    n = lib().dion_workspace_bytes(arr, len(shapes), int(rank))
     if n == 0:
-        raise ValueError("invalid shape or rank for dion_workspace_bytes")
+        raise ValueError("invalid shapes or rank for dion_workspace_bytes")
     return int(n)
 
 
@@ -270,30 +271,27 @@ def _q_mat(q):
 
 
 def dion_step(X, M, G, Q, mu, lr, P_out=None, ws=None, stream=None):
-    """One Dion step for each (X, M, G, Q): X, M updated in place, Q replaced by the new right
-    factor (n x r, float32). Matrices are grouped by shape; each group is one C call.
-    P_out: optional float32 tensors (m x r, contiguous) receiving the final P."""
+    """One Dion step for each (X, M, G, Q), any mix of shapes, one rank: X and M updated in
+    place, Q replaced by the new right factor (n x r, float32). P_out: optional float32
+    tensors (m x r, contiguous) receiving the final P."""
     Xs, Ms, Gs, Qs = _as_list(X), _as_list(M), _as_list(G), _as_list(Q)
-    Ps = _as_list(P_out) if P_out is not None else [None] * len(Xs)
-    groups = {}
-    for i, x in enumerate(Xs):
-        groups.setdefault((tuple(x.shape), Qs[i].shape[1]), []).append(i)
-    for (shape, rank), idx in groups.items():
-        need = dion_workspace_bytes(shape, rank, len(idx))
-        w = ws if ws is not None and ws.numel() >= need else \
-            torch.empty(need, dtype=torch.uint8, device=Xs[idx[0]].device)
-        qarr = (_abi.MaoMat * len(idx))()
-        for k, i in enumerate(idx):
-            qarr[k] = _q_mat(Qs[i])
-        parr = None
-        if any(Ps[i] is not None for i in idx):
-            parr = (ctypes.c_void_p * len(idx))(
-                *[Ps[i].data_ptr() if Ps[i] is not None else None for i in idx])
-        st = lib().dion_step(
-            _mats([Xs[i] for i in idx]), _mats([Ms[i] for i in idx]), _mats([Gs[i] for i in idx]),
-            qarr, parr, len(idx), int(rank), float(mu), float(lr), _abi.MAO_BF16,
-            ctypes.c_void_p(w.data_ptr()), w.numel(), _stream(stream))
-        _abi.check("dion_step", st)
+    rank = Qs[0].shape[1]
+    if any(q.shape[1] != rank for q in Qs):
+        raise ValueError("one rank per call")
+    qarr = (_abi.MaoMat * len(Qs))()
+    for k, q in enumerate(Qs):
+        qarr[k] = _q_mat(q)
+    parr = None
+    if P_out is not None:
+        Ps = _as_list(P_out)
+        parr = (ctypes.c_void_p * len(Ps))(*[p.data_ptr() if p is not None else None for p in Ps])
+    if ws is None:
+        ws = torch.empty(dion_workspace_bytes([tuple(x.shape) for x in Xs], rank),
+                         dtype=torch.uint8, device=Xs[0].device)
+    st = lib().dion_step(_mats(Xs), _mats(Ms), _mats(Gs), qarr, parr, len(Xs), int(rank),
+                         float(mu), float(lr), _abi.MAO_BF16, ctypes.c_void_p(ws.data_ptr()),
+                         ws.numel(), _stream(stream))
+    _abi.check("dion_step", st)
 
 
 def sync_status(stream=None):

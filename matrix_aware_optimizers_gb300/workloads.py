@@ -1,6 +1,6 @@
 """Seeded synthetic workloads of the optimizer step (random draws only).
 
-This module holds the five workload definitions (shapes, dtypes, hyper-parameters)
+This module holds the workload definitions (shapes, dtypes, hyper-parameters)
 and draws their inputs. It contains none of the method's arithmetic, so both the
 CUDA path and the fp64 oracle can take their inputs from it.
 
@@ -22,7 +22,7 @@ QUINTIC = (3.4445, -4.7750, 2.0315)
 class Workload:
     index: int
     name: str
-    kind: str                    # "sign" (Sign-Muon over simulated workers) or "muon"
+    kind: str                    # "sign" (Sign-Muon over simulated workers), "muon" or "dion"
     shapes: List[Tuple[int, int]]
     workers: int = 1             # Sign-Muon: simulated workers
     m_dtype: torch.dtype = torch.bfloat16
@@ -38,6 +38,7 @@ class Workload:
     steps: int = 5
     coeffs: Tuple[float, float, float] = QUINTIC
     eps: float = 1e-7
+    rank: int = 0                # Dion: rank r of the low-rank factors
 
     @property
     def elements(self):
@@ -69,6 +70,10 @@ WORKLOADS = {
                 g_std=0.01, m0_std=0.01, w_std=0.02, mu=0.95, lr=0.02),
     5: Workload(5, "muon_moe128_2048x768_bf16", "muon", _moe128(), g_std=0.02, m0_std=0.01,
                 w_std=0.02, expert_scales=True, mu=0.95, lr=0.02),
+    # Dion on the same 12-layer d = 768 shapes with r = d / 4 (the page's rank sweep uses
+    # d / 4, d / 8 and d / 16 at d = 768)
+    6: Workload(6, "dion_gpt12_d768_r192", "dion", _gpt12(), g_std=0.02, m0_std=0.01,
+                w_std=0.02, mu=0.95, lr=0.02, rank=192),
 }
 
 
@@ -86,7 +91,8 @@ def _normal(gen, shape, std, dtype, device):
 
 
 def generate(wl: Workload, device, seed: Optional[int] = None, shapes=None):
-    """Inputs of one step: dict with lists W, M, G (Sign-Muon: one W, W_n of M and G).
+    """Inputs of one step: dict with lists W, M, G (Sign-Muon: one W, W_n of M and G;
+    Dion adds Q, the previous right factors: n x r float32 standard normal draws).
 
     `shapes` replaces the workload's shape list (smaller parity cases of the same recipe).
     """
@@ -113,6 +119,9 @@ def generate(wl: Workload, device, seed: Optional[int] = None, shapes=None):
         W.append(_normal(gen, (R, C), wl.w_std, wl.w_dtype, device))
         M.append(_normal(gen, (R, C), wl.m0_std, wl.m_dtype, device))
         G.append(_normal(gen, (R, C), wl.g_std * sc, wl.g_dtype, device))
+    if wl.kind == "dion":
+        Q = [_normal(gen, (C, wl.rank), 1.0, torch.float32, device) for (R, C) in shapes]
+        return {"W": W, "M": M, "G": G, "Q": Q}
     return {"W": W, "M": M, "G": G}
 
 

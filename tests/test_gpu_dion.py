@@ -78,7 +78,8 @@ def test_dion_bf16_parameters(cuda):
 
 def test_dion_batch_and_mixed_shapes(cuda):
     gen = torch.Generator().manual_seed(82)
-    shapes = [(256, 768, 64), (256, 768, 64), (768, 256, 64), (384, 384, 96), (256, 768, 64)]
+    shapes = [(256, 768, 64), (256, 768, 64), (768, 256, 64), (384, 384, 64), (256, 768, 64),
+              (520, 1000, 64)]
     sets = [_inputs(gen, m, n, r, "bf16", "f32", cuda) for m, n, r in shapes]
     hosts = [[to_np(t) for t in s] for s in sets]
     Ps = [torch.empty((m, r), dtype=torch.float32, device=cuda) for m, n, r in shapes]
