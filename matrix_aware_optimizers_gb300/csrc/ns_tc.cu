@@ -6,6 +6,9 @@
 //   NS_GRAM   A  = alpha * X X^T              (symmetric: upper and diagonal tiles only)
 //   NS_POLY   B' = a I + b A + c A A          (symmetric; A A = A A^T by symmetry)
 //   NS_APPLY  X' = beta * B' X                (X B' in the tall orientation; B' symmetric)
+// and, for the Dion step, plain products into fp32 outputs (the final NS_APPLY
+// instantiation with no scale) and an in-place rank-k update of the caller's matrices:
+//   TC_UPDATE out <- out + a * (A B^T)
 // A symmetric result is stored as its upper and diagonal 256 x 256 tiles. A product that
 // reads it takes each 128-deep k-block below the diagonal from the transposed view of the
 // stored upper block (an MN-major load of the same buffer), so no tile is ever mirrored.
