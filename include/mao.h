@@ -290,6 +290,16 @@ mao_status dion_step(const mao_mat* X, const mao_mat* M, const mao_mat* G, const
                      int32_t compute, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Bound of every device-side wait of the tensor-core kernels (default 4 s), used by launches
+ * enqueued after the call; process-wide. A wait that runs past it makes the kernel stop
+ * early (its outputs are then incomplete) and mao_sync_status() report MAO_ERR_TIMEOUT.
+ * 0 makes every wait that does not complete at once give up: the way to exercise that path
+ * without a GPU fault. mao_get_wait_limit returns the current bound.
+ */
+void mao_set_wait_limit(uint64_t ns);
+uint64_t mao_get_wait_limit(void);
+
+/*
  * Synchronise `stream`, then read and clear the device-side error words that kernels set
  * when a bounded wait gives up or a factorisation meets a non-positive pivot. Returns
  * MAO_OK, MAO_ERR_TIMEOUT, MAO_ERR_NUMERIC or MAO_ERR_CUDA.

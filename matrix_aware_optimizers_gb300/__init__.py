@@ -294,6 +294,15 @@ def dion_step(X, M, G, Q, mu, lr, P_out=None, ws=None, stream=None):
     _abi.check("dion_step", st)
 
 
+def set_wait_limit(ns):
+    """Bound (ns) of every device-side wait of the tensor-core kernels; 0 gives up at once."""
+    lib().mao_set_wait_limit(int(ns))
+
+
+def get_wait_limit():
+    return int(lib().mao_get_wait_limit())
+
+
 def sync_status(stream=None):
     st = lib().mao_sync_status(_stream(stream))
     _abi.check("mao_sync_status", st)

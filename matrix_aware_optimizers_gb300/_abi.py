@@ -39,6 +39,8 @@ EXPORTS = (
     "apply_update",
     "dion_workspace_bytes",
     "dion_step",
+    "mao_set_wait_limit",
+    "mao_get_wait_limit",
     "mao_sync_status",
     "mao_launch_count",
     "mao_profile_begin",
@@ -125,6 +127,10 @@ def load():
     lib.dion_step.argtypes = [P(MaoMat), P(MaoMat), P(MaoMat), P(MaoMat), P(ctypes.c_void_p),
                               ctypes.c_int32, ctypes.c_int32, ctypes.c_float, ctypes.c_float,
                               ctypes.c_int32, vp, ctypes.c_size_t, vp]
+    lib.mao_set_wait_limit.restype = None
+    lib.mao_set_wait_limit.argtypes = [ctypes.c_uint64]
+    lib.mao_get_wait_limit.restype = ctypes.c_uint64
+    lib.mao_get_wait_limit.argtypes = []
     lib.mao_sync_status.restype = ctypes.c_int
     lib.mao_sync_status.argtypes = [vp]
     lib.mao_launch_count.restype = ctypes.c_int64

@@ -60,6 +60,12 @@ Profile g_prof;
 
 void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
+namespace {
+std::atomic<unsigned long long> g_wait_limit{4000000000ull};  // 4 s
+}  // namespace
+
+unsigned long long wait_limit_ns() { return g_wait_limit.load(std::memory_order_relaxed); }
+
 void profile_before_launch(cudaStream_t stream) {
   if (g_prof.on && g_prof.used < g_prof.cap) cudaEventRecord(g_prof.ev[2 * g_prof.used], stream);
 }
@@ -195,6 +201,10 @@ mao_status apply_update(const mao_mat* W, const uint32_t* const* vote, const mao
   }
   return update_launch(W, vote, U, batch, lr, static_cast<cudaStream_t>(stream));
 }
+
+void mao_set_wait_limit(uint64_t ns) { g_wait_limit.store(ns, std::memory_order_relaxed); }
+
+uint64_t mao_get_wait_limit(void) { return g_wait_limit.load(std::memory_order_relaxed); }
 
 mao_status mao_sync_status(void* stream) {
   const mao_status a = tc_read_and_clear_error(static_cast<cudaStream_t>(stream));

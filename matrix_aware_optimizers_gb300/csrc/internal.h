@@ -26,6 +26,9 @@ mao_status ns_run(const mao_mat* in, const mao_mat* out, int32_t batch, int32_t 
                   uint32_t* const* sign_bits, void* workspace, size_t workspace_bytes,
                   cudaStream_t stream);
 
+// Bound of every device-side wait in the tensor-core kernels (mao_set_wait_limit).
+unsigned long long wait_limit_ns();
+
 // Launch accounting (every kernel launch of the library calls this once).
 void count_launch();
 // Optional timing of the tensor-core product launches (see mao_profile_begin).

@@ -375,7 +375,7 @@ mao_status run_tc_stage(const Buffers& buf, const std::vector<const NsGroupPlan*
   p.c = co[2];
   p.scale = first ? scale : nullptr;
   p.out_table = table;
-  p.timeout_ns = 4000000000ull;
+  p.timeout_ns = wait_limit_ns();
   int tiles = 0;
   for (size_t gi = 0; gi < round.size(); ++gi) {
     const NsGroupPlan& g = *round[gi];

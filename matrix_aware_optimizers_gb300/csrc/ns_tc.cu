@@ -34,8 +34,10 @@
 //                bulk tensor stores
 // Barriers: full[s] (even CTA; both CTAs' loads complete on it), empty[s] (both CTAs),
 // tfull[a] (both), tempty[a] (even CTA; the pair's eight epilogue warps arrive on it).
-// Every wait is bounded by %globaltimer: a wait that gives up sets the device error word
-// and the CTA's abort flag; the CTA lets in-flight products land, frees TMEM and returns.
+// Every wait is bounded by %globaltimer (the limit is a launch parameter): a wait that
+// gives up sets the device error word and the CTA's abort flag; the CTA then lets its
+// in-flight loads (bounded waits on the armed stages), products (a drain commit) and stores
+// land, frees TMEM and returns.
 #include <cudaTypedefs.h>
 
 #include <mutex>
@@ -131,14 +133,35 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
   return ok != 0;
 }
 
+// Non-blocking test of the same phase (no suspension inside the instruction).
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.b32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Waits for the phase of `parity` to complete. Gives up after `limit_ns` or when another
-// role raised the CTA's abort flag; a timeout sets the abort flag and the error word.
+// role raised the CTA's abort flag; a timeout sets the abort flag and the error word. A
+// limit of 0 gives up at once unless a non-blocking test finds the phase complete (each
+// try_wait may suspend the thread for a while, so polling alone could always succeed).
 template <bool CLUSTER = false>
 __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                        uint64_t limit_ns) {
   auto test = [&]() {
     return CLUSTER ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
   };
+  if (limit_ns == 0) {
+    if (mbar_test_wait(bar, parity)) return true;
+    *abort_flag = 1;
+    atomicOr(&g_tc_error, 1u);
+    return false;
+  }
   if (test()) return true;
   const uint64_t t0 = globaltimer();
   while (true) {
@@ -548,6 +571,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads(FINAL), 1)
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
+    uint32_t armed = 0, armed_phase = 0;  // leader: stages armed at least once, their phase
     for (int tile = pair; ok && tile < p.total_tiles; tile += npairs) {
       Tile t;
       decode_tile(p, tile, t);
@@ -568,8 +592,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads(FINAL), 1)
 #ifdef MAO_TC_TRACE
           const long long tw = clock64();
 #endif
-          if (!mbar_wait(smem_u32(&empty_bar[stage]), phase ^ 1u, abort_flag, limit)) okw = 0;
-          else if (leader) mbar_expect_tx(smem_u32(&full_bar[stage]), 2u * STAGE_BYTES);
+          if (!mbar_wait(smem_u32(&empty_bar[stage]), phase ^ 1u, abort_flag, limit)) {
+            okw = 0;
+          } else if (leader) {
+            mbar_expect_tx(smem_u32(&full_bar[stage]), 2u * STAGE_BYTES);
+            armed |= 1u << stage;
+            armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
+          }
 #ifdef MAO_TC_TRACE
           if (leader) TRACE_ADD(0, tw);
 #endif
@@ -593,6 +622,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads(FINAL), 1)
           phase ^= 1u;
         }
       }
+    }
+    // after an abort, the loads already issued land before the CTA leaves: the leader's full
+    // barriers count both CTAs' bytes of every armed stage (bounded waits)
+    if (*abort_flag && leader && lane == 0) {
+      for (int s = 0; s < STAGES; ++s)
+        if ((armed >> s) & 1u) mbar_drain(smem_u32(&full_bar[s]), (armed_phase >> s) & 1u, 20000000ull);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -787,6 +822,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads(FINAL), 1)
 #ifdef MAO_TC_TRACE
   if (threadIdx.x == 0 && leader) TRACE_ADD(7, t_cta);
 #endif
+  if (*abort_flag) {  // an aborted CTA also gives the peer's copies in flight 50 us to land
+    const uint64_t t0 = globaltimer();
+    while (globaltimer() - t0 < 50000ull) {
+    }
+  }
   cluster_sync_all();  // no CTA leaves while its peer may still touch its shared memory
   tc_fence_after();
   if (warp == 1) {

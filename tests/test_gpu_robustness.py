@@ -1,0 +1,110 @@
+"""Robustness checks on the GPU: poisoned workspaces, tiny odd shapes, a forced time-out.
+
+* Poisoned workspace: every byte of the workspace set to 0xFF (NaN patterns in fp32 and
+  bf16) before a call must give bit-identical results to a zero-filled workspace, so no
+  product reads a workspace region that the call did not write first.
+* Tiny odd shapes (1x1, 1x33, 33x1, 31x7, 127x129) against the oracle.
+* Forced time-out: with the wait limit at 0, a tensor-core launch gives up at its first wait
+  that does not complete at once; mao_sync_status reports MAO_ERR_TIMEOUT, the error word
+  is cleared, and the next call (limit restored) is correct. No trap, no fault, no hang:
+  every wait in the kernel is bounded and the aborted CTAs drain their copies and products.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import matrix_aware_optimizers_gb300 as mao
+import oracle
+from helpers import rand_matrix, rel_fro, to_np
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"f32": 1e-4, "bf16": 2e-2}
+
+
+def _ws(nbytes, fill, device):
+    return torch.full((nbytes,), fill, dtype=torch.uint8, device=device)
+
+
+@pytest.mark.parametrize("compute", ["bf16", "f32"])
+def test_poisoned_workspace_newton_schulz(cuda, compute):
+    gen = torch.Generator().manual_seed(90)
+    Xs = [rand_matrix(gen, s, torch.bfloat16, cuda) for s in [(300, 700), (700, 300), (64, 64)]]
+    need = mao.ns_workspace_bytes(Xs, compute)
+    outs = []
+    for fill in (0x00, 0xFF):
+        U = [torch.empty(x.shape, dtype=torch.float32, device=cuda) for x in Xs]
+        mao.ns_orthogonalize(Xs, U, 5, mao.QUINTIC, 1e-7, compute, ws=_ws(need, fill, cuda))
+        mao.sync_status()
+        outs.append(U)
+    for a, b in zip(*outs):
+        assert torch.equal(a, b)
+        assert torch.isfinite(a).all()
+
+
+def test_poisoned_workspace_blockwise_and_signs(cuda):
+    gen = torch.Generator().manual_seed(91)
+    X = rand_matrix(gen, (320, 1000), torch.bfloat16, cuda)
+    need = mao.ns_blockwise_workspace_bytes([X], (128, 256), "bf16")
+    res = []
+    for fill in (0x00, 0xFF):
+        U = torch.empty(X.shape, dtype=torch.float32, device=cuda)
+        mao.ns_orthogonalize_blockwise(X, U, (128, 256), ws=_ws(need, fill, cuda))
+        bits = torch.zeros(mao.packed_words(*X.shape), dtype=torch.int32, device=cuda)
+        ws2 = _ws(mao.ns_workspace_bytes([X], "bf16"), fill, cuda)
+        mao.ns_orthogonalize(X, None, sign_bits=bits, ws=ws2)
+        mao.sync_status()
+        res.append((U, bits))
+    assert torch.equal(res[0][0], res[1][0]) and torch.equal(res[0][1], res[1][1])
+
+
+def test_poisoned_workspace_dion(cuda):
+    gen = torch.Generator().manual_seed(92)
+    shapes = [(256, 640), (640, 256)]
+    base = [(torch.randn(s, generator=gen).to(cuda), torch.randn(s, generator=gen).to(cuda),
+             torch.randn(s, generator=gen).to(cuda), torch.randn((s[1], 32), generator=gen).to(cuda))
+            for s in shapes]
+    need = mao.dion_workspace_bytes(shapes, 32)
+    res = []
+    for fill in (0x00, 0xFF):
+        X = [b[0].clone() for b in base]
+        M = [b[1].clone() for b in base]
+        Q = [b[3].clone() for b in base]
+        mao.dion_step(X, M, [b[2] for b in base], Q, 0.9, 0.1, ws=_ws(need, fill, cuda))
+        mao.sync_status()
+        res.append(X + M + Q)
+    for a, b in zip(*res):
+        assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("shape", [(1, 1), (1, 33), (33, 1), (31, 7), (127, 129)])
+@pytest.mark.parametrize("compute", ["f32", "bf16"])
+def test_tiny_odd_shapes(cuda, shape, compute):
+    if compute == "bf16" and min(shape) == 7:
+        pytest.skip("short side below 64 on the bf16 path: checked on fp32 (accuracy note)")
+    gen = torch.Generator().manual_seed(93)
+    X = rand_matrix(gen, shape, torch.float32, cuda)
+    U = torch.empty(shape, dtype=torch.float32, device=cuda)
+    mao.ns_orthogonalize(X, U, 5, mao.QUINTIC, 1e-7, compute)
+    mao.sync_status()
+    assert rel_fro(to_np(U), oracle.newton_schulz(to_np(X), 5, oracle.QUINTIC)) <= TOL[compute]
+
+
+def test_forced_timeout_is_reported_and_recovers(cuda):
+    gen = torch.Generator().manual_seed(94)
+    X = rand_matrix(gen, (512, 1024), torch.bfloat16, cuda)
+    U = torch.empty(X.shape, dtype=torch.float32, device=cuda)
+    old = mao.get_wait_limit()
+    try:
+        mao.set_wait_limit(0)
+        mao.ns_orthogonalize(X, U, 5, mao.QUINTIC, 1e-7, "bf16")
+        with pytest.raises(mao.MaoError) as err:
+            mao.sync_status()
+        assert err.value.status == 6  # MAO_ERR_TIMEOUT
+    finally:
+        mao.set_wait_limit(old)
+    mao.sync_status()  # the error word was cleared by the first read
+    mao.ns_orthogonalize(X, U, 5, mao.QUINTIC, 1e-7, "bf16")
+    mao.sync_status()
+    assert rel_fro(to_np(U), oracle.newton_schulz(to_np(X), 5, oracle.QUINTIC)) <= TOL["bf16"]
