@@ -561,6 +561,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads(FINAL), 1)
   cluster_sync_all();  // both CTAs' barriers exist before any cross-CTA arrival
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
+  // Launched as a programmatic dependent of the previous kernel in the stream: the set-up
+  // above may overlap that kernel's last CTAs; nothing below runs before it has completed
+  // and its memory is visible. The next launch may start its own set-up from here on.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const uint64_t limit = p.timeout_ns;
 #ifdef MAO_TC_TRACE
   const long long t_cta = clock64();
@@ -912,11 +917,21 @@ mao_status tc_gemm_launch(const TcParams& p, cudaStream_t stream) {
     return MAO_ERR_INVALID_ARG;
   const Kernel k = p.stage == TC_UPDATE ? kernels[4] : kernels[final_out ? 3 : p.stage - NS_GRAM];
   const int pairs = p.total_tiles < num_sms() / 2 ? p.total_tiles : num_sms() / 2;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(2 * pairs));
+  cfg.blockDim = dim3(unsigned(threads(final_out)));
+  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   profile_before_launch(stream);
-  k<<<2 * pairs, threads(final_out), SMEM_BYTES, stream>>>(p);
+  const cudaError_t err = cudaLaunchKernelEx(&cfg, k, p);
   count_launch();
   profile_after_launch(stream);
-  return cuda_status(cudaGetLastError());
+  return err == cudaSuccess ? cuda_status(cudaGetLastError()) : MAO_ERR_CUDA;
 }
 
 #ifdef MAO_TC_TRACE
