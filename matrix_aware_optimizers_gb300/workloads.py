@@ -10,7 +10,6 @@ workload index minus one unless a seed is given; normal draws in fp32, then cast
 """
 
 import dataclasses
-import math
 from typing import List, Optional, Tuple
 
 import torch
@@ -123,27 +122,3 @@ def generate(wl: Workload, device, seed: Optional[int] = None, shapes=None):
         Q = [_normal(gen, (C, wl.rank), 1.0, torch.float32, device) for (R, C) in shapes]
         return {"W": W, "M": M, "G": G, "Q": Q}
     return {"W": W, "M": M, "G": G}
-
-
-def ns_dense_flops(shapes, steps):
-    """(4 m^2 n + 2 m^3) per iteration and matrix, m = min(R, C), n = max(R, C)."""
-    tot = 0
-    for R, C in shapes:
-        m, n = min(R, C), max(R, C)
-        tot += steps * (4 * m * m * n + 2 * m ** 3)
-    return tot
-
-
-def ns_executed_flops(shapes, steps, bm=128, bn=256):
-    """Tensor-core flops the tiled schedule issues (upper-triangle tiles for the first two
-    products, including the full diagonal tiles and the ragged column tiles)."""
-    tot = 0
-    for R, C in shapes:
-        m, n = min(R, C), max(R, C)
-        syrk_area = 0
-        for ib in range(math.ceil(m / bm)):
-            cols = m - bm * ib
-            rows = min(bm, m - bm * ib)
-            syrk_area += rows * cols
-        tot += steps * (2 * syrk_area * n + 2 * syrk_area * m + 2 * m * m * n)
-    return tot
