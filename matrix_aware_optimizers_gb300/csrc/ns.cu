@@ -365,9 +365,11 @@ int syrk_tiles(int64_t m) {
 
 mao_status run_tc_stage(const Buffers& buf, const std::vector<const NsGroupPlan*>& round,
                         int stage, int cur, bool first, bool last, const float* co,
-                        const float* scale, const OutEntry* table, cudaStream_t stream) {
+                        const float* scale, const OutEntry* table, int out_mode,
+                        cudaStream_t stream) {
   TcParams p;
   memset(&p, 0, sizeof(p));
+  p.out_mode = last ? out_mode : tc::OUT_WORKSPACE;
   p.ngroups = int32_t(round.size());
   p.stage = stage;
   p.a = co[0];
@@ -631,13 +633,22 @@ mao_status ns_run(const mao_mat* in, const mao_mat* out, int32_t batch, int32_t 
     std::vector<const NsGroupPlan*> round;
     for (size_t g = g0; g < plan.groups.size() && round.size() < size_t(max_groups); ++g)
       round.push_back(&plan.groups[g]);
+    // the last product writes every U of the round as bf16 rows with 16-byte stores when
+    // all of them allow it and none asks for signs
+    int out_mode = tc::OUT_CALLER_BF16;
+    for (const NsGroupPlan* g : round)
+      for (int k = 0; k < g->count; ++k) {
+        const OutEntry& e = entries[plan.input_of[g->slot0 + k]];
+        if (!e.out || e.bits || e.dtype != MAO_BF16 || !(e.flags & OUT_VEC)) out_mode = tc::OUT_CALLER;
+      }
     for (int it = 0; it < steps; ++it) {
       const float* co = coeffs + (coeff_stride ? 3 * it : 0);
       const int cur = it & 1;
       const bool first = it == 0, last = it == steps - 1;
       for (int stage = NS_GRAM; stage <= NS_APPLY; ++stage) {
         const mao_status st =
-            tcpath ? run_tc_stage(buf, round, stage, cur, first, last, co, scale, table, stream)
+            tcpath ? run_tc_stage(buf, round, stage, cur, first, last, co, scale, table, out_mode,
+                                  stream)
                    : run_simt_stage(buf, round, stage, cur, first, last, co, scale, table, stream);
         if (st != MAO_OK) return st;
       }

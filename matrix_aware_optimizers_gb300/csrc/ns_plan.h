@@ -65,15 +65,17 @@ constexpr int STAGES = MAO_TC_STAGES;
 constexpr int CHUNK_BYTES = HALF * CHUNK * 2;     // 16 KB
 constexpr int HALF_BYTES = 2 * CHUNK_BYTES;       // 32 KB
 constexpr int STAGE_BYTES = 2 * HALF_BYTES;       // A half + B half
-// Epilogue warps: the products that write the workspace use two warps per 32-lane TMEM
-// quadrant (eight), each taking every other 64-column block of the tile, with one staging
-// buffer each; the last product, which writes the caller's outputs, uses one warp per
-// quadrant (four) with two staging buffers each. Both layouts stage 32 KB.
-constexpr int EPI_WARPS_WS = 8;
-constexpr int EPI_WARPS_FINAL = 4;
-constexpr int epi_warps(bool final_out) { return final_out ? EPI_WARPS_FINAL : EPI_WARPS_WS; }
+// Output modes of a launch: the workspace (bulk tensor stores), the caller's outputs in any
+// form (U in fp32 or bf16 with any row stride, packed signs, in-place updates), or the
+// caller's bf16 U with 16-byte aligned rows and no signs.
+enum OutMode : int { OUT_WORKSPACE = 0, OUT_CALLER = 1, OUT_CALLER_BF16 = 2 };
+// Epilogue warps: two per 32-lane TMEM quadrant (eight), each taking every other 64-column
+// block of the tile, with one staging buffer each; OUT_CALLER uses one warp per quadrant
+// (four) with two staging buffers each (its general output code needs more registers).
+// Both layouts stage 32 KB.
+constexpr int epi_warps(int mode) { return mode == OUT_CALLER ? 4 : 8; }
 // warp 0 TMA, warp 1 MMA, then the epilogue warps
-constexpr int threads(bool final_out) { return 64 + 32 * epi_warps(final_out); }
+constexpr int threads(int mode) { return 64 + 32 * epi_warps(mode); }
 constexpr int TMEM_COLS = 512;   // two 256-column fp32 accumulators
 // Epilogue staging: 32 x 64 bf16 row-major blocks (128-byte rows, 16-byte chunks XOR-
 // swizzled by row).
@@ -113,6 +115,7 @@ struct TcGroup {
 struct TcParams {
   TcGroup g[tc::MAX_GROUPS];
   int32_t ngroups, total_tiles, stage;
+  int32_t out_mode;              // final launches: OUT_CALLER or OUT_CALLER_BF16
   float a, b, c;                 // this iteration's coefficients
   const float* scale;            // first iteration: per-slot 1/(||X||_F + eps); else null
   const OutEntry* out_table;     // per-slot final outputs

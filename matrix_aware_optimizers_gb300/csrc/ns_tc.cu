@@ -24,16 +24,19 @@
 // M=256, N=256, K=16 products that read both halves; each CTA's TMEM receives its 128
 // output rows (two 256-column fp32 accumulators, double-buffered).
 //
-// Roles per CTA (192 threads):
+// Roles per CTA (320 threads; 192 in the instantiations that write the caller's outputs):
 //   warp 0       TMA producer: lane 0 waits for a free stage (and in the even CTA arms the
 //                pair's full barrier); lanes 0 and 1 then issue the A and B boxes
 //   warp 1       TMEM allocation (both CTAs); in the even CTA one thread issues tcgen05.mma
 //                and multicasts tcgen05.commit to both CTAs' barriers
-//   warps 2..5   epilogue: tcgen05.ld of their 32-lane quadrant, fp32 arithmetic, then
-//                32 x 64 blocks staged in shared memory (128-byte swizzle) and written by
-//                bulk tensor stores
+//   warps 2..9   epilogue: tcgen05.ld of their 32-lane quadrant (two warps per quadrant,
+//                alternate 64-column blocks), fp32 arithmetic, then 32 x 64 blocks staged in
+//                shared memory (128-byte swizzle) and written by bulk tensor stores; the
+//                caller-output instantiations use warps 2..5, one per quadrant
 // Barriers: full[s] (even CTA; both CTAs' loads complete on it), empty[s] (both CTAs),
-// tfull[a] (both), tempty[a] (even CTA; the pair's eight epilogue warps arrive on it).
+// tfull[a] (both), tempty[a] (even CTA; every epilogue warp of the pair arrives on it).
+// The kernel is launched as a programmatic dependent of the previous kernel in the stream:
+// its set-up (barriers, TMEM) overlaps that kernel's tail.
 // Every wait is bounded by %globaltimer (the limit is a launch parameter): a wait that
 // gives up sets the device error word and the CTA's abort flag; the CTA then lets its
 // in-flight loads (bounded waits on the armed stages), products (a drain commit) and stores
@@ -505,13 +508,14 @@ __device__ __forceinline__ void update_final(const OutEntry& e, int i0, int jb, 
 
 // ------------------------------------------------------------------ the kernel
 
-// STAGE selects the epilogue (NS_GRAM, NS_POLY, NS_APPLY); FINAL (NS_APPLY only) writes
-// the caller's outputs instead of the workspace. Each instantiation holds only its own
-// epilogue code.
-template <int STAGE, bool FINAL>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads(FINAL), 1)
+// STAGE selects the epilogue (NS_GRAM, NS_POLY, NS_APPLY, TC_UPDATE); MODE the output
+// (OutMode: workspace, the caller's outputs, or the caller's bf16 U). Each instantiation
+// holds only its own epilogue code.
+template <int STAGE, int MODE>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads(MODE), 1)
     ns_tc_kernel(const __grid_constant__ TcParams p) {
-  constexpr int NEPI = epi_warps(FINAL);  // epilogue warps
+  constexpr bool FINAL = MODE != OUT_WORKSPACE;
+  constexpr int NEPI = epi_warps(MODE);   // epilogue warps
   constexpr int SPLIT = NEPI / 4;         // epilogue warps per TMEM quadrant
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -716,7 +720,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads(FINAL), 1)
     // ------------------------------------------------------------ epilogue (both CTAs)
     const int quad = warp & 3;              // TMEM lanes 32*quad .. 32*quad+31 = this warp's rows
     const int part = (warp - 2) / 4;        // which of the quadrant's SPLIT warps
-    // staging: FINAL, four warps with two buffers each; otherwise eight warps with one
+    // staging: OUT_CALLER, four warps with two buffers each; otherwise eight warps with one
     uint8_t* buf[2] = {staging + (warp - 2) * (2 / SPLIT) * EP_BYTES,
                        staging + ((warp - 2) * (2 / SPLIT) + (SPLIT == 1 ? 1 : 0)) * EP_BYTES};
     const uint32_t tempty_leader[2] = {mapa_shared(smem_u32(&tempty_bar[0]), 0),
@@ -790,6 +794,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads(FINAL), 1)
         }
         if (STAGE == TC_UPDATE) {
           update_final(oe, i0, jb, G.M, G.N, lane, w, p.a);
+        } else if (MODE == OUT_CALLER_BF16) {
+          stage_rows(S, lane, w);
+          __syncwarp();
+          store_rows(S, reinterpret_cast<__nv_bfloat16*>(oe.out), oe.ld, i0, jb, G.M, G.N, lane);
+          __syncwarp();
         } else if (FINAL) {
           store_final(oe, S, i0, jb, G.M, G.N, G.orig_cols, lane, w);
         } else {
@@ -895,9 +904,10 @@ mao_status tc_encode_store_map(CUtensorMap* map, const void* base, int64_t rows,
 mao_status tc_gemm_launch(const TcParams& p, cudaStream_t stream) {
   if (p.total_tiles <= 0) return MAO_OK;
   using Kernel = void (*)(TcParams);
-  const Kernel kernels[5] = {ns_tc_kernel<NS_GRAM, false>, ns_tc_kernel<NS_POLY, false>,
-                             ns_tc_kernel<NS_APPLY, false>, ns_tc_kernel<NS_APPLY, true>,
-                             ns_tc_kernel<TC_UPDATE, true>};
+  const Kernel kernels[6] = {
+      ns_tc_kernel<NS_GRAM, OUT_WORKSPACE>, ns_tc_kernel<NS_POLY, OUT_WORKSPACE>,
+      ns_tc_kernel<NS_APPLY, OUT_WORKSPACE>, ns_tc_kernel<NS_APPLY, OUT_CALLER>,
+      ns_tc_kernel<TC_UPDATE, OUT_CALLER>,   ns_tc_kernel<NS_APPLY, OUT_CALLER_BF16>};
   static std::once_flag attr_once[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return MAO_ERR_CUDA;
@@ -915,11 +925,16 @@ mao_status tc_gemm_launch(const TcParams& p, cudaStream_t stream) {
   const bool final_out = p.g[0].final_out != 0 || p.stage == TC_UPDATE;
   if (p.stage < NS_GRAM || p.stage > TC_UPDATE || (final_out && p.stage < NS_APPLY))
     return MAO_ERR_INVALID_ARG;
-  const Kernel k = p.stage == TC_UPDATE ? kernels[4] : kernels[final_out ? 3 : p.stage - NS_GRAM];
+  const int mode = !final_out ? OUT_WORKSPACE
+                   : (p.stage == NS_APPLY && p.out_mode == OUT_CALLER_BF16 ? OUT_CALLER_BF16
+                                                                           : OUT_CALLER);
+  const Kernel k = p.stage == TC_UPDATE  ? kernels[4]
+                   : mode == OUT_CALLER_BF16 ? kernels[5]
+                   : kernels[final_out ? 3 : p.stage - NS_GRAM];
   const int pairs = p.total_tiles < num_sms() / 2 ? p.total_tiles : num_sms() / 2;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(unsigned(2 * pairs));
-  cfg.blockDim = dim3(unsigned(threads(final_out)));
+  cfg.blockDim = dim3(unsigned(threads(mode)));
   cfg.dynamicSmemBytes = SMEM_BYTES;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
