@@ -321,8 +321,8 @@ __device__ __forceinline__ void decode_tile(const TcParams& p, int tile, Tile& t
 
 // ------------------------------------------------------------------ epilogue
 //
-// Each epilogue warp owns 32 output rows i0..i0+31 (lane = row) and walks its tile's
-// columns in blocks of 64. A block's values pass through a per-warp staging buffer:
+// Each epilogue warp owns 32 output rows i0..i0+31 (lane = row) and walks its share of the
+// tile's columns in blocks of 64. A block's values pass through a per-warp staging buffer:
 //   32 rows of 128 bytes; 16-byte chunk k of row r sits at chunk position k ^ (r & 7) (the
 //   128-byte swizzle of the output's bulk-store map), so row-wise and column-wise accesses
 //   of the warp hit distinct banks
@@ -907,7 +907,7 @@ mao_status tc_gemm_launch(const TcParams& p, cudaStream_t stream) {
   const Kernel kernels[6] = {
       ns_tc_kernel<NS_GRAM, OUT_WORKSPACE>, ns_tc_kernel<NS_POLY, OUT_WORKSPACE>,
       ns_tc_kernel<NS_APPLY, OUT_WORKSPACE>, ns_tc_kernel<NS_APPLY, OUT_CALLER>,
-      ns_tc_kernel<TC_UPDATE, OUT_CALLER>,   ns_tc_kernel<NS_APPLY, OUT_CALLER_BF16>};
+      ns_tc_kernel<TC_UPDATE, OUT_CALLER_BF16>, ns_tc_kernel<NS_APPLY, OUT_CALLER_BF16>};
   static std::once_flag attr_once[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return MAO_ERR_CUDA;
@@ -925,9 +925,12 @@ mao_status tc_gemm_launch(const TcParams& p, cudaStream_t stream) {
   const bool final_out = p.g[0].final_out != 0 || p.stage == TC_UPDATE;
   if (p.stage < NS_GRAM || p.stage > TC_UPDATE || (final_out && p.stage < NS_APPLY))
     return MAO_ERR_INVALID_ARG;
+  // the rank-k update writes through its own per-lane path: eight epilogue warps
   const int mode = !final_out ? OUT_WORKSPACE
-                   : (p.stage == NS_APPLY && p.out_mode == OUT_CALLER_BF16 ? OUT_CALLER_BF16
-                                                                           : OUT_CALLER);
+                   : p.stage == TC_UPDATE ||
+                           (p.stage == NS_APPLY && p.out_mode == OUT_CALLER_BF16)
+                       ? OUT_CALLER_BF16
+                       : OUT_CALLER;
   const Kernel k = p.stage == TC_UPDATE  ? kernels[4]
                    : mode == OUT_CALLER_BF16 ? kernels[5]
                    : kernels[final_out ? 3 : p.stage - NS_GRAM];
