@@ -224,7 +224,7 @@ __device__ __forceinline__ float* blk(float* A, int I, int J) {
 // A pivot that is not positive sets the device error word and is replaced by 1e-30 (P had
 // dependent columns). Rows and columns past r are the identity. L goes to global memory
 // (row-major, zeros above the diagonal) and D_J to e.D.
-__global__ void __launch_bounds__(kCholThreads) dion_chol_kernel(const __grid_constant__ DionCommon c) {
+__global__ void __launch_bounds__(kCholThreads, 1) dion_chol_kernel(const __grid_constant__ DionCommon c) {
   extern __shared__ float sm[];
   const DionSlot& e = c.slots[blockIdx.x];
   const int r = c.r;
@@ -254,32 +254,26 @@ __global__ void __launch_bounds__(kCholThreads) dion_chol_kernel(const __grid_co
   for (int J = 0; J < nb; ++J) {
     if (warp == 0) {
       float* Ad = blk(A, J, J);
-      // lane i holds row i of the diagonal block; right-looking steps on unscaled columns,
-      // column j of other rows fetched by shuffles
-      float a[32], pv[32];
-#pragma unroll
-      for (int k = 0; k < 32; ++k) a[k] = k <= lane ? Ad[lane * 33 + k] : 0.0f;
-#pragma unroll
+      // right-looking steps on unscaled columns: at step j, lane k > j updates its column k
+      // below the diagonal, A_ik -= A_ij A_kj / A_jj for i >= k (column j is only read)
       for (int j = 0; j < 32; ++j) {
-        float pj = __shfl_sync(0xFFFFFFFFu, a[j], j);
+        float pj = Ad[j * 33 + j];
         if (!(pj > 0.0f)) {
           if (lane == 0) atomicOr(&g_dion_error, 1u);
           pj = 1e-30f;
         }
-        pv[j] = pj;
-        const float aij = lane > j ? a[j] / pj : 0.0f;
-#pragma unroll
-        for (int k = j + 1; k < 32; ++k) {
-          const float akj = __shfl_sync(0xFFFFFFFFu, a[j], k);
-          if (lane >= k) a[k] = __fmaf_rn(-aij, akj, a[k]);
+        if (lane > j) {
+          const float akj = Ad[lane * 33 + j] / pj;
+          for (int i = lane; i < 32; ++i) Ad[i * 33 + lane] = __fmaf_rn(-Ad[i * 33 + j], akj, Ad[i * 33 + lane]);
         }
+        __syncwarp();
+        if (lane == j) Ad[j * 33 + j] = pj;  // the sanitised pivot, kept for the scaling
+        __syncwarp();
       }
-      // L_ik = A_ik / sqrt(pivot_k) for k < i, L_ii = sqrt(pivot_i)
-#pragma unroll
-      for (int k = 0; k < 32; ++k) {
-        if (k < lane) Ad[lane * 33 + k] = a[k] * rsqrtf(pv[k]);
-        if (k == lane) Ad[lane * 33 + k] = sqrtf(pv[k]);
-      }
+      // L_ik = A_ik / sqrt(pivot_k) for k < i (lane = row), then L_ii = sqrt(pivot_i)
+      for (int k = 0; k < lane; ++k) Ad[lane * 33 + k] *= rsqrtf(Ad[k * 33 + k]);
+      __syncwarp();
+      Ad[lane * 33 + lane] = sqrtf(Ad[lane * 33 + lane]);
       __syncwarp();
       // D_J = L_JJ^-1, lane = column
       float x[32];
