@@ -53,6 +53,9 @@ def parse_args():
     ap.add_argument("--sweep-hbm", action="store_true",
                     help="time each HBM-bound kernel alone on L2-cold buffers of 256 MB-4 GB "
                          "and print one JSON line per kernel and size")
+    ap.add_argument("--graph", action="store_true",
+                    help="time replays of one captured CUDA graph of the step (the library's "
+                         "calls are capture-safe)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
@@ -542,6 +545,20 @@ def main():
     for _ in range(Wu):
         step()
     mao.sync_status()
+    run = step
+    if args.graph:  # one captured step, replayed (no host launch work per step)
+        graph = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        captured0 = mao.launch_count()
+        with torch.cuda.graph(graph, stream=side):
+            step()
+        torch.cuda.synchronize()
+        per_replay = mao.launch_count() - captured0  # kernels of the library in one replay
+        run = graph.replay
+        for _ in range(Wu):
+            run()
+        mao.sync_status()
 
     # ---------------- timed region: K whole steps, inputs resident in HBM
     if wl.kind == "dion":  # P = B Q, R = B^T P and the two rank-r updates, per shape
@@ -556,12 +573,14 @@ def main():
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(K):
-        step()
+        run()
     e1.record(stream)
     torch.cuda.synchronize()
     barrier()
     clk = clocks.stop()
     launches = mao.launch_count() - launches0
+    if args.graph:  # replays launch the captured kernels without host calls
+        launches = per_replay * K
     mao.sync_status()
     ms_total = max_over_ranks(e0.elapsed_time(e1))
     ms_step = ms_total / K
@@ -603,7 +622,7 @@ def main():
     peaks, peak_src = load_peaks()
     if wl.kind == "dion":
         line = dion_line(wl, step, K, Wu, world, value, ms_step, reps_tc, ms_prof, st_ns, tc_ms,
-                         launches, clk, peaks, peak_src)
+                         launches, clk, peaks, peak_src, graph=args.graph)
         finish_line(args, line, wl, step, K, world, rank, dev, barrier, max_over_ranks)
         return
 
@@ -646,7 +665,8 @@ def main():
         "metric": metric_name(wl), "value": value, "unit": "steps/s", "n_gpus": world,
         "steps": K, "warmup": Wu, "ms_per_step": ms_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": wl.compute, "data": "synthetic",
-        "config": config_block(wl, touched, args.variant, args.post_polar),
+        "config": dict(config_block(wl, touched, args.variant, args.post_polar),
+                       launch="CUDA graph replay" if args.graph else "eager"),
         "ns_tflops_dense": dense / (st_ns / 1000.0) / 1e12,
         "ns_tflops_alg": alg / (st_ns / 1000.0) / 1e12,
         "stages_ms": {"momentum": st_mom, "ns": st_ns, "update": st_upd},
@@ -662,7 +682,7 @@ def main():
 
 
 def dion_line(wl, step, K, Wu, world, value, ms_step, reps_tc, ms_prof, st_step, tc_ms, launches,
-              clk, peaks, peak_src):
+              clk, peaks, peak_src, graph=False):
     """Bench line of a Dion workload: the step is HBM-bound (every matrix element is read and
     written a fixed number of times, 8 m n r flops against about 10 bytes per element)."""
     hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
@@ -681,6 +701,7 @@ def dion_line(wl, step, K, Wu, world, value, ms_step, reps_tc, ms_prof, st_step,
         sum(w.numel() * esize(w.dtype) for w in step.W) * 2
     c = config_block(wl, touched)
     c["rank"] = wl.rank
+    c["launch"] = "CUDA graph replay" if graph else "eager"
     return {
         "metric": metric_name(wl), "value": value, "unit": "steps/s", "n_gpus": world,
         "steps": K, "warmup": Wu, "ms_per_step": ms_step, "higher_is_better": True,
