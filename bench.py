@@ -53,6 +53,9 @@ def parse_args():
     ap.add_argument("--sweep-hbm", action="store_true",
                     help="time each HBM-bound kernel alone on L2-cold buffers of 256 MB-4 GB "
                          "and print one JSON line per kernel and size")
+    ap.add_argument("--block", default=None, metavar="ROWSxCOLS",
+                    help="Muon workloads: blockwise Newton-Schulz, every ROWS x COLS block of "
+                         "each matrix orthogonalised on its own")
     ap.add_argument("--graph", action="store_true",
                     help="time replays of one captured CUDA graph of the step (the library's "
                          "calls are capture-safe)")
@@ -151,7 +154,7 @@ class ClockSampler:
 class Step:
     """Device buffers and the sequence of C-ABI calls of one optimizer step."""
 
-    def __init__(self, wl, inputs, device, variant="bits", post_polar=False):
+    def __init__(self, wl, inputs, device, variant="bits", post_polar=False, block=None):
         """variant: "bits" (1-bit all-gather) or "int8" (integer SUM all-reduce) aggregation
         of a Sign-Muon workload; post_polar: the optional Newton–Schulz step on S_bar."""
         import torch
@@ -160,9 +163,12 @@ class Step:
             raise ValueError("the aggregation variants apply to Sign-Muon workloads only")
         if variant not in ("bits", "int8"):
             raise ValueError(variant)
+        if block is not None and wl.kind != "muon":
+            raise ValueError("blockwise Newton-Schulz applies to the Muon workloads")
         self.mao = mao
         self.wl = wl
         self.variant, self.post_polar = variant, post_polar
+        self.block = block
         self.W, self.M, self.G = inputs["W"], inputs["M"], inputs["G"]
         self.dev = device
         if wl.kind == "dion":
@@ -192,7 +198,11 @@ class Step:
                 self.U_bar = torch.empty_like(self.W[0])
         else:
             self.U = [torch.empty_like(w) for w in self.W]
-        self.ws = mao.workspace(self.M, wl.compute, device)
+        if block is not None:
+            n = mao.ns_blockwise_workspace_bytes(self.M, block, wl.compute)
+            self.ws = torch.empty(n, dtype=torch.uint8, device=device)
+        else:
+            self.ws = mao.workspace(self.M, wl.compute, device)
 
     def momentum(self):
         if self.wl.kind == "dion":  # B = M + G is the first stage of the Dion call
@@ -203,6 +213,10 @@ class Step:
         wl = self.wl
         if wl.kind == "dion":
             self.mao.dion_step(self.W, self.M, self.G, self.Q, wl.mu, wl.lr, ws=self.ws)
+            return
+        if self.block is not None:
+            self.mao.ns_orthogonalize_blockwise(self.M, self.U, self.block, wl.steps, wl.coeffs,
+                                                wl.eps, wl.compute, ws=self.ws)
             return
         if wl.kind == "sign" and self.variant == "bits":
             self.mao.ns_orthogonalize(self.M, self.U, wl.steps, wl.coeffs, wl.eps, wl.compute,
@@ -260,7 +274,8 @@ def stage_bytes(wl, step):
 
 # ------------------------------------------------------------------ oracle arm
 
-def oracle_sample(wl, host, budget_s, max_items=None, variant="bits", post_polar=False):
+def oracle_sample(wl, host, budget_s, max_items=None, variant="bits", post_polar=False,
+                  block=None):
     """Time the fp64 oracle on whole matrices of the workload (cycling) for ~budget_s.
 
     Returns (fraction of one step processed, seconds, description)."""
@@ -283,6 +298,11 @@ def oracle_sample(wl, host, budget_s, max_items=None, variant="bits", post_polar
         if wl.kind == "dion":
             oracle.dion_step(host["W"][i], host["M"][i], host["G"][i], host["Q"][i], wl.mu, wl.lr)
             done_flops += shapes[i][0] * shapes[i][1]
+        elif wl.kind == "muon" and block is not None:
+            M = oracle.momentum(host["M"][i], host["G"][i], wl.mu, store)
+            U = oracle.blockwise_newton_schulz(M, block[0], block[1], wl.steps, wl.coeffs, wl.eps)
+            oracle.apply_update_f64(host["W"][i], U, wl.lr)
+            done_flops += dense_flops([shapes[i]], wl.steps)
         elif wl.kind == "muon":
             oracle.muon_step([host["W"][i]], [host["M"][i]], [host["G"][i]], wl.mu, wl.lr,
                              wl.steps, wl.coeffs, wl.eps, m_store=store)
@@ -333,7 +353,7 @@ def host_copy(inputs):
     return {k: [t.float().cpu().numpy() for t in v] for k, v in inputs.items()}
 
 
-def run_reference(args, wl):
+def run_reference(args, wl, block=None):
     import torch
     from matrix_aware_optimizers_gb300 import workloads
     rank = int(os.environ.get("RANK", "0"))
@@ -347,7 +367,7 @@ def run_reference(args, wl):
         shapes = [(4096, 4096)] * 4 + [(4096, 14336), (14336, 4096), (4096, 14336)]
     inputs = workloads.generate(wl, "cpu", shapes=shapes if wl.index == 4 else None)
     host = host_copy(inputs)
-    var = dict(variant=args.variant, post_polar=args.post_polar)
+    var = dict(variant=args.variant, post_polar=args.post_polar, block=block)
     for _ in range(Wu):
         oracle_sample(wl, host, 0.0, max_items=1, **var)
     frac, secs = 0.0, 0.0
@@ -361,7 +381,8 @@ def run_reference(args, wl):
         "n_gpus": args.gpus, "steps": K, "warmup": Wu, "ms_per_step": 1000.0 / value,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f64", "data": "synthetic",
-        "config": config_block(wl, None, args.variant, args.post_polar),
+        "config": dict(config_block(wl, None, args.variant, args.post_polar),
+                       **({"blockwise": "%dx%d blocks" % block} if block else {})),
         "cpu_baseline": {"value": value, "unit": "steps/s", "cores": blas_threads(),
                          "kind": "oracle",
                          "sample": "each step: one matrix of the workload (cycling), fp64 numpy "
@@ -506,10 +527,15 @@ def main():
     args = parse_args()
     from matrix_aware_optimizers_gb300 import workloads
     wl = workloads.workload(args.config)
+    block = None
+    if args.block:
+        block = tuple(int(v) for v in args.block.lower().split("x"))
+        if wl.kind != "muon" or len(block) != 2 or min(block) < 1:
+            sys.exit("--block ROWSxCOLS applies to the Muon workloads (--config 2, 4 or 5)")
     if wl.kind != "sign" and (args.variant != "bits" or args.post_polar):
         sys.exit("--variant / --post-polar apply to the Sign-Muon workloads (--config 1 or 3)")
     if args.impl == "reference":
-        run_reference(args, wl)
+        run_reference(args, wl, block)
         return
 
     import torch
@@ -532,7 +558,7 @@ def main():
     K = args.steps if args.steps is not None else DEFAULT_STEPS[wl.index]
     Wu = max(3, args.warmup if args.warmup is not None else DEFAULT_WARMUP[wl.index])
     inputs = workloads.generate(wl, dev, seed=(wl.index - 1) + 1000 * rank)
-    step = Step(wl, inputs, dev, args.variant, args.post_polar)
+    step = Step(wl, inputs, dev, args.variant, args.post_polar, block)
     stream = torch.cuda.current_stream()
 
     def barrier():
@@ -563,6 +589,10 @@ def main():
     # ---------------- timed region: K whole steps, inputs resident in HBM
     if wl.kind == "dion":  # P = B Q, R = B^T P and the two rank-r updates, per shape
         n_tc_per_step = 4 * ((len(set(wl.shapes)) + 7) // 8)
+    elif block is not None:
+        bshapes = {(min(block[0], R - i), min(block[1], C - j)) for R, C in set(wl.shapes)
+                   for i in range(0, R, block[0]) for j in range(0, C, block[1])}
+        n_tc_per_step = 3 * wl.steps * ((len(bshapes) + 7) // 8)
     else:
         n_tc_per_step = 3 * wl.steps * ((len(set(wl.shapes)) + 7) // 8 + (1 if args.post_polar else 0))
     launches0 = mao.launch_count()
@@ -628,6 +658,9 @@ def main():
 
     # ---------------- roofline of the dominant kernel (tensor-core NS product kernel)
     shapes = [tuple(m.shape) for m in step.M]
+    if block is not None:  # the products run on the blocks
+        shapes = [(min(block[0], R - i), min(block[1], C - j)) for R, C in shapes
+                  for i in range(0, R, block[0]) for j in range(0, C, block[1])]
     alg = alg_flops(shapes, wl.steps)
     dense = dense_flops(shapes, wl.steps)
     # the post-vote polar step is one more Newton–Schulz on a matrix of W's shape
@@ -666,7 +699,8 @@ def main():
         "steps": K, "warmup": Wu, "ms_per_step": ms_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": wl.compute, "data": "synthetic",
         "config": dict(config_block(wl, touched, args.variant, args.post_polar),
-                       launch="CUDA graph replay" if args.graph else "eager"),
+                       launch="CUDA graph replay" if args.graph else "eager",
+                       **({"blockwise": "%dx%d blocks" % block} if block else {})),
         "ns_tflops_dense": dense / (st_ns / 1000.0) / 1e12,
         "ns_tflops_alg": alg / (st_ns / 1000.0) / 1e12,
         "stages_ms": {"momentum": st_mom, "ns": st_ns, "update": st_upd},
@@ -725,7 +759,7 @@ def finish_line(args, line, wl, step, K, world, rank, dev, barrier, max_over_ran
             wl, "cpu", shapes=None if wl.index != 4 else
             [(4096, 4096)] * 4 + [(4096, 14336), (14336, 4096), (4096, 14336)]))
         frac, secs, desc = oracle_sample(wl, host, args.cpu_seconds, variant=args.variant,
-                                         post_polar=args.post_polar)
+                                         post_polar=args.post_polar, block=step.block)
         line["cpu_baseline"] = {"value": frac / secs, "unit": "steps/s", "cores": blas_threads(),
                                 "kind": "oracle", "sample": desc + ", %.1f s" % secs}
     if rank == 0:
