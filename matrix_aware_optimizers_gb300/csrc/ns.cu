@@ -402,6 +402,7 @@ mao_status run_tc_stage(const Buffers& buf, const std::vector<const NsGroupPlan*
       G.out_mstride = as;
       G.res = nullptr;
       G.syrk = 1;
+      G.same_ab = 1;
     } else if (stage == NS_POLY) {
       srcA = srcB = buf.a(g);
       rowsA = rowsB = g.m;
@@ -416,6 +417,7 @@ mao_status run_tc_stage(const Buffers& buf, const std::vector<const NsGroupPlan*
       G.res_ld = g.lda;
       G.res_mstride = as;
       G.syrk = 1;
+      G.same_ab = 1;
     } else {
       if (!g.tall) {  // X' = B' X : A-operand B' (K-major), B-operand X (MN-major)
         srcA = buf.b(g); rowsA = g.m; ldA = g.lda;

@@ -107,6 +107,8 @@ struct TcGroup {
                             // diagonal 256-tiles: blocks below the diagonal are read
                             // through the transposed (MN-major) view of the upper block
   int32_t syrk;             // symmetric result: only upper and diagonal tiles computed
+  int32_t same_ab;          // A and B operands are the same buffer, layout and view: a
+                            // diagonal tile loads one half and multiplies it by itself
   int32_t tiles_m, tiles_n, tiles_per_mat, tile_begin;
   int32_t final_out;        // last NS_APPLY: write U / signs through the slot's OutEntry
   int32_t orig_cols;        // C of the original matrix (sign-bit indexing)

@@ -595,6 +595,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads(MODE), 1)
       const int op_tile = (is_a ? t.row0 : t.col0) / BN;           // 256-tile of the operand rows
       const uint32_t off = is_a ? 0u : uint32_t(HALF_BYTES);
       const int rc = (is_a ? t.row0 : t.col0) + HALF * int(cta);  // this CTA's M/N range
+      // a diagonal tile of a product of a buffer with itself: the B half equals the A half
+      const bool share = G.same_ab && t.row0 == t.col0;
+      const uint32_t tx_bytes = (share ? 2u : 4u) * uint32_t(HALF_BYTES);  // both CTAs
       for (int kb = 0; kb < t.nkb; ++kb) {
         int okw = 1;
         if (lane == 0) {
@@ -604,7 +607,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads(MODE), 1)
           if (!mbar_wait(smem_u32(&empty_bar[stage]), phase ^ 1u, abort_flag, limit)) {
             okw = 0;
           } else if (leader) {
-            mbar_expect_tx(smem_u32(&full_bar[stage]), 2u * STAGE_BYTES);
+            mbar_expect_tx(smem_u32(&full_bar[stage]), tx_bytes);
             armed |= 1u << stage;
             armed_phase = (armed_phase & ~(1u << stage)) | (phase << stage);
           }
@@ -617,7 +620,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads(MODE), 1)
           ok = false;
           break;
         }
-        if (active) {
+        if (active && !(share && !is_a)) {
           const uint32_t fb = mapa_shared(smem_u32(&full_bar[stage]), 0);
           const uint32_t dst = smem_u32(ring + stage * STAGE_BYTES) + off;
           const int k0 = kb * BK;
@@ -683,7 +686,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads(MODE), 1)
 #endif
           tc_fence_after();
           const uint32_t a_base = smem_u32(ring + stage * STAGE_BYTES);
-          const uint32_t b_base = a_base + HALF_BYTES;
+          // a diagonal tile of a buffer times itself reads the A half as B
+          const uint32_t b_base = (G.same_ab && t.row0 == t.col0) ? a_base : a_base + HALF_BYTES;
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
             // K-major: chunk kk/4 holds k 64*(kk/4).., 16 k-elements are 32 bytes along the
