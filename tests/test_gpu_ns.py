@@ -128,3 +128,15 @@ def test_ns_output_symmetry_invariant(cuda):
     XT = X.t().contiguous()
     (U, UT), _ = _run([X, XT], "bf16")
     assert rel_fro(to_np(UT), to_np(U).T) <= 2e-2
+
+
+@pytest.mark.parametrize("compute", ["f32", "bf16"])
+def test_ns_more_shape_groups_than_one_launch_holds(cuda, compute):
+    # eleven distinct shapes: two rounds of grouped launches (at most eight groups each)
+    gen = torch.Generator().manual_seed(29)
+    dt = torch.bfloat16 if compute == "bf16" else torch.float32
+    shapes = [(64 + 32 * i, 96 + 48 * i) for i in range(8)] + [(300, 100), (100, 300), (256, 256)]
+    Xs = [rand_matrix(gen, s, dt, cuda, 0.01 * (i + 1)) for i, s in enumerate(shapes)]
+    Us, _ = _run(Xs, compute)
+    for X, U in zip(Xs, Us):
+        assert rel_fro(to_np(U), oracle.newton_schulz(to_np(X), 5, QUINTIC)) <= TOL[compute]
