@@ -587,8 +587,9 @@ def main():
         mao.sync_status()
 
     # ---------------- timed region: K whole steps, inputs resident in HBM
-    if wl.kind == "dion":  # P = B Q, R = B^T P and the two rank-r updates, per shape
-        n_tc_per_step = 4 * ((len(set(wl.shapes)) + 7) // 8)
+    if wl.kind == "dion":  # every launch of the call: four products per round of shapes,
+        # the set-up launches and the CUDA-core kernels
+        n_tc_per_step = 4 * ((len(set(wl.shapes)) + 7) // 8) + (len(wl.shapes) + 15) // 16 + 16
     elif block is not None:
         bshapes = {(min(block[0], R - i), min(block[1], C - j)) for R, C in set(wl.shapes)
                    for i in range(0, R, block[0]) for j in range(0, C, block[1])}
@@ -629,9 +630,13 @@ def main():
         step()
     p1.record(stream)
     torch.cuda.synchronize()
-    tc_ms = mao.profile_end()
+    tagged = mao.profile_end_tagged()
     mao.sync_status()
     ms_prof = p0.elapsed_time(p1)
+    tc_ms = [ms for ms, tag in tagged if tag == "tc"]
+    kernel_ms = {}  # per launch kind: milliseconds per step
+    for ms, tag in tagged:
+        kernel_ms[tag] = kernel_ms.get(tag, 0.0) + ms / reps_tc
 
     # ---------------- per-stage times (separate pass, same stream)
     reps = max(3, min(K, 50))
@@ -652,7 +657,7 @@ def main():
     peaks, peak_src = load_peaks()
     if wl.kind == "dion":
         line = dion_line(wl, step, K, Wu, world, value, ms_step, reps_tc, ms_prof, st_ns, tc_ms,
-                         launches, clk, peaks, peak_src, graph=args.graph)
+                         launches, clk, peaks, peak_src, graph=args.graph, kernel_ms=kernel_ms)
         finish_line(args, line, wl, step, K, world, rank, dev, barrier, max_over_ranks)
         return
 
@@ -716,7 +721,7 @@ def main():
 
 
 def dion_line(wl, step, K, Wu, world, value, ms_step, reps_tc, ms_prof, st_step, tc_ms, launches,
-              clk, peaks, peak_src, graph=False):
+              clk, peaks, peak_src, graph=False, kernel_ms=None):
     """Bench line of a Dion workload: the step is HBM-bound (every matrix element is read and
     written a fixed number of times, 8 m n r flops against about 10 bytes per element)."""
     hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
@@ -741,6 +746,7 @@ def dion_line(wl, step, K, Wu, world, value, ms_step, reps_tc, ms_prof, st_step,
         "steps": K, "warmup": Wu, "ms_per_step": ms_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": wl.compute, "data": "synthetic",
         "config": c, "stages_ms": {"dion_step": st_step}, "roofline": roof,
+        "kernels_ms_per_step": {k: round(v, 4) for k, v in (kernel_ms or {}).items()},
         "gpu_launches": launches, "clocks": clk,
     }
 

@@ -311,9 +311,10 @@ mao_status mao_sync_status(void* stream);
  *
  * mao_launch_count: number of kernels this library has launched in this process.
  *
- * mao_profile_begin: from now on, every launch of the Newton–Schulz tensor-core product
- *   kernel (three per iteration) is bracketed by a pair of CUDA events recorded on the
- *   launch's stream, for up to max_launches launches (1..1<<20). Creates the events
+ * mao_profile_begin: from now on, every launch of the tensor-core product kernel (three
+ *   per Newton–Schulz iteration, four per Dion step) and of the Dion CUDA-core kernels is
+ *   bracketed by a pair of CUDA events recorded on the launch's stream, for up to
+ *   max_launches launches (1..1<<20). Creates the events
  *   (host-side driver objects, no device memory). Not thread-safe: one profiling session
  *   per process. Returns MAO_ERR_INVALID_ARG for a bad count, MAO_ERR_CUDA on failure.
  *
@@ -321,10 +322,24 @@ mao_status mao_sync_status(void* stream);
  *   milliseconds of up to max_out recorded launches into ms_out (host array, may be NULL
  *   when max_out is 0), destroys the events and returns the number of launches recorded
  *   (negative on a CUDA error).
+ *
+ * mao_profile_end_tagged: as mao_profile_end, and also writes one tag per recorded launch
+ *   into tags_out (host array of max_out entries, may be NULL): MAO_PROF_TC for the
+ *   tensor-core product kernel, otherwise the MAO_PROF_DION_* value of the Dion kernel.
  */
+enum {
+  MAO_PROF_TC = 0,
+  MAO_PROF_DION_SETUP = 1,     /* device table of the slots */
+  MAO_PROF_DION_STAGE = 2,     /* B = M + G and its bf16 copy; bf16 copy of Q_prev */
+  MAO_PROF_DION_GRAM = 3,      /* P^T P */
+  MAO_PROF_DION_CHOL = 4,      /* Cholesky factor and its inverse */
+  MAO_PROF_DION_TRMM = 5,      /* P L^-T */
+  MAO_PROF_DION_NORM = 6       /* column norms of R, Q = ColumnNormalize(R) */
+};
 int64_t mao_launch_count(void);
 mao_status mao_profile_begin(int32_t max_launches);
 int32_t mao_profile_end(float* ms_out, int32_t max_out);
+int32_t mao_profile_end_tagged(float* ms_out, int32_t* tags_out, int32_t max_out);
 
 #ifdef __cplusplus
 }

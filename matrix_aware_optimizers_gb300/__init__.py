@@ -313,8 +313,13 @@ def launch_count():
     return int(lib().mao_launch_count())
 
 
+PROFILE_TAGS = {0: "tc", 1: "dion_setup", 2: "dion_stage", 3: "dion_gram", 4: "dion_chol",
+                5: "dion_trmm", 6: "dion_norm"}
+
+
 def profile_begin(max_launches):
-    """Record CUDA events around each tensor-core product launch (benchmarking)."""
+    """Record CUDA events around each tensor-core product launch and each Dion CUDA-core
+    kernel launch (benchmarking)."""
     _abi.check("mao_profile_begin", lib().mao_profile_begin(int(max_launches)))
 
 
@@ -325,3 +330,13 @@ def profile_end(max_out=1 << 20):
     if n < 0:
         raise MaoError("mao_profile_end", _abi.MAO_ERR_CUDA)
     return [buf[i] for i in range(min(n, max_out))]
+
+
+def profile_end_tagged(max_out=1 << 20):
+    """Stop recording; returns (milliseconds, tag name) per recorded launch."""
+    buf = (ctypes.c_float * max_out)()
+    tags = (ctypes.c_int32 * max_out)()
+    n = lib().mao_profile_end_tagged(buf, tags, max_out)
+    if n < 0:
+        raise MaoError("mao_profile_end_tagged", _abi.MAO_ERR_CUDA)
+    return [(buf[i], PROFILE_TAGS.get(tags[i], str(tags[i]))) for i in range(min(n, max_out))]

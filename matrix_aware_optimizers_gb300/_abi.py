@@ -45,6 +45,7 @@ EXPORTS = (
     "mao_launch_count",
     "mao_profile_begin",
     "mao_profile_end",
+    "mao_profile_end_tagged",
 )
 
 
@@ -139,6 +140,8 @@ def load():
     lib.mao_profile_begin.argtypes = [ctypes.c_int32]
     lib.mao_profile_end.restype = ctypes.c_int32
     lib.mao_profile_end.argtypes = [P(ctypes.c_float), ctypes.c_int32]
+    lib.mao_profile_end_tagged.restype = ctypes.c_int32
+    lib.mao_profile_end_tagged.argtypes = [P(ctypes.c_float), P(ctypes.c_int32), ctypes.c_int32]
     _LIB = lib
     return lib
 

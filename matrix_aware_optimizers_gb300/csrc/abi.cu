@@ -54,6 +54,7 @@ struct Profile {
   int32_t cap = 0;
   int32_t used = 0;
   std::vector<cudaEvent_t> ev;  // 2 per launch
+  std::vector<int32_t> tag;     // 1 per launch
 };
 Profile g_prof;
 }  // namespace
@@ -66,8 +67,11 @@ std::atomic<unsigned long long> g_wait_limit{4000000000ull};  // 4 s
 
 unsigned long long wait_limit_ns() { return g_wait_limit.load(std::memory_order_relaxed); }
 
-void profile_before_launch(cudaStream_t stream) {
-  if (g_prof.on && g_prof.used < g_prof.cap) cudaEventRecord(g_prof.ev[2 * g_prof.used], stream);
+void profile_before_launch(cudaStream_t stream, int tag) {
+  if (g_prof.on && g_prof.used < g_prof.cap) {
+    g_prof.tag[g_prof.used] = tag;
+    cudaEventRecord(g_prof.ev[2 * g_prof.used], stream);
+  }
 }
 
 void profile_after_launch(cudaStream_t stream) {
@@ -226,6 +230,7 @@ mao_status mao_profile_begin(int32_t max_launches) {
       return MAO_ERR_CUDA;
     }
   }
+  g_prof.tag.assign(size_t(max_launches), 0);
   g_prof.cap = max_launches;
   g_prof.used = 0;
   g_prof.on = true;
@@ -233,6 +238,10 @@ mao_status mao_profile_begin(int32_t max_launches) {
 }
 
 int32_t mao_profile_end(float* ms_out, int32_t max_out) {
+  return mao_profile_end_tagged(ms_out, nullptr, max_out);
+}
+
+int32_t mao_profile_end_tagged(float* ms_out, int32_t* tags_out, int32_t max_out) {
   if (!g_prof.on) return 0;
   g_prof.on = false;
   int32_t n = g_prof.used;
@@ -243,6 +252,7 @@ int32_t mao_profile_end(float* ms_out, int32_t max_out) {
         cudaEventElapsedTime(&ms, g_prof.ev[2 * i], g_prof.ev[2 * i + 1]) != cudaSuccess)
       ok = false;
     if (ms_out && i < max_out) ms_out[i] = ms;
+    if (tags_out && i < max_out) tags_out[i] = g_prof.tag[i];
   }
   for (auto& e : g_prof.ev) cudaEventDestroy(e);
   g_prof.ev.clear();

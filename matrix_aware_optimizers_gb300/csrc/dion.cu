@@ -10,8 +10,9 @@
 //   X <- X - lr P Q^T               tensor-core rank-r update, in place
 //
 // The orthonormal basis is the Q factor of the thin QR with a positive triangular
-// diagonal, computed as Cholesky QR applied twice: S = P^T P, S = L L^T, P <- P L^-T
-// (a blocked forward substitution with the inverses of L's 32 x 32 diagonal blocks).
+// diagonal, computed as Cholesky QR applied twice: S = P^T P, S = L L^T, P <- P W^T with
+// W = L^-1 (the factorisation kernel also inverts L, so the product with P is one parallel
+// triangular multiply instead of a sequential substitution).
 // The three dense products run on the same tcgen05 kernel as Newton–Schulz, over up to
 // eight shape groups per launch; the r x r work (Gram matrices, Cholesky, triangular
 // solve) runs in fp32 on CUDA cores, every matrix of the call in one launch per stage.
@@ -35,7 +36,8 @@ __device__ unsigned int g_dion_error;  // bit 0: a Cholesky pivot was not positi
 namespace {
 
 constexpr int kMaxRank = 256;
-constexpr int kGramRows = 1024;   // rows of P summed by one partial Gram tile
+constexpr int kGramRows = 512;    // rows of P summed by one partial Gram tile
+constexpr int kGramTilesMax = 10; // lower 64 x 64 tiles of an r x r Gram, r <= 256
 constexpr int kNormRows = 256;    // rows of R summed by one partial column norm
 constexpr int kSetup = 16;        // table entries written per set-up launch
 constexpr int kCholThreads = 512;
@@ -49,7 +51,10 @@ struct DionSlot {
   float* Pout;                      // optional copy of the final P (m x r, row stride r)
   __nv_bfloat16 *Bw, *Qw, *Rw, *Pw; // bf16 operands, rows of ldn / ldr elements
   float *P0, *P1, *Rf;              // fp32 [m|n][ldr]
-  float *S, *L, *D, *cn;            // [gchunks][r][r]; L [r][r]; [nb][32][32]; [nchunks + 1][r]
+  float *Sp, *Sf;                   // partial Grams [gchunks][tiles][64 x 64]; final [tiles][64 x 64]
+  float* W;                         // L^-1 [ldr][ldr], zeros above the diagonal and past r
+  float* cn;                        // column norms of R: partials [nchunks][r], then the norms
+  int32_t* cnt;                     // arrival counters of the Gram tiles [2 passes][tiles]
   int64_t ldm, ldg, ldx, ldq;
   int32_t m, n, ldn;
   int32_t dtm, dtg, dtx;
@@ -79,6 +84,7 @@ __global__ void dion_setup_kernel(const __grid_constant__ SetupParams p) {
   const DionSlot& e = p.s[k];
   const int z = p.z0 + k;
   const_cast<DionSlot*>(p.c.slots)[z] = e;
+  for (int t = 0; t < 2 * kGramTilesMax; ++t) e.cnt[t] = 0;
   OutEntry o;
   o.bits = nullptr;
   o.out = e.P0;
@@ -157,250 +163,428 @@ __global__ void __launch_bounds__(256) dion_stage_q_kernel(const __grid_constant
 
 // ------------------------------------------------------- Cholesky QR: S = P^T P
 
-// Lower 64 x 64 tile (ti >= tj) of the partial Gram of rows [chunk*kGramRows, ...) of P;
-// grid (tile pairs, row chunks, slots). 256 threads, 4 x 4 outputs each.
-__global__ void __launch_bounds__(256) dion_gram_kernel(const __grid_constant__ DionCommon c,
-                                                        int from_p1) {
+// 16-byte asynchronous copy global -> shared (cp.async, L2 only); bytes past `src_bytes`
+// (0..16) are zero-filled and not read.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, int src_bytes) {
+  const uint32_t d = uint32_t(__cvta_generic_to_shared(dst));
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(d), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait1() { asm volatile("cp.async.wait_group 1;\n" ::: "memory"); }
+
+// Bytes of the 16-byte group of columns [c0, c0 + 4) of a row that lie before column r.
+__device__ __forceinline__ int bytes_before(int c0, int r) {
+  return 4 * max(0, min(4, r - c0));
+}
+
+constexpr int kGramThreads = 64;
+
+// Lower 64 x 64 tile (ti >= tj) of S = P^T P; grid (tiles, row chunks, slots), 64 threads,
+// 8 x 8 outputs each (rows 4 ty + x and 32 + 4 ty + x, columns 4 tx + y and 32 + 4 tx + y,
+// so the row reads of a warp are contiguous). A CTA sums the kGramRows rows of its chunk
+// in 32-row slabs, double-buffered in shared memory by cp.async (columns past r and rows
+// past the chunk are zero-filled: P's columns past r are never written). With one chunk the
+// tile goes straight to Sf. Otherwise every CTA writes its partial tile, and the CTA that
+// arrives last at the tile's counter adds the partials in chunk order (a fixed order, so
+// the result does not depend on which CTA finishes last) and writes Sf.
+__global__ void __launch_bounds__(kGramThreads) dion_gram_kernel(const __grid_constant__ DionCommon c,
+                                                                 int pass) {
   const DionSlot& e = c.slots[blockIdx.z];
-  if (int(blockIdx.y) >= e.gchunks) return;
-  int ti = 0, t = int(blockIdx.x);
+  const int gch = e.gchunks;
+  if (int(blockIdx.y) >= gch) return;
+  const int tile = int(blockIdx.x);
+  int ti = 0, t = tile;
   while (t > ti) { t -= ti + 1; ++ti; }
   const int tj = t;
-  const int r = c.r;
+  const bool diag = ti == tj;
+  const int r = c.r, ldr = c.ldr;
   const int64_t r0 = int64_t(blockIdx.y) * kGramRows;
   const int64_t r1 = min(int64_t(e.m), r0 + kGramRows);
-  __shared__ float As[32][64 + 4], Bs[32][64 + 4];
-  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
-  float acc[4][4] = {};
-  const float* P = from_p1 ? e.P1 : e.P0;
-  for (int64_t k0 = r0; k0 < r1; k0 += 32) {
-    for (int q = threadIdx.x; q < 32 * 64; q += 256) {
-      const int kk = q >> 6, cc = q & 63;
-      const int64_t row = k0 + kk;
-      const int ca = ti * 64 + cc, cb = tj * 64 + cc;
-      As[kk][cc] = (row < r1 && ca < r) ? P[row * c.ldr + ca] : 0.0f;
-      Bs[kk][cc] = (row < r1 && cb < r) ? P[row * c.ldr + cb] : 0.0f;
+  const float* P = pass == 0 ? e.P0 : e.P1;
+
+  __shared__ __align__(16) float As[2][32][64], Bs[2][32][64];
+  __shared__ int last;
+  const int tid = threadIdx.x;
+  const int tx = tid & 7, ty = tid >> 3;
+  auto issue = [&](int64_t k0, int buf) {
+#pragma unroll
+    for (int h = 0; h < 8; ++h) {
+      const int q = tid + kGramThreads * h;
+      const int row = q >> 4, c4 = 4 * (q & 15);
+      const int64_t g = k0 + row;
+      const bool ok = g < r1;
+      const float* src = P + (ok ? g : r0) * ldr;
+      cp_async16(&As[buf][row][c4], src + ti * 64 + c4, ok ? bytes_before(ti * 64 + c4, r) : 0);
+      if (!diag) cp_async16(&Bs[buf][row][c4], src + tj * 64 + c4, ok ? bytes_before(tj * 64 + c4, r) : 0);
     }
+    cp_async_commit();
+  };
+  float acc[8][8] = {};
+  const int nslab = int((r1 - r0 + 31) / 32);
+  issue(r0, 0);
+  for (int sl = 0; sl < nslab; ++sl) {
+    if (sl + 1 < nslab) issue(r0 + 32 * (sl + 1), (sl + 1) & 1);
+    else cp_async_commit();  // an empty group keeps the wait count uniform
+    cp_async_wait1();
     __syncthreads();
-#pragma unroll 8
+    const float(*Ab)[64] = As[sl & 1];
+    const float(*Bb)[64] = diag ? As[sl & 1] : Bs[sl & 1];
+#pragma unroll 4
     for (int kk = 0; kk < 32; ++kk) {
-      float a[4], b[4];
+      const float4 a0 = *reinterpret_cast<const float4*>(&Ab[kk][4 * ty]);
+      const float4 a1 = *reinterpret_cast<const float4*>(&Ab[kk][32 + 4 * ty]);
+      const float4 b0 = *reinterpret_cast<const float4*>(&Bb[kk][4 * tx]);
+      const float4 b1 = *reinterpret_cast<const float4*>(&Bb[kk][32 + 4 * tx]);
+      const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+      const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
 #pragma unroll
-      for (int x = 0; x < 4; ++x) {
-        a[x] = As[kk][ty * 4 + x];
-        b[x] = Bs[kk][tx * 4 + x];
-      }
+      for (int x = 0; x < 8; ++x)
 #pragma unroll
-      for (int x = 0; x < 4; ++x)
-#pragma unroll
-        for (int y = 0; y < 4; ++y) acc[x][y] = __fmaf_rn(a[x], b[y], acc[x][y]);
+        for (int y = 0; y < 8; ++y) acc[x][y] = __fmaf_rn(av[x], bv[y], acc[x][y]);
     }
     __syncthreads();
   }
-  float* S = e.S + size_t(blockIdx.y) * r * r;
+  const int ntiles = (ldr / 64) * (ldr / 64 + 1) / 2;
+  float* dst = gch == 1 ? e.Sf + size_t(tile) * 4096
+                        : e.Sp + (size_t(blockIdx.y) * ntiles + tile) * 4096;
 #pragma unroll
-  for (int x = 0; x < 4; ++x)
-#pragma unroll
-    for (int y = 0; y < 4; ++y) {
-      const int i = ti * 64 + ty * 4 + x, j = tj * 64 + tx * 4 + y;
-      if (i < r && j < r) S[size_t(i) * r + j] = acc[x][y];
+  for (int x = 0; x < 8; ++x) {
+    float* row = dst + (4 * ty + (x & 3) + 32 * (x >> 2)) * 64;
+    *reinterpret_cast<float4*>(row + 4 * tx) = make_float4(acc[x][0], acc[x][1], acc[x][2], acc[x][3]);
+    *reinterpret_cast<float4*>(row + 32 + 4 * tx) = make_float4(acc[x][4], acc[x][5], acc[x][6], acc[x][7]);
+  }
+  if (gch == 1) return;
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) last = atomicAdd(&e.cnt[pass * kGramTilesMax + tile], 1) == gch - 1;
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+  // the last CTA: Sf = sum of the partials in chunk order
+  for (int q = tid; q < 1024; q += kGramThreads) {
+    float4 s = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    for (int ch = 0; ch < gch; ++ch) {
+      const float4 v = __ldcg(reinterpret_cast<const float4*>(e.Sp + (size_t(ch) * ntiles + tile) * 4096) + q);
+      s.x += v.x;
+      s.y += v.y;
+      s.z += v.z;
+      s.w += v.w;
     }
+    reinterpret_cast<float4*>(e.Sf + size_t(tile) * 4096)[q] = s;
+  }
 }
 
 // Lower blocks of a matrix cut into 32 x 32 blocks, block (I, J) with I >= J at index
-// I (I + 1) / 2 + J, each block 32 rows of 33 floats (the pad keeps column reads of a warp
-// on distinct banks).
+// I (I + 1) / 2 + J, each block 32 rows of kLd = 36 floats: rows start on 16-byte
+// boundaries (broadcast row reads take 16 bytes at a time), a warp's column reads are
+// contiguous, and 16-byte row reads of a quarter warp (lane = row) fall on distinct banks.
+constexpr int kLd = 36;
+constexpr int kBlk = 32 * kLd;  // floats of one block
+
 __device__ __forceinline__ float* blk(float* A, int I, int J) {
-  return A + (I * (I + 1) / 2 + J) * (32 * 33);
+  return A + (I * (I + 1) / 2 + J) * kBlk;
 }
 
-// One CTA per slot: S (the partial Grams added in chunk order) = L L^T by blocked
-// right-looking Cholesky with 32 x 32 blocks in shared memory. For each block column J:
-//   warp 0 factors the diagonal block (unscaled right-looking steps, then column scaling)
-//   and inverts it (D_J, lane = column, forward substitution in registers);
-//   the panel below is L_IJ = A_IJ D_J^T (one warp per row, lane = column);
-//   every trailing lower block gets A_IK -= L_IJ L_KJ^T (one warp per block, lane =
-//   column, the lane's row of L_KJ held in registers).
-// A pivot that is not positive sets the device error word and is replaced by 1e-30 (P had
-// dependent columns). Rows and columns past r are the identity. L goes to global memory
-// (row-major, zeros above the diagonal) and D_J to e.D.
+__device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+
+// Factors the 32 x 32 block Ad = L L^T in registers (lane = row; the diagonal pivot of step j
+// comes from lane j, the multipliers of rows k > j from lane k) and writes L back (zeros
+// above the diagonal). A pivot that is not positive is replaced by 1e-30 and reported.
+// Not inlined: inlined into the kernel, its a[] array lands in local memory.
+__device__ __noinline__ bool chol32(float* Ad, int lane) {
+  float a[32];
+#pragma unroll
+  for (int q = 0; q < 32; q += 4) {
+    const float4 v = ld4(Ad + lane * kLd + q);
+    a[q] = v.x;
+    a[q + 1] = v.y;
+    a[q + 2] = v.z;
+    a[q + 3] = v.w;
+  }
+  bool bad = false;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    float p = __shfl_sync(0xFFFFFFFFu, a[j], j);
+    if (!(p > 0.0f)) {
+      bad = true;
+      p = 1e-30f;
+    }
+    const float ljj = sqrtf(p);
+    const float inv = 1.0f / ljj;
+    a[j] = lane == j ? ljj : (lane > j ? a[j] * inv : 0.0f);
+#pragma unroll
+    for (int k = j + 1; k < 32; ++k) {
+      const float lkj = __shfl_sync(0xFFFFFFFFu, a[j], k);
+      if (lane >= k) a[k] = __fmaf_rn(-a[j], lkj, a[k]);
+    }
+  }
+#pragma unroll
+  for (int q = 0; q < 32; ++q) Ad[lane * kLd + q] = q <= lane ? a[q] : 0.0f;
+  __syncwarp();
+  return bad;
+}
+
+// In place: the lower 32 x 32 block L becomes D = L^-1 (lane = column of D, forward
+// substitution in registers, four partial sums per dot product, the rows of L read 16 bytes
+// at a time); zeros above the diagonal.
+__device__ __forceinline__ void inv32(float* Ad, int lane) {
+  float x[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    float s[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+    for (int k4 = 0; k4 < i; k4 += 4) {
+      const float4 l = ld4(Ad + i * kLd + k4);
+      const float lv[4] = {l.x, l.y, l.z, l.w};
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (k4 + u < i) s[u] = __fmaf_rn(lv[u], k4 + u >= lane ? x[k4 + u] : 0.0f, s[u]);
+    }
+    const float lii = Ad[i * kLd + i];
+    x[i] = i < lane ? 0.0f : (i == lane ? 1.0f / lii : -((s[0] + s[1]) + (s[2] + s[3])) / lii);
+  }
+  __syncwarp();
+#pragma unroll
+  for (int i = 0; i < 32; ++i) Ad[i * kLd + lane] = x[i];
+  __syncwarp();
+}
+
+// One CTA per slot: S = L L^T (blocked right-looking Cholesky, 32 x 32 blocks in shared
+// memory), then W = L^-1, written to e.W ([ldr][ldr], zeros above the diagonal and past r).
+//   Cholesky, for each block column J: warp 0 factors the diagonal block (chol32) and
+//   inverts it in place (inv32: the diagonal block now holds D_J = L_JJ^-1, which is all
+//   that later steps need of it); the panel below becomes L_IJ = A_IJ D_J^T (one warp per
+//   row); the trailing lower blocks get A_IK -= L_IJ L_KJ^T (one warp per 8-row quarter of
+//   a block, the lane's row of L_KJ in registers).
+//   Inverse, block row by block row (I = 1 .. nb - 1; W_JJ = D_J):
+//   T_J = sum_{K = J .. I-1} L_IK W_KJ for every J < I, then W_IJ = -D_I T_J in place of
+//   L_IJ (row block I of L is no longer needed once all T_J are formed).
+// Rows and columns past r are the identity. A pivot that is not positive sets the device
+// error word (P had dependent columns).
 __global__ void __launch_bounds__(kCholThreads, 1) dion_chol_kernel(const __grid_constant__ DionCommon c) {
-  extern __shared__ float sm[];
+  extern __shared__ __align__(16) float sm[];
   const DionSlot& e = c.slots[blockIdx.x];
-  const int r = c.r;
+  const int r = c.r, ldr = c.ldr;
   const int nb = (r + 31) / 32;
-  float* A = sm;                                // nb (nb + 1) / 2 blocks
-  float* Dsm = sm + nb * (nb + 1) / 2 * 32 * 33;  // [32][33], the current D_J
+  const int nlow = nb * (nb + 1) / 2;
+  float* A = sm;                  // nlow blocks
+  float* Tt = A + nlow * kBlk;    // nb - 1 blocks: T_J of the current block row
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   constexpr int kWarps = kCholThreads / 32;
-  const int gch = e.gchunks;
-  const float* S = e.S;
-  // load the lower blocks (rows i >= k in the diagonal blocks), identity past r
-  for (int b = warp; b < nb * (nb + 1) / 2; b += kWarps) {
+  // load the lower blocks from the 64 x 64 Gram tiles; identity past r
+  for (int b = warp; b < nlow; b += kWarps) {
     int I = 0, J = b;
     while (J > I) { J -= I + 1; ++I; }
     float* Ab = blk(A, I, J);
-    for (int ii = 0; ii < 32; ++ii) {
-      const int i = 32 * I + ii, k = 32 * J + lane;
-      float v = 0.0f;
-      if (i < r && k < r && k <= i)
-        for (int ch = 0; ch < gch; ++ch) v += S[(size_t(ch) * r + i) * r + k];
-      else if (i == k)
-        v = 1.0f;
-      Ab[ii * 33 + lane] = v;
+    const int k = 32 * J + lane;
+#pragma unroll 4
+    for (int ii0 = 0; ii0 < 32; ii0 += 8) {
+      float v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int i = 32 * I + ii0 + u;
+        v[u] = i == k ? 1.0f : 0.0f;
+        if (i < r && k < r && k <= i) {
+          const int ti = i / 64, tk = k / 64;
+          v[u] = e.Sf[size_t(ti * (ti + 1) / 2 + tk) * 4096 + (i % 64) * 64 + (k % 64)];
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) Ab[(ii0 + u) * kLd + lane] = v[u];
     }
   }
   __syncthreads();
   for (int J = 0; J < nb; ++J) {
+    float* Dj = blk(A, J, J);
     if (warp == 0) {
-      float* Ad = blk(A, J, J);
-      // right-looking steps on unscaled columns: at step j, lane k > j updates its column k
-      // below the diagonal, A_ik -= A_ij A_kj / A_jj for i >= k (column j is only read)
-      for (int j = 0; j < 32; ++j) {
-        float pj = Ad[j * 33 + j];
-        if (!(pj > 0.0f)) {
-          if (lane == 0) atomicOr(&g_dion_error, 1u);
-          pj = 1e-30f;
-        }
-        if (lane > j) {
-          const float akj = Ad[lane * 33 + j] / pj;
-          for (int i = lane; i < 32; ++i) Ad[i * 33 + lane] = __fmaf_rn(-Ad[i * 33 + j], akj, Ad[i * 33 + lane]);
-        }
-        __syncwarp();
-        if (lane == j) Ad[j * 33 + j] = pj;  // the sanitised pivot, kept for the scaling
-        __syncwarp();
-      }
-      // L_ik = A_ik / sqrt(pivot_k) for k < i (lane = row), then L_ii = sqrt(pivot_i)
-      for (int k = 0; k < lane; ++k) Ad[lane * 33 + k] *= rsqrtf(Ad[k * 33 + k]);
-      __syncwarp();
-      Ad[lane * 33 + lane] = sqrtf(Ad[lane * 33 + lane]);
-      __syncwarp();
-      // D_J = L_JJ^-1, lane = column
-      float x[32];
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        float sum = 0.0f;
-#pragma unroll
-        for (int k = 0; k < i; ++k) sum = __fmaf_rn(Ad[i * 33 + k], k >= lane ? x[k] : 0.0f, sum);
-        const float lii = Ad[i * 33 + i];
-        x[i] = i < lane ? 0.0f : (i == lane ? 1.0f / lii : -sum / lii);
-      }
-      float* D = e.D + size_t(J) * 32 * 32;
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        Dsm[i * 33 + lane] = x[i];
-        D[i * 32 + lane] = x[i];
-      }
+      if (chol32(Dj, lane) && lane == 0) atomicOr(&g_dion_error, 1u);
+      inv32(Dj, lane);
     }
     __syncthreads();
-    // panel: L_IJ = A_IJ D^T, one warp per row of the blocks below
     for (int row = 32 * (J + 1) + warp; row < 32 * nb; row += kWarps) {
-      float* Ap = blk(A, row / 32, J) + (row % 32) * 33;
-      float acc = 0.0f;
-      for (int q = 0; q <= lane; ++q) acc = __fmaf_rn(Ap[q], Dsm[lane * 33 + q], acc);
+      float* Ap = blk(A, row / 32, J) + (row % 32) * kLd;
+      float s0 = 0.0f, s1 = 0.0f;
+#pragma unroll
+      for (int q = 0; q < 32; q += 4) {
+        const float4 a = ld4(Ap + q), d = ld4(Dj + lane * kLd + q);
+        s0 = __fmaf_rn(a.x, d.x, s0);
+        s1 = __fmaf_rn(a.y, d.y, s1);
+        s0 = __fmaf_rn(a.z, d.z, s0);
+        s1 = __fmaf_rn(a.w, d.w, s1);
+      }
       __syncwarp();
-      Ap[lane] = acc;
+      Ap[lane] = s0 + s1;
     }
     __syncthreads();
-    // trailing lower blocks (I, K), J < K <= I: one warp per block
     const int t = nb - J - 1;
-    for (int b = warp; b < t * (t + 1) / 2; b += kWarps) {
-      int I = 0, K = b;
+    for (int item = warp; item < 2 * t * (t + 1); item += kWarps) {
+      const int quarter = item & 3;
+      int I = 0, K = item >> 2;
       while (K > I) { K -= I + 1; ++I; }
       I += J + 1;
       K += J + 1;
-      float lk[32];
-      const float* Lk = blk(A, K, J) + lane * 33;
+      float4 lk[8];
+      const float* Lk = blk(A, K, J) + lane * kLd;
 #pragma unroll
-      for (int q = 0; q < 32; ++q) lk[q] = Lk[q];
-      const float* Li = blk(A, I, J);
-      float* Ab = blk(A, I, K);
-      for (int ii = 0; ii < 32; ++ii) {
-        float sum = 0.0f;
+      for (int q = 0; q < 8; ++q) lk[q] = ld4(Lk + 4 * q);
+      const float* Li = blk(A, I, J) + quarter * 8 * kLd;
+      float* Ab = blk(A, I, K) + quarter * 8 * kLd;
 #pragma unroll
-        for (int q = 0; q < 32; ++q) sum = __fmaf_rn(Li[ii * 33 + q], lk[q], sum);
-        Ab[ii * 33 + lane] -= sum;
+      for (int tt = 0; tt < 8; ++tt) {
+        float s0 = 0.0f, s1 = 0.0f;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const float4 l = ld4(Li + tt * kLd + 4 * q);
+          s0 = __fmaf_rn(l.x, lk[q].x, s0);
+          s1 = __fmaf_rn(l.y, lk[q].y, s1);
+          s0 = __fmaf_rn(l.z, lk[q].z, s0);
+          s1 = __fmaf_rn(l.w, lk[q].w, s1);
+        }
+        Ab[tt * kLd + lane] -= s0 + s1;
       }
     }
     __syncthreads();
   }
-  // L to global memory, row-major r x r, zeros above the diagonal
-  for (int q = threadIdx.x; q < r * r; q += kCholThreads) {
-    const int i = q / r, k = q - i * r;
-    e.L[q] = k <= i ? blk(A, i / 32, k / 32)[(i % 32) * 33 + (k % 32)] : 0.0f;
+  // W = L^-1, block row by block row
+  for (int I = 1; I < nb; ++I) {
+    for (int item = warp; item < 4 * I; item += kWarps) {
+      const int J = item >> 2, quarter = item & 3;
+      float acc[8] = {};
+      for (int K = J; K < I; ++K) {
+        const float* Wk = blk(A, K, J);  // W_KJ (D_J on the diagonal)
+        const float* Li = blk(A, I, K) + quarter * 8 * kLd;
+#pragma unroll 2
+        for (int q = 0; q < 32; q += 4) {
+          const float w0 = Wk[q * kLd + lane], w1 = Wk[(q + 1) * kLd + lane];
+          const float w2 = Wk[(q + 2) * kLd + lane], w3 = Wk[(q + 3) * kLd + lane];
+#pragma unroll
+          for (int tt = 0; tt < 8; ++tt) {
+            const float4 l = ld4(Li + tt * kLd + q);
+            acc[tt] = __fmaf_rn(l.x, w0, acc[tt]);
+            acc[tt] = __fmaf_rn(l.y, w1, acc[tt]);
+            acc[tt] = __fmaf_rn(l.z, w2, acc[tt]);
+            acc[tt] = __fmaf_rn(l.w, w3, acc[tt]);
+          }
+        }
+      }
+      float* T = Tt + J * kBlk + quarter * 8 * kLd;
+#pragma unroll
+      for (int tt = 0; tt < 8; ++tt) T[tt * kLd + lane] = acc[tt];
+    }
+    __syncthreads();
+    const float* Di = blk(A, I, I);
+    for (int item = warp; item < 4 * I; item += kWarps) {
+      const int J = item >> 2, quarter = item & 3;
+      const float* T = Tt + J * kBlk;
+      const float* Dr = Di + quarter * 8 * kLd;
+      float acc[8] = {};
+#pragma unroll 2
+      for (int q = 0; q < 32; q += 4) {
+        const float t0 = T[q * kLd + lane], t1 = T[(q + 1) * kLd + lane];
+        const float t2 = T[(q + 2) * kLd + lane], t3 = T[(q + 3) * kLd + lane];
+#pragma unroll
+        for (int tt = 0; tt < 8; ++tt) {
+          const float4 d = ld4(Dr + tt * kLd + q);
+          acc[tt] = __fmaf_rn(d.x, t0, acc[tt]);
+          acc[tt] = __fmaf_rn(d.y, t1, acc[tt]);
+          acc[tt] = __fmaf_rn(d.z, t2, acc[tt]);
+          acc[tt] = __fmaf_rn(d.w, t3, acc[tt]);
+        }
+      }
+      float* Wb = blk(A, I, J) + quarter * 8 * kLd;
+#pragma unroll
+      for (int tt = 0; tt < 8; ++tt) Wb[tt * kLd + lane] = -acc[tt];
+    }
+    __syncthreads();
+  }
+  // W to global memory: [ldr][ldr], zeros above the diagonal and past r
+  for (int q = threadIdx.x; q < ldr * ldr; q += kCholThreads) {
+    const int i = q / ldr, k = q - i * ldr;
+    float v = 0.0f;
+    if (i < r && k < r && k <= i) v = blk(A, i / 32, k / 32)[(i % 32) * kLd + (k % 32)];
+    e.W[q] = v;
   }
 }
 
-// Pout = Pin L^-T by blocked forward substitution over 32-column blocks J:
-//   Pout[:, J] = (Pin[:, J] - Pout[:, <J] L[J, <J]^T) D_J^T,   D_J = L[J, J]^-1.
-// One CTA (256 threads, 8 rows x 1 column each) per 64 rows of one slot; the rows of Pout
-// stay in shared memory, and the rows of L[J, <J] and D_J are staged there per block
-// (coalesced loads). The last pass also writes the bf16 operand copy Pw (zero padding up
-// to ldr) and the caller's P copy.
-constexpr int kTrsmThreads = 256;
+// Pout = Pin W^T (W = L^-1 lower triangular, so Pout[:, j] needs columns k <= j of Pin).
+// grid (row tiles x column tiles of 64, slots), 64 threads, 8 x 8 outputs each: rows
+// rg + 8 x and columns tx + 8 y. Both operands sit in shared memory with k contiguous (rows
+// of 36 floats, double-buffered by cp.async), so every 16-byte read of a quarter warp falls
+// on distinct banks. Pass 0 writes P1 (fp32, zeros past r); pass 1 writes the bf16 operand
+// Pw (zeros up to ldr) and, if asked, the caller's fp32 copy of P.
+constexpr int kTrmmThreads = 64;
 
-__global__ void __launch_bounds__(kTrsmThreads) dion_trsm_kernel(const __grid_constant__ DionCommon c,
+__global__ void __launch_bounds__(kTrmmThreads) dion_trmm_kernel(const __grid_constant__ DionCommon c,
                                                                  int pass) {
-  extern __shared__ float tsm[];
   const DionSlot& e = c.slots[blockIdx.y];
-  const int64_t i0 = int64_t(blockIdx.x) * 64;
-  if (i0 >= e.m) return;
   const int r = c.r, ldr = c.ldr;
-  const int pld = r + 1;
-  float* Pn = tsm;              // [64][r + 1]
-  float* T = Pn + 64 * pld;     // [64][33]
-  float* Ls = T + 64 * 33;      // [32][r + 1]: rows of L[J, <J]
-  float* Ds = Ls + 32 * pld;    // [32][33]: D_J
+  const int ctiles = ldr / 64;
+  const int64_t i0 = int64_t(blockIdx.x / ctiles) * 64;
+  if (i0 >= e.m) return;
+  const int j0 = int(blockIdx.x % ctiles) * 64;
+  const int kend = min(r, j0 + 64);
   const float* Pin = pass == 0 ? e.P0 : e.P1;
-  float* Pout = pass == 0 ? e.P1 : e.P0;
-  const int cc = threadIdx.x % 32, rg = threadIdx.x / 32;  // column in the block, row group
-  const int nb = (r + 31) / 32;
-  for (int J = 0; J < nb; ++J) {
-    const int j0 = 32 * J;
-    for (int q = threadIdx.x; q < 32 * j0; q += kTrsmThreads) {
-      const int rr = q / j0, k = q - rr * j0;
-      Ls[rr * pld + k] = (j0 + rr < r) ? e.L[size_t(j0 + rr) * r + k] : 0.0f;
-    }
-    for (int q = threadIdx.x; q < 32 * 32; q += kTrsmThreads)
-      Ds[(q / 32) * 33 + q % 32] = e.D[size_t(J) * 1024 + q];
-    const int gj = j0 + cc;
-    float acc[8];
+
+  __shared__ __align__(16) float As[2][64][36], Bs[2][64][36];
+  const int tid = threadIdx.x;
+  const int tx = tid & 7, rg = tid >> 3;
+  auto issue = [&](int k0, int buf) {
 #pragma unroll
-    for (int t = 0; t < 8; ++t) {
-      const int64_t row = i0 + rg * 8 + t;
-      acc[t] = (row < e.m && gj < r) ? Pin[row * ldr + gj] : 0.0f;
+    for (int h = 0; h < 8; ++h) {
+      const int q = tid + kTrmmThreads * h;
+      const int row = q >> 3, k4 = 4 * (q & 7);
+      const int64_t g = i0 + row;
+      const bool ok = g < e.m;
+      cp_async16(&As[buf][row][k4], Pin + (ok ? g : i0) * ldr + k0 + k4,
+                 ok ? bytes_before(k0 + k4, r) : 0);
+      cp_async16(&Bs[buf][row][k4], e.W + size_t(j0 + row) * ldr + k0 + k4, 16);
     }
+    cp_async_commit();
+  };
+  float acc[8][8] = {};
+  const int nslab = (kend + 31) / 32;
+  issue(0, 0);
+  for (int sl = 0; sl < nslab; ++sl) {
+    if (sl + 1 < nslab) issue(32 * (sl + 1), (sl + 1) & 1);
+    else cp_async_commit();
+    cp_async_wait1();
     __syncthreads();
-    for (int k = 0; k < j0; ++k) {
-      const float l = Ls[cc * pld + k];
+    const float(*Ab)[36] = As[sl & 1];
+    const float(*Bb)[36] = Bs[sl & 1];
+#pragma unroll 2
+    for (int kk = 0; kk < 32; kk += 4) {
+      float4 a[8];
 #pragma unroll
-      for (int t = 0; t < 8; ++t) acc[t] = __fmaf_rn(-Pn[(rg * 8 + t) * pld + k], l, acc[t]);
-    }
+      for (int x = 0; x < 8; ++x) a[x] = *reinterpret_cast<const float4*>(&Ab[rg + 8 * x][kk]);
 #pragma unroll
-    for (int t = 0; t < 8; ++t) T[(rg * 8 + t) * 33 + cc] = acc[t];
-    __syncthreads();
-    float out[8] = {};
-    for (int q = 0; q <= cc; ++q) {
-      const float d = Ds[cc * 33 + q];
+      for (int y = 0; y < 8; ++y) {
+        const float4 b = *reinterpret_cast<const float4*>(&Bb[tx + 8 * y][kk]);
 #pragma unroll
-      for (int t = 0; t < 8; ++t) out[t] = __fmaf_rn(T[(rg * 8 + t) * 33 + q], d, out[t]);
-    }
-    if (gj < r) {
-#pragma unroll
-      for (int t = 0; t < 8; ++t) Pn[(rg * 8 + t) * pld + gj] = out[t];
+        for (int x = 0; x < 8; ++x) {
+          acc[x][y] = __fmaf_rn(a[x].x, b.x, acc[x][y]);
+          acc[x][y] = __fmaf_rn(a[x].y, b.y, acc[x][y]);
+          acc[x][y] = __fmaf_rn(a[x].z, b.z, acc[x][y]);
+          acc[x][y] = __fmaf_rn(a[x].w, b.w, acc[x][y]);
+        }
+      }
     }
     __syncthreads();
   }
-  // write back: fp32 P (columns < r), bf16 Pw (columns < ldr), the caller's copy
-  for (int q = threadIdx.x; q < 64 * ldr; q += kTrsmThreads) {
-    const int t = q / ldr, j = q - t * ldr;
-    const int64_t row = i0 + t;
+#pragma unroll
+  for (int x = 0; x < 8; ++x) {
+    const int64_t row = i0 + rg + 8 * x;
     if (row >= e.m) continue;
-    const float v = j < r ? Pn[t * pld + j] : 0.0f;
-    if (j < r) Pout[row * ldr + j] = v;
-    if (pass == 1) {
-      e.Pw[row * ldr + j] = __float2bfloat16_rn(v);
-      if (e.Pout && j < r) e.Pout[row * r + j] = v;
+#pragma unroll
+    for (int y = 0; y < 8; ++y) {
+      const int j = j0 + tx + 8 * y;
+      const float v = j < r ? acc[x][y] : 0.0f;
+      if (pass == 0) {
+        e.P1[row * ldr + j] = v;
+      } else {
+        e.Pw[row * ldr + j] = __float2bfloat16_rn(v);
+        if (e.Pout && j < r) e.Pout[row * r + j] = v;
+      }
     }
   }
 }
@@ -471,7 +655,7 @@ __global__ void __launch_bounds__(256) dion_q_kernel(const __grid_constant__ Dio
 struct DionGroup {
   int64_t m, n;
   int32_t count, slot0;
-  size_t off_bw, off_qw, off_rw, off_pw, off_p0, off_p1, off_rf, off_s, off_l, off_d, off_cn;
+  size_t off_bw, off_qw, off_rw, off_pw, off_p0, off_p1, off_rf, off_sp, off_sf, off_w, off_cn, off_cnt;
 };
 
 struct DionPlan {
@@ -524,9 +708,11 @@ void make_dion_plan(const mao_mat* X, int32_t batch, int32_t rank, DionPlan& pla
     g.off_p0 = take(c * m * ldr * 4);
     g.off_p1 = take(c * m * ldr * 4);
     g.off_rf = take(c * n * ldr * 4);
-    g.off_s = take(c * gch * r * r * 4);
-    g.off_l = take(c * r * r * 4);
-    g.off_d = take(c * size_t(ceil_div(rank, 32)) * 32 * 32 * 4);
+    const size_t ntiles = (ldr / 64) * (ldr / 64 + 1) / 2;
+    g.off_sp = take(gch > 1 ? c * gch * ntiles * 4096 * 4 : 0);
+    g.off_sf = take(c * ntiles * 4096 * 4);
+    g.off_w = take(c * ldr * ldr * 4);
+    g.off_cnt = take(c * 2 * kGramTilesMax * 4);
     g.off_cn = take(c * (nch + 1) * r * 4);
     for (int b : mem) plan.input_of.push_back(b);
     slot += g.count;
@@ -633,23 +819,18 @@ mao_status dion_run(const mao_mat* X, const mao_mat* M, const mao_mat* G, const 
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return MAO_ERR_CUDA;
   cudaError_t attr_err = cudaSuccess;
-  auto chol_bytes = [](int rk) {
+  auto chol_bytes = [](int rk) {  // lower blocks and the row temporaries of the inverse
     const size_t nbk = size_t(ceil_div(rk, 32));
-    return sizeof(float) * (nbk * (nbk + 1) / 2 * 32 * 33 + 32 * 33);
+    return sizeof(float) * size_t(kBlk) * (nbk * (nbk + 1) / 2 + nbk - 1);
   };
-  auto trsm_bytes = [](int rk) {
-    return sizeof(float) * (96 * size_t(rk + 1) + 64 * 33 + 32 * 33);
-  };
-  const size_t chol_max = chol_bytes(kMaxRank), trsm_max = trsm_bytes(kMaxRank);
+  const size_t chol_max = chol_bytes(kMaxRank);
   std::call_once(attr_once[dev & 63], [&] {
     attr_err = cudaFuncSetAttribute(dion_chol_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     int(chol_max));
-    if (attr_err == cudaSuccess)
-      attr_err = cudaFuncSetAttribute(dion_trsm_kernel,
-                                      cudaFuncAttributeMaxDynamicSharedMemorySize, int(trsm_max));
   });
   if (attr_err != cudaSuccess) return MAO_ERR_CUDA;
-  auto launched = [] {
+  auto launched = [stream] {
+    profile_after_launch(stream);
     count_launch();
     return cudaGetLastError() == cudaSuccess;
   };
@@ -677,9 +858,12 @@ mao_status dion_run(const mao_mat* X, const mao_mat* M, const mao_mat* G, const 
       e.Rf = reinterpret_cast<float*>(ws + g.off_rf) + size_t(k) * g.n * plan.ldr;
       e.gchunks = int32_t(ceil_div(g.m, kGramRows));
       e.nchunks = int32_t(ceil_div(g.n, kNormRows));
-      e.S = reinterpret_cast<float*>(ws + g.off_s) + size_t(k) * e.gchunks * rank * rank;
-      e.L = reinterpret_cast<float*>(ws + g.off_l) + size_t(k) * rank * rank;
-      e.D = reinterpret_cast<float*>(ws + g.off_d) + size_t(k) * ceil_div(rank, 32) * 32 * 32;
+      const size_t ntiles = size_t(plan.ldr / 64) * size_t(plan.ldr / 64 + 1) / 2;
+      e.Sp = e.gchunks > 1 ? reinterpret_cast<float*>(ws + g.off_sp) + size_t(k) * e.gchunks * ntiles * 4096
+                           : nullptr;
+      e.Sf = reinterpret_cast<float*>(ws + g.off_sf) + size_t(k) * ntiles * 4096;
+      e.W = reinterpret_cast<float*>(ws + g.off_w) + size_t(k) * plan.ldr * plan.ldr;
+      e.cnt = reinterpret_cast<int32_t*>(ws + g.off_cnt) + size_t(k) * 2 * kGramTilesMax;
       e.cn = reinterpret_cast<float*>(ws + g.off_cn) + size_t(k) * (e.nchunks + 1) * rank;
       e.ldm = M[b].ld;
       e.ldg = G[b].ld;
@@ -703,29 +887,36 @@ mao_status dion_run(const mao_mat* X, const mao_mat* M, const mao_mat* G, const 
     sp.z0 = z0;
     sp.c = c;
     for (int k = 0; k < sp.n; ++k) sp.s[k] = slots[z0 + k];
+    profile_before_launch(stream, MAO_PROF_DION_SETUP);
     dion_setup_kernel<<<1, kSetup, 0, stream>>>(sp);
     if (!launched()) return MAO_ERR_CUDA;
   }
   const unsigned nb = unsigned(batch);
   auto blocks = [](int64_t units) { return unsigned(ceil_div(units, 256)); };
   // 1. B = M + G (M <- B), Bw; Qw = bf16(Q_prev)
+  profile_before_launch(stream, MAO_PROF_DION_STAGE);
   dion_stage_kernel<<<dim3(blocks(plan.max_units), nb), 256, 0, stream>>>(c);
   if (!launched()) return MAO_ERR_CUDA;
+  profile_before_launch(stream, MAO_PROF_DION_STAGE);
   dion_stage_q_kernel<<<dim3(blocks(plan.max_qunits), nb), 256, 0, stream>>>(c);
   if (!launched()) return MAO_ERR_CUDA;
   // 2. P = B Q_prev (fp32)
   mao_status st = dion_tc(plan, ws, c.tP, 0, 1.0f, stream);
   if (st != MAO_OK) return st;
-  // 3. Cholesky QR, twice: P0 -> P1 -> P0 (+ Pw, caller's P)
+  // 3. Cholesky QR, twice: P0 -> P1 (fp32) -> Pw (bf16; + the caller's fp32 P)
   const int T = int(ceil_div(rank, 64));
-  const size_t chol_smem = chol_bytes(rank), trsm_smem = trsm_bytes(rank);
+  const size_t chol_smem = chol_bytes(rank);
+  const unsigned ctiles = unsigned(plan.ldr / 64);
   for (int pass = 0; pass < 2; ++pass) {
-    dion_gram_kernel<<<dim3(unsigned(T * (T + 1) / 2), unsigned(plan.max_gchunks), nb), 256, 0,
-                       stream>>>(c, pass);
+    profile_before_launch(stream, MAO_PROF_DION_GRAM);
+    dion_gram_kernel<<<dim3(unsigned(T * (T + 1) / 2), unsigned(plan.max_gchunks), nb),
+                       kGramThreads, 0, stream>>>(c, pass);
     if (!launched()) return MAO_ERR_CUDA;
+    profile_before_launch(stream, MAO_PROF_DION_CHOL);
     dion_chol_kernel<<<nb, kCholThreads, chol_smem, stream>>>(c);
     if (!launched()) return MAO_ERR_CUDA;
-    dion_trsm_kernel<<<dim3(unsigned(plan.max_rowtiles), nb), kTrsmThreads, trsm_smem, stream>>>(
+    profile_before_launch(stream, MAO_PROF_DION_TRMM);
+    dion_trmm_kernel<<<dim3(unsigned(plan.max_rowtiles) * ctiles, nb), kTrmmThreads, 0, stream>>>(
         c, pass);
     if (!launched()) return MAO_ERR_CUDA;
   }
@@ -733,10 +924,13 @@ mao_status dion_run(const mao_mat* X, const mao_mat* M, const mao_mat* G, const 
   st = dion_tc(plan, ws, c.tR, 1, 1.0f, stream);
   if (st != MAO_OK) return st;
   // 5. Q = ColumnNormalize(R) (caller's Q), bf16 copies of Q and R
+  profile_before_launch(stream, MAO_PROF_DION_NORM);
   dion_colnorm_kernel<<<dim3(unsigned(T), unsigned(plan.max_nchunks), nb), 256, 0, stream>>>(c);
   if (!launched()) return MAO_ERR_CUDA;
+  profile_before_launch(stream, MAO_PROF_DION_NORM);
   dion_norm_kernel<<<nb, 256, 0, stream>>>(c);
   if (!launched()) return MAO_ERR_CUDA;
+  profile_before_launch(stream, MAO_PROF_DION_NORM);
   dion_q_kernel<<<dim3(blocks(plan.max_qunits), nb), 256, 0, stream>>>(c);
   if (!launched()) return MAO_ERR_CUDA;
   // 6. M <- B - (1 - mu) P R^T ; X <- X - lr P Q^T (in place)

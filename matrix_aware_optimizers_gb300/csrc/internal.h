@@ -31,8 +31,9 @@ unsigned long long wait_limit_ns();
 
 // Launch accounting (every kernel launch of the library calls this once).
 void count_launch();
-// Optional timing of the tensor-core product launches (see mao_profile_begin).
-void profile_before_launch(cudaStream_t stream);
+// Optional timing of launches (see mao_profile_begin); tag 0 = tensor-core product kernel,
+// other tags name the Dion CUDA-core kernels (mao_profile_end_tagged).
+void profile_before_launch(cudaStream_t stream, int tag = 0);
 void profile_after_launch(cudaStream_t stream);
 
 // Reads and clears the device error word of the tensor-core kernels (after a stream sync).

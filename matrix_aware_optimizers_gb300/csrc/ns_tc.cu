@@ -461,6 +461,23 @@ __device__ __forceinline__ void store_final(const OutEntry& e, uint8_t* S, int i
   }
 }
 
+// In-place updates of bf16 rows with 16-byte accesses: the old values of a lane's 64
+// columns are loaded before the accumulator is ready (both of a warp's blocks at once, so
+// 8 KB per warp are in flight) and written back by update_final_pre.
+__device__ __forceinline__ bool update_vec_bf16(const OutEntry& e, int i, int jb, int M, int N) {
+  return (e.flags & OUT_VEC) && e.dtype == MAO_BF16 && i < M && jb + 64 <= N;
+}
+
+__device__ __forceinline__ void load_out_row(const OutEntry& e, int i, int jb, int M, int N,
+                                             uint4 (&r)[8]) {
+  if (update_vec_bf16(e, i, jb, M, N)) {
+    const uint4* g = reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(e.out) +
+                                                    int64_t(i) * e.ld + jb);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) r[k] = g[k];
+  }
+}
+
 // In-place update of the caller's matrix for this lane's row, columns jb..jb+63:
 // out = fmaf(alpha, acc, out) in fp32, rounded to out's dtype.
 __device__ __forceinline__ void update_final(const OutEntry& e, int i0, int jb, int M, int N,
@@ -503,6 +520,31 @@ __device__ __forceinline__ void update_final(const OutEntry& e, int i0, int jb, 
         store_elem(e.out, idx, e.dtype, __fmaf_rn(alpha, w[c], load_elem(e.out, idx, e.dtype)));
       }
     }
+  }
+}
+
+// update_final with the old values already in registers (load_out_row) where
+// update_vec_bf16 holds; otherwise the plain path.
+__device__ __forceinline__ void update_final_pre(const OutEntry& e, int i0, int jb, int M, int N,
+                                                 int lane, const float* w, float alpha,
+                                                 const uint4 (&r)[8]) {
+  const int i = i0 + lane;
+  if (!update_vec_bf16(e, i, jb, M, N)) {
+    update_final(e, i0, jb, M, N, lane, w, alpha);
+    return;
+  }
+  uint4* g = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(e.out) + int64_t(i) * e.ld + jb);
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    uint4 u = r[k];
+    uint32_t* h = reinterpret_cast<uint32_t*>(&u);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float lo = __uint_as_float(h[q] << 16), hi = __uint_as_float(h[q] & 0xFFFF0000u);
+      h[q] = pack_bf16x2(__fmaf_rn(alpha, w[8 * k + 2 * q], lo),
+                         __fmaf_rn(alpha, w[8 * k + 2 * q + 1], hi));
+    }
+    g[k] = u;
   }
 }
 
@@ -757,6 +799,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads(MODE), 1)
         if (part < nb) load_res_row(res, G.res_ld, i, t.col0 + 64 * part, G.M, res0);
         if (part + SPLIT < nb) load_res_row(res, G.res_ld, i, t.col0 + 64 * (part + SPLIT), G.M, res1);
       }
+      // TC_UPDATE: the old values of the caller's rows, likewise
+      if (STAGE == TC_UPDATE) {
+        static_assert(STAGE != TC_UPDATE || SPLIT == 2, "prefetch registers cover two blocks");
+        if (part < nb) load_out_row(oe, i, t.col0 + 64 * part, G.M, G.N, res0);
+        if (part + SPLIT < nb) load_out_row(oe, i, t.col0 + 64 * (part + SPLIT), G.M, G.N, res1);
+      }
 #ifdef MAO_TC_TRACE
       const long long tw2 = clock64();
 #endif
@@ -797,7 +845,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads(MODE), 1)
           for (int c = 0; c < 64; ++c) w[c] *= s;
         }
         if (STAGE == TC_UPDATE) {
-          update_final(oe, i0, jb, G.M, G.N, lane, w, p.a);
+          update_final_pre(oe, i0, jb, G.M, G.N, lane, w, p.a, nth == 0 ? res0 : res1);
         } else if (MODE == OUT_CALLER_BF16) {
           stage_rows(S, lane, w);
           __syncwarp();
