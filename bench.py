@@ -589,7 +589,7 @@ def main():
     # ---------------- timed region: K whole steps, inputs resident in HBM
     if wl.kind == "dion":  # every launch of the call: four products per round of shapes,
         # the set-up launches and the CUDA-core kernels
-        n_tc_per_step = 4 * ((len(set(wl.shapes)) + 7) // 8) + (len(wl.shapes) + 15) // 16 + 16
+        n_tc_per_step = 4 * ((len(set(wl.shapes)) + 7) // 8) + (len(wl.shapes) + 95) // 96 + 16
     elif block is not None:
         bshapes = {(min(block[0], R - i), min(block[1], C - j)) for R, C in set(wl.shapes)
                    for i in range(0, R, block[0]) for j in range(0, C, block[1])}

@@ -39,7 +39,7 @@ constexpr int kMaxRank = 256;
 constexpr int kGramRows = 512;    // rows of P summed by one partial Gram tile
 constexpr int kGramTilesMax = 10; // lower 64 x 64 tiles of an r x r Gram, r <= 256
 constexpr int kNormRows = 256;    // rows of R summed by one partial column norm
-constexpr int kSetup = 16;        // table entries written per set-up launch
+constexpr int kSetup = 96;        // table entries written per set-up launch (kernel parameters <= 32 KB)
 constexpr int kCholThreads = 512;
 
 // Everything the CUDA-core kernels need about one matrix slot.
@@ -61,6 +61,7 @@ struct DionSlot {
   int32_t flags_m, flags_x;
   int32_t gchunks, nchunks;         // partial Gram row chunks of P, partial norm chunks of R
   int32_t vec;                      // M and G: bf16/f32 rows that allow 16-byte accesses
+  int32_t qvec;                     // Q: 16-byte aligned rows (ldq a multiple of 4)
 };
 
 struct DionCommon {
@@ -69,22 +70,51 @@ struct DionCommon {
   int32_t r, ldr, count;
 };
 
+// A launch of the Gram or the triangular-multiply kernel covers the slots of up to
+// kLaunchGroups shape groups with exactly the CTAs they need: group g owns CTAs
+// [begin, begin + count * per_slot), per_slot CTAs for each of its slots slot0 .. .
+constexpr int kLaunchGroups = 16;
+struct DionLaunchGroup {
+  int32_t slot0, count, per_slot, begin;
+};
+struct DionGridParams {
+  DionCommon c;
+  DionLaunchGroup g[kLaunchGroups];
+  int32_t ng, pass;
+};
+
+// The slot and the CTA's index among the slot's CTAs.
+__device__ __forceinline__ void grid_slot(const DionGridParams& P, int& slot, int& local) {
+  int gi = 0;
+  while (gi + 1 < P.ng && P.g[gi + 1].begin <= int(blockIdx.x)) ++gi;
+  const DionLaunchGroup& g = P.g[gi];
+  const int k = int(blockIdx.x) - g.begin;
+  slot = g.slot0 + k / g.per_slot;
+  local = k - (k / g.per_slot) * g.per_slot;
+}
+
 struct SetupParams {
   DionSlot s[kSetup];
   int32_t n, z0;
   DionCommon c;
 };
+static_assert(sizeof(SetupParams) <= 32000, "set-up parameters exceed the kernel parameter limit");
 
 // ---------------------------------------------------------------- set-up
 
-// Thread k writes slot z0 + k of the device table and its four output entries.
-__global__ void dion_setup_kernel(const __grid_constant__ SetupParams p) {
-  const int k = threadIdx.x;
-  if (k >= p.n) return;
+// CTA k writes slot z0 + k of the device table (one 4-byte word per thread: the parameter
+// reads of a warp then differ only in the word, not the slot), zeroes the slot's Gram
+// counters and writes its four output entries.
+__global__ void __launch_bounds__(64) dion_setup_kernel(const __grid_constant__ SetupParams p) {
+  const int k = blockIdx.x;
   const DionSlot& e = p.s[k];
   const int z = p.z0 + k;
-  const_cast<DionSlot*>(p.c.slots)[z] = e;
-  for (int t = 0; t < 2 * kGramTilesMax; ++t) e.cnt[t] = 0;
+  static_assert(sizeof(DionSlot) % 4 == 0 && sizeof(DionSlot) / 4 <= 128, "slot copy by words");
+  const uint32_t* src = reinterpret_cast<const uint32_t*>(&e);
+  uint32_t* dst = reinterpret_cast<uint32_t*>(const_cast<DionSlot*>(p.c.slots) + z);
+  for (int w = threadIdx.x; w < int(sizeof(DionSlot) / 4); w += 64) dst[w] = src[w];
+  if (threadIdx.x < 2 * kGramTilesMax) e.cnt[threadIdx.x] = 0;
+  if (threadIdx.x != 0) return;
   OutEntry o;
   o.bits = nullptr;
   o.out = e.P0;
@@ -145,6 +175,41 @@ __global__ void __launch_bounds__(256) dion_stage_kernel(const __grid_constant__
   store8(e.Bw, row * e.ldn + col0, MAO_BF16, b);
 }
 
+// Columns j0 .. j0 + 7 of row i of the caller's Q (zeros at and past r), 16 bytes at a time
+// where the row allows it.
+__device__ __forceinline__ void load_q8(const DionSlot& e, int r, int64_t i, int j0, float (&v)[8]) {
+  const float* q = e.Q + i * e.ldq;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int j = j0 + 4 * h;
+    if (e.qvec && j + 4 <= r) {
+      const float4 x = *reinterpret_cast<const float4*>(q + j);
+      v[4 * h] = x.x;
+      v[4 * h + 1] = x.y;
+      v[4 * h + 2] = x.z;
+      v[4 * h + 3] = x.w;
+    } else {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) v[4 * h + k] = j + k < r ? q[j + k] : 0.0f;
+    }
+  }
+}
+
+__device__ __forceinline__ void store_q8(const DionSlot& e, int r, int64_t i, int j0, const float (&v)[8]) {
+  float* q = e.Q + i * e.ldq;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int j = j0 + 4 * h;
+    if (e.qvec && j + 4 <= r) {
+      *reinterpret_cast<float4*>(q + j) = make_float4(v[4 * h], v[4 * h + 1], v[4 * h + 2], v[4 * h + 3]);
+    } else {
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        if (j + k < r) q[j + k] = v[4 * h + k];
+    }
+  }
+}
+
 // Qw = bf16(Q_prev), zero-padded to ldr columns; blockIdx.y = slot.
 __global__ void __launch_bounds__(256) dion_stage_q_kernel(const __grid_constant__ DionCommon c) {
   const DionSlot& e = c.slots[blockIdx.y];
@@ -153,11 +218,7 @@ __global__ void __launch_bounds__(256) dion_stage_q_kernel(const __grid_constant
   if (u >= uint32_t(e.n) * upr) return;
   const uint32_t i = u / upr, j0 = (u - i * upr) * 8;
   float v[8];
-#pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    const int j = int(j0) + k;
-    v[k] = j < c.r ? e.Q[size_t(i) * e.ldq + j] : 0.0f;
-  }
+  load_q8(e, c.r, i, int(j0), v);
   store8(e.Qw, size_t(i) * c.ldr + j0, MAO_BF16, v);
 }
 
@@ -188,20 +249,23 @@ constexpr int kGramThreads = 64;
 // tile goes straight to Sf. Otherwise every CTA writes its partial tile, and the CTA that
 // arrives last at the tile's counter adds the partials in chunk order (a fixed order, so
 // the result does not depend on which CTA finishes last) and writes Sf.
-__global__ void __launch_bounds__(kGramThreads) dion_gram_kernel(const __grid_constant__ DionCommon c,
-                                                                 int pass) {
-  const DionSlot& e = c.slots[blockIdx.z];
+__global__ void __launch_bounds__(kGramThreads) dion_gram_kernel(const __grid_constant__ DionGridParams P) {
+  const DionCommon& c = P.c;
+  const int pass = P.pass;
+  int slot, local;
+  grid_slot(P, slot, local);
+  const DionSlot& e = c.slots[slot];
   const int gch = e.gchunks;
-  if (int(blockIdx.y) >= gch) return;
-  const int tile = int(blockIdx.x);
+  const int ntiles = (c.ldr / 64) * (c.ldr / 64 + 1) / 2;
+  const int tile = local % ntiles, chunk = local / ntiles;
   int ti = 0, t = tile;
   while (t > ti) { t -= ti + 1; ++ti; }
   const int tj = t;
   const bool diag = ti == tj;
   const int r = c.r, ldr = c.ldr;
-  const int64_t r0 = int64_t(blockIdx.y) * kGramRows;
+  const int64_t r0 = int64_t(chunk) * kGramRows;
   const int64_t r1 = min(int64_t(e.m), r0 + kGramRows);
-  const float* P = pass == 0 ? e.P0 : e.P1;
+  const float* Pm = pass == 0 ? e.P0 : e.P1;
 
   __shared__ __align__(16) float As[2][32][64], Bs[2][32][64];
   __shared__ int last;
@@ -214,7 +278,7 @@ __global__ void __launch_bounds__(kGramThreads) dion_gram_kernel(const __grid_co
       const int row = q >> 4, c4 = 4 * (q & 15);
       const int64_t g = k0 + row;
       const bool ok = g < r1;
-      const float* src = P + (ok ? g : r0) * ldr;
+      const float* src = Pm + (ok ? g : r0) * ldr;
       cp_async16(&As[buf][row][c4], src + ti * 64 + c4, ok ? bytes_before(ti * 64 + c4, r) : 0);
       if (!diag) cp_async16(&Bs[buf][row][c4], src + tj * 64 + c4, ok ? bytes_before(tj * 64 + c4, r) : 0);
     }
@@ -245,9 +309,8 @@ __global__ void __launch_bounds__(kGramThreads) dion_gram_kernel(const __grid_co
     }
     __syncthreads();
   }
-  const int ntiles = (ldr / 64) * (ldr / 64 + 1) / 2;
   float* dst = gch == 1 ? e.Sf + size_t(tile) * 4096
-                        : e.Sp + (size_t(blockIdx.y) * ntiles + tile) * 4096;
+                        : e.Sp + (size_t(chunk) * ntiles + tile) * 4096;
 #pragma unroll
   for (int x = 0; x < 8; ++x) {
     float* row = dst + (4 * ty + (x & 3) + 32 * (x >> 2)) * 64;
@@ -290,9 +353,10 @@ __device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast
 
 // Factors the 32 x 32 block Ad = L L^T in registers (lane = row; the diagonal pivot of step j
 // comes from lane j, the multipliers of rows k > j from lane k) and writes L back (zeros
-// above the diagonal). A pivot that is not positive is replaced by 1e-30 and reported.
-// Not inlined: inlined into the kernel, its a[] array lands in local memory.
-__device__ __noinline__ bool chol32(float* Ad, int lane) {
+// above the diagonal) and 1 / L_jj to rinv[j]. The pivot's reciprocal square root comes
+// from rsqrtf (L_jj = p rsqrt(p)). A pivot that is not positive is replaced by 1e-30 and
+// reported. Not inlined: inlined into the kernel, its a[] array lands in local memory.
+__device__ __noinline__ bool chol32(float* Ad, float* rinv, int lane) {
   float a[32];
 #pragma unroll
   for (int q = 0; q < 32; q += 4) {
@@ -303,6 +367,7 @@ __device__ __noinline__ bool chol32(float* Ad, int lane) {
     a[q + 3] = v.w;
   }
   bool bad = false;
+  float my_inv = 0.0f;
 #pragma unroll
   for (int j = 0; j < 32; ++j) {
     float p = __shfl_sync(0xFFFFFFFFu, a[j], j);
@@ -310,9 +375,9 @@ __device__ __noinline__ bool chol32(float* Ad, int lane) {
       bad = true;
       p = 1e-30f;
     }
-    const float ljj = sqrtf(p);
-    const float inv = 1.0f / ljj;
-    a[j] = lane == j ? ljj : (lane > j ? a[j] * inv : 0.0f);
+    const float inv = rsqrtf(p);
+    if (lane == j) my_inv = inv;
+    a[j] = lane == j ? p * inv : (lane > j ? a[j] * inv : 0.0f);
 #pragma unroll
     for (int k = j + 1; k < 32; ++k) {
       const float lkj = __shfl_sync(0xFFFFFFFFu, a[j], k);
@@ -321,14 +386,15 @@ __device__ __noinline__ bool chol32(float* Ad, int lane) {
   }
 #pragma unroll
   for (int q = 0; q < 32; ++q) Ad[lane * kLd + q] = q <= lane ? a[q] : 0.0f;
+  rinv[lane] = my_inv;
   __syncwarp();
   return bad;
 }
 
 // In place: the lower 32 x 32 block L becomes D = L^-1 (lane = column of D, forward
-// substitution in registers, four partial sums per dot product, the rows of L read 16 bytes
-// at a time); zeros above the diagonal.
-__device__ __forceinline__ void inv32(float* Ad, int lane) {
+// substitution in registers with the reciprocals rinv of L's diagonal, four partial sums per
+// dot product, the rows of L read 16 bytes at a time); zeros above the diagonal.
+__device__ __forceinline__ void inv32(float* Ad, const float* rinv, int lane) {
   float x[32];
 #pragma unroll
   for (int i = 0; i < 32; ++i) {
@@ -339,10 +405,10 @@ __device__ __forceinline__ void inv32(float* Ad, int lane) {
       const float lv[4] = {l.x, l.y, l.z, l.w};
 #pragma unroll
       for (int u = 0; u < 4; ++u)
-        if (k4 + u < i) s[u] = __fmaf_rn(lv[u], k4 + u >= lane ? x[k4 + u] : 0.0f, s[u]);
+        if (k4 + u < i) s[u] = __fmaf_rn(lv[u], x[k4 + u], s[u]);
     }
-    const float lii = Ad[i * kLd + i];
-    x[i] = i < lane ? 0.0f : (i == lane ? 1.0f / lii : -((s[0] + s[1]) + (s[2] + s[3])) / lii);
+    const float ri = rinv[i];
+    x[i] = i < lane ? 0.0f : (i == lane ? ri : -((s[0] + s[1]) + (s[2] + s[3])) * ri);
   }
   __syncwarp();
 #pragma unroll
@@ -352,11 +418,12 @@ __device__ __forceinline__ void inv32(float* Ad, int lane) {
 
 // One CTA per slot: S = L L^T (blocked right-looking Cholesky, 32 x 32 blocks in shared
 // memory), then W = L^-1, written to e.W ([ldr][ldr], zeros above the diagonal and past r).
-//   Cholesky, for each block column J: warp 0 factors the diagonal block (chol32) and
-//   inverts it in place (inv32: the diagonal block now holds D_J = L_JJ^-1, which is all
-//   that later steps need of it); the panel below becomes L_IJ = A_IJ D_J^T (one warp per
-//   row); the trailing lower blocks get A_IK -= L_IJ L_KJ^T (one warp per 8-row quarter of
-//   a block, the lane's row of L_KJ in registers).
+//   Cholesky, for each block column J: the panel below the diagonal becomes
+//   L_IJ = A_IJ D_J^T (one warp per row); block column J + 1 gets A_I,J+1 -= L_IJ L_J+1,J^T;
+//   then warp 0 factors the diagonal block J + 1 (chol32) and inverts it in place (inv32:
+//   the diagonal block then holds D = L_JJ^-1, which is all that later steps need of it)
+//   while the other warps update the remaining trailing blocks A_IK, J + 2 <= K <= I (one
+//   warp per 8-row quarter of a block, the lane's row of L_KJ in registers).
 //   Inverse, block row by block row (I = 1 .. nb - 1; W_JJ = D_J):
 //   T_J = sum_{K = J .. I-1} L_IK W_KJ for every J < I, then W_IJ = -D_I T_J in place of
 //   L_IJ (row block I of L is no longer needed once all T_J are formed).
@@ -364,6 +431,7 @@ __device__ __forceinline__ void inv32(float* Ad, int lane) {
 // error word (P had dependent columns).
 __global__ void __launch_bounds__(kCholThreads, 1) dion_chol_kernel(const __grid_constant__ DionCommon c) {
   extern __shared__ __align__(16) float sm[];
+  __shared__ float rinv[32];
   const DionSlot& e = c.slots[blockIdx.x];
   const int r = c.r, ldr = c.ldr;
   const int nb = (r + 31) / 32;
@@ -378,30 +446,49 @@ __global__ void __launch_bounds__(kCholThreads, 1) dion_chol_kernel(const __grid
     while (J > I) { J -= I + 1; ++I; }
     float* Ab = blk(A, I, J);
     const int k = 32 * J + lane;
-#pragma unroll 4
-    for (int ii0 = 0; ii0 < 32; ii0 += 8) {
-      float v[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int i = 32 * I + ii0 + u;
-        v[u] = i == k ? 1.0f : 0.0f;
-        if (i < r && k < r && k <= i) {
-          const int ti = i / 64, tk = k / 64;
-          v[u] = e.Sf[size_t(ti * (ti + 1) / 2 + tk) * 4096 + (i % 64) * 64 + (k % 64)];
-        }
-      }
-#pragma unroll
-      for (int u = 0; u < 8; ++u) Ab[(ii0 + u) * kLd + lane] = v[u];
+    const float* src = e.Sf + size_t((I / 2) * (I / 2 + 1) / 2 + J / 2) * 4096 + 32 * (I % 2) * 64 +
+                       32 * (J % 2) + lane;
+#pragma unroll 8
+    for (int ii = 0; ii < 32; ++ii) {
+      const int i = 32 * I + ii;
+      float v = i == k ? 1.0f : 0.0f;
+      if (i < r && k < r && k <= i) v = src[ii * 64];
+      Ab[ii * kLd + lane] = v;
     }
   }
+  // factors and inverts diagonal block J (warp 0)
+  auto factor = [&](int J) {
+    float* Dj = blk(A, J, J);
+    if (chol32(Dj, rinv, lane) && lane == 0) atomicOr(&g_dion_error, 1u);
+    inv32(Dj, rinv, lane);
+  };
+  // rows 8 quarter .. 8 quarter + 7 of A_IK -= L_IJ L_KJ^T
+  auto update = [&](int J, int I, int K, int quarter) {
+    float4 lk[8];
+    const float* Lk = blk(A, K, J) + lane * kLd;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) lk[q] = ld4(Lk + 4 * q);
+    const float* Li = blk(A, I, J) + quarter * 8 * kLd;
+    float* Ab = blk(A, I, K) + quarter * 8 * kLd;
+#pragma unroll
+    for (int tt = 0; tt < 8; ++tt) {
+      float s0 = 0.0f, s1 = 0.0f;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const float4 l = ld4(Li + tt * kLd + 4 * q);
+        s0 = __fmaf_rn(l.x, lk[q].x, s0);
+        s1 = __fmaf_rn(l.y, lk[q].y, s1);
+        s0 = __fmaf_rn(l.z, lk[q].z, s0);
+        s1 = __fmaf_rn(l.w, lk[q].w, s1);
+      }
+      Ab[tt * kLd + lane] -= s0 + s1;
+    }
+  };
+  __syncthreads();
+  if (warp == 0) factor(0);
   __syncthreads();
   for (int J = 0; J < nb; ++J) {
-    float* Dj = blk(A, J, J);
-    if (warp == 0) {
-      if (chol32(Dj, lane) && lane == 0) atomicOr(&g_dion_error, 1u);
-      inv32(Dj, lane);
-    }
-    __syncthreads();
+    const float* Dj = blk(A, J, J);
     for (int row = 32 * (J + 1) + warp; row < 32 * nb; row += kWarps) {
       float* Ap = blk(A, row / 32, J) + (row % 32) * kLd;
       float s0 = 0.0f, s1 = 0.0f;
@@ -417,31 +504,18 @@ __global__ void __launch_bounds__(kCholThreads, 1) dion_chol_kernel(const __grid
       Ap[lane] = s0 + s1;
     }
     __syncthreads();
-    const int t = nb - J - 1;
-    for (int item = warp; item < 2 * t * (t + 1); item += kWarps) {
-      const int quarter = item & 3;
-      int I = 0, K = item >> 2;
-      while (K > I) { K -= I + 1; ++I; }
-      I += J + 1;
-      K += J + 1;
-      float4 lk[8];
-      const float* Lk = blk(A, K, J) + lane * kLd;
-#pragma unroll
-      for (int q = 0; q < 8; ++q) lk[q] = ld4(Lk + 4 * q);
-      const float* Li = blk(A, I, J) + quarter * 8 * kLd;
-      float* Ab = blk(A, I, K) + quarter * 8 * kLd;
-#pragma unroll
-      for (int tt = 0; tt < 8; ++tt) {
-        float s0 = 0.0f, s1 = 0.0f;
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const float4 l = ld4(Li + tt * kLd + 4 * q);
-          s0 = __fmaf_rn(l.x, lk[q].x, s0);
-          s1 = __fmaf_rn(l.y, lk[q].y, s1);
-          s0 = __fmaf_rn(l.z, lk[q].z, s0);
-          s1 = __fmaf_rn(l.w, lk[q].w, s1);
-        }
-        Ab[tt * kLd + lane] -= s0 + s1;
+    if (J + 1 == nb) break;
+    for (int item = warp; item < 4 * (nb - 1 - J); item += kWarps)
+      update(J, J + 1 + (item >> 2), J + 1, item & 3);
+    __syncthreads();
+    if (warp == 0) {
+      factor(J + 1);
+    } else {
+      const int t2 = nb - J - 2;
+      for (int item = warp - 1; item < 2 * t2 * (t2 + 1); item += kWarps - 1) {
+        int I = 0, K = item >> 2;
+        while (K > I) { K -= I + 1; ++I; }
+        update(J, I + J + 2, K + J + 2, item & 3);
       }
     }
     __syncthreads();
@@ -498,12 +572,18 @@ __global__ void __launch_bounds__(kCholThreads, 1) dion_chol_kernel(const __grid
     }
     __syncthreads();
   }
-  // W to global memory: [ldr][ldr], zeros above the diagonal and past r
-  for (int q = threadIdx.x; q < ldr * ldr; q += kCholThreads) {
-    const int i = q / ldr, k = q - i * ldr;
-    float v = 0.0f;
-    if (i < r && k < r && k <= i) v = blk(A, i / 32, k / 32)[(i % 32) * kLd + (k % 32)];
-    e.W[q] = v;
+  // W to global memory: [ldr][ldr], zeros above the diagonal and past r; one warp per row,
+  // 16 bytes per lane
+  for (int i = warp; i < ldr; i += kWarps) {
+    for (int k4 = 4 * lane; k4 < ldr; k4 += 128) {
+      float v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int k = k4 + u;
+        v[u] = (i < r && k < r && k <= i) ? blk(A, i / 32, k / 32)[(i % 32) * kLd + (k % 32)] : 0.0f;
+      }
+      *reinterpret_cast<float4*>(e.W + size_t(i) * ldr + k4) = make_float4(v[0], v[1], v[2], v[3]);
+    }
   }
 }
 
@@ -515,14 +595,16 @@ __global__ void __launch_bounds__(kCholThreads, 1) dion_chol_kernel(const __grid
 // Pw (zeros up to ldr) and, if asked, the caller's fp32 copy of P.
 constexpr int kTrmmThreads = 64;
 
-__global__ void __launch_bounds__(kTrmmThreads) dion_trmm_kernel(const __grid_constant__ DionCommon c,
-                                                                 int pass) {
-  const DionSlot& e = c.slots[blockIdx.y];
+__global__ void __launch_bounds__(kTrmmThreads) dion_trmm_kernel(const __grid_constant__ DionGridParams P) {
+  const DionCommon& c = P.c;
+  const int pass = P.pass;
+  int slot, local;
+  grid_slot(P, slot, local);
+  const DionSlot& e = c.slots[slot];
   const int r = c.r, ldr = c.ldr;
   const int ctiles = ldr / 64;
-  const int64_t i0 = int64_t(blockIdx.x / ctiles) * 64;
-  if (i0 >= e.m) return;
-  const int j0 = int(blockIdx.x % ctiles) * 64;
+  const int64_t i0 = int64_t(local / ctiles) * 64;
+  const int j0 = int(local % ctiles) * 64;
   const int kend = min(r, j0 + 64);
   const float* Pin = pass == 0 ? e.P0 : e.P1;
 
@@ -552,7 +634,7 @@ __global__ void __launch_bounds__(kTrmmThreads) dion_trmm_kernel(const __grid_co
     __syncthreads();
     const float(*Ab)[36] = As[sl & 1];
     const float(*Bb)[36] = Bs[sl & 1];
-#pragma unroll 2
+#pragma unroll 1
     for (int kk = 0; kk < 32; kk += 4) {
       float4 a[8];
 #pragma unroll
@@ -592,60 +674,78 @@ __global__ void __launch_bounds__(kTrmmThreads) dion_trmm_kernel(const __grid_co
 // ------------------------------------------------------ R -> Q = ColumnNormalize(R)
 
 // Partial column sums of squares of R over rows [chunk*kNormRows, ...); grid
-// (ceil(r / 64), row chunks, slots); 4 row phases per column, summed in a fixed order.
+// (ceil(r / 64), row chunks, slots). Thread (phase, g) takes columns 4 g .. 4 g + 3 of the
+// block's 64 (16-byte loads) and rows phase, phase + 16, ...; the 16 phases are added in a
+// fixed order. Columns at or past r hold no data and are skipped.
 __global__ void __launch_bounds__(256) dion_colnorm_kernel(const __grid_constant__ DionCommon c) {
   const DionSlot& e = c.slots[blockIdx.z];
   if (int(blockIdx.y) >= e.nchunks) return;
-  const int cc = threadIdx.x & 63, phase = threadIdx.x >> 6;
-  const int j = int(blockIdx.x) * 64 + cc;
+  const int g = threadIdx.x & 15, phase = threadIdx.x >> 4;
+  const int j = int(blockIdx.x) * 64 + 4 * g;
   const int64_t r0 = int64_t(blockIdx.y) * kNormRows;
   const int64_t r1 = min(int64_t(e.n), r0 + kNormRows);
-  float s = 0.0f;
-  if (j < c.r)
-    for (int64_t i = r0 + phase; i < r1; i += 4) {
-      const float v = e.Rf[i * c.ldr + j];
-      s = __fmaf_rn(v, v, s);
+  float4 s = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+  if (j < c.r) {
+#pragma unroll 4
+    for (int64_t i = r0 + phase; i < r1; i += 16) {
+      const float4 v = *reinterpret_cast<const float4*>(e.Rf + i * c.ldr + j);
+      s.x = __fmaf_rn(v.x, v.x, s.x);
+      s.y = __fmaf_rn(v.y, v.y, s.y);
+      s.z = __fmaf_rn(v.z, v.z, s.z);
+      s.w = __fmaf_rn(v.w, v.w, s.w);
     }
-  __shared__ float part[4][64];
-  part[phase][cc] = s;
+  }
+  __shared__ float4 part[16][16];
+  part[phase][g] = s;
   __syncthreads();
-  if (phase == 0 && j < c.r)
-    e.cn[size_t(blockIdx.y) * c.r + j] = ((part[0][cc] + part[1][cc]) + part[2][cc]) + part[3][cc];
+  if (phase == 0) {
+    float4 t = part[0][g];
+#pragma unroll
+    for (int q = 1; q < 16; ++q) {
+      t.x += part[q][g].x;
+      t.y += part[q][g].y;
+      t.z += part[q][g].z;
+      t.w += part[q][g].w;
+    }
+    float* out = e.cn + size_t(blockIdx.y) * c.r;
+    const float tv[4] = {t.x, t.y, t.z, t.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      if (j + k < c.r) out[j + k] = tv[k];
+  }
 }
 
-// Column norms: the partial sums added in chunk order, square root; one block per slot.
-// The norms go after the partials (e.cn + nchunks * r).
+// Reciprocal column norms: the partial sums added in chunk order, then 1 / sqrt (0 for a
+// zero column); one block per slot. They go after the partials (e.cn + nchunks * r).
 __global__ void __launch_bounds__(256) dion_norm_kernel(const __grid_constant__ DionCommon c) {
   const DionSlot& e = c.slots[blockIdx.x];
   for (int j = threadIdx.x; j < c.r; j += blockDim.x) {
     float ss = 0.0f;
     for (int ch = 0; ch < e.nchunks; ++ch) ss += e.cn[size_t(ch) * c.r + j];
-    e.cn[size_t(e.nchunks) * c.r + j] = sqrtf(ss);
+    e.cn[size_t(e.nchunks) * c.r + j] = ss > 0.0f ? 1.0f / sqrtf(ss) : 0.0f;
   }
 }
 
-// Q = R / c (a zero column stays zero) into the caller's Q, and the bf16 copies Qw, Rw;
-// 8 columns per thread.
+// Q = R / ||R_:j|| (times the reciprocal norm; a zero column stays zero) into the caller's
+// Q, and the bf16 copies Qw, Rw; 8 columns per thread, 16-byte accesses.
 __global__ void __launch_bounds__(256) dion_q_kernel(const __grid_constant__ DionCommon c) {
   const DionSlot& e = c.slots[blockIdx.y];
   const uint32_t upr = uint32_t(c.ldr) / 8;
   const uint32_t u = blockIdx.x * blockDim.x + threadIdx.x;
   if (u >= uint32_t(e.n) * upr) return;
   const uint32_t i = u / upr, j0 = (u - i * upr) * 8;
-  const float* cn = e.cn + size_t(e.nchunks) * c.r;
+  const float* rn = e.cn + size_t(e.nchunks) * c.r;
+  const float4* rp = reinterpret_cast<const float4*>(e.Rf + size_t(i) * c.ldr + j0);
+  const float4 r0 = rp[0], r1 = rp[1];
+  const float raw[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
   float rv[8], qv[8];
 #pragma unroll
   for (int k = 0; k < 8; ++k) {
     const int j = int(j0) + k;
-    rv[k] = 0.0f;
-    qv[k] = 0.0f;
-    if (j < c.r) {
-      rv[k] = e.Rf[size_t(i) * c.ldr + j];
-      const float nrm = cn[j];
-      qv[k] = nrm > 0.0f ? rv[k] / nrm : 0.0f;
-      e.Q[size_t(i) * e.ldq + j] = qv[k];
-    }
+    rv[k] = j < c.r ? raw[k] : 0.0f;
+    qv[k] = j < c.r ? rv[k] * rn[j] : 0.0f;
   }
+  store_q8(e, c.r, i, int(j0), qv);
   store8(e.Qw, size_t(i) * c.ldr + j0, MAO_BF16, qv);
   store8(e.Rw, size_t(i) * c.ldr + j0, MAO_BF16, rv);
 }
@@ -663,7 +763,7 @@ struct DionPlan {
   std::vector<int> input_of;  // slot -> caller's index
   int64_t r = 0, ldr = 0;
   size_t off_slots = 0, off_tables = 0, total = 0;
-  int64_t max_units = 0, max_qunits = 0, max_rowtiles = 0, max_gchunks = 0, max_nchunks = 0;
+  int64_t max_units = 0, max_qunits = 0, max_nchunks = 0;
 };
 
 void make_dion_plan(const mao_mat* X, int32_t batch, int32_t rank, DionPlan& plan) {
@@ -718,8 +818,6 @@ void make_dion_plan(const mao_mat* X, int32_t batch, int32_t rank, DionPlan& pla
     slot += g.count;
     plan.max_units = std::max<int64_t>(plan.max_units, g.m * int64_t(ldn / 8));
     plan.max_qunits = std::max<int64_t>(plan.max_qunits, g.n * int64_t(ldr / 8));
-    plan.max_rowtiles = std::max<int64_t>(plan.max_rowtiles, ceil_div(g.m, 64));
-    plan.max_gchunks = std::max<int64_t>(plan.max_gchunks, int64_t(gch));
     plan.max_nchunks = std::max<int64_t>(plan.max_nchunks, int64_t(nch));
     plan.groups.push_back(g);
   }
@@ -878,6 +976,7 @@ mao_status dion_run(const mao_mat* X, const mao_mat* M, const mao_mat* G, const 
       e.flags_m = out_flags(M[b]);
       e.flags_x = out_flags(X[b]);
       e.vec = vec8_ok(M[b]) && vec8_ok(G[b]) ? 1 : 0;
+      e.qvec = (reinterpret_cast<uintptr_t>(Q[b].data) % 16 == 0 && Q[b].ld % 4 == 0) ? 1 : 0;
     }
   }
   for (int z0 = 0; z0 < batch; z0 += kSetup) {
@@ -888,7 +987,7 @@ mao_status dion_run(const mao_mat* X, const mao_mat* M, const mao_mat* G, const 
     sp.c = c;
     for (int k = 0; k < sp.n; ++k) sp.s[k] = slots[z0 + k];
     profile_before_launch(stream, MAO_PROF_DION_SETUP);
-    dion_setup_kernel<<<1, kSetup, 0, stream>>>(sp);
+    dion_setup_kernel<<<unsigned(sp.n), 64, 0, stream>>>(sp);
     if (!launched()) return MAO_ERR_CUDA;
   }
   const unsigned nb = unsigned(batch);
@@ -904,28 +1003,51 @@ mao_status dion_run(const mao_mat* X, const mao_mat* M, const mao_mat* G, const 
   mao_status st = dion_tc(plan, ws, c.tP, 0, 1.0f, stream);
   if (st != MAO_OK) return st;
   // 3. Cholesky QR, twice: P0 -> P1 (fp32) -> Pw (bf16; + the caller's fp32 P)
-  const int T = int(ceil_div(rank, 64));
   const size_t chol_smem = chol_bytes(rank);
-  const unsigned ctiles = unsigned(plan.ldr / 64);
+  const int ctiles = int(plan.ldr / 64);
+  const int ntiles = ctiles * (ctiles + 1) / 2;
+  // one launch per kLaunchGroups shape groups, exactly the CTAs the slots need
+  auto grid_launches = [&](bool gram, int pass) {
+    for (size_t g0 = 0; g0 < plan.groups.size(); g0 += kLaunchGroups) {
+      DionGridParams gp;
+      memset(&gp, 0, sizeof(gp));
+      gp.c = c;
+      gp.pass = pass;
+      int64_t ctas = 0;
+      for (size_t gi = g0; gi < plan.groups.size() && gp.ng < kLaunchGroups; ++gi) {
+        const DionGroup& g = plan.groups[gi];
+        DionLaunchGroup& lg = gp.g[gp.ng++];
+        lg.slot0 = g.slot0;
+        lg.count = g.count;
+        lg.per_slot = gram ? ntiles * int(ceil_div(g.m, kGramRows)) : int(ceil_div(g.m, 64)) * ctiles;
+        lg.begin = int32_t(ctas);
+        ctas += int64_t(lg.per_slot) * g.count;
+      }
+      if (ctas > 0x7FFFFFFF) return false;
+      if (gram) {
+        profile_before_launch(stream, MAO_PROF_DION_GRAM);
+        dion_gram_kernel<<<unsigned(ctas), kGramThreads, 0, stream>>>(gp);
+      } else {
+        profile_before_launch(stream, MAO_PROF_DION_TRMM);
+        dion_trmm_kernel<<<unsigned(ctas), kTrmmThreads, 0, stream>>>(gp);
+      }
+      if (!launched()) return false;
+    }
+    return true;
+  };
   for (int pass = 0; pass < 2; ++pass) {
-    profile_before_launch(stream, MAO_PROF_DION_GRAM);
-    dion_gram_kernel<<<dim3(unsigned(T * (T + 1) / 2), unsigned(plan.max_gchunks), nb),
-                       kGramThreads, 0, stream>>>(c, pass);
-    if (!launched()) return MAO_ERR_CUDA;
+    if (!grid_launches(true, pass)) return MAO_ERR_CUDA;
     profile_before_launch(stream, MAO_PROF_DION_CHOL);
     dion_chol_kernel<<<nb, kCholThreads, chol_smem, stream>>>(c);
     if (!launched()) return MAO_ERR_CUDA;
-    profile_before_launch(stream, MAO_PROF_DION_TRMM);
-    dion_trmm_kernel<<<dim3(unsigned(plan.max_rowtiles) * ctiles, nb), kTrmmThreads, 0, stream>>>(
-        c, pass);
-    if (!launched()) return MAO_ERR_CUDA;
+    if (!grid_launches(false, pass)) return MAO_ERR_CUDA;
   }
   // 4. R = B^T P (fp32)
   st = dion_tc(plan, ws, c.tR, 1, 1.0f, stream);
   if (st != MAO_OK) return st;
   // 5. Q = ColumnNormalize(R) (caller's Q), bf16 copies of Q and R
   profile_before_launch(stream, MAO_PROF_DION_NORM);
-  dion_colnorm_kernel<<<dim3(unsigned(T), unsigned(plan.max_nchunks), nb), 256, 0, stream>>>(c);
+  dion_colnorm_kernel<<<dim3(unsigned(ctiles), unsigned(plan.max_nchunks), nb), 256, 0, stream>>>(c);
   if (!launched()) return MAO_ERR_CUDA;
   profile_before_launch(stream, MAO_PROF_DION_NORM);
   dion_norm_kernel<<<nb, 256, 0, stream>>>(c);

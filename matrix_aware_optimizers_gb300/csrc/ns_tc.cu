@@ -461,21 +461,60 @@ __device__ __forceinline__ void store_final(const OutEntry& e, uint8_t* S, int i
   }
 }
 
-// In-place updates of bf16 rows with 16-byte accesses: the old values of a lane's 64
-// columns are loaded before the accumulator is ready (both of a warp's blocks at once, so
-// 8 KB per warp are in flight) and written back by update_final_pre.
-__device__ __forceinline__ bool update_vec_bf16(const OutEntry& e, int i, int jb, int M, int N) {
-  return (e.flags & OUT_VEC) && e.dtype == MAO_BF16 && i < M && jb + 64 <= N;
+// TC_UPDATE on bf16 rows with 16-byte accesses: a warp's block (32 rows x 64 columns) moves
+// between memory and registers in row-contiguous 128-byte pieces (8 lanes per row, four rows
+// per instruction: lane l holds 16-byte chunk l % 8 of rows l / 8 + 4 q). The old values are
+// loaded before the accumulator is ready; upd_apply turns them into the new values through
+// the warp's staging buffer (one row per lane for the arithmetic), and upd_store writes them
+// once the accumulator has been released.
+__device__ __forceinline__ bool upd_block_vec(const OutEntry& e, int jb, int N) {
+  return (e.flags & OUT_VEC) && e.dtype == MAO_BF16 && jb + 64 <= N;
 }
 
-__device__ __forceinline__ void load_out_row(const OutEntry& e, int i, int jb, int M, int N,
-                                             uint4 (&r)[8]) {
-  if (update_vec_bf16(e, i, jb, M, N)) {
-    const uint4* g = reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(e.out) +
-                                                    int64_t(i) * e.ld + jb);
+__device__ __forceinline__ void upd_load(const OutEntry& e, int i0, int jb, int M, int lane,
+                                         uint4 (&r)[8]) {
+  const __nv_bfloat16* base = reinterpret_cast<const __nv_bfloat16*>(e.out) + jb + 8 * (lane & 7);
 #pragma unroll
-    for (int k = 0; k < 8; ++k) r[k] = g[k];
+  for (int q = 0; q < 8; ++q) {
+    const int gi = i0 + (lane >> 3) + 4 * q;
+    if (gi < M) r[q] = *reinterpret_cast<const uint4*>(base + int64_t(gi) * e.ld);
   }
+}
+
+__device__ __forceinline__ void upd_store(const OutEntry& e, int i0, int jb, int M, int lane,
+                                          const uint4 (&r)[8]) {
+  __nv_bfloat16* base = reinterpret_cast<__nv_bfloat16*>(e.out) + jb + 8 * (lane & 7);
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const int gi = i0 + (lane >> 3) + 4 * q;
+    if (gi < M) *reinterpret_cast<uint4*>(base + int64_t(gi) * e.ld) = r[q];
+  }
+}
+
+// r (old values, chunk layout of upd_load) -> new values fmaf(alpha, acc, old) rounded to
+// bf16, same layout; w is this lane's row of the accumulator block.
+__device__ __forceinline__ void upd_apply(uint8_t* S, int lane, const float* w, float alpha,
+                                          uint4 (&r)[8]) {
+  const int sg = lane & 7;
+#pragma unroll
+  for (int q = 0; q < 8; ++q) *reinterpret_cast<uint4*>(S + srow((lane >> 3) + 4 * q, sg)) = r[q];
+  __syncwarp();
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    uint4 u = *reinterpret_cast<const uint4*>(S + srow(lane, k));
+    uint32_t* h = reinterpret_cast<uint32_t*>(&u);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float lo = __uint_as_float(h[q] << 16), hi = __uint_as_float(h[q] & 0xFFFF0000u);
+      h[q] = pack_bf16x2(__fmaf_rn(alpha, w[8 * k + 2 * q], lo),
+                         __fmaf_rn(alpha, w[8 * k + 2 * q + 1], hi));
+    }
+    *reinterpret_cast<uint4*>(S + srow(lane, k)) = u;
+  }
+  __syncwarp();
+#pragma unroll
+  for (int q = 0; q < 8; ++q) r[q] = *reinterpret_cast<const uint4*>(S + srow((lane >> 3) + 4 * q, sg));
+  __syncwarp();
 }
 
 // In-place update of the caller's matrix for this lane's row, columns jb..jb+63:
@@ -520,31 +559,6 @@ __device__ __forceinline__ void update_final(const OutEntry& e, int i0, int jb, 
         store_elem(e.out, idx, e.dtype, __fmaf_rn(alpha, w[c], load_elem(e.out, idx, e.dtype)));
       }
     }
-  }
-}
-
-// update_final with the old values already in registers (load_out_row) where
-// update_vec_bf16 holds; otherwise the plain path.
-__device__ __forceinline__ void update_final_pre(const OutEntry& e, int i0, int jb, int M, int N,
-                                                 int lane, const float* w, float alpha,
-                                                 const uint4 (&r)[8]) {
-  const int i = i0 + lane;
-  if (!update_vec_bf16(e, i, jb, M, N)) {
-    update_final(e, i0, jb, M, N, lane, w, alpha);
-    return;
-  }
-  uint4* g = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(e.out) + int64_t(i) * e.ld + jb);
-#pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    uint4 u = r[k];
-    uint32_t* h = reinterpret_cast<uint32_t*>(&u);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const float lo = __uint_as_float(h[q] << 16), hi = __uint_as_float(h[q] & 0xFFFF0000u);
-      h[q] = pack_bf16x2(__fmaf_rn(alpha, w[8 * k + 2 * q], lo),
-                         __fmaf_rn(alpha, w[8 * k + 2 * q + 1], hi));
-    }
-    g[k] = u;
   }
 }
 
@@ -802,8 +816,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads(MODE), 1)
       // TC_UPDATE: the old values of the caller's rows, likewise
       if (STAGE == TC_UPDATE) {
         static_assert(STAGE != TC_UPDATE || SPLIT == 2, "prefetch registers cover two blocks");
-        if (part < nb) load_out_row(oe, i, t.col0 + 64 * part, G.M, G.N, res0);
-        if (part + SPLIT < nb) load_out_row(oe, i, t.col0 + 64 * (part + SPLIT), G.M, G.N, res1);
+        const int jb0 = t.col0 + 64 * part, jb1 = t.col0 + 64 * (part + SPLIT);
+        if (part < nb && upd_block_vec(oe, jb0, G.N)) upd_load(oe, i0, jb0, G.M, lane, res0);
+        if (part + SPLIT < nb && upd_block_vec(oe, jb1, G.N)) upd_load(oe, i0, jb1, G.M, lane, res1);
       }
 #ifdef MAO_TC_TRACE
       const long long tw2 = clock64();
@@ -845,7 +860,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads(MODE), 1)
           for (int c = 0; c < 64; ++c) w[c] *= s;
         }
         if (STAGE == TC_UPDATE) {
-          update_final_pre(oe, i0, jb, G.M, G.N, lane, w, p.a, nth == 0 ? res0 : res1);
+          if (upd_block_vec(oe, jb, G.N)) upd_apply(S, lane, w, p.a, nth == 0 ? res0 : res1);
+          else update_final(oe, i0, jb, G.M, G.N, lane, w, p.a);
         } else if (MODE == OUT_CALLER_BF16) {
           stage_rows(S, lane, w);
           __syncwarp();
@@ -872,6 +888,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads(MODE), 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(tempty_leader[acc]);
+      // TC_UPDATE: the rows are written after the accumulator is released, so that the
+      // arrive (a release at cluster scope) does not wait for these stores
+      if (STAGE == TC_UPDATE) {
+        const int jb0 = t.col0 + 64 * part, jb1 = t.col0 + 64 * (part + SPLIT);
+        if (part < nb && upd_block_vec(oe, jb0, G.N)) upd_store(oe, i0, jb0, G.M, lane, res0);
+        if (part + SPLIT < nb && upd_block_vec(oe, jb1, G.N)) upd_store(oe, i0, jb1, G.M, lane, res1);
+      }
 #ifdef MAO_TC_TRACE
       if (lane == 0 && leader) {
         TRACE_ADD(4, tb);
