@@ -51,8 +51,8 @@ struct DionSlot {
   float* Pout;                      // optional copy of the final P (m x r, row stride r)
   __nv_bfloat16 *Bw, *Qw, *Rw, *Pw; // bf16 operands, rows of ldn / ldr elements
   float *P0, *P1, *Rf;              // fp32 [m|n][ldr]
-  float *Sp, *Sf;                   // partial Grams [gchunks][tiles][64 x 64]; final [tiles][64 x 64]
-  float* W;                         // L^-1 [ldr][ldr], zeros above the diagonal and past r
+  float *Sp, *Sf;                   // partial Grams [gchunks][tiles][64 x 64]; S in lower 32 x 32 blocks
+  float* W;                         // L^-1 in lower 32 x 32 blocks (layout of blk())
   float* cn;                        // column norms of R: partials [nchunks][r], then the norms
   int32_t* cnt;                     // arrival counters of the Gram tiles [2 passes][tiles]
   int64_t ldm, ldg, ldx, ldq;
@@ -224,6 +224,26 @@ __global__ void __launch_bounds__(256) dion_stage_q_kernel(const __grid_constant
 
 // ------------------------------------------------------- Cholesky QR: S = P^T P
 
+// Lower blocks of a matrix cut into 32 x 32 blocks, block (I, J) with I >= J at index
+// I (I + 1) / 2 + J, each block 32 rows of kLd = 36 floats: rows start on 16-byte
+// boundaries (broadcast row reads take 16 bytes at a time), a warp's column reads are
+// contiguous, and 16-byte row reads of a quarter warp (lane = row) fall on distinct banks.
+constexpr int kLd = 36;
+constexpr int kBlk = 32 * kLd;  // floats of one block
+
+__device__ __forceinline__ float* blk(float* A, int I, int J) {
+  return A + (I * (I + 1) / 2 + J) * kBlk;
+}
+
+__device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+
+// Address in the lower-block layout of element (row, col) (col a multiple of 4) of the
+// 64 x 64 Gram tile (ti, tj); null for the upper 32 x 32 block of a diagonal tile.
+__device__ __forceinline__ float* sf_at(float* Sf, int ti, int tj, int row, int col) {
+  const int I = 2 * ti + row / 32, J = 2 * tj + col / 32;
+  return I < J ? nullptr : blk(Sf, I, J) + (row % 32) * kLd + (col % 32);
+}
+
 // 16-byte asynchronous copy global -> shared (cp.async, L2 only); bytes past `src_bytes`
 // (0..16) are zero-filled and not read.
 __device__ __forceinline__ void cp_async16(void* dst, const void* src, int src_bytes) {
@@ -233,6 +253,13 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src, int src_b
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait1() { asm volatile("cp.async.wait_group 1;\n" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
+
+// Two floats rounded to bf16 (round to nearest even), the first in the low half.
+__device__ __forceinline__ uint32_t bf16_pair(float a, float b) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
 
 // Bytes of the 16-byte group of columns [c0, c0 + 4) of a row that lie before column r.
 __device__ __forceinline__ int bytes_before(int c0, int r) {
@@ -241,14 +268,15 @@ __device__ __forceinline__ int bytes_before(int c0, int r) {
 
 constexpr int kGramThreads = 64;
 
-// Lower 64 x 64 tile (ti >= tj) of S = P^T P; grid (tiles, row chunks, slots), 64 threads,
-// 8 x 8 outputs each (rows 4 ty + x and 32 + 4 ty + x, columns 4 tx + y and 32 + 4 tx + y,
-// so the row reads of a warp are contiguous). A CTA sums the kGramRows rows of its chunk
-// in 32-row slabs, double-buffered in shared memory by cp.async (columns past r and rows
-// past the chunk are zero-filled: P's columns past r are never written). With one chunk the
-// tile goes straight to Sf. Otherwise every CTA writes its partial tile, and the CTA that
-// arrives last at the tile's counter adds the partials in chunk order (a fixed order, so
-// the result does not depend on which CTA finishes last) and writes Sf.
+// Lower 64 x 64 tile (ti >= tj) of S = P^T P; one CTA per (tile, row chunk) of a slot
+// (DionGridParams), 64 threads, 8 x 8 outputs each (rows 4 ty + x and 32 + 4 ty + x,
+// columns 4 tx + y and 32 + 4 tx + y, so the row reads of a warp are contiguous). A CTA
+// sums the kGramRows rows of its chunk in 32-row slabs, double-buffered in shared memory by
+// cp.async (columns past r and rows past the chunk are zero-filled: P's columns past r are
+// never written). With one chunk the tile goes straight to Sf, in the lower-block layout of
+// the Cholesky kernel. Otherwise every CTA writes its partial tile, and the CTA that arrives
+// last at the tile's counter adds the partials in chunk order (a fixed order, so the result
+// does not depend on which CTA finishes last) and writes Sf.
 __global__ void __launch_bounds__(kGramThreads) dion_gram_kernel(const __grid_constant__ DionGridParams P) {
   const DionCommon& c = P.c;
   const int pass = P.pass;
@@ -309,15 +337,24 @@ __global__ void __launch_bounds__(kGramThreads) dion_gram_kernel(const __grid_co
     }
     __syncthreads();
   }
-  float* dst = gch == 1 ? e.Sf + size_t(tile) * 4096
-                        : e.Sp + (size_t(chunk) * ntiles + tile) * 4096;
+  if (gch == 1) {  // straight to Sf, in the lower-block layout of the Cholesky kernel
+#pragma unroll
+    for (int x = 0; x < 8; ++x) {
+      const int row = 4 * ty + (x & 3) + 32 * (x >> 2);
+      float* dst0 = sf_at(e.Sf, ti, tj, row, 4 * tx);
+      float* dst1 = sf_at(e.Sf, ti, tj, row, 32 + 4 * tx);
+      if (dst0) *reinterpret_cast<float4*>(dst0) = make_float4(acc[x][0], acc[x][1], acc[x][2], acc[x][3]);
+      if (dst1) *reinterpret_cast<float4*>(dst1) = make_float4(acc[x][4], acc[x][5], acc[x][6], acc[x][7]);
+    }
+    return;
+  }
+  float* dst = e.Sp + (size_t(chunk) * ntiles + tile) * 4096;
 #pragma unroll
   for (int x = 0; x < 8; ++x) {
     float* row = dst + (4 * ty + (x & 3) + 32 * (x >> 2)) * 64;
     *reinterpret_cast<float4*>(row + 4 * tx) = make_float4(acc[x][0], acc[x][1], acc[x][2], acc[x][3]);
     *reinterpret_cast<float4*>(row + 32 + 4 * tx) = make_float4(acc[x][4], acc[x][5], acc[x][6], acc[x][7]);
   }
-  if (gch == 1) return;
   __threadfence();
   __syncthreads();
   if (tid == 0) last = atomicAdd(&e.cnt[pass * kGramTilesMax + tile], 1) == gch - 1;
@@ -334,22 +371,10 @@ __global__ void __launch_bounds__(kGramThreads) dion_gram_kernel(const __grid_co
       s.z += v.z;
       s.w += v.w;
     }
-    reinterpret_cast<float4*>(e.Sf + size_t(tile) * 4096)[q] = s;
+    float* d = sf_at(e.Sf, ti, tj, q / 16, 4 * (q % 16));
+    if (d) *reinterpret_cast<float4*>(d) = s;
   }
 }
-
-// Lower blocks of a matrix cut into 32 x 32 blocks, block (I, J) with I >= J at index
-// I (I + 1) / 2 + J, each block 32 rows of kLd = 36 floats: rows start on 16-byte
-// boundaries (broadcast row reads take 16 bytes at a time), a warp's column reads are
-// contiguous, and 16-byte row reads of a quarter warp (lane = row) fall on distinct banks.
-constexpr int kLd = 36;
-constexpr int kBlk = 32 * kLd;  // floats of one block
-
-__device__ __forceinline__ float* blk(float* A, int I, int J) {
-  return A + (I * (I + 1) / 2 + J) * kBlk;
-}
-
-__device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
 
 // Factors the 32 x 32 block Ad = L L^T in registers (lane = row; the diagonal pivot of step j
 // comes from lane j, the multipliers of rows k > j from lane k) and writes L back (zeros
@@ -417,18 +442,20 @@ __device__ __forceinline__ void inv32(float* Ad, const float* rinv, int lane) {
 }
 
 // One CTA per slot: S = L L^T (blocked right-looking Cholesky, 32 x 32 blocks in shared
-// memory), then W = L^-1, written to e.W ([ldr][ldr], zeros above the diagonal and past r).
+// memory), then W = L^-1, written to e.W in the same lower-block layout.
 //   Cholesky, for each block column J: the panel below the diagonal becomes
 //   L_IJ = A_IJ D_J^T (one warp per row); block column J + 1 gets A_I,J+1 -= L_IJ L_J+1,J^T;
 //   then warp 0 factors the diagonal block J + 1 (chol32) and inverts it in place (inv32:
 //   the diagonal block then holds D = L_JJ^-1, which is all that later steps need of it)
-//   while the other warps update the remaining trailing blocks A_IK, J + 2 <= K <= I (one
-//   warp per 8-row quarter of a block, the lane's row of L_KJ in registers).
-//   Inverse, block row by block row (I = 1 .. nb - 1; W_JJ = D_J):
+//   while the warps off warp 0's sub-partition update the remaining trailing blocks A_IK,
+//   J + 2 <= K <= I (one warp per 8-row quarter of a block, the lane's row of L_KJ in
+//   registers) and take inverse step J.
+//   Inverse step I (block row I of W, once row block I of L and D_I are final; W_JJ = D_J):
 //   T_J = sum_{K = J .. I-1} L_IK W_KJ for every J < I, then W_IJ = -D_I T_J in place of
 //   L_IJ (row block I of L is no longer needed once all T_J are formed).
-// Rows and columns past r are the identity. A pivot that is not positive sets the device
-// error word (P had dependent columns).
+// S arrives in this block layout (the Gram kernel writes it so). Rows and columns past r are
+// the identity. A pivot that is not positive sets the device error word (P had dependent
+// columns).
 __global__ void __launch_bounds__(kCholThreads, 1) dion_chol_kernel(const __grid_constant__ DionCommon c) {
   extern __shared__ __align__(16) float sm[];
   __shared__ float rinv[32];
@@ -440,22 +467,16 @@ __global__ void __launch_bounds__(kCholThreads, 1) dion_chol_kernel(const __grid
   float* Tt = A + nlow * kBlk;    // nb - 1 blocks: T_J of the current block row
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   constexpr int kWarps = kCholThreads / 32;
-  // load the lower blocks from the 64 x 64 Gram tiles; identity past r
-  for (int b = warp; b < nlow; b += kWarps) {
-    int I = 0, J = b;
-    while (J > I) { J -= I + 1; ++I; }
-    float* Ab = blk(A, I, J);
-    const int k = 32 * J + lane;
-    const float* src = e.Sf + size_t((I / 2) * (I / 2 + 1) / 2 + J / 2) * 4096 + 32 * (I % 2) * 64 +
-                       32 * (J % 2) + lane;
-#pragma unroll 8
-    for (int ii = 0; ii < 32; ++ii) {
-      const int i = 32 * I + ii;
-      float v = i == k ? 1.0f : 0.0f;
-      if (i < r && k < r && k <= i) v = src[ii * 64];
-      Ab[ii * kLd + lane] = v;
-    }
-  }
+  constexpr int kHelpers = kWarps - kWarps / 4;  // warps with warp % 4 != 0
+  // the lower blocks of S (their Gram entries past r are zero), then ones on the diagonal
+  // past r
+  for (int q = threadIdx.x; q < nlow * kBlk / 4; q += kCholThreads)
+    cp_async16(A + 4 * q, e.Sf + 4 * q, 16);
+  cp_async_commit();
+  cp_async_wait_all();
+  __syncthreads();
+  for (int i = r + int(threadIdx.x); i < 32 * nb; i += kCholThreads)
+    blk(A, i / 32, i / 32)[(i % 32) * kLd + (i % 32)] = 1.0f;
   // factors and inverts diagonal block J (warp 0)
   auto factor = [&](int J) {
     float* Dj = blk(A, J, J);
@@ -484,6 +505,57 @@ __global__ void __launch_bounds__(kCholThreads, 1) dion_chol_kernel(const __grid
       Ab[tt * kLd + lane] -= s0 + s1;
     }
   };
+  // inverse step I on nw warps, this one numbered h; sync() separates its two phases
+  auto inverse_step = [&](int I, int h, int nw, auto sync) {
+    for (int item = h; item < 4 * I; item += nw) {
+      const int J = item >> 2, quarter = item & 3;
+      float acc[8] = {};
+      for (int K = J; K < I; ++K) {
+        const float* Wk = blk(A, K, J);  // W_KJ (D_J on the diagonal)
+        const float* Li = blk(A, I, K) + quarter * 8 * kLd;
+#pragma unroll 2
+        for (int q = 0; q < 32; q += 4) {
+          const float w0v = Wk[q * kLd + lane], w1v = Wk[(q + 1) * kLd + lane];
+          const float w2v = Wk[(q + 2) * kLd + lane], w3v = Wk[(q + 3) * kLd + lane];
+#pragma unroll
+          for (int tt = 0; tt < 8; ++tt) {
+            const float4 l = ld4(Li + tt * kLd + q);
+            acc[tt] = __fmaf_rn(l.x, w0v, acc[tt]);
+            acc[tt] = __fmaf_rn(l.y, w1v, acc[tt]);
+            acc[tt] = __fmaf_rn(l.z, w2v, acc[tt]);
+            acc[tt] = __fmaf_rn(l.w, w3v, acc[tt]);
+          }
+        }
+      }
+      float* T = Tt + J * kBlk + quarter * 8 * kLd;
+#pragma unroll
+      for (int tt = 0; tt < 8; ++tt) T[tt * kLd + lane] = acc[tt];
+    }
+    sync();
+    const float* Di = blk(A, I, I);
+    for (int item = h; item < 4 * I; item += nw) {
+      const int J = item >> 2, quarter = item & 3;
+      const float* T = Tt + J * kBlk;
+      const float* Dr = Di + quarter * 8 * kLd;
+      float acc[8] = {};
+#pragma unroll 2
+      for (int q = 0; q < 32; q += 4) {
+        const float t0 = T[q * kLd + lane], t1 = T[(q + 1) * kLd + lane];
+        const float t2 = T[(q + 2) * kLd + lane], t3 = T[(q + 3) * kLd + lane];
+#pragma unroll
+        for (int tt = 0; tt < 8; ++tt) {
+          const float4 d = ld4(Dr + tt * kLd + q);
+          acc[tt] = __fmaf_rn(d.x, t0, acc[tt]);
+          acc[tt] = __fmaf_rn(d.y, t1, acc[tt]);
+          acc[tt] = __fmaf_rn(d.z, t2, acc[tt]);
+          acc[tt] = __fmaf_rn(d.w, t3, acc[tt]);
+        }
+      }
+      float* Wb = blk(A, I, J) + quarter * 8 * kLd;
+#pragma unroll
+      for (int tt = 0; tt < 8; ++tt) Wb[tt * kLd + lane] = -acc[tt];
+    }
+  };
   __syncthreads();
   if (warp == 0) factor(0);
   __syncthreads();
@@ -510,88 +582,37 @@ __global__ void __launch_bounds__(kCholThreads, 1) dion_chol_kernel(const __grid
     __syncthreads();
     if (warp == 0) {
       factor(J + 1);
-    } else {
+    } else if (warp % 4 != 0) {
+      // the warps that do not share warp 0's sub-partition (warp w runs on sub-partition
+      // w % 4), numbered h = 0 .. kHelpers - 1
+      const int h = warp - warp / 4 - 1;
       const int t2 = nb - J - 2;
-      for (int item = warp - 1; item < 2 * t2 * (t2 + 1); item += kWarps - 1) {
+      for (int item = h; item < 2 * t2 * (t2 + 1); item += kHelpers) {
         int I = 0, K = item >> 2;
         while (K > I) { K -= I + 1; ++I; }
         update(J, I + J + 2, K + J + 2, item & 3);
       }
+      if (J >= 1)
+        inverse_step(J, h, kHelpers, [] {
+          asm volatile("bar.sync 1, %0;" ::"r"(32 * kHelpers) : "memory");
+        });
     }
     __syncthreads();
   }
-  // W = L^-1, block row by block row
-  for (int I = 1; I < nb; ++I) {
-    for (int item = warp; item < 4 * I; item += kWarps) {
-      const int J = item >> 2, quarter = item & 3;
-      float acc[8] = {};
-      for (int K = J; K < I; ++K) {
-        const float* Wk = blk(A, K, J);  // W_KJ (D_J on the diagonal)
-        const float* Li = blk(A, I, K) + quarter * 8 * kLd;
-#pragma unroll 2
-        for (int q = 0; q < 32; q += 4) {
-          const float w0 = Wk[q * kLd + lane], w1 = Wk[(q + 1) * kLd + lane];
-          const float w2 = Wk[(q + 2) * kLd + lane], w3 = Wk[(q + 3) * kLd + lane];
-#pragma unroll
-          for (int tt = 0; tt < 8; ++tt) {
-            const float4 l = ld4(Li + tt * kLd + q);
-            acc[tt] = __fmaf_rn(l.x, w0, acc[tt]);
-            acc[tt] = __fmaf_rn(l.y, w1, acc[tt]);
-            acc[tt] = __fmaf_rn(l.z, w2, acc[tt]);
-            acc[tt] = __fmaf_rn(l.w, w3, acc[tt]);
-          }
-        }
-      }
-      float* T = Tt + J * kBlk + quarter * 8 * kLd;
-#pragma unroll
-      for (int tt = 0; tt < 8; ++tt) T[tt * kLd + lane] = acc[tt];
-    }
-    __syncthreads();
-    const float* Di = blk(A, I, I);
-    for (int item = warp; item < 4 * I; item += kWarps) {
-      const int J = item >> 2, quarter = item & 3;
-      const float* T = Tt + J * kBlk;
-      const float* Dr = Di + quarter * 8 * kLd;
-      float acc[8] = {};
-#pragma unroll 2
-      for (int q = 0; q < 32; q += 4) {
-        const float t0 = T[q * kLd + lane], t1 = T[(q + 1) * kLd + lane];
-        const float t2 = T[(q + 2) * kLd + lane], t3 = T[(q + 3) * kLd + lane];
-#pragma unroll
-        for (int tt = 0; tt < 8; ++tt) {
-          const float4 d = ld4(Dr + tt * kLd + q);
-          acc[tt] = __fmaf_rn(d.x, t0, acc[tt]);
-          acc[tt] = __fmaf_rn(d.y, t1, acc[tt]);
-          acc[tt] = __fmaf_rn(d.z, t2, acc[tt]);
-          acc[tt] = __fmaf_rn(d.w, t3, acc[tt]);
-        }
-      }
-      float* Wb = blk(A, I, J) + quarter * 8 * kLd;
-#pragma unroll
-      for (int tt = 0; tt < 8; ++tt) Wb[tt * kLd + lane] = -acc[tt];
-    }
-    __syncthreads();
-  }
-  // W to global memory: [ldr][ldr], zeros above the diagonal and past r; one warp per row,
-  // 16 bytes per lane
-  for (int i = warp; i < ldr; i += kWarps) {
-    for (int k4 = 4 * lane; k4 < ldr; k4 += 128) {
-      float v[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int k = k4 + u;
-        v[u] = (i < r && k < r && k <= i) ? blk(A, i / 32, k / 32)[(i % 32) * kLd + (k % 32)] : 0.0f;
-      }
-      *reinterpret_cast<float4*>(e.W + size_t(i) * ldr + k4) = make_float4(v[0], v[1], v[2], v[3]);
-    }
-  }
+  if (nb >= 2) inverse_step(nb - 1, warp, kWarps, [] { __syncthreads(); });
+  __syncthreads();
+  // W to global memory in the same lower-block layout (zeros above the diagonal; the
+  // identity past r)
+  for (int q = threadIdx.x; q < nlow * kBlk / 4; q += kCholThreads)
+    reinterpret_cast<float4*>(e.W)[q] = reinterpret_cast<const float4*>(A)[q];
 }
 
 // Pout = Pin W^T (W = L^-1 lower triangular, so Pout[:, j] needs columns k <= j of Pin).
-// grid (row tiles x column tiles of 64, slots), 64 threads, 8 x 8 outputs each: rows
-// rg + 8 x and columns tx + 8 y. Both operands sit in shared memory with k contiguous (rows
-// of 36 floats, double-buffered by cp.async), so every 16-byte read of a quarter warp falls
-// on distinct banks. Pass 0 writes P1 (fp32, zeros past r); pass 1 writes the bf16 operand
+// One CTA per 64 x 64 output tile (row tile, column tile) of a slot (DionGridParams), 64
+// threads, 8 x 8 outputs each: rows rg + 8 x and columns tx + 8 y. Both operands sit in
+// shared memory with k contiguous (rows of 36 floats, double-buffered by cp.async), so every
+// 16-byte read of a quarter warp falls on distinct banks; W comes from its lower-block
+// layout (blocks above the diagonal read as zeros). Pass 0 writes P1 (fp32, zeros past r); pass 1 writes the bf16 operand
 // Pw (zeros up to ldr) and, if asked, the caller's fp32 copy of P.
 constexpr int kTrmmThreads = 64;
 
@@ -606,21 +627,29 @@ __global__ void __launch_bounds__(kTrmmThreads) dion_trmm_kernel(const __grid_co
   const int64_t i0 = int64_t(local / ctiles) * 64;
   const int j0 = int(local % ctiles) * 64;
   const int kend = min(r, j0 + 64);
+  const int nbw = (r + 31) / 32;  // block rows of W
   const float* Pin = pass == 0 ? e.P0 : e.P1;
 
   __shared__ __align__(16) float As[2][64][36], Bs[2][64][36];
   const int tid = threadIdx.x;
   const int tx = tid & 7, rg = tid >> 3;
+  // thread -> rows lr + 8 h of the slab (h = 0 .. 7), k columns k4 .. k4 + 3; rows 0 .. 31
+  // of the W tile lie in block row jb0, rows 32 .. 63 in jb0 + 1
+  const int lr = tid >> 3, k4 = 4 * (tid & 7);
+  const int jb0 = j0 / 32;
   auto issue = [&](int k0, int buf) {
+    const int kb = k0 / 32;
 #pragma unroll
     for (int h = 0; h < 8; ++h) {
-      const int q = tid + kTrmmThreads * h;
-      const int row = q >> 3, k4 = 4 * (q & 7);
+      const int row = lr + 8 * h;
       const int64_t g = i0 + row;
       const bool ok = g < e.m;
       cp_async16(&As[buf][row][k4], Pin + (ok ? g : i0) * ldr + k0 + k4,
                  ok ? bytes_before(k0 + k4, r) : 0);
-      cp_async16(&Bs[buf][row][k4], e.W + size_t(j0 + row) * ldr + k0 + k4, 16);
+      const int jb = jb0 + (h >= 4 ? 1 : 0);
+      const bool wok = jb < nbw && kb <= jb;  // a stored block (else zeros)
+      cp_async16(&Bs[buf][row][k4], wok ? blk(e.W, jb, kb) + (row & 31) * kLd + k4 : e.W,
+                 wok ? 16 : 0);
     }
     cp_async_commit();
   };
@@ -653,19 +682,41 @@ __global__ void __launch_bounds__(kTrmmThreads) dion_trmm_kernel(const __grid_co
     }
     __syncthreads();
   }
+  // the tile goes through shared memory (64 rows of 68 floats) so that every row is
+  // written with 16-byte stores
+  float(*Ct)[68] = reinterpret_cast<float(*)[68]>(&As[0][0][0]);
+  static_assert(sizeof(As) >= 64 * 68 * sizeof(float), "output tile fits in the operand buffers");
 #pragma unroll
-  for (int x = 0; x < 8; ++x) {
-    const int64_t row = i0 + rg + 8 * x;
+  for (int x = 0; x < 8; ++x)
+#pragma unroll
+    for (int y = 0; y < 8; ++y) Ct[rg + 8 * x][tx + 8 * y] = j0 + tx + 8 * y < r ? acc[x][y] : 0.0f;
+  __syncthreads();
+  // thread -> rows lr + 8 h, columns k4 .. k4 + 3 and 32 + k4 .. 32 + k4 + 3
+  const bool pvec = e.Pout && (reinterpret_cast<uintptr_t>(e.Pout) % 16 == 0) && (r % 4 == 0);
+#pragma unroll
+  for (int h = 0; h < 8; ++h) {
+    const int rr = lr + 8 * h;
+    const int64_t row = i0 + rr;
     if (row >= e.m) continue;
 #pragma unroll
-    for (int y = 0; y < 8; ++y) {
-      const int j = j0 + tx + 8 * y;
-      const float v = j < r ? acc[x][y] : 0.0f;
+    for (int half = 0; half < 2; ++half) {
+      const int cc = 32 * half + k4;
+      const int j = j0 + cc;
+      const float4 v = *reinterpret_cast<const float4*>(&Ct[rr][cc]);
       if (pass == 0) {
-        e.P1[row * ldr + j] = v;
+        *reinterpret_cast<float4*>(e.P1 + row * ldr + j) = v;
       } else {
-        e.Pw[row * ldr + j] = __float2bfloat16_rn(v);
-        if (e.Pout && j < r) e.Pout[row * r + j] = v;
+        *reinterpret_cast<uint2*>(e.Pw + row * ldr + j) = make_uint2(bf16_pair(v.x, v.y), bf16_pair(v.z, v.w));
+        if (e.Pout) {
+          if (pvec && j + 4 <= r) {
+            *reinterpret_cast<float4*>(e.Pout + row * r + j) = v;
+          } else {
+            const float vv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+              if (j + u < r) e.Pout[row * r + j + u] = vv[u];
+          }
+        }
       }
     }
   }
@@ -810,8 +861,10 @@ void make_dion_plan(const mao_mat* X, int32_t batch, int32_t rank, DionPlan& pla
     g.off_rf = take(c * n * ldr * 4);
     const size_t ntiles = (ldr / 64) * (ldr / 64 + 1) / 2;
     g.off_sp = take(gch > 1 ? c * gch * ntiles * 4096 * 4 : 0);
-    g.off_sf = take(c * ntiles * 4096 * 4);
-    g.off_w = take(c * ldr * ldr * 4);
+    const size_t nsb = (ldr / 32) * (ldr / 32 + 1) / 2;  // lower 32 x 32 blocks of S
+    g.off_sf = take(c * nsb * kBlk * 4);
+    const size_t nbw = size_t(ceil_div(rank, 32));
+    g.off_w = take(c * nbw * (nbw + 1) / 2 * kBlk * 4);
     g.off_cnt = take(c * 2 * kGramTilesMax * 4);
     g.off_cn = take(c * (nch + 1) * r * 4);
     for (int b : mem) plan.input_of.push_back(b);
@@ -959,8 +1012,10 @@ mao_status dion_run(const mao_mat* X, const mao_mat* M, const mao_mat* G, const 
       const size_t ntiles = size_t(plan.ldr / 64) * size_t(plan.ldr / 64 + 1) / 2;
       e.Sp = e.gchunks > 1 ? reinterpret_cast<float*>(ws + g.off_sp) + size_t(k) * e.gchunks * ntiles * 4096
                            : nullptr;
-      e.Sf = reinterpret_cast<float*>(ws + g.off_sf) + size_t(k) * ntiles * 4096;
-      e.W = reinterpret_cast<float*>(ws + g.off_w) + size_t(k) * plan.ldr * plan.ldr;
+      const size_t nsb = size_t(plan.ldr / 32) * size_t(plan.ldr / 32 + 1) / 2;
+      e.Sf = reinterpret_cast<float*>(ws + g.off_sf) + size_t(k) * nsb * kBlk;
+      const size_t nbw = size_t(ceil_div(rank, 32));
+      e.W = reinterpret_cast<float*>(ws + g.off_w) + size_t(k) * nbw * (nbw + 1) / 2 * kBlk;
       e.cnt = reinterpret_cast<int32_t*>(ws + g.off_cnt) + size_t(k) * 2 * kGramTilesMax;
       e.cn = reinterpret_cast<float*>(ws + g.off_cn) + size_t(k) * (e.nchunks + 1) * rank;
       e.ldm = M[b].ld;
