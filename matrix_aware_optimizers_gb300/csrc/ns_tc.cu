@@ -106,9 +106,12 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
                : "memory");
 }
 
+// Arrive on a barrier of the leader CTA. The signal it carries (this warp's TMEM reads are
+// done) is ordered by tcgen05.fence::before_thread_sync, not by the arrive's memory
+// semantics, so the arrive keeps the default CTA-scope release: a cluster-scope release
+// would also wait for this thread's earlier global stores.
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
-               : "memory");
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
