@@ -59,6 +59,9 @@ def parse_args():
     ap.add_argument("--graph", action="store_true",
                     help="time replays of one captured CUDA graph of the step (the library's "
                          "calls are capture-safe)")
+    ap.add_argument("--unfused", action="store_true",
+                    help="Muon workloads: momentum, Newton-Schulz and update as three calls "
+                         "instead of one muon_step call")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
@@ -154,9 +157,12 @@ class ClockSampler:
 class Step:
     """Device buffers and the sequence of C-ABI calls of one optimizer step."""
 
-    def __init__(self, wl, inputs, device, variant="bits", post_polar=False, block=None):
+    def __init__(self, wl, inputs, device, variant="bits", post_polar=False, block=None,
+                 fused=True):
         """variant: "bits" (1-bit all-gather) or "int8" (integer SUM all-reduce) aggregation
-        of a Sign-Muon workload; post_polar: the optional Newton–Schulz step on S_bar."""
+        of a Sign-Muon workload; post_polar: the optional Newton–Schulz step on S_bar;
+        fused: a Muon workload on the tensor cores runs as one muon_step call (momentum in
+        the staging pass, the update in the last product) instead of the three calls."""
         import torch
         import matrix_aware_optimizers_gb300 as mao
         if wl.kind != "sign" and (variant != "bits" or post_polar):
@@ -169,6 +175,7 @@ class Step:
         self.wl = wl
         self.variant, self.post_polar = variant, post_polar
         self.block = block
+        self.fused = fused and wl.kind == "muon" and block is None and wl.compute == "bf16"
         self.W, self.M, self.G = inputs["W"], inputs["M"], inputs["G"]
         self.dev = device
         if wl.kind == "dion":
@@ -196,8 +203,10 @@ class Step:
                 self.sbar = torch.zeros(self.nbits, dtype=torch.int8, device=device)
             if post_polar:
                 self.U_bar = torch.empty_like(self.W[0])
-        else:
+        elif not self.fused:
             self.U = [torch.empty_like(w) for w in self.W]
+        else:
+            self.U = []
         if block is not None:
             n = mao.ns_blockwise_workspace_bytes(self.M, block, wl.compute)
             self.ws = torch.empty(n, dtype=torch.uint8, device=device)
@@ -250,6 +259,11 @@ class Step:
             self.mao.apply_update(self.W, wl.lr, vote=self.vote)
 
     def __call__(self):
+        if self.fused:
+            wl = self.wl
+            self.mao.muon_step(self.W, self.M, self.G, wl.mu, wl.lr, wl.steps, wl.coeffs, wl.eps,
+                               wl.compute, ws=self.ws)
+            return
         self.momentum()
         self.ns()
         self.update()
@@ -558,7 +572,7 @@ def main():
     K = args.steps if args.steps is not None else DEFAULT_STEPS[wl.index]
     Wu = max(3, args.warmup if args.warmup is not None else DEFAULT_WARMUP[wl.index])
     inputs = workloads.generate(wl, dev, seed=(wl.index - 1) + 1000 * rank)
-    step = Step(wl, inputs, dev, args.variant, args.post_polar, block)
+    step = Step(wl, inputs, dev, args.variant, args.post_polar, block, fused=not args.unfused)
     stream = torch.cuda.current_stream()
 
     def barrier():
@@ -640,19 +654,32 @@ def main():
 
     # ---------------- per-stage times (separate pass, same stream)
     reps = max(3, min(K, 50))
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(reps)]
-    for r in range(reps):
-        ev[r][0].record(stream)
-        step.momentum()
-        ev[r][1].record(stream)
-        step.ns()
-        ev[r][2].record(stream)
-        step.update()
-        ev[r][3].record(stream)
-    torch.cuda.synchronize()
-    st_mom = statistics.median(e[0].elapsed_time(e[1]) for e in ev)
-    st_ns = statistics.median(e[1].elapsed_time(e[2]) for e in ev)
-    st_upd = statistics.median(e[2].elapsed_time(e[3]) for e in ev)
+    if step.fused:
+        # one call: the Newton–Schulz share is the tensor-core launches' time from the pass
+        # above (the momentum rides on the staging pass, the update on the last product)
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(reps)]
+        for r in range(reps):
+            ev[r][0].record(stream)
+            step()
+            ev[r][1].record(stream)
+        torch.cuda.synchronize()
+        st_step = statistics.median(e[0].elapsed_time(e[1]) for e in ev)
+        st_mom = st_upd = None
+        st_ns = sum(tc_ms) / reps_tc
+    else:
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(reps)]
+        for r in range(reps):
+            ev[r][0].record(stream)
+            step.momentum()
+            ev[r][1].record(stream)
+            step.ns()
+            ev[r][2].record(stream)
+            step.update()
+            ev[r][3].record(stream)
+        torch.cuda.synchronize()
+        st_mom = statistics.median(e[0].elapsed_time(e[1]) for e in ev)
+        st_ns = statistics.median(e[1].elapsed_time(e[2]) for e in ev)
+        st_upd = statistics.median(e[2].elapsed_time(e[3]) for e in ev)
 
     peaks, peak_src = load_peaks()
     if wl.kind == "dion":
@@ -694,10 +721,18 @@ def main():
         roof = {"kernel": "elementwise stages", "bound": "hbm", "achieved": gbs, "peak": hbm,
                 "unit": "GB/s", "frac": gbs / hbm, "traffic": None,
                 "peak_source": "%s hbm_gbs" % peak_src}
-    mom_b, upd_b = stage_bytes(wl, step)
     hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
     touched = sum(m.numel() * esize(m.dtype) for m in step.M) * 2 + \
         sum(w.numel() * esize(w.dtype) for w in step.W) * 2
+    if step.fused:
+        stages = {"muon_step": st_step, "ns_tc_launches": st_ns}
+        ew_gbs = {"momentum": None, "update": None, "peak": hbm,
+                  "fused": "momentum in the staging pass, update in the last product"}
+    else:
+        mom_b, upd_b = stage_bytes(wl, step)
+        stages = {"momentum": st_mom, "ns": st_ns, "update": st_upd}
+        ew_gbs = {"momentum": mom_b / (st_mom / 1000.0) / 1e9,
+                  "update": upd_b / (st_upd / 1000.0) / 1e9 if upd_b else None, "peak": hbm}
 
     line = {
         "metric": metric_name(wl), "value": value, "unit": "steps/s", "n_gpus": world,
@@ -705,13 +740,13 @@ def main():
         "scaling": "weak", "vs_baseline": None, "dtype": wl.compute, "data": "synthetic",
         "config": dict(config_block(wl, touched, args.variant, args.post_polar),
                        launch="CUDA graph replay" if args.graph else "eager",
+                       **({"step_call": "muon_step (momentum, Newton-Schulz and update in one "
+                                        "call)"} if step.fused else {}),
                        **({"blockwise": "%dx%d blocks" % block} if block else {})),
         "ns_tflops_dense": dense / (st_ns / 1000.0) / 1e12,
         "ns_tflops_alg": alg / (st_ns / 1000.0) / 1e12,
-        "stages_ms": {"momentum": st_mom, "ns": st_ns, "update": st_upd},
-        "elementwise_gbs": {"momentum": mom_b / (st_mom / 1000.0) / 1e9,
-                            "update": upd_b / (st_upd / 1000.0) / 1e9 if upd_b else None,
-                            "peak": hbm},
+        "stages_ms": stages,
+        "elementwise_gbs": ew_gbs,
         "roofline": roof,
         "gpu_launches": launches,
         "clocks": clk,
@@ -799,7 +834,10 @@ def run_e2e(step, K, world, dev, barrier, max_over_ranks):
     Copies run on their own streams and overlap other work where the data allow it: the
     gradients of step k+1 go into the second of two device slabs while step k computes, and
     the weights of step k are read back while step k+1 runs its momentum and Newton–Schulz
-    stages (its update waits for that read). Every step still moves all of its bytes.
+    stages (its update waits for that read). A fused Muon step updates W inside its one call:
+    its W is first copied to a second device slab, and the read-back drains that copy while
+    the next step runs (the device copy is part of the timed step). Every step still moves
+    all of its bytes.
     """
     import torch
     main = torch.cuda.current_stream()
@@ -811,7 +849,9 @@ def run_e2e(step, K, world, dev, barrier, max_over_ranks):
     W_dev, W_views = _slab(step.W, dev)
     G_orig, W_orig = step.G, step.W
     step.W = W_views
-    staged = step.wl.kind != "dion"  # Dion updates W inside its one call
+    fused = getattr(step, "fused", False)
+    staged = step.wl.kind != "dion" and not fused  # Dion and muon_step update W in one call
+    W_snap = torch.empty_like(W_dev) if fused else W_dev
     h2d = G_host.numel() * G_host.element_size()
     d2h = W_host.numel() * W_host.element_size()
     s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
@@ -840,6 +880,11 @@ def run_e2e(step, K, world, dev, barrier, max_over_ranks):
             step.ns()
             main.wait_event(w_read)           # the previous read-back of W is complete
             step.update()
+        elif fused:
+            step()
+            g_free[b].record(main)
+            main.wait_event(w_read)           # the previous read-back is done with the copy
+            W_snap.copy_(W_dev)
         else:
             main.wait_event(w_read)
             step()
@@ -847,7 +892,7 @@ def run_e2e(step, K, world, dev, barrier, max_over_ranks):
         w_done.record(main)
         s_out.wait_event(w_done)
         with torch.cuda.stream(s_out):
-            W_host.copy_(W_dev, non_blocking=True)
+            W_host.copy_(W_snap, non_blocking=True)
         w_read.record(s_out)
     main.wait_event(w_read)
     e1.record(main)
@@ -860,7 +905,8 @@ def run_e2e(step, K, world, dev, barrier, max_over_ranks):
     return {"value": job_throughput(ms, K, world), "unit": "steps/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": K,
             "copies": "one pinned H2D slab and one D2H slab per step, on copy streams overlapping "
-                      "the neighbouring steps' compute"}
+                      "the neighbouring steps' compute" +
+                      ("; W copied to a device slab first (fused step)" if fused else "")}
 
 
 def read_traffic(wl):

@@ -145,6 +145,31 @@ mao_status ns_orthogonalize(const mao_mat* in, const mao_mat* out, int32_t batch
                             int32_t compute, uint32_t* const* sign_bits, void* workspace,
                             size_t workspace_bytes, void* stream);
 
+/*
+ * One whole Muon step in one call ([Dion] ablation section for the heavy-ball momentum
+ * M <- mu M + G; [SignMuon] §2 "Fluxo Algorítmico" for the polar factor of the momentum and
+ * the update W <- W - eta U): for each matrix
+ *   M <- fmaf(mu, M, G)       rounded to M's dtype, written back
+ *   U  = Newton–Schulz(M)     exactly as ns_orthogonalize with compute = MAO_BF16
+ *   W <- fmaf(-lr, U, W)      rounded to W's dtype
+ * The momentum is applied by the staging pass that copies M into the workspace, and the
+ * last product updates W in its epilogue: U is never stored, and W's update uses U's fp32
+ * values (the composed calls round U to the caller's U buffer first).
+ *
+ *   W, M, G      f32 or bf16 matrices of equal shape per entry (M and G also as for
+ *                muon_momentum_update); W and M are updated in place. No two of W[b], M[b],
+ *                G[b] may overlap.
+ *   mu, lr       finite; steps, coeffs, coeff_stride, eps as for ns_orthogonalize.
+ *   compute      MAO_BF16 (tensor cores) only; MAO_F32 returns MAO_ERR_UNSUPPORTED.
+ *   workspace    >= ns_workspace_bytes(M, batch, MAO_BF16) bytes, 256-byte aligned.
+ * Errors: as ns_orthogonalize (argument checks before any launch; device time-outs through
+ * mao_sync_status).
+ */
+mao_status muon_step(const mao_mat* W, const mao_mat* M, const mao_mat* G, int32_t batch,
+                     float mu, float lr, int32_t steps, const float* coeffs,
+                     int32_t coeff_stride, float eps, int32_t compute, void* workspace,
+                     size_t workspace_bytes, void* stream);
+
 /* Size of the scratch area ns_orthogonalize_noalloc uses (16 MiB per device). */
 #define MAO_NOALLOC_WORKSPACE_BYTES (16u * 1024u * 1024u)
 

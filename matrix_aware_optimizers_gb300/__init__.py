@@ -8,6 +8,7 @@ Functions (same names as the C ABI):
   muon_momentum_update(M, G, mu)                     M <- mu*M + G
   ns_workspace_bytes(X, compute)                     workspace size for ns_orthogonalize
   ns_orthogonalize(inp, out, steps, coeffs, ...)     Newton–Schulz polar factor (+ packed signs)
+  muon_step(W, M, G, mu, lr, ...)                    momentum + Newton–Schulz + update, fused
   ns_orthogonalize_blockwise(inp, out, block, ...)   Newton–Schulz of every block on its own
   sign_pack_bits(U, bits)                            sign + 1-bit pack
   majority_vote_packed(bits, nbits, vote)            vote over workers' packed signs
@@ -140,6 +141,25 @@ def ns_orthogonalize(inp, out, steps=5, coeffs=QUINTIC, eps=1e-7, compute="bf16"
         float(eps), _COMPUTE[compute], barr, ctypes.c_void_p(ws.data_ptr()), ws.numel(),
         _stream(stream))
     _abi.check("ns_orthogonalize", st)
+
+
+def muon_step(W, M, G, mu, lr, steps=5, coeffs=QUINTIC, eps=1e-7, compute="bf16", ws=None,
+              stream=None):
+    """One whole Muon step in place: M <- mu*M + G, U = Newton-Schulz(M), W <- W - lr*U.
+
+    U is never stored: the last product updates W from U's fp32 values. The workspace is
+    that of ns_orthogonalize(M) (workspace(M, "bf16", device)).
+    """
+    Ws, Ms, Gs = _as_list(W), _as_list(M), _as_list(G)
+    if not (len(Ws) == len(Ms) == len(Gs)):
+        raise ValueError("W, M and G need the same number of matrices")
+    carr, stride = _coeff_args(coeffs, steps)
+    if ws is None:
+        ws = workspace(Ms, compute, Ms[0].device)
+    st = lib().muon_step(_mats(Ws), _mats(Ms), _mats(Gs), len(Ws), float(mu), float(lr),
+                         int(steps), carr, stride, float(eps), _COMPUTE[compute],
+                         ctypes.c_void_p(ws.data_ptr()), ws.numel(), _stream(stream))
+    _abi.check("muon_step", st)
 
 
 def _coeff_args(coeffs, steps):

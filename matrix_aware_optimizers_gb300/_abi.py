@@ -29,6 +29,7 @@ EXPORTS = (
     "muon_momentum_update",
     "ns_workspace_bytes",
     "ns_orthogonalize",
+    "muon_step",
     "ns_orthogonalize_noalloc",
     "ns_blockwise_workspace_bytes",
     "ns_orthogonalize_blockwise",
@@ -99,6 +100,11 @@ def load():
     lib.ns_orthogonalize.argtypes = [
         P(MaoMat), P(MaoMat), ctypes.c_int32, ctypes.c_int32, P(ctypes.c_float), ctypes.c_int32,
         ctypes.c_float, ctypes.c_int32, P(ctypes.c_void_p), vp, ctypes.c_size_t, vp]
+    lib.muon_step.restype = ctypes.c_int
+    lib.muon_step.argtypes = [
+        P(MaoMat), P(MaoMat), P(MaoMat), ctypes.c_int32, ctypes.c_float, ctypes.c_float,
+        ctypes.c_int32, P(ctypes.c_float), ctypes.c_int32, ctypes.c_float, ctypes.c_int32, vp,
+        ctypes.c_size_t, vp]
     lib.ns_orthogonalize_noalloc.restype = ctypes.c_int
     lib.ns_orthogonalize_noalloc.argtypes = [
         P(MaoMat), P(MaoMat), ctypes.c_int32, ctypes.c_int32, P(ctypes.c_float), ctypes.c_int32,

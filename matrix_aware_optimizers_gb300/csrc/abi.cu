@@ -151,6 +151,35 @@ mao_status ns_orthogonalize(const mao_mat* in, const mao_mat* out, int32_t batch
                 workspace_bytes, static_cast<cudaStream_t>(stream));
 }
 
+mao_status muon_step(const mao_mat* W, const mao_mat* M, const mao_mat* G, int32_t batch,
+                     float mu, float lr, int32_t steps, const float* coeffs,
+                     int32_t coeff_stride, float eps, int32_t compute, void* workspace,
+                     size_t workspace_bytes, void* stream) {
+  if (!W || !M || !G || batch < 1 || steps < 1 || steps > 64 || !coeffs) return MAO_ERR_INVALID_ARG;
+  if (coeff_stride != 0 && coeff_stride != 3) return MAO_ERR_INVALID_ARG;
+  if (!std::isfinite(eps) || eps < 0.0f || !std::isfinite(mu) || !std::isfinite(lr))
+    return MAO_ERR_INVALID_ARG;
+  for (int i = 0; i < (coeff_stride ? 3 * steps : 3); ++i)
+    if (!std::isfinite(coeffs[i])) return MAO_ERR_INVALID_ARG;
+  if (compute != MAO_BF16) return MAO_ERR_UNSUPPORTED;
+  for (int b = 0; b < batch; ++b) {
+    mao_status st = check_mat(W[b]);
+    if (st == MAO_OK) st = check_mat(M[b]);
+    if (st == MAO_OK) st = check_mat(G[b]);
+    if (st != MAO_OK) return st;
+    if (M[b].rows != W[b].rows || M[b].cols != W[b].cols || G[b].rows != W[b].rows ||
+        G[b].cols != W[b].cols)
+      return MAO_ERR_INVALID_ARG;
+  }
+  if (!workspace) return MAO_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0) return MAO_ERR_MISALIGNED;
+  if (device_cc() / 10 != 10) return MAO_ERR_UNSUPPORTED;
+  if (workspace_bytes < ns_workspace_size(M, batch, compute)) return MAO_ERR_WORKSPACE;
+  const NsFuse fuse{G, mu, lr};
+  return ns_run(M, W, batch, steps, coeffs, coeff_stride, eps, compute, nullptr, workspace,
+                workspace_bytes, static_cast<cudaStream_t>(stream), &fuse);
+}
+
 mao_status sign_pack_bits(const mao_mat* U, uint32_t* bits, void* stream) {
   if (!U || !bits) return MAO_ERR_INVALID_ARG;
   const mao_status st = check_mat(*U);

@@ -21,10 +21,17 @@ mao_status vote_launch(const uint32_t* bits, int32_t n_workers, int64_t stride, 
                        uint32_t* vote, cudaStream_t stream);
 
 size_t ns_workspace_size(const mao_mat* X, int32_t batch, int32_t compute);
+// A whole Muon step around Newton–Schulz (muon_step): the staging pass first sets
+// in[b] <- fmaf(mu, in[b], G[b]) (rounded to its dtype) and orthogonalises the new values;
+// the last product then updates out[b] <- out[b] - lr * U in place instead of writing U.
+struct NsFuse {
+  const mao_mat* G;
+  float mu, lr;
+};
 mao_status ns_run(const mao_mat* in, const mao_mat* out, int32_t batch, int32_t steps,
                   const float* coeffs, int32_t coeff_stride, float eps, int32_t compute,
                   uint32_t* const* sign_bits, void* workspace, size_t workspace_bytes,
-                  cudaStream_t stream);
+                  cudaStream_t stream, const NsFuse* fuse = nullptr);
 
 // Bound of every device-side wait in the tensor-core kernels (mao_set_wait_limit).
 unsigned long long wait_limit_ns();

@@ -119,17 +119,20 @@ constexpr int kStageMax = 48;
 struct StageEntry {
   const void* src;
   void* dst;
+  const void* g;        // momentum fused in (muon_step): G, and src is written back
   int64_t src_ld, dst_ld, rows, cols, units_per_row, units;
+  int64_t g_ld;
   int64_t block_begin;  // first block of this entry in the launch
   int64_t partial0;     // partial-sum index of that block
   int64_t nblocks;      // blocks (= partial sums) of this entry
   OutEntry out;
-  int32_t src_dt, vec_src, slot, pad;
+  int32_t src_dt, vec_src, slot, g_dt;
 };
 
 struct StageParams {
   StageEntry e[kStageMax];
   int32_t n, ws_dt;
+  float mu;             // momentum coefficient of the fused entries
   OutEntry* table;
   int64_t* prange;      // per slot: first partial, number of partials
   float* partials;
@@ -203,6 +206,30 @@ __global__ void __launch_bounds__(kStageThreads) stage_in_kernel(const __grid_co
     const int valid = int(left >= 8 ? 8 : (left > 0 ? left : 0));
     float v[8];
     stage_load8(e, row, col0, valid, v);
+    if (e.g && valid > 0) {
+      // momentum: M <- fmaf(mu, M, G) rounded to M's dtype, written back; the rounded
+      // values are what Newton–Schulz orthogonalises (as if M had been updated first)
+      float gv[8];
+      if (e.vec_src && valid == 8) {
+        load8(e.g, row * e.g_ld + col0, e.g_dt, gv);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) gv[i] = i < valid ? load_elem(e.g, row * e.g_ld + col0 + i, e.g_dt) : 0.0f;
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float m = __fmaf_rn(p.mu, v[i], gv[i]);
+        v[i] = i < valid ? (e.src_dt == MAO_BF16 ? __bfloat162float(__float2bfloat16_rn(m)) : m) : 0.0f;
+      }
+      void* mo = const_cast<void*>(e.src);
+      if (e.vec_src && valid == 8) {
+        store8(mo, row * e.src_ld + col0, e.src_dt, v);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          if (i < valid) store_elem(mo, row * e.src_ld + col0 + i, e.src_dt, v[i]);
+      }
+    }
 #pragma unroll
     for (int i = 0; i < 8; ++i) sq = __fmaf_rn(v[i], v[i], sq);
     store8(e.dst, row * e.dst_ld + col0, p.ws_dt, v);
@@ -363,10 +390,12 @@ int syrk_tiles(int64_t m) {
   return t;
 }
 
+// update_alpha (finite): the last product updates the outputs in place,
+// out <- out + update_alpha * U (TC_UPDATE), instead of writing U.
 mao_status run_tc_stage(const Buffers& buf, const std::vector<const NsGroupPlan*>& round,
                         int stage, int cur, bool first, bool last, const float* co,
                         const float* scale, const OutEntry* table, int out_mode,
-                        cudaStream_t stream) {
+                        cudaStream_t stream, float update_alpha = NAN) {
   TcParams p;
   memset(&p, 0, sizeof(p));
   p.out_mode = last ? out_mode : tc::OUT_WORKSPACE;
@@ -458,6 +487,10 @@ mao_status run_tc_stage(const Buffers& buf, const std::vector<const NsGroupPlan*
     tiles = int(t64);
   }
   p.total_tiles = tiles;
+  if (last && stage == NS_APPLY && std::isfinite(update_alpha)) {
+    p.stage = TC_UPDATE;
+    p.a = update_alpha;
+  }
   return tc_gemm_launch(p, stream);
 }
 
@@ -545,7 +578,7 @@ mao_status run_simt_stage(const Buffers& buf, const std::vector<const NsGroupPla
 mao_status ns_run(const mao_mat* in, const mao_mat* out, int32_t batch, int32_t steps,
                   const float* coeffs, int32_t coeff_stride, float eps, int32_t compute,
                   uint32_t* const* sign_bits, void* workspace, size_t workspace_bytes,
-                  cudaStream_t stream) {
+                  cudaStream_t stream, const NsFuse* fuse) {
   NsPlan plan;
   make_ns_plan(in, batch, compute, plan);
   if (workspace_bytes < plan.total) return MAO_ERR_WORKSPACE;
@@ -556,6 +589,7 @@ mao_status ns_run(const mao_mat* in, const mao_mat* out, int32_t batch, int32_t 
   int64_t* prange = reinterpret_cast<int64_t*>(ws + plan.off_prange);
   const bool tcpath = compute == MAO_BF16;
   const int32_t ws_dt = tcpath ? MAO_BF16 : MAO_F32;
+  if (fuse && (!tcpath || sign_bits)) return MAO_ERR_UNSUPPORTED;
 
   // ---- output entries; sign buffers filled by atomics start from zero
   std::vector<OutEntry> entries(batch);
@@ -583,6 +617,7 @@ mao_status ns_run(const mao_mat* in, const mao_mat* out, int32_t batch, int32_t 
       StageParams p;
       memset(&p, 0, sizeof(p));
       p.ws_dt = ws_dt;
+      p.mu = fuse ? fuse->mu : 0.0f;
       p.table = table;
       p.prange = prange;
       p.partials = partials;
@@ -602,7 +637,12 @@ mao_status ns_run(const mao_mat* in, const mao_mat* out, int32_t batch, int32_t 
         else if (in[b].dtype == MAO_SIGN1)
           e.vec_src = 0;
         else
-          e.vec_src = vec8_ok(in[b]) ? 1 : 0;
+          e.vec_src = vec8_ok(in[b]) && (!fuse || vec8_ok(fuse->G[b])) ? 1 : 0;
+        if (fuse) {
+          e.g = fuse->G[b].data;
+          e.g_ld = fuse->G[b].ld;
+          e.g_dt = fuse->G[b].dtype;
+        }
         e.dst = ws + gp->off_x[0] + size_t(s - gp->slot0) * size_t(gp->R * gp->ldx) * plan.es;
         e.dst_ld = gp->ldx;
         e.rows = in[b].rows;
@@ -650,7 +690,7 @@ mao_status ns_run(const mao_mat* in, const mao_mat* out, int32_t batch, int32_t 
       for (int stage = NS_GRAM; stage <= NS_APPLY; ++stage) {
         const mao_status st =
             tcpath ? run_tc_stage(buf, round, stage, cur, first, last, co, scale, table, out_mode,
-                                  stream)
+                                  stream, fuse ? -fuse->lr : NAN)
                    : run_simt_stage(buf, round, stage, cur, first, last, co, scale, table, stream);
         if (st != MAO_OK) return st;
       }

@@ -9,6 +9,7 @@
 // and, for the Dion step, plain products into fp32 outputs (the final NS_APPLY
 // instantiation with no scale) and an in-place rank-k update of the caller's matrices:
 //   TC_UPDATE out <- out + a * (A B^T)
+// which also serves as the last product of a fused Muon step (W <- W - lr U, U = B' X).
 // A symmetric result is stored as its upper and diagonal 256 x 256 tiles. A product that
 // reads it takes each 128-deep k-block below the diagonal from the transposed view of the
 // stored upper block (an MN-major load of the same buffer), so no tile is ever mirrored.
@@ -858,7 +859,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads(MODE), 1)
 #pragma unroll
             for (int c = 0; c < 64; ++c) w[c] += (jb + c == i) ? p.a : 0.0f;
           }
-        } else if (STAGE == NS_APPLY && scaled) {
+        } else if ((STAGE == NS_APPLY || STAGE == TC_UPDATE) && scaled) {
+          // (TC_UPDATE: the last product of a one-step Newton–Schulz updating W in place)
 #pragma unroll
           for (int c = 0; c < 64; ++c) w[c] *= s;
         }

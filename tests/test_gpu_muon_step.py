@@ -1,0 +1,86 @@
+"""GPU checks of the fused Muon step (muon_step: momentum, Newton–Schulz, update in one call).
+
+* Against the composed calls (muon_momentum_update, ns_orthogonalize into an fp32 U,
+  apply_update): M and W bit-identical. The fused path feeds the same fp32 accumulator values
+  into the same fmaf(-lr, u, w) that apply_update computes from the stored fp32 U.
+* Against the fp64 oracle ([SignMuon] §2 "Fluxo Algorítmico"; momentum form from [Dion]):
+  M bit-exact; the change of W within the bf16 Newton–Schulz tolerance (relative Frobenius
+  2e-2 of lr*U) plus one rounding of W to its storage type.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import matrix_aware_optimizers_gb300 as mao
+import oracle
+from helpers import rel_fro, to_np
+
+pytestmark = pytest.mark.gpu
+
+TOL = 2e-2
+DT = {"f32": torch.float32, "bf16": torch.bfloat16}
+EPS = {"f32": 2.0 ** -24, "bf16": 2.0 ** -9}
+
+
+def _inputs(gen, shapes, wdt, mdt, gdt, dev):
+    W = [(torch.randn(s, generator=gen) * 0.02).to(DT[wdt]).to(dev) for s in shapes]
+    M = [(torch.randn(s, generator=gen) * 0.01).to(DT[mdt]).to(dev) for s in shapes]
+    G = [(torch.randn(s, generator=gen) * 0.02).to(DT[gdt]).to(dev) for s in shapes]
+    return W, M, G
+
+
+SHAPES = [(256, 640), (640, 256), (384, 384), (300, 700), (256, 640), (130, 520)]
+
+
+@pytest.mark.parametrize("wdt,mdt,gdt", [("bf16", "bf16", "bf16"), ("bf16", "f32", "bf16"),
+                                         ("f32", "f32", "f32")])
+@pytest.mark.parametrize("steps", [5, 1])
+def test_muon_step_matches_composed_calls(cuda, wdt, mdt, gdt, steps):
+    gen = torch.Generator().manual_seed(60 + steps)
+    W, M, G = _inputs(gen, SHAPES, wdt, mdt, gdt, cuda)
+    W2, M2 = [w.clone() for w in W], [m.clone() for m in M]
+    mu, lr = 0.95, 0.02
+    mao.muon_step(W, M, G, mu, lr, steps, mao.QUINTIC, 1e-7)
+    mao.sync_status()
+    # composed: momentum, Newton-Schulz into fp32 U, update from U
+    mao.muon_momentum_update(M2, G, mu)
+    U = [torch.empty(m.shape, dtype=torch.float32, device=cuda) for m in M2]
+    mao.ns_orthogonalize(M2, U, steps, mao.QUINTIC, 1e-7, "bf16")
+    mao.apply_update(W2, lr, U=U)
+    mao.sync_status()
+    for a, b in zip(M, M2):
+        assert torch.equal(a, b)
+    for a, b in zip(W, W2):
+        assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("wdt,mdt", [("bf16", "bf16"), ("bf16", "f32")])
+def test_muon_step_oracle_parity(cuda, wdt, mdt):
+    gen = torch.Generator().manual_seed(70)
+    shapes = [(256, 640), (640, 256), (384, 384), (300, 700)]
+    W, M, G = _inputs(gen, shapes, wdt, mdt, "bf16", cuda)
+    host = [[to_np(t) for t in ts] for ts in (W, M, G)]
+    mu, lr = 0.95, 0.5  # a large lr makes the update dominate W's rounding
+    coeffs = [mao.QUINTIC] * 4 + [(1.5, -0.5, 0.0)]  # per-step coefficients
+    mao.muon_step(W, M, G, mu, lr, 5, coeffs, 1e-7)
+    mao.sync_status()
+    out = oracle.muon_step(host[0], host[1], host[2], mu, lr, steps=5, coeffs=coeffs,
+                           m_store="bf16" if mdt == "bf16" else "f32")
+    for k in range(len(shapes)):
+        assert np.array_equal(to_np(M[k]), out["M"][k])
+        w0, w_new, w_ref = host[0][k].astype(np.float64), to_np(W[k]).astype(np.float64), out["W"][k]
+        err = np.linalg.norm(w_new - w_ref)
+        assert err <= TOL * np.linalg.norm(w0 - w_ref) + EPS[wdt] * np.linalg.norm(w_ref)
+
+
+def test_muon_step_rejects_bad_arguments(cuda):
+    W = torch.zeros((64, 96), dtype=torch.bfloat16, device=cuda)
+    M, G = W.clone(), W.clone()
+    with pytest.raises(mao.MaoError):  # fp32 compute: not fused
+        mao.muon_step(W, M, G, 0.9, 0.1, compute="f32",
+                      ws=torch.empty(1 << 20, dtype=torch.uint8, device=cuda))
+    with pytest.raises(mao.MaoError):  # shapes differ
+        mao.muon_step(W, M, torch.zeros((64, 95), dtype=torch.bfloat16, device=cuda), 0.9, 0.1)
+    with pytest.raises(mao.MaoError):  # workspace too small
+        mao.muon_step(W, M, G, 0.9, 0.1, ws=torch.empty(256, dtype=torch.uint8, device=cuda))

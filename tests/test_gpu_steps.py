@@ -8,6 +8,8 @@ then checks sampled outputs one by one:
     entry, and (fp32) lies where |U| < 1e-3 rms(U); agreement >= 99.9% (fp32) / 99% (bf16,
     the bound implied by the 2e-2 value tolerance);
   * vote and update: bit-exact on the GPU's own inputs (packed words, stored U).
+The Muon workloads also run as bench.py runs them by default, one fused muon_step call: W
+and M must equal, bit for bit, the composed calls with U written as fp32.
 """
 
 import numpy as np
@@ -34,7 +36,7 @@ def _run_step(wl, dev, keep_u=False):
     """One step through bench.Step; returns the step object and host copies of the inputs."""
     inp = workloads.generate(wl, dev)
     host_in = {k: [to_np(t) for t in v] for k, v in inp.items()}
-    step = bench.Step(wl, inp, dev)
+    step = bench.Step(wl, inp, dev, fused=False)  # the three calls, U stored
     step.momentum()
     M_after = [m.clone() for m in step.M]
     U_vals = None
@@ -142,3 +144,30 @@ def test_config4_dense32_full(cuda):
     ev = torch.linalg.eigvalsh(gram).clamp_min(0).sqrt().cpu().numpy()
     assert ev.max() <= 1.2024 * 1.02
     assert np.mean(ev >= 0.6798 * 0.98) >= 0.95
+
+
+def _check_fused_equals_composed(wl, dev, sample):
+    """bench.Step's default (fused) step against the composed calls with an fp32 U."""
+    inp = workloads.generate(wl, dev)
+    fused = bench.Step(wl, {k: [t.clone() for t in v] for k, v in inp.items()}, dev)
+    assert fused.fused
+    fused()
+    W, M, G = inp["W"], inp["M"], inp["G"]
+    mao.muon_momentum_update(M, G, wl.mu)
+    for i in sample:
+        U = torch.empty(M[i].shape, dtype=torch.float32, device=dev)
+        mao.ns_orthogonalize(M[i], U, wl.steps, wl.coeffs, wl.eps, wl.compute)
+        mao.apply_update(W[i], wl.lr, U=U)
+    mao.sync_status()
+    for i in range(len(W)):
+        assert torch.equal(fused.M[i], M[i]), i
+    for i in sample:
+        assert torch.equal(fused.W[i], W[i]), i
+
+
+def test_config2_fused_step_equals_composed_full(cuda):
+    _check_fused_equals_composed(workloads.workload(2), cuda, [0, 1, 2, 3, 46])
+
+
+def test_config5_fused_step_equals_composed_full(cuda):
+    _check_fused_equals_composed(workloads.workload(5), cuda, [0, 1, 2, 192, 384])
