@@ -213,6 +213,11 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t sr
       "r"(x), "r"(y), "r"(z), "r"(src)
       : "memory");
 }
+// Asks L2 to fetch [src, src + bytes) (bytes a multiple of 16, src 16-byte aligned).
+__device__ __forceinline__ void prefetch_l2_bulk(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ void bulk_commit() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
@@ -658,6 +663,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads(MODE), 1)
       // a diagonal tile of a product of a buffer with itself: the B half equals the A half
       const bool share = G.same_ab && t.row0 == t.col0;
       const uint32_t tx_bytes = (share ? 2u : 4u) * uint32_t(HALF_BYTES);  // both CTAs
+      if (STAGE == TC_UPDATE && t.nkb <= 2) {
+        // a short product (rank-r update): the epilogue, which will read this CTA's 128 rows
+        // of the caller's matrix a tile or two from now, is the bottleneck. Have L2 fetch
+        // them while the operands load (one row segment per lane). With longer products the
+        // producer is on the critical path and the prefetch does not pay.
+        const OutEntry oe = p.out_table[G.slot0 + t.z];
+        if (oe.flags & OUT_VEC) {
+          const int es = oe.dtype == MAO_BF16 ? 2 : 4;
+          const uint32_t bytes = uint32_t(min(BN, G.N - t.col0) * es) & ~15u;
+          const int r0 = t.row0 + HALF * int(cta);
+          for (int rr = lane; rr < HALF && bytes; rr += 32) {
+            const int64_t row = r0 + rr;
+            if (row < G.M)
+              prefetch_l2_bulk(reinterpret_cast<const uint8_t*>(oe.out) + (row * oe.ld + t.col0) * es, bytes);
+          }
+        }
+      }
       for (int kb = 0; kb < t.nkb; ++kb) {
         int okw = 1;
         if (lane == 0) {
