@@ -258,11 +258,14 @@ class Step:
         else:
             self.mao.apply_update(self.W, wl.lr, vote=self.vote)
 
+    def fused_call(self, W_out=None):
+        wl = self.wl
+        self.mao.muon_step(self.W, self.M, self.G, wl.mu, wl.lr, wl.steps, wl.coeffs, wl.eps,
+                           wl.compute, ws=self.ws, W_out=W_out)
+
     def __call__(self):
         if self.fused:
-            wl = self.wl
-            self.mao.muon_step(self.W, self.M, self.G, wl.mu, wl.lr, wl.steps, wl.coeffs, wl.eps,
-                               wl.compute, ws=self.ws)
+            self.fused_call()
             return
         self.momentum()
         self.ns()
@@ -834,9 +837,9 @@ def run_e2e(step, K, world, dev, barrier, max_over_ranks):
     Copies run on their own streams and overlap other work where the data allow it: the
     gradients of step k+1 go into the second of two device slabs while step k computes, and
     the weights of step k are read back while step k+1 runs its momentum and Newton–Schulz
-    stages (its update waits for that read). A fused Muon step updates W inside its one call:
-    its W is first copied to a second device slab, and the read-back drains that copy while
-    the next step runs (the device copy is part of the timed step). Every step still moves
+    stages (its update waits for that read). A fused Muon step reads W from one of two device
+    slabs and writes the new W into the other (muon_step's W_out), so the read-back of step
+    k's weights overlaps step k+1, which writes the slab step k read. Every step still moves
     all of its bytes.
     """
     import torch
@@ -851,7 +854,9 @@ def run_e2e(step, K, world, dev, barrier, max_over_ranks):
     step.W = W_views
     fused = getattr(step, "fused", False)
     staged = step.wl.kind != "dion" and not fused  # Dion and muon_step update W in one call
-    W_snap = torch.empty_like(W_dev) if fused else W_dev
+    # fused: two weight slabs, read one and write the other; one read-back event per slab
+    W_bufs = [(W_dev, W_views)] + ([_slab(step.W, dev)] if fused else [])
+    w_read_slab = [torch.cuda.Event() for _ in W_bufs]
     h2d = G_host.numel() * G_host.element_size()
     d2h = W_host.numel() * W_host.element_size()
     s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
@@ -861,6 +866,9 @@ def run_e2e(step, K, world, dev, barrier, max_over_ranks):
     for ev in g_free:
         ev.record(main)
     w_read.record(main)
+    for ev in w_read_slab:
+        ev.record(main)
+    W_src = W_dev
     barrier()
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
@@ -881,10 +889,12 @@ def run_e2e(step, K, world, dev, barrier, max_over_ranks):
             main.wait_event(w_read)           # the previous read-back of W is complete
             step.update()
         elif fused:
-            step()
+            src, dst = k % 2, 1 - k % 2
+            step.W = W_bufs[src][1]
+            main.wait_event(w_read_slab[dst])  # step k-2's weights have been read back
+            step.fused_call(W_out=W_bufs[dst][1])
             g_free[b].record(main)
-            main.wait_event(w_read)           # the previous read-back is done with the copy
-            W_snap.copy_(W_dev)
+            W_src = W_bufs[dst][0]
         else:
             main.wait_event(w_read)
             step()
@@ -892,21 +902,25 @@ def run_e2e(step, K, world, dev, barrier, max_over_ranks):
         w_done.record(main)
         s_out.wait_event(w_done)
         with torch.cuda.stream(s_out):
-            W_host.copy_(W_snap, non_blocking=True)
+            W_host.copy_(W_src, non_blocking=True)
         w_read.record(s_out)
+        if fused:
+            w_read_slab[1 - k % 2].record(s_out)
     main.wait_event(w_read)
     e1.record(main)
     torch.cuda.synchronize()
     barrier()
     ms = max_over_ranks(e0.elapsed_time(e1))
+    last_views = W_bufs[K % 2][1] if fused else W_views
     step.G, step.W = G_orig, W_orig
-    for w, v in zip(W_orig, W_views):
+    for w, v in zip(W_orig, last_views):
         w.copy_(v)
     return {"value": job_throughput(ms, K, world), "unit": "steps/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": K,
             "copies": "one pinned H2D slab and one D2H slab per step, on copy streams overlapping "
                       "the neighbouring steps' compute" +
-                      ("; W copied to a device slab first (fused step)" if fused else "")}
+                      ("; two device weight slabs, read one, write the other (fused step)"
+                       if fused else "")}
 
 
 def read_traffic(wl):

@@ -151,22 +151,26 @@ mao_status ns_orthogonalize(const mao_mat* in, const mao_mat* out, int32_t batch
  * the update W <- W - eta U): for each matrix
  *   M <- fmaf(mu, M, G)       rounded to M's dtype, written back
  *   U  = Newton–Schulz(M)     exactly as ns_orthogonalize with compute = MAO_BF16
- *   W <- fmaf(-lr, U, W)      rounded to W's dtype
+ *   W' = fmaf(-lr, U, W)      rounded to W's dtype, into W_out[b] (or W[b] in place)
  * The momentum is applied by the staging pass that copies M into the workspace, and the
  * last product updates W in its epilogue: U is never stored, and W's update uses U's fp32
  * values (the composed calls round U to the caller's U buffer first).
  *
  *   W, M, G      f32 or bf16 matrices of equal shape per entry (M and G also as for
- *                muon_momentum_update); W and M are updated in place. No two of W[b], M[b],
- *                G[b] may overlap.
+ *                muon_momentum_update); M is updated in place. No two of W[b], M[b], G[b]
+ *                may overlap.
+ *   W_out        NULL (W is updated in place) or HOST array of `batch` matrices of W's shape
+ *                and dtype receiving W' (W then is only read; W_out[b] may alias W[b] but
+ *                must not overlap M[b] or G[b]). Double-buffered weights avoid a copy when
+ *                the previous W' is still being read elsewhere.
  *   mu, lr       finite; steps, coeffs, coeff_stride, eps as for ns_orthogonalize.
  *   compute      MAO_BF16 (tensor cores) only; MAO_F32 returns MAO_ERR_UNSUPPORTED.
  *   workspace    >= ns_workspace_bytes(M, batch, MAO_BF16) bytes, 256-byte aligned.
  * Errors: as ns_orthogonalize (argument checks before any launch; device time-outs through
  * mao_sync_status).
  */
-mao_status muon_step(const mao_mat* W, const mao_mat* M, const mao_mat* G, int32_t batch,
-                     float mu, float lr, int32_t steps, const float* coeffs,
+mao_status muon_step(const mao_mat* W, const mao_mat* M, const mao_mat* G, const mao_mat* W_out,
+                     int32_t batch, float mu, float lr, int32_t steps, const float* coeffs,
                      int32_t coeff_stride, float eps, int32_t compute, void* workspace,
                      size_t workspace_bytes, void* stream);
 

@@ -144,19 +144,22 @@ def ns_orthogonalize(inp, out, steps=5, coeffs=QUINTIC, eps=1e-7, compute="bf16"
 
 
 def muon_step(W, M, G, mu, lr, steps=5, coeffs=QUINTIC, eps=1e-7, compute="bf16", ws=None,
-              stream=None):
-    """One whole Muon step in place: M <- mu*M + G, U = Newton-Schulz(M), W <- W - lr*U.
+              W_out=None, stream=None):
+    """One whole Muon step: M <- mu*M + G, U = Newton-Schulz(M), W' = W - lr*U into W_out
+    (W itself when W_out is None).
 
     U is never stored: the last product updates W from U's fp32 values. The workspace is
     that of ns_orthogonalize(M) (workspace(M, "bf16", device)).
     """
     Ws, Ms, Gs = _as_list(W), _as_list(M), _as_list(G)
-    if not (len(Ws) == len(Ms) == len(Gs)):
-        raise ValueError("W, M and G need the same number of matrices")
+    Wo = _as_list(W_out) if W_out is not None else None
+    if not (len(Ws) == len(Ms) == len(Gs)) or (Wo is not None and len(Wo) != len(Ws)):
+        raise ValueError("W, M, G (and W_out) need the same number of matrices")
     carr, stride = _coeff_args(coeffs, steps)
     if ws is None:
         ws = workspace(Ms, compute, Ms[0].device)
-    st = lib().muon_step(_mats(Ws), _mats(Ms), _mats(Gs), len(Ws), float(mu), float(lr),
+    st = lib().muon_step(_mats(Ws), _mats(Ms), _mats(Gs), _mats(Wo) if Wo is not None else None,
+                         len(Ws), float(mu), float(lr),
                          int(steps), carr, stride, float(eps), _COMPUTE[compute],
                          ctypes.c_void_p(ws.data_ptr()), ws.numel(), _stream(stream))
     _abi.check("muon_step", st)

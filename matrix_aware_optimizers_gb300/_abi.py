@@ -102,7 +102,7 @@ def load():
         ctypes.c_float, ctypes.c_int32, P(ctypes.c_void_p), vp, ctypes.c_size_t, vp]
     lib.muon_step.restype = ctypes.c_int
     lib.muon_step.argtypes = [
-        P(MaoMat), P(MaoMat), P(MaoMat), ctypes.c_int32, ctypes.c_float, ctypes.c_float,
+        P(MaoMat), P(MaoMat), P(MaoMat), P(MaoMat), ctypes.c_int32, ctypes.c_float, ctypes.c_float,
         ctypes.c_int32, P(ctypes.c_float), ctypes.c_int32, ctypes.c_float, ctypes.c_int32, vp,
         ctypes.c_size_t, vp]
     lib.ns_orthogonalize_noalloc.restype = ctypes.c_int

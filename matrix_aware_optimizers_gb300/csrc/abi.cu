@@ -151,8 +151,8 @@ mao_status ns_orthogonalize(const mao_mat* in, const mao_mat* out, int32_t batch
                 workspace_bytes, static_cast<cudaStream_t>(stream));
 }
 
-mao_status muon_step(const mao_mat* W, const mao_mat* M, const mao_mat* G, int32_t batch,
-                     float mu, float lr, int32_t steps, const float* coeffs,
+mao_status muon_step(const mao_mat* W, const mao_mat* M, const mao_mat* G, const mao_mat* W_out,
+                     int32_t batch, float mu, float lr, int32_t steps, const float* coeffs,
                      int32_t coeff_stride, float eps, int32_t compute, void* workspace,
                      size_t workspace_bytes, void* stream) {
   if (!W || !M || !G || batch < 1 || steps < 1 || steps > 64 || !coeffs) return MAO_ERR_INVALID_ARG;
@@ -170,14 +170,21 @@ mao_status muon_step(const mao_mat* W, const mao_mat* M, const mao_mat* G, int32
     if (M[b].rows != W[b].rows || M[b].cols != W[b].cols || G[b].rows != W[b].rows ||
         G[b].cols != W[b].cols)
       return MAO_ERR_INVALID_ARG;
+    if (W_out) {
+      st = check_mat(W_out[b]);
+      if (st != MAO_OK) return st;
+      if (W_out[b].rows != W[b].rows || W_out[b].cols != W[b].cols ||
+          W_out[b].dtype != W[b].dtype)
+        return MAO_ERR_INVALID_ARG;
+    }
   }
   if (!workspace) return MAO_ERR_INVALID_ARG;
   if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0) return MAO_ERR_MISALIGNED;
   if (device_cc() / 10 != 10) return MAO_ERR_UNSUPPORTED;
   if (workspace_bytes < ns_workspace_size(M, batch, compute)) return MAO_ERR_WORKSPACE;
-  const NsFuse fuse{G, mu, lr};
-  return ns_run(M, W, batch, steps, coeffs, coeff_stride, eps, compute, nullptr, workspace,
-                workspace_bytes, static_cast<cudaStream_t>(stream), &fuse);
+  const NsFuse fuse{G, W_out ? W : nullptr, mu, lr};
+  return ns_run(M, W_out ? W_out : W, batch, steps, coeffs, coeff_stride, eps, compute, nullptr,
+                workspace, workspace_bytes, static_cast<cudaStream_t>(stream), &fuse);
 }
 
 mao_status sign_pack_bits(const mao_mat* U, uint32_t* bits, void* stream) {

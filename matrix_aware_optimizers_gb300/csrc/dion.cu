@@ -117,6 +117,8 @@ __global__ void __launch_bounds__(64) dion_setup_kernel(const __grid_constant__ 
   if (threadIdx.x != 0) return;
   OutEntry o;
   o.bits = nullptr;
+  o.src = nullptr;
+  o.src_ld = 0;
   o.out = e.P0;
   o.ld = p.c.ldr;
   o.dtype = MAO_F32;

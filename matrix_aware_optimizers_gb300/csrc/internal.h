@@ -26,6 +26,7 @@ size_t ns_workspace_size(const mao_mat* X, int32_t batch, int32_t compute);
 // the last product then updates out[b] <- out[b] - lr * U in place instead of writing U.
 struct NsFuse {
   const mao_mat* G;
+  const mao_mat* W_in;  // null: out[b] is updated in place; else out[b] <- W_in[b] - lr * U
   float mu, lr;
 };
 mao_status ns_run(const mao_mat* in, const mao_mat* out, int32_t batch, int32_t steps,
@@ -55,6 +56,9 @@ struct OutEntry {
   int64_t ld;       // U row stride (elements)
   int32_t dtype;    // U dtype
   int32_t flags;    // bit 0: 16-byte vector stores allowed; bit 1: one sign word per 32 columns
+  const void* src;  // in-place updates (TC_UPDATE): the old values, of out's dtype, or null
+                    // for out itself (out <- src + a (A B^T))
+  int64_t src_ld;   // row stride of src (elements)
 };
 
 enum OutFlags : int32_t { OUT_VEC = 1, OUT_WORDS = 2 };

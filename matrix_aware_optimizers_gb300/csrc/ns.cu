@@ -595,13 +595,17 @@ mao_status ns_run(const mao_mat* in, const mao_mat* out, int32_t batch, int32_t 
   std::vector<OutEntry> entries(batch);
   for (int b = 0; b < batch; ++b) {
     OutEntry& e = entries[b];
+    e.src = fuse && fuse->W_in ? fuse->W_in[b].data : nullptr;
+    e.src_ld = fuse && fuse->W_in ? fuse->W_in[b].ld : 0;
     e.out = out[b].data;
     e.bits = sign_bits ? sign_bits[b] : nullptr;
     e.ld = out[b].ld;
     e.dtype = out[b].dtype;
     e.flags = 0;
     if (e.out && (reinterpret_cast<uintptr_t>(e.out) % 16 == 0) &&
-        ((out[b].ld * elem_size(out[b].dtype)) % 16 == 0))
+        ((out[b].ld * elem_size(out[b].dtype)) % 16 == 0) &&
+        (!e.src || (reinterpret_cast<uintptr_t>(e.src) % 16 == 0 &&
+                    (e.src_ld * elem_size(out[b].dtype)) % 16 == 0)))
       e.flags |= OUT_VEC;
     if (tcpath && in[b].cols % 32 == 0) e.flags |= OUT_WORDS;
     if (e.bits && !(e.flags & OUT_WORDS)) {

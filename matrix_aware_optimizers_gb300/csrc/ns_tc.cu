@@ -480,13 +480,18 @@ __device__ __forceinline__ bool upd_block_vec(const OutEntry& e, int jb, int N) 
   return (e.flags & OUT_VEC) && e.dtype == MAO_BF16 && jb + 64 <= N;
 }
 
+// The old values of an update: e.src (row stride e.src_ld) or, when null, e.out itself.
+__device__ __forceinline__ const void* upd_src(const OutEntry& e) { return e.src ? e.src : e.out; }
+__device__ __forceinline__ int64_t upd_src_ld(const OutEntry& e) { return e.src ? e.src_ld : e.ld; }
+
 __device__ __forceinline__ void upd_load(const OutEntry& e, int i0, int jb, int M, int lane,
                                          uint4 (&r)[8]) {
-  const __nv_bfloat16* base = reinterpret_cast<const __nv_bfloat16*>(e.out) + jb + 8 * (lane & 7);
+  const __nv_bfloat16* base = reinterpret_cast<const __nv_bfloat16*>(upd_src(e)) + jb + 8 * (lane & 7);
+  const int64_t ld = upd_src_ld(e);
 #pragma unroll
   for (int q = 0; q < 8; ++q) {
     const int gi = i0 + (lane >> 3) + 4 * q;
-    if (gi < M) r[q] = *reinterpret_cast<const uint4*>(base + int64_t(gi) * e.ld);
+    if (gi < M) r[q] = *reinterpret_cast<const uint4*>(base + int64_t(gi) * ld);
   }
 }
 
@@ -526,19 +531,22 @@ __device__ __forceinline__ void upd_apply(uint8_t* S, int lane, const float* w, 
   __syncwarp();
 }
 
-// In-place update of the caller's matrix for this lane's row, columns jb..jb+63:
-// out = fmaf(alpha, acc, out) in fp32, rounded to out's dtype.
+// Update of the caller's matrix for this lane's row, columns jb..jb+63:
+// out = fmaf(alpha, acc, old) in fp32, rounded to out's dtype (old: upd_src).
 __device__ __forceinline__ void update_final(const OutEntry& e, int i0, int jb, int M, int N,
                                              int lane, const float* w, float alpha) {
   const int i = i0 + lane;
   if (i >= M) return;
+  const int64_t sld = upd_src_ld(e);
   if ((e.flags & OUT_VEC) && jb + 64 <= N) {
     if (e.dtype == MAO_BF16) {
       uint4* g = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(e.out) +
                                           int64_t(i) * e.ld + jb);
+      const uint4* gs = reinterpret_cast<const uint4*>(
+          reinterpret_cast<const __nv_bfloat16*>(upd_src(e)) + int64_t(i) * sld + jb);
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
-        uint4 u = g[k];
+        uint4 u = gs[k];
         uint32_t* h = reinterpret_cast<uint32_t*>(&u);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
@@ -550,9 +558,11 @@ __device__ __forceinline__ void update_final(const OutEntry& e, int i0, int jb, 
       }
     } else {
       float4* g = reinterpret_cast<float4*>(reinterpret_cast<float*>(e.out) + int64_t(i) * e.ld + jb);
+      const float4* gs =
+          reinterpret_cast<const float4*>(reinterpret_cast<const float*>(upd_src(e)) + int64_t(i) * sld + jb);
 #pragma unroll
       for (int k = 0; k < 16; ++k) {
-        float4 v = g[k];
+        float4 v = gs[k];
         v.x = __fmaf_rn(alpha, w[4 * k], v.x);
         v.y = __fmaf_rn(alpha, w[4 * k + 1], v.y);
         v.z = __fmaf_rn(alpha, w[4 * k + 2], v.z);
@@ -564,8 +574,8 @@ __device__ __forceinline__ void update_final(const OutEntry& e, int i0, int jb, 
 #pragma unroll
     for (int c = 0; c < 64; ++c) {
       if (jb + c < N) {
-        const int64_t idx = int64_t(i) * e.ld + jb + c;
-        store_elem(e.out, idx, e.dtype, __fmaf_rn(alpha, w[c], load_elem(e.out, idx, e.dtype)));
+        const float old = load_elem(upd_src(e), int64_t(i) * sld + jb + c, e.dtype);
+        store_elem(e.out, int64_t(i) * e.ld + jb + c, e.dtype, __fmaf_rn(alpha, w[c], old));
       }
     }
   }
@@ -676,7 +686,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads(MODE), 1)
           for (int rr = lane; rr < HALF && bytes; rr += 32) {
             const int64_t row = r0 + rr;
             if (row < G.M)
-              prefetch_l2_bulk(reinterpret_cast<const uint8_t*>(oe.out) + (row * oe.ld + t.col0) * es, bytes);
+              prefetch_l2_bulk(reinterpret_cast<const uint8_t*>(upd_src(oe)) + (row * upd_src_ld(oe) + t.col0) * es,
+                               bytes);
           }
         }
       }

@@ -84,3 +84,29 @@ def test_muon_step_rejects_bad_arguments(cuda):
         mao.muon_step(W, M, torch.zeros((64, 95), dtype=torch.bfloat16, device=cuda), 0.9, 0.1)
     with pytest.raises(mao.MaoError):  # workspace too small
         mao.muon_step(W, M, G, 0.9, 0.1, ws=torch.empty(256, dtype=torch.uint8, device=cuda))
+
+
+def test_muon_step_out_of_place(cuda):
+    gen = torch.Generator().manual_seed(75)
+    W, M, G = _inputs(gen, SHAPES, "bf16", "bf16", "bf16", cuda)
+    W0 = [w.clone() for w in W]
+    M2 = [m.clone() for m in M]
+    W_out = [torch.full_like(w, float("nan")) for w in W]
+    mao.muon_step(W, M, G, 0.95, 0.02, W_out=W_out)
+    W_in_place = [w.clone() for w in W0]
+    mao.muon_step(W_in_place, M2, G, 0.95, 0.02)
+    W_alias = [w.clone() for w in W0]
+    mao.sync_status()
+    for a, b in zip(W, W0):
+        assert torch.equal(a, b)  # W only read
+    for a, b in zip(W_out, W_in_place):
+        assert torch.equal(a, b)
+    for a, b in zip(M, M2):
+        assert torch.equal(a, b)
+    # W_out aliasing W is the in-place update
+    gen = torch.Generator().manual_seed(75)
+    _, Ma, Ga = _inputs(gen, SHAPES, "bf16", "bf16", "bf16", cuda)
+    mao.muon_step(W_alias, Ma, Ga, 0.95, 0.02, W_out=W_alias)
+    mao.sync_status()
+    for a, b in zip(W_alias, W_in_place):
+        assert torch.equal(a, b)
