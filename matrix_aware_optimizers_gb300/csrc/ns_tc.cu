@@ -213,9 +213,10 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t sr
       "r"(x), "r"(y), "r"(z), "r"(src)
       : "memory");
 }
-// Asks L2 to fetch [src, src + bytes) (bytes a multiple of 16, src 16-byte aligned).
-__device__ __forceinline__ void prefetch_l2_bulk(const void* src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+// Asks L2 to fetch the line holding `src` (through the load/store path: bulk prefetches
+// would queue in the TMA unit behind, or ahead of, the operand loads).
+__device__ __forceinline__ void prefetch_l2(const void* src) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(src) : "memory");
 }
 
 __device__ __forceinline__ void bulk_commit() {
@@ -676,18 +677,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads(MODE), 1)
       if (STAGE == TC_UPDATE && t.nkb <= 2) {
         // a short product (rank-r update): the epilogue, which will read this CTA's 128 rows
         // of the caller's matrix a tile or two from now, is the bottleneck. Have L2 fetch
-        // them while the operands load (one row segment per lane). With longer products the
-        // producer is on the critical path and the prefetch does not pay.
+        // them while the operands load. With longer products the prefetched rows displace
+        // operand panels from L2 and the prefetch does not pay.
         const OutEntry oe = p.out_table[G.slot0 + t.z];
         if (oe.flags & OUT_VEC) {
           const int es = oe.dtype == MAO_BF16 ? 2 : 4;
           const uint32_t bytes = uint32_t(min(BN, G.N - t.col0) * es) & ~15u;
           const int r0 = t.row0 + HALF * int(cta);
-          for (int rr = lane; rr < HALF && bytes; rr += 32) {
-            const int64_t row = r0 + rr;
-            if (row < G.M)
-              prefetch_l2_bulk(reinterpret_cast<const uint8_t*>(upd_src(oe)) + (row * upd_src_ld(oe) + t.col0) * es,
-                               bytes);
+          // one 128-byte line per lane and step, eight lines (up to 1 KB) per row
+          const uint8_t* src = reinterpret_cast<const uint8_t*>(upd_src(oe));
+          const int64_t sld = upd_src_ld(oe);
+          for (int q = lane; q < HALF * 8; q += 32) {
+            const int64_t row = r0 + (q >> 3);
+            const uint32_t off = uint32_t(q & 7) * 128u;
+            if (row < G.M && off < bytes) prefetch_l2(src + (row * sld + t.col0) * es + off);
           }
         }
       }
