@@ -13,11 +13,13 @@
 // diagonal, computed as Cholesky QR applied twice: S = P^T P, S = L L^T, P <- P W^T with
 // W = L^-1 (the factorisation kernel also inverts L, so the product with P is one parallel
 // triangular multiply instead of a sequential substitution).
-// The three dense products run on the same tcgen05 kernel as Newton–Schulz, over up to
-// eight shape groups per launch; the r x r work (Gram matrices, Cholesky, triangular
-// solve) runs in fp32 on CUDA cores, every matrix of the call in one launch per stage.
-// Per-matrix descriptors live in a device table in the workspace (written by a set-up
-// kernel), so a call of any size and any mix of shapes takes a fixed number of launches.
+// The dense products (B Q, B^T P and the two rank-r updates) run on the same tcgen05 kernel
+// as Newton–Schulz, over up to eight shape groups per launch; the Cholesky QR (Gram
+// matrices, Cholesky and inverse, triangular multiply) runs in fp32 on CUDA cores, every
+// matrix of the call in one launch per stage (the Gram and multiply launches cover up to
+// sixteen shape groups each, with exactly the CTAs their slots need). Per-matrix
+// descriptors live in a device table in the workspace (written by a set-up kernel), so a
+// call of any size and any mix of shapes takes a fixed number of launches.
 #include <algorithm>
 #include <cmath>
 #include <cstring>

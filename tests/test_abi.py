@@ -155,3 +155,31 @@ def test_blockwise_arguments_and_sizes(lib):
                                           None) == _abi.MAO_ERR_INVALID_ARG
     assert lib.ns_orthogonalize_blockwise(X, X, 1, 128, 256, 5, co, 1, 1e-7, 1, ws, 1 << 40,
                                           None) == _abi.MAO_ERR_INVALID_ARG
+
+
+def test_muon_step_arguments_rejected_before_any_launch(lib):
+    fake = 0x10000
+    co = (ctypes.c_float * 3)(3.4445, -4.775, 2.0315)
+    ws = ctypes.c_void_p(fake)
+    W = _mats((64, 96), data=fake)
+    M = _mats((64, 96), data=fake + 4096)
+    G = _mats((64, 96), data=fake + 8192)
+
+    def call(W=W, M=M, G=G, W_out=None, batch=1, mu=0.95, lr=0.02, steps=5, coeffs=co,
+             stride=0, eps=1e-7, compute=_abi.MAO_BF16, ws=ws, nbytes=1 << 30):
+        return lib.muon_step(W, M, G, W_out, batch, mu, lr, steps, coeffs, stride, eps, compute,
+                             ws, nbytes, None)
+
+    assert call(W=None) == _abi.MAO_ERR_INVALID_ARG
+    assert call(batch=0) == _abi.MAO_ERR_INVALID_ARG
+    assert call(steps=0) == _abi.MAO_ERR_INVALID_ARG
+    assert call(stride=2) == _abi.MAO_ERR_INVALID_ARG
+    assert call(mu=float("nan")) == _abi.MAO_ERR_INVALID_ARG
+    assert call(lr=float("inf")) == _abi.MAO_ERR_INVALID_ARG
+    assert call(eps=-1.0) == _abi.MAO_ERR_INVALID_ARG
+    assert call(compute=_abi.MAO_F32) == _abi.MAO_ERR_UNSUPPORTED  # tensor-core path only
+    assert call(G=_mats((64, 95), data=fake)) == _abi.MAO_ERR_INVALID_ARG
+    assert call(W_out=_mats((64, 96), dtype=_abi.MAO_F32, data=fake)) == _abi.MAO_ERR_INVALID_ARG
+    assert call(W_out=_mats((64, 95), data=fake)) == _abi.MAO_ERR_INVALID_ARG
+    assert call(ws=None) == _abi.MAO_ERR_INVALID_ARG
+    assert call(ws=ctypes.c_void_p(fake + 16)) == _abi.MAO_ERR_MISALIGNED
