@@ -2,11 +2,11 @@
 // algorithm section): for each parameter matrix X (m x n) with momentum M, gradient G and
 // the previous right factor Q (n x r),
 //
-//   B = M + G                       stage kernel: M <- B in place, bf16 copy Bw
+//   B = M + G                       stage kernel: bf16 copy Bw (and M <- B for an fp32 M)
 //   P = orthonormalise(B Q)         tensor-core product (fp32 P), then Cholesky QR twice
 //   R = B^T P                       tensor-core product (fp32 R)
 //   Q <- ColumnNormalize(R)         column norms, then Q (fp32, caller) and bf16 copies
-//   M <- B - (1 - mu) P R^T         tensor-core rank-r update, in place
+//   M <- B - (1 - mu) P R^T         tensor-core rank-r update (B read from M, or from Bw)
 //   X <- X - lr P Q^T               tensor-core rank-r update, in place
 //
 // The orthonormal basis is the Q factor of the thin QR with a positive triangular
@@ -132,7 +132,13 @@ __global__ void __launch_bounds__(64) dion_setup_kernel(const __grid_constant__ 
   o.ld = e.ldm;
   o.dtype = e.dtm;
   o.flags = e.flags_m;
+  if (e.dtm == MAO_BF16) {  // B was not written back to M: the update reads it from Bw
+    o.src = e.Bw;
+    o.src_ld = e.ldn;
+  }
   p.c.tM[z] = o;
+  o.src = nullptr;
+  o.src_ld = 0;
   o.out = e.X;
   o.ld = e.ldx;
   o.dtype = e.dtx;
@@ -146,8 +152,9 @@ __device__ __forceinline__ float round_to(float v, int32_t dt) {
   return dt == MAO_BF16 ? __bfloat162float(__float2bfloat16_rn(v)) : v;
 }
 
-// Units of 8 columns over the zero-padded rows of Bw; blockIdx.y = slot. M <- M + G in
-// place (rounded to M's dtype) and Bw = bf16 of the stored B.
+// Units of 8 columns over the zero-padded rows of Bw; blockIdx.y = slot. Bw = bf16 of
+// B = M + G rounded to M's dtype, and M <- B when M is fp32. A bf16 M is left as it is:
+// Bw then holds B exactly, and the M update reads B from there (its output entry's source).
 __global__ void __launch_bounds__(256) dion_stage_kernel(const __grid_constant__ DionCommon c) {
   const DionSlot& e = c.slots[blockIdx.y];
   const uint32_t upr = uint32_t(e.ldn) / 8;
@@ -161,7 +168,7 @@ __global__ void __launch_bounds__(256) dion_stage_kernel(const __grid_constant__
     load8(e.G, row * e.ldg + col0, e.dtg, gv);
 #pragma unroll
     for (int k = 0; k < 8; ++k) b[k] = mv[k] + gv[k];
-    store8(e.M, row * e.ldm + col0, e.dtm, b);
+    if (e.dtm != MAO_BF16) store8(e.M, row * e.ldm + col0, e.dtm, b);
 #pragma unroll
     for (int k = 0; k < 8; ++k) b[k] = round_to(b[k], e.dtm);
   } else {
@@ -171,7 +178,7 @@ __global__ void __launch_bounds__(256) dion_stage_kernel(const __grid_constant__
       b[k] = 0.0f;
       if (j < e.n) {
         const float v = load_elem(e.M, row * e.ldm + j, e.dtm) + load_elem(e.G, row * e.ldg + j, e.dtg);
-        store_elem(e.M, row * e.ldm + j, e.dtm, v);
+        if (e.dtm != MAO_BF16) store_elem(e.M, row * e.ldm + j, e.dtm, v);
         b[k] = round_to(v, e.dtm);
       }
     }
