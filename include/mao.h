@@ -59,7 +59,7 @@ extern "C" {
 typedef enum mao_status {
   MAO_OK = 0,
   MAO_ERR_INVALID_ARG = 1,  /* null pointer, bad size, bad enum */
-  MAO_ERR_UNSUPPORTED = 2,  /* valid request this build cannot serve (device, limits) */
+  MAO_ERR_UNSUPPORTED = 2,  /* valid request the library cannot serve (device, limits) */
   MAO_ERR_MISALIGNED = 3,   /* pointer not aligned to its element size / workspace to 256 B */
   MAO_ERR_WORKSPACE = 4,    /* workspace smaller than ns_workspace_bytes() */
   MAO_ERR_CUDA = 5,         /* a CUDA runtime call or launch failed */
