@@ -471,7 +471,9 @@ __device__ __forceinline__ void store_final(const OutEntry& e, uint8_t* S, int i
 // per instruction: lane l holds 16-byte chunk l % 8 of rows l / 8 + 4 q). The old values are
 // loaded before the accumulator is ready; upd_apply turns them into the new values through
 // the warp's staging buffer (one row per lane for the arithmetic), and upd_store writes them
-// once the accumulator has been released.
+// once the accumulator has been released. Both go around the L1 (L1::no_allocate): with the
+// operand ring and staging in shared memory only a small L1 is left, and lines allocated for
+// rows that are used once throttle the loads in flight.
 __device__ __forceinline__ bool upd_block_vec(const OutEntry& e, int jb, int N) {
   return (e.flags & OUT_VEC) && e.dtype == MAO_BF16 && jb + 64 <= N;
 }
@@ -487,7 +489,13 @@ __device__ __forceinline__ void upd_load(const OutEntry& e, int i0, int jb, int 
 #pragma unroll
   for (int q = 0; q < 8; ++q) {
     const int gi = i0 + (lane >> 3) + 4 * q;
-    if (gi < M) r[q] = *reinterpret_cast<const uint4*>(base + int64_t(gi) * ld);
+    if (gi < M) {
+      uint4 v;
+      asm volatile("ld.global.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                   : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                   : "l"(base + int64_t(gi) * ld));
+      r[q] = v;
+    }
   }
 }
 
@@ -497,7 +505,9 @@ __device__ __forceinline__ void upd_store(const OutEntry& e, int i0, int jb, int
 #pragma unroll
   for (int q = 0; q < 8; ++q) {
     const int gi = i0 + (lane >> 3) + 4 * q;
-    if (gi < M) *reinterpret_cast<uint4*>(base + int64_t(gi) * e.ld) = r[q];
+    if (gi < M)
+      asm volatile("st.global.L1::no_allocate.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(base + int64_t(gi) * e.ld),
+                   "r"(r[q].x), "r"(r[q].y), "r"(r[q].z), "r"(r[q].w) : "memory");
   }
 }
 
