@@ -68,7 +68,9 @@ constexpr int STAGE_BYTES = 2 * HALF_BYTES;       // A half + B half
 // Output modes of a launch: the workspace (bulk tensor stores), the caller's outputs in any
 // form (U in fp32 or bf16 with any row stride, packed signs, in-place updates), or the
 // caller's bf16 U with 16-byte aligned rows and no signs.
-enum OutMode : int { OUT_WORKSPACE = 0, OUT_CALLER = 1, OUT_CALLER_BF16 = 2 };
+// OUT_UPDATE_STREAM: the in-place update of a short product (rank-k update), whose
+// epilogue streams the caller's rows through shared memory (below).
+enum OutMode : int { OUT_WORKSPACE = 0, OUT_CALLER = 1, OUT_CALLER_BF16 = 2, OUT_UPDATE_STREAM = 3 };
 // Epilogue warps: two per 32-lane TMEM quadrant (eight), each taking every other 64-column
 // block of the tile, with one staging buffer each; OUT_CALLER uses one warp per quadrant
 // (four) with two staging buffers each (its general output code needs more registers).
@@ -81,10 +83,25 @@ constexpr int TMEM_COLS = 512;   // two 256-column fp32 accumulators
 // swizzled by row).
 constexpr int EP_BYTES = 32 * 64 * 2;             // 4 KB
 constexpr int STAGING_BYTES = 8 * EP_BYTES;       // 32 KB
+// OUT_UPDATE_STREAM: a 2-stage operand ring (a short product keeps the tensor cores busy
+// with one tile's operands in flight), and per epilogue warp a ring of STREAM_SLOTS staging
+// blocks into which the warp copies the old values of its next blocks (cp.async) while it
+// works on the current ones.
+constexpr int STREAM_STAGES = 2;
+constexpr int STREAM_SLOTS = 3;
+constexpr int STREAM_MAX_KB = 2;                  // products of at most 2 k-blocks (K <= 256)
+constexpr int stages_of(int mode) { return mode == OUT_UPDATE_STREAM ? STREAM_STAGES : STAGES; }
+constexpr int staging_of(int mode) {
+  return mode == OUT_UPDATE_STREAM ? 8 * STREAM_SLOTS * EP_BYTES : STAGING_BYTES;
+}
+constexpr size_t smem_of(int mode) {
+  return 1024 /*align*/ + size_t(stages_of(mode)) * STAGE_BYTES + size_t(staging_of(mode)) +
+         256 /*barriers*/;
+}
 constexpr int MAX_GROUPS = 8;
-constexpr size_t SMEM_BYTES = 1024 /*align*/ + size_t(STAGES) * STAGE_BYTES +
-                              size_t(STAGING_BYTES) + 256 /*barriers*/;
+constexpr size_t SMEM_BYTES = smem_of(OUT_WORKSPACE);
 static_assert(SMEM_BYTES <= 232448, "shared memory budget of one CTA");
+static_assert(smem_of(OUT_UPDATE_STREAM) <= 232448, "shared memory budget of one CTA");
 }  // namespace tc
 
 enum NsStage : int32_t { NS_GRAM = 1, NS_POLY = 2, NS_APPLY = 3 };

@@ -537,6 +537,64 @@ __device__ __forceinline__ void upd_apply(uint8_t* S, int lane, const float* w, 
   __syncwarp();
 }
 
+// OUT_UPDATE_STREAM: the old values of a 32 x 64 block travel straight into a staging
+// slot (16-byte cp.async per lane, same chunk layout as upd_load, L2 only), are turned
+// into the new values in place (one row per lane), and leave with coalesced 16-byte stores.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ void slot_fill(const OutEntry& e, uint8_t* S, int i0, int jb, int M,
+                                          int lane) {
+  const __nv_bfloat16* base = reinterpret_cast<const __nv_bfloat16*>(upd_src(e)) + jb + 8 * (lane & 7);
+  const int64_t ld = upd_src_ld(e);
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const int r = (lane >> 3) + 4 * q;
+    const int gi = i0 + r;
+    if (gi < M) cp_async16(smem_u32(S + srow(r, lane & 7)), base + int64_t(gi) * ld);
+  }
+}
+
+__device__ __forceinline__ void slot_apply(uint8_t* S, int lane, const float* w, float alpha) {
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    uint4 u = *reinterpret_cast<const uint4*>(S + srow(lane, k));
+    uint32_t* h = reinterpret_cast<uint32_t*>(&u);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float lo = __uint_as_float(h[q] << 16), hi = __uint_as_float(h[q] & 0xFFFF0000u);
+      h[q] = pack_bf16x2(__fmaf_rn(alpha, w[8 * k + 2 * q], lo),
+                         __fmaf_rn(alpha, w[8 * k + 2 * q + 1], hi));
+    }
+    *reinterpret_cast<uint4*>(S + srow(lane, k)) = u;
+  }
+}
+
+__device__ __forceinline__ void slot_store(const OutEntry& e, const uint8_t* S, int i0, int jb,
+                                           int M, int lane) {
+  __nv_bfloat16* base = reinterpret_cast<__nv_bfloat16*>(e.out) + jb + 8 * (lane & 7);
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const int r = (lane >> 3) + 4 * q;
+    const int gi = i0 + r;
+    if (gi < M) {
+      const uint4 v = *reinterpret_cast<const uint4*>(S + srow(r, lane & 7));
+      asm volatile("st.global.L1::no_allocate.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(
+                       base + int64_t(gi) * e.ld),
+                   "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                   : "memory");
+    }
+  }
+}
+
 // Update of the caller's matrix for this lane's row, columns jb..jb+63:
 // out = fmaf(alpha, acc, old) in fp32, rounded to out's dtype (old: upd_src).
 __device__ __forceinline__ void update_final(const OutEntry& e, int i0, int jb, int M, int N,
@@ -598,16 +656,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads(MODE), 1)
   constexpr bool FINAL = MODE != OUT_WORKSPACE;
   constexpr int NEPI = epi_warps(MODE);   // epilogue warps
   constexpr int SPLIT = NEPI / 4;         // epilogue warps per TMEM quadrant
+  constexpr int NST = stages_of(MODE);    // operand ring stages
+  constexpr bool STREAM = MODE == OUT_UPDATE_STREAM;
+  static_assert(!STREAM || STAGE == TC_UPDATE, "the streamed epilogue is the update's");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* ring = smem;
-  uint8_t* staging = smem + STAGES * STAGE_BYTES;
+  uint8_t* staging = smem + NST * STAGE_BYTES;
   uint64_t* bars =
-      reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES + STAGING_BYTES);
-  uint64_t* full_bar = bars;                // [STAGES]  (used in the even CTA)
-  uint64_t* empty_bar = bars + STAGES;      // [STAGES]
-  uint64_t* tfull_bar = bars + 2 * STAGES;  // [2]
+      reinterpret_cast<uint64_t*>(smem + NST * STAGE_BYTES + staging_of(MODE));
+  uint64_t* full_bar = bars;                // [NST]  (used in the even CTA)
+  uint64_t* empty_bar = bars + NST;         // [NST]
+  uint64_t* tfull_bar = bars + 2 * NST;     // [2]
   uint64_t* tempty_bar = tfull_bar + 2;     // [2]       (used in the even CTA)
   uint64_t* drain_bar = tempty_bar + 2;     // [1]
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain_bar + 1);
@@ -621,7 +682,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads(MODE), 1)
   const int npairs = gridDim.x >> 1;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
+    for (int s = 0; s < NST; ++s) {
       mbar_init(smem_u32(&full_bar[s]), 1);
       mbar_init(smem_u32(&empty_bar[s]), 1);
     }
@@ -730,7 +791,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads(MODE), 1)
           if (mn) tma_load_4d_pair(dst, map, fb, 0, k0, rc / CHUNK, t.z);
           else tma_load_4d_pair(dst, map, fb, 0, rc, k0 / CHUNK, t.z);
         }
-        if (++stage == STAGES) {
+        if (++stage == NST) {
           stage = 0;
           phase ^= 1u;
         }
@@ -739,7 +800,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads(MODE), 1)
     // after an abort, the loads already issued land before the CTA leaves: the leader's full
     // barriers count both CTAs' bytes of every armed stage (bounded waits)
     if (*abort_flag && leader && lane == 0) {
-      for (int s = 0; s < STAGES; ++s)
+      for (int s = 0; s < NST; ++s)
         if ((armed >> s) & 1u) mbar_drain(smem_u32(&full_bar[s]), (armed_phase >> s) & 1u, 20000000ull);
     }
     __syncwarp();
@@ -807,7 +868,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads(MODE), 1)
 #ifdef MAO_TC_TRACE
           atomicAdd(&g_tc_trace[8], (unsigned long long)(clock64() - t_issue));
 #endif
-          if (++stage == STAGES) {
+          if (++stage == NST) {
             stage = 0;
             phase ^= 1u;
           }
@@ -820,6 +881,123 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads(MODE), 1)
         mbar_drain(smem_u32(drain_bar), 0u, 1000000000ull);
       }
     }
+    __syncwarp();
+  } else if (STREAM) {
+    // ------------------------------------------- streamed update epilogue (both CTAs)
+    // Warp (quad, part) takes blocks part and part + 2 of its tiles: item 2k + e is block
+    // part + 2e of the warp's k-th tile. Item j's old values are copied into slot j % 3 of
+    // the warp's ring, one commit group per item (empty for a block that is absent or
+    // written by the per-row path): items 2k + 2 at the start of tile k, 2k + 3 once item
+    // 2k has been written out. So a block's rows are in flight for about a tile before the
+    // accumulator is applied to them, and no register holds them meanwhile.
+    const int quad = warp & 3;
+    const int part = (warp - 2) / 4;
+    uint8_t* slots = staging + (warp - 2) * STREAM_SLOTS * EP_BYTES;
+    const uint32_t tempty_leader[2] = {mapa_shared(smem_u32(&tempty_bar[0]), 0),
+                                       mapa_shared(smem_u32(&tempty_bar[1]), 0)};
+    auto fill = [&](const Tile& t, const OutEntry& e, int pos, int j) {
+      const TcGroup& G = p.g[t.g];
+      const int nb = min(BN / 64, (G.N - t.col0 + 63) / 64);
+      const int b = part + SPLIT * pos;
+      const int jb = t.col0 + 64 * b;
+      if (b < nb && upd_block_vec(e, jb, G.N))
+        slot_fill(e, slots + (j % STREAM_SLOTS) * EP_BYTES, t.row0 + HALF * int(cta) + 32 * quad,
+                  jb, G.M, lane);
+      cp_async_commit();
+    };
+    int tile = pair;
+    Tile tc, tn;
+    OutEntry oc, on;
+    bool hc = tile < p.total_tiles;
+    bool hn = tile + npairs < p.total_tiles;
+    if (hc) {
+      decode_tile(p, tile, tc);
+      oc = p.out_table[p.g[tc.g].slot0 + tc.z];
+    }
+    if (hn) {
+      decode_tile(p, tile + npairs, tn);
+      on = p.out_table[p.g[tn.g].slot0 + tn.z];
+    }
+    if (hc) {
+      fill(tc, oc, 0, 0);
+      fill(tc, oc, 1, 1);
+    }
+    for (int local = 0; hc; ++local) {
+      // the tile after next: its entry is loaded now and used a tile from now
+      const int tile2 = tile + 2 * npairs;
+      const bool h2 = tile2 < p.total_tiles;
+      Tile t2;
+      OutEntry o2;
+      if (h2) {
+        decode_tile(p, tile2, t2);
+        o2 = p.out_table[p.g[t2.g].slot0 + t2.z];
+      }
+      const int j0 = 2 * local;
+      if (hn) fill(tn, on, 0, j0 + 2);
+      else cp_async_commit();
+      const TcGroup& G = p.g[tc.g];
+      const int acc = local & 1;
+      const uint32_t acc_phase = uint32_t(local >> 1) & 1u;
+      const bool scaled = p.scale != nullptr;
+      const float s = scaled ? p.scale[G.slot0 + tc.z] : 1.0f;
+      const int i0 = tc.row0 + HALF * int(cta) + 32 * quad;
+      const int nb = min(BN / 64, (G.N - tc.col0 + 63) / 64);
+#ifdef MAO_TC_TRACE
+      const long long tw2 = clock64();
+#endif
+      if (!mbar_wait(smem_u32(&tfull_bar[acc]), acc_phase, abort_flag, limit)) break;
+      tc_fence_after();
+#ifdef MAO_TC_TRACE
+      if (lane == 0 && leader) TRACE_ADD(3, tw2);
+      const long long tb = clock64();
+#endif
+      const uint32_t trow = tmem_base + (uint32_t(32 * quad) << 16) + uint32_t(acc * BN);
+      bool vec[2] = {false, false};
+#pragma unroll
+      for (int pos = 0; pos < 2; ++pos) {
+        const int b = part + SPLIT * pos;
+        if (pos == 0) cp_async_wait<2>();
+        else cp_async_wait<1>();
+        __syncwarp();
+        if (b >= nb) continue;
+        const int jb = tc.col0 + 64 * b;
+        float w[64];
+        tmem_ld64(trow + uint32_t(64 * b), w);
+        if (scaled) {
+#pragma unroll
+          for (int c = 0; c < 64; ++c) w[c] *= s;
+        }
+        vec[pos] = upd_block_vec(oc, jb, G.N);
+        if (vec[pos]) slot_apply(slots + ((j0 + pos) % STREAM_SLOTS) * EP_BYTES, lane, w, p.a);
+        else update_final(oc, i0, jb, G.M, G.N, lane, w, p.a);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(tempty_leader[acc]);
+      // the new rows leave after the accumulator has been released
+      if (vec[0]) slot_store(oc, slots + (j0 % STREAM_SLOTS) * EP_BYTES, i0, tc.col0 + 64 * part,
+                             G.M, lane);
+      __syncwarp();
+      if (hn) fill(tn, on, 1, j0 + 3);
+      else cp_async_commit();
+      if (vec[1]) slot_store(oc, slots + ((j0 + 1) % STREAM_SLOTS) * EP_BYTES, i0,
+                             tc.col0 + 64 * (part + SPLIT), G.M, lane);
+      __syncwarp();
+#ifdef MAO_TC_TRACE
+      if (lane == 0 && leader) {
+        TRACE_ADD(4, tb);
+        if (warp == 2) atomicAdd(&g_tc_trace[6], 1ull);
+      }
+#endif
+      tile += npairs;
+      tc = tn;
+      oc = on;
+      hc = hn;
+      tn = t2;
+      on = o2;
+      hn = h2;
+    }
+    asm volatile("cp.async.wait_all;" ::: "memory");
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue (both CTAs)
@@ -1024,18 +1202,20 @@ mao_status tc_encode_store_map(CUtensorMap* map, const void* base, int64_t rows,
 mao_status tc_gemm_launch(const TcParams& p, cudaStream_t stream) {
   if (p.total_tiles <= 0) return MAO_OK;
   using Kernel = void (*)(TcParams);
-  const Kernel kernels[6] = {
+  const Kernel kernels[7] = {
       ns_tc_kernel<NS_GRAM, OUT_WORKSPACE>, ns_tc_kernel<NS_POLY, OUT_WORKSPACE>,
       ns_tc_kernel<NS_APPLY, OUT_WORKSPACE>, ns_tc_kernel<NS_APPLY, OUT_CALLER>,
-      ns_tc_kernel<TC_UPDATE, OUT_CALLER_BF16>, ns_tc_kernel<NS_APPLY, OUT_CALLER_BF16>};
+      ns_tc_kernel<TC_UPDATE, OUT_CALLER_BF16>, ns_tc_kernel<NS_APPLY, OUT_CALLER_BF16>,
+      ns_tc_kernel<TC_UPDATE, OUT_UPDATE_STREAM>};
   static std::once_flag attr_once[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return MAO_ERR_CUDA;
   cudaError_t attr_err = cudaSuccess;
   std::call_once(attr_once[dev & 63], [&] {
-    for (Kernel k : kernels) {
+    for (int i = 0; i < 7; ++i) {
+      const size_t bytes = smem_of(i == 6 ? OUT_UPDATE_STREAM : OUT_WORKSPACE);
       const cudaError_t e =
-          cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, int(SMEM_BYTES));
+          cudaFuncSetAttribute(kernels[i], cudaFuncAttributeMaxDynamicSharedMemorySize, int(bytes));
       if (e != cudaSuccess) attr_err = e;
     }
   });
@@ -1045,20 +1225,25 @@ mao_status tc_gemm_launch(const TcParams& p, cudaStream_t stream) {
   const bool final_out = p.g[0].final_out != 0 || p.stage == TC_UPDATE;
   if (p.stage < NS_GRAM || p.stage > TC_UPDATE || (final_out && p.stage < NS_APPLY))
     return MAO_ERR_INVALID_ARG;
-  // the rank-k update writes through its own per-lane path: eight epilogue warps
+  // the update writes through its own paths with eight epilogue warps: streamed through
+  // shared memory when every product is short (the epilogue bounds it), else from registers
+  bool short_k = true;
+  for (int g = 0; g < p.ngroups; ++g) short_k = short_k && p.g[g].K <= STREAM_MAX_KB * BK;
   const int mode = !final_out ? OUT_WORKSPACE
+                   : p.stage == TC_UPDATE && short_k ? OUT_UPDATE_STREAM
                    : p.stage == TC_UPDATE ||
                            (p.stage == NS_APPLY && p.out_mode == OUT_CALLER_BF16)
                        ? OUT_CALLER_BF16
                        : OUT_CALLER;
-  const Kernel k = p.stage == TC_UPDATE  ? kernels[4]
+  const Kernel k = mode == OUT_UPDATE_STREAM ? kernels[6]
+                   : p.stage == TC_UPDATE  ? kernels[4]
                    : mode == OUT_CALLER_BF16 ? kernels[5]
                    : kernels[final_out ? 3 : p.stage - NS_GRAM];
   const int pairs = p.total_tiles < num_sms() / 2 ? p.total_tiles : num_sms() / 2;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(unsigned(2 * pairs));
   cfg.blockDim = dim3(unsigned(threads(mode)));
-  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.dynamicSmemBytes = smem_of(mode);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
