@@ -373,20 +373,31 @@ __device__ __forceinline__ void store_rows(const uint8_t* S, __nv_bfloat16* dst,
   }
 }
 
-// This lane's residual row: 64 bf16 values (row i, columns jb..jb+63) as eight 16-byte
-// words, loaded straight into registers (zeros for rows at or beyond M). Rows of the
+// The warp's 32 residual rows of a block (columns jb..jb+63) in row-contiguous 128-byte
+// pieces: lane l holds 16-byte chunk l % 8 of rows l / 8 + 4 q (zeros past M). res_rows
+// later turns them into one row per lane through the warp's staging buffer. Rows of the
 // workspace are 128-byte aligned and zero-padded to a multiple of 64 columns, so the 64
 // columns of a block are always addressable.
-__device__ __forceinline__ void load_res_row(const __nv_bfloat16* src, int64_t ld, int i, int jb,
-                                             int M, uint4 (&r)[8]) {
-  if (i < M) {
-    const uint4* q = reinterpret_cast<const uint4*>(src + int64_t(i) * ld + jb);
+__device__ __forceinline__ void load_res_block(const __nv_bfloat16* src, int64_t ld, int i0,
+                                               int jb, int M, int lane, uint4 (&r)[8]) {
+  const __nv_bfloat16* base = src + jb + 8 * (lane & 7);
 #pragma unroll
-    for (int k = 0; k < 8; ++k) r[k] = __ldg(q + k);
-  } else {
-#pragma unroll
-    for (int k = 0; k < 8; ++k) r[k] = make_uint4(0u, 0u, 0u, 0u);
+  for (int q = 0; q < 8; ++q) {
+    const int gi = i0 + (lane >> 3) + 4 * q;
+    r[q] = gi < M ? __ldg(reinterpret_cast<const uint4*>(base + int64_t(gi) * ld))
+                  : make_uint4(0u, 0u, 0u, 0u);
   }
+}
+
+// r (load_res_block's layout) -> this lane's row, through the 4 KB staging buffer S.
+__device__ __forceinline__ void res_rows(uint8_t* S, int lane, uint4 (&r)[8]) {
+  const int sg = lane & 7;
+#pragma unroll
+  for (int q = 0; q < 8; ++q) *reinterpret_cast<uint4*>(S + srow((lane >> 3) + 4 * q, sg)) = r[q];
+  __syncwarp();
+#pragma unroll
+  for (int k = 0; k < 8; ++k) r[k] = *reinterpret_cast<const uint4*>(S + srow(lane, k));
+  __syncwarp();
 }
 
 // Element c (0..63) of a residual row held as eight 16-byte words.
@@ -1033,8 +1044,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads(MODE), 1)
         const __nv_bfloat16* res =
             reinterpret_cast<const __nv_bfloat16*>(G.res) + int64_t(t.z) * G.res_mstride;
         static_assert(STAGE != NS_POLY || SPLIT == 2, "residual registers cover two blocks");
-        if (part < nb) load_res_row(res, G.res_ld, i, t.col0 + 64 * part, G.M, res0);
-        if (part + SPLIT < nb) load_res_row(res, G.res_ld, i, t.col0 + 64 * (part + SPLIT), G.M, res1);
+        if (part < nb) load_res_block(res, G.res_ld, i0, t.col0 + 64 * part, G.M, lane, res0);
+        if (part + SPLIT < nb)
+          load_res_block(res, G.res_ld, i0, t.col0 + 64 * (part + SPLIT), G.M, lane, res1);
       }
       // TC_UPDATE: the old values of the caller's rows, likewise
       if (STAGE == TC_UPDATE) {
@@ -1070,7 +1082,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads(MODE), 1)
           }
         } else if (STAGE == NS_POLY) {
           // B' = c (A A) + b A, plus a on the diagonal
-          const uint4(&r)[8] = nth == 0 ? res0 : res1;
+          // the staging buffer must have been read by this warp's previous bulk store
+          uint4(&r)[8] = nth == 0 ? res0 : res1;
+          if (lane == 0) bulk_wait_read();
+          __syncwarp();
+          res_rows(S, lane, r);
 #pragma unroll
           for (int c = 0; c < 64; ++c) w[c] = __fmaf_rn(p.c, w[c], p.b * res_elem(r, c));
           if (i0 < jb + 64 && jb < i0 + 32) {  // the block meets the diagonal
