@@ -178,6 +178,36 @@ __device__ __forceinline__ void stage_load8(const StageEntry& e, int64_t row, in
   }
 }
 
+// One unit (8 elements of a row, `valid` of them inside the matrix) of the general path:
+// the source values as fp32. With momentum fused in, M <- fmaf(mu, M, G) rounded to M's
+// dtype is written back, and the rounded values are what Newton–Schulz orthogonalises (as
+// if M had been updated first).
+__device__ __forceinline__ void stage_unit(const StageEntry& e, float mu, int64_t row,
+                                           int64_t col0, int valid, float (&v)[8]) {
+  stage_load8(e, row, col0, valid, v);
+  if (!e.g || valid <= 0) return;
+  float gv[8];
+  if (e.vec_src && valid == 8) {
+    load8(e.g, row * e.g_ld + col0, e.g_dt, gv);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) gv[i] = i < valid ? load_elem(e.g, row * e.g_ld + col0 + i, e.g_dt) : 0.0f;
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float m = __fmaf_rn(mu, v[i], gv[i]);
+    v[i] = i < valid ? (e.src_dt == MAO_BF16 ? __bfloat162float(__float2bfloat16_rn(m)) : m) : 0.0f;
+  }
+  void* mo = const_cast<void*>(e.src);
+  if (e.vec_src && valid == 8) {
+    store8(mo, row * e.src_ld + col0, e.src_dt, v);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      if (i < valid) store_elem(mo, row * e.src_ld + col0 + i, e.src_dt, v[i]);
+  }
+}
+
 // Copies each input into its workspace slot (converting to the compute type) and writes
 // one fp32 partial sum of squares per block; records the slot's output entry.
 __global__ void __launch_bounds__(kStageThreads) stage_in_kernel(const __grid_constant__ StageParams p) {
@@ -195,44 +225,85 @@ __global__ void __launch_bounds__(kStageThreads) stage_in_kernel(const __grid_co
   }
   float sq = 0.0f;
   const int64_t u0 = blk * kStageUnitsPerBlock;
-#pragma unroll 1
-  for (int t = 0; t < kStageUnitsPerBlock / kStageThreads; ++t) {
-    const int64_t u = u0 + t * kStageThreads + threadIdx.x;
-    if (u >= e.units) break;
-    // units cover the padded workspace row: columns >= cols are written as zeros
-    const int64_t row = u / e.units_per_row;
-    const int64_t col0 = (u - row * e.units_per_row) * 8;
-    const int64_t left = e.cols - col0;
-    const int valid = int(left >= 8 ? 8 : (left > 0 ? left : 0));
-    float v[8];
-    stage_load8(e, row, col0, valid, v);
-    if (e.g && valid > 0) {
-      // momentum: M <- fmaf(mu, M, G) rounded to M's dtype, written back; the rounded
-      // values are what Newton–Schulz orthogonalises (as if M had been updated first)
-      float gv[8];
-      if (e.vec_src && valid == 8) {
-        load8(e.g, row * e.g_ld + col0, e.g_dt, gv);
-      } else {
+  constexpr int U = kStageUnitsPerBlock / kStageThreads;
+  if (e.src_dt == MAO_BF16 && p.ws_dt == MAO_BF16 && e.vec_src && (!e.g || e.g_dt == MAO_BF16) &&
+      e.units <= 0xFFFFFFFFll) {
+    // bf16 rows with 16-byte accesses: every unit's loads are issued before any arithmetic,
+    // and the values stay packed until used. Same arithmetic and order as the loop below.
+    const uint32_t upr = uint32_t(e.units_per_row);
+    uint4 m[U], g[U];
+    uint32_t row[U], col0[U];
+    bool live[U], full[U];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) gv[i] = i < valid ? load_elem(e.g, row * e.g_ld + col0 + i, e.g_dt) : 0.0f;
-      }
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float m = __fmaf_rn(p.mu, v[i], gv[i]);
-        v[i] = i < valid ? (e.src_dt == MAO_BF16 ? __bfloat162float(__float2bfloat16_rn(m)) : m) : 0.0f;
-      }
-      void* mo = const_cast<void*>(e.src);
-      if (e.vec_src && valid == 8) {
-        store8(mo, row * e.src_ld + col0, e.src_dt, v);
-      } else {
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-          if (i < valid) store_elem(mo, row * e.src_ld + col0 + i, e.src_dt, v[i]);
+    for (int t = 0; t < U; ++t) {
+      const int64_t u = u0 + t * kStageThreads + threadIdx.x;
+      live[t] = u < e.units;
+      const uint32_t uu = live[t] ? uint32_t(u) : 0u;
+      row[t] = uu / upr;
+      col0[t] = (uu - row[t] * upr) * 8u;
+      full[t] = live[t] && int64_t(col0[t]) + 8 <= e.cols;
+      if (full[t]) {
+        m[t] = *reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(e.src) +
+                                               int64_t(row[t]) * e.src_ld + col0[t]);
+        if (e.g)
+          g[t] = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(e.g) +
+                                                      int64_t(row[t]) * e.g_ld + col0[t]));
       }
     }
 #pragma unroll
-    for (int i = 0; i < 8; ++i) sq = __fmaf_rn(v[i], v[i], sq);
-    store8(e.dst, row * e.dst_ld + col0, p.ws_dt, v);
+    for (int t = 0; t < U; ++t) {
+      if (!live[t]) continue;
+      float v[8];
+      if (full[t]) {
+        uint32_t* h = reinterpret_cast<uint32_t*>(&m[t]);
+        const uint32_t* hg = reinterpret_cast<const uint32_t*>(&g[t]);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          v[2 * k] = __uint_as_float(h[k] << 16);
+          v[2 * k + 1] = __uint_as_float(h[k] & 0xFFFF0000u);
+        }
+        if (e.g) {
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const __nv_bfloat162 b = __floats2bfloat162_rn(
+                __fmaf_rn(p.mu, v[2 * k], __uint_as_float(hg[k] << 16)),
+                __fmaf_rn(p.mu, v[2 * k + 1], __uint_as_float(hg[k] & 0xFFFF0000u)));
+            h[k] = *reinterpret_cast<const uint32_t*>(&b);
+            v[2 * k] = __uint_as_float(h[k] << 16);
+            v[2 * k + 1] = __uint_as_float(h[k] & 0xFFFF0000u);
+          }
+          *reinterpret_cast<uint4*>(const_cast<__nv_bfloat16*>(
+              reinterpret_cast<const __nv_bfloat16*>(e.src) + int64_t(row[t]) * e.src_ld + col0[t])) = m[t];
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) sq = __fmaf_rn(v[i], v[i], sq);
+        *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(e.dst) + int64_t(row[t]) * e.dst_ld +
+                                  col0[t]) = m[t];
+      } else {
+        const int64_t left = e.cols - int64_t(col0[t]);
+        const int valid = int(left >= 8 ? 8 : (left > 0 ? left : 0));
+        stage_unit(e, p.mu, row[t], col0[t], valid, v);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) sq = __fmaf_rn(v[i], v[i], sq);
+        store8(e.dst, int64_t(row[t]) * e.dst_ld + col0[t], p.ws_dt, v);
+      }
+    }
+  } else {
+#pragma unroll 1
+    for (int t = 0; t < U; ++t) {
+      const int64_t u = u0 + t * kStageThreads + threadIdx.x;
+      if (u >= e.units) break;
+      // units cover the padded workspace row: columns >= cols are written as zeros
+      const int64_t row = u / e.units_per_row;
+      const int64_t col0 = (u - row * e.units_per_row) * 8;
+      const int64_t left = e.cols - col0;
+      const int valid = int(left >= 8 ? 8 : (left > 0 ? left : 0));
+      float v[8];
+      stage_unit(e, p.mu, row, col0, valid, v);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) sq = __fmaf_rn(v[i], v[i], sq);
+      store8(e.dst, row * e.dst_ld + col0, p.ws_dt, v);
+    }
   }
   // fixed-order block reduction: warp tree, then warp 0 over the warp sums
   __shared__ float wsum[kStageThreads / 32];
