@@ -152,15 +152,8 @@ __device__ __forceinline__ float round_to(float v, int32_t dt) {
   return dt == MAO_BF16 ? __bfloat162float(__float2bfloat16_rn(v)) : v;
 }
 
-// Units of 8 columns over the zero-padded rows of Bw; blockIdx.y = slot. Bw = bf16 of
-// B = M + G rounded to M's dtype, and M <- B when M is fp32. A bf16 M is left as it is:
-// Bw then holds B exactly, and the M update reads B from there (its output entry's source).
-__global__ void __launch_bounds__(256) dion_stage_kernel(const __grid_constant__ DionCommon c) {
-  const DionSlot& e = c.slots[blockIdx.y];
-  const uint32_t upr = uint32_t(e.ldn) / 8;
-  const uint32_t u = blockIdx.x * blockDim.x + threadIdx.x;
-  if (u >= uint32_t(e.m) * upr) return;
-  const int64_t row = u / upr, col0 = int64_t(u - uint32_t(row) * upr) * 8;
+// One unit of the general path: Bw(row, col0 .. col0 + 7), and M when it is fp32.
+__device__ __forceinline__ void dion_stage_unit(const DionSlot& e, int64_t row, int64_t col0) {
   float b[8];
   if (e.vec && col0 + 8 <= e.n) {
     float mv[8], gv[8];
@@ -184,6 +177,68 @@ __global__ void __launch_bounds__(256) dion_stage_kernel(const __grid_constant__
     }
   }
   store8(e.Bw, row * e.ldn + col0, MAO_BF16, b);
+}
+
+// Units of 8 columns over the zero-padded rows of Bw; blockIdx.y = slot. Bw = bf16 of
+// B = M + G rounded to M's dtype, and M <- B when M is fp32. A bf16 M is left as it is:
+// Bw then holds B exactly, and the M update reads B from there (its output entry's source).
+// kStageUnits units per thread, 256 kStageUnits per block (a thread's units are 256 apart,
+// so each load instruction of a warp reads 512 contiguous bytes).
+constexpr int kStageUnits = 4;
+
+__global__ void __launch_bounds__(256) dion_stage_kernel(const __grid_constant__ DionCommon c) {
+  const DionSlot& e = c.slots[blockIdx.y];
+  const uint32_t upr = uint32_t(e.ldn) / 8;
+  const uint32_t units = uint32_t(e.m) * upr;
+  const uint32_t ub = blockIdx.x * (256u * kStageUnits) + threadIdx.x;
+  if (ub >= units) return;
+  if (e.vec && e.dtm == MAO_BF16 && e.dtg == MAO_BF16) {
+    // bf16 M and G: every unit's loads are issued before any arithmetic; B = bf16(M + G)
+    // as in dion_stage_unit
+    uint4 mv[kStageUnits], gv[kStageUnits];
+    uint32_t row[kStageUnits], col0[kStageUnits];
+    bool live[kStageUnits], full[kStageUnits];
+#pragma unroll
+    for (int t = 0; t < kStageUnits; ++t) {
+      const uint32_t u = ub + 256u * t;
+      live[t] = u < units;
+      row[t] = (live[t] ? u : 0u) / upr;
+      col0[t] = ((live[t] ? u : 0u) - row[t] * upr) * 8u;
+      full[t] = live[t] && int64_t(col0[t]) + 8 <= e.n;
+      if (full[t]) {
+        mv[t] = *reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(e.M) +
+                                                int64_t(row[t]) * e.ldm + col0[t]);
+        gv[t] = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(e.G) +
+                                                     int64_t(row[t]) * e.ldg + col0[t]));
+      }
+    }
+#pragma unroll
+    for (int t = 0; t < kStageUnits; ++t) {
+      if (!live[t]) continue;
+      if (!full[t]) {
+        dion_stage_unit(e, row[t], col0[t]);
+        continue;
+      }
+      uint32_t* hm = reinterpret_cast<uint32_t*>(&mv[t]);
+      const uint32_t* hg = reinterpret_cast<const uint32_t*>(&gv[t]);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const __nv_bfloat162 b =
+            __floats2bfloat162_rn(__uint_as_float(hm[k] << 16) + __uint_as_float(hg[k] << 16),
+                                  __uint_as_float(hm[k] & 0xFFFF0000u) + __uint_as_float(hg[k] & 0xFFFF0000u));
+        hm[k] = *reinterpret_cast<const uint32_t*>(&b);
+      }
+      *reinterpret_cast<uint4*>(e.Bw + int64_t(row[t]) * e.ldn + col0[t]) = mv[t];
+    }
+    return;
+  }
+#pragma unroll 1
+  for (int t = 0; t < kStageUnits; ++t) {
+    const uint32_t u = ub + 256u * t;
+    if (u >= units) break;
+    const uint32_t row = u / upr;
+    dion_stage_unit(e, row, int64_t(u - row * upr) * 8);
+  }
 }
 
 // Columns j0 .. j0 + 7 of row i of the caller's Q (zeros at and past r), 16 bytes at a time
@@ -1060,7 +1115,7 @@ mao_status dion_run(const mao_mat* X, const mao_mat* M, const mao_mat* G, const 
   auto blocks = [](int64_t units) { return unsigned(ceil_div(units, 256)); };
   // 1. B = M + G (M <- B), Bw; Qw = bf16(Q_prev)
   profile_before_launch(stream, MAO_PROF_DION_STAGE);
-  dion_stage_kernel<<<dim3(blocks(plan.max_units), nb), 256, 0, stream>>>(c);
+  dion_stage_kernel<<<dim3(unsigned(ceil_div(plan.max_units, 256 * kStageUnits)), nb), 256, 0, stream>>>(c);
   if (!launched()) return MAO_ERR_CUDA;
   profile_before_launch(stream, MAO_PROF_DION_STAGE);
   dion_stage_q_kernel<<<dim3(blocks(plan.max_qunits), nb), 256, 0, stream>>>(c);
