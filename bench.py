@@ -259,7 +259,13 @@ class Step:
             self.mao.apply_update(self.W, wl.lr, vote=self.vote)
 
     def fused_call(self, W_out=None):
+        """The one-call step (muon_step, or dion_step for Dion) writing the new weights to
+        W_out (None: in place)."""
         wl = self.wl
+        if wl.kind == "dion":
+            self.mao.dion_step(self.W, self.M, self.G, self.Q, wl.mu, wl.lr, ws=self.ws,
+                               X_out=W_out)
+            return
         self.mao.muon_step(self.W, self.M, self.G, wl.mu, wl.lr, wl.steps, wl.coeffs, wl.eps,
                            wl.compute, ws=self.ws, W_out=W_out)
 
@@ -837,10 +843,10 @@ def run_e2e(step, K, world, dev, barrier, max_over_ranks):
     Copies run on their own streams and overlap other work where the data allow it: the
     gradients of step k+1 go into the second of two device slabs while step k computes, and
     the weights of step k are read back while step k+1 runs its momentum and Newton–Schulz
-    stages (its update waits for that read). A fused Muon step reads W from one of two device
-    slabs and writes the new W into the other (muon_step's W_out), so the read-back of step
-    k's weights overlaps step k+1, which writes the slab step k read. Every step still moves
-    all of its bytes.
+    stages (its update waits for that read). A one-call step (muon_step, or dion_step) reads
+    W from one of two device slabs and writes the new W into the other (its W_out / X_out),
+    so the read-back of step k's weights overlaps step k+1, which writes the slab step k
+    read. Every step still moves all of its bytes.
     """
     import torch
     main = torch.cuda.current_stream()
@@ -852,8 +858,8 @@ def run_e2e(step, K, world, dev, barrier, max_over_ranks):
     W_dev, W_views = _slab(step.W, dev)
     G_orig, W_orig = step.G, step.W
     step.W = W_views
-    fused = getattr(step, "fused", False)
-    staged = step.wl.kind != "dion" and not fused  # Dion and muon_step update W in one call
+    dion = step.wl.kind == "dion"
+    fused = getattr(step, "fused", False) or dion  # one call updates W: muon_step, dion_step
     # fused: two weight slabs, read one and write the other; one read-back event per slab
     W_bufs = [(W_dev, W_views)] + ([_slab(step.W, dev)] if fused else [])
     w_read_slab = [torch.cuda.Event() for _ in W_bufs]
@@ -882,23 +888,19 @@ def run_e2e(step, K, world, dev, barrier, max_over_ranks):
         g_ready[b].record(s_in)
         main.wait_event(g_ready[b])
         step.G = G_dev[b][1]
-        if staged:
+        if not fused:
             step.momentum()
             g_free[b].record(main)
             step.ns()
             main.wait_event(w_read)           # the previous read-back of W is complete
             step.update()
-        elif fused:
+        else:
             src, dst = k % 2, 1 - k % 2
             step.W = W_bufs[src][1]
             main.wait_event(w_read_slab[dst])  # step k-2's weights have been read back
             step.fused_call(W_out=W_bufs[dst][1])
             g_free[b].record(main)
             W_src = W_bufs[dst][0]
-        else:
-            main.wait_event(w_read)
-            step()
-            g_free[b].record(main)
         w_done.record(main)
         s_out.wait_event(w_done)
         with torch.cuda.stream(s_out):
@@ -919,8 +921,8 @@ def run_e2e(step, K, world, dev, barrier, max_over_ranks):
             "d2h_bytes_per_step": d2h, "steps": K,
             "copies": "one pinned H2D slab and one D2H slab per step, on copy streams overlapping "
                       "the neighbouring steps' compute" +
-                      ("; two device weight slabs, read one, write the other (fused step)"
-                       if fused else "")}
+                      ("; two device weight slabs, read one, write the other (%s)"
+                       % ("dion_step's X_out" if dion else "muon_step's W_out") if fused else "")}
 
 
 def read_traffic(wl):

@@ -302,6 +302,10 @@ mao_status apply_update(const mao_mat* W, const uint32_t* const* vote, const mao
  * column by its Euclidean norm (a zero column stays zero).
  *   X[b], M[b]  in/out, f32 or bf16, m x n;  G[b] in, f32 or bf16, m x n.
  *   Q[b]        in/out, f32, n x r (any ld): the previous right factor in, the new one out.
+ *   X_out       NULL (X is updated in place), or HOST array of `batch` matrices of X[b]'s
+ *               shape and dtype receiving X - lr P Q^T; X is then only read. X_out[b] may
+ *               be X[b] itself (same data and ld: in place) and must not overlap it
+ *               otherwise. Lets a caller read back one step's X while the next step runs.
  *   P_out       NULL, or HOST array of `batch` device pointers (each may be NULL): the
  *               final P, m x r fp32, row stride r.
  *   rank        1..256, at most min(m, n) of every matrix; batch <= 65535.
@@ -309,14 +313,16 @@ mao_status apply_update(const mao_mat* W, const uint32_t* const* vote, const mao
  *               the three dense products (B Q, B^T P, P R^T / P Q^T) as bf16 with fp32
  *               accumulation on tcgen05 tensor cores; everything else is fp32.
  *   workspace   >= dion_workspace_bytes(X, batch, rank) bytes, 256-byte aligned.
- *   Errors: MAO_ERR_INVALID_ARG for mismatched shapes of X, M, G, Q or a bad rank;
+ *   Errors: MAO_ERR_INVALID_ARG for mismatched shapes of X, M, G, Q, X_out (or X_out's
+ *   dtype differing from X's) or a bad rank;
  *   B Q without full column rank (a non-positive Cholesky pivot) is reported by
  *   mao_sync_status() as MAO_ERR_NUMERIC (the pivot is replaced by 1e-30).
  */
 size_t dion_workspace_bytes(const mao_mat* X, int32_t batch, int32_t rank);
 mao_status dion_step(const mao_mat* X, const mao_mat* M, const mao_mat* G, const mao_mat* Q,
-                     float* const* P_out, int32_t batch, int32_t rank, float mu, float lr,
-                     int32_t compute, void* workspace, size_t workspace_bytes, void* stream);
+                     const mao_mat* X_out, float* const* P_out, int32_t batch, int32_t rank,
+                     float mu, float lr, int32_t compute, void* workspace,
+                     size_t workspace_bytes, void* stream);
 
 /*
  * Bound of every device-side wait of the tensor-core kernels (default 4 s), used by launches

@@ -293,10 +293,11 @@ def _q_mat(q):
                        _abi.MAO_F32, 0)
 
 
-def dion_step(X, M, G, Q, mu, lr, P_out=None, ws=None, stream=None):
+def dion_step(X, M, G, Q, mu, lr, P_out=None, ws=None, stream=None, X_out=None):
     """One Dion step for each (X, M, G, Q), any mix of shapes, one rank: X and M updated in
     place, Q replaced by the new right factor (n x r, float32). P_out: optional float32
-    tensors (m x r, contiguous) receiving the final P."""
+    tensors (m x r, contiguous) receiving the final P. X_out: optional tensors of X's shapes
+    and dtypes receiving the new X (X is then only read)."""
     Xs, Ms, Gs, Qs = _as_list(X), _as_list(M), _as_list(G), _as_list(Q)
     rank = Qs[0].shape[1]
     if any(q.shape[1] != rank for q in Qs):
@@ -311,7 +312,13 @@ def dion_step(X, M, G, Q, mu, lr, P_out=None, ws=None, stream=None):
     if ws is None:
         ws = torch.empty(dion_workspace_bytes([tuple(x.shape) for x in Xs], rank),
                          dtype=torch.uint8, device=Xs[0].device)
-    st = lib().dion_step(_mats(Xs), _mats(Ms), _mats(Gs), qarr, parr, len(Xs), int(rank),
+    xo = None
+    if X_out is not None:
+        Xos = _as_list(X_out)
+        if len(Xos) != len(Xs):
+            raise ValueError("X_out needs one tensor per X")
+        xo = _mats(Xos)
+    st = lib().dion_step(_mats(Xs), _mats(Ms), _mats(Gs), qarr, xo, parr, len(Xs), int(rank),
                          float(mu), float(lr), _abi.MAO_BF16, ctypes.c_void_p(ws.data_ptr()),
                          ws.numel(), _stream(stream))
     _abi.check("dion_step", st)

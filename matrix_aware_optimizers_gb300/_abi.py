@@ -131,7 +131,8 @@ def load():
     lib.dion_workspace_bytes.restype = ctypes.c_size_t
     lib.dion_workspace_bytes.argtypes = [P(MaoMat), ctypes.c_int32, ctypes.c_int32]
     lib.dion_step.restype = ctypes.c_int
-    lib.dion_step.argtypes = [P(MaoMat), P(MaoMat), P(MaoMat), P(MaoMat), P(ctypes.c_void_p),
+    lib.dion_step.argtypes = [P(MaoMat), P(MaoMat), P(MaoMat), P(MaoMat), P(MaoMat),
+                              P(ctypes.c_void_p),
                               ctypes.c_int32, ctypes.c_int32, ctypes.c_float, ctypes.c_float,
                               ctypes.c_int32, vp, ctypes.c_size_t, vp]
     lib.mao_set_wait_limit.restype = None

@@ -49,6 +49,7 @@ struct DionSlot {
   void* M;
   const void* G;
   void* X;
+  void* Xo;                         // the updated X (X itself, or the caller's X_out)
   float* Q;
   float* Pout;                      // optional copy of the final P (m x r, row stride r)
   __nv_bfloat16 *Bw, *Qw, *Rw, *Pw; // bf16 operands, rows of ldn / ldr elements
@@ -57,7 +58,7 @@ struct DionSlot {
   float* W;                         // L^-1 in lower 32 x 32 blocks (layout of blk())
   float* cn;                        // column norms of R: partials [nchunks][r], then the norms
   int32_t* cnt;                     // arrival counters of the Gram tiles [2 passes][tiles]
-  int64_t ldm, ldg, ldx, ldq;
+  int64_t ldm, ldg, ldx, ldq, ldxo;
   int32_t m, n, ldn;
   int32_t dtm, dtg, dtx;
   int32_t flags_m, flags_x;
@@ -137,10 +138,11 @@ __global__ void __launch_bounds__(64) dion_setup_kernel(const __grid_constant__ 
     o.src_ld = e.ldn;
   }
   p.c.tM[z] = o;
-  o.src = nullptr;
-  o.src_ld = 0;
-  o.out = e.X;
-  o.ld = e.ldx;
+  // X <- X - lr P Q^T, written to Xo (reading X when Xo is another matrix)
+  o.src = e.Xo != e.X ? e.X : nullptr;
+  o.src_ld = e.Xo != e.X ? e.ldx : 0;
+  o.out = e.Xo;
+  o.ld = e.ldxo;
   o.dtype = e.dtx;
   o.flags = e.flags_x;
   p.c.tX[z] = o;
@@ -1016,8 +1018,8 @@ size_t dion_workspace_size(const mao_mat* X, int32_t batch, int32_t rank) {
 }
 
 mao_status dion_run(const mao_mat* X, const mao_mat* M, const mao_mat* G, const mao_mat* Q,
-                    float* const* P_out, int32_t batch, int32_t rank, float mu, float lr,
-                    void* workspace, cudaStream_t stream) {
+                    const mao_mat* X_out, float* const* P_out, int32_t batch, int32_t rank,
+                    float mu, float lr, void* workspace, cudaStream_t stream) {
   DionPlan plan;
   make_dion_plan(X, batch, rank, plan);
   uint8_t* ws = reinterpret_cast<uint8_t*>(workspace);
@@ -1064,6 +1066,7 @@ mao_status dion_run(const mao_mat* X, const mao_mat* M, const mao_mat* G, const 
       e.M = M[b].data;
       e.G = G[b].data;
       e.X = X[b].data;
+      e.Xo = X_out ? X_out[b].data : X[b].data;
       e.Q = reinterpret_cast<float*>(Q[b].data);
       e.Pout = P_out ? P_out[b] : nullptr;
       e.Bw = reinterpret_cast<__nv_bfloat16*>(ws + g.off_bw) + size_t(k) * g.m * ldn;
@@ -1087,6 +1090,7 @@ mao_status dion_run(const mao_mat* X, const mao_mat* M, const mao_mat* G, const 
       e.ldm = M[b].ld;
       e.ldg = G[b].ld;
       e.ldx = X[b].ld;
+      e.ldxo = X_out ? X_out[b].ld : X[b].ld;
       e.ldq = Q[b].ld;
       e.m = int32_t(g.m);
       e.n = int32_t(g.n);
@@ -1095,7 +1099,7 @@ mao_status dion_run(const mao_mat* X, const mao_mat* M, const mao_mat* G, const 
       e.dtg = G[b].dtype;
       e.dtx = X[b].dtype;
       e.flags_m = out_flags(M[b]);
-      e.flags_x = out_flags(X[b]);
+      e.flags_x = out_flags(X[b]) & (X_out ? out_flags(X_out[b]) : ~0);
       e.vec = vec8_ok(M[b]) && vec8_ok(G[b]) ? 1 : 0;
       e.qvec = (reinterpret_cast<uintptr_t>(Q[b].data) % 16 == 0 && Q[b].ld % 4 == 0) ? 1 : 0;
     }
@@ -1217,8 +1221,9 @@ size_t dion_workspace_bytes(const mao_mat* X, int32_t batch, int32_t rank) {
 }
 
 mao_status dion_step(const mao_mat* X, const mao_mat* M, const mao_mat* G, const mao_mat* Q,
-                     float* const* P_out, int32_t batch, int32_t rank, float mu, float lr,
-                     int32_t compute, void* workspace, size_t workspace_bytes, void* stream) {
+                     const mao_mat* X_out, float* const* P_out, int32_t batch, int32_t rank,
+                     float mu, float lr, int32_t compute, void* workspace,
+                     size_t workspace_bytes, void* stream) {
   if (!X || !M || !G || !Q || batch < 1 || rank < 1 || rank > kMaxRank) return MAO_ERR_INVALID_ARG;
   if (!std::isfinite(mu) || !std::isfinite(lr)) return MAO_ERR_INVALID_ARG;
   if (compute != MAO_BF16) return MAO_ERR_UNSUPPORTED;
@@ -1233,6 +1238,13 @@ mao_status dion_step(const mao_mat* X, const mao_mat* M, const mao_mat* G, const
       return MAO_ERR_INVALID_ARG;
     if (Q[b].dtype != MAO_F32 || Q[b].rows != n || Q[b].cols != rank) return MAO_ERR_INVALID_ARG;
     if (rank > std::min(m, n)) return MAO_ERR_INVALID_ARG;
+    if (X_out) {
+      st = check_mat(X_out[b]);
+      if (st != MAO_OK) return st;
+      if (X_out[b].rows != m || X_out[b].cols != n || X_out[b].dtype != X[b].dtype)
+        return MAO_ERR_INVALID_ARG;
+      if (X_out[b].data == X[b].data && X_out[b].ld != X[b].ld) return MAO_ERR_INVALID_ARG;
+    }
     if (P_out && P_out[b] && reinterpret_cast<uintptr_t>(P_out[b]) % 4 != 0)
       return MAO_ERR_MISALIGNED;
   }
@@ -1241,7 +1253,7 @@ mao_status dion_step(const mao_mat* X, const mao_mat* M, const mao_mat* G, const
   if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0) return MAO_ERR_MISALIGNED;
   if (device_cc() / 10 != 10) return MAO_ERR_UNSUPPORTED;
   if (workspace_bytes < dion_workspace_size(X, batch, rank)) return MAO_ERR_WORKSPACE;
-  return dion_run(X, M, G, Q, P_out, batch, rank, mu, lr, workspace,
+  return dion_run(X, M, G, Q, X_out, P_out, batch, rank, mu, lr, workspace,
                   static_cast<cudaStream_t>(stream));
 }
 

@@ -150,3 +150,40 @@ def test_dion_rejects_bad_arguments(cuda):
         mao.dion_step(X, X.clone(), torch.zeros((64, 95), device=cuda), Q, 0.9, 1.0)
     with pytest.raises(ValueError):    # Q must be float32
         mao.dion_step(X, X.clone(), X.clone(), Q.to(torch.bfloat16), 0.9, 1.0)
+
+
+@pytest.mark.parametrize("xdt", ["bf16", "f32"])
+def test_dion_step_out_of_place(cuda, xdt):
+    """X_out receives exactly what the in-place step writes to X, X is only read, M and Q
+    come out the same; X_out aliasing X is the in-place step."""
+    gen = torch.Generator().manual_seed(91)
+    shapes = [(256, 640), (768, 768), (300, 1000), (200, 72)]  # one rank per call: 32
+    sets = [_inputs(gen, m, n, 32, "bf16", xdt, cuda) for m, n in shapes]
+    X = [s[0] for s in sets]
+    X0 = [x.clone() for x in X]
+    M1, M2 = [s[1].clone() for s in sets], [s[1].clone() for s in sets]
+    Q1, Q2 = [s[3].clone() for s in sets], [s[3].clone() for s in sets]
+    G = [s[2] for s in sets]
+    X_out = [torch.full_like(x, float("nan")) for x in X]
+    mao.dion_step(X, M1, G, Q1, mu=0.9, lr=0.3, X_out=X_out)
+    X_in = [x.clone() for x in X0]
+    mao.dion_step(X_in, M2, G, Q2, mu=0.9, lr=0.3)
+    X_alias = [x.clone() for x in X0]
+    M3, Q3 = [s[1].clone() for s in sets], [s[3].clone() for s in sets]
+    mao.dion_step(X_alias, M3, G, Q3, mu=0.9, lr=0.3, X_out=X_alias)
+    mao.sync_status()
+    for k in range(len(sets)):
+        assert torch.equal(X[k], X0[k])
+        assert torch.equal(X_out[k], X_in[k])
+        assert torch.equal(X_alias[k], X_in[k])
+        assert torch.equal(M1[k], M2[k]) and torch.equal(Q1[k], Q2[k])
+
+
+def test_dion_rejects_bad_x_out(cuda):
+    X = torch.zeros((64, 96), device=cuda)
+    Q = torch.zeros((96, 8), device=cuda)
+    with pytest.raises(mao.MaoError):  # X_out of another shape
+        mao.dion_step(X, X.clone(), X.clone(), Q, 0.9, 1.0, X_out=torch.zeros((64, 95), device=cuda))
+    with pytest.raises(mao.MaoError):  # X_out of another dtype
+        mao.dion_step(X, X.clone(), X.clone(), Q, 0.9, 1.0,
+                      X_out=torch.zeros((64, 96), dtype=torch.bfloat16, device=cuda))
