@@ -800,8 +800,7 @@ def finish_line(args, line, wl, step, K, world, rank, dev, barrier, max_over_ran
     from matrix_aware_optimizers_gb300 import workloads
     # ---------------- end to end: host gradients in, host weights out, every step
     if not args.no_e2e:
-        line["e2e"] = run_e2e(step, K if wl.index != 4 else min(K, 2), world, dev, barrier,
-                              max_over_ranks)
+        line["e2e"] = run_e2e(step, K, world, dev, barrier, max_over_ranks)
 
     # ---------------- CPU baseline: the oracle on a bounded sample (rank 0, N = 1)
     if world == 1 and rank == 0 and not args.no_cpu_baseline:
