@@ -956,7 +956,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads(MODE), 1)
 #ifdef MAO_TC_TRACE
       const long long tw2 = clock64();
 #endif
-      if (!mbar_wait(smem_u32(&tfull_bar[acc]), acc_phase, abort_flag, limit)) break;
+      // every lane waits; the warp goes on only if all of them saw the accumulator (the
+      // TMEM loads below are warp-wide), so a lane that timed out stops the whole warp
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&tfull_bar[acc]), acc_phase, abort_flag, limit)))
+        break;
       tc_fence_after();
 #ifdef MAO_TC_TRACE
       if (lane == 0 && leader) TRACE_ADD(3, tw2);
@@ -1058,7 +1061,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads(MODE), 1)
 #ifdef MAO_TC_TRACE
       const long long tw2 = clock64();
 #endif
-      if (!mbar_wait(smem_u32(&tfull_bar[acc]), acc_phase, abort_flag, limit)) break;
+      // every lane waits; the warp goes on only if all of them saw the accumulator (the
+      // TMEM loads below are warp-wide), so a lane that timed out stops the whole warp
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&tfull_bar[acc]), acc_phase, abort_flag, limit)))
+        break;
       tc_fence_after();
 #ifdef MAO_TC_TRACE
       if (lane == 0 && leader) TRACE_ADD(3, tw2);

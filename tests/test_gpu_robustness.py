@@ -108,3 +108,46 @@ def test_forced_timeout_is_reported_and_recovers(cuda):
     mao.ns_orthogonalize(X, U, 5, mao.QUINTIC, 1e-7, "bf16")
     mao.sync_status()
     assert rel_fro(to_np(U), oracle.newton_schulz(to_np(X), 5, oracle.QUINTIC)) <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("kind", ["muon_short", "muon_long", "dion"])
+def test_forced_timeout_one_call_steps(cuda, kind):
+    """The fused steps under a wait limit of 0: muon_step whose last product is short
+    (K = 256: the streamed update epilogue) or long (K = 384: the update from registers),
+    and dion_step (streamed rank-r updates). The time-out is reported, and a run after it
+    equals a run before it bit for bit."""
+    gen = torch.Generator().manual_seed(95)
+    if kind == "dion":
+        shapes = [(256, 640), (640, 256)]
+        base = [(torch.randn(s, generator=gen).to(cuda), torch.randn(s, generator=gen).to(cuda),
+                 torch.randn(s, generator=gen).to(cuda),
+                 torch.randn((s[1], 32), generator=gen).to(cuda)) for s in shapes]
+
+        def run():
+            X, M, Q = [b[0].clone() for b in base], [b[1].clone() for b in base], [b[3].clone() for b in base]
+            mao.dion_step(X, M, [b[2] for b in base], Q, 0.9, 0.1)
+            return X + M + Q
+    else:
+        shapes = [(256, 640), (640, 256)] if kind == "muon_short" else [(384, 768)]
+        base = [tuple(rand_matrix(gen, s, torch.bfloat16, cuda) for _ in range(3)) for s in shapes]
+
+        def run():
+            W, M = [b[0].clone() for b in base], [b[1].clone() for b in base]
+            mao.muon_step(W, M, [b[2] for b in base], 0.95, 0.5)
+            return W + M
+    before = run()
+    mao.sync_status()
+    old = mao.get_wait_limit()
+    try:
+        mao.set_wait_limit(0)
+        run()
+        with pytest.raises(mao.MaoError) as err:
+            mao.sync_status()
+        assert err.value.status == 6  # MAO_ERR_TIMEOUT (before any numeric report)
+    finally:
+        mao.set_wait_limit(old)
+    mao.sync_status()
+    after = run()
+    mao.sync_status()
+    for a, b in zip(before, after):
+        assert torch.equal(a, b)
