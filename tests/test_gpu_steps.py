@@ -171,3 +171,30 @@ def test_config2_fused_step_equals_composed_full(cuda):
 
 def test_config5_fused_step_equals_composed_full(cuda):
     _check_fused_equals_composed(workloads.workload(5), cuda, [0, 1, 2, 192, 384])
+
+
+def test_config6_dion_full(cuda):
+    """One Dion step over the 48 matrices (four shape groups of twelve, rank 192), run as
+    bench.py runs it; one matrix of each shape in the first layer and one in the last
+    against the fp64 oracle, matrix by matrix ([Dion] algorithm section). Q within the bf16
+    product tolerance; M and X within it plus their roundings to bf16 storage (unit
+    roundoff 2^-8 each: B = M + G as stored, then the new value)."""
+    wl = workloads.workload(6)
+    inp = workloads.generate(wl, cuda)
+    host = {k: [to_np(t) for t in v] for k, v in inp.items()}
+    step = bench.Step(wl, inp, cuda)
+    step()
+    mao.sync_status()
+    u = 2.0 ** -8
+    for i in [0, 1, 2, 3, 46]:
+        out = oracle.dion_step(host["W"][i], host["M"][i], host["G"][i], host["Q"][i], wl.mu, wl.lr)
+        Q = to_np(step.Q[i])
+        assert rel_fro(Q, out["Q"]) <= TOL["bf16"], i
+        assert np.allclose(np.linalg.norm(Q, axis=0), 1.0, atol=1e-4), i
+        B = host["M"][i].astype(np.float64) + host["G"][i]
+        err_m = np.linalg.norm(to_np(step.M[i]) - out["M"])
+        assert err_m <= TOL["bf16"] * np.linalg.norm(B - out["M"]) + u * np.linalg.norm(out["M"]) \
+            + u * np.linalg.norm(B), i
+        X0 = host["W"][i].astype(np.float64)
+        err_x = np.linalg.norm(to_np(step.W[i]) - out["X"])
+        assert err_x <= TOL["bf16"] * np.linalg.norm(X0 - out["X"]) + 1.01 * u * np.linalg.norm(out["X"]), i
