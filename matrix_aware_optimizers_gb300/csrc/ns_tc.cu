@@ -34,6 +34,12 @@
 //                alternate 64-column blocks), fp32 arithmetic, then 32 x 64 blocks staged in
 //                shared memory (128-byte swizzle) and written by bulk tensor stores; the
 //                caller-output instantiations use warps 2..5, one per quadrant
+// The in-place update (TC_UPDATE) reads and writes the caller's rows with 16-byte accesses
+// from its eight epilogue warps. For a short product (K <= 256, a rank-k update) it runs as
+// OUT_UPDATE_STREAM: a 2-stage operand ring, and per epilogue warp three 4 KB slots into
+// which the warp copies (cp.async) the old values of its next blocks about a tile ahead.
+// A long product (the last one of a fused Muon step) keeps the 3-stage ring and loads the
+// old values into registers before its accumulator is ready.
 // Barriers: full[s] (even CTA; both CTAs' loads complete on it), empty[s] (both CTAs),
 // tfull[a] (both), tempty[a] (even CTA; every epilogue warp of the pair arrives on it).
 // The kernel is launched as a programmatic dependent of the previous kernel in the stream:
