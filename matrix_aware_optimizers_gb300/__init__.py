@@ -344,7 +344,7 @@ def launch_count():
 
 
 PROFILE_TAGS = {0: "tc", 1: "dion_setup", 2: "dion_stage", 3: "dion_gram", 4: "dion_chol",
-                5: "dion_trmm", 6: "dion_norm"}
+                5: "dion_split", 6: "dion_norm"}
 
 
 def profile_begin(max_launches):

@@ -12,12 +12,16 @@
 // The orthonormal basis is the Q factor of the thin QR with a positive triangular
 // diagonal, computed as Cholesky QR applied twice: S = P^T P, S = L L^T, P <- P W^T with
 // W = L^-1 (the factorisation kernel also inverts L, so the product with P is one parallel
-// triangular multiply instead of a sequential substitution).
+// multiply instead of a sequential substitution).
 // The dense products (B Q, B^T P and the two rank-r updates) run on the same tcgen05 kernel
-// as Newton–Schulz, over up to eight shape groups per launch; the Cholesky QR (Gram
-// matrices, Cholesky and inverse, triangular multiply) runs in fp32 on CUDA cores, every
-// matrix of the call in one launch per stage (the Gram and multiply launches cover up to
-// sixteen shape groups each, with exactly the CTAs their slots need). Per-matrix
+// as Newton–Schulz, over up to eight shape groups per launch. The Gram matrices and the
+// Cholesky factorisation with its inverse run in fp32 on CUDA cores. The multiply P W^T runs
+// on the tensor cores with both factors split into bf16 parts, p = p_hi + p_lo and
+// w = w_hi + w_lo (lo = bf16(x - hi)): [P_hi P_hi P_lo] [W_hi W_lo W_hi]^T =
+// P_hi W_hi^T + P_hi W_lo^T + P_lo W_hi^T, about 2^-16 relative, with fp32 accumulation
+// (P enters the later products as bf16, 2^-9). Every matrix of the call is covered by one
+// launch per stage (the Gram launches by up to sixteen shape groups each, with exactly the
+// CTAs their slots need). Per-matrix
 // descriptors live in a device table in the workspace (written by a set-up kernel), so a
 // call of any size and any mix of shapes takes a fixed number of launches.
 #include <algorithm>
@@ -55,7 +59,8 @@ struct DionSlot {
   __nv_bfloat16 *Bw, *Qw, *Rw, *Pw; // bf16 operands, rows of ldn / ldr elements
   float *P0, *P1, *Rf;              // fp32 [m|n][ldr]
   float *Sp, *Sf;                   // partial Grams [gchunks][tiles][64 x 64]; S in lower 32 x 32 blocks
-  float* W;                         // L^-1 in lower 32 x 32 blocks (layout of blk())
+  __nv_bfloat16* Ys;                // P split for the triangular multiply [m][3 ldr]: hi | hi | lo
+  __nv_bfloat16* Wsp;               // L^-1 split [ldr][3 ldr]: hi | lo | hi (rows j, columns k)
   float* cn;                        // column norms of R: partials [nchunks][r], then the norms
   int32_t* cnt;                     // arrival counters of the Gram tiles [2 passes][tiles]
   int64_t ldm, ldg, ldx, ldq, ldxo;
@@ -69,11 +74,11 @@ struct DionSlot {
 
 struct DionCommon {
   const DionSlot* slots;            // device table [count]
-  OutEntry *tP, *tR, *tM, *tX;      // output tables of the tensor-core launches [count]
+  OutEntry *tP, *tR, *tM, *tX, *tP1; // output tables of the tensor-core launches [count]
   int32_t r, ldr, count;
 };
 
-// A launch of the Gram or the triangular-multiply kernel covers the slots of up to
+// A launch of the Gram kernel covers the slots of up to
 // kLaunchGroups shape groups with exactly the CTAs they need: group g owns CTAs
 // [begin, begin + count * per_slot), per_slot CTAs for each of its slots slot0 .. .
 constexpr int kLaunchGroups = 16;
@@ -127,6 +132,8 @@ __global__ void __launch_bounds__(64) dion_setup_kernel(const __grid_constant__ 
   o.dtype = MAO_F32;
   o.flags = OUT_VEC;
   p.c.tP[z] = o;
+  o.out = e.P1;
+  p.c.tP1[z] = o;
   o.out = e.Rf;
   p.c.tR[z] = o;
   o.out = e.M;
@@ -510,7 +517,7 @@ __device__ __forceinline__ void inv32(float* Ad, const float* rinv, int lane) {
 }
 
 // One CTA per slot: S = L L^T (blocked right-looking Cholesky, 32 x 32 blocks in shared
-// memory), then W = L^-1, written to e.W in the same lower-block layout.
+// memory), then W = L^-1, written to e.Wsp as the split bf16 operand of the multiply P W^T.
 //   Cholesky, for each block column J: the panel below the diagonal becomes
 //   L_IJ = A_IJ D_J^T (one warp per row); block column J + 1 gets A_I,J+1 -= L_IJ L_J+1,J^T;
 //   then warp 0 factors the diagonal block J + 1 (chol32) and inverts it in place (inv32:
@@ -669,126 +676,97 @@ __global__ void __launch_bounds__(kCholThreads, 1) dion_chol_kernel(const __grid
   }
   if (nb >= 2) inverse_step(nb - 1, warp, kWarps, [] { __syncthreads(); });
   __syncthreads();
-  // W to global memory in the same lower-block layout (zeros above the diagonal; the
-  // identity past r)
-  for (int q = threadIdx.x; q < nlow * kBlk / 4; q += kCholThreads)
-    reinterpret_cast<float4*>(e.W)[q] = reinterpret_cast<const float4*>(A)[q];
-}
-
-// Pout = Pin W^T (W = L^-1 lower triangular, so Pout[:, j] needs columns k <= j of Pin).
-// One CTA per 64 x 64 output tile (row tile, column tile) of a slot (DionGridParams), 64
-// threads, 8 x 8 outputs each: rows rg + 8 x and columns tx + 8 y. Both operands sit in
-// shared memory with k contiguous (rows of 36 floats, double-buffered by cp.async), so every
-// 16-byte read of a quarter warp falls on distinct banks; W comes from its lower-block
-// layout (blocks above the diagonal read as zeros). Pass 0 writes P1 (fp32, zeros past r); pass 1 writes the bf16 operand
-// Pw (zeros up to ldr) and, if asked, the caller's fp32 copy of P.
-constexpr int kTrmmThreads = 64;
-
-__global__ void __launch_bounds__(kTrmmThreads) dion_trmm_kernel(const __grid_constant__ DionGridParams P) {
-  const DionCommon& c = P.c;
-  const int pass = P.pass;
-  int slot, local;
-  grid_slot(P, slot, local);
-  const DionSlot& e = c.slots[slot];
-  const int r = c.r, ldr = c.ldr;
-  const int ctiles = ldr / 64;
-  const int64_t i0 = int64_t(local / ctiles) * 64;
-  const int j0 = int(local % ctiles) * 64;
-  const int kend = min(r, j0 + 64);
-  const int nbw = (r + 31) / 32;  // block rows of W
-  const float* Pin = pass == 0 ? e.P0 : e.P1;
-
-  __shared__ __align__(16) float As[2][64][36], Bs[2][64][36];
-  const int tid = threadIdx.x;
-  const int tx = tid & 7, rg = tid >> 3;
-  // thread -> rows lr + 8 h of the slab (h = 0 .. 7), k columns k4 .. k4 + 3; rows 0 .. 31
-  // of the W tile lie in block row jb0, rows 32 .. 63 in jb0 + 1
-  const int lr = tid >> 3, k4 = 4 * (tid & 7);
-  const int jb0 = j0 / 32;
-  auto issue = [&](int k0, int buf) {
-    const int kb = k0 / 32;
+  // W to global memory as the bf16 operand of the multiply P W^T on the tensor cores: row j
+  // holds hi(W_j) | lo(W_j) | hi(W_j), ldr columns each, lo = bf16(w - hi); zeros above the
+  // diagonal, the identity past r
+  {
+    const int ldr = c.ldr, q8 = ldr / 8, nbw32 = 32 * nb;
+    for (int q = threadIdx.x; q < ldr * q8; q += kCholThreads) {
+      const int j = q / q8, k0 = (q - j * q8) * 8;
+      float w[8], lo[8];
 #pragma unroll
-    for (int h = 0; h < 8; ++h) {
-      const int row = lr + 8 * h;
-      const int64_t g = i0 + row;
-      const bool ok = g < e.m;
-      cp_async16(&As[buf][row][k4], Pin + (ok ? g : i0) * ldr + k0 + k4,
-                 ok ? bytes_before(k0 + k4, r) : 0);
-      const int jb = jb0 + (h >= 4 ? 1 : 0);
-      const bool wok = jb < nbw && kb <= jb;  // a stored block (else zeros)
-      cp_async16(&Bs[buf][row][k4], wok ? blk(e.W, jb, kb) + (row & 31) * kLd + k4 : e.W,
-                 wok ? 16 : 0);
-    }
-    cp_async_commit();
-  };
-  float acc[8][8] = {};
-  const int nslab = (kend + 31) / 32;
-  issue(0, 0);
-  for (int sl = 0; sl < nslab; ++sl) {
-    if (sl + 1 < nslab) issue(32 * (sl + 1), (sl + 1) & 1);
-    else cp_async_commit();
-    cp_async_wait1();
-    __syncthreads();
-    const float(*Ab)[36] = As[sl & 1];
-    const float(*Bb)[36] = Bs[sl & 1];
-#pragma unroll 1
-    for (int kk = 0; kk < 32; kk += 4) {
-      float4 a[8];
-#pragma unroll
-      for (int x = 0; x < 8; ++x) a[x] = *reinterpret_cast<const float4*>(&Ab[rg + 8 * x][kk]);
-#pragma unroll
-      for (int y = 0; y < 8; ++y) {
-        const float4 b = *reinterpret_cast<const float4*>(&Bb[tx + 8 * y][kk]);
-#pragma unroll
-        for (int x = 0; x < 8; ++x) {
-          acc[x][y] = __fmaf_rn(a[x].x, b.x, acc[x][y]);
-          acc[x][y] = __fmaf_rn(a[x].y, b.y, acc[x][y]);
-          acc[x][y] = __fmaf_rn(a[x].z, b.z, acc[x][y]);
-          acc[x][y] = __fmaf_rn(a[x].w, b.w, acc[x][y]);
-        }
+      for (int u = 0; u < 8; ++u) {
+        const int k = k0 + u;
+        w[u] = (j < nbw32 && k < nbw32) ? (k <= j ? blk(A, j >> 5, k >> 5)[(j & 31) * kLd + (k & 31)] : 0.0f)
+                                        : (j == k ? 1.0f : 0.0f);
+        lo[u] = w[u] - __bfloat162float(__float2bfloat16_rn(w[u]));
       }
-    }
-    __syncthreads();
-  }
-  // the tile goes through shared memory (64 rows of 68 floats) so that every row is
-  // written with 16-byte stores
-  float(*Ct)[68] = reinterpret_cast<float(*)[68]>(&As[0][0][0]);
-  static_assert(sizeof(As) >= 64 * 68 * sizeof(float), "output tile fits in the operand buffers");
-#pragma unroll
-  for (int x = 0; x < 8; ++x)
-#pragma unroll
-    for (int y = 0; y < 8; ++y) Ct[rg + 8 * x][tx + 8 * y] = j0 + tx + 8 * y < r ? acc[x][y] : 0.0f;
-  __syncthreads();
-  // thread -> rows lr + 8 h, columns k4 .. k4 + 3 and 32 + k4 .. 32 + k4 + 3
-  const bool pvec = e.Pout && (reinterpret_cast<uintptr_t>(e.Pout) % 16 == 0) && (r % 4 == 0);
-#pragma unroll
-  for (int h = 0; h < 8; ++h) {
-    const int rr = lr + 8 * h;
-    const int64_t row = i0 + rr;
-    if (row >= e.m) continue;
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      const int cc = 32 * half + k4;
-      const int j = j0 + cc;
-      const float4 v = *reinterpret_cast<const float4*>(&Ct[rr][cc]);
-      if (pass == 0) {
-        *reinterpret_cast<float4*>(e.P1 + row * ldr + j) = v;
-      } else {
-        *reinterpret_cast<uint2*>(e.Pw + row * ldr + j) = make_uint2(bf16_pair(v.x, v.y), bf16_pair(v.z, v.w));
-        if (e.Pout) {
-          if (pvec && j + 4 <= r) {
-            *reinterpret_cast<float4*>(e.Pout + row * r + j) = v;
-          } else {
-            const float vv[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-            for (int u = 0; u < 4; ++u)
-              if (j + u < r) e.Pout[row * r + j + u] = vv[u];
-          }
-        }
-      }
+      const uint4 h = make_uint4(bf16_pair(w[0], w[1]), bf16_pair(w[2], w[3]), bf16_pair(w[4], w[5]),
+                                 bf16_pair(w[6], w[7]));
+      const uint4 l = make_uint4(bf16_pair(lo[0], lo[1]), bf16_pair(lo[2], lo[3]), bf16_pair(lo[4], lo[5]),
+                                 bf16_pair(lo[6], lo[7]));
+      __nv_bfloat16* row = e.Wsp + size_t(j) * 3 * ldr;
+      *reinterpret_cast<uint4*>(row + k0) = h;
+      *reinterpret_cast<uint4*>(row + ldr + k0) = l;
+      *reinterpret_cast<uint4*>(row + 2 * ldr + k0) = h;
     }
   }
 }
+
+// P (fp32 [m][ldr]; pass 0: P0, pass 1: P1) split for the triangular multiply on the tensor
+// cores: Ys = hi | hi | lo (bf16 [m][3 ldr]), hi = bf16(p), lo = bf16(p - hi); columns at
+// and past r are written as zeros (they meet W's zero columns, and NaN x 0 would not vanish).
+__global__ void __launch_bounds__(256) dion_split_kernel(const __grid_constant__ DionCommon c, int pass) {
+  const DionSlot& e = c.slots[blockIdx.y];
+  const uint32_t upr = uint32_t(c.ldr) / 8;
+  const uint32_t u = blockIdx.x * 256u + threadIdx.x;
+  if (u >= uint32_t(e.m) * upr) return;
+  const uint32_t row = u / upr, k0 = (u - row * upr) * 8;
+  const float* P = (pass == 0 ? e.P0 : e.P1) + size_t(row) * c.ldr + k0;
+  float v[8];
+  if (int(k0) + 8 <= c.r) {
+    const float4 x = *reinterpret_cast<const float4*>(P), y = *reinterpret_cast<const float4*>(P + 4);
+    v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w; v[4] = y.x; v[5] = y.y; v[6] = y.z; v[7] = y.w;
+  } else {
+#pragma unroll
+    for (int q = 0; q < 8; ++q) v[q] = int(k0) + q < c.r ? P[q] : 0.0f;
+  }
+  float lo[8];
+#pragma unroll
+  for (int q = 0; q < 8; ++q) lo[q] = v[q] - __bfloat162float(__float2bfloat16_rn(v[q]));
+  const uint4 h = make_uint4(bf16_pair(v[0], v[1]), bf16_pair(v[2], v[3]), bf16_pair(v[4], v[5]),
+                             bf16_pair(v[6], v[7]));
+  const uint4 l = make_uint4(bf16_pair(lo[0], lo[1]), bf16_pair(lo[2], lo[3]), bf16_pair(lo[4], lo[5]),
+                             bf16_pair(lo[6], lo[7]));
+  __nv_bfloat16* y = e.Ys + size_t(row) * 3 * c.ldr + k0;
+  *reinterpret_cast<uint4*>(y) = h;
+  *reinterpret_cast<uint4*>(y + c.ldr) = h;
+  *reinterpret_cast<uint4*>(y + 2 * c.ldr) = l;
+}
+
+// The final P (fp32 in P0) to the bf16 operand Pw (zeros from r up to ldr) and, if asked,
+// the caller's fp32 copy (row stride r).
+__global__ void __launch_bounds__(256) dion_finish_kernel(const __grid_constant__ DionCommon c) {
+  const DionSlot& e = c.slots[blockIdx.y];
+  const uint32_t upr = uint32_t(c.ldr) / 8;
+  const uint32_t u = blockIdx.x * 256u + threadIdx.x;
+  if (u >= uint32_t(e.m) * upr) return;
+  const uint32_t row = u / upr, k0 = (u - row * upr) * 8;
+  const float* P = e.P0 + size_t(row) * c.ldr + k0;
+  const bool full = int(k0) + 8 <= c.r;
+  float v[8];
+  if (full) {
+    const float4 x = *reinterpret_cast<const float4*>(P), y = *reinterpret_cast<const float4*>(P + 4);
+    v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w; v[4] = y.x; v[5] = y.y; v[6] = y.z; v[7] = y.w;
+  } else {
+#pragma unroll
+    for (int q = 0; q < 8; ++q) v[q] = int(k0) + q < c.r ? P[q] : 0.0f;
+  }
+  *reinterpret_cast<uint4*>(e.Pw + size_t(row) * c.ldr + k0) =
+      make_uint4(bf16_pair(v[0], v[1]), bf16_pair(v[2], v[3]), bf16_pair(v[4], v[5]), bf16_pair(v[6], v[7]));
+  if (e.Pout) {
+    float* d = e.Pout + size_t(row) * c.r + k0;
+    if (full && c.r % 4 == 0 && reinterpret_cast<uintptr_t>(e.Pout) % 16 == 0) {
+      *reinterpret_cast<float4*>(d) = make_float4(v[0], v[1], v[2], v[3]);
+      *reinterpret_cast<float4*>(d + 4) = make_float4(v[4], v[5], v[6], v[7]);
+    } else {
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        if (int(k0) + q < c.r) d[q] = v[q];
+    }
+  }
+}
+
 
 // ------------------------------------------------------ R -> Q = ColumnNormalize(R)
 
@@ -874,7 +852,8 @@ __global__ void __launch_bounds__(256) dion_q_kernel(const __grid_constant__ Dio
 struct DionGroup {
   int64_t m, n;
   int32_t count, slot0;
-  size_t off_bw, off_qw, off_rw, off_pw, off_p0, off_p1, off_rf, off_sp, off_sf, off_w, off_cn, off_cnt;
+  size_t off_bw, off_qw, off_rw, off_pw, off_p0, off_p1, off_rf, off_sp, off_sf, off_ys, off_wsp, off_cn,
+      off_cnt;
 };
 
 struct DionPlan {
@@ -908,7 +887,7 @@ void make_dion_plan(const mao_mat* X, int32_t batch, int32_t rank, DionPlan& pla
     return at;
   };
   plan.off_slots = take(sizeof(DionSlot) * size_t(batch));
-  plan.off_tables = take(4 * sizeof(OutEntry) * size_t(batch));
+  plan.off_tables = take(5 * sizeof(OutEntry) * size_t(batch));
   const size_t r = size_t(rank), ldr = size_t(plan.ldr);
   int slot = 0;
   for (const auto& mem : members) {
@@ -931,8 +910,8 @@ void make_dion_plan(const mao_mat* X, int32_t batch, int32_t rank, DionPlan& pla
     g.off_sp = take(gch > 1 ? c * gch * ntiles * 4096 * 4 : 0);
     const size_t nsb = (ldr / 32) * (ldr / 32 + 1) / 2;  // lower 32 x 32 blocks of S
     g.off_sf = take(c * nsb * kBlk * 4);
-    const size_t nbw = size_t(ceil_div(rank, 32));
-    g.off_w = take(c * nbw * (nbw + 1) / 2 * kBlk * 4);
+    g.off_ys = take(c * m * 3 * ldr * 2);
+    g.off_wsp = take(c * ldr * 3 * ldr * 2);
     g.off_cnt = take(c * 2 * kGramTilesMax * 4);
     g.off_cn = take(c * (nch + 1) * r * 4);
     for (int b : mem) plan.input_of.push_back(b);
@@ -959,7 +938,7 @@ mao_status dion_tc(const DionPlan& plan, uint8_t* ws, const OutEntry* table, int
   for (size_t g0 = 0; g0 < plan.groups.size(); g0 += tc::MAX_GROUPS) {
     TcParams p;
     memset(&p, 0, sizeof(p));
-    p.stage = op >= 2 ? TC_UPDATE : NS_APPLY;
+    p.stage = (op == 2 || op == 3) ? TC_UPDATE : NS_APPLY;
     p.a = alpha;
     p.scale = nullptr;
     p.out_table = table;
@@ -981,6 +960,11 @@ mao_status dion_tc(const DionPlan& plan, uint8_t* ws, const OutEntry* table, int
           A = ws + g.off_bw; rowsA = g.m; ldA = ldn; G.a_mn = 1;
           B = ws + g.off_pw; rowsB = g.m; ldB = ldr; G.b_mn = 1;
           G.M = int32_t(g.n); G.N = int32_t(r); G.K = int32_t(g.m);
+          break;
+        case 4:  // (m x 3 ldr)(3 ldr x r): [P_hi P_hi P_lo] [W_hi W_lo W_hi]^T, both K-major
+          A = ws + g.off_ys; rowsA = g.m; ldA = 3 * ldr; G.a_mn = 0;
+          B = ws + g.off_wsp; rowsB = ldr; ldB = 3 * ldr; G.b_mn = 0;
+          G.M = int32_t(g.m); G.N = int32_t(r); G.K = int32_t(3 * ldr);
           break;
         default:  // (m x r)(r x n): Pw K-major, Rw / Qw K-major
           A = ws + g.off_pw; rowsA = g.m; ldA = ldr; G.a_mn = 0;
@@ -1030,6 +1014,7 @@ mao_status dion_run(const mao_mat* X, const mao_mat* M, const mao_mat* G, const 
   c.tR = tables + batch;
   c.tM = tables + 2 * batch;
   c.tX = tables + 3 * batch;
+  c.tP1 = tables + 4 * batch;
   c.r = rank;
   c.ldr = int32_t(plan.ldr);
   c.count = batch;
@@ -1083,8 +1068,8 @@ mao_status dion_run(const mao_mat* X, const mao_mat* M, const mao_mat* G, const 
                            : nullptr;
       const size_t nsb = size_t(plan.ldr / 32) * size_t(plan.ldr / 32 + 1) / 2;
       e.Sf = reinterpret_cast<float*>(ws + g.off_sf) + size_t(k) * nsb * kBlk;
-      const size_t nbw = size_t(ceil_div(rank, 32));
-      e.W = reinterpret_cast<float*>(ws + g.off_w) + size_t(k) * nbw * (nbw + 1) / 2 * kBlk;
+      e.Ys = reinterpret_cast<__nv_bfloat16*>(ws + g.off_ys) + size_t(k) * g.m * 3 * plan.ldr;
+      e.Wsp = reinterpret_cast<__nv_bfloat16*>(ws + g.off_wsp) + size_t(k) * plan.ldr * 3 * plan.ldr;
       e.cnt = reinterpret_cast<int32_t*>(ws + g.off_cnt) + size_t(k) * 2 * kGramTilesMax;
       e.cn = reinterpret_cast<float*>(ws + g.off_cn) + size_t(k) * (e.nchunks + 1) * rank;
       e.ldm = M[b].ld;
@@ -1149,24 +1134,30 @@ mao_status dion_run(const mao_mat* X, const mao_mat* M, const mao_mat* G, const 
         ctas += int64_t(lg.per_slot) * g.count;
       }
       if (ctas > 0x7FFFFFFF) return false;
-      if (gram) {
-        profile_before_launch(stream, MAO_PROF_DION_GRAM);
-        dion_gram_kernel<<<unsigned(ctas), kGramThreads, 0, stream>>>(gp);
-      } else {
-        profile_before_launch(stream, MAO_PROF_DION_TRMM);
-        dion_trmm_kernel<<<unsigned(ctas), kTrmmThreads, 0, stream>>>(gp);
-      }
+      profile_before_launch(stream, MAO_PROF_DION_GRAM);
+      dion_gram_kernel<<<unsigned(ctas), kGramThreads, 0, stream>>>(gp);
       if (!launched()) return false;
     }
     return true;
   };
+  int64_t max_m = 0;
+  for (const auto& g : plan.groups) max_m = std::max<int64_t>(max_m, g.m);
+  const unsigned split_blocks = unsigned(ceil_div(max_m * (plan.ldr / 8), 256));
   for (int pass = 0; pass < 2; ++pass) {
     if (!grid_launches(true, pass)) return MAO_ERR_CUDA;
+    profile_before_launch(stream, MAO_PROF_DION_SPLIT);
+    dion_split_kernel<<<dim3(split_blocks, nb), 256, 0, stream>>>(c, pass);
+    if (!launched()) return MAO_ERR_CUDA;
     profile_before_launch(stream, MAO_PROF_DION_CHOL);
     dion_chol_kernel<<<nb, kCholThreads, chol_smem, stream>>>(c);
     if (!launched()) return MAO_ERR_CUDA;
-    if (!grid_launches(false, pass)) return MAO_ERR_CUDA;
+    // P1 = P0 W1^T (pass 0), P = P1 W2^T into P0 (pass 1), on the tensor cores
+    const mao_status st = dion_tc(plan, ws, pass == 0 ? c.tP1 : c.tP, 4, 1.0f, stream);
+    if (st != MAO_OK) return st;
   }
+  profile_before_launch(stream, MAO_PROF_DION_SPLIT);
+  dion_finish_kernel<<<dim3(split_blocks, nb), 256, 0, stream>>>(c);
+  if (!launched()) return MAO_ERR_CUDA;
   // 4. R = B^T P (fp32)
   st = dion_tc(plan, ws, c.tR, 1, 1.0f, stream);
   if (st != MAO_OK) return st;
