@@ -298,9 +298,10 @@ mao_status apply_update(const mao_mat* W, const uint32_t* const* vote, const mao
  *   M <- B - (1 - mu) P R^T;  Q <- ColumnNormalize(R);  X <- X - lr P Q^T
  *
  * orthonormalise gives the Q factor of the thin QR of B Q with a positive triangular
- * diagonal, computed as Cholesky QR applied twice: the Gram matrix and its Cholesky factor
- * L in fp32, the product with L^-1 on the tensor cores from bf16 parts of both factors
- * (three products, about 2^-16 relative, fp32 accumulation); ColumnNormalize divides each
+ * diagonal, computed as Cholesky QR applied twice: the Gram matrix P^T P and the product
+ * with L^-1 on the tensor cores from bf16 parts of their fp32 factors (fp32 accumulation;
+ * the Gram to about fp32 accuracy, the product to about 2^-17), the Cholesky factor L and
+ * its inverse in fp32 on CUDA cores; ColumnNormalize divides each
  * column by its Euclidean norm (a zero column stays zero).
  *   X[b], M[b]  in/out, f32 or bf16, m x n;  G[b] in, f32 or bf16, m x n.
  *   Q[b]        in/out, f32, n x r (any ld): the previous right factor in, the new one out.
@@ -368,7 +369,7 @@ enum {
   MAO_PROF_TC = 0,
   MAO_PROF_DION_SETUP = 1,     /* device table of the slots */
   MAO_PROF_DION_STAGE = 2,     /* B = M + G and its bf16 copy; bf16 copy of Q_prev */
-  MAO_PROF_DION_GRAM = 3,      /* P^T P */
+  MAO_PROF_DION_GRAM = 3,      /* P^T P assembled from its tensor-core parts (the products are MAO_PROF_TC) */
   MAO_PROF_DION_CHOL = 4,      /* Cholesky factor and its inverse */
   MAO_PROF_DION_SPLIT = 5,     /* P split into bf16 parts for P L^-T (whose product is MAO_PROF_TC), and the final P to bf16 */
   MAO_PROF_DION_NORM = 6       /* column norms of R, Q = ColumnNormalize(R) */

@@ -14,14 +14,15 @@
 // W = L^-1 (the factorisation kernel also inverts L, so the product with P is one parallel
 // multiply instead of a sequential substitution).
 // The dense products (B Q, B^T P and the two rank-r updates) run on the same tcgen05 kernel
-// as Newton–Schulz, over up to eight shape groups per launch. The Gram matrices and the
-// Cholesky factorisation with its inverse run in fp32 on CUDA cores. The multiply P W^T runs
-// on the tensor cores with both factors split into bf16 parts, p = p_hi + p_lo and
-// w = w_hi + w_lo (lo = bf16(x - hi)): [P_hi P_hi P_lo] [W_hi W_lo W_hi]^T =
-// P_hi W_hi^T + P_hi W_lo^T + P_lo W_hi^T, about 2^-16 relative, with fp32 accumulation
-// (P enters the later products as bf16, 2^-9). Every matrix of the call is covered by one
-// launch per stage (the Gram launches by up to sixteen shape groups each, with exactly the
-// CTAs their slots need). Per-matrix
+// as Newton–Schulz, over up to eight shape groups per launch. The Cholesky factorisation and
+// its inverse run in fp32 on CUDA cores, one CTA per matrix. The two products of Cholesky QR
+// run on the tensor cores from bf16 parts of their fp32 factors (x = hi + mid + lo with
+// hi = bf16(x), mid = bf16(x - hi), lo = bf16(x - hi - mid)), fp32 accumulation:
+//   Gram    S = P^T P from D = [P_hi P_mid]^T [P_hi P_mid P_lo]: hh + hm + mh + hl + lh + mm,
+//           leaving out terms below 2^-26 of |P|^2, so the Cholesky factor is as good as
+//           with an fp32 Gram (Cholesky QR needs kappa(P)^2 times the Gram's error < 1);
+//   multiply P W^T (W = L^-1) = [P_hi P_hi P_mid] [W_hi W_lo W_hi]^T, about 2^-17 relative
+//           (P enters the later products as bf16, 2^-9). Per-matrix
 // descriptors live in a device table in the workspace (written by a set-up kernel), so a
 // call of any size and any mix of shapes takes a fixed number of launches.
 #include <algorithm>
@@ -42,8 +43,6 @@ __device__ unsigned int g_dion_error;  // bit 0: a Cholesky pivot was not positi
 namespace {
 
 constexpr int kMaxRank = 256;
-constexpr int kGramRows = 512;    // rows of P summed by one partial Gram tile
-constexpr int kGramTilesMax = 10; // lower 64 x 64 tiles of an r x r Gram, r <= 256
 constexpr int kNormRows = 256;    // rows of R summed by one partial column norm
 constexpr int kSetup = 96;        // table entries written per set-up launch (kernel parameters <= 32 KB)
 constexpr int kCholThreads = 512;
@@ -58,48 +57,26 @@ struct DionSlot {
   float* Pout;                      // optional copy of the final P (m x r, row stride r)
   __nv_bfloat16 *Bw, *Qw, *Rw, *Pw; // bf16 operands, rows of ldn / ldr elements
   float *P0, *P1, *Rf;              // fp32 [m|n][ldr]
-  float *Sp, *Sf;                   // partial Grams [gchunks][tiles][64 x 64]; S in lower 32 x 32 blocks
-  __nv_bfloat16* Ys;                // P split for the triangular multiply [m][3 ldr]: hi | hi | lo
+  float* Sf;                        // S = P^T P in lower 32 x 32 blocks (layout of blk())
+  __nv_bfloat16* Ys;                // P in bf16 parts [m][4 ldr]: hi | hi | mid | lo
+  float* D;                         // Gram work product [2 ldr][3 ldr] (fp32)
   __nv_bfloat16* Wsp;               // L^-1 split [ldr][3 ldr]: hi | lo | hi (rows j, columns k)
   float* cn;                        // column norms of R: partials [nchunks][r], then the norms
-  int32_t* cnt;                     // arrival counters of the Gram tiles [2 passes][tiles]
   int64_t ldm, ldg, ldx, ldq, ldxo;
   int32_t m, n, ldn;
   int32_t dtm, dtg, dtx;
   int32_t flags_m, flags_x;
-  int32_t gchunks, nchunks;         // partial Gram row chunks of P, partial norm chunks of R
+  int32_t nchunks;                  // partial norm chunks of R
   int32_t vec;                      // M and G: bf16/f32 rows that allow 16-byte accesses
   int32_t qvec;                     // Q: 16-byte aligned rows (ldq a multiple of 4)
 };
 
 struct DionCommon {
   const DionSlot* slots;            // device table [count]
-  OutEntry *tP, *tR, *tM, *tX, *tP1; // output tables of the tensor-core launches [count]
+  OutEntry *tP, *tR, *tM, *tX, *tP1, *tG;  // output tables of the tensor-core launches [count]
   int32_t r, ldr, count;
 };
 
-// A launch of the Gram kernel covers the slots of up to
-// kLaunchGroups shape groups with exactly the CTAs they need: group g owns CTAs
-// [begin, begin + count * per_slot), per_slot CTAs for each of its slots slot0 .. .
-constexpr int kLaunchGroups = 16;
-struct DionLaunchGroup {
-  int32_t slot0, count, per_slot, begin;
-};
-struct DionGridParams {
-  DionCommon c;
-  DionLaunchGroup g[kLaunchGroups];
-  int32_t ng, pass;
-};
-
-// The slot and the CTA's index among the slot's CTAs.
-__device__ __forceinline__ void grid_slot(const DionGridParams& P, int& slot, int& local) {
-  int gi = 0;
-  while (gi + 1 < P.ng && P.g[gi + 1].begin <= int(blockIdx.x)) ++gi;
-  const DionLaunchGroup& g = P.g[gi];
-  const int k = int(blockIdx.x) - g.begin;
-  slot = g.slot0 + k / g.per_slot;
-  local = k - (k / g.per_slot) * g.per_slot;
-}
 
 struct SetupParams {
   DionSlot s[kSetup];
@@ -111,8 +88,7 @@ static_assert(sizeof(SetupParams) <= 32000, "set-up parameters exceed the kernel
 // ---------------------------------------------------------------- set-up
 
 // CTA k writes slot z0 + k of the device table (one 4-byte word per thread: the parameter
-// reads of a warp then differ only in the word, not the slot), zeroes the slot's Gram
-// counters and writes its four output entries.
+// reads of a warp then differ only in the word, not the slot) and its six output entries.
 __global__ void __launch_bounds__(64) dion_setup_kernel(const __grid_constant__ SetupParams p) {
   const int k = blockIdx.x;
   const DionSlot& e = p.s[k];
@@ -121,7 +97,6 @@ __global__ void __launch_bounds__(64) dion_setup_kernel(const __grid_constant__ 
   const uint32_t* src = reinterpret_cast<const uint32_t*>(&e);
   uint32_t* dst = reinterpret_cast<uint32_t*>(const_cast<DionSlot*>(p.c.slots) + z);
   for (int w = threadIdx.x; w < int(sizeof(DionSlot) / 4); w += 64) dst[w] = src[w];
-  if (threadIdx.x < 2 * kGramTilesMax) e.cnt[threadIdx.x] = 0;
   if (threadIdx.x != 0) return;
   OutEntry o;
   o.bits = nullptr;
@@ -134,6 +109,10 @@ __global__ void __launch_bounds__(64) dion_setup_kernel(const __grid_constant__ 
   p.c.tP[z] = o;
   o.out = e.P1;
   p.c.tP1[z] = o;
+  o.out = e.D;
+  o.ld = 3 * p.c.ldr;
+  p.c.tG[z] = o;
+  o.ld = p.c.ldr;
   o.out = e.Rf;
   p.c.tR[z] = o;
   o.out = e.M;
@@ -312,13 +291,6 @@ __device__ __forceinline__ float* blk(float* A, int I, int J) {
 
 __device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
 
-// Address in the lower-block layout of element (row, col) (col a multiple of 4) of the
-// 64 x 64 Gram tile (ti, tj); null for the upper 32 x 32 block of a diagonal tile.
-__device__ __forceinline__ float* sf_at(float* Sf, int ti, int tj, int row, int col) {
-  const int I = 2 * ti + row / 32, J = 2 * tj + col / 32;
-  return I < J ? nullptr : blk(Sf, I, J) + (row % 32) * kLd + (col % 32);
-}
-
 // 16-byte asynchronous copy global -> shared (cp.async, L2 only); bytes past `src_bytes`
 // (0..16) are zero-filled and not read.
 __device__ __forceinline__ void cp_async16(void* dst, const void* src, int src_bytes) {
@@ -327,7 +299,6 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src, int src_b
                : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait1() { asm volatile("cp.async.wait_group 1;\n" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
 
 // Two floats rounded to bf16 (round to nearest even), the first in the low half.
@@ -336,120 +307,6 @@ __device__ __forceinline__ uint32_t bf16_pair(float a, float b) {
   return *reinterpret_cast<const uint32_t*>(&h);
 }
 
-// Bytes of the 16-byte group of columns [c0, c0 + 4) of a row that lie before column r.
-__device__ __forceinline__ int bytes_before(int c0, int r) {
-  return 4 * max(0, min(4, r - c0));
-}
-
-constexpr int kGramThreads = 64;
-
-// Lower 64 x 64 tile (ti >= tj) of S = P^T P; one CTA per (tile, row chunk) of a slot
-// (DionGridParams), 64 threads, 8 x 8 outputs each (rows 4 ty + x and 32 + 4 ty + x,
-// columns 4 tx + y and 32 + 4 tx + y, so the row reads of a warp are contiguous). A CTA
-// sums the kGramRows rows of its chunk in 32-row slabs, double-buffered in shared memory by
-// cp.async (columns past r and rows past the chunk are zero-filled: P's columns past r are
-// never written). With one chunk the tile goes straight to Sf, in the lower-block layout of
-// the Cholesky kernel. Otherwise every CTA writes its partial tile, and the CTA that arrives
-// last at the tile's counter adds the partials in chunk order (a fixed order, so the result
-// does not depend on which CTA finishes last) and writes Sf.
-__global__ void __launch_bounds__(kGramThreads) dion_gram_kernel(const __grid_constant__ DionGridParams P) {
-  const DionCommon& c = P.c;
-  const int pass = P.pass;
-  int slot, local;
-  grid_slot(P, slot, local);
-  const DionSlot& e = c.slots[slot];
-  const int gch = e.gchunks;
-  const int ntiles = (c.ldr / 64) * (c.ldr / 64 + 1) / 2;
-  const int tile = local % ntiles, chunk = local / ntiles;
-  int ti = 0, t = tile;
-  while (t > ti) { t -= ti + 1; ++ti; }
-  const int tj = t;
-  const bool diag = ti == tj;
-  const int r = c.r, ldr = c.ldr;
-  const int64_t r0 = int64_t(chunk) * kGramRows;
-  const int64_t r1 = min(int64_t(e.m), r0 + kGramRows);
-  const float* Pm = pass == 0 ? e.P0 : e.P1;
-
-  __shared__ __align__(16) float As[2][32][64], Bs[2][32][64];
-  __shared__ int last;
-  const int tid = threadIdx.x;
-  const int tx = tid & 7, ty = tid >> 3;
-  auto issue = [&](int64_t k0, int buf) {
-#pragma unroll
-    for (int h = 0; h < 8; ++h) {
-      const int q = tid + kGramThreads * h;
-      const int row = q >> 4, c4 = 4 * (q & 15);
-      const int64_t g = k0 + row;
-      const bool ok = g < r1;
-      const float* src = Pm + (ok ? g : r0) * ldr;
-      cp_async16(&As[buf][row][c4], src + ti * 64 + c4, ok ? bytes_before(ti * 64 + c4, r) : 0);
-      if (!diag) cp_async16(&Bs[buf][row][c4], src + tj * 64 + c4, ok ? bytes_before(tj * 64 + c4, r) : 0);
-    }
-    cp_async_commit();
-  };
-  float acc[8][8] = {};
-  const int nslab = int((r1 - r0 + 31) / 32);
-  issue(r0, 0);
-  for (int sl = 0; sl < nslab; ++sl) {
-    if (sl + 1 < nslab) issue(r0 + 32 * (sl + 1), (sl + 1) & 1);
-    else cp_async_commit();  // an empty group keeps the wait count uniform
-    cp_async_wait1();
-    __syncthreads();
-    const float(*Ab)[64] = As[sl & 1];
-    const float(*Bb)[64] = diag ? As[sl & 1] : Bs[sl & 1];
-#pragma unroll 4
-    for (int kk = 0; kk < 32; ++kk) {
-      const float4 a0 = *reinterpret_cast<const float4*>(&Ab[kk][4 * ty]);
-      const float4 a1 = *reinterpret_cast<const float4*>(&Ab[kk][32 + 4 * ty]);
-      const float4 b0 = *reinterpret_cast<const float4*>(&Bb[kk][4 * tx]);
-      const float4 b1 = *reinterpret_cast<const float4*>(&Bb[kk][32 + 4 * tx]);
-      const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-      const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
-#pragma unroll
-      for (int x = 0; x < 8; ++x)
-#pragma unroll
-        for (int y = 0; y < 8; ++y) acc[x][y] = __fmaf_rn(av[x], bv[y], acc[x][y]);
-    }
-    __syncthreads();
-  }
-  if (gch == 1) {  // straight to Sf, in the lower-block layout of the Cholesky kernel
-#pragma unroll
-    for (int x = 0; x < 8; ++x) {
-      const int row = 4 * ty + (x & 3) + 32 * (x >> 2);
-      float* dst0 = sf_at(e.Sf, ti, tj, row, 4 * tx);
-      float* dst1 = sf_at(e.Sf, ti, tj, row, 32 + 4 * tx);
-      if (dst0) *reinterpret_cast<float4*>(dst0) = make_float4(acc[x][0], acc[x][1], acc[x][2], acc[x][3]);
-      if (dst1) *reinterpret_cast<float4*>(dst1) = make_float4(acc[x][4], acc[x][5], acc[x][6], acc[x][7]);
-    }
-    return;
-  }
-  float* dst = e.Sp + (size_t(chunk) * ntiles + tile) * 4096;
-#pragma unroll
-  for (int x = 0; x < 8; ++x) {
-    float* row = dst + (4 * ty + (x & 3) + 32 * (x >> 2)) * 64;
-    *reinterpret_cast<float4*>(row + 4 * tx) = make_float4(acc[x][0], acc[x][1], acc[x][2], acc[x][3]);
-    *reinterpret_cast<float4*>(row + 32 + 4 * tx) = make_float4(acc[x][4], acc[x][5], acc[x][6], acc[x][7]);
-  }
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) last = atomicAdd(&e.cnt[pass * kGramTilesMax + tile], 1) == gch - 1;
-  __syncthreads();
-  if (!last) return;
-  __threadfence();
-  // the last CTA: Sf = sum of the partials in chunk order
-  for (int q = tid; q < 1024; q += kGramThreads) {
-    float4 s = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-    for (int ch = 0; ch < gch; ++ch) {
-      const float4 v = __ldcg(reinterpret_cast<const float4*>(e.Sp + (size_t(ch) * ntiles + tile) * 4096) + q);
-      s.x += v.x;
-      s.y += v.y;
-      s.z += v.z;
-      s.w += v.w;
-    }
-    float* d = sf_at(e.Sf, ti, tj, q / 16, 4 * (q % 16));
-    if (d) *reinterpret_cast<float4*>(d) = s;
-  }
-}
 
 // Factors the 32 x 32 block Ad = L L^T in registers (lane = row; the diagonal pivot of step j
 // comes from lane j, the multipliers of rows k > j from lane k) and writes L back (zeros
@@ -528,7 +385,7 @@ __device__ __forceinline__ void inv32(float* Ad, const float* rinv, int lane) {
 //   Inverse step I (block row I of W, once row block I of L and D_I are final; W_JJ = D_J):
 //   T_J = sum_{K = J .. I-1} L_IK W_KJ for every J < I, then W_IJ = -D_I T_J in place of
 //   L_IJ (row block I of L is no longer needed once all T_J are formed).
-// S arrives in this block layout (the Gram kernel writes it so). Rows and columns past r are
+// S arrives in this block layout (the assemble kernel writes it so). Rows and columns past r are
 // the identity. A pivot that is not positive sets the device error word (P had dependent
 // columns).
 __global__ void __launch_bounds__(kCholThreads, 1) dion_chol_kernel(const __grid_constant__ DionCommon c) {
@@ -703,9 +560,11 @@ __global__ void __launch_bounds__(kCholThreads, 1) dion_chol_kernel(const __grid
   }
 }
 
-// P (fp32 [m][ldr]; pass 0: P0, pass 1: P1) split for the triangular multiply on the tensor
-// cores: Ys = hi | hi | lo (bf16 [m][3 ldr]), hi = bf16(p), lo = bf16(p - hi); columns at
-// and past r are written as zeros (they meet W's zero columns, and NaN x 0 would not vanish).
+// P (fp32 [m][ldr]; pass 0: P0, pass 1: P1) in bf16 parts for the tensor-core products of
+// Cholesky QR: Ys = hi | hi | mid | lo (bf16 [m][4 ldr]) with hi = bf16(p), mid = bf16(p - hi),
+// lo = bf16(p - hi - mid) (each difference exact in fp32). The multiply by L^-T reads the
+// first three, the Gram matrix the last three. Columns at and past r are written as zeros
+// (they meet zero columns of the other factor, and NaN x 0 would not vanish).
 __global__ void __launch_bounds__(256) dion_split_kernel(const __grid_constant__ DionCommon c, int pass) {
   const DionSlot& e = c.slots[blockIdx.y];
   const uint32_t upr = uint32_t(c.ldr) / 8;
@@ -721,17 +580,50 @@ __global__ void __launch_bounds__(256) dion_split_kernel(const __grid_constant__
 #pragma unroll
     for (int q = 0; q < 8; ++q) v[q] = int(k0) + q < c.r ? P[q] : 0.0f;
   }
-  float lo[8];
+  float mid[8], lo[8];
 #pragma unroll
-  for (int q = 0; q < 8; ++q) lo[q] = v[q] - __bfloat162float(__float2bfloat16_rn(v[q]));
+  for (int q = 0; q < 8; ++q) {
+    const float d = v[q] - __bfloat162float(__float2bfloat16_rn(v[q]));
+    mid[q] = d;
+    lo[q] = d - __bfloat162float(__float2bfloat16_rn(d));
+  }
   const uint4 h = make_uint4(bf16_pair(v[0], v[1]), bf16_pair(v[2], v[3]), bf16_pair(v[4], v[5]),
                              bf16_pair(v[6], v[7]));
+  const uint4 md = make_uint4(bf16_pair(mid[0], mid[1]), bf16_pair(mid[2], mid[3]),
+                              bf16_pair(mid[4], mid[5]), bf16_pair(mid[6], mid[7]));
   const uint4 l = make_uint4(bf16_pair(lo[0], lo[1]), bf16_pair(lo[2], lo[3]), bf16_pair(lo[4], lo[5]),
                              bf16_pair(lo[6], lo[7]));
-  __nv_bfloat16* y = e.Ys + size_t(row) * 3 * c.ldr + k0;
+  __nv_bfloat16* y = e.Ys + size_t(row) * 4 * c.ldr + k0;
   *reinterpret_cast<uint4*>(y) = h;
   *reinterpret_cast<uint4*>(y + c.ldr) = h;
-  *reinterpret_cast<uint4*>(y + 2 * c.ldr) = l;
+  *reinterpret_cast<uint4*>(y + 2 * c.ldr) = md;
+  *reinterpret_cast<uint4*>(y + 3 * c.ldr) = l;
+}
+
+// S = P^T P from the Gram work product D = [hi | mid]^T [hi | mid | lo] (rows: hi, then mid
+// from row ldr; columns: hi, mid from ldr, lo from 2 ldr):
+//   S = hi^T hi + hi^T mid + mid^T hi + hi^T lo + lo^T hi + mid^T mid,
+// summed smallest first in a fixed order, into the lower 32 x 32 blocks the Cholesky kernel
+// reads (entries at or past r are zero). The terms left out (mid^T lo, lo^T mid, lo^T lo) are
+// below 2^-26 of |P|^2.
+__global__ void __launch_bounds__(256) dion_assemble_kernel(const __grid_constant__ DionCommon c) {
+  const DionSlot& e = c.slots[blockIdx.y];
+  const int r = c.r, ldr = c.ldr, ldd = 3 * ldr;
+  const int q = blockIdx.x * 256 + threadIdx.x;  // element of the lower blocks
+  const int nb = (r + 31) / 32;
+  if (q >= nb * (nb + 1) / 2 * 1024) return;
+  int b = q >> 10, I = 0;
+  while (b > I) { b -= I + 1; ++I; }
+  const int J = b, ii = (q >> 5) & 31, kk = q & 31;
+  const int i = 32 * I + ii, k = 32 * J + kk;
+  float v = 0.0f;
+  if (i < r && k < r) {
+    const float* D = e.D;
+    const float small = D[size_t(ldr + i) * ldd + ldr + k] + D[size_t(i) * ldd + 2 * ldr + k] +
+                        D[size_t(k) * ldd + 2 * ldr + i];
+    v = (small + (D[size_t(i) * ldd + ldr + k] + D[size_t(k) * ldd + ldr + i])) + D[size_t(i) * ldd + k];
+  }
+  blk(e.Sf, I, J)[ii * kLd + kk] = v;
 }
 
 // The final P (fp32 in P0) to the bf16 operand Pw (zeros from r up to ldr) and, if asked,
@@ -852,8 +744,7 @@ __global__ void __launch_bounds__(256) dion_q_kernel(const __grid_constant__ Dio
 struct DionGroup {
   int64_t m, n;
   int32_t count, slot0;
-  size_t off_bw, off_qw, off_rw, off_pw, off_p0, off_p1, off_rf, off_sp, off_sf, off_ys, off_wsp, off_cn,
-      off_cnt;
+  size_t off_bw, off_qw, off_rw, off_pw, off_p0, off_p1, off_rf, off_sf, off_ys, off_d, off_wsp, off_cn;
 };
 
 struct DionPlan {
@@ -887,7 +778,7 @@ void make_dion_plan(const mao_mat* X, int32_t batch, int32_t rank, DionPlan& pla
     return at;
   };
   plan.off_slots = take(sizeof(DionSlot) * size_t(batch));
-  plan.off_tables = take(5 * sizeof(OutEntry) * size_t(batch));
+  plan.off_tables = take(6 * sizeof(OutEntry) * size_t(batch));
   const size_t r = size_t(rank), ldr = size_t(plan.ldr);
   int slot = 0;
   for (const auto& mem : members) {
@@ -898,7 +789,7 @@ void make_dion_plan(const mao_mat* X, int32_t batch, int32_t rank, DionPlan& pla
     g.slot0 = slot;
     const size_t c = size_t(g.count), m = size_t(g.m), n = size_t(g.n);
     const size_t ldn = size_t(round_up(g.n, tc::LD_ALIGN));
-    const size_t gch = size_t(ceil_div(g.m, kGramRows)), nch = size_t(ceil_div(g.n, kNormRows));
+    const size_t nch = size_t(ceil_div(g.n, kNormRows));
     g.off_bw = take(c * m * ldn * 2);
     g.off_qw = take(c * n * ldr * 2);
     g.off_rw = take(c * n * ldr * 2);
@@ -906,13 +797,11 @@ void make_dion_plan(const mao_mat* X, int32_t batch, int32_t rank, DionPlan& pla
     g.off_p0 = take(c * m * ldr * 4);
     g.off_p1 = take(c * m * ldr * 4);
     g.off_rf = take(c * n * ldr * 4);
-    const size_t ntiles = (ldr / 64) * (ldr / 64 + 1) / 2;
-    g.off_sp = take(gch > 1 ? c * gch * ntiles * 4096 * 4 : 0);
     const size_t nsb = (ldr / 32) * (ldr / 32 + 1) / 2;  // lower 32 x 32 blocks of S
     g.off_sf = take(c * nsb * kBlk * 4);
-    g.off_ys = take(c * m * 3 * ldr * 2);
+    g.off_ys = take(c * m * 4 * ldr * 2);
+    g.off_d = take(c * 2 * ldr * 3 * ldr * 4);
     g.off_wsp = take(c * ldr * 3 * ldr * 2);
-    g.off_cnt = take(c * 2 * kGramTilesMax * 4);
     g.off_cn = take(c * (nch + 1) * r * 4);
     for (int b : mem) plan.input_of.push_back(b);
     slot += g.count;
@@ -949,7 +838,7 @@ mao_status dion_tc(const DionPlan& plan, uint8_t* ws, const OutEntry* table, int
       TcGroup& G = p.g[p.ngroups++];
       const int64_t ldn = round_up(g.n, tc::LD_ALIGN);
       const void *A, *B;
-      int64_t rowsA, ldA, rowsB, ldB;
+      int64_t rowsA, ldA, rowsB, ldB, colsA = -1, colsB = -1;
       switch (op) {
         case 0:  // (m x n)(n x r): Bw K-major, Qw MN-major
           A = ws + g.off_bw; rowsA = g.m; ldA = ldn; G.a_mn = 0;
@@ -961,10 +850,15 @@ mao_status dion_tc(const DionPlan& plan, uint8_t* ws, const OutEntry* table, int
           B = ws + g.off_pw; rowsB = g.m; ldB = ldr; G.b_mn = 1;
           G.M = int32_t(g.n); G.N = int32_t(r); G.K = int32_t(g.m);
           break;
-        case 4:  // (m x 3 ldr)(3 ldr x r): [P_hi P_hi P_lo] [W_hi W_lo W_hi]^T, both K-major
-          A = ws + g.off_ys; rowsA = g.m; ldA = 3 * ldr; G.a_mn = 0;
+        case 4:  // (m x 3 ldr)(3 ldr x r): [P_hi P_hi P_mid] [W_hi W_lo W_hi]^T, both K-major
+          A = ws + g.off_ys; rowsA = g.m; ldA = 4 * ldr; colsA = 3 * ldr; G.a_mn = 0;
           B = ws + g.off_wsp; rowsB = ldr; ldB = 3 * ldr; G.b_mn = 0;
           G.M = int32_t(g.m); G.N = int32_t(r); G.K = int32_t(3 * ldr);
+          break;
+        case 5:  // (2 ldr x m)(m x 3 ldr): [P_hi P_mid]^T [P_hi P_mid P_lo], both MN-major
+          A = ws + g.off_ys + ldr * 2; rowsA = g.m; ldA = 4 * ldr; colsA = 2 * ldr; G.a_mn = 1;
+          B = ws + g.off_ys + ldr * 2; rowsB = g.m; ldB = 4 * ldr; colsB = 3 * ldr; G.b_mn = 1;
+          G.M = int32_t(2 * ldr); G.N = int32_t(3 * ldr); G.K = int32_t(g.m);
           break;
         default:  // (m x r)(r x n): Pw K-major, Rw / Qw K-major
           A = ws + g.off_pw; rowsA = g.m; ldA = ldr; G.a_mn = 0;
@@ -976,8 +870,8 @@ mao_status dion_tc(const DionPlan& plan, uint8_t* ws, const OutEntry* table, int
       G.slot0 = g.slot0;
       G.orig_cols = G.N;
       G.final_out = 1;
-      mao_status st = tc_encode_map(&G.tmA, A, rowsA, ldA, g.count);
-      if (st == MAO_OK) st = tc_encode_map(&G.tmB, B, rowsB, ldB, g.count);
+      mao_status st = tc_encode_map(&G.tmA, A, rowsA, ldA, g.count, colsA);
+      if (st == MAO_OK) st = tc_encode_map(&G.tmB, B, rowsB, ldB, g.count, colsB);
       if (st != MAO_OK) return st;
       G.tiles_m = int32_t(ceil_div(G.M, tc::TILE_M));
       G.tiles_n = int32_t(ceil_div(G.N, tc::BN));
@@ -1015,6 +909,7 @@ mao_status dion_run(const mao_mat* X, const mao_mat* M, const mao_mat* G, const 
   c.tM = tables + 2 * batch;
   c.tX = tables + 3 * batch;
   c.tP1 = tables + 4 * batch;
+  c.tG = tables + 5 * batch;
   c.r = rank;
   c.ldr = int32_t(plan.ldr);
   c.count = batch;
@@ -1061,16 +956,12 @@ mao_status dion_run(const mao_mat* X, const mao_mat* M, const mao_mat* G, const 
       e.P0 = reinterpret_cast<float*>(ws + g.off_p0) + size_t(k) * g.m * plan.ldr;
       e.P1 = reinterpret_cast<float*>(ws + g.off_p1) + size_t(k) * g.m * plan.ldr;
       e.Rf = reinterpret_cast<float*>(ws + g.off_rf) + size_t(k) * g.n * plan.ldr;
-      e.gchunks = int32_t(ceil_div(g.m, kGramRows));
       e.nchunks = int32_t(ceil_div(g.n, kNormRows));
-      const size_t ntiles = size_t(plan.ldr / 64) * size_t(plan.ldr / 64 + 1) / 2;
-      e.Sp = e.gchunks > 1 ? reinterpret_cast<float*>(ws + g.off_sp) + size_t(k) * e.gchunks * ntiles * 4096
-                           : nullptr;
       const size_t nsb = size_t(plan.ldr / 32) * size_t(plan.ldr / 32 + 1) / 2;
       e.Sf = reinterpret_cast<float*>(ws + g.off_sf) + size_t(k) * nsb * kBlk;
-      e.Ys = reinterpret_cast<__nv_bfloat16*>(ws + g.off_ys) + size_t(k) * g.m * 3 * plan.ldr;
+      e.Ys = reinterpret_cast<__nv_bfloat16*>(ws + g.off_ys) + size_t(k) * g.m * 4 * plan.ldr;
+      e.D = reinterpret_cast<float*>(ws + g.off_d) + size_t(k) * 2 * plan.ldr * 3 * plan.ldr;
       e.Wsp = reinterpret_cast<__nv_bfloat16*>(ws + g.off_wsp) + size_t(k) * plan.ldr * 3 * plan.ldr;
-      e.cnt = reinterpret_cast<int32_t*>(ws + g.off_cnt) + size_t(k) * 2 * kGramTilesMax;
       e.cn = reinterpret_cast<float*>(ws + g.off_cn) + size_t(k) * (e.nchunks + 1) * rank;
       e.ldm = M[b].ld;
       e.ldg = G[b].ld;
@@ -1114,39 +1005,20 @@ mao_status dion_run(const mao_mat* X, const mao_mat* M, const mao_mat* G, const 
   if (st != MAO_OK) return st;
   // 3. Cholesky QR, twice: P0 -> P1 (fp32) -> Pw (bf16; + the caller's fp32 P)
   const size_t chol_smem = chol_bytes(rank);
-  const int ctiles = int(plan.ldr / 64);
-  const int ntiles = ctiles * (ctiles + 1) / 2;
-  // one launch per kLaunchGroups shape groups, exactly the CTAs the slots need
-  auto grid_launches = [&](bool gram, int pass) {
-    for (size_t g0 = 0; g0 < plan.groups.size(); g0 += kLaunchGroups) {
-      DionGridParams gp;
-      memset(&gp, 0, sizeof(gp));
-      gp.c = c;
-      gp.pass = pass;
-      int64_t ctas = 0;
-      for (size_t gi = g0; gi < plan.groups.size() && gp.ng < kLaunchGroups; ++gi) {
-        const DionGroup& g = plan.groups[gi];
-        DionLaunchGroup& lg = gp.g[gp.ng++];
-        lg.slot0 = g.slot0;
-        lg.count = g.count;
-        lg.per_slot = gram ? ntiles * int(ceil_div(g.m, kGramRows)) : int(ceil_div(g.m, 64)) * ctiles;
-        lg.begin = int32_t(ctas);
-        ctas += int64_t(lg.per_slot) * g.count;
-      }
-      if (ctas > 0x7FFFFFFF) return false;
-      profile_before_launch(stream, MAO_PROF_DION_GRAM);
-      dion_gram_kernel<<<unsigned(ctas), kGramThreads, 0, stream>>>(gp);
-      if (!launched()) return false;
-    }
-    return true;
-  };
   int64_t max_m = 0;
   for (const auto& g : plan.groups) max_m = std::max<int64_t>(max_m, g.m);
   const unsigned split_blocks = unsigned(ceil_div(max_m * (plan.ldr / 8), 256));
+  const int nbk = int(ceil_div(rank, 32));
+  const unsigned assemble_blocks = unsigned(nbk * (nbk + 1) / 2 * 4);
   for (int pass = 0; pass < 2; ++pass) {
-    if (!grid_launches(true, pass)) return MAO_ERR_CUDA;
     profile_before_launch(stream, MAO_PROF_DION_SPLIT);
     dion_split_kernel<<<dim3(split_blocks, nb), 256, 0, stream>>>(c, pass);
+    if (!launched()) return MAO_ERR_CUDA;
+    // S = P^T P on the tensor cores from P's parts, assembled in the Cholesky's block layout
+    mao_status sg = dion_tc(plan, ws, c.tG, 5, 1.0f, stream);
+    if (sg != MAO_OK) return sg;
+    profile_before_launch(stream, MAO_PROF_DION_GRAM);
+    dion_assemble_kernel<<<dim3(assemble_blocks, nb), 256, 0, stream>>>(c);
     if (!launched()) return MAO_ERR_CUDA;
     profile_before_launch(stream, MAO_PROF_DION_CHOL);
     dion_chol_kernel<<<nb, kCholThreads, chol_smem, stream>>>(c);
@@ -1163,7 +1035,7 @@ mao_status dion_run(const mao_mat* X, const mao_mat* M, const mao_mat* G, const 
   if (st != MAO_OK) return st;
   // 5. Q = ColumnNormalize(R) (caller's Q), bf16 copies of Q and R
   profile_before_launch(stream, MAO_PROF_DION_NORM);
-  dion_colnorm_kernel<<<dim3(unsigned(ctiles), unsigned(plan.max_nchunks), nb), 256, 0, stream>>>(c);
+  dion_colnorm_kernel<<<dim3(unsigned(plan.ldr / 64), unsigned(plan.max_nchunks), nb), 256, 0, stream>>>(c);
   if (!launched()) return MAO_ERR_CUDA;
   profile_before_launch(stream, MAO_PROF_DION_NORM);
   dion_norm_kernel<<<nb, 256, 0, stream>>>(c);

@@ -141,8 +141,10 @@ struct TcParams {
   unsigned long long timeout_ns; // bound of every barrier wait
 };
 
+// Operand map of [count][rows][ld] bf16 buffers (ld a multiple of 64); cols (a multiple of
+// 64, at most ld; -1 for ld) limits the columns read, later ones load as zeros.
 mao_status tc_encode_map(CUtensorMap* map, const void* base, int64_t rows, int64_t ld,
-                         int64_t count);
+                         int64_t count, int64_t cols = -1);
 // Bulk-store map of a workspace output buffer [count][rows][ld] bf16 (64 x 32 blocks).
 mao_status tc_encode_store_map(CUtensorMap* map, const void* base, int64_t rows, int64_t ld,
                                int64_t count);

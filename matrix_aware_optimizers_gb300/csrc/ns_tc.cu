@@ -1195,11 +1195,13 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }  // namespace
 
 mao_status tc_encode_map(CUtensorMap* map, const void* base, int64_t rows, int64_t ld,
-                         int64_t count) {
+                         int64_t count, int64_t cols) {
   auto fn = encode_fn();
-  if (!fn || ld % CHUNK != 0) return MAO_ERR_UNSUPPORTED;
-  // dims: 64 columns of a chunk, rows, column chunks (128 bytes apart), matrices
-  const cuuint64_t dims[4] = {cuuint64_t(CHUNK), cuuint64_t(rows), cuuint64_t(ld / CHUNK),
+  if (cols < 0) cols = ld;
+  if (!fn || ld % CHUNK != 0 || cols % CHUNK != 0 || cols > ld) return MAO_ERR_UNSUPPORTED;
+  // dims: 64 columns of a chunk, rows, column chunks (128 bytes apart; the first cols / 64
+  // of each row, chunks past them read as zeros), matrices
+  const cuuint64_t dims[4] = {cuuint64_t(CHUNK), cuuint64_t(rows), cuuint64_t(cols / CHUNK),
                               cuuint64_t(count)};
   const cuuint64_t strides[3] = {cuuint64_t(ld) * 2, cuuint64_t(CHUNK) * 2,
                                  cuuint64_t(rows) * cuuint64_t(ld) * 2};
