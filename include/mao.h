@@ -312,9 +312,10 @@ mao_status apply_update(const mao_mat* W, const uint32_t* const* vote, const mao
  *   P_out       NULL, or HOST array of `batch` device pointers (each may be NULL): the
  *               final P, m x r fp32, row stride r.
  *   rank        1..256, at most min(m, n) of every matrix; batch <= 65535.
- *   compute     MAO_BF16 only: B, Q, P and R enter
- *               the three dense products (B Q, B^T P, P R^T / P Q^T) as bf16 with fp32
- *               accumulation on tcgen05 tensor cores; everything else is fp32.
+ *   compute     MAO_BF16 only: B, Q, P and R enter the dense products (B Q, B^T P,
+ *               P R^T / P Q^T) as bf16 with fp32 accumulation on tcgen05 tensor cores; the
+ *               two products of Cholesky QR use bf16 parts of fp32 factors as above; the
+ *               rest (staging sums, Cholesky, norms, the updates' arithmetic) is fp32.
  *   workspace   >= dion_workspace_bytes(X, batch, rank) bytes, 256-byte aligned.
  *   Errors: MAO_ERR_INVALID_ARG for mismatched shapes of X, M, G, Q, X_out (or X_out's
  *   dtype differing from X's) or a bad rank;
@@ -371,7 +372,7 @@ enum {
   MAO_PROF_DION_STAGE = 2,     /* B = M + G and its bf16 copy; bf16 copy of Q_prev */
   MAO_PROF_DION_GRAM = 3,      /* P^T P assembled from its tensor-core parts (the products are MAO_PROF_TC) */
   MAO_PROF_DION_CHOL = 4,      /* Cholesky factor and its inverse */
-  MAO_PROF_DION_SPLIT = 5,     /* P split into bf16 parts for P L^-T (whose product is MAO_PROF_TC), and the final P to bf16 */
+  MAO_PROF_DION_SPLIT = 5,     /* P split into bf16 parts for the Cholesky QR products (MAO_PROF_TC), and the final P to bf16 */
   MAO_PROF_DION_NORM = 6       /* column norms of R, Q = ColumnNormalize(R) */
 };
 int64_t mao_launch_count(void);
