@@ -177,6 +177,10 @@ mao_status muon_step(const mao_mat* W, const mao_mat* M, const mao_mat* G, const
 /* Size of the scratch area ns_orthogonalize_noalloc uses (16 MiB per device). */
 #define MAO_NOALLOC_WORKSPACE_BYTES (16u * 1024u * 1024u)
 
+/* MAO_NOALLOC_WORKSPACE_BYTES as compiled into the library (no counterpart on the pages):
+ * the largest ns_workspace_bytes() that ns_orthogonalize_noalloc accepts. */
+size_t ns_noalloc_workspace_bytes(void);
+
 /*
  * ns_orthogonalize without a workspace argument. The pages have no counterpart of this
  * call: it exists for callers that cannot call cudaMalloc, such as code inside a host
@@ -190,9 +194,12 @@ mao_status muon_step(const mao_mat* W, const mao_mat* M, const mao_mat* G, const
  *     bf16); larger requests return MAO_ERR_WORKSPACE before any device work.
  *   Memory: allocates nothing. Every GPU that loads this library holds the 16 MiB array
  *     until the process exits, whether or not the call is used.
- *   Set-up: the first call on each device looks up the array's device address
- *     (cudaGetSymbolAddress) with that device current; make that first call before any
- *     stream capture on the device.
+ *   Set-up: every call made outside stream capture looks up the array's device address
+ *     (cudaGetSymbolAddress) with the current device, so a call after cudaDeviceReset or
+ *     in another context finds the array where that context loaded it. A call made while
+ *     its stream is being captured reuses the address of the last call on that device, so
+ *     make the first call on each device (and the first after a device reset) outside any
+ *     capture; a captured call without such an earlier call returns MAO_ERR_UNSUPPORTED.
  *   Sharing: all calls on a device use the same array, which keeps the last call's
  *     contents (nothing in it needs to start at zero). Calls whose work overlaps on the GPU
  *     (other streams, other host threads) race on it: order them on one stream or with

@@ -19,9 +19,6 @@ MAO_BF16 = 1
 MAO_I8 = 2      # ns_orthogonalize input only
 MAO_SIGN1 = 3   # ns_orthogonalize input only (packed signs, ld == cols)
 
-# scratch size of ns_orthogonalize_noalloc (MAO_NOALLOC_WORKSPACE_BYTES in mao.h)
-NOALLOC_WORKSPACE_BYTES = 16 * 1024 * 1024
-
 # every symbol include/mao.h declares
 EXPORTS = (
     "mao_abi_version",
@@ -31,6 +28,7 @@ EXPORTS = (
     "ns_orthogonalize",
     "muon_step",
     "ns_orthogonalize_noalloc",
+    "ns_noalloc_workspace_bytes",
     "ns_blockwise_workspace_bytes",
     "ns_orthogonalize_blockwise",
     "sign_pack_bits",
@@ -109,6 +107,8 @@ def load():
     lib.ns_orthogonalize_noalloc.argtypes = [
         P(MaoMat), P(MaoMat), ctypes.c_int32, ctypes.c_int32, P(ctypes.c_float), ctypes.c_int32,
         ctypes.c_float, ctypes.c_int32, P(ctypes.c_void_p), vp]
+    lib.ns_noalloc_workspace_bytes.restype = ctypes.c_size_t
+    lib.ns_noalloc_workspace_bytes.argtypes = []
     lib.ns_blockwise_workspace_bytes.restype = ctypes.c_size_t
     lib.ns_blockwise_workspace_bytes.argtypes = [P(MaoMat), ctypes.c_int32, ctypes.c_int64,
                                                  ctypes.c_int64, ctypes.c_int32]

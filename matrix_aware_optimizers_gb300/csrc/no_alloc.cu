@@ -25,17 +25,25 @@ constexpr int kMaxDevices = 64;
 void* g_scratch_ptr[kMaxDevices];
 std::mutex g_scratch_mutex;
 
-// Device address of the scratch area on the current device, resolved once per device.
-mao_status scratch_address(void** ptr) {
+// Device address of the scratch area on the current device. Outside stream capture it is
+// looked up on every call: after a cudaDeviceReset, or in another context on the same
+// device, the module is loaded again and the array may sit at another address. During a
+// capture the address of the last lookup on this device is used (a capture must not be the
+// first use of the call on a device, nor the first use after a reset).
+mao_status scratch_address(cudaStream_t stream, void** ptr) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return MAO_ERR_CUDA;
   if (dev < 0 || dev >= kMaxDevices) return MAO_ERR_UNSUPPORTED;
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) return MAO_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_scratch_mutex);
-  if (g_scratch_ptr[dev] == nullptr) {
+  if (cap == cudaStreamCaptureStatusNone) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
       return MAO_ERR_CUDA;
     g_scratch_ptr[dev] = p;
+  } else if (g_scratch_ptr[dev] == nullptr) {
+    return MAO_ERR_UNSUPPORTED;  // first use on this device inside a capture
   }
   *ptr = g_scratch_ptr[dev];
   return MAO_OK;
@@ -45,6 +53,8 @@ mao_status scratch_address(void** ptr) {
 }  // namespace mao
 
 using namespace mao;
+
+extern "C" size_t ns_noalloc_workspace_bytes(void) { return size_t(MAO_NOALLOC_WORKSPACE_BYTES); }
 
 extern "C" mao_status ns_orthogonalize_noalloc(const mao_mat* in, const mao_mat* out,
                                                int32_t batch, int32_t steps,
@@ -72,7 +82,7 @@ extern "C" mao_status ns_orthogonalize_noalloc(const mao_mat* in, const mao_mat*
   if (need > size_t(MAO_NOALLOC_WORKSPACE_BYTES)) return MAO_ERR_WORKSPACE;
   if (compute == MAO_BF16 && device_cc() / 10 != 10) return MAO_ERR_UNSUPPORTED;
   void* scratch = nullptr;
-  const mao_status st = scratch_address(&scratch);
+  const mao_status st = scratch_address(static_cast<cudaStream_t>(stream), &scratch);
   if (st != MAO_OK) return st;
   // Nothing in the scratch area has to start at zero: every region the products read is
   // written earlier in the same call (staged inputs, norms, A, B, X), so the contents a

@@ -34,7 +34,7 @@ def check_sign_agreement(u_gpu, u_ref, bits_gpu, strict_rms=None):
     """
     u_ref = np.asarray(u_ref, np.float64).reshape(-1)
     u_gpu = np.asarray(u_gpu, np.float64).reshape(-1)
-    ref_bits = (u_ref >= 0).astype(np.uint8)  # oracle rule: u < 0 -> -1, else +1
+    ref_bits = (~(u_ref < 0)).astype(np.uint8)  # oracle rule: u < 0 -> -1, else +1 (NaN: +1)
     bad = np.nonzero(bits_gpu != ref_bits)[0]
     if bad.size:
         err = np.abs(u_gpu[bad] - u_ref[bad])
@@ -52,3 +52,16 @@ def rand_matrix(gen, shape, dtype, device, scale=1.0, ld=None):
         return (torch.randn(shape, generator=gen, device="cpu") * scale).to(dtype).to(device)
     big = (torch.randn((R, ld), generator=gen, device="cpu") * scale).to(dtype).to(device)
     return big[:, :C]
+
+
+def sign_criterion(u_ref, bits_gpu, rel=1e-3):
+    """The end-to-end sign criterion as stated for the step: the share of entries whose
+    GPU sign equals the oracle's, and the share of the disagreements that lie where
+    |U_ref| < rel * rms(U_ref). Returns (agreement, flips, share_small)."""
+    u_ref = np.asarray(u_ref, np.float64).reshape(-1)
+    ref_bits = (~(u_ref < 0)).astype(np.uint8)
+    bad = np.nonzero(np.asarray(bits_gpu) != ref_bits)[0]
+    rms = np.sqrt(np.mean(u_ref ** 2))
+    small = int(np.count_nonzero(np.abs(u_ref[bad]) < rel * rms)) if bad.size else 0
+    share = small / bad.size if bad.size else 1.0
+    return 1.0 - bad.size / u_ref.size, int(bad.size), share

@@ -18,7 +18,7 @@ import torch
 
 import bench
 import oracle
-from helpers import bits_of, check_sign_agreement, rel_fro, to_np, words_np
+from helpers import bits_of, check_sign_agreement, rel_fro, sign_criterion, to_np, words_np
 from matrix_aware_optimizers_gb300 import workloads
 import matrix_aware_optimizers_gb300 as mao
 
@@ -94,7 +94,7 @@ def test_config2_muon_gpt12_d768_full(cuda):
     _check_muon(wl, step, host, M_after, W_before, [0, 1, 2, 3, 46])
 
 
-def test_config3_sign_muon_4096_w8_full(cuda):
+def test_config3_sign_muon_4096_w8_full(cuda, record_property):
     wl = workloads.workload(3)
     step, host, M_after, U, W_before = _run_step(wl, cuda, keep_u=True)
     R, C = wl.shapes[0]
@@ -103,9 +103,19 @@ def test_config3_sign_muon_4096_w8_full(cuda):
     assert np.array_equal(to_np(M_after[m]), oracle.momentum(host["M"][m], host["G"][m], wl.mu, "bf16"))
     u_ref = oracle.newton_schulz(to_np(M_after[m]), wl.steps, wl.coeffs, wl.eps)
     u_gpu = to_np(U[m])
-    assert rel_fro(u_gpu, u_ref) <= TOL["bf16"]
-    frac = check_sign_agreement(u_gpu, u_ref, bits_of(words_np(step.bits[m]), n))
+    err = rel_fro(u_gpu, u_ref)
+    assert err <= TOL["bf16"]
+    bits_m = bits_of(words_np(step.bits[m]), n)
+    frac = check_sign_agreement(u_gpu, u_ref, bits_m)
     assert frac >= AGREE["bf16"], frac
+    # the criterion as the step states it: >= 99.9% agreement, every flip where
+    # |U| < 1e-3 rms(U). The bf16 path does not meet it (its 2e-2 value tolerance allows
+    # about 0.3% flips at 1% error); both figures are reported, not asserted.
+    agree, flips, share_small = sign_criterion(u_ref, bits_m)
+    print("config 3 worker 0: U rel. Frobenius error %.4e; sign agreement %.5f (%d flips of %d); "
+          "share of flips with |U| < 1e-3 rms(U): %.4f" % (err, agree, flips, n, share_small))
+    record_property("sign_agreement", agree)
+    record_property("sign_flips_small_share", share_small)
     # fused signs equal the signs of the fp32 values the same epilogue produced
     for w in range(wl.workers):
         uw = to_np(U[w]).reshape(-1)
@@ -132,10 +142,17 @@ def test_config4_dense32_full(cuda):
     if free < 160 * 2 ** 30:
         pytest.skip("needs about 130 GB of free device memory")
     step, host, M_after, _, W_before = _run_step(wl, cuda)
-    # one attention matrix (4096 x 4096) and the tall MLP matrix of layer 31 (sampled
-    # entries of the momentum; the 14336 x 4096 NS is checked through its properties)
+    # one attention matrix (4096 x 4096) and the tall MLP matrix of layer 31, both against
+    # the oracle; the tall one's U also through the quintic's singular-value band
     _check_muon(wl, step, host, M_after, W_before, [0])
     i = 7 * 31 + 5  # 14336 x 4096
+    # the tall matrix through the oracle, element by element (about 5.5e12 fp64 flops)
+    assert np.array_equal(to_np(M_after[i]), oracle.momentum(host["M"][i], host["G"][i], wl.mu, "f32"))
+    u_ref = oracle.newton_schulz(to_np(M_after[i]), wl.steps, wl.coeffs, wl.eps)
+    err = rel_fro(to_np(step.U[i]), u_ref)
+    print("config 4 matrix %d (14336 x 4096): U rel. Frobenius error %.4e" % (i, err))
+    assert err <= TOL["bf16"], err
+    del u_ref
     u = step.U[i].float()
     # polar-factor property at any size: the Gram matrix of U has eigenvalues in the
     # quintic's output band (singular values of U in [0.68, 1.21] for sigma >= 1.5e-3,

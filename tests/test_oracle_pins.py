@@ -304,6 +304,79 @@ def test_sign_muon_step_composition():
     assert np.allclose(out["W"], W_ref, rtol=2 ** -8, atol=0)
 
 
+def _read_sections(path):
+    """Sections [name] of 'key values...' lines; matrix rows separated by ';'."""
+    cases, cur = {}, None
+    with open(path) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if not line:
+                continue
+            if line.startswith("["):
+                cur = cases.setdefault(line.strip("[]"), {})
+                continue
+            key, rest = line.split(None, 1)
+            if ";" in rest or key in ("M", "G", "M_new", "U", "W", "W_new"):
+                cur[key] = np.array([[float(v) for v in row.split()] for row in rest.split(";")])
+            else:
+                vals = [float(v) for v in rest.split()]
+                cur[key] = vals if len(vals) > 1 else vals[0]
+    return cases
+
+
+def test_muon_step_hand_table(golden_dir):
+    """oracle.muon_step against hand-worked steps (tests/golden/muon_step_hand.txt): dyadic
+    momentum with known singular values, the polynomial applied to them by hand, and the
+    update W - eta U entry by entry (wide and tall orientations, cubic and quintic, eta as
+    the fp32 value of lr)."""
+    cases = _read_sections(os.path.join(golden_dir, "muon_step_hand.txt"))
+    assert len(cases) == 5
+    for name, c in cases.items():
+        out = oracle.muon_step([c["W"]], [c["M"]], [c["G"]], c["mu"], c["lr"], int(c["steps"]),
+                               tuple(c["coeffs"]), eps=0.0, m_store="f32")
+        assert np.array_equal(out["M"][0], c["M_new"]), name
+        assert np.allclose(out["U"][0], c["U"], rtol=0, atol=1e-15), name
+        assert np.allclose(out["W"][0], c["W_new"], rtol=0, atol=1e-15), name
+        # the same update through apply_update_f64 on the hand-worked U
+        assert np.allclose(oracle.apply_update_f64(c["W"], c["U"], c["lr"]), c["W_new"],
+                           rtol=0, atol=1e-15), name
+
+
+def test_apply_update_f64_lr_is_fp32_value():
+    # W - float32(lr) * D: lr = 0.02 is 10737418 * 2^-29 in fp32; with D = 1 and W = 0 the
+    # fp64 result is exactly that value, negated
+    got = oracle.apply_update_f64(np.zeros((1, 2)), np.array([[1.0, -2.0]]), 0.02)
+    eta = 10737418 * 2.0 ** -29
+    assert got.tolist() == [[-eta, 2 * eta]]
+    assert eta != 0.02
+
+
+@pytest.mark.parametrize("shape", [(24, 40), (40, 24), (32, 32)])
+@pytest.mark.parametrize("m_store", ["f32", "bf16"])
+def test_muon_step_matches_svd_route(shape, m_store):
+    """oracle.muon_step against an independent route: the momentum built from bf16-exact
+    dyadic inputs with mu = 1/2 (so mu M + G is exact in every precision and needs no
+    rounding), the polar direction by the SVD closed form U diag(p^5(s/(||M||+eps))) V^T,
+    and the update W - float32(lr) U by plain subtraction."""
+    rng = np.random.default_rng(shape[0] * 100 + shape[1] + len(m_store))
+    n = 3
+    Ws = [rng.integers(-64, 65, shape) / 256.0 for _ in range(n)]
+    Ms = [rng.integers(-32, 33, shape) / 64.0 for _ in range(n)]
+    Gs = [rng.integers(-32, 33, shape) / 128.0 for _ in range(n)]
+    lr = 0.02
+    out = oracle.muon_step(Ws, Ms, Gs, 0.5, lr, 5, QUINTIC, m_store=m_store)
+    eta = float(np.float32(lr))
+    for i in range(n):
+        M_new = 0.5 * Ms[i] + Gs[i]
+        assert np.array_equal(out["M"][i], M_new)
+        U = _ns_by_svd(M_new, 5, QUINTIC)
+        assert np.linalg.norm(out["U"][i] - U) <= 1e-10 * np.linalg.norm(U)
+        W_new = Ws[i] - eta * U
+        assert np.linalg.norm(out["W"][i] - W_new) <= 1e-12 * np.linalg.norm(Ws[i] - W_new)
+        # a sign slip (W + eta U) or a transposed direction would be far off
+        assert np.linalg.norm(out["W"][i] - (Ws[i] + eta * U)) > 1.0 * eta * np.linalg.norm(U)
+
+
 def test_dense_flop_count():
     # (4 m^2 n + 2 m^3) per iteration: 64 x 128, 5 steps
     assert oracle.ns_dense_flops(64, 128, 5) == 5 * (4 * 64 * 64 * 128 + 2 * 64 ** 3) == 13_107_200
