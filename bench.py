@@ -14,12 +14,24 @@ every stage through the C ABI of libmao.so.
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config C] [--impl reference]
   python bench.py --sweep-hbm      (each HBM-bound kernel alone on L2-cold buffers)
 
-Default workload: the 12-layer d=768 transformer-shaped Muon step (48 bf16 matrices).
-`--impl reference` times the fp64 CPU oracle on the same workload and metric (each
-step a bounded sample: one matrix of the workload, cycling), on rank 0 only.
+Default workload: the 12-layer d=768 transformer-shaped Muon step (48 bf16 matrices). On
+one GPU the default run also measures the other four workloads (64x128 Sign-Muon, 4096^2
+Sign-Muon with 8 workers, the 32-layer dense model, the 128-expert MoE) and reports them
+under "per_config" (--no-per-config skips them).
+
+Across N GPUs (torchrun) a Muon workload runs layer-wise: every matrix is owned by one rank
+(longest-first on Newton–Schulz flops) and the updated weights are all-gathered; a Sign-Muon
+workload splits its workers over the ranks and all-gathers the packed signs (or all-reduces
+the int8 signs). The job's total work is fixed ("scaling": "strong"). Dion runs as replicas.
+
+`--impl reference` times the fp64 CPU oracle on the same workload and metric on rank 0
+only: whole steps where one takes seconds (the 64x128 and 12-layer workloads), otherwise
+each step a bounded sample of the workload (its first matrices or workers), reported as
+such.
 """
 
 import argparse
+import gc
 import json
 import os
 import statistics
@@ -31,13 +43,29 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
-DEFAULT_STEPS = {1: 2000, 2: 400, 3: 60, 4: 4, 5: 100, 6: 400}
+DEFAULT_STEPS = {1: 2000, 2: 400, 3: 60, 4: 10, 5: 100, 6: 400}
 DEFAULT_WARMUP = {1: 20, 2: 10, 3: 5, 4: 3, 5: 5, 6: 10}
+# workloads measured beside the default one (steps, warm-up steps), on one GPU
+PER_CONFIG = {1: (2000, 20), 3: (60, 5), 4: (10, 3), 5: (100, 5)}
+PARITY_TESTS = {
+    1: "tests/test_gpu_steps.py::test_config1_sign_muon_64x128_f32",
+    2: "tests/test_gpu_steps.py::test_config2_muon_gpt12_d768_full, "
+       "test_config2_fused_step_equals_composed_full",
+    3: "tests/test_gpu_steps.py::test_config3_sign_muon_4096_w8_full",
+    4: "tests/test_gpu_steps.py::test_config4_dense32_full",
+    5: "tests/test_gpu_steps.py::test_config5_moe_grouped_full, "
+       "test_config5_fused_step_equals_composed_full",
+    6: "tests/test_gpu_steps.py::test_config6_dion_full",
+}
+# the oracle arm times whole steps when one step is at most this many dense NS flops
+REFERENCE_WHOLE_STEP_FLOPS = 4e12
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# kernels timed over a window at least this long run under the power cap: sustained peak
+SUSTAINED_WINDOW_S = 1.0
 
 
-def parse_args():
+def parse_args(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=None)
@@ -64,7 +92,9 @@ def parse_args():
                          "instead of one muon_step call")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    return ap.parse_args()
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="do not measure the other workloads beside the default one")
+    return ap.parse_args(argv)
 
 
 def load_peaks():
@@ -75,6 +105,19 @@ def load_peaks():
         return p, "measured"
     except (OSError, ValueError):
         return dict(FALLBACK_PEAKS), "fallback"
+
+
+def choose_peak(peaks, src, window_s):
+    """The bf16 denominator of a tensor-core kernel timed over `window_s` seconds: the burst
+    figure for a kernel timed alone in a short window, the sustained one for a window long
+    enough to run under the power cap. Returns (peak, source text)."""
+    if window_s >= SUSTAINED_WINDOW_S:
+        return (peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]),
+                "%s bf16_tflops_sustained (per-launch timing window %.2f s >= %.0f s)"
+                % (src, window_s, SUSTAINED_WINDOW_S))
+    return (peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]),
+            "%s bf16_tflops burst (per-launch timing window %.2f s < %.0f s)"
+            % (src, window_s, SUSTAINED_WINDOW_S))
 
 
 # ------------------------------------------------------------------ work model
@@ -158,11 +201,13 @@ class Step:
     """Device buffers and the sequence of C-ABI calls of one optimizer step."""
 
     def __init__(self, wl, inputs, device, variant="bits", post_polar=False, block=None,
-                 fused=True):
+                 fused=True, dplan=None):
         """variant: "bits" (1-bit all-gather) or "int8" (integer SUM all-reduce) aggregation
         of a Sign-Muon workload; post_polar: the optional Newton–Schulz step on S_bar;
         fused: a Muon workload on the tensor cores runs as one muon_step call (momentum in
-        the staging pass, the update in the last product) instead of the three calls."""
+        the staging pass, the update in the last product) instead of the three calls;
+        dplan: the step across ranks (distributed.LayerwiseMuon for a Muon workload,
+        distributed.SignExchange for a Sign-Muon workload), None on one GPU."""
         import torch
         import matrix_aware_optimizers_gb300 as mao
         if wl.kind != "sign" and (variant != "bits" or post_polar):
@@ -178,6 +223,10 @@ class Step:
         self.fused = fused and wl.kind == "muon" and block is None and wl.compute == "bf16"
         self.W, self.M, self.G = inputs["W"], inputs["M"], inputs["G"]
         self.dev = device
+        self.dplan = dplan
+        if dplan is not None:
+            self._init_dist(wl, device, variant, post_polar, block)
+            return
         if wl.kind == "dion":
             # one Dion step per call: the previous right factors Q are updated in place
             self.Q = inputs["Q"]
@@ -269,7 +318,74 @@ class Step:
         self.mao.muon_step(self.W, self.M, self.G, wl.mu, wl.lr, wl.steps, wl.coeffs, wl.eps,
                            wl.compute, ws=self.ws, W_out=W_out)
 
+    def _init_dist(self, wl, device, variant, post_polar, block):
+        import torch
+        from matrix_aware_optimizers_gb300 import distributed
+        mao, plan = self.mao, self.dplan
+        if block is not None or post_polar:
+            raise ValueError("the step across ranks runs without blocks or the post-vote polar step")
+        if wl.kind == "muon":
+            if not self.fused:
+                raise ValueError("the layer-wise step runs the one-call muon_step")
+            # every rank holds every weight (the layout of the all-gather); momenta and
+            # gradients only of the matrices it owns
+            self.flat, views = plan.layout.allocate(device)
+            for v, w in zip(views, self.W):
+                v.copy_(w)
+            self.W = views
+            self.M = [self.M[i] for i in plan.mine]
+            self.G = [self.G[i] for i in plan.mine]
+            self.U = []
+            self.ws = mao.workspace(self.M, wl.compute, device) if self.M else None
+            self.shapes_own = [tuple(m.shape) for m in self.M]
+            return
+        if wl.kind != "sign":
+            raise ValueError("Dion runs as replicas across ranks")
+        ex = plan
+        mine = range(ex.first_worker, ex.first_worker + ex.local)
+        self.M = [self.M[m] for m in mine]
+        self.G = [self.G[m] for m in mine]
+        self.nbits = ex.nbits
+        self.vote = torch.zeros(ex.stride, dtype=torch.int32, device=device)
+        if variant == "bits":
+            self.words = ex.allocate_words(device)
+            self.bits = ex.my_words(self.words)
+            self.U = [None] * ex.local
+        else:
+            self.U = [torch.empty_like(m) for m in self.M]
+            self.s8 = torch.zeros((ex.local, ex.s_stride), dtype=torch.int8, device=device)
+            self.total = torch.zeros(ex.nbits, dtype=torch.int8, device=device)
+        self.ws = mao.workspace(self.M, wl.compute, device)
+        self.shapes_own = [tuple(m.shape) for m in self.M]
+        self._distributed = distributed
+
+    def dist_call(self):
+        """One step of this rank across ranks: its share of the work, then the exchange."""
+        from matrix_aware_optimizers_gb300 import distributed
+        wl, plan = self.wl, self.dplan
+        if wl.kind == "muon":
+            if self.M:
+                self.mao.muon_step([self.W[i] for i in plan.mine], self.M, self.G, wl.mu, wl.lr,
+                                   wl.steps, wl.coeffs, wl.eps, wl.compute, ws=self.ws)
+            distributed.allgather_weights(plan.layout, self.flat, plan.group)
+        elif self.variant == "bits":
+            distributed.sign_muon_step(plan, self.W[0], self.M, self.G, self.words, self.vote,
+                                       wl.mu, wl.lr, wl.steps, wl.coeffs, wl.eps, wl.compute,
+                                       ws=self.ws)
+        else:
+            distributed.sign_muon_step_int8(plan, self.W[0], self.M, self.G, self.U, self.s8,
+                                            self.total, self.vote, wl.mu, wl.lr, wl.steps,
+                                            wl.coeffs, wl.eps, wl.compute, ws=self.ws)
+
+    @property
+    def whole_call(self):
+        """The step is one call (or one call and its exchange): no per-stage timing."""
+        return self.fused or self.dplan is not None
+
     def __call__(self):
+        if self.dplan is not None:
+            self.dist_call()
+            return
         if self.fused:
             self.fused_call()
             return
@@ -306,10 +422,11 @@ def oracle_sample(wl, host, budget_s, max_items=None, variant="bits", post_polar
 
     import oracle
     shapes = [tuple(x.shape) for x in host["M"]] if wl.kind != "sign" else [tuple(host["W"][0].shape)]
-    total = dense_flops(shapes, wl.steps) * (wl.workers + (1 if post_polar else 0)
-                                             if wl.kind == "sign" else 1)
+    # the fraction is of the workload's whole step (host may hold only a prefix of it)
+    total = dense_flops(wl.shapes, wl.steps) * (wl.workers + (1 if post_polar else 0)
+                                                if wl.kind == "sign" else 1)
     if wl.kind == "dion":  # work fraction by matrix elements (every element costs 8 r flops)
-        total = sum(r * c for r, c in shapes)
+        total = sum(r * c for r, c in wl.shapes)
     store = "bf16" if wl.m_dtype.itemsize == 2 else "f32"
     wstore = "bf16" if wl.w_dtype.itemsize == 2 else "f32"
     done_flops, t_used, items = 0, 0.0, 0
@@ -376,40 +493,72 @@ def host_copy(inputs):
     return {k: [t.float().cpu().numpy() for t in v] for k, v in inputs.items()}
 
 
+def reference_items(wl, post_polar=False):
+    """Matrices (Muon, Dion) or workers (Sign-Muon) one timed oracle step covers: all of
+    them when the whole step costs at most REFERENCE_WHOLE_STEP_FLOPS dense Newton–Schulz
+    flops, else the longest prefix within that (at least one)."""
+    if wl.kind == "dion":
+        return len(wl.shapes)
+    if wl.kind == "sign":
+        per = dense_flops(wl.shapes, wl.steps)
+        n_all = wl.workers
+        if per * (n_all + (1 if post_polar else 0)) <= REFERENCE_WHOLE_STEP_FLOPS:
+            return n_all
+        return max(1, int(REFERENCE_WHOLE_STEP_FLOPS // per))
+    tot, n = 0, 0
+    for s in wl.shapes:
+        tot += dense_flops([s], wl.steps)
+        if n >= 1 and tot > REFERENCE_WHOLE_STEP_FLOPS:
+            break
+        n += 1
+    return n
+
+
 def run_reference(args, wl, block=None):
-    import torch
+    """The oracle arm: the fp64 CPU oracle timed on the host cores, on rank 0 only, for the
+    same workload, metric and config as the GPU arm."""
     from matrix_aware_optimizers_gb300 import workloads
     rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", str(args.gpus)))
     if rank != 0:
         return
-    K = args.steps if args.steps is not None else DEFAULT_STEPS[wl.index]
-    Wu = args.warmup if args.warmup is not None else DEFAULT_WARMUP[wl.index]
-    shapes = wl.shapes if wl.kind == "muon" else wl.shapes
-    # one matrix of the workload per reference step
-    if wl.index == 4:
+    K = args.steps if args.steps is not None else 3
+    Wu = args.warmup if args.warmup is not None else 1
+    shapes = None
+    if wl.index == 4:  # the oracle needs host copies of the inputs: generate one layer
         shapes = [(4096, 4096)] * 4 + [(4096, 14336), (14336, 4096), (4096, 14336)]
-    inputs = workloads.generate(wl, "cpu", shapes=shapes if wl.index == 4 else None)
+    inputs = workloads.generate(wl, "cpu", shapes=shapes)
     host = host_copy(inputs)
     var = dict(variant=args.variant, post_polar=args.post_polar, block=block)
-    for _ in range(Wu):
-        oracle_sample(wl, host, 0.0, max_items=1, **var)
+    items = reference_items(wl, args.post_polar)
+    whole = items == (wl.workers if wl.kind == "sign" else len(wl.shapes))
+    for _ in range(Wu):  # warm-up: one matrix (or worker) each
+        oracle_sample(wl, host, float("inf"), max_items=1, **var)
     frac, secs = 0.0, 0.0
+    t0 = time.perf_counter()
     for _ in range(K):
-        f, s, _ = oracle_sample(wl, host, 0.0, max_items=1, **var)
+        f, s, _ = oracle_sample(wl, host, float("inf"), max_items=items, **var)
         frac += f
         secs += s
+    wall = time.perf_counter() - t0
     value = frac / secs
+    if whole:
+        sample = ("whole steps: every matrix (or worker) of the workload per timed step, fp64 "
+                  "numpy momentum + Newton-Schulz + update (+ sign, vote)")
+    else:
+        sample = ("each timed step: the first %d %s of the workload (%.4f of one step), fp64 "
+                  "numpy; value = work done / time, ms_per_step = time per timed step"
+                  % (items, "workers" if wl.kind == "sign" else "matrices", frac / K))
     line = {
         "impl": "reference", "metric": metric_name(wl), "value": value, "unit": "steps/s",
-        "n_gpus": args.gpus, "steps": K, "warmup": Wu, "ms_per_step": 1000.0 / value,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "n_gpus": args.gpus, "steps": K, "warmup": Wu, "ms_per_step": 1000.0 * wall / K,
+        "higher_is_better": True, "scaling": scaling_of(wl, world), "vs_baseline": None,
         "dtype": "f64", "data": "synthetic",
-        "config": dict(config_block(wl, None, args.variant, args.post_polar),
-                       **({"blockwise": "%dx%d blocks" % block} if block else {})),
+        "config": config_block(wl, args.variant, args.post_polar, block, world),
+        "step_fraction": frac / K,
+        "warmup_sample": "one matrix (or worker) per warm-up step",
         "cpu_baseline": {"value": value, "unit": "steps/s", "cores": blas_threads(),
-                         "kind": "oracle",
-                         "sample": "each step: one matrix of the workload (cycling), fp64 numpy "
-                                   "momentum + Newton-Schulz + update; value = work fraction / time"},
+                         "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "steps/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -427,10 +576,18 @@ def reduce_max(x, device, world):
     return float(t.item())
 
 
-def job_throughput(ms_max, steps, world):
-    """Whole-job steps/s: every rank steps its own copy of the workload (weak scaling), so
-    the job completes world * steps steps in the slowest rank's time."""
-    return world * steps / (ms_max / 1000.0)
+def scaling_of(wl, world):
+    """Across ranks a Muon or Sign-Muon step splits one fixed step (strong scaling); Dion
+    runs one copy per rank (weak). One GPU: strong (nothing is split)."""
+    return "weak" if (wl.kind == "dion" and world > 1) else "strong"
+
+
+def job_throughput(ms_max, steps, world, scaling="weak"):
+    """Whole-job steps/s over the slowest rank's time: with weak scaling every rank steps
+    its own copy of the workload (world * steps steps), with strong scaling the ranks
+    together take `steps` steps."""
+    n = world * steps if scaling == "weak" else steps
+    return n / (ms_max / 1000.0)
 
 
 def metric_name(wl):
@@ -449,18 +606,44 @@ def dion_min_bytes(step):
     return tot
 
 
-def config_block(wl, step_bytes, variant="bits", post_polar=False):
+def touched_bytes(wl):
+    """Bytes of the step's matrices read and written once (M of every worker, and W)."""
+    n_m = wl.elements * (wl.workers if wl.kind == "sign" else 1)
+    return 2 * n_m * esize(wl.m_dtype) + 2 * wl.elements * esize(wl.w_dtype)
+
+
+def parallelism_of(wl, world):
+    if world == 1:
+        return "one GPU"
+    if wl.kind == "muon":
+        return ("layer-wise over %d ranks: whole matrices per rank (longest first on "
+                "Newton-Schulz flops), then an all-gather(v) of the updated weights" % world)
+    if wl.kind == "sign":
+        return ("%d workers split over %d ranks; packed signs all-gathered (int8 variant: "
+                "SUM all-reduce), vote and update on every rank" % (wl.workers, world))
+    return "replicas: each of %d ranks steps its own copy of the workload" % world
+
+
+def config_block(wl, variant="bits", post_polar=False, block=None, world=1):
+    """The workload's description, identical for the GPU arm and the oracle arm."""
     c = {"workload": wl.name, "kind": wl.kind, "matrices": len(wl.shapes),
          "elements": wl.elements, "workers": wl.workers, "ns_steps": wl.steps,
          "coeffs": list(wl.coeffs), "mu": wl.mu, "lr": wl.lr, "compute": wl.compute,
-         "parallelism": "replicas: each rank steps its own copy of the workload"}
+         "parallelism": parallelism_of(wl, world)}
+    tb = touched_bytes(wl)
+    if tb > L2_BYTES:
+        c["l2"] = "inputs larger than L2: %.0f MB of matrices touched per step vs 129 MB L2" % (tb / 1e6)
+    else:
+        c["l2"] = ("inputs smaller than L2 (%.2f MB touched per step, not flushed): the step "
+                   "is launch-latency bound" % (tb / 1e6))
     if wl.kind == "sign":
         c["aggregation"] = ("1-bit packed all-gather + local vote" if variant == "bits" else
                             "int8 SUM all-reduce + local threshold")
         c["post_vote_polar"] = bool(post_polar)
-    if step_bytes is not None:
-        c["l2"] = ("inputs larger than L2: %.0f MB of matrices touched per step vs 129 MB L2"
-                   % (step_bytes / 1e6))
+    if wl.kind == "dion":
+        c["rank"] = wl.rank
+    if block is not None:
+        c["blockwise"] = "%dx%d blocks" % tuple(block)
     return c
 
 
@@ -546,56 +729,48 @@ def sweep_hbm(dev, reps=20):
 
 # ------------------------------------------------------------------ main arm
 
-def main():
-    args = parse_args()
-    from matrix_aware_optimizers_gb300 import workloads
-    wl = workloads.workload(args.config)
-    block = None
-    if args.block:
-        block = tuple(int(v) for v in args.block.lower().split("x"))
-        if wl.kind != "muon" or len(block) != 2 or min(block) < 1:
-            sys.exit("--block ROWSxCOLS applies to the Muon workloads (--config 2, 4 or 5)")
-    if wl.kind != "sign" and (args.variant != "bits" or args.post_polar):
-        sys.exit("--variant / --post-polar apply to the Sign-Muon workloads (--config 1 or 3)")
-    if args.impl == "reference":
-        run_reference(args, wl, block)
-        return
+def _tc_launches_per_step(wl, step, block, post_polar):
+    """Tensor-core (and Dion CUDA-core) launches of one step, for the profiling capacity."""
+    if wl.kind == "dion":  # four products per round of shapes, set-up and CUDA-core kernels
+        return 4 * ((len(set(wl.shapes)) + 7) // 8) + (len(wl.shapes) + 95) // 96 + 16
+    shapes = getattr(step, "shapes_own", None) or [tuple(m.shape) for m in step.M]
+    if block is not None:
+        shapes = {(min(block[0], R - i), min(block[1], C - j)) for R, C in set(shapes)
+                  for i in range(0, R, block[0]) for j in range(0, C, block[1])}
+    return 3 * wl.steps * ((len(set(shapes)) + 7) // 8 + (1 if post_polar else 0))
 
+
+def measure(opts, wl, dev, world, rank, local, block, K, Wu, barrier, max_over_ranks):
+    """Time K steps of workload `wl` (after Wu warm-up steps) and the per-launch and
+    per-stage passes after them; returns (bench line without e2e / CPU baseline, step)."""
     import torch
-    import torch.distributed as dist
     import matrix_aware_optimizers_gb300 as mao
+    from matrix_aware_optimizers_gb300 import distributed, workloads
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dplan = None
+    seed = wl.index - 1
     if world > 1:
-        dist.init_process_group("nccl")
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
-    mao.lib()
-    if args.sweep_hbm:
-        if rank == 0:
-            sweep_hbm(dev)
-        return
-
-    K = args.steps if args.steps is not None else DEFAULT_STEPS[wl.index]
-    Wu = max(3, args.warmup if args.warmup is not None else DEFAULT_WARMUP[wl.index])
-    inputs = workloads.generate(wl, dev, seed=(wl.index - 1) + 1000 * rank)
-    step = Step(wl, inputs, dev, args.variant, args.post_polar, block, fused=not args.unfused)
+        if wl.kind == "muon" and block is None and not opts.unfused:
+            dplan = distributed.LayerwiseMuon(wl.shapes, wl.w_dtype, wl.steps)
+        elif wl.kind == "sign" and not opts.post_polar and wl.workers % world == 0:
+            dplan = distributed.SignExchange(wl.shapes[0][0], wl.shapes[0][1], wl.workers)
+        else:
+            seed += 1000 * rank  # replicas: every rank its own copy
+    scaling = "strong" if (world == 1 or dplan is not None) else "weak"
+    inputs = workloads.generate(wl, dev, seed=seed)
+    step = Step(wl, inputs, dev, opts.variant, opts.post_polar, block, fused=not opts.unfused,
+                dplan=dplan)
+    del inputs
     stream = torch.cuda.current_stream()
-
-    def barrier():
-        if world > 1:
-            dist.barrier()
-
-    def max_over_ranks(x):
-        return reduce_max(x, dev, world)
 
     for _ in range(Wu):
         step()
     mao.sync_status()
     run = step
-    if args.graph:  # one captured step, replayed (no host launch work per step)
+    per_replay = None
+    if opts.graph:  # one captured step, replayed (no host launch work per step)
+        if dplan is not None:
+            raise ValueError("--graph runs on one GPU")
         graph = torch.cuda.CUDAGraph()
         side = torch.cuda.Stream()
         side.wait_stream(stream)
@@ -610,15 +785,7 @@ def main():
         mao.sync_status()
 
     # ---------------- timed region: K whole steps, inputs resident in HBM
-    if wl.kind == "dion":  # every launch of the call: four products per round of shapes,
-        # the set-up launches and the CUDA-core kernels
-        n_tc_per_step = 4 * ((len(set(wl.shapes)) + 7) // 8) + (len(wl.shapes) + 95) // 96 + 16
-    elif block is not None:
-        bshapes = {(min(block[0], R - i), min(block[1], C - j)) for R, C in set(wl.shapes)
-                   for i in range(0, R, block[0]) for j in range(0, C, block[1])}
-        n_tc_per_step = 3 * wl.steps * ((len(bshapes) + 7) // 8)
-    else:
-        n_tc_per_step = 3 * wl.steps * ((len(set(wl.shapes)) + 7) // 8 + (1 if args.post_polar else 0))
+    n_tc_per_step = _tc_launches_per_step(wl, step, block, opts.post_polar)
     launches0 = mao.launch_count()
     clocks = ClockSampler(local)
     barrier()
@@ -633,12 +800,12 @@ def main():
     barrier()
     clk = clocks.stop()
     launches = mao.launch_count() - launches0
-    if args.graph:  # replays launch the captured kernels without host calls
+    if per_replay is not None:  # replays launch the captured kernels without host calls
         launches = per_replay * K
     mao.sync_status()
     ms_total = max_over_ranks(e0.elapsed_time(e1))
     ms_step = ms_total / K
-    value = job_throughput(ms_total, K, world)
+    value = job_throughput(ms_total, K, world, scaling)
 
     # ---------------- kernel-timing pass: the same steps with a CUDA event pair around every
     # tensor-core launch (on its stream). Kept out of the timed region above: an event
@@ -663,7 +830,7 @@ def main():
 
     # ---------------- per-stage times (separate pass, same stream)
     reps = max(3, min(K, 50))
-    if step.fused:
+    if step.whole_call:
         # one call: the Newton–Schulz share is the tensor-core launches' time from the pass
         # above (the momentum rides on the staging pass, the update on the last product)
         ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(reps)]
@@ -691,29 +858,33 @@ def main():
         st_upd = statistics.median(e[2].elapsed_time(e[3]) for e in ev)
 
     peaks, peak_src = load_peaks()
+    cfg = config_block(wl, opts.variant, opts.post_polar, block, world)
+    launch = {"launch": "CUDA graph replay" if opts.graph else "eager"}
     if wl.kind == "dion":
         line = dion_line(wl, step, K, Wu, world, value, ms_step, reps_tc, ms_prof, st_ns, tc_ms,
-                         launches, clk, peaks, peak_src, graph=args.graph, kernel_ms=kernel_ms)
-        finish_line(args, line, wl, step, K, world, rank, dev, barrier, max_over_ranks)
-        return
+                         launches, clk, peaks, peak_src, cfg, scaling, kernel_ms=kernel_ms)
+        line["step"] = launch
+        return line, step
 
     # ---------------- roofline of the dominant kernel (tensor-core NS product kernel)
-    shapes = [tuple(m.shape) for m in step.M]
+    shapes = getattr(step, "shapes_own", None) or [tuple(m.shape) for m in step.M]
     if block is not None:  # the products run on the blocks
         shapes = [(min(block[0], R - i), min(block[1], C - j)) for R, C in shapes
                   for i in range(0, R, block[0]) for j in range(0, C, block[1])]
     alg = alg_flops(shapes, wl.steps)
     dense = dense_flops(shapes, wl.steps)
     # the post-vote polar step is one more Newton–Schulz on a matrix of W's shape
-    alg_tc = alg + (alg_flops([tuple(step.W[0].shape)], wl.steps) if args.post_polar else 0)
+    alg_tc = alg + (alg_flops([tuple(step.W[0].shape)], wl.steps) if opts.post_polar else 0)
     tc_total_ms = sum(tc_ms)
+    hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
     if wl.compute == "bf16" and tc_ms:
         tflops = alg_tc * reps_tc / (tc_total_ms / 1000.0) / 1e12
-        peak = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
+        peak, peak_text = choose_peak(peaks, peak_src, ms_prof / 1000.0)
         roof = {"kernel": "ns_tc_kernel", "bound": "tensor", "achieved": tflops, "peak": peak,
                 "unit": "TFLOP/s", "frac": tflops / peak, "traffic": None,
-                "peak_source": "%s bf16_tflops_sustained (kernel inside a long step loop)" % peak_src,
-                "work": "symmetric-minimum flops m(m+1)n + m^2(m+1) + 2m^2n per iteration",
+                "peak_source": peak_text,
+                "work": "symmetric-minimum flops m(m+1)n + m^2(m+1) + 2m^2n per iteration"
+                        + (" (this rank's matrices)" if dplan is not None else ""),
                 "launches": len(tc_ms), "avg_launch_ms": tc_total_ms / len(tc_ms),
                 "stage_avg_ms": {name: statistics.mean(tc_ms[i::3]) for i, name in
                                  enumerate(("gram", "poly", "apply"))},
@@ -721,37 +892,35 @@ def main():
                 "timing": "per-launch CUDA events over %d further steps after the timed region"
                           % reps_tc}
         traffic = read_traffic(wl)
-        if traffic is not None:
+        if traffic is not None and dplan is None:
             roof["traffic"] = traffic
     else:
-        hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
         mom_b, upd_b = stage_bytes(wl, step)
         gbs = (mom_b + (upd_b or 0)) / ((st_mom + (st_upd if upd_b else 0)) / 1000.0) / 1e9
         roof = {"kernel": "elementwise stages", "bound": "hbm", "achieved": gbs, "peak": hbm,
                 "unit": "GB/s", "frac": gbs / hbm, "traffic": None,
                 "peak_source": "%s hbm_gbs" % peak_src}
-    hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
-    touched = sum(m.numel() * esize(m.dtype) for m in step.M) * 2 + \
-        sum(w.numel() * esize(w.dtype) for w in step.W) * 2
-    if step.fused:
-        stages = {"muon_step": st_step, "ns_tc_launches": st_ns}
+    if step.whole_call:
+        stages = {"whole_step": st_step, "ns_tc_launches": st_ns}
         ew_gbs = {"momentum": None, "update": None, "peak": hbm,
-                  "fused": "momentum in the staging pass, update in the last product"}
+                  "fused": "momentum in the staging pass, update in the last product"
+                  if step.fused else "one call per stage and the exchange; no per-stage split"}
     else:
         mom_b, upd_b = stage_bytes(wl, step)
         stages = {"momentum": st_mom, "ns": st_ns, "update": st_upd}
         ew_gbs = {"momentum": mom_b / (st_mom / 1000.0) / 1e9,
                   "update": upd_b / (st_upd / 1000.0) / 1e9 if upd_b else None, "peak": hbm}
-
+    if step.fused:
+        launch["call"] = "muon_step (momentum, Newton-Schulz and update in one call)"
+    if dplan is not None:
+        launch["exchange"] = ("all-gather(v) of updated weights" if wl.kind == "muon" else
+                              "all-gather of packed signs" if opts.variant == "bits" else
+                              "int8 SUM all-reduce")
     line = {
         "metric": metric_name(wl), "value": value, "unit": "steps/s", "n_gpus": world,
         "steps": K, "warmup": Wu, "ms_per_step": ms_step, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": wl.compute, "data": "synthetic",
-        "config": dict(config_block(wl, touched, args.variant, args.post_polar),
-                       launch="CUDA graph replay" if args.graph else "eager",
-                       **({"step_call": "muon_step (momentum, Newton-Schulz and update in one "
-                                        "call)"} if step.fused else {}),
-                       **({"blockwise": "%dx%d blocks" % block} if block else {})),
+        "scaling": scaling, "vs_baseline": None, "dtype": wl.compute, "data": "synthetic",
+        "config": cfg, "step": launch,
         "ns_tflops_dense": dense / (st_ns / 1000.0) / 1e12,
         "ns_tflops_alg": alg / (st_ns / 1000.0) / 1e12,
         "stages_ms": stages,
@@ -760,12 +929,99 @@ def main():
         "gpu_launches": launches,
         "clocks": clk,
     }
+    return line, step
 
-    finish_line(args, line, wl, step, K, world, rank, dev, barrier, max_over_ranks)
+
+def per_config_runs(args, dev, local, barrier, max_over_ranks):
+    """The other workloads, each measured alone on this GPU (no e2e or CPU baseline)."""
+    import torch
+    from matrix_aware_optimizers_gb300 import workloads
+    out = {}
+    opts = parse_args([])  # defaults: 1-bit aggregation, eager, the one-call Muon step
+    for c, (K, Wu) in PER_CONFIG.items():
+        wl = workloads.workload(c)
+        try:
+            line, step = measure(opts, wl, dev, 1, 0, local, None, K, Wu, barrier, max_over_ranks)
+        except Exception as e:  # report, keep the default line
+            out[str(c)] = {"workload": wl.name, "error": "%s: %s" % (type(e).__name__, e)}
+            continue
+        finally:
+            gc.collect()
+            torch.cuda.empty_cache()
+        r = line["roofline"]
+        out[str(c)] = {
+            "workload": wl.name, "metric": line["metric"], "value": line["value"],
+            "unit": "steps/s", "steps": K, "warmup": Wu, "ms_per_step": line["ms_per_step"],
+            "ns_tflops_alg": line["ns_tflops_alg"], "ns_tflops_dense": line["ns_tflops_dense"],
+            "roofline": {k: r.get(k) for k in ("kernel", "bound", "achieved", "peak", "unit",
+                                               "frac", "peak_source", "avg_launch_ms")},
+            "stages_ms": line["stages_ms"], "gpu_launches": line["gpu_launches"],
+            "clocks": line["clocks"], "parity": PARITY_TESTS[c],
+        }
+        del step, line
+        gc.collect()
+        torch.cuda.empty_cache()
+    return out
+
+
+def main():
+    args = parse_args()
+    from matrix_aware_optimizers_gb300 import workloads
+    wl = workloads.workload(args.config)
+    block = None
+    if args.block:
+        block = tuple(int(v) for v in args.block.lower().split("x"))
+        if wl.kind != "muon" or len(block) != 2 or min(block) < 1:
+            sys.exit("--block ROWSxCOLS applies to the Muon workloads (--config 2, 4 or 5)")
+    if wl.kind != "sign" and (args.variant != "bits" or args.post_polar):
+        sys.exit("--variant / --post-polar apply to the Sign-Muon workloads (--config 1 or 3)")
+    if args.impl == "reference":
+        run_reference(args, wl, block)
+        return
+
+    import torch
+    import torch.distributed as dist
+    import matrix_aware_optimizers_gb300 as mao
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    mao.lib()
+    if args.sweep_hbm:
+        if rank == 0:
+            sweep_hbm(dev)
+        return
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    def max_over_ranks(x):
+        return reduce_max(x, dev, world)
+
+    K = args.steps if args.steps is not None else DEFAULT_STEPS[wl.index]
+    Wu = max(3, args.warmup if args.warmup is not None else DEFAULT_WARMUP[wl.index])
+    line, step = measure(args, wl, dev, world, rank, local, block, K, Wu, barrier,
+                         max_over_ranks)
+    line = finish_line(args, line, wl, step, K, world, rank, dev, barrier, max_over_ranks)
+    default_run = args.config == 2 and block is None and not args.graph and not args.unfused
+    if world == 1 and default_run and not args.no_per_config:
+        del step
+        gc.collect()
+        torch.cuda.empty_cache()
+        line["per_config"] = per_config_runs(args, dev, local, barrier, max_over_ranks)
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
 
 
 def dion_line(wl, step, K, Wu, world, value, ms_step, reps_tc, ms_prof, st_step, tc_ms, launches,
-              clk, peaks, peak_src, graph=False, kernel_ms=None):
+              clk, peaks, peak_src, cfg, scaling, kernel_ms=None):
     """Bench line of a Dion workload: the step is HBM-bound (every matrix element is read and
     written a fixed number of times, 8 m n r flops against about 10 bytes per element)."""
     hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
@@ -780,27 +1036,25 @@ def dion_line(wl, step, K, Wu, world, value, ms_step, reps_tc, ms_prof, st_step,
             "tc_launches": len(tc_ms),
             "tc_share_of_step": tc_total / ms_prof if tc_ms else None,
             "tc_tflops": flops * reps_tc / (tc_total / 1000.0) / 1e12 if tc_ms else None}
-    touched = sum(m.numel() * esize(m.dtype) for m in step.M) * 2 + \
-        sum(w.numel() * esize(w.dtype) for w in step.W) * 2
-    c = config_block(wl, touched)
-    c["rank"] = wl.rank
-    c["launch"] = "CUDA graph replay" if graph else "eager"
     return {
         "metric": metric_name(wl), "value": value, "unit": "steps/s", "n_gpus": world,
         "steps": K, "warmup": Wu, "ms_per_step": ms_step, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": wl.compute, "data": "synthetic",
-        "config": c, "stages_ms": {"dion_step": st_step}, "roofline": roof,
+        "scaling": scaling, "vs_baseline": None, "dtype": wl.compute, "data": "synthetic",
+        "config": cfg, "stages_ms": {"dion_step": st_step}, "roofline": roof,
         "kernels_ms_per_step": {k: round(v, 4) for k, v in (kernel_ms or {}).items()},
         "gpu_launches": launches, "clocks": clk,
     }
 
 
 def finish_line(args, line, wl, step, K, world, rank, dev, barrier, max_over_ranks):
-    import torch.distributed as dist
+    """Adds the end-to-end leg and (one GPU, rank 0) the oracle's CPU baseline to `line`."""
     from matrix_aware_optimizers_gb300 import workloads
     # ---------------- end to end: host gradients in, host weights out, every step
     if not args.no_e2e:
-        line["e2e"] = run_e2e(step, K, world, dev, barrier, max_over_ranks)
+        if step.dplan is not None:
+            line["e2e"] = run_e2e_dist(step, K, dev, barrier, max_over_ranks)
+        else:
+            line["e2e"] = run_e2e(step, K, world, dev, barrier, max_over_ranks, line["scaling"])
 
     # ---------------- CPU baseline: the oracle on a bounded sample (rank 0, N = 1)
     if world == 1 and rank == 0 and not args.no_cpu_baseline:
@@ -811,10 +1065,7 @@ def finish_line(args, line, wl, step, K, world, rank, dev, barrier, max_over_ran
                                          post_polar=args.post_polar, block=step.block)
         line["cpu_baseline"] = {"value": frac / secs, "unit": "steps/s", "cores": blas_threads(),
                                 "kind": "oracle", "sample": desc + ", %.1f s" % secs}
-    if rank == 0:
-        print(json.dumps(line))
-    if world > 1:
-        dist.destroy_process_group()
+    return line
 
 
 def _slab(tensors, device, pin=False):
@@ -835,7 +1086,7 @@ def _slab(tensors, device, pin=False):
     return buf, views
 
 
-def run_e2e(step, K, world, dev, barrier, max_over_ranks):
+def run_e2e(step, K, world, dev, barrier, max_over_ranks, scaling="strong"):
     """The same step with host data: every step copies its gradients from pinned host memory
     (one copy of one contiguous slab) and reads the updated weights back (one copy).
 
@@ -916,12 +1167,49 @@ def run_e2e(step, K, world, dev, barrier, max_over_ranks):
     step.G, step.W = G_orig, W_orig
     for w, v in zip(W_orig, last_views):
         w.copy_(v)
-    return {"value": job_throughput(ms, K, world), "unit": "steps/s", "h2d_bytes_per_step": h2d,
+    return {"value": job_throughput(ms, K, world, scaling), "unit": "steps/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": K,
             "copies": "one pinned H2D slab and one D2H slab per step, on copy streams overlapping "
                       "the neighbouring steps' compute" +
                       ("; two device weight slabs, read one, write the other (%s)"
                        % ("dion_step's X_out" if dion else "muon_step's W_out") if fused else "")}
+
+
+def run_e2e_dist(step, K, dev, barrier, max_over_ranks):
+    """End to end across ranks: every step, each rank copies its share of the gradients in
+    from pinned host memory (the matrices it owns, or its workers' gradients) and reads its
+    result back (the weights it updated; Sign-Muon: the new W), around the step and its
+    exchange. Copies and compute run in order on the step's stream."""
+    import torch
+    main = torch.cuda.current_stream()
+    G_host, _ = _slab([g.cpu() for g in step.G], "cpu", pin=True)
+    G_dev, G_views = _slab(step.G, dev)
+    G_orig = step.G
+    step.G = G_views
+    if step.wl.kind == "muon":
+        out_dev = step.dplan.layout.segment(step.flat, step.dplan.rank)
+    else:
+        out_dev = step.W[0].view(-1)
+    out_host = torch.empty(out_dev.shape, dtype=out_dev.dtype).pin_memory()
+    barrier()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(main)
+    for _ in range(K):
+        G_dev.copy_(G_host, non_blocking=True)
+        step()
+        out_host.copy_(out_dev, non_blocking=True)
+    e1.record(main)
+    torch.cuda.synchronize()
+    barrier()
+    ms = max_over_ranks(e0.elapsed_time(e1))
+    step.G = G_orig
+    return {"value": job_throughput(ms, K, step.dplan.world, "strong"), "unit": "steps/s",
+            "h2d_bytes_per_step": G_host.numel() * G_host.element_size(),
+            "d2h_bytes_per_step": out_host.numel() * out_host.element_size(), "steps": K,
+            "copies": "rank 0's figures: its gradient slab in, its updated weights out, in "
+                      "stream order with the step"}
 
 
 def read_traffic(wl):

@@ -39,3 +39,33 @@ def test_reference_arm_variants_and_dion():
     assert d["config"]["aggregation"].startswith("int8") and d["config"]["post_vote_polar"]
     d = _run("--impl", "reference", "--config", "6", "--steps", "1", "--warmup", "1")
     assert d["metric"].startswith("Dion") and d["value"] > 0
+
+
+def test_peak_choice_by_timing_window():
+    import bench
+    peaks = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+    p, src = bench.choose_peak(peaks, "measured", 0.05)
+    assert p == 1900.0 and "burst" in src
+    p, src = bench.choose_peak(peaks, "measured", 4.0)
+    assert p == 1700.0 and "sustained" in src
+
+
+def test_reference_covers_whole_steps_where_affordable():
+    import bench
+    from matrix_aware_optimizers_gb300 import workloads
+    assert bench.reference_items(workloads.workload(1)) == 4      # every worker
+    assert bench.reference_items(workloads.workload(2)) == 48     # every matrix
+    assert bench.reference_items(workloads.workload(3)) == 1      # one 4096^2 worker
+    assert bench.reference_items(workloads.workload(4)) == 1
+    assert 1 < bench.reference_items(workloads.workload(5)) < 385
+
+
+def test_both_arms_describe_the_same_config():
+    # the GPU arm and the oracle arm build the config from the workload and the flags only
+    import bench
+    from matrix_aware_optimizers_gb300 import workloads
+    wl = workloads.workload(2)
+    d = _run("--impl", "reference", "--config", "2", "--steps", "1", "--warmup", "1")
+    assert d["config"] == json.loads(json.dumps(bench.config_block(wl, "bits", False, None, 1)))
+    assert d["step_fraction"] == 1.0
+    assert abs(d["value"] * d["ms_per_step"] / 1000.0 - 1.0) < 0.05
