@@ -17,6 +17,7 @@
 
 #include "common.cuh"
 #include "ns_plan.h"
+#include "ns_small.h"
 
 namespace mao {
 
@@ -661,6 +662,27 @@ mao_status ns_run(const mao_mat* in, const mao_mat* out, int32_t batch, int32_t 
   const bool tcpath = compute == MAO_BF16;
   const int32_t ws_dt = tcpath ? MAO_BF16 : MAO_F32;
   if (fuse && (!tcpath || sign_bits)) return MAO_ERR_UNSUPPORTED;
+  // small fp32 matrices: the whole call in one launch, one cluster per matrix. The choice
+  // is made per matrix, so a matrix's result does not depend on the rest of the batch.
+  if (!fuse && compute == MAO_F32) {
+    std::vector<mao_mat> in_s, out_s, in_r, out_r;
+    std::vector<uint32_t*> bits_s, bits_r;
+    for (int b = 0; b < batch; ++b) {
+      const bool small = ns_small_eligible(&in[b], &out[b], 1, steps, compute);
+      (small ? in_s : in_r).push_back(in[b]);
+      (small ? out_s : out_r).push_back(out[b]);
+      (small ? bits_s : bits_r).push_back(sign_bits ? sign_bits[b] : nullptr);
+    }
+    if (!in_s.empty()) {
+      const mao_status st =
+          ns_small_run(in_s.data(), out_s.data(), int32_t(in_s.size()), steps, coeffs,
+                       coeff_stride, eps, sign_bits ? bits_s.data() : nullptr, stream);
+      if (st != MAO_OK || in_r.empty()) return st;
+      return ns_run(in_r.data(), out_r.data(), int32_t(in_r.size()), steps, coeffs, coeff_stride,
+                    eps, compute, sign_bits ? bits_r.data() : nullptr, workspace,
+                    workspace_bytes, stream, nullptr);
+    }
+  }
 
   // ---- output entries; sign buffers filled by atomics start from zero
   std::vector<OutEntry> entries(batch);

@@ -1,0 +1,350 @@
+// Newton–Schulz of small matrices on the fp32 accuracy path, the whole iteration in one
+// launch.
+//
+// For a matrix whose working set (X twice, A, and this CTA's rows of B) fits in one SM's
+// shared memory, the per-product launches of the general path cost more than the
+// arithmetic. Here a cluster of eight CTAs owns one matrix for the whole call: every CTA
+// holds all of X and A in shared memory and computes one eighth of the rows of each
+// product ("分散ニュートン・シュルツ" of the Megatron Muon article: three products per
+// iteration; the iteration of the Sign-Muon summary, §2 "Mecanismo Central" item 1):
+//   A  = s^2 X X^T            rows of this CTA, then the other CTAs' rows copied in
+//   B' = a I + b A + c A A    rows of this CTA (local)
+//   X' = s B' X               rows of this CTA into the other X buffer, then the others'
+// with s = 1/(||X||_F + eps) in the first iteration and 1 afterwards (the same placement
+// of the normalisation as the general path). After a cluster barrier each CTA copies the
+// rows the other CTAs computed with 16-byte distributed shared-memory loads. A CTA writes
+// its A rows again only after the next barrier, when every copy of them is done, and the
+// X buffers alternate, so two barriers per iteration order every access; one more after
+// the last copy keeps every CTA resident until no other CTA reads its shared memory. Every
+// CTA computes the Frobenius norm itself from its full copy in the same fixed order, so
+// all eight hold the same s. At the end each CTA writes one eighth of
+// U (in the matrix's own orientation) and of the packed signs, whole words, so the sign
+// buffer needs no clearing. All arithmetic is fp32 FFMA with one accumulation chain per
+// output, in k order.
+#include <algorithm>
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+#include "ns_small.h"
+
+namespace mao {
+namespace {
+
+constexpr int kCluster = 8;
+constexpr int kThreads = 256;
+
+struct SmallEntry {
+  const void* src;
+  void* out;        // U (may be null)
+  uint32_t* bits;   // packed signs (may be null)
+  int64_t src_ld, out_ld;
+  int32_t R, C, src_dt, out_dt;
+};
+
+struct SmallParams {
+  SmallEntry e[kSmallMaxPerLaunch];
+  float co[3 * 64];  // (a, b, c) of every iteration
+  int32_t steps;
+  float eps;
+};
+
+struct Layout {
+  int m, n, nx, ma, rpc;
+};
+
+__host__ __device__ inline Layout layout_of(int R, int C) {
+  Layout l;
+  l.m = R < C ? R : C;
+  l.n = R < C ? C : R;
+  l.nx = ((l.n + 3) & ~3) + 4;  // X row stride (floats): 16-byte rows, conflict-free columns
+  l.ma = ((l.m + 3) & ~3) + 4;  // A and B' row stride
+  l.rpc = (l.m + kCluster - 1) / kCluster;
+  return l;
+}
+
+__host__ __device__ inline size_t smem_floats(const Layout& l) {
+  // X ping-pong, A, this CTA's rows of B', then 256 doubles for the norm's reduction
+  return size_t(2) * l.m * l.nx + size_t(l.m) * l.ma + size_t(l.rpc) * l.ma + 2 * kThreads;
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ void cluster_barrier() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint32_t remote(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+
+// Copies the rows of buf that the other CTAs of the cluster own (rows [q*rpc, q*rpc + rpc)
+// of CTA q, `quads` 16-byte units per row of stride ld floats) from their shared memory
+// into this CTA's copy, with 16-byte distributed shared-memory loads.
+__device__ __forceinline__ void pull_rows(float* buf, int ld, int quads, int m, int rpc,
+                                          uint32_t self, int tid) {
+  const int mine0 = min(m, int(self) * rpc), mine1 = min(m, mine0 + rpc);
+  const int others = m - (mine1 - mine0);
+  for (int t = tid; t < others * quads; t += kThreads) {
+    int row = t / quads;
+    const int q4 = t - row * quads;
+    if (row >= mine0) row += mine1 - mine0;  // skip this CTA's own rows
+    float* dst = buf + size_t(row) * ld + 4 * q4;
+    const uint32_t src = remote(smem_addr(dst), uint32_t(row / rpc));
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(src)
+                 : "memory");
+    *reinterpret_cast<float4*>(dst) = v;
+  }
+}
+
+// acc0 = sum_k P[i0][k] Q[j][k], acc1 = sum_k P[i1][k] Q[j][k] over kq quads (rows of
+// stride ld floats, zero-padded to whole quads).
+__device__ __forceinline__ void dot2(const float* P0, const float* P1, const float* Qj, int kq,
+                                     float& acc0, float& acc1) {
+  const float4* a = reinterpret_cast<const float4*>(P0);
+  const float4* b = reinterpret_cast<const float4*>(P1);
+  const float4* q = reinterpret_cast<const float4*>(Qj);
+  float s0 = 0.0f, s1 = 0.0f;
+#pragma unroll 4
+  for (int k = 0; k < kq; ++k) {
+    const float4 x = q[k], u = a[k], v = b[k];
+    s0 = __fmaf_rn(u.x, x.x, s0);
+    s0 = __fmaf_rn(u.y, x.y, s0);
+    s0 = __fmaf_rn(u.z, x.z, s0);
+    s0 = __fmaf_rn(u.w, x.w, s0);
+    s1 = __fmaf_rn(v.x, x.x, s1);
+    s1 = __fmaf_rn(v.y, x.y, s1);
+    s1 = __fmaf_rn(v.z, x.z, s1);
+    s1 = __fmaf_rn(v.w, x.w, s1);
+  }
+  acc0 = s0;
+  acc1 = s1;
+}
+
+__global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
+    ns_small_kernel(const __grid_constant__ SmallParams p) {
+  extern __shared__ float4 smem_f4[];
+  float* sm = reinterpret_cast<float*>(smem_f4);
+  const SmallEntry& e = p.e[blockIdx.x / kCluster];
+  const uint32_t crank = cluster_rank();
+  const int tid = threadIdx.x;
+  const bool tall = e.R > e.C;
+  const Layout L = layout_of(e.R, e.C);
+  const int m = L.m, n = L.n, nx = L.nx, ma = L.ma;
+  const int r0 = min(m, int(crank) * L.rpc), r1 = min(m, r0 + L.rpc);  // this CTA's rows
+  float* Xb[2] = {sm, sm + size_t(m) * nx};
+  float* A = sm + size_t(2) * m * nx;
+  float* Bm = A + size_t(m) * ma;
+  double* red = reinterpret_cast<double*>(Bm + size_t(L.rpc) * ma);
+
+  // ---- the matrix into X[0] (X = M, or M^T for a tall M), zero-padded rows, and the sum of
+  // squares in a fixed order (the same in every CTA of the cluster)
+  double ss = 0.0;
+  if (!tall) {
+    for (int idx = tid; idx < m * nx; idx += kThreads) {
+      const int i = idx / nx, k = idx - i * nx;
+      const float v = k < n ? load_elem(e.src, int64_t(i) * e.src_ld + k, e.src_dt) : 0.0f;
+      Xb[0][idx] = v;
+      ss += double(v) * double(v);
+    }
+  } else {
+    for (int idx = tid; idx < n * e.C; idx += kThreads) {  // source row-major: M[k][i]
+      const int k = idx / e.C, i = idx - k * e.C;
+      const float v = load_elem(e.src, int64_t(k) * e.src_ld + i, e.src_dt);
+      Xb[0][size_t(i) * nx + k] = v;
+      ss += double(v) * double(v);
+    }
+    for (int idx = tid; idx < m * (nx - n); idx += kThreads) {
+      const int i = idx / (nx - n), k = n + idx - i * (nx - n);
+      Xb[0][size_t(i) * nx + k] = 0.0f;
+    }
+  }
+  for (int idx = tid; idx < m * (ma - m); idx += kThreads) {  // A's padding columns stay 0
+    const int i = idx / (ma - m), k = m + idx - i * (ma - m);
+    A[size_t(i) * ma + k] = 0.0f;
+  }
+  red[tid] = ss;
+  __syncthreads();
+  for (int w = kThreads / 2; w > 0; w >>= 1) {
+    if (tid < w) red[tid] += red[tid + w];
+    __syncthreads();
+  }
+  const float s = float(1.0 / (sqrt(red[0]) + double(p.eps)));
+  // every CTA of the cluster is running before any distributed shared-memory access
+  cluster_barrier();
+
+  const int xq = (n + 3) / 4, aq = (m + 3) / 4;
+  const int pairs = (r1 - r0 + 1) / 2;
+  for (int it = 0; it < p.steps; ++it) {
+    const float ca = p.co[3 * it], cb = p.co[3 * it + 1], cc = p.co[3 * it + 2];
+    const float* X = Xb[it & 1];
+    float* Xn = Xb[(it + 1) & 1];
+    const float s2 = it == 0 ? s * s : 1.0f;
+    const float s1 = it == 0 ? s : 1.0f;
+    // A = s^2 X X^T: rows i0, i0 + 1 of this CTA against row j; then the other rows
+    for (int t = tid; t < pairs * m; t += kThreads) {
+      const int j = t % m, i0 = r0 + 2 * (t / m), i1 = min(i0 + 1, r1 - 1);
+      float v0, v1;
+      dot2(X + size_t(i0) * nx, X + size_t(i1) * nx, X + size_t(j) * nx, xq, v0, v1);
+      A[size_t(i0) * ma + j] = s2 * v0;
+      if (i0 + 1 < r1) A[size_t(i1) * ma + j] = s2 * v1;
+    }
+    cluster_barrier();
+    pull_rows(A, ma, aq, m, L.rpc, crank, tid);
+    __syncthreads();
+    // B' = a I + b A + c A A (A A = A A^T): this CTA's rows, local
+    for (int t = tid; t < pairs * m; t += kThreads) {
+      const int j = t % m, i0 = r0 + 2 * (t / m), i1 = min(i0 + 1, r1 - 1);
+      float v0, v1;
+      dot2(A + size_t(i0) * ma, A + size_t(i1) * ma, A + size_t(j) * ma, aq, v0, v1);
+      Bm[size_t(i0 - r0) * ma + j] =
+          __fmaf_rn(cc, v0, cb * A[size_t(i0) * ma + j]) + (i0 == j ? ca : 0.0f);
+      if (i0 + 1 < r1)
+        Bm[size_t(i1 - r0) * ma + j] =
+            __fmaf_rn(cc, v1, cb * A[size_t(i1) * ma + j]) + (i1 == j ? ca : 0.0f);
+    }
+    __syncthreads();
+    // X' = s B' X: row i, columns 4q .. 4q + 3 (zeros past n); then the other rows
+    for (int t = tid; t < (r1 - r0) * xq; t += kThreads) {
+      const int il = t / xq, q = t - il * xq;
+      const float* brow = Bm + size_t(il) * ma;
+      float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+#pragma unroll 4
+      for (int k = 0; k < m; ++k) {
+        const float bv = brow[k];
+        const float4 xv = reinterpret_cast<const float4*>(X + size_t(k) * nx)[q];
+        acc.x = __fmaf_rn(bv, xv.x, acc.x);
+        acc.y = __fmaf_rn(bv, xv.y, acc.y);
+        acc.z = __fmaf_rn(bv, xv.z, acc.z);
+        acc.w = __fmaf_rn(bv, xv.w, acc.w);
+      }
+      const int j = 4 * q;
+      *reinterpret_cast<float4*>(Xn + size_t(r0 + il) * nx + j) =
+          make_float4(s1 * acc.x, j + 1 < n ? s1 * acc.y : 0.0f, j + 2 < n ? s1 * acc.z : 0.0f,
+                      j + 3 < n ? s1 * acc.w : 0.0f);
+    }
+    cluster_barrier();
+    pull_rows(Xn, nx, xq, m, L.rpc, crank, tid);
+    __syncthreads();
+  }
+
+  // no CTA leaves (or reuses its buffers) while another may still copy rows from it
+  cluster_barrier();
+
+  // ---- outputs from the final X (complete in every CTA): one eighth each
+  const float* Xf = Xb[p.steps & 1];
+  const int N = e.R * e.C;  // below 2^31: the working set fits one SM
+  auto value = [&](int k) {  // entry k of U in its own row-major orientation
+    const int r = k / e.C, c = k - r * e.C;
+    return tall ? Xf[size_t(c) * nx + r] : Xf[size_t(r) * nx + c];
+  };
+  if (e.out) {
+    const int per = (N + kCluster - 1) / kCluster;
+    const int k0 = int(crank) * per, k1 = min(N, k0 + per);
+    for (int k = k0 + tid; k < k1; k += kThreads) {
+      const int r = k / e.C, c = k - r * e.C;
+      store_elem(e.out, int64_t(r) * e.out_ld + c, e.out_dt, value(k));
+    }
+  }
+  if (e.bits) {
+    const int W = (N + 31) / 32;
+    const int per = (W + kCluster - 1) / kCluster;
+    const int w0 = int(crank) * per, w1 = min(W, w0 + per);
+    for (int w = w0 + tid; w < w1; w += kThreads) {
+      uint32_t word = 0;
+      int r = (32 * w) / e.C, c = 32 * w - r * e.C;
+      for (int b = 0; b < 32 && 32 * w + b < N; ++b) {
+        const float v = tall ? Xf[size_t(c) * nx + r] : Xf[size_t(r) * nx + c];
+        if (!(v < 0.0f)) word |= 1u << b;
+        if (++c == e.C) {
+          c = 0;
+          ++r;
+        }
+      }
+      e.bits[w] = word;
+    }
+  }
+}
+
+}  // namespace
+
+size_t ns_small_smem_bytes(int64_t R, int64_t C) {
+  if (R < 1 || C < 1 || R > 4096 || C > 4096) return ~size_t(0);
+  return smem_floats(layout_of(int(R), int(C))) * sizeof(float);
+}
+
+bool ns_small_eligible(const mao_mat* in, const mao_mat* out, int32_t batch, int32_t steps,
+                       int32_t compute) {
+  if (compute != MAO_F32 || steps < 1 || steps > 64) return false;
+  for (int b = 0; b < batch; ++b) {
+    if (in[b].dtype != MAO_F32 && in[b].dtype != MAO_BF16) return false;
+    if (ns_small_smem_bytes(in[b].rows, in[b].cols) > kSmallSmemMax) return false;
+    if (out[b].data && out[b].dtype != MAO_F32 && out[b].dtype != MAO_BF16) return false;
+  }
+  return true;
+}
+
+mao_status ns_small_run(const mao_mat* in, const mao_mat* out, int32_t batch, int32_t steps,
+                        const float* coeffs, int32_t coeff_stride, float eps,
+                        uint32_t* const* sign_bits, cudaStream_t stream) {
+  static std::once_flag attr_once[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MAO_ERR_CUDA;
+  cudaError_t attr_err = cudaSuccess;
+  std::call_once(attr_once[dev & 63], [&] {
+    attr_err = cudaFuncSetAttribute(ns_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    int(kSmallSmemMax));
+  });
+  if (attr_err != cudaSuccess) return MAO_ERR_CUDA;
+  for (int b0 = 0; b0 < batch; b0 += kSmallMaxPerLaunch) {
+    const int nb = std::min(batch - b0, kSmallMaxPerLaunch);
+    SmallParams p;
+    memset(&p, 0, sizeof(p));
+    p.steps = steps;
+    p.eps = eps;
+    for (int it = 0; it < steps; ++it)
+      for (int q = 0; q < 3; ++q) p.co[3 * it + q] = coeffs[(coeff_stride ? 3 * it : 0) + q];
+    size_t smem = 0;
+    for (int k = 0; k < nb; ++k) {
+      const mao_mat& x = in[b0 + k];
+      SmallEntry& e = p.e[k];
+      e.src = x.data;
+      e.src_ld = x.ld;
+      e.src_dt = x.dtype;
+      e.out = out[b0 + k].data;
+      e.out_ld = out[b0 + k].ld;
+      e.out_dt = out[b0 + k].dtype;
+      e.bits = sign_bits ? sign_bits[b0 + k] : nullptr;
+      e.R = int32_t(x.rows);
+      e.C = int32_t(x.cols);
+      smem = std::max(smem, ns_small_smem_bytes(x.rows, x.cols));
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(kCluster * nb));
+    cfg.blockDim = dim3(unsigned(kThreads));
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    const cudaError_t err = cudaLaunchKernelEx(&cfg, ns_small_kernel, p);
+    count_launch();
+    if (err != cudaSuccess) return MAO_ERR_CUDA;
+    const mao_status st = cuda_status(cudaGetLastError());
+    if (st != MAO_OK) return st;
+  }
+  return MAO_OK;
+}
+
+}  // namespace mao
