@@ -120,6 +120,15 @@ def choose_peak(peaks, src, window_s):
             % (src, window_s, SUSTAINED_WINDOW_S))
 
 
+def fp32_peak_tflops(dev):
+    """fp32 FFMA peak of the device: SMs x 128 lanes x 2 flops x the maximum SM clock."""
+    import torch
+    props = torch.cuda.get_device_properties(dev)
+    peaks, _ = load_peaks()
+    mhz = peaks.get("sm_max_mhz", 2070.0)
+    return props.multi_processor_count * 128 * 2 * mhz * 1e6 / 1e12
+
+
 # ------------------------------------------------------------------ work model
 
 def alg_flops(shapes, steps):
@@ -221,6 +230,9 @@ class Step:
         self.variant, self.post_polar = variant, post_polar
         self.block = block
         self.fused = fused and wl.kind == "muon" and block is None and wl.compute == "bf16"
+        # Sign-Muon, 1-bit variant: the four stages as one sign_muon_step call
+        self.fused_sign = fused and wl.kind == "sign" and variant == "bits" and not post_polar \
+            and dplan is None
         self.W, self.M, self.G = inputs["W"], inputs["M"], inputs["G"]
         self.dev = device
         self.dplan = dplan
@@ -380,7 +392,7 @@ class Step:
     @property
     def whole_call(self):
         """The step is one call (or one call and its exchange): no per-stage timing."""
-        return self.fused or self.dplan is not None
+        return self.fused or self.fused_sign or self.dplan is not None
 
     def __call__(self):
         if self.dplan is not None:
@@ -388,6 +400,11 @@ class Step:
             return
         if self.fused:
             self.fused_call()
+            return
+        if self.fused_sign:
+            wl = self.wl
+            self.mao.sign_muon_step(self.W[0], self.M, self.G, self.words, self.vote, wl.mu,
+                                    wl.lr, wl.steps, wl.coeffs, wl.eps, wl.compute, ws=self.ws)
             return
         self.momentum()
         self.ns()
@@ -841,7 +858,8 @@ def measure(opts, wl, dev, world, rank, local, block, K, Wu, barrier, max_over_r
         torch.cuda.synchronize()
         st_step = statistics.median(e[0].elapsed_time(e[1]) for e in ev)
         st_mom = st_upd = None
-        st_ns = sum(tc_ms) / reps_tc
+        # the Newton–Schulz share: the tensor-core launches, or the one-launch fp32 kernel
+        st_ns = sum(tc_ms) / reps_tc if tc_ms else kernel_ms.get("ns_small", st_step)
     else:
         ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(reps)]
         for r in range(reps):
@@ -894,6 +912,18 @@ def measure(opts, wl, dev, world, rank, local, block, K, Wu, barrier, max_over_r
         traffic = read_traffic(wl)
         if traffic is not None and dplan is None:
             roof["traffic"] = traffic
+    elif wl.compute == "f32" and kernel_ms.get("ns_small"):
+        # the one-launch fp32 Newton–Schulz: FFMA work against the fp32 CUDA-core peak
+        small_ms = kernel_ms["ns_small"]  # per step
+        gflop = dense_flops(shapes, wl.steps) / (small_ms / 1000.0) / 1e12
+        peak = fp32_peak_tflops(dev)
+        roof = {"kernel": "ns_small_kernel", "bound": "alu", "achieved": gflop, "peak": peak,
+                "unit": "TFLOP/s", "frac": gflop / peak, "traffic": None,
+                "peak_source": "derived: SMs x 128 fp32 FMA lanes x 2 flops x max SM clock",
+                "work": "dense flops 4m^2n + 2m^3 per iteration", "avg_launch_ms": small_ms,
+                "launches": int(round(len([1 for _, t in tagged if t == "ns_small"]) / reps_tc)),
+                "note": "one cluster of 8 CTAs per matrix: a latency-bound launch on %d of the "
+                        "GPU's SMs" % (8 * len(shapes))}
     else:
         mom_b, upd_b = stage_bytes(wl, step)
         gbs = (mom_b + (upd_b or 0)) / ((st_mom + (st_upd if upd_b else 0)) / 1000.0) / 1e9
@@ -904,7 +934,9 @@ def measure(opts, wl, dev, world, rank, local, block, K, Wu, barrier, max_over_r
         stages = {"whole_step": st_step, "ns_tc_launches": st_ns}
         ew_gbs = {"momentum": None, "update": None, "peak": hbm,
                   "fused": "momentum in the staging pass, update in the last product"
-                  if step.fused else "one call per stage and the exchange; no per-stage split"}
+                  if step.fused else "one call for the whole step; no per-stage split"
+                  if step.fused_sign else
+                  "one call per stage and the exchange; no per-stage split"}
     else:
         mom_b, upd_b = stage_bytes(wl, step)
         stages = {"momentum": st_mom, "ns": st_ns, "update": st_upd}
@@ -912,6 +944,9 @@ def measure(opts, wl, dev, world, rank, local, block, K, Wu, barrier, max_over_r
                   "update": upd_b / (st_upd / 1000.0) / 1e9 if upd_b else None, "peak": hbm}
     if step.fused:
         launch["call"] = "muon_step (momentum, Newton-Schulz and update in one call)"
+    if step.fused_sign:
+        launch["call"] = ("sign_muon_step (momentum, Newton-Schulz with packed signs, vote and "
+                          "update in one call)")
     if dplan is not None:
         launch["exchange"] = ("all-gather(v) of updated weights" if wl.kind == "muon" else
                               "all-gather of packed signs" if opts.variant == "bits" else
@@ -1138,7 +1173,11 @@ def run_e2e(step, K, world, dev, barrier, max_over_ranks, scaling="strong"):
         g_ready[b].record(s_in)
         main.wait_event(g_ready[b])
         step.G = G_dev[b][1]
-        if not fused:
+        if getattr(step, "fused_sign", False):
+            main.wait_event(w_read)           # the previous read-back of W is complete
+            step()                            # one sign_muon_step call
+            g_free[b].record(main)
+        elif not fused:
             step.momentum()
             g_free[b].record(main)
             step.ns()
@@ -1167,8 +1206,31 @@ def run_e2e(step, K, world, dev, barrier, max_over_ranks, scaling="strong"):
     step.G, step.W = G_orig, W_orig
     for w, v in zip(W_orig, last_views):
         w.copy_(v)
+    # the host link alone: the same K copies each way, concurrently, with no compute; the
+    # e2e figure cannot exceed this rate
+    c0 = torch.cuda.Event(enable_timing=True)
+    c1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    c0.record(main)
+    s_in.wait_stream(main)
+    s_out.wait_stream(main)
+    for k in range(K):
+        with torch.cuda.stream(s_in):
+            G_dev[k % 2][0].copy_(G_host, non_blocking=True)
+        with torch.cuda.stream(s_out):
+            W_host.copy_(W_bufs[k % len(W_bufs)][0], non_blocking=True)
+    main.wait_stream(s_in)
+    main.wait_stream(s_out)
+    c1.record(main)
+    torch.cuda.synchronize()
+    ms_copy = max_over_ranks(c0.elapsed_time(c1))
     return {"value": job_throughput(ms, K, world, scaling), "unit": "steps/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": K,
+            "copy_only": {"value": job_throughput(ms_copy, K, world, scaling),
+                          "h2d_gbs": h2d * K / (ms_copy / 1000.0) / 1e9,
+                          "d2h_gbs": d2h * K / (ms_copy / 1000.0) / 1e9,
+                          "note": "the step's copies alone, both directions at once: the "
+                                  "host-link bound of the e2e figure"},
             "copies": "one pinned H2D slab and one D2H slab per step, on copy streams overlapping "
                       "the neighbouring steps' compute" +
                       ("; two device weight slabs, read one, write the other (%s)"

@@ -174,6 +174,30 @@ mao_status muon_step(const mao_mat* W, const mao_mat* M, const mao_mat* G, const
                      int32_t coeff_stride, float eps, int32_t compute, void* workspace,
                      size_t workspace_bytes, void* stream);
 
+/*
+ * One whole Sign-Muon step in one call ([SignMuon] §2 "Fluxo Algorítmico", steps 1-4, with
+ * the 1-bit all-gather variant; on one GPU the W_n workers' packed buffers already sit in
+ * the all-gather layout): the four stages of the calls above, in order on `stream`,
+ *   M^(m) <- fmaf(mu, M^(m), G^(m))          muon_momentum_update over the workers
+ *   U^(m)  = Newton–Schulz(M^(m))             ns_orthogonalize, signs only: the packed
+ *                                             signs of U^(m) into words + m*stride
+ *   vote   = sign(sum_m S^(m)), ties -> +1    majority_vote_packed
+ *   W     <- fmaf(-lr, vote, W)               apply_update with the vote
+ * with the results of those calls bit for bit (U itself is not stored).
+ *   W          one f32 or bf16 matrix (in/out).
+ *   M, G       HOST arrays of n_workers matrices of W's shape (M in/out, G read).
+ *   words      device, n_workers rows of worker_stride_words >= ceil(R*C/32) uint32 words
+ *              (written); vote: device, ceil(R*C/32) words (written).
+ *   steps, coeffs, coeff_stride, eps, compute as ns_orthogonalize; workspace of at least
+ *   ns_workspace_bytes(M, n_workers, compute) bytes, 256-byte aligned.
+ * Errors: as the four calls (argument checks before any launch).
+ */
+mao_status sign_muon_step(const mao_mat* W, const mao_mat* M, const mao_mat* G,
+                          int32_t n_workers, uint32_t* words, int64_t worker_stride_words,
+                          uint32_t* vote, float mu, float lr, int32_t steps, const float* coeffs,
+                          int32_t coeff_stride, float eps, int32_t compute, void* workspace,
+                          size_t workspace_bytes, void* stream);
+
 /* Size of the scratch area ns_orthogonalize_noalloc uses (16 MiB per device). */
 #define MAO_NOALLOC_WORKSPACE_BYTES (16u * 1024u * 1024u)
 
@@ -358,7 +382,8 @@ mao_status mao_sync_status(void* stream);
  * mao_launch_count: number of kernels this library has launched in this process.
  *
  * mao_profile_begin: from now on, every launch of the tensor-core product kernel (three
- *   per Newton–Schulz iteration, four per Dion step) and of the Dion CUDA-core kernels is
+ *   per Newton–Schulz iteration, four per Dion step), of the Dion CUDA-core kernels and of
+ *   the one-launch fp32 Newton–Schulz of small matrices is
  *   bracketed by a pair of CUDA events recorded on the launch's stream, for up to
  *   max_launches launches (1..1<<20). Creates the events
  *   (host-side driver objects, no device memory). Not thread-safe: one profiling session
@@ -371,7 +396,8 @@ mao_status mao_sync_status(void* stream);
  *
  * mao_profile_end_tagged: as mao_profile_end, and also writes one tag per recorded launch
  *   into tags_out (host array of max_out entries, may be NULL): MAO_PROF_TC for the
- *   tensor-core product kernel, otherwise the MAO_PROF_DION_* value of the Dion kernel.
+ *   tensor-core product kernel, otherwise the MAO_PROF_DION_* value of the Dion kernel or
+ *   MAO_PROF_NS_SMALL.
  */
 enum {
   MAO_PROF_TC = 0,
@@ -380,7 +406,8 @@ enum {
   MAO_PROF_DION_GRAM = 3,      /* P^T P assembled from its tensor-core parts (the products are MAO_PROF_TC) */
   MAO_PROF_DION_CHOL = 4,      /* Cholesky factor and its inverse */
   MAO_PROF_DION_SPLIT = 5,     /* P split into bf16 parts for the Cholesky QR products (MAO_PROF_TC), and the final P to bf16 */
-  MAO_PROF_DION_NORM = 6       /* column norms of R, Q = ColumnNormalize(R) */
+  MAO_PROF_DION_NORM = 6,      /* column norms of R, Q = ColumnNormalize(R) */
+  MAO_PROF_NS_SMALL = 7        /* the one-launch fp32 Newton–Schulz of small matrices */
 };
 int64_t mao_launch_count(void);
 mao_status mao_profile_begin(int32_t max_launches);

@@ -9,6 +9,7 @@ Functions (same names as the C ABI):
   ns_workspace_bytes(X, compute)                     workspace size for ns_orthogonalize
   ns_orthogonalize(inp, out, steps, coeffs, ...)     Newton–Schulz polar factor (+ packed signs)
   muon_step(W, M, G, mu, lr, ...)                    momentum + Newton–Schulz + update, fused
+  sign_muon_step(W, M, G, words, vote, mu, lr, ...)  momentum + NS signs + vote + update
   ns_orthogonalize_blockwise(inp, out, block, ...)   Newton–Schulz of every block on its own
   sign_pack_bits(U, bits)                            sign + 1-bit pack
   majority_vote_packed(bits, nbits, vote)            vote over workers' packed signs
@@ -163,6 +164,26 @@ def muon_step(W, M, G, mu, lr, steps=5, coeffs=QUINTIC, eps=1e-7, compute="bf16"
                          int(steps), carr, stride, float(eps), _COMPUTE[compute],
                          ctypes.c_void_p(ws.data_ptr()), ws.numel(), _stream(stream))
     _abi.check("muon_step", st)
+
+
+def sign_muon_step(W, M, G, words, vote, mu, lr, steps=5, coeffs=QUINTIC, eps=1e-7,
+                   compute="bf16", ws=None, stream=None):
+    """One whole Sign-Muon step: momentum of every worker, Newton-Schulz with the packed
+    signs into words[m] (int32 tensor [W_n][stride]), the majority vote into `vote` and
+    W <- W - lr * vote; the same results as the four separate calls."""
+    Ms, Gs = _as_list(M), _as_list(G)
+    if len(Ms) != len(Gs) or words.dim() != 2 or words.shape[0] != len(Ms) or \
+            words.stride(1) != 1 or words.dtype != torch.int32:
+        raise ValueError("need one M and G per worker and int32 words [W_n][stride]")
+    carr, stride = _coeff_args(coeffs, steps)
+    if ws is None:
+        ws = workspace(Ms, compute, Ms[0].device)
+    st = lib().sign_muon_step(ctypes.byref(_mat(W)), _mats(Ms), _mats(Gs), len(Ms),
+                              ctypes.c_void_p(words.data_ptr()), words.stride(0),
+                              ctypes.c_void_p(vote.data_ptr()), float(mu), float(lr), int(steps),
+                              carr, stride, float(eps), _COMPUTE[compute],
+                              ctypes.c_void_p(ws.data_ptr()), ws.numel(), _stream(stream))
+    _abi.check("sign_muon_step", st)
 
 
 def _coeff_args(coeffs, steps):
@@ -344,7 +365,7 @@ def launch_count():
 
 
 PROFILE_TAGS = {0: "tc", 1: "dion_setup", 2: "dion_stage", 3: "dion_gram", 4: "dion_chol",
-                5: "dion_split", 6: "dion_norm"}
+                5: "dion_split", 6: "dion_norm", 7: "ns_small"}
 
 
 def profile_begin(max_launches):

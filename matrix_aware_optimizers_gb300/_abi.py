@@ -27,6 +27,7 @@ EXPORTS = (
     "ns_workspace_bytes",
     "ns_orthogonalize",
     "muon_step",
+    "sign_muon_step",
     "ns_orthogonalize_noalloc",
     "ns_noalloc_workspace_bytes",
     "ns_blockwise_workspace_bytes",
@@ -103,6 +104,11 @@ def load():
         P(MaoMat), P(MaoMat), P(MaoMat), P(MaoMat), ctypes.c_int32, ctypes.c_float, ctypes.c_float,
         ctypes.c_int32, P(ctypes.c_float), ctypes.c_int32, ctypes.c_float, ctypes.c_int32, vp,
         ctypes.c_size_t, vp]
+    lib.sign_muon_step.restype = ctypes.c_int
+    lib.sign_muon_step.argtypes = [
+        P(MaoMat), P(MaoMat), P(MaoMat), ctypes.c_int32, vp, ctypes.c_int64, vp, ctypes.c_float,
+        ctypes.c_float, ctypes.c_int32, P(ctypes.c_float), ctypes.c_int32, ctypes.c_float,
+        ctypes.c_int32, vp, ctypes.c_size_t, vp]
     lib.ns_orthogonalize_noalloc.restype = ctypes.c_int
     lib.ns_orthogonalize_noalloc.argtypes = [
         P(MaoMat), P(MaoMat), ctypes.c_int32, ctypes.c_int32, P(ctypes.c_float), ctypes.c_int32,

@@ -7,6 +7,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "ns_small.h"
 
 namespace mao {
 
@@ -187,6 +188,54 @@ mao_status muon_step(const mao_mat* W, const mao_mat* M, const mao_mat* G, const
                 workspace, workspace_bytes, static_cast<cudaStream_t>(stream), &fuse);
 }
 
+mao_status sign_muon_step(const mao_mat* W, const mao_mat* M, const mao_mat* G,
+                          int32_t n_workers, uint32_t* words, int64_t worker_stride_words,
+                          uint32_t* vote, float mu, float lr, int32_t steps, const float* coeffs,
+                          int32_t coeff_stride, float eps, int32_t compute, void* workspace,
+                          size_t workspace_bytes, void* stream) {
+  if (!W || !M || !G || !words || !vote || n_workers < 1 || n_workers > 65535 || steps < 1 ||
+      steps > 64 || !coeffs)
+    return MAO_ERR_INVALID_ARG;
+  if (coeff_stride != 0 && coeff_stride != 3) return MAO_ERR_INVALID_ARG;
+  if (!valid_dtype(compute) || !std::isfinite(eps) || eps < 0.0f || !std::isfinite(mu) ||
+      !std::isfinite(lr))
+    return MAO_ERR_INVALID_ARG;
+  for (int i = 0; i < (coeff_stride ? 3 * steps : 3); ++i)
+    if (!std::isfinite(coeffs[i])) return MAO_ERR_INVALID_ARG;
+  mao_status st = check_mat(*W);
+  if (st != MAO_OK) return st;
+  const int64_t nbits = W->rows * W->cols;
+  if (worker_stride_words < ceil_div(nbits, 32)) return MAO_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(words) % 4 != 0 || reinterpret_cast<uintptr_t>(vote) % 4 != 0)
+    return MAO_ERR_MISALIGNED;
+  std::vector<mao_mat> out(n_workers);
+  std::vector<uint32_t*> bits(n_workers);
+  for (int m = 0; m < n_workers; ++m) {
+    st = check_mat(M[m]);
+    if (st == MAO_OK) st = check_mat(G[m]);
+    if (st != MAO_OK) return st;
+    if (M[m].rows != W->rows || M[m].cols != W->cols || G[m].rows != W->rows ||
+        G[m].cols != W->cols)
+      return MAO_ERR_INVALID_ARG;
+    out[m] = M[m];
+    out[m].data = nullptr;  // signs only
+    bits[m] = words + int64_t(m) * worker_stride_words;
+  }
+  if (!workspace) return MAO_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0) return MAO_ERR_MISALIGNED;
+  if (compute == MAO_BF16 && device_cc() / 10 != 10) return MAO_ERR_UNSUPPORTED;
+  if (workspace_bytes < ns_workspace_size(M, n_workers, compute)) return MAO_ERR_WORKSPACE;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  st = momentum_launch(M, G, n_workers, mu, s);
+  if (st == MAO_OK)
+    st = ns_run(M, out.data(), n_workers, steps, coeffs, coeff_stride, eps, compute,
+                bits.data(), workspace, workspace_bytes, s);
+  if (st == MAO_OK) st = vote_launch(words, n_workers, worker_stride_words, nbits, vote, s);
+  const uint32_t* vp = vote;
+  if (st == MAO_OK) st = update_launch(W, &vp, nullptr, 1, lr, s);
+  return st;
+}
+
 mao_status sign_pack_bits(const mao_mat* U, uint32_t* bits, void* stream) {
   if (!U || !bits) return MAO_ERR_INVALID_ARG;
   const mao_status st = check_mat(*U);
@@ -249,8 +298,9 @@ uint64_t mao_get_wait_limit(void) { return g_wait_limit.load(std::memory_order_r
 mao_status mao_sync_status(void* stream) {
   const mao_status a = tc_read_and_clear_error(static_cast<cudaStream_t>(stream));
   const mao_status b = dion_read_and_clear_error(static_cast<cudaStream_t>(stream));
-  if (a == MAO_ERR_CUDA || b == MAO_ERR_CUDA) return MAO_ERR_CUDA;
-  return a != MAO_OK ? a : b;
+  const mao_status c = small_read_and_clear_error(static_cast<cudaStream_t>(stream));
+  if (a == MAO_ERR_CUDA || b == MAO_ERR_CUDA || c == MAO_ERR_CUDA) return MAO_ERR_CUDA;
+  return a != MAO_OK ? a : b != MAO_OK ? b : c;
 }
 
 int64_t mao_launch_count(void) { return g_launches.load(); }

@@ -308,12 +308,17 @@ __device__ __forceinline__ uint32_t bf16_pair(float a, float b) {
 }
 
 
-// Factors the 32 x 32 block Ad = L L^T in registers (lane = row; the diagonal pivot of step j
-// comes from lane j, the multipliers of rows k > j from lane k) and writes L back (zeros
-// above the diagonal) and 1 / L_jj to rinv[j]. The pivot's reciprocal square root comes
-// from rsqrtf (L_jj = p rsqrt(p)). A pivot that is not positive is replaced by 1e-30 and
-// reported. Not inlined: inlined into the kernel, its a[] array lands in local memory.
-__device__ __noinline__ bool chol32(float* Ad, float* rinv, int lane) {
+// Factors the 32 x 32 block Ad = L L^T in registers (lane = row), column by column in the
+// left-looking order: for column j, lane j (whose row of L is final up to column j - 1)
+// puts that row into `row` (shared memory), every lane forms the dot product of its own row
+// with it from 16-byte broadcast reads (four partial sums), and the pivot
+// p = A_jj - sum_k L_jk^2 comes from lane j; L_ij = (A_ij - sum_k L_ik L_jk) / L_jj. One
+// broadcast of a row per column replaces the shuffles of every multiplier of a
+// right-looking step. Writes L back (zeros above the diagonal) and 1 / L_jj to rinv[j]; the
+// pivot's reciprocal square root comes from rsqrtf (L_jj = p rsqrt(p)). A pivot that is not
+// positive is replaced by 1e-30 and reported. Not inlined: inlined into the kernel, its a[]
+// array lands in local memory.
+__device__ __noinline__ bool chol32(float* Ad, float* rinv, float* row, int lane) {
   float a[32];
 #pragma unroll
   for (int q = 0; q < 32; q += 4) {
@@ -327,19 +332,34 @@ __device__ __noinline__ bool chol32(float* Ad, float* rinv, int lane) {
   float my_inv = 0.0f;
 #pragma unroll
   for (int j = 0; j < 32; ++j) {
-    float p = __shfl_sync(0xFFFFFFFFu, a[j], j);
+    float v = a[j];
+    if (j > 0) {
+      if (lane == j) {
+#pragma unroll
+        for (int q = 0; q < j; q += 4)
+          *reinterpret_cast<float4*>(row + q) = make_float4(a[q], a[q + 1], a[q + 2], a[q + 3]);
+      }
+      __syncwarp();
+      float s[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+      for (int q = 0; q < j; q += 4) {
+        const float4 r = ld4(row + q);
+        s[0] = __fmaf_rn(a[q], r.x, s[0]);
+        if (q + 1 < j) s[1] = __fmaf_rn(a[q + 1], r.y, s[1]);
+        if (q + 2 < j) s[2] = __fmaf_rn(a[q + 2], r.z, s[2]);
+        if (q + 3 < j) s[3] = __fmaf_rn(a[q + 3], r.w, s[3]);
+      }
+      v -= (s[0] + s[1]) + (s[2] + s[3]);
+      __syncwarp();  // the row is read by every lane before lane j + 1 overwrites it
+    }
+    float p = __shfl_sync(0xFFFFFFFFu, v, j);
     if (!(p > 0.0f)) {
       bad = true;
       p = 1e-30f;
     }
     const float inv = rsqrtf(p);
     if (lane == j) my_inv = inv;
-    a[j] = lane == j ? p * inv : (lane > j ? a[j] * inv : 0.0f);
-#pragma unroll
-    for (int k = j + 1; k < 32; ++k) {
-      const float lkj = __shfl_sync(0xFFFFFFFFu, a[j], k);
-      if (lane >= k) a[k] = __fmaf_rn(-a[j], lkj, a[k]);
-    }
+    a[j] = lane == j ? p * inv : (lane > j ? v * inv : 0.0f);
   }
 #pragma unroll
   for (int q = 0; q < 32; ++q) Ad[lane * kLd + q] = q <= lane ? a[q] : 0.0f;
@@ -391,6 +411,7 @@ __device__ __forceinline__ void inv32(float* Ad, const float* rinv, int lane) {
 __global__ void __launch_bounds__(kCholThreads, 1) dion_chol_kernel(const __grid_constant__ DionCommon c) {
   extern __shared__ __align__(16) float sm[];
   __shared__ float rinv[32];
+  __shared__ __align__(16) float crow[32];  // chol32's broadcast row
   const DionSlot& e = c.slots[blockIdx.x];
   const int r = c.r, ldr = c.ldr;
   const int nb = (r + 31) / 32;
@@ -412,7 +433,7 @@ __global__ void __launch_bounds__(kCholThreads, 1) dion_chol_kernel(const __grid
   // factors and inverts diagonal block J (warp 0)
   auto factor = [&](int J) {
     float* Dj = blk(A, J, J);
-    if (chol32(Dj, rinv, lane) && lane == 0) atomicOr(&g_dion_error, 1u);
+    if (chol32(Dj, rinv, crow, lane) && lane == 0) atomicOr(&g_dion_error, 1u);
     inv32(Dj, rinv, lane);
   };
   // rows 8 quarter .. 8 quarter + 7 of A_IK -= L_IJ L_KJ^T
@@ -824,6 +845,23 @@ int out_flags(const mao_mat& a) {
 mao_status dion_tc(const DionPlan& plan, uint8_t* ws, const OutEntry* table, int op, float alpha,
                    cudaStream_t stream) {
   const int64_t r = plan.r, ldr = plan.ldr;
+  // The kernel deals tiles to CTA pairs round-robin in list order; listing the groups with
+  // the deepest products (the most k-blocks per tile) first spreads the long tiles over the
+  // pairs before the short ones fill the gaps.
+  std::vector<size_t> order(plan.groups.size());
+  for (size_t i = 0; i < order.size(); ++i) order[i] = i;
+  auto depth = [&](size_t i) {
+    const DionGroup& g = plan.groups[i];
+    switch (op) {
+      case 0: return g.n;
+      case 1: return g.m;
+      case 4: return 3 * ldr;
+      case 5: return g.m;
+      default: return r;
+    }
+  };
+  std::stable_sort(order.begin(), order.end(),
+                   [&](size_t x, size_t y) { return depth(x) > depth(y); });
   for (size_t g0 = 0; g0 < plan.groups.size(); g0 += tc::MAX_GROUPS) {
     TcParams p;
     memset(&p, 0, sizeof(p));
@@ -834,7 +872,7 @@ mao_status dion_tc(const DionPlan& plan, uint8_t* ws, const OutEntry* table, int
     p.timeout_ns = wait_limit_ns();
     int64_t tiles = 0;
     for (size_t gi = g0; gi < plan.groups.size() && p.ngroups < tc::MAX_GROUPS; ++gi) {
-      const DionGroup& g = plan.groups[gi];
+      const DionGroup& g = plan.groups[order[gi]];
       TcGroup& G = p.g[p.ngroups++];
       const int64_t ldn = round_up(g.n, tc::LD_ALIGN);
       const void *A, *B;

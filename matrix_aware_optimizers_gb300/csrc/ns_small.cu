@@ -7,17 +7,18 @@
 // holds all of X and A in shared memory and computes one eighth of the rows of each
 // product ("分散ニュートン・シュルツ" of the Megatron Muon article: three products per
 // iteration; the iteration of the Sign-Muon summary, §2 "Mecanismo Central" item 1):
-//   A  = s^2 X X^T            rows of this CTA, then the other CTAs' rows copied in
+//   A  = s^2 X X^T            rows of this CTA, sent to every other CTA
 //   B' = a I + b A + c A A    rows of this CTA (local)
-//   X' = s B' X               rows of this CTA into the other X buffer, then the others'
+//   X' = s B' X               rows of this CTA into the other X buffer, sent likewise
 // with s = 1/(||X||_F + eps) in the first iteration and 1 afterwards (the same placement
-// of the normalisation as the general path). After a cluster barrier each CTA copies the
-// rows the other CTAs computed with 16-byte distributed shared-memory loads. A CTA writes
-// its A rows again only after the next barrier, when every copy of them is done, and the
-// X buffers alternate, so two barriers per iteration order every access; one more after
-// the last copy keeps every CTA resident until no other CTA reads its shared memory. Every
-// CTA computes the Frobenius norm itself from its full copy in the same fixed order, so
-// all eight hold the same s. At the end each CTA writes one eighth of
+// of the normalisation as the general path). A CTA sends its rows with one bulk
+// asynchronous copy per peer (shared memory to the peer's shared memory), whose bytes
+// complete on the peer's barrier for that exchange; each CTA waits on its own barrier for
+// the other seven CTAs' rows. No buffer is written while a peer may still read it: a CTA
+// sends its A rows of the next iteration only after it holds every CTA's X rows of that
+// iteration, which each CTA sends only after it has used the current A, and the X buffers
+// alternate. Every CTA computes the Frobenius norm itself from its full copy in the same
+// fixed order, so all eight hold the same s. At the end each CTA writes one eighth of
 // U (in the matrix's own orientation) and of the packed signs, whole words, so the sign
 // buffer needs no clearing. All arithmetic is fp32 FFMA with one accumulation chain per
 // output, in k order.
@@ -89,26 +90,92 @@ __device__ __forceinline__ uint32_t remote(uint32_t addr, uint32_t rank) {
   return r;
 }
 
-// Copies the rows of buf that the other CTAs of the cluster own (rows [q*rpc, q*rpc + rpc)
-// of CTA q, `quads` 16-byte units per row of stride ld floats) from their shared memory
-// into this CTA's copy, with 16-byte distributed shared-memory loads.
-__device__ __forceinline__ void pull_rows(float* buf, int ld, int quads, int m, int rpc,
-                                          uint32_t self, int tid) {
-  const int mine0 = min(m, int(self) * rpc), mine1 = min(m, mine0 + rpc);
-  const int others = m - (mine1 - mine0);
-  for (int t = tid; t < others * quads; t += kThreads) {
-    int row = t / quads;
-    const int q4 = t - row * quads;
-    if (row >= mine0) row += mine1 - mine0;  // skip this CTA's own rows
-    float* dst = buf + size_t(row) * ld + 4 * q4;
-    const uint32_t src = remote(smem_addr(dst), uint32_t(row / rpc));
-    float4 v;
-    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                 : "r"(src)
-                 : "memory");
-    *reinterpret_cast<float4*>(dst) = v;
+__device__ unsigned int g_small_error;  // bit 0: a row exchange did not complete in time
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Sends this CTA's rows [r0, r1) of buf (row stride ld floats, contiguous) to the same place
+// in every other CTA of the cluster with bulk asynchronous copies, each completing its bytes
+// on the receiver's barrier `bar` (same offset in every CTA). One thread issues them once
+// every writer of the rows has fenced its writes for the async proxy and passed a CTA
+// barrier; it waits until the copies have read the rows before returning, so the rows may
+// be overwritten afterwards.
+__device__ __forceinline__ void push_rows(const float* buf, int ld, int r0, int r1,
+                                          uint64_t* bar, uint32_t self) {
+  if (r1 <= r0) return;
+  const uint32_t bytes = uint32_t(r1 - r0) * uint32_t(ld) * 4u;
+  const uint32_t src = smem_addr(buf + size_t(r0) * ld);
+  for (uint32_t q = 0; q < kCluster; ++q) {
+    if (q == self) continue;
+    asm volatile(
+        "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(remote(src, q)), "r"(src), "r"(bytes), "r"(remote(smem_addr(bar), q))
+        : "memory");
   }
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+// Arms this CTA's barrier for the bytes the other CTAs send in this phase (one arrival).
+__device__ __forceinline__ void expect_rows(uint64_t* bar, int ld, int m, int own_rows) {
+  const uint32_t bytes = uint32_t(m - own_rows) * uint32_t(ld) * 4u;
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+// Waits (every thread) for the barrier's phase `parity`: the other CTAs' rows have landed.
+// Bounded: after about 2 s the error word is set and the kernel goes on with what it has
+// (wrong results, reported by mao_sync_status), so no wait can hang the GPU.
+__device__ __forceinline__ void wait_rows(uint64_t* bar, uint32_t parity) {
+  const uint32_t a = smem_addr(bar);
+  uint32_t ok = 0;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.b32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(a), "r"(parity)
+      : "memory");
+  if (ok) return;
+  const uint64_t t0 = globaltimer_ns();
+  while (!ok) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.b32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(a), "r"(parity)
+        : "memory");
+    if (!ok && globaltimer_ns() - t0 > 2000000000ull) {
+      atomicOr(&g_small_error, 1u);
+      return;
+    }
+  }
+}
+
+// Four consecutive elements of a row as fp32 (k + 3 < n and `vec`: one 16-byte (f32) or
+// 8-byte (bf16) load; otherwise element by element, zeros past n).
+__device__ __forceinline__ float4 load4(const void* src, int64_t row_off, int k, int n, int dt,
+                                        bool vec) {
+  if (vec && k + 3 < n) {
+    if (dt == MAO_BF16) {
+      const uint2 raw = __ldg(reinterpret_cast<const uint2*>(
+          reinterpret_cast<const __nv_bfloat16*>(src) + row_off + k));
+      const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.x));
+      const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.y));
+      return make_float4(a.x, a.y, b.x, b.y);
+    }
+    return __ldg(reinterpret_cast<const float4*>(reinterpret_cast<const float*>(src) + row_off + k));
+  }
+  float4 v;
+  v.x = k < n ? load_elem(src, row_off + k, dt) : 0.0f;
+  v.y = k + 1 < n ? load_elem(src, row_off + k + 1, dt) : 0.0f;
+  v.z = k + 2 < n ? load_elem(src, row_off + k + 2, dt) : 0.0f;
+  v.w = k + 3 < n ? load_elem(src, row_off + k + 3, dt) : 0.0f;
+  return v;
 }
 
 // acc0 = sum_k P[i0][k] Q[j][k], acc1 = sum_k P[i1][k] Q[j][k] over kq quads (rows of
@@ -150,23 +217,49 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
   float* A = sm + size_t(2) * m * nx;
   float* Bm = A + size_t(m) * ma;
   double* red = reinterpret_cast<double*>(Bm + size_t(L.rpc) * ma);
+  __shared__ uint64_t bar_a, bar_x;  // arrivals of the other CTAs' rows of A and of X
+  if (tid == 0) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&bar_a)) : "memory");
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&bar_x)) : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
 
   // ---- the matrix into X[0] (X = M, or M^T for a tall M), zero-padded rows, and the sum of
-  // squares in a fixed order (the same in every CTA of the cluster)
-  double ss = 0.0;
+  // squares in a fixed order (the same in every CTA of the cluster): per thread in fp32,
+  // then the threads' sums in fp64
+  float ss = 0.0f;
   if (!tall) {
-    for (int idx = tid; idx < m * nx; idx += kThreads) {
-      const int i = idx / nx, k = idx - i * nx;
-      const float v = k < n ? load_elem(e.src, int64_t(i) * e.src_ld + k, e.src_dt) : 0.0f;
-      Xb[0][idx] = v;
-      ss += double(v) * double(v);
+    const int es = e.src_dt == MAO_BF16 ? 2 : 4;
+    const bool vec = (reinterpret_cast<uintptr_t>(e.src) % (4 * es) == 0) && (e.src_ld % 4 == 0);
+    const int quads = nx / 4;  // the last quad of every row is padding
+    constexpr int kU = 8;
+    for (int t0 = tid; t0 < m * quads; t0 += kU * kThreads) {
+      float4 v[kU];
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int t = t0 + u * kThreads;
+        const int i = t / quads, q = t - i * quads;
+        v[u] = t < m * quads ? load4(e.src, int64_t(i) * e.src_ld, 4 * q, n, e.src_dt, vec)
+                             : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      }
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int t = t0 + u * kThreads;
+        if (t < m * quads) {
+          reinterpret_cast<float4*>(Xb[0])[t] = v[u];
+          ss = __fmaf_rn(v[u].x, v[u].x, ss);
+          ss = __fmaf_rn(v[u].y, v[u].y, ss);
+          ss = __fmaf_rn(v[u].z, v[u].z, ss);
+          ss = __fmaf_rn(v[u].w, v[u].w, ss);
+        }
+      }
     }
   } else {
     for (int idx = tid; idx < n * e.C; idx += kThreads) {  // source row-major: M[k][i]
       const int k = idx / e.C, i = idx - k * e.C;
       const float v = load_elem(e.src, int64_t(k) * e.src_ld + i, e.src_dt);
       Xb[0][size_t(i) * nx + k] = v;
-      ss += double(v) * double(v);
+      ss = __fmaf_rn(v, v, ss);
     }
     for (int idx = tid; idx < m * (nx - n); idx += kThreads) {
       const int i = idx / (nx - n), k = n + idx - i * (nx - n);
@@ -177,14 +270,16 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
     const int i = idx / (ma - m), k = m + idx - i * (ma - m);
     A[size_t(i) * ma + k] = 0.0f;
   }
-  red[tid] = ss;
+  // fixed-order reduction: a shuffle tree within each warp, then the eight warp sums
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, o);
+  if ((tid & 31) == 0) red[tid >> 5] = double(ss);
   __syncthreads();
-  for (int w = kThreads / 2; w > 0; w >>= 1) {
-    if (tid < w) red[tid] += red[tid + w];
-    __syncthreads();
-  }
-  const float s = float(1.0 / (sqrt(red[0]) + double(p.eps)));
-  // every CTA of the cluster is running before any distributed shared-memory access
+  double tot = 0.0;
+#pragma unroll
+  for (int w = 0; w < kThreads / 32; ++w) tot += red[w];
+  const float s = float(1.0 / (sqrt(tot) + double(p.eps)));
+  // every CTA of the cluster is running, its barriers initialised, before any copy to it
   cluster_barrier();
 
   const int xq = (n + 3) / 4, aq = (m + 3) / 4;
@@ -195,7 +290,9 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
     float* Xn = Xb[(it + 1) & 1];
     const float s2 = it == 0 ? s * s : 1.0f;
     const float s1 = it == 0 ? s : 1.0f;
-    // A = s^2 X X^T: rows i0, i0 + 1 of this CTA against row j; then the other rows
+    const uint32_t parity = uint32_t(it) & 1u;
+    // A = s^2 X X^T: rows i0, i0 + 1 of this CTA against row j, sent to every other CTA
+    if (tid == 0) expect_rows(&bar_a, ma, m, r1 - r0);
     for (int t = tid; t < pairs * m; t += kThreads) {
       const int j = t % m, i0 = r0 + 2 * (t / m), i1 = min(i0 + 1, r1 - 1);
       float v0, v1;
@@ -203,9 +300,10 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
       A[size_t(i0) * ma + j] = s2 * v0;
       if (i0 + 1 < r1) A[size_t(i1) * ma + j] = s2 * v1;
     }
-    cluster_barrier();
-    pull_rows(A, ma, aq, m, L.rpc, crank, tid);
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     __syncthreads();
+    if (tid == 0) push_rows(A, ma, r0, r1, &bar_a, crank);
+    wait_rows(&bar_a, parity);
     // B' = a I + b A + c A A (A A = A A^T): this CTA's rows, local
     for (int t = tid; t < pairs * m; t += kThreads) {
       const int j = t % m, i0 = r0 + 2 * (t / m), i1 = min(i0 + 1, r1 - 1);
@@ -218,7 +316,8 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
             __fmaf_rn(cc, v1, cb * A[size_t(i1) * ma + j]) + (i1 == j ? ca : 0.0f);
     }
     __syncthreads();
-    // X' = s B' X: row i, columns 4q .. 4q + 3 (zeros past n); then the other rows
+    // X' = s B' X: row i, columns 4q .. 4q + 3 (zeros past n), sent to every other CTA
+    if (tid == 0) expect_rows(&bar_x, nx, m, r1 - r0);
     for (int t = tid; t < (r1 - r0) * xq; t += kThreads) {
       const int il = t / xq, q = t - il * xq;
       const float* brow = Bm + size_t(il) * ma;
@@ -237,12 +336,12 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
           make_float4(s1 * acc.x, j + 1 < n ? s1 * acc.y : 0.0f, j + 2 < n ? s1 * acc.z : 0.0f,
                       j + 3 < n ? s1 * acc.w : 0.0f);
     }
-    cluster_barrier();
-    pull_rows(Xn, nx, xq, m, L.rpc, crank, tid);
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     __syncthreads();
+    if (tid == 0) push_rows(Xn, nx, r0, r1, &bar_x, crank);
+    wait_rows(&bar_x, parity);
   }
-
-  // no CTA leaves (or reuses its buffers) while another may still copy rows from it
+  // every CTA has received all of its rows before any CTA leaves
   cluster_barrier();
 
   // ---- outputs from the final X (complete in every CTA): one eighth each
@@ -281,6 +380,23 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
 }
 
 }  // namespace
+
+mao_status small_read_and_clear_error(cudaStream_t stream) {
+  unsigned int v = 0;
+  if (cudaMemcpyFromSymbolAsync(&v, g_small_error, sizeof(v), 0, cudaMemcpyDeviceToHost,
+                                stream) != cudaSuccess)
+    return MAO_ERR_CUDA;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return MAO_ERR_CUDA;
+  if (v) {
+    const unsigned int zero = 0;
+    if (cudaMemcpyToSymbolAsync(g_small_error, &zero, sizeof(zero), 0, cudaMemcpyHostToDevice,
+                                stream) != cudaSuccess ||
+        cudaStreamSynchronize(stream) != cudaSuccess)
+      return MAO_ERR_CUDA;
+    return MAO_ERR_TIMEOUT;
+  }
+  return MAO_OK;
+}
 
 size_t ns_small_smem_bytes(int64_t R, int64_t C) {
   if (R < 1 || C < 1 || R > 4096 || C > 4096) return ~size_t(0);
@@ -338,8 +454,10 @@ mao_status ns_small_run(const mao_mat* in, const mao_mat* out, int32_t batch, in
     cfg.blockDim = dim3(unsigned(kThreads));
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
+    profile_before_launch(stream, MAO_PROF_NS_SMALL);
     const cudaError_t err = cudaLaunchKernelEx(&cfg, ns_small_kernel, p);
     count_launch();
+    profile_after_launch(stream);
     if (err != cudaSuccess) return MAO_ERR_CUDA;
     const mao_status st = cuda_status(cudaGetLastError());
     if (st != MAO_OK) return st;

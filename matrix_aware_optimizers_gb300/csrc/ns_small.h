@@ -22,5 +22,7 @@ bool ns_small_eligible(const mao_mat* in, const mao_mat* out, int32_t batch, int
 mao_status ns_small_run(const mao_mat* in, const mao_mat* out, int32_t batch, int32_t steps,
                         const float* coeffs, int32_t coeff_stride, float eps,
                         uint32_t* const* sign_bits, cudaStream_t stream);
+// Reads and clears the small kernel's error word (a row exchange that timed out).
+mao_status small_read_and_clear_error(cudaStream_t stream);
 
 }  // namespace mao

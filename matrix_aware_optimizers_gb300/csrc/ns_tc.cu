@@ -159,6 +159,19 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// The same non-blocking test with cluster-scope acquire.
+__device__ __forceinline__ bool mbar_test_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.b32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Waits for the phase of `parity` to complete. Gives up after `limit_ns` or when another
 // role raised the CTA's abort flag; a timeout sets the abort flag and the error word. A
 // limit of 0 gives up at once unless a non-blocking test finds the phase complete (each
@@ -188,6 +201,15 @@ __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile i
       return false;
     }
   }
+}
+
+// mbar_wait with its common case inline: a phase that is already complete costs one
+// non-blocking test and no call.
+template <bool CLUSTER = false>
+__device__ __forceinline__ bool mbar_wait_fast(uint32_t bar, uint32_t parity,
+                                               volatile int* abort_flag, uint64_t limit_ns) {
+  const bool done = CLUSTER ? mbar_test_wait_cluster(bar, parity) : mbar_test_wait(bar, parity);
+  return done || mbar_wait<CLUSTER>(bar, parity, abort_flag, limit_ns);
 }
 
 // Bounded wait used only while draining after an abort (ignores the abort flag).
@@ -727,6 +749,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads(MODE), 1)
   // Launched as a programmatic dependent of the previous kernel in the stream: the set-up
   // above may overlap that kernel's last CTAs; nothing below runs before it has completed
   // and its memory is visible. The next launch may start its own set-up from here on.
+  // the first tile's parameters reach the constant cache while the previous kernel
+  // finishes (they do not depend on it); one warp is enough, the cache is the SM's
+  if (warp == 1 && pair < p.total_tiles) {
+    Tile t0;
+    decode_tile(p, pair, t0);
+    const TcGroup& G0 = p.g[t0.g];
+    const int touch = t0.row0 ^ t0.col0 ^ t0.nkb ^ G0.M ^ G0.N ^ G0.a_mn ^ G0.b_mn ^
+                      G0.a_sym ^ G0.b_sym ^ G0.same_ab ^ G0.slot0 ^ G0.syrk ^ G0.final_out ^
+                      int(G0.res_ld) ^ int(G0.out_ld);
+    asm volatile("" ::"r"(touch));
+  }
+  // the producer's lanes fetch the tensor maps while the previous kernel finishes
+  if (warp == 0 && lane < 2 * p.ngroups) {
+    const TcGroup& G = p.g[lane >> 1];
+    const CUtensorMap* map = (lane & 1) ? &G.tmB : &G.tmA;
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+  }
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const uint64_t limit = p.timeout_ns;
@@ -783,7 +822,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads(MODE), 1)
 #ifdef MAO_TC_TRACE
           const long long tw = clock64();
 #endif
-          if (!mbar_wait(smem_u32(&empty_bar[stage]), phase ^ 1u, abort_flag, limit)) {
+          if (!mbar_wait_fast(smem_u32(&empty_bar[stage]), phase ^ 1u, abort_flag, limit)) {
             okw = 0;
           } else if (leader) {
             mbar_expect_tx(smem_u32(&full_bar[stage]), tx_bytes);
@@ -838,7 +877,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads(MODE), 1)
 #ifdef MAO_TC_TRACE
         const long long tw0 = clock64();
 #endif
-        if (!mbar_wait<true>(smem_u32(&tempty_bar[acc]), acc_phase ^ 1u, abort_flag, limit)) {
+        if (!mbar_wait_fast<true>(smem_u32(&tempty_bar[acc]), acc_phase ^ 1u, abort_flag, limit)) {
           ok = false;
           break;
         }
@@ -854,7 +893,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads(MODE), 1)
 #ifdef MAO_TC_TRACE
           const long long tw1 = clock64();
 #endif
-          if (!mbar_wait(smem_u32(&full_bar[stage]), phase, abort_flag, limit)) {
+          if (!mbar_wait_fast(smem_u32(&full_bar[stage]), phase, abort_flag, limit)) {
             ok = false;
             break;
           }
@@ -964,7 +1003,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads(MODE), 1)
 #endif
       // every lane waits; the warp goes on only if all of them saw the accumulator (the
       // TMEM loads below are warp-wide), so a lane that timed out stops the whole warp
-      if (!__all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&tfull_bar[acc]), acc_phase, abort_flag, limit)))
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait_fast(smem_u32(&tfull_bar[acc]), acc_phase, abort_flag, limit)))
         break;
       tc_fence_after();
 #ifdef MAO_TC_TRACE
@@ -1069,7 +1108,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads(MODE), 1)
 #endif
       // every lane waits; the warp goes on only if all of them saw the accumulator (the
       // TMEM loads below are warp-wide), so a lane that timed out stops the whole warp
-      if (!__all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&tfull_bar[acc]), acc_phase, abort_flag, limit)))
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait_fast(smem_u32(&tfull_bar[acc]), acc_phase, abort_flag, limit)))
         break;
       tc_fence_after();
 #ifdef MAO_TC_TRACE

@@ -183,3 +183,27 @@ def test_muon_step_arguments_rejected_before_any_launch(lib):
     assert call(W_out=_mats((64, 95), data=fake)) == _abi.MAO_ERR_INVALID_ARG
     assert call(ws=None) == _abi.MAO_ERR_INVALID_ARG
     assert call(ws=ctypes.c_void_p(fake + 16)) == _abi.MAO_ERR_MISALIGNED
+
+
+def test_sign_muon_step_argument_checks(lib):
+    fake = 0x10000
+    co = (ctypes.c_float * 3)(3.4445, -4.775, 2.0315)
+    ws = ctypes.c_void_p(fake)
+    W = _mats((6, 40), dtype=_abi.MAO_F32, data=fake)
+    M = (_abi.MaoMat * 2)(*[_abi.MaoMat(fake, 6, 40, 40, _abi.MAO_F32, 0) for _ in range(2)])
+    p = ctypes.c_void_p(fake)
+    nw = (6 * 40 + 31) // 32
+
+    def call(W=W, M=M, n=2, words=p, stride=nw, vote=p, ws=ws, wsb=1 << 30):
+        return lib.sign_muon_step(W, M, M, n, words, stride, vote, 0.95, 0.02, 5, co, 0, 1e-7,
+                                  0, ws, wsb, None)
+
+    assert call(words=None) == _abi.MAO_ERR_INVALID_ARG
+    assert call(vote=None) == _abi.MAO_ERR_INVALID_ARG
+    assert call(n=0) == _abi.MAO_ERR_INVALID_ARG
+    assert call(stride=nw - 1) == _abi.MAO_ERR_INVALID_ARG          # rows would overlap
+    assert call(words=ctypes.c_void_p(fake + 2)) == _abi.MAO_ERR_MISALIGNED
+    assert call(ws=None) == _abi.MAO_ERR_INVALID_ARG
+    assert call(wsb=16) == _abi.MAO_ERR_WORKSPACE
+    other = (_abi.MaoMat * 2)(*[_abi.MaoMat(fake, 6, 41, 41, _abi.MAO_F32, 0) for _ in range(2)])
+    assert call(M=other) == _abi.MAO_ERR_INVALID_ARG                 # worker shape != W

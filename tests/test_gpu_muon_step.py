@@ -110,3 +110,43 @@ def test_muon_step_out_of_place(cuda):
     mao.sync_status()
     for a, b in zip(W_alias, W_in_place):
         assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("shape,dt,compute", [((64, 128), "f32", "f32"),
+                                              ((300, 500), "bf16", "bf16"),
+                                              ((500, 300), "bf16", "bf16")])
+def test_sign_muon_step_equals_composed_calls(cuda, shape, dt, compute):
+    """sign_muon_step (one call) against muon_momentum_update, ns_orthogonalize with packed
+    signs, majority_vote_packed and apply_update: M, every worker's words, the vote and W bit
+    for bit ([SignMuon] §2 "Fluxo Algorítmico", steps 1-4)."""
+    g = torch.Generator()
+    g.manual_seed(21)
+    Wn = 4
+    R, C = shape
+    W0 = (torch.randn(shape, generator=g) * 0.02).to(DT[dt]).to(cuda)
+    M0 = torch.randn(shape, generator=g).to(DT[dt]).to(cuda)
+    Gs = [torch.randn(shape, generator=g).to(DT[dt]).to(cuda) for _ in range(Wn)]
+    nw = mao.packed_words(R, C)
+    stride = (nw + 3) // 4 * 4
+    # one call
+    W1, M1 = W0.clone(), [M0.clone() for _ in range(Wn)]
+    words1 = torch.zeros((Wn, stride), dtype=torch.int32, device=cuda)
+    vote1 = torch.zeros(stride, dtype=torch.int32, device=cuda)
+    mao.sign_muon_step(W1, M1, Gs, words1, vote1, 0.95, 1e-3, 5, mao.QUINTIC, 1e-7, compute)
+    # the composed calls
+    W2, M2 = W0.clone(), [M0.clone() for _ in range(Wn)]
+    words2 = torch.zeros((Wn, stride), dtype=torch.int32, device=cuda)
+    mao.muon_momentum_update(M2, Gs, 0.95)
+    mao.ns_orthogonalize(M2, None, 5, mao.QUINTIC, 1e-7, compute,
+                         sign_bits=[words2[m, :nw] for m in range(Wn)])
+    vote2 = mao.majority_vote_packed(words2, R * C)
+    mao.apply_update(W2, 1e-3, vote=vote2)
+    mao.sync_status()
+    for a, b in zip(M1, M2):
+        assert torch.equal(a, b)
+    assert torch.equal(words1[:, :nw], words2[:, :nw])
+    assert torch.equal(vote1[:nw], vote2[:nw])
+    assert torch.equal(W1, W2)
+    # and the vote against the oracle's vote of these words
+    w = words2[:, :nw].cpu().numpy().view(np.uint32)
+    assert np.array_equal(vote1[:nw].cpu().numpy().view(np.uint32), oracle.majority_vote(w, R * C))
