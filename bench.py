@@ -1164,6 +1164,48 @@ def run_e2e(step, K, world, dev, barrier, max_over_ranks, scaling="strong"):
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
+    host_call = getattr(step, "fused", False) and not dion
+    if host_call:
+        # one muon_step_host call per step (host gradients in, host weights out, through the
+        # C ABI), rotating over n streams with n gradient slabs, n weight slabs and n host
+        # weight buffers: step k reads weight slab k % n and writes slab (k + 1) % n, and
+        # waits for step k-1's compute event; everything else a step touches was last used
+        # on its own stream, so each step's copies overlap its neighbours' compute
+        wl = step.wl
+        n = 3 if h2d <= (4 << 30) else 2
+        streams = [torch.cuda.Stream() for _ in range(n)]
+        done = [torch.cuda.Event() for _ in range(n)]
+        Gs = [G_dev[0], G_dev[1]] + [_slab(G_orig, dev) for _ in range(n - 2)]
+        Ws = [W_bufs[0], W_bufs[1]] + [_slab(W_orig, dev) for _ in range(n - 2)]
+        W_hosts = [W_host] + [_slab([w.cpu() for w in W_orig], "cpu", pin=True)[0]
+                              for _ in range(n - 1)]
+        for st_, ev in zip(streams, done):
+            ev.record(st_)
+        torch.cuda.synchronize()
+        e0.record(main)
+        for st_ in streams:
+            st_.wait_stream(main)
+        for k in range(K):
+            b = k % n
+            step.mao.muon_step_host(
+                Ws[b][1], step.M, Gs[b][1], wl.mu, wl.lr, G_host, Gs[b][0], W_hosts[b],
+                Ws[(k + 1) % n][0], wl.steps, wl.coeffs, wl.eps, wl.compute, ws=step.ws,
+                W_out=Ws[(k + 1) % n][1], stream=streams[b],
+                wait_event=done[(k - 1) % n] if k > 0 else None, record_event=done[b])
+        for st_ in streams:
+            main.wait_stream(st_)
+        e1.record(main)
+        torch.cuda.synchronize()
+        barrier()
+        ms = max_over_ranks(e0.elapsed_time(e1))
+        for w, v in zip(W_orig, Ws[K % n][1]):
+            w.copy_(v)
+        step.G, step.W = G_orig, W_orig
+        return {"value": job_throughput(ms, K, world, scaling), "unit": "steps/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": K,
+                "call": "muon_step_host (C ABI: host gradients in, host weights out)",
+                "copies": "one pinned H2D slab and one D2H slab per step inside each call; %d "
+                          "streams in rotation, step k waiting on step k-1's compute event" % n}
     e0.record(main)
     for k in range(K):
         b = k % 2

@@ -175,6 +175,29 @@ mao_status muon_step(const mao_mat* W, const mao_mat* M, const mao_mat* G, const
                      size_t workspace_bytes, void* stream);
 
 /*
+ * muon_step with the data on the host: the gradients come in from host memory and the new
+ * weights go back to it, all enqueued on `stream` (no counterpart on the pages: the
+ * end-to-end form of the step a training loop calls with host-resident gradients). In
+ * stream order:
+ *   1. g_bytes bytes from g_host (host, preferably pinned) to g_dev (device);
+ *   2. if wait_event is not NULL, the stream waits for it (a cudaEvent_t);
+ *   3. muon_step(W, M, G, W_out, ...) exactly as that call (G must lie in g_dev's bytes);
+ *   4. if record_event is not NULL, it is recorded (a cudaEvent_t);
+ *   5. w_bytes bytes from w_dev (device: the new weights, W_out's or W's storage) to w_host.
+ * Byte counts may be 0 (that copy is skipped). The events let a caller alternate two streams
+ * so that one step's copies overlap its neighbours' compute: step k waits for the event
+ * step k-1 recorded after its compute. Argument errors of muon_step, and a NULL buffer for a
+ * non-zero copy, are reported before anything is enqueued; a failed copy returns
+ * MAO_ERR_CUDA.
+ */
+mao_status muon_step_host(const mao_mat* W, const mao_mat* M, const mao_mat* G,
+                          const mao_mat* W_out, int32_t batch, float mu, float lr, int32_t steps,
+                          const float* coeffs, int32_t coeff_stride, float eps, int32_t compute,
+                          void* workspace, size_t workspace_bytes, const void* g_host,
+                          void* g_dev, size_t g_bytes, void* w_host, const void* w_dev,
+                          size_t w_bytes, void* stream, void* wait_event, void* record_event);
+
+/*
  * One whole Sign-Muon step in one call ([SignMuon] §2 "Fluxo Algorítmico", steps 1-4, with
  * the 1-bit all-gather variant; on one GPU the W_n workers' packed buffers already sit in
  * the all-gather layout): the four stages of the calls above, in order on `stream`,

@@ -9,6 +9,7 @@ Functions (same names as the C ABI):
   ns_workspace_bytes(X, compute)                     workspace size for ns_orthogonalize
   ns_orthogonalize(inp, out, steps, coeffs, ...)     Newton–Schulz polar factor (+ packed signs)
   muon_step(W, M, G, mu, lr, ...)                    momentum + Newton–Schulz + update, fused
+  muon_step_host(W, M, G, mu, lr, g_host, ...)      muon_step with host gradients / weights
   sign_muon_step(W, M, G, words, vote, mu, lr, ...)  momentum + NS signs + vote + update
   ns_orthogonalize_blockwise(inp, out, block, ...)   Newton–Schulz of every block on its own
   sign_pack_bits(U, bits)                            sign + 1-bit pack
@@ -164,6 +165,34 @@ def muon_step(W, M, G, mu, lr, steps=5, coeffs=QUINTIC, eps=1e-7, compute="bf16"
                          int(steps), carr, stride, float(eps), _COMPUTE[compute],
                          ctypes.c_void_p(ws.data_ptr()), ws.numel(), _stream(stream))
     _abi.check("muon_step", st)
+
+
+def muon_step_host(W, M, G, mu, lr, g_host, g_dev, w_host, w_dev, steps=5, coeffs=QUINTIC,
+                   eps=1e-7, compute="bf16", ws=None, W_out=None, stream=None, wait_event=None,
+                   record_event=None):
+    """muon_step with host data: g_host (pinned CPU tensor) is copied into g_dev (the device
+    tensor whose storage holds G) before the step, and w_dev (the device tensor holding the
+    new weights) into w_host (pinned CPU tensor) after it, all on `stream`; wait_event /
+    record_event (torch.cuda.Event) order the step's compute across streams."""
+    Ws, Ms, Gs = _as_list(W), _as_list(M), _as_list(G)
+    Wo = _as_list(W_out) if W_out is not None else None
+    if g_host.is_cuda or w_host.is_cuda or not g_dev.is_cuda or not w_dev.is_cuda:
+        raise ValueError("g_host / w_host must be host tensors and g_dev / w_dev device tensors")
+    gb = g_host.numel() * g_host.element_size()
+    wb = w_dev.numel() * w_dev.element_size()
+    if g_dev.numel() * g_dev.element_size() != gb or w_host.numel() * w_host.element_size() != wb:
+        raise ValueError("host and device buffers of different sizes")
+    carr, stride = _coeff_args(coeffs, steps)
+    if ws is None:
+        ws = workspace(Ms, compute, Ms[0].device)
+    ev = lambda e: ctypes.c_void_p(e.cuda_event if e is not None else None)  # noqa: E731
+    st = lib().muon_step_host(
+        _mats(Ws), _mats(Ms), _mats(Gs), _mats(Wo) if Wo is not None else None, len(Ws),
+        float(mu), float(lr), int(steps), carr, stride, float(eps), _COMPUTE[compute],
+        ctypes.c_void_p(ws.data_ptr()), ws.numel(), ctypes.c_void_p(g_host.data_ptr()),
+        ctypes.c_void_p(g_dev.data_ptr()), gb, ctypes.c_void_p(w_host.data_ptr()),
+        ctypes.c_void_p(w_dev.data_ptr()), wb, _stream(stream), ev(wait_event), ev(record_event))
+    _abi.check("muon_step_host", st)
 
 
 def sign_muon_step(W, M, G, words, vote, mu, lr, steps=5, coeffs=QUINTIC, eps=1e-7,

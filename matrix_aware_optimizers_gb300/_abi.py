@@ -27,6 +27,7 @@ EXPORTS = (
     "ns_workspace_bytes",
     "ns_orthogonalize",
     "muon_step",
+    "muon_step_host",
     "sign_muon_step",
     "ns_orthogonalize_noalloc",
     "ns_noalloc_workspace_bytes",
@@ -104,6 +105,11 @@ def load():
         P(MaoMat), P(MaoMat), P(MaoMat), P(MaoMat), ctypes.c_int32, ctypes.c_float, ctypes.c_float,
         ctypes.c_int32, P(ctypes.c_float), ctypes.c_int32, ctypes.c_float, ctypes.c_int32, vp,
         ctypes.c_size_t, vp]
+    lib.muon_step_host.restype = ctypes.c_int
+    lib.muon_step_host.argtypes = [
+        P(MaoMat), P(MaoMat), P(MaoMat), P(MaoMat), ctypes.c_int32, ctypes.c_float, ctypes.c_float,
+        ctypes.c_int32, P(ctypes.c_float), ctypes.c_int32, ctypes.c_float, ctypes.c_int32, vp,
+        ctypes.c_size_t, vp, vp, ctypes.c_size_t, vp, vp, ctypes.c_size_t, vp, vp, vp]
     lib.sign_muon_step.restype = ctypes.c_int
     lib.sign_muon_step.argtypes = [
         P(MaoMat), P(MaoMat), P(MaoMat), ctypes.c_int32, vp, ctypes.c_int64, vp, ctypes.c_float,

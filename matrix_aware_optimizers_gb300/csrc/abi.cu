@@ -152,10 +152,14 @@ mao_status ns_orthogonalize(const mao_mat* in, const mao_mat* out, int32_t batch
                 workspace_bytes, static_cast<cudaStream_t>(stream));
 }
 
-mao_status muon_step(const mao_mat* W, const mao_mat* M, const mao_mat* G, const mao_mat* W_out,
-                     int32_t batch, float mu, float lr, int32_t steps, const float* coeffs,
-                     int32_t coeff_stride, float eps, int32_t compute, void* workspace,
-                     size_t workspace_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+// Argument checks of muon_step (and muon_step_host): MAO_OK when the step may be enqueued.
+mao_status muon_step_check(const mao_mat* W, const mao_mat* M, const mao_mat* G,
+                           const mao_mat* W_out, int32_t batch, float mu, float lr,
+                           int32_t steps, const float* coeffs, int32_t coeff_stride, float eps,
+                           int32_t compute, const void* workspace, size_t workspace_bytes) {
   if (!W || !M || !G || batch < 1 || steps < 1 || steps > 64 || !coeffs) return MAO_ERR_INVALID_ARG;
   if (coeff_stride != 0 && coeff_stride != 3) return MAO_ERR_INVALID_ARG;
   if (!std::isfinite(eps) || eps < 0.0f || !std::isfinite(mu) || !std::isfinite(lr))
@@ -183,9 +187,50 @@ mao_status muon_step(const mao_mat* W, const mao_mat* M, const mao_mat* G, const
   if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0) return MAO_ERR_MISALIGNED;
   if (device_cc() / 10 != 10) return MAO_ERR_UNSUPPORTED;
   if (workspace_bytes < ns_workspace_size(M, batch, compute)) return MAO_ERR_WORKSPACE;
+  return MAO_OK;
+}
+}  // namespace
+
+extern "C" {
+
+mao_status muon_step(const mao_mat* W, const mao_mat* M, const mao_mat* G, const mao_mat* W_out,
+                     int32_t batch, float mu, float lr, int32_t steps, const float* coeffs,
+                     int32_t coeff_stride, float eps, int32_t compute, void* workspace,
+                     size_t workspace_bytes, void* stream) {
+  const mao_status st = muon_step_check(W, M, G, W_out, batch, mu, lr, steps, coeffs,
+                                        coeff_stride, eps, compute, workspace, workspace_bytes);
+  if (st != MAO_OK) return st;
   const NsFuse fuse{G, W_out ? W : nullptr, mu, lr};
   return ns_run(M, W_out ? W_out : W, batch, steps, coeffs, coeff_stride, eps, compute, nullptr,
                 workspace, workspace_bytes, static_cast<cudaStream_t>(stream), &fuse);
+}
+
+mao_status muon_step_host(const mao_mat* W, const mao_mat* M, const mao_mat* G,
+                          const mao_mat* W_out, int32_t batch, float mu, float lr, int32_t steps,
+                          const float* coeffs, int32_t coeff_stride, float eps, int32_t compute,
+                          void* workspace, size_t workspace_bytes, const void* g_host,
+                          void* g_dev, size_t g_bytes, void* w_host, const void* w_dev,
+                          size_t w_bytes, void* stream, void* wait_event, void* record_event) {
+  if ((g_bytes && (!g_host || !g_dev)) || (w_bytes && (!w_host || !w_dev)))
+    return MAO_ERR_INVALID_ARG;
+  mao_status st = muon_step_check(W, M, G, W_out, batch, mu, lr, steps, coeffs, coeff_stride,
+                                  eps, compute, workspace, workspace_bytes);
+  if (st != MAO_OK) return st;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (g_bytes && cudaMemcpyAsync(g_dev, g_host, g_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
+    return MAO_ERR_CUDA;
+  if (wait_event &&
+      cudaStreamWaitEvent(s, static_cast<cudaEvent_t>(wait_event), 0) != cudaSuccess)
+    return MAO_ERR_CUDA;
+  const NsFuse fuse{G, W_out ? W : nullptr, mu, lr};
+  st = ns_run(M, W_out ? W_out : W, batch, steps, coeffs, coeff_stride, eps, compute, nullptr,
+              workspace, workspace_bytes, s, &fuse);
+  if (st != MAO_OK) return st;
+  if (record_event && cudaEventRecord(static_cast<cudaEvent_t>(record_event), s) != cudaSuccess)
+    return MAO_ERR_CUDA;
+  if (w_bytes && cudaMemcpyAsync(w_host, w_dev, w_bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return MAO_ERR_CUDA;
+  return MAO_OK;
 }
 
 mao_status sign_muon_step(const mao_mat* W, const mao_mat* M, const mao_mat* G,

@@ -150,3 +150,56 @@ def test_sign_muon_step_equals_composed_calls(cuda, shape, dt, compute):
     # and the vote against the oracle's vote of these words
     w = words2[:, :nw].cpu().numpy().view(np.uint32)
     assert np.array_equal(vote1[:nw].cpu().numpy().view(np.uint32), oracle.majority_vote(w, R * C))
+
+
+def test_muon_step_host_equals_muon_step(cuda):
+    """muon_step_host (host gradients in, host weights out, through the C ABI) against
+    muon_step on device data: M and W bit for bit, and the host copy of W' equal to the
+    device result; two calls on two streams ordered by the events."""
+    g = torch.Generator()
+    g.manual_seed(31)
+    shapes = [(256, 640), (640, 256), (384, 384)]
+    W, M, G = _inputs(g, shapes, "bf16", "bf16", "bf16", cuda)
+    # gradients in one device slab and one pinned host slab
+    sizes = [r * c for r, c in shapes]
+    g_dev = torch.empty(sum(sizes), dtype=torch.bfloat16, device=cuda)
+    G_views, o = [], 0
+    for (r, c), n in zip(shapes, sizes):
+        G_views.append(g_dev[o:o + n].view(r, c))
+        o += n
+    g_host = torch.cat([x.reshape(-1).cpu() for x in G]).pin_memory()
+    w_dev = torch.empty(sum(sizes), dtype=torch.bfloat16, device=cuda)
+    W_out, o = [], 0
+    for (r, c), n in zip(shapes, sizes):
+        W_out.append(w_dev[o:o + n].view(r, c))
+        o += n
+    w_host = torch.empty(sum(sizes), dtype=torch.bfloat16).pin_memory()
+    M1 = [m.clone() for m in M]
+    s0, s1 = torch.cuda.Stream(), torch.cuda.Stream()
+    ev0, ev1 = torch.cuda.Event(), torch.cuda.Event()
+    ev0.record(s0)
+    ev1.record(s1)
+    s0.wait_stream(torch.cuda.current_stream())
+    s1.wait_stream(torch.cuda.current_stream())
+    # step 1 on s0 (W -> W_out), step 2 on s1 (W_out -> W) after step 1's compute
+    W1 = [w.clone() for w in W]
+    mao.muon_step_host(W1, M1, G_views, 0.95, 0.02, g_host, g_dev, w_host, w_dev, W_out=W_out,
+                       stream=s0, record_event=ev0)
+    mao.muon_step_host(W_out, M1, G_views, 0.95, 0.02, g_host, g_dev, w_host, w_dev, W_out=W1,
+                       stream=s1, wait_event=ev0, record_event=ev1)
+    torch.cuda.synchronize()
+    mao.sync_status()
+    # the same two steps on device data
+    W2 = [w.clone() for w in W]
+    M2 = [m.clone() for m in M]
+    mao.muon_step(W2, M2, G, 0.95, 0.02)
+    first = [w.clone() for w in W2]
+    mao.muon_step(W2, M2, G, 0.95, 0.02)
+    mao.sync_status()
+    for a, b in zip(M1, M2):
+        assert torch.equal(a, b)
+    for a, b in zip(W1, W2):
+        assert torch.equal(a, b)
+    # the host copy holds the first call's W' (the second call's copy reads w_dev, which
+    # still holds step 1's output: step 2 wrote W1)
+    assert torch.equal(w_host, torch.cat([x.reshape(-1).cpu() for x in first]))
