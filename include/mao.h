@@ -434,6 +434,16 @@ enum {
 };
 int64_t mao_launch_count(void);
 mao_status mao_profile_begin(int32_t max_launches);
+/*
+ * mao_profile_span_begin / mao_profile_span_end: as mao_profile_begin / mao_profile_end, but
+ *   one event pair per Newton–Schulz call on the tensor cores (ns_orthogonalize, muon_step,
+ *   ...): recorded before its first product launch and after its last, so the products keep
+ *   overlapping one another's set-up (programmatic dependent launch) while they are timed.
+ *   Returns the number of recorded spans and their durations in milliseconds. Independent of
+ *   the per-launch session; use one of them at a time.
+ */
+mao_status mao_profile_span_begin(int32_t max_spans);
+int32_t mao_profile_span_end(float* ms_out, int32_t max_out);
 int32_t mao_profile_end(float* ms_out, int32_t max_out);
 int32_t mao_profile_end_tagged(float* ms_out, int32_t* tags_out, int32_t max_out);
 

@@ -420,3 +420,18 @@ def profile_end_tagged(max_out=1 << 20):
     if n < 0:
         raise MaoError("mao_profile_end_tagged", _abi.MAO_ERR_CUDA)
     return [(buf[i], PROFILE_TAGS.get(tags[i], str(tags[i]))) for i in range(min(n, max_out))]
+
+
+def profile_span_begin(max_spans):
+    """Record one CUDA event pair around each Newton–Schulz call's run of tensor-core products
+    (benchmarking; the products keep overlapping one another's set-up)."""
+    _abi.check("mao_profile_span_begin", lib().mao_profile_span_begin(int(max_spans)))
+
+
+def profile_span_end(max_out=1 << 16):
+    """Stop recording; returns the recorded spans in milliseconds."""
+    buf = (ctypes.c_float * max_out)()
+    n = lib().mao_profile_span_end(buf, max_out)
+    if n < 0:
+        raise MaoError("mao_profile_span_end", _abi.MAO_ERR_CUDA)
+    return [buf[i] for i in range(min(n, max_out))]

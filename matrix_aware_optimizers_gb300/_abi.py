@@ -45,6 +45,8 @@ EXPORTS = (
     "mao_sync_status",
     "mao_launch_count",
     "mao_profile_begin",
+    "mao_profile_span_begin",
+    "mao_profile_span_end",
     "mao_profile_end",
     "mao_profile_end_tagged",
 )
@@ -157,6 +159,10 @@ def load():
     lib.mao_launch_count.argtypes = []
     lib.mao_profile_begin.restype = ctypes.c_int
     lib.mao_profile_begin.argtypes = [ctypes.c_int32]
+    lib.mao_profile_span_begin.restype = ctypes.c_int
+    lib.mao_profile_span_begin.argtypes = [ctypes.c_int32]
+    lib.mao_profile_span_end.restype = ctypes.c_int32
+    lib.mao_profile_span_end.argtypes = [P(ctypes.c_float), ctypes.c_int32]
     lib.mao_profile_end.restype = ctypes.c_int32
     lib.mao_profile_end.argtypes = [P(ctypes.c_float), ctypes.c_int32]
     lib.mao_profile_end_tagged.restype = ctypes.c_int32

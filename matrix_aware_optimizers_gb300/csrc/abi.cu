@@ -82,6 +82,21 @@ void profile_after_launch(cudaStream_t stream) {
   }
 }
 
+namespace {
+Profile g_span;  // event pairs around whole runs of tensor-core products
+}  // namespace
+
+void profile_span_begin(cudaStream_t stream) {
+  if (g_span.on && g_span.used < g_span.cap) cudaEventRecord(g_span.ev[2 * g_span.used], stream);
+}
+
+void profile_span_end(cudaStream_t stream) {
+  if (g_span.on && g_span.used < g_span.cap) {
+    cudaEventRecord(g_span.ev[2 * g_span.used + 1], stream);
+    ++g_span.used;
+  }
+}
+
 }  // namespace mao
 
 using namespace mao;
@@ -366,6 +381,41 @@ mao_status mao_profile_begin(int32_t max_launches) {
   g_prof.used = 0;
   g_prof.on = true;
   return MAO_OK;
+}
+
+mao_status mao_profile_span_begin(int32_t max_spans) {
+  if (max_spans < 1 || max_spans > (1 << 20) || g_span.on) return MAO_ERR_INVALID_ARG;
+  g_span.ev.assign(size_t(2) * max_spans, nullptr);
+  for (auto& e : g_span.ev) {
+    if (cudaEventCreate(&e) != cudaSuccess) {
+      for (auto& f : g_span.ev)
+        if (f) cudaEventDestroy(f);
+      g_span.ev.clear();
+      return MAO_ERR_CUDA;
+    }
+  }
+  g_span.cap = max_spans;
+  g_span.used = 0;
+  g_span.on = true;
+  return MAO_OK;
+}
+
+int32_t mao_profile_span_end(float* ms_out, int32_t max_out) {
+  if (!g_span.on) return 0;
+  g_span.on = false;
+  const int32_t n = g_span.used;
+  bool ok = true;
+  for (int32_t i = 0; i < n; ++i) {
+    float ms = 0.0f;
+    if (cudaEventSynchronize(g_span.ev[2 * i + 1]) != cudaSuccess ||
+        cudaEventElapsedTime(&ms, g_span.ev[2 * i], g_span.ev[2 * i + 1]) != cudaSuccess)
+      ok = false;
+    if (ms_out && i < max_out) ms_out[i] = ms;
+  }
+  for (auto& e : g_span.ev) cudaEventDestroy(e);
+  g_span.ev.clear();
+  g_span.used = 0;
+  return ok ? n : -1;
 }
 
 int32_t mao_profile_end(float* ms_out, int32_t max_out) {

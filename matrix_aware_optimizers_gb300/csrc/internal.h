@@ -43,6 +43,11 @@ void count_launch();
 // other tags name the Dion CUDA-core kernels (mao_profile_end_tagged).
 void profile_before_launch(cudaStream_t stream, int tag = 0);
 void profile_after_launch(cudaStream_t stream);
+// Optional timing of whole runs of tensor-core products (mao_profile_span_begin): one event
+// before the first product of a Newton–Schulz call and one after its last, so the products
+// keep overlapping one another's set-up (programmatic dependent launch) while timed.
+void profile_span_begin(cudaStream_t stream);
+void profile_span_end(cudaStream_t stream);
 
 // Reads and clears the device error word of the tensor-core kernels (after a stream sync).
 mao_status tc_read_and_clear_error(cudaStream_t stream);

@@ -766,6 +766,7 @@ mao_status ns_run(const mao_mat* in, const mao_mat* out, int32_t batch, int32_t 
   if (cudaGetLastError() != cudaSuccess) return MAO_ERR_CUDA;
 
   // ---- the iterations, for rounds of up to eight shape groups
+  if (tcpath) profile_span_begin(stream);
   const Buffers buf{ws, &plan};
   const int max_groups = tcpath ? tc::MAX_GROUPS : kSimtMaxGroups;
   for (size_t g0 = 0; g0 < plan.groups.size(); g0 += max_groups) {
@@ -793,6 +794,7 @@ mao_status ns_run(const mao_mat* in, const mao_mat* out, int32_t batch, int32_t 
       }
     }
   }
+  if (tcpath) profile_span_end(stream);
   return MAO_OK;
 }
 

@@ -766,7 +766,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads(MODE), 1)
     const CUtensorMap* map = (lane & 1) ? &G.tmB : &G.tmA;
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
   }
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  // The epilogue warps read global memory written by earlier kernels, so they wait here.
+  // The MMA warp touches only shared memory and TMEM, filled by the producer's loads, and
+  // the producer waits just before its first load: both get their first tile's barriers
+  // ready while the previous kernel finishes.
+  if (warp >= 2) asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const uint64_t limit = p.timeout_ns;
 #ifdef MAO_TC_TRACE
@@ -778,6 +782,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads(MODE), 1)
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
+    bool dep_done = false;  // griddepcontrol.wait passed (before the first global access)
     uint32_t armed = 0, armed_phase = 0;  // leader: stages armed at least once, their phase
     for (int tile = pair; ok && tile < p.total_tiles; tile += npairs) {
       Tile t;
@@ -801,6 +806,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads(MODE), 1)
         // of the caller's matrix a tile or two from now, is the bottleneck. Have L2 fetch
         // them while the operands load. With longer products the prefetched rows displace
         // operand panels from L2 and the prefetch does not pay.
+        if (!dep_done) {
+          asm volatile("griddepcontrol.wait;" ::: "memory");
+          dep_done = true;
+        }
         const OutEntry oe = p.out_table[G.slot0 + t.z];
         if (oe.flags & OUT_VEC) {
           const int es = oe.dtype == MAO_BF16 ? 2 : 4;
@@ -837,6 +846,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads(MODE), 1)
         if (!okw) {
           ok = false;
           break;
+        }
+        if (!dep_done) {  // the first load reads what the previous kernel wrote
+          asm volatile("griddepcontrol.wait;" ::: "memory");
+          dep_done = true;
         }
         if (active && !(share && !is_a)) {
           const uint32_t fb = mapa_shared(smem_u32(&full_bar[stage]), 0);
