@@ -90,6 +90,9 @@ def parse_args(argv=None):
     ap.add_argument("--unfused", action="store_true",
                     help="Muon workloads: momentum, Newton-Schulz and update as three calls "
                          "instead of one muon_step call")
+    ap.add_argument("--compute", default=None, choices=["bf16", "f32"],
+                    help="Newton-Schulz arithmetic (default: the workload's): f32 is the "
+                         "accuracy path (fp32 storage, FFMA products)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-per-config", action="store_true",
@@ -938,18 +941,22 @@ def measure(opts, wl, dev, world, rank, local, block, K, Wu, barrier, max_over_r
         traffic = read_traffic(wl)
         if traffic is not None and dplan is None:
             roof["traffic"] = traffic
-    elif wl.compute == "f32" and kernel_ms.get("ns_small"):
-        # the one-launch fp32 Newton–Schulz: FFMA work against the fp32 CUDA-core peak
-        small_ms = kernel_ms["ns_small"]  # per step
+    elif wl.compute == "f32" and (kernel_ms.get("ns_small") or step.whole_call):
+        # the fp32 Newton–Schulz: FFMA work against the fp32 CUDA-core peak (the one-launch
+        # kernel's own time, else the Newton–Schulz stage's or the whole call's)
+        small_ms = kernel_ms.get("ns_small") or st_ns  # per step
         gflop = dense_flops(shapes, wl.steps) / (small_ms / 1000.0) / 1e12
         peak = fp32_peak_tflops(dev)
-        roof = {"kernel": "ns_small_kernel", "bound": "alu", "achieved": gflop, "peak": peak,
+        roof = {"kernel": "ns_small_kernel" if kernel_ms.get("ns_small") else
+                "ns_simt_kernel (timed with the rest of the call)",
+                "bound": "alu", "achieved": gflop, "peak": peak,
                 "unit": "TFLOP/s", "frac": gflop / peak, "traffic": None,
                 "peak_source": "derived: SMs x 128 fp32 FMA lanes x 2 flops x max SM clock",
                 "work": "dense flops 4m^2n + 2m^3 per iteration", "avg_launch_ms": small_ms,
                 "launches": int(round(len([1 for _, t in tagged if t == "ns_small"]) / reps_tc)),
-                "note": "one cluster of 8 CTAs per matrix: a latency-bound launch on %d of the "
-                        "GPU's SMs" % (8 * len(shapes))}
+                "note": ("one cluster of 8 CTAs per matrix: a latency-bound launch on %d of "
+                         "the GPU's SMs" % (8 * len(shapes))) if kernel_ms.get("ns_small") else
+                        "64x64 FFMA tiles, one launch per product"}
     else:
         mom_b, upd_b = stage_bytes(wl, step)
         gbs = (mom_b + (upd_b or 0)) / ((st_mom + (st_upd if upd_b else 0)) / 1000.0) / 1e9
@@ -1030,6 +1037,11 @@ def main():
     args = parse_args()
     from matrix_aware_optimizers_gb300 import workloads
     wl = workloads.workload(args.config)
+    if args.compute is not None and args.compute != wl.compute:
+        import dataclasses
+        if wl.kind == "dion":
+            sys.exit("--compute applies to the Muon and Sign-Muon workloads")
+        wl = dataclasses.replace(wl, compute=args.compute)
     block = None
     if args.block:
         block = tuple(int(v) for v in args.block.lower().split("x"))

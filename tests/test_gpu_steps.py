@@ -215,3 +215,33 @@ def test_config6_dion_full(cuda):
         X0 = host["W"][i].astype(np.float64)
         err_x = np.linalg.norm(to_np(step.W[i]) - out["X"])
         assert err_x <= TOL["bf16"] * np.linalg.norm(X0 - out["X"]) + 1.01 * u * np.linalg.norm(out["X"]), i
+
+
+def test_config3_fp32_path_meets_sign_criterion(cuda, record_property):
+    """The 4096^2, 8-worker Sign-Muon step on the fp32 accuracy path (compute = f32, the same
+    bf16 inputs): worker 0's signs meet the criterion as stated for the step (>= 99.9%
+    agreement with the fp64 oracle's U, every flip where |U| < 1e-3 rms(U)), and the vote and
+    update stay bit-exact on the GPU's own words ([SignMuon] §2 steps 2-4)."""
+    import dataclasses
+    wl = dataclasses.replace(workloads.workload(3), compute="f32")
+    step, host, M_after, U, W_before = _run_step(wl, cuda, keep_u=True)
+    R, C = wl.shapes[0]
+    n = R * C
+    u_ref = oracle.newton_schulz(to_np(M_after[0]), wl.steps, wl.coeffs, wl.eps)
+    u_gpu = to_np(U[0])
+    err = rel_fro(u_gpu, u_ref)
+    assert err <= TOL["f32"], err
+    bits0 = bits_of(words_np(step.bits[0]), n)
+    frac = check_sign_agreement(u_gpu, u_ref, bits0, strict_rms=1e-3)
+    agree, flips, share_small = sign_criterion(u_ref, bits0)
+    print("config 3, fp32 path, worker 0: U rel. Frobenius error %.3e; sign agreement %.6f "
+          "(%d flips); share of flips with |U| < 1e-3 rms(U): %.3f" % (err, agree, flips, share_small))
+    record_property("sign_agreement_f32", agree)
+    assert agree >= AGREE["f32"] and frac == agree
+    assert share_small == 1.0
+    nw = (n + 31) // 32
+    words = words_np(step.words)[:, :nw]
+    vote = words_np(step.vote)[:nw]
+    assert np.array_equal(vote, oracle.majority_vote(words, n))
+    S_bar = oracle.unpack_signs(vote, n).reshape(R, C)
+    assert np.array_equal(to_np(step.W[0]), oracle.apply_update(to_np(W_before[0]), S_bar, wl.lr, "bf16"))
