@@ -185,6 +185,8 @@ def muon_step_host(W, M, G, mu, lr, g_host, g_dev, w_host, w_dev, steps=5, coeff
     carr, stride = _coeff_args(coeffs, steps)
     if ws is None:
         ws = workspace(Ms, compute, Ms[0].device)
+    if record_event is not None and not record_event.cuda_event:
+        record_event.record(stream)  # a torch event exists only once recorded
     ev = lambda e: ctypes.c_void_p(e.cuda_event if e is not None else None)  # noqa: E731
     st = lib().muon_step_host(
         _mats(Ws), _mats(Ms), _mats(Gs), _mats(Wo) if Wo is not None else None, len(Ws),
