@@ -308,116 +308,239 @@ __device__ __forceinline__ uint32_t bf16_pair(float a, float b) {
 }
 
 
-// Factors the 32 x 32 block Ad = L L^T in registers (lane = row), column by column in the
-// left-looking order: for column j, lane j (whose row of L is final up to column j - 1)
-// puts that row into `row` (shared memory), every lane forms the dot product of its own row
-// with it from 16-byte broadcast reads (four partial sums), and the pivot
-// p = A_jj - sum_k L_jk^2 comes from lane j; L_ij = (A_ij - sum_k L_ik L_jk) / L_jj. One
-// broadcast of a row per column replaces the shuffles of every multiplier of a
-// right-looking step. Writes L back (zeros above the diagonal) and 1 / L_jj to rinv[j]; the
-// pivot's reciprocal square root comes from rsqrtf (L_jj = p rsqrt(p)). A pivot that is not
-// positive is replaced by 1e-30 and reported. Not inlined: inlined into the kernel, its a[]
-// array lands in local memory.
-__device__ __noinline__ bool chol32(float* Ad, float* rinv, float* row, int lane) {
-  float a[32];
+// Factors the 32 x 32 diagonal block Ad = L L^T and forms D = L^-1 alongside, in registers:
+// lane i holds row i of A (which becomes row i of L) and column i of D. Right-looking: at
+// pivot j the pivot p = A_jj comes from lane j by a shuffle, every lane forms its
+// L_ij = A_ij / sqrt(p) (lane j: sqrt(p) = p rsqrt(p)) and puts it into `col` (two
+// alternating buffers in shared memory, lane i at position i - j + 31, so that the entries
+// below the pivot start on a 16-byte boundary), then reads them back with 16-byte broadcast
+// reads to update its row, A_ik -= L_ij L_kj for k > j, and its column c of D by forward
+// substitution, D_jc = rhs_jc / L_jj and rhs_kc -= L_kj D_jc for k > j. One shuffle and one
+// column broadcast per pivot serve both the factor and its inverse. The registers hold only
+// the entries at and past the current pivot, moved down one place by each pivot's update,
+// so the pivot loop is the same code for every j and stays rolled (its instructions come
+// from the instruction cache after the first pivot, not from memory). Row j of D is written
+// to Ad at pivot j (zeros above the diagonal). A pivot that is not positive is replaced by
+// 1e-30 and reported.
+__device__ __noinline__ bool chol_inv32(float* Ad, float* col, int lane) {
+  float a[32], x[32];  // a[k]: A_lane,j+k; x[k]: rhs_j+k,lane (at pivot j)
 #pragma unroll
   for (int q = 0; q < 32; q += 4) {
     const float4 v = ld4(Ad + lane * kLd + q);
-    a[q] = v.x;
-    a[q + 1] = v.y;
-    a[q + 2] = v.z;
-    a[q + 3] = v.w;
+    a[q] = q <= lane ? v.x : 0.0f;
+    a[q + 1] = q + 1 <= lane ? v.y : 0.0f;
+    a[q + 2] = q + 2 <= lane ? v.z : 0.0f;
+    a[q + 3] = q + 3 <= lane ? v.w : 0.0f;
   }
+#pragma unroll
+  for (int k = 0; k < 32; ++k) x[k] = k == lane ? 1.0f : 0.0f;
+  __syncwarp();  // every row is in registers before row 0 of D overwrites it
   bool bad = false;
-  float my_inv = 0.0f;
-#pragma unroll
+#pragma unroll 1
   for (int j = 0; j < 32; ++j) {
-    float v = a[j];
-    if (j > 0) {
-      if (lane == j) {
-#pragma unroll
-        for (int q = 0; q < j; q += 4)
-          *reinterpret_cast<float4*>(row + q) = make_float4(a[q], a[q + 1], a[q + 2], a[q + 3]);
-      }
-      __syncwarp();
-      float s[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll
-      for (int q = 0; q < j; q += 4) {
-        const float4 r = ld4(row + q);
-        s[0] = __fmaf_rn(a[q], r.x, s[0]);
-        if (q + 1 < j) s[1] = __fmaf_rn(a[q + 1], r.y, s[1]);
-        if (q + 2 < j) s[2] = __fmaf_rn(a[q + 2], r.z, s[2]);
-        if (q + 3 < j) s[3] = __fmaf_rn(a[q + 3], r.w, s[3]);
-      }
-      v -= (s[0] + s[1]) + (s[2] + s[3]);
-      __syncwarp();  // the row is read by every lane before lane j + 1 overwrites it
-    }
-    float p = __shfl_sync(0xFFFFFFFFu, v, j);
+    float p = __shfl_sync(0xFFFFFFFFu, a[0], j);
     if (!(p > 0.0f)) {
       bad = true;
       p = 1e-30f;
     }
     const float inv = rsqrtf(p);
-    if (lane == j) my_inv = inv;
-    a[j] = lane == j ? p * inv : (lane > j ? v * inv : 0.0f);
-  }
+    const float d = x[0] * inv;  // D_j,lane
+    Ad[j * kLd + lane] = d;
+    const float l = lane > j ? a[0] * inv : (lane == j ? p * inv : 0.0f);
+    float* cb = col + 64 * (j & 1);
+    cb[lane - j + 31] = l;  // L_ij at cb[32 + (i - j - 1)]
+    __syncwarp();
+    float c[32];
 #pragma unroll
-  for (int q = 0; q < 32; ++q) Ad[lane * kLd + q] = q <= lane ? a[q] : 0.0f;
-  rinv[lane] = my_inv;
+    for (int q = 0; q < 32; q += 4) {
+      const float4 v = ld4(cb + 32 + q);
+      c[q] = v.x;
+      c[q + 1] = v.y;
+      c[q + 2] = v.z;
+      c[q + 3] = v.w;
+    }
+#pragma unroll
+    for (int k = 0; k < 31; ++k) a[k] = __fmaf_rn(-l, c[k], a[k + 1]);
+    a[31] = 0.0f;
+#pragma unroll
+    for (int k = 0; k < 31; ++k) x[k] = __fmaf_rn(-c[k], d, x[k + 1]);
+    x[31] = 0.0f;
+  }
   __syncwarp();
   return bad;
 }
 
-// In place: the lower 32 x 32 block L becomes D = L^-1 (lane = column of D, forward
-// substitution in registers with the reciprocals rinv of L's diagonal, four partial sums per
-// dot product, the rows of L read 16 bytes at a time); zeros above the diagonal.
-__device__ __forceinline__ void inv32(float* Ad, const float* rinv, int lane) {
-  float x[32];
+// L_IJ = A_IJ D_J^T (D_J = L_JJ^-1) for the rows [row0, row1) of block column J: warp w of
+// nw takes rows row0 + w, row0 + w + nw, ...; lane = column, the lane's row of D_J held in
+// registers across the rows.
+__device__ __forceinline__ void chol_panel(float* A, int J, int row0, int row1, int w, int nw, int lane) {
+  if (row0 + w >= row1) return;
+  const float* Dj = blk(A, J, J) + lane * kLd;
+  float4 d[8];
 #pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    float s[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+  for (int q = 0; q < 8; ++q) d[q] = ld4(Dj + 4 * q);
+  for (int row = row0 + w; row < row1; row += nw) {
+    float* Ap = blk(A, row >> 5, J) + (row & 31) * kLd;
+    float s0 = 0.0f, s1 = 0.0f;
 #pragma unroll
-    for (int k4 = 0; k4 < i; k4 += 4) {
-      const float4 l = ld4(Ad + i * kLd + k4);
-      const float lv[4] = {l.x, l.y, l.z, l.w};
-#pragma unroll
-      for (int u = 0; u < 4; ++u)
-        if (k4 + u < i) s[u] = __fmaf_rn(lv[u], x[k4 + u], s[u]);
+    for (int q = 0; q < 8; ++q) {
+      const float4 v = ld4(Ap + 4 * q);
+      s0 = __fmaf_rn(v.x, d[q].x, s0);
+      s1 = __fmaf_rn(v.y, d[q].y, s1);
+      s0 = __fmaf_rn(v.z, d[q].z, s0);
+      s1 = __fmaf_rn(v.w, d[q].w, s1);
     }
-    const float ri = rinv[i];
-    x[i] = i < lane ? 0.0f : (i == lane ? ri : -((s[0] + s[1]) + (s[2] + s[3])) * ri);
+    __syncwarp();
+    Ap[lane] = s0 + s1;
   }
-  __syncwarp();
+}
+
+// Rows r0 .. r0 + NR - 1 of A_IK -= L_IJ L_KJ^T (lane = column, the lane's row of L_KJ in
+// registers, rows of L_IJ by 16-byte broadcast reads).
+template <int NR>
+__device__ __forceinline__ void chol_update(float* A, int J, int I, int K, int r0, int lane) {
+  float4 lk[8];
+  const float* Lk = blk(A, K, J) + lane * kLd;
 #pragma unroll
-  for (int i = 0; i < 32; ++i) Ad[i * kLd + lane] = x[i];
-  __syncwarp();
+  for (int q = 0; q < 8; ++q) lk[q] = ld4(Lk + 4 * q);
+  const float* Li = blk(A, I, J) + r0 * kLd;
+  float* Ab = blk(A, I, K) + r0 * kLd;
+#pragma unroll
+  for (int tt = 0; tt < NR; ++tt) {
+    float s0 = 0.0f, s1 = 0.0f;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const float4 l = ld4(Li + tt * kLd + 4 * q);
+      s0 = __fmaf_rn(l.x, lk[q].x, s0);
+      s1 = __fmaf_rn(l.y, lk[q].y, s1);
+      s0 = __fmaf_rn(l.z, lk[q].z, s0);
+      s1 = __fmaf_rn(l.w, lk[q].w, s1);
+    }
+    Ab[tt * kLd + lane] -= s0 + s1;
+  }
+}
+
+// Block row K of W = L^-1 to global memory as the bf16 operand of the multiply P W^T on
+// the tensor cores: row j holds hi(W_j) | lo(W_j) | hi(W_j), ldr columns each,
+// lo = bf16(w - hi). Block (K, J) comes from Wr + J kBlk for J < K and is D_K = Dk for J = K;
+// zeros above the diagonal. With `last`, the rows past the 32 nb rows of the blocks follow as
+// the identity. Thread t of nt. Not inlined (one copy of the code for all block rows).
+__device__ __noinline__ void chol_write_w(const float* Wr, const float* Dk, __nv_bfloat16* Wsp, int K, int nb,
+                                             int ldr, bool last, int t, int nt) {
+  const int q8 = ldr / 8, nbw32 = 32 * nb;
+  const int j0 = 32 * K, j1 = last ? ldr : 32 * (K + 1);
+  for (int q = t; q < (j1 - j0) * q8; q += nt) {
+    const int dj = q / q8, j = j0 + dj, k0 = (q - dj * q8) * 8;
+    float w[8], lo[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int k = k0 + u;
+      float val;
+      if (j < nbw32 && k < nbw32) {
+        const int J = k >> 5;
+        const float* src = J < K ? Wr + J * kBlk : Dk;
+        val = J <= K && k <= j ? src[(j & 31) * kLd + (k & 31)] : 0.0f;
+      } else {
+        val = j == k ? 1.0f : 0.0f;
+      }
+      w[u] = val;
+      lo[u] = val - __bfloat162float(__float2bfloat16_rn(val));
+    }
+    const uint4 h = make_uint4(bf16_pair(w[0], w[1]), bf16_pair(w[2], w[3]), bf16_pair(w[4], w[5]),
+                               bf16_pair(w[6], w[7]));
+    const uint4 l = make_uint4(bf16_pair(lo[0], lo[1]), bf16_pair(lo[2], lo[3]), bf16_pair(lo[4], lo[5]),
+                               bf16_pair(lo[6], lo[7]));
+    __nv_bfloat16* row = Wsp + size_t(j) * 3 * ldr;
+    *reinterpret_cast<uint4*>(row + k0) = h;
+    *reinterpret_cast<uint4*>(row + ldr + k0) = l;
+    *reinterpret_cast<uint4*>(row + 2 * ldr + k0) = h;
+  }
+}
+
+// Rows r0 .. r0 + NR - 1 (NR a multiple of 8), column `lane`, of Out = scale Lft In
+// (+ Out with ACC), 32 x 32 blocks, eight rows at a time: In's column is read into
+// registers first and Lft's rows by 16-byte broadcast reads, eight independent sums per
+// lane. Out may be Lft with SYNC (the warp has read a group's rows before any lane writes
+// them); with LOWER, Lft is lower triangular and the products above its diagonal are
+// skipped.
+template <int NR, bool ACC, bool LOWER, bool SYNC>
+__device__ __forceinline__ void blk_rows(const float* Lft, const float* In, float* Out, int r0, float scale,
+                                         int lane) {
+  static_assert(NR % 8 == 0, "rows in groups of eight");
+  float v[32];
+#pragma unroll
+  for (int k = 0; k < 32; ++k) v[k] = In[k * kLd + lane];
+#pragma unroll 1
+  for (int g = r0; g < r0 + NR; g += 8) {
+    float o[8] = {};
+#pragma unroll
+    for (int q = 0; q < 32; q += 4) {
+      if (LOWER && q > g + 7) break;
+#pragma unroll
+      for (int t = 0; t < 8; ++t) {
+        const float4 l = ld4(Lft + (g + t) * kLd + q);
+        o[t] = __fmaf_rn(l.x, v[q], o[t]);
+        o[t] = __fmaf_rn(l.y, v[q + 1], o[t]);
+        o[t] = __fmaf_rn(l.z, v[q + 2], o[t]);
+        o[t] = __fmaf_rn(l.w, v[q + 3], o[t]);
+      }
+    }
+    if (SYNC) __syncwarp();
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+      float* out = Out + (g + t) * kLd + lane;
+      *out = ACC ? *out + scale * o[t] : scale * o[t];
+    }
+  }
+  if (SYNC) __syncwarp();
+}
+
+// Inverse step K, part 1, 2 or 3 (see the kernel below), one 8-row quarter of a block per
+// item; nb - 1 - K block rows lie below K. Not inlined: the loop over the block columns
+// and the last two steps share its code, which is then fetched from memory once.
+__device__ __noinline__ void chol_inv_item(float* A, float* Wr, int part, int K, int item, int lane) {
+  const int r0 = 8 * (item & 3), b = item >> 2;
+  if (part == 1) {  // item < 4 K: W_KJ = -D_K T_KJ into Wr
+    blk_rows<8, false, true, false>(blk(A, K, K), blk(A, K, b), Wr + b * kBlk, r0, -1.0f, lane);
+  } else if (part == 2) {  // item < 4 (nb - 1 - K) K: T_IJ += L_IK W_KJ
+    const int I = K + 1 + b / K, J = b % K;
+    blk_rows<8, true, false, false>(blk(A, I, K), Wr + J * kBlk, blk(A, I, J), r0, 1.0f, lane);
+  } else {  // item < 4 (nb - 1 - K): T_IK = L_IK D_K
+    const int I = K + 1 + b;
+    blk_rows<8, false, false, true>(blk(A, I, K), blk(A, K, K), blk(A, I, K), r0, 1.0f, lane);
+  }
 }
 
 // One CTA per slot: S = L L^T (blocked right-looking Cholesky, 32 x 32 blocks in shared
-// memory), then W = L^-1, written to e.Wsp as the split bf16 operand of the multiply P W^T.
-//   Cholesky, for each block column J: the panel below the diagonal becomes
-//   L_IJ = A_IJ D_J^T (one warp per row); block column J + 1 gets A_I,J+1 -= L_IJ L_J+1,J^T;
-//   then warp 0 factors the diagonal block J + 1 (chol32) and inverts it in place (inv32:
-//   the diagonal block then holds D = L_JJ^-1, which is all that later steps need of it)
-//   while the warps off warp 0's sub-partition update the remaining trailing blocks A_IK,
-//   J + 2 <= K <= I (one warp per 8-row quarter of a block, the lane's row of L_KJ in
-//   registers) and take inverse step J.
-//   Inverse step I (block row I of W, once row block I of L and D_I are final; W_JJ = D_J):
-//   T_J = sum_{K = J .. I-1} L_IK W_KJ for every J < I, then W_IJ = -D_I T_J in place of
-//   L_IJ (row block I of L is no longer needed once all T_J are formed).
-// S arrives in this block layout (the assemble kernel writes it so). Rows and columns past r are
-// the identity. A pivot that is not positive sets the device error word (P had dependent
-// columns).
+// memory) and W = L^-1, written to e.Wsp as the split bf16 operand of the multiply P W^T.
+// After block J's factorisation the diagonal block holds D_J = L_JJ^-1, which is all that
+// later steps need of it. W is formed right-looking as well: block (I, J) of the lower
+// triangle passes from A_IJ to L_IJ (panel) and then to the sum
+// T_IJ = sum_{K = J .. } L_IK W_KJ over the block rows K of W final so far (starting with
+// L_IJ D_J); W_IJ = -D_I T_IJ once all K < I have been added. Inverse step K, once block row
+// K of the sums and block column K of L are final:
+//   (1) W_KJ = -D_K T_KJ for J < K, into the row buffer Wr (block row K of W is then final
+//       and goes to global memory from there),
+//   (2) T_IJ += L_IK W_KJ for I > K, J < K,
+//   (3) T_IK = L_IK D_K for I > K (in place of L_IK, after (2) has read it).
+// For each block column J of the factorisation:
+//   critical path (all warps): block row J + 1 of the panel, L_J+1,J = A_J+1,J D_J^T, then
+//   the diagonal block A_J+1,J+1 -= L_J+1,J L_J+1,J^T; then warp 0 factors and inverts the
+//   diagonal block J + 1 (chol_inv32) while the warps off warp 0's sub-partition finish the
+//   panel (L_IJ for I >= J + 2), update the trailing blocks A_IK, J + 1 <= K <= I,
+//   I >= J + 2, and take inverse step J - 1 (all of it in items of eight rows).
+// The last two inverse steps run on all warps at the end. S arrives in this block layout
+// (the assemble kernel writes it so). Rows and columns past r are the identity. A pivot
+// that is not positive sets the device error word (P had dependent columns).
 __global__ void __launch_bounds__(kCholThreads, 1) dion_chol_kernel(const __grid_constant__ DionCommon c) {
   extern __shared__ __align__(16) float sm[];
-  __shared__ float rinv[32];
-  __shared__ __align__(16) float crow[32];  // chol32's broadcast row
+  __shared__ __align__(16) float col[128];  // chol_inv32's column broadcast (two buffers)
   const DionSlot& e = c.slots[blockIdx.x];
   const int r = c.r, ldr = c.ldr;
   const int nb = (r + 31) / 32;
   const int nlow = nb * (nb + 1) / 2;
-  float* A = sm;                  // nlow blocks
-  float* Tt = A + nlow * kBlk;    // nb - 1 blocks: T_J of the current block row
+  float* A = sm;                 // nlow blocks
+  float* Wr = A + nlow * kBlk;   // nb - 1 blocks: the block row of W of the current inverse step
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   constexpr int kWarps = kCholThreads / 32;
   constexpr int kHelpers = kWarps - kWarps / 4;  // warps with warp % 4 != 0
@@ -430,155 +553,85 @@ __global__ void __launch_bounds__(kCholThreads, 1) dion_chol_kernel(const __grid
   __syncthreads();
   for (int i = r + int(threadIdx.x); i < 32 * nb; i += kCholThreads)
     blk(A, i / 32, i / 32)[(i % 32) * kLd + (i % 32)] = 1.0f;
-  // factors and inverts diagonal block J (warp 0)
-  auto factor = [&](int J) {
-    float* Dj = blk(A, J, J);
-    if (chol32(Dj, rinv, crow, lane) && lane == 0) atomicOr(&g_dion_error, 1u);
-    inv32(Dj, rinv, lane);
-  };
-  // rows 8 quarter .. 8 quarter + 7 of A_IK -= L_IJ L_KJ^T
-  auto update = [&](int J, int I, int K, int quarter) {
-    float4 lk[8];
-    const float* Lk = blk(A, K, J) + lane * kLd;
-#pragma unroll
-    for (int q = 0; q < 8; ++q) lk[q] = ld4(Lk + 4 * q);
-    const float* Li = blk(A, I, J) + quarter * 8 * kLd;
-    float* Ab = blk(A, I, K) + quarter * 8 * kLd;
-#pragma unroll
-    for (int tt = 0; tt < 8; ++tt) {
-      float s0 = 0.0f, s1 = 0.0f;
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const float4 l = ld4(Li + tt * kLd + 4 * q);
-        s0 = __fmaf_rn(l.x, lk[q].x, s0);
-        s1 = __fmaf_rn(l.y, lk[q].y, s1);
-        s0 = __fmaf_rn(l.z, lk[q].z, s0);
-        s1 = __fmaf_rn(l.w, lk[q].w, s1);
-      }
-      Ab[tt * kLd + lane] -= s0 + s1;
-    }
-  };
-  // inverse step I on nw warps, this one numbered h; sync() separates its two phases
-  auto inverse_step = [&](int I, int h, int nw, auto sync) {
-    for (int item = h; item < 4 * I; item += nw) {
-      const int J = item >> 2, quarter = item & 3;
-      float acc[8] = {};
-      for (int K = J; K < I; ++K) {
-        const float* Wk = blk(A, K, J);  // W_KJ (D_J on the diagonal)
-        const float* Li = blk(A, I, K) + quarter * 8 * kLd;
-#pragma unroll 2
-        for (int q = 0; q < 32; q += 4) {
-          const float w0v = Wk[q * kLd + lane], w1v = Wk[(q + 1) * kLd + lane];
-          const float w2v = Wk[(q + 2) * kLd + lane], w3v = Wk[(q + 3) * kLd + lane];
-#pragma unroll
-          for (int tt = 0; tt < 8; ++tt) {
-            const float4 l = ld4(Li + tt * kLd + q);
-            acc[tt] = __fmaf_rn(l.x, w0v, acc[tt]);
-            acc[tt] = __fmaf_rn(l.y, w1v, acc[tt]);
-            acc[tt] = __fmaf_rn(l.z, w2v, acc[tt]);
-            acc[tt] = __fmaf_rn(l.w, w3v, acc[tt]);
-          }
-        }
-      }
-      float* T = Tt + J * kBlk + quarter * 8 * kLd;
-#pragma unroll
-      for (int tt = 0; tt < 8; ++tt) T[tt * kLd + lane] = acc[tt];
-    }
-    sync();
-    const float* Di = blk(A, I, I);
-    for (int item = h; item < 4 * I; item += nw) {
-      const int J = item >> 2, quarter = item & 3;
-      const float* T = Tt + J * kBlk;
-      const float* Dr = Di + quarter * 8 * kLd;
-      float acc[8] = {};
-#pragma unroll 2
-      for (int q = 0; q < 32; q += 4) {
-        const float t0 = T[q * kLd + lane], t1 = T[(q + 1) * kLd + lane];
-        const float t2 = T[(q + 2) * kLd + lane], t3 = T[(q + 3) * kLd + lane];
-#pragma unroll
-        for (int tt = 0; tt < 8; ++tt) {
-          const float4 d = ld4(Dr + tt * kLd + q);
-          acc[tt] = __fmaf_rn(d.x, t0, acc[tt]);
-          acc[tt] = __fmaf_rn(d.y, t1, acc[tt]);
-          acc[tt] = __fmaf_rn(d.z, t2, acc[tt]);
-          acc[tt] = __fmaf_rn(d.w, t3, acc[tt]);
-        }
-      }
-      float* Wb = blk(A, I, J) + quarter * 8 * kLd;
-#pragma unroll
-      for (int tt = 0; tt < 8; ++tt) Wb[tt * kLd + lane] = -acc[tt];
-    }
-  };
+  auto inv1 = [&](int K, int item) { chol_inv_item(A, Wr, 1, K, item, lane); };
+  auto inv2 = [&](int K, int item) { chol_inv_item(A, Wr, 2, K, item, lane); };
+  auto inv3 = [&](int K, int item) { chol_inv_item(A, Wr, 3, K, item, lane); };
   __syncthreads();
-  if (warp == 0) factor(0);
+  if (warp == 0 && chol_inv32(blk(A, 0, 0), col, lane) && lane == 0) atomicOr(&g_dion_error, 1u);
   __syncthreads();
-  for (int J = 0; J < nb; ++J) {
-    const float* Dj = blk(A, J, J);
-    for (int row = 32 * (J + 1) + warp; row < 32 * nb; row += kWarps) {
-      float* Ap = blk(A, row / 32, J) + (row % 32) * kLd;
-      float s0 = 0.0f, s1 = 0.0f;
-#pragma unroll
-      for (int q = 0; q < 32; q += 4) {
-        const float4 a = ld4(Ap + q), d = ld4(Dj + lane * kLd + q);
-        s0 = __fmaf_rn(a.x, d.x, s0);
-        s1 = __fmaf_rn(a.y, d.y, s1);
-        s0 = __fmaf_rn(a.z, d.z, s0);
-        s1 = __fmaf_rn(a.w, d.w, s1);
-      }
-      __syncwarp();
-      Ap[lane] = s0 + s1;
-    }
+  for (int J = 0; J + 1 < nb; ++J) {
+    // the critical path: block row J + 1 of the panel (two rows per warp), then the
+    // diagonal block J + 1 (two rows per warp)
+    chol_panel(A, J, 32 * (J + 1), 32 * (J + 2), warp, kWarps, lane);
     __syncthreads();
-    if (J + 1 == nb) break;
-    for (int item = warp; item < 4 * (nb - 1 - J); item += kWarps)
-      update(J, J + 1 + (item >> 2), J + 1, item & 3);
+    chol_update<2>(A, J, J + 1, J + 1, 2 * warp, lane);
     __syncthreads();
     if (warp == 0) {
-      factor(J + 1);
+      if (chol_inv32(blk(A, J + 1, J + 1), col, lane) && lane == 0) atomicOr(&g_dion_error, 1u);
     } else if (warp % 4 != 0) {
       // the warps that do not share warp 0's sub-partition (warp w runs on sub-partition
       // w % 4), numbered h = 0 .. kHelpers - 1
       const int h = warp - warp / 4 - 1;
-      const int t2 = nb - J - 2;
-      for (int item = h; item < 2 * t2 * (t2 + 1); item += kHelpers) {
-        int I = 0, K = item >> 2;
-        while (K > I) { K -= I + 1; ++I; }
-        update(J, I + J + 2, K + J + 2, item & 3);
+      auto hsync = [] { asm volatile("bar.sync 1, %0;" ::"r"(32 * kHelpers) : "memory"); };
+      const int K = J - 1;       // inverse step taken in this block column
+      const int t = nb - J - 2;  // block rows below J + 1
+      // the rest of block column J of the panel; inverse step K part (1)
+      const int np = 4 * t, n1 = K > 0 ? 4 * K : 0;
+      for (int item = h; item < np + n1; item += kHelpers) {
+        if (item < np) {
+          const int row0 = 32 * (J + 2) + 8 * item;
+          chol_panel(A, J, row0, row0 + 8, 0, 1, lane);
+        } else {
+          inv1(K, item - np);
+        }
       }
-      if (J >= 1)
-        inverse_step(J, h, kHelpers, [] {
-          asm volatile("bar.sync 1, %0;" ::"r"(32 * kHelpers) : "memory");
-        });
+      hsync();
+      // trailing blocks: t blocks of column J + 1 below the diagonal, then the triangle
+      // K' >= J + 2; inverse step K part (2); block row K of W to global memory
+      const int nu = 4 * (t + t * (t + 1) / 2), n2 = K > 0 ? 4 * (nb - 1 - K) * K : 0;
+      for (int item = h; item < nu + n2; item += kHelpers) {
+        if (item >= nu) {
+          inv2(K, item - nu);
+          continue;
+        }
+        int b = item >> 2, I, Kc;
+        if (b < t) {
+          I = J + 2 + b;
+          Kc = J + 1;
+        } else {
+          b -= t;
+          I = 0;
+          Kc = b;
+          while (Kc > I) {
+            Kc -= I + 1;
+            ++I;
+          }
+          I += J + 2;
+          Kc += J + 2;
+        }
+        chol_update<8>(A, J, I, Kc, 8 * (item & 3), lane);
+      }
+      if (K >= 0) chol_write_w(Wr, blk(A, K, K), e.Wsp, K, nb, ldr, false, h * 32 + lane, 32 * kHelpers);
+      hsync();
+      if (K >= 0)
+        for (int item = h; item < 4 * (nb - 1 - K); item += kHelpers) inv3(K, item);
     }
     __syncthreads();
   }
-  if (nb >= 2) inverse_step(nb - 1, warp, kWarps, [] { __syncthreads(); });
-  __syncthreads();
-  // W to global memory as the bf16 operand of the multiply P W^T on the tensor cores: row j
-  // holds hi(W_j) | lo(W_j) | hi(W_j), ldr columns each, lo = bf16(w - hi); zeros above the
-  // diagonal, the identity past r
-  {
-    const int ldr = c.ldr, q8 = ldr / 8, nbw32 = 32 * nb;
-    for (int q = threadIdx.x; q < ldr * q8; q += kCholThreads) {
-      const int j = q / q8, k0 = (q - j * q8) * 8;
-      float w[8], lo[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int k = k0 + u;
-        w[u] = (j < nbw32 && k < nbw32) ? (k <= j ? blk(A, j >> 5, k >> 5)[(j & 31) * kLd + (k & 31)] : 0.0f)
-                                        : (j == k ? 1.0f : 0.0f);
-        lo[u] = w[u] - __bfloat162float(__float2bfloat16_rn(w[u]));
-      }
-      const uint4 h = make_uint4(bf16_pair(w[0], w[1]), bf16_pair(w[2], w[3]), bf16_pair(w[4], w[5]),
-                                 bf16_pair(w[6], w[7]));
-      const uint4 l = make_uint4(bf16_pair(lo[0], lo[1]), bf16_pair(lo[2], lo[3]), bf16_pair(lo[4], lo[5]),
-                                 bf16_pair(lo[6], lo[7]));
-      __nv_bfloat16* row = e.Wsp + size_t(j) * 3 * ldr;
-      *reinterpret_cast<uint4*>(row + k0) = h;
-      *reinterpret_cast<uint4*>(row + ldr + k0) = l;
-      *reinterpret_cast<uint4*>(row + 2 * ldr + k0) = h;
-    }
+  // inverse steps nb - 2 and nb - 1 on all warps
+  const int K = nb - 2;
+  if (K >= 0) {
+    for (int item = warp; item < 4 * K; item += kWarps) inv1(K, item);
+    __syncthreads();
+    for (int item = warp; item < 4 * K; item += kWarps) inv2(K, item);
+    chol_write_w(Wr, blk(A, K, K), e.Wsp, K, nb, ldr, false, threadIdx.x, kCholThreads);
+    __syncthreads();
+    if (warp < 4) inv3(K, warp);
+    __syncthreads();
   }
+  for (int item = warp; item < 4 * (nb - 1); item += kWarps) inv1(nb - 1, item);
+  __syncthreads();
+  chol_write_w(Wr, blk(A, nb - 1, nb - 1), e.Wsp, nb - 1, nb, ldr, true, threadIdx.x, kCholThreads);
 }
 
 // P (fp32 [m][ldr]; pass 0: P0, pass 1: P1) in bf16 parts for the tensor-core products of
@@ -956,7 +1009,7 @@ mao_status dion_run(const mao_mat* X, const mao_mat* M, const mao_mat* G, const 
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return MAO_ERR_CUDA;
   cudaError_t attr_err = cudaSuccess;
-  auto chol_bytes = [](int rk) {  // lower blocks and the row temporaries of the inverse
+  auto chol_bytes = [](int rk) {  // the lower blocks and one block row of W
     const size_t nbk = size_t(ceil_div(rk, 32));
     return sizeof(float) * size_t(kBlk) * (nbk * (nbk + 1) / 2 + nbk - 1);
   };
