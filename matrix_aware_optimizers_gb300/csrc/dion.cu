@@ -56,9 +56,10 @@ struct DionSlot {
   float* Q;
   float* Pout;                      // optional copy of the final P (m x r, row stride r)
   __nv_bfloat16 *Bw, *Qw, *Rw, *Pw; // bf16 operands, rows of ldn / ldr elements
-  float *P0, *P1, *Rf;              // fp32 [m|n][ldr]
+  float* Rf;                        // fp32 R [n][ldr]
   float* Sf;                        // S = P^T P in lower 32 x 32 blocks (layout of blk())
-  __nv_bfloat16* Ys;                // P in bf16 parts [m][4 ldr]: hi | hi | mid | lo
+  __nv_bfloat16 *Ys, *Ys2;          // P in bf16 parts [m][4 ldr]: hi | hi | mid | lo (B Q_prev,
+                                    // then after the first Cholesky QR pass)
   float* D;                         // Gram work product [2 ldr][3 ldr] (fp32)
   __nv_bfloat16* Wsp;               // L^-1 split [ldr][3 ldr]: hi | lo | hi (rows j, columns k)
   float* cn;                        // column norms of R: partials [nchunks][r], then the norms
@@ -73,7 +74,7 @@ struct DionSlot {
 
 struct DionCommon {
   const DionSlot* slots;            // device table [count]
-  OutEntry *tP, *tR, *tM, *tX, *tP1, *tG;  // output tables of the tensor-core launches [count]
+  OutEntry *tP, *tR, *tM, *tX, *tG;  // output tables of the tensor-core launches [count]
   int32_t r, ldr, count;
 };
 
@@ -88,7 +89,7 @@ static_assert(sizeof(SetupParams) <= 32000, "set-up parameters exceed the kernel
 // ---------------------------------------------------------------- set-up
 
 // CTA k writes slot z0 + k of the device table (one 4-byte word per thread: the parameter
-// reads of a warp then differ only in the word, not the slot) and its six output entries.
+// reads of a warp then differ only in the word, not the slot) and its five output entries.
 __global__ void __launch_bounds__(64) dion_setup_kernel(const __grid_constant__ SetupParams p) {
   const int k = blockIdx.x;
   const DionSlot& e = p.s[k];
@@ -98,19 +99,24 @@ __global__ void __launch_bounds__(64) dion_setup_kernel(const __grid_constant__ 
   uint32_t* dst = reinterpret_cast<uint32_t*>(const_cast<DionSlot*>(p.c.slots) + z);
   for (int w = threadIdx.x; w < int(sizeof(DionSlot) / 4); w += 64) dst[w] = src[w];
   if (threadIdx.x != 0) return;
-  OutEntry o;
-  o.bits = nullptr;
-  o.src = nullptr;
-  o.src_ld = 0;
-  o.out = e.P0;
+  OutEntry o = {};
+  // the final P: the bf16 operand Pw, and the caller's fp32 copy if asked for
+  o.out = e.Pw;
   o.ld = p.c.ldr;
-  o.dtype = MAO_F32;
+  o.dtype = MAO_BF16;
   o.flags = OUT_VEC;
+  if (e.Pout) {
+    o.copy = e.Pout;
+    o.copy_ld = p.c.r;
+    o.copy_cols = p.c.r;
+    if (reinterpret_cast<uintptr_t>(e.Pout) % 16 == 0 && p.c.r % 4 == 0) o.flags |= OUT_COPY_VEC;
+  }
   p.c.tP[z] = o;
-  o.out = e.P1;
-  p.c.tP1[z] = o;
+  o = OutEntry{};
   o.out = e.D;
   o.ld = 3 * p.c.ldr;
+  o.dtype = MAO_F32;
+  o.flags = OUT_VEC;
   p.c.tG[z] = o;
   o.ld = p.c.ldr;
   o.out = e.Rf;
@@ -634,46 +640,6 @@ __global__ void __launch_bounds__(kCholThreads, 1) dion_chol_kernel(const __grid
   chol_write_w(Wr, blk(A, nb - 1, nb - 1), e.Wsp, nb - 1, nb, ldr, true, threadIdx.x, kCholThreads);
 }
 
-// P (fp32 [m][ldr]; pass 0: P0, pass 1: P1) in bf16 parts for the tensor-core products of
-// Cholesky QR: Ys = hi | hi | mid | lo (bf16 [m][4 ldr]) with hi = bf16(p), mid = bf16(p - hi),
-// lo = bf16(p - hi - mid) (each difference exact in fp32). The multiply by L^-T reads the
-// first three, the Gram matrix the last three. Columns at and past r are written as zeros
-// (they meet zero columns of the other factor, and NaN x 0 would not vanish).
-__global__ void __launch_bounds__(256) dion_split_kernel(const __grid_constant__ DionCommon c, int pass) {
-  const DionSlot& e = c.slots[blockIdx.y];
-  const uint32_t upr = uint32_t(c.ldr) / 8;
-  const uint32_t u = blockIdx.x * 256u + threadIdx.x;
-  if (u >= uint32_t(e.m) * upr) return;
-  const uint32_t row = u / upr, k0 = (u - row * upr) * 8;
-  const float* P = (pass == 0 ? e.P0 : e.P1) + size_t(row) * c.ldr + k0;
-  float v[8];
-  if (int(k0) + 8 <= c.r) {
-    const float4 x = *reinterpret_cast<const float4*>(P), y = *reinterpret_cast<const float4*>(P + 4);
-    v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w; v[4] = y.x; v[5] = y.y; v[6] = y.z; v[7] = y.w;
-  } else {
-#pragma unroll
-    for (int q = 0; q < 8; ++q) v[q] = int(k0) + q < c.r ? P[q] : 0.0f;
-  }
-  float mid[8], lo[8];
-#pragma unroll
-  for (int q = 0; q < 8; ++q) {
-    const float d = v[q] - __bfloat162float(__float2bfloat16_rn(v[q]));
-    mid[q] = d;
-    lo[q] = d - __bfloat162float(__float2bfloat16_rn(d));
-  }
-  const uint4 h = make_uint4(bf16_pair(v[0], v[1]), bf16_pair(v[2], v[3]), bf16_pair(v[4], v[5]),
-                             bf16_pair(v[6], v[7]));
-  const uint4 md = make_uint4(bf16_pair(mid[0], mid[1]), bf16_pair(mid[2], mid[3]),
-                              bf16_pair(mid[4], mid[5]), bf16_pair(mid[6], mid[7]));
-  const uint4 l = make_uint4(bf16_pair(lo[0], lo[1]), bf16_pair(lo[2], lo[3]), bf16_pair(lo[4], lo[5]),
-                             bf16_pair(lo[6], lo[7]));
-  __nv_bfloat16* y = e.Ys + size_t(row) * 4 * c.ldr + k0;
-  *reinterpret_cast<uint4*>(y) = h;
-  *reinterpret_cast<uint4*>(y + c.ldr) = h;
-  *reinterpret_cast<uint4*>(y + 2 * c.ldr) = md;
-  *reinterpret_cast<uint4*>(y + 3 * c.ldr) = l;
-}
-
 // S = P^T P from the Gram work product D = [hi | mid]^T [hi | mid | lo] (rows: hi, then mid
 // from row ldr; columns: hi, mid from ldr, lo from 2 ldr):
 //   S = hi^T hi + hi^T mid + mid^T hi + hi^T lo + lo^T hi + mid^T mid,
@@ -699,40 +665,6 @@ __global__ void __launch_bounds__(256) dion_assemble_kernel(const __grid_constan
   }
   blk(e.Sf, I, J)[ii * kLd + kk] = v;
 }
-
-// The final P (fp32 in P0) to the bf16 operand Pw (zeros from r up to ldr) and, if asked,
-// the caller's fp32 copy (row stride r).
-__global__ void __launch_bounds__(256) dion_finish_kernel(const __grid_constant__ DionCommon c) {
-  const DionSlot& e = c.slots[blockIdx.y];
-  const uint32_t upr = uint32_t(c.ldr) / 8;
-  const uint32_t u = blockIdx.x * 256u + threadIdx.x;
-  if (u >= uint32_t(e.m) * upr) return;
-  const uint32_t row = u / upr, k0 = (u - row * upr) * 8;
-  const float* P = e.P0 + size_t(row) * c.ldr + k0;
-  const bool full = int(k0) + 8 <= c.r;
-  float v[8];
-  if (full) {
-    const float4 x = *reinterpret_cast<const float4*>(P), y = *reinterpret_cast<const float4*>(P + 4);
-    v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w; v[4] = y.x; v[5] = y.y; v[6] = y.z; v[7] = y.w;
-  } else {
-#pragma unroll
-    for (int q = 0; q < 8; ++q) v[q] = int(k0) + q < c.r ? P[q] : 0.0f;
-  }
-  *reinterpret_cast<uint4*>(e.Pw + size_t(row) * c.ldr + k0) =
-      make_uint4(bf16_pair(v[0], v[1]), bf16_pair(v[2], v[3]), bf16_pair(v[4], v[5]), bf16_pair(v[6], v[7]));
-  if (e.Pout) {
-    float* d = e.Pout + size_t(row) * c.r + k0;
-    if (full && c.r % 4 == 0 && reinterpret_cast<uintptr_t>(e.Pout) % 16 == 0) {
-      *reinterpret_cast<float4*>(d) = make_float4(v[0], v[1], v[2], v[3]);
-      *reinterpret_cast<float4*>(d + 4) = make_float4(v[4], v[5], v[6], v[7]);
-    } else {
-#pragma unroll
-      for (int q = 0; q < 8; ++q)
-        if (int(k0) + q < c.r) d[q] = v[q];
-    }
-  }
-}
-
 
 // ------------------------------------------------------ R -> Q = ColumnNormalize(R)
 
@@ -818,7 +750,7 @@ __global__ void __launch_bounds__(256) dion_q_kernel(const __grid_constant__ Dio
 struct DionGroup {
   int64_t m, n;
   int32_t count, slot0;
-  size_t off_bw, off_qw, off_rw, off_pw, off_p0, off_p1, off_rf, off_sf, off_ys, off_d, off_wsp, off_cn;
+  size_t off_bw, off_qw, off_rw, off_pw, off_rf, off_sf, off_ys, off_ys2, off_d, off_wsp, off_cn;
 };
 
 struct DionPlan {
@@ -852,7 +784,7 @@ void make_dion_plan(const mao_mat* X, int32_t batch, int32_t rank, DionPlan& pla
     return at;
   };
   plan.off_slots = take(sizeof(DionSlot) * size_t(batch));
-  plan.off_tables = take(6 * sizeof(OutEntry) * size_t(batch));
+  plan.off_tables = take(5 * sizeof(OutEntry) * size_t(batch));
   const size_t r = size_t(rank), ldr = size_t(plan.ldr);
   int slot = 0;
   for (const auto& mem : members) {
@@ -868,12 +800,11 @@ void make_dion_plan(const mao_mat* X, int32_t batch, int32_t rank, DionPlan& pla
     g.off_qw = take(c * n * ldr * 2);
     g.off_rw = take(c * n * ldr * 2);
     g.off_pw = take(c * m * ldr * 2);
-    g.off_p0 = take(c * m * ldr * 4);
-    g.off_p1 = take(c * m * ldr * 4);
     g.off_rf = take(c * n * ldr * 4);
     const size_t nsb = (ldr / 32) * (ldr / 32 + 1) / 2;  // lower 32 x 32 blocks of S
     g.off_sf = take(c * nsb * kBlk * 4);
     g.off_ys = take(c * m * 4 * ldr * 2);
+    g.off_ys2 = take(c * m * 4 * ldr * 2);
     g.off_d = take(c * 2 * ldr * 3 * ldr * 4);
     g.off_wsp = take(c * ldr * 3 * ldr * 2);
     g.off_cn = take(c * (nch + 1) * r * 4);
@@ -894,9 +825,10 @@ int out_flags(const mao_mat& a) {
 }
 
 // Tensor-core launches of one product over every group (up to eight groups per launch).
-// op: 0 = P = B Q, 1 = R = B^T P, 2 = M update (P R^T), 3 = X update (P Q^T).
+// op: 0 = P = B Q, 1 = R = B^T P, 2 = M update (P R^T), 3 = X update (P Q^T), 4 = the multiply
+// P W^T and 5 = the Gram product of Cholesky QR pass `pass` (P's parts from Ys, then Ys2).
 mao_status dion_tc(const DionPlan& plan, uint8_t* ws, const OutEntry* table, int op, float alpha,
-                   cudaStream_t stream) {
+                   cudaStream_t stream, int pass = 0) {
   const int64_t r = plan.r, ldr = plan.ldr;
   // The kernel deals tiles to CTA pairs round-robin in list order; listing the groups with
   // the deepest products (the most k-blocks per tile) first spreads the long tiles over the
@@ -931,24 +863,26 @@ mao_status dion_tc(const DionPlan& plan, uint8_t* ws, const OutEntry* table, int
       const void *A, *B;
       int64_t rowsA, ldA, rowsB, ldB, colsA = -1, colsB = -1;
       switch (op) {
-        case 0:  // (m x n)(n x r): Bw K-major, Qw MN-major
+        case 0:  // (m x n)(n x ldr): Bw K-major, Qw MN-major (zeros past r)
           A = ws + g.off_bw; rowsA = g.m; ldA = ldn; G.a_mn = 0;
           B = ws + g.off_qw; rowsB = g.n; ldB = ldr; G.b_mn = 1;
-          G.M = int32_t(g.m); G.N = int32_t(r); G.K = int32_t(g.n);
+          G.M = int32_t(g.m); G.N = int32_t(ldr); G.K = int32_t(g.n);
           break;
         case 1:  // (n x m)(m x r): Bw MN-major, Pw MN-major
           A = ws + g.off_bw; rowsA = g.m; ldA = ldn; G.a_mn = 1;
           B = ws + g.off_pw; rowsB = g.m; ldB = ldr; G.b_mn = 1;
           G.M = int32_t(g.n); G.N = int32_t(r); G.K = int32_t(g.m);
           break;
-        case 4:  // (m x 3 ldr)(3 ldr x r): [P_hi P_hi P_mid] [W_hi W_lo W_hi]^T, both K-major
-          A = ws + g.off_ys; rowsA = g.m; ldA = 4 * ldr; colsA = 3 * ldr; G.a_mn = 0;
+        case 4:  // (m x 3 ldr)(3 ldr x ldr): [P_hi P_hi P_mid] [W_hi W_lo W_hi]^T, both K-major
+          A = ws + (pass == 0 ? g.off_ys : g.off_ys2); rowsA = g.m; ldA = 4 * ldr; colsA = 3 * ldr;
+          G.a_mn = 0;
           B = ws + g.off_wsp; rowsB = ldr; ldB = 3 * ldr; G.b_mn = 0;
-          G.M = int32_t(g.m); G.N = int32_t(r); G.K = int32_t(3 * ldr);
+          G.M = int32_t(g.m); G.N = int32_t(ldr); G.K = int32_t(3 * ldr);
           break;
         case 5:  // (2 ldr x m)(m x 3 ldr): [P_hi P_mid]^T [P_hi P_mid P_lo], both MN-major
-          A = ws + g.off_ys + ldr * 2; rowsA = g.m; ldA = 4 * ldr; colsA = 2 * ldr; G.a_mn = 1;
-          B = ws + g.off_ys + ldr * 2; rowsB = g.m; ldB = 4 * ldr; colsB = 3 * ldr; G.b_mn = 1;
+          A = ws + (pass == 0 ? g.off_ys : g.off_ys2) + ldr * 2; rowsA = g.m; ldA = 4 * ldr;
+          colsA = 2 * ldr; G.a_mn = 1;
+          B = static_cast<const uint8_t*>(A); rowsB = g.m; ldB = 4 * ldr; colsB = 3 * ldr; G.b_mn = 1;
           G.M = int32_t(2 * ldr); G.N = int32_t(3 * ldr); G.K = int32_t(g.m);
           break;
         default:  // (m x r)(r x n): Pw K-major, Rw / Qw K-major
@@ -960,9 +894,19 @@ mao_status dion_tc(const DionPlan& plan, uint8_t* ws, const OutEntry* table, int
       G.count = g.count;
       G.slot0 = g.slot0;
       G.orig_cols = G.N;
-      G.final_out = 1;
+      // B Q_prev and the first pass's P W^T go to the workspace as the bf16 parts of the next
+      // Cholesky QR pass (bulk stores); the rest through the slots' output entries
+      const bool parts = op == 0 || (op == 4 && pass == 0);
+      G.final_out = parts ? 0 : 1;
+      G.split_out = parts ? 1 : 0;
       mao_status st = tc_encode_map(&G.tmA, A, rowsA, ldA, g.count, colsA);
       if (st == MAO_OK) st = tc_encode_map(&G.tmB, B, rowsB, ldB, g.count, colsB);
+      if (st == MAO_OK && parts) {
+        G.out = ws + (op == 0 ? g.off_ys : g.off_ys2);
+        G.out_ld = 4 * ldr;
+        G.out_mstride = g.m * 4 * ldr;
+        st = tc_encode_store_map(&G.tmOR, G.out, g.m, 4 * ldr, g.count);
+      }
       if (st != MAO_OK) return st;
       G.tiles_m = int32_t(ceil_div(G.M, tc::TILE_M));
       G.tiles_n = int32_t(ceil_div(G.N, tc::BN));
@@ -999,8 +943,7 @@ mao_status dion_run(const mao_mat* X, const mao_mat* M, const mao_mat* G, const 
   c.tR = tables + batch;
   c.tM = tables + 2 * batch;
   c.tX = tables + 3 * batch;
-  c.tP1 = tables + 4 * batch;
-  c.tG = tables + 5 * batch;
+  c.tG = tables + 4 * batch;
   c.r = rank;
   c.ldr = int32_t(plan.ldr);
   c.count = batch;
@@ -1044,13 +987,12 @@ mao_status dion_run(const mao_mat* X, const mao_mat* M, const mao_mat* G, const 
       e.Qw = reinterpret_cast<__nv_bfloat16*>(ws + g.off_qw) + size_t(k) * g.n * plan.ldr;
       e.Rw = reinterpret_cast<__nv_bfloat16*>(ws + g.off_rw) + size_t(k) * g.n * plan.ldr;
       e.Pw = reinterpret_cast<__nv_bfloat16*>(ws + g.off_pw) + size_t(k) * g.m * plan.ldr;
-      e.P0 = reinterpret_cast<float*>(ws + g.off_p0) + size_t(k) * g.m * plan.ldr;
-      e.P1 = reinterpret_cast<float*>(ws + g.off_p1) + size_t(k) * g.m * plan.ldr;
       e.Rf = reinterpret_cast<float*>(ws + g.off_rf) + size_t(k) * g.n * plan.ldr;
       e.nchunks = int32_t(ceil_div(g.n, kNormRows));
       const size_t nsb = size_t(plan.ldr / 32) * size_t(plan.ldr / 32 + 1) / 2;
       e.Sf = reinterpret_cast<float*>(ws + g.off_sf) + size_t(k) * nsb * kBlk;
       e.Ys = reinterpret_cast<__nv_bfloat16*>(ws + g.off_ys) + size_t(k) * g.m * 4 * plan.ldr;
+      e.Ys2 = reinterpret_cast<__nv_bfloat16*>(ws + g.off_ys2) + size_t(k) * g.m * 4 * plan.ldr;
       e.D = reinterpret_cast<float*>(ws + g.off_d) + size_t(k) * 2 * plan.ldr * 3 * plan.ldr;
       e.Wsp = reinterpret_cast<__nv_bfloat16*>(ws + g.off_wsp) + size_t(k) * plan.ldr * 3 * plan.ldr;
       e.cn = reinterpret_cast<float*>(ws + g.off_cn) + size_t(k) * (e.nchunks + 1) * rank;
@@ -1091,22 +1033,16 @@ mao_status dion_run(const mao_mat* X, const mao_mat* M, const mao_mat* G, const 
   profile_before_launch(stream, MAO_PROF_DION_STAGE);
   dion_stage_q_kernel<<<dim3(blocks(plan.max_qunits), nb), 256, 0, stream>>>(c);
   if (!launched()) return MAO_ERR_CUDA;
-  // 2. P = B Q_prev (fp32)
-  mao_status st = dion_tc(plan, ws, c.tP, 0, 1.0f, stream);
+  // 2. P = B Q_prev, as the bf16 parts Ys
+  mao_status st = dion_tc(plan, ws, nullptr, 0, 1.0f, stream);
   if (st != MAO_OK) return st;
-  // 3. Cholesky QR, twice: P0 -> P1 (fp32) -> Pw (bf16; + the caller's fp32 P)
+  // 3. Cholesky QR, twice: Ys -> Ys2 -> Pw (bf16; + the caller's fp32 P)
   const size_t chol_smem = chol_bytes(rank);
-  int64_t max_m = 0;
-  for (const auto& g : plan.groups) max_m = std::max<int64_t>(max_m, g.m);
-  const unsigned split_blocks = unsigned(ceil_div(max_m * (plan.ldr / 8), 256));
   const int nbk = int(ceil_div(rank, 32));
   const unsigned assemble_blocks = unsigned(nbk * (nbk + 1) / 2 * 4);
   for (int pass = 0; pass < 2; ++pass) {
-    profile_before_launch(stream, MAO_PROF_DION_SPLIT);
-    dion_split_kernel<<<dim3(split_blocks, nb), 256, 0, stream>>>(c, pass);
-    if (!launched()) return MAO_ERR_CUDA;
     // S = P^T P on the tensor cores from P's parts, assembled in the Cholesky's block layout
-    mao_status sg = dion_tc(plan, ws, c.tG, 5, 1.0f, stream);
+    mao_status sg = dion_tc(plan, ws, c.tG, 5, 1.0f, stream, pass);
     if (sg != MAO_OK) return sg;
     profile_before_launch(stream, MAO_PROF_DION_GRAM);
     dion_assemble_kernel<<<dim3(assemble_blocks, nb), 256, 0, stream>>>(c);
@@ -1114,13 +1050,10 @@ mao_status dion_run(const mao_mat* X, const mao_mat* M, const mao_mat* G, const 
     profile_before_launch(stream, MAO_PROF_DION_CHOL);
     dion_chol_kernel<<<nb, kCholThreads, chol_smem, stream>>>(c);
     if (!launched()) return MAO_ERR_CUDA;
-    // P1 = P0 W1^T (pass 0), P = P1 W2^T into P0 (pass 1), on the tensor cores
-    const mao_status st = dion_tc(plan, ws, pass == 0 ? c.tP1 : c.tP, 4, 1.0f, stream);
+    // P W^T on the tensor cores: into Ys2 (pass 0), into Pw and the caller's P (pass 1)
+    const mao_status st = dion_tc(plan, ws, pass == 0 ? nullptr : c.tP, 4, 1.0f, stream, pass);
     if (st != MAO_OK) return st;
   }
-  profile_before_launch(stream, MAO_PROF_DION_SPLIT);
-  dion_finish_kernel<<<dim3(split_blocks, nb), 256, 0, stream>>>(c);
-  if (!launched()) return MAO_ERR_CUDA;
   // 4. R = B^T P (fp32)
   st = dion_tc(plan, ws, c.tR, 1, 1.0f, stream);
   if (st != MAO_OK) return st;

@@ -64,8 +64,12 @@ struct OutEntry {
   const void* src;  // in-place updates (TC_UPDATE): the old values, of out's dtype, or null
                     // for out itself (out <- src + a (A B^T))
   int64_t src_ld;   // row stride of src (elements)
+  float* copy;      // optional fp32 copy of the first copy_cols columns (final products)
+  int32_t copy_ld;  // row stride of copy (elements)
+  int32_t copy_cols;
 };
 
-enum OutFlags : int32_t { OUT_VEC = 1, OUT_WORDS = 2 };
+// OUT_COPY_VEC: copy's rows allow 16-byte stores.
+enum OutFlags : int32_t { OUT_VEC = 1, OUT_WORDS = 2, OUT_COPY_VEC = 4 };
 
 }  // namespace mao

@@ -128,6 +128,9 @@ struct TcGroup {
                             // diagonal tile loads one half and multiplies it by itself
   int32_t tiles_m, tiles_n, tiles_per_mat, tile_begin;
   int32_t final_out;        // last NS_APPLY: write U / signs through the slot's OutEntry
+  int32_t split_out;        // workspace output as the bf16 parts hi | hi | mid | lo of the
+                            // fp32 values (hi = bf16(x), mid = bf16(x - hi),
+                            // lo = bf16(x - hi - mid)), out_ld / 4 columns apart
   int32_t orig_cols;        // C of the original matrix (sign-bit indexing)
 };
 

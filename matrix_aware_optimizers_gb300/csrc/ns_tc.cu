@@ -435,53 +435,51 @@ __device__ __forceinline__ float res_elem(const uint4 (&r)[8], int c) {
   return __uint_as_float((c & 1) ? (w & 0xFFFF0000u) : (w << 16));
 }
 
-// Final output of the last product for this lane's row, columns jb..jb+63: U (through the
-// slot's output entry) and/or its packed signs, taken from the fp32 values.
+// fp32 rows: this lane's row, columns jb..jb+63 (those below ncols), to dst. With vec (rows
+// 16-byte aligned) two 32-column halves go through the staging buffer as 32 x 32 blocks of
+// 128-byte rows; otherwise each lane writes its own row.
+__device__ __forceinline__ void store_rows_f32(uint8_t* S, float* dst, int64_t ld, int i0, int jb, int M,
+                                               int ncols, int lane, const float* w, bool vec) {
+  if (vec) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        *reinterpret_cast<float4*>(S + srow(lane, k)) =
+            make_float4(w[32 * h + 4 * k], w[32 * h + 4 * k + 1], w[32 * h + 4 * k + 2], w[32 * h + 4 * k + 3]);
+      __syncwarp();
+      const int sg = lane & 7;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const int r = (lane >> 3) + 4 * q;
+        const int gi = i0 + r;
+        const int gj = jb + 32 * h + 4 * sg;
+        if (gi >= M) continue;
+        const float4 val = *reinterpret_cast<const float4*>(S + srow(r, sg));
+        float* g = dst + int64_t(gi) * ld + gj;
+        if (gj + 4 <= ncols) {
+          *reinterpret_cast<float4*>(g) = val;
+        } else {
+          const float* f = reinterpret_cast<const float*>(&val);
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            if (gj + k < ncols) g[k] = f[k];
+        }
+      }
+      __syncwarp();
+    }
+  } else if (i0 + lane < M) {
+#pragma unroll
+    for (int c = 0; c < 64; ++c)
+      if (jb + c < ncols) dst[int64_t(i0 + lane) * ld + jb + c] = w[c];
+  }
+}
+
+// Final output of the last product for this lane's row, columns jb..jb+63: packed signs,
+// an fp32 copy, and U through the slot's output entry, taken from the fp32 values w.
 __device__ __forceinline__ void store_final(const OutEntry& e, uint8_t* S, int i0, int jb, int M,
                                             int N, int orig_cols, int lane, const float* w) {
   const int i = i0 + lane;
-  if (e.out) {
-    if ((e.flags & OUT_VEC) && e.dtype == MAO_BF16) {
-      stage_rows(S, lane, w);
-      __syncwarp();
-      store_rows(S, reinterpret_cast<__nv_bfloat16*>(e.out), e.ld, i0, jb, M, N, lane);
-      __syncwarp();
-    } else if (e.flags & OUT_VEC) {
-      // fp32: two 32-column halves, each a 32 x 32 fp32 block of 128-byte rows
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-          *reinterpret_cast<float4*>(S + srow(lane, k)) =
-              make_float4(w[32 * h + 4 * k], w[32 * h + 4 * k + 1], w[32 * h + 4 * k + 2],
-                          w[32 * h + 4 * k + 3]);
-        __syncwarp();
-        const int sg = lane & 7;
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const int r = (lane >> 3) + 4 * q;
-          const int gi = i0 + r;
-          const int gj = jb + 32 * h + 4 * sg;
-          if (gi >= M) continue;
-          const float4 val = *reinterpret_cast<const float4*>(S + srow(r, sg));
-          float* g = reinterpret_cast<float*>(e.out) + int64_t(gi) * e.ld + gj;
-          if (gj + 4 <= N) {
-            *reinterpret_cast<float4*>(g) = val;
-          } else {
-            const float* f = reinterpret_cast<const float*>(&val);
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-              if (gj + k < N) g[k] = f[k];
-          }
-        }
-        __syncwarp();
-      }
-    } else if (i < M) {
-#pragma unroll
-      for (int c = 0; c < 64; ++c)
-        if (jb + c < N) store_elem(e.out, int64_t(i) * e.ld + jb + c, e.dtype, w[c]);
-    }
-  }
   if (e.bits && i < M) {
     if (e.flags & OUT_WORDS) {  // C % 32 == 0: each 32 columns are one word
 #pragma unroll
@@ -502,6 +500,20 @@ __device__ __forceinline__ void store_final(const OutEntry& e, uint8_t* S, int i
         }
       }
     }
+  }
+  if (e.copy) store_rows_f32(S, e.copy, e.copy_ld, i0, jb, M, e.copy_cols, lane, w, (e.flags & OUT_COPY_VEC) != 0);
+  if (!e.out) return;
+  if ((e.flags & OUT_VEC) && e.dtype == MAO_BF16) {
+    stage_rows(S, lane, w);
+    __syncwarp();
+    store_rows(S, reinterpret_cast<__nv_bfloat16*>(e.out), e.ld, i0, jb, M, N, lane);
+    __syncwarp();
+  } else if ((e.flags & OUT_VEC) && e.dtype == MAO_F32) {
+    store_rows_f32(S, reinterpret_cast<float*>(e.out), e.ld, i0, jb, M, N, lane, w, true);
+  } else if (i < M) {
+#pragma unroll
+    for (int c = 0; c < 64; ++c)
+      if (jb + c < N) store_elem(e.out, int64_t(i) * e.ld + jb + c, e.dtype, w[c]);
   }
 }
 
@@ -1172,6 +1184,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads(MODE), 1)
           __syncwarp();
         } else if (FINAL) {
           store_final(oe, S, i0, jb, G.M, G.N, G.orig_cols, lane, w);
+        } else if (STAGE == NS_APPLY && G.split_out) {
+          // the bf16 parts hi | hi | mid | lo of the fp32 values, out_ld / 4 columns apart,
+          // each through the staging buffer and bulk stores (the buffer must have been read
+          // by the warp's previous bulk store before it is rewritten)
+          const int pl = int(G.out_ld >> 2);
+#pragma unroll 1
+          for (int q = 0; q < 3; ++q) {
+            if (lane == 0) bulk_wait_read();
+            __syncwarp();
+            stage_rows(S, lane, w);
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              if (q == 0) tma_store_3d(&G.tmOR, smem_u32(S), jb, i0, t.z);
+              tma_store_3d(&G.tmOR, smem_u32(S), jb + (q + 1) * pl, i0, t.z);
+              bulk_commit();
+            }
+            __syncwarp();
+            if (q < 2) {
+#pragma unroll
+              for (int c = 0; c < 64; ++c) w[c] -= __bfloat162float(__float2bfloat16_rn(w[c]));
+            }
+          }
         } else {
           // workspace outputs cover the zero-padded row: the bulk store writes the whole
           // 64-column block (its padding columns hold zeros). The single staging buffer
