@@ -74,7 +74,7 @@ struct DionSlot {
 
 struct DionCommon {
   const DionSlot* slots;            // device table [count]
-  OutEntry *tP, *tR, *tM, *tX, *tG;  // output tables of the tensor-core launches [count]
+  OutEntry *tP, *tM, *tX;  // output tables of the tensor-core launches [count]
   int32_t r, ldr, count;
 };
 
@@ -89,7 +89,8 @@ static_assert(sizeof(SetupParams) <= 32000, "set-up parameters exceed the kernel
 // ---------------------------------------------------------------- set-up
 
 // CTA k writes slot z0 + k of the device table (one 4-byte word per thread: the parameter
-// reads of a warp then differ only in the word, not the slot) and its five output entries.
+// reads of a warp then differ only in the word, not the slot) and its three output entries:
+// the final P when the caller asked for a copy of it, and the two in-place updates.
 __global__ void __launch_bounds__(64) dion_setup_kernel(const __grid_constant__ SetupParams p) {
   const int k = blockIdx.x;
   const DionSlot& e = p.s[k];
@@ -113,14 +114,6 @@ __global__ void __launch_bounds__(64) dion_setup_kernel(const __grid_constant__ 
   }
   p.c.tP[z] = o;
   o = OutEntry{};
-  o.out = e.D;
-  o.ld = 3 * p.c.ldr;
-  o.dtype = MAO_F32;
-  o.flags = OUT_VEC;
-  p.c.tG[z] = o;
-  o.ld = p.c.ldr;
-  o.out = e.Rf;
-  p.c.tR[z] = o;
   o.out = e.M;
   o.ld = e.ldm;
   o.dtype = e.dtm;
@@ -784,7 +777,7 @@ void make_dion_plan(const mao_mat* X, int32_t batch, int32_t rank, DionPlan& pla
     return at;
   };
   plan.off_slots = take(sizeof(DionSlot) * size_t(batch));
-  plan.off_tables = take(5 * sizeof(OutEntry) * size_t(batch));
+  plan.off_tables = take(3 * sizeof(OutEntry) * size_t(batch));
   const size_t r = size_t(rank), ldr = size_t(plan.ldr);
   int slot = 0;
   for (const auto& mem : members) {
@@ -827,6 +820,9 @@ int out_flags(const mao_mat& a) {
 // Tensor-core launches of one product over every group (up to eight groups per launch).
 // op: 0 = P = B Q, 1 = R = B^T P, 2 = M update (P R^T), 3 = X update (P Q^T), 4 = the multiply
 // P W^T and 5 = the Gram product of Cholesky QR pass `pass` (P's parts from Ys, then Ys2).
+// B Q_prev, R, the Gram products and the multiplies go to workspace buffers through bulk
+// stores (eight epilogue warps); only the final P with a caller's copy, and the updates, go
+// through the slots' output entries (`table`).
 mao_status dion_tc(const DionPlan& plan, uint8_t* ws, const OutEntry* table, int op, float alpha,
                    cudaStream_t stream, int pass = 0) {
   const int64_t r = plan.r, ldr = plan.ldr;
@@ -868,10 +864,10 @@ mao_status dion_tc(const DionPlan& plan, uint8_t* ws, const OutEntry* table, int
           B = ws + g.off_qw; rowsB = g.n; ldB = ldr; G.b_mn = 1;
           G.M = int32_t(g.m); G.N = int32_t(ldr); G.K = int32_t(g.n);
           break;
-        case 1:  // (n x m)(m x r): Bw MN-major, Pw MN-major
+        case 1:  // (n x m)(m x ldr): Bw MN-major, Pw MN-major (zeros past r)
           A = ws + g.off_bw; rowsA = g.m; ldA = ldn; G.a_mn = 1;
           B = ws + g.off_pw; rowsB = g.m; ldB = ldr; G.b_mn = 1;
-          G.M = int32_t(g.n); G.N = int32_t(r); G.K = int32_t(g.m);
+          G.M = int32_t(g.n); G.N = int32_t(ldr); G.K = int32_t(g.m);
           break;
         case 4:  // (m x 3 ldr)(3 ldr x ldr): [P_hi P_hi P_mid] [W_hi W_lo W_hi]^T, both K-major
           A = ws + (pass == 0 ? g.off_ys : g.off_ys2); rowsA = g.m; ldA = 4 * ldr; colsA = 3 * ldr;
@@ -894,18 +890,22 @@ mao_status dion_tc(const DionPlan& plan, uint8_t* ws, const OutEntry* table, int
       G.count = g.count;
       G.slot0 = g.slot0;
       G.orig_cols = G.N;
-      // B Q_prev and the first pass's P W^T go to the workspace as the bf16 parts of the next
-      // Cholesky QR pass (bulk stores); the rest through the slots' output entries
-      const bool parts = op == 0 || (op == 4 && pass == 0);
-      G.final_out = parts ? 0 : 1;
-      G.split_out = parts ? 1 : 0;
+      // workspace outputs: B Q_prev and the first pass's P W^T as the bf16 parts of the next
+      // Cholesky QR pass, the final P W^T as Pw (bf16) unless the caller wants a copy of P,
+      // R and the Gram product in fp32
+      const bool ws_out = op == 0 || op == 1 || op == 5 || (op == 4 && (pass == 0 || !table));
+      G.final_out = ws_out ? 0 : 1;
       mao_status st = tc_encode_map(&G.tmA, A, rowsA, ldA, g.count, colsA);
       if (st == MAO_OK) st = tc_encode_map(&G.tmB, B, rowsB, ldB, g.count, colsB);
-      if (st == MAO_OK && parts) {
-        G.out = ws + (op == 0 ? g.off_ys : g.off_ys2);
-        G.out_ld = 4 * ldr;
-        G.out_mstride = g.m * 4 * ldr;
-        st = tc_encode_store_map(&G.tmOR, G.out, g.m, 4 * ldr, g.count);
+      if (st == MAO_OK && ws_out) {
+        const int64_t rows = G.M, ld = op == 0 || op == 4 ? (pass == 0 ? 4 * ldr : ldr) : G.N;
+        G.out = ws + (op == 0 ? g.off_ys : op == 1 ? g.off_rf : op == 5 ? g.off_d
+                      : pass == 0 ? g.off_ys2 : g.off_pw);
+        G.out_ld = ld;
+        G.out_mstride = rows * ld;
+        G.out_kind = op == 1 || op == 5 ? OUTK_F32 : (op == 0 || pass == 0) ? OUTK_PARTS : OUTK_BF16;
+        st = G.out_kind == OUTK_F32 ? tc_encode_store_map_f32(&G.tmOR, G.out, rows, ld, g.count)
+                                    : tc_encode_store_map(&G.tmOR, G.out, rows, ld, g.count);
       }
       if (st != MAO_OK) return st;
       G.tiles_m = int32_t(ceil_div(G.M, tc::TILE_M));
@@ -940,10 +940,8 @@ mao_status dion_run(const mao_mat* X, const mao_mat* M, const mao_mat* G, const 
   c.slots = reinterpret_cast<const DionSlot*>(ws + plan.off_slots);
   OutEntry* tables = reinterpret_cast<OutEntry*>(ws + plan.off_tables);
   c.tP = tables;
-  c.tR = tables + batch;
-  c.tM = tables + 2 * batch;
-  c.tX = tables + 3 * batch;
-  c.tG = tables + 4 * batch;
+  c.tM = tables + batch;
+  c.tX = tables + 2 * batch;
   c.r = rank;
   c.ldr = int32_t(plan.ldr);
   c.count = batch;
@@ -1042,7 +1040,7 @@ mao_status dion_run(const mao_mat* X, const mao_mat* M, const mao_mat* G, const 
   const unsigned assemble_blocks = unsigned(nbk * (nbk + 1) / 2 * 4);
   for (int pass = 0; pass < 2; ++pass) {
     // S = P^T P on the tensor cores from P's parts, assembled in the Cholesky's block layout
-    mao_status sg = dion_tc(plan, ws, c.tG, 5, 1.0f, stream, pass);
+    mao_status sg = dion_tc(plan, ws, nullptr, 5, 1.0f, stream, pass);
     if (sg != MAO_OK) return sg;
     profile_before_launch(stream, MAO_PROF_DION_GRAM);
     dion_assemble_kernel<<<dim3(assemble_blocks, nb), 256, 0, stream>>>(c);
@@ -1051,11 +1049,11 @@ mao_status dion_run(const mao_mat* X, const mao_mat* M, const mao_mat* G, const 
     dion_chol_kernel<<<nb, kCholThreads, chol_smem, stream>>>(c);
     if (!launched()) return MAO_ERR_CUDA;
     // P W^T on the tensor cores: into Ys2 (pass 0), into Pw and the caller's P (pass 1)
-    const mao_status st = dion_tc(plan, ws, pass == 0 ? nullptr : c.tP, 4, 1.0f, stream, pass);
+    const mao_status st = dion_tc(plan, ws, pass == 1 && P_out ? c.tP : nullptr, 4, 1.0f, stream, pass);
     if (st != MAO_OK) return st;
   }
   // 4. R = B^T P (fp32)
-  st = dion_tc(plan, ws, c.tR, 1, 1.0f, stream);
+  st = dion_tc(plan, ws, nullptr, 1, 1.0f, stream);
   if (st != MAO_OK) return st;
   // 5. Q = ColumnNormalize(R) (caller's Q), bf16 copies of Q and R
   profile_before_launch(stream, MAO_PROF_DION_NORM);

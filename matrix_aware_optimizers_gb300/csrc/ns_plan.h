@@ -105,6 +105,7 @@ static_assert(smem_of(OUT_UPDATE_STREAM) <= 232448, "shared memory budget of one
 }  // namespace tc
 
 enum NsStage : int32_t { NS_GRAM = 1, NS_POLY = 2, NS_APPLY = 3 };
+enum OutKind : int32_t { OUTK_BF16 = 0, OUTK_PARTS = 1, OUTK_F32 = 2 };
 // Products of the same kernel outside Newton–Schulz: an in-place rank-k update of the
 // caller's matrix, out <- out + a * (A B^T), written through the slot's OutEntry.
 constexpr int32_t TC_UPDATE = 4;
@@ -128,9 +129,10 @@ struct TcGroup {
                             // diagonal tile loads one half and multiplies it by itself
   int32_t tiles_m, tiles_n, tiles_per_mat, tile_begin;
   int32_t final_out;        // last NS_APPLY: write U / signs through the slot's OutEntry
-  int32_t split_out;        // workspace output as the bf16 parts hi | hi | mid | lo of the
-                            // fp32 values (hi = bf16(x), mid = bf16(x - hi),
-                            // lo = bf16(x - hi - mid)), out_ld / 4 columns apart
+  int32_t out_kind;         // workspace output (NS_APPLY): OUTK_BF16; OUTK_PARTS, the bf16
+                            // parts hi | hi | mid | lo of the fp32 values (hi = bf16(x),
+                            // mid = bf16(x - hi), lo = bf16(x - hi - mid)), out_ld / 4
+                            // columns apart; OUTK_F32 (tmOR from tc_encode_store_map_f32)
   int32_t orig_cols;        // C of the original matrix (sign-bit indexing)
 };
 
@@ -149,6 +151,9 @@ struct TcParams {
 mao_status tc_encode_map(CUtensorMap* map, const void* base, int64_t rows, int64_t ld,
                          int64_t count, int64_t cols = -1);
 // Bulk-store map of a workspace output buffer [count][rows][ld] bf16 (64 x 32 blocks).
+// fp32 [count][rows][ld] for bulk stores of 32 x 32 blocks (128-byte swizzle)
+mao_status tc_encode_store_map_f32(CUtensorMap* map, const void* base, int64_t rows, int64_t ld,
+                                   int64_t count);
 mao_status tc_encode_store_map(CUtensorMap* map, const void* base, int64_t rows, int64_t ld,
                                int64_t count);
 mao_status tc_gemm_launch(const TcParams& p, cudaStream_t stream);

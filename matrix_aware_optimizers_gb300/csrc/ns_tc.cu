@@ -1184,7 +1184,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads(MODE), 1)
           __syncwarp();
         } else if (FINAL) {
           store_final(oe, S, i0, jb, G.M, G.N, G.orig_cols, lane, w);
-        } else if (STAGE == NS_APPLY && G.split_out) {
+        } else if (STAGE == NS_APPLY && G.out_kind == OUTK_F32) {
+          // fp32: two 32-column halves, each through the staging buffer (32 rows of 128
+          // bytes) and a bulk store
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            if (lane == 0) bulk_wait_read();
+            __syncwarp();
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              *reinterpret_cast<float4*>(S + srow(lane, k)) =
+                  make_float4(w[32 * h + 4 * k], w[32 * h + 4 * k + 1], w[32 * h + 4 * k + 2],
+                              w[32 * h + 4 * k + 3]);
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_3d(&G.tmOR, smem_u32(S), jb + 32 * h, i0, t.z);
+              bulk_commit();
+            }
+            __syncwarp();
+          }
+        } else if (STAGE == NS_APPLY && G.out_kind == OUTK_PARTS) {
           // the bf16 parts hi | hi | mid | lo of the fp32 values, out_ld / 4 columns apart,
           // each through the staging buffer and bulk stores (the buffer must have been read
           // by the warp's previous bulk store before it is rewritten)
@@ -1297,6 +1317,21 @@ mao_status tc_encode_map(CUtensorMap* map, const void* base, int64_t rows, int64
   const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims,
                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MAO_OK : MAO_ERR_UNSUPPORTED;
+}
+
+mao_status tc_encode_store_map_f32(CUtensorMap* map, const void* base, int64_t rows, int64_t ld,
+                                   int64_t count) {
+  auto fn = encode_fn();
+  if (!fn) return MAO_ERR_UNSUPPORTED;
+  const cuuint64_t dims[3] = {cuuint64_t(ld), cuuint64_t(rows), cuuint64_t(count)};
+  const cuuint64_t strides[2] = {cuuint64_t(ld) * 4, cuuint64_t(rows) * cuuint64_t(ld) * 4};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const cuuint32_t box[3] = {32, 32, 1};  // 32 rows of 128 bytes, 128-byte swizzle
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? MAO_OK : MAO_ERR_UNSUPPORTED;
 }
