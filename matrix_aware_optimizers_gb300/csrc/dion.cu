@@ -826,7 +826,7 @@ int out_flags(const mao_mat& a) {
 mao_status dion_tc(const DionPlan& plan, uint8_t* ws, const OutEntry* table, int op, float alpha,
                    cudaStream_t stream, int pass = 0) {
   const int64_t r = plan.r, ldr = plan.ldr;
-  // The kernel deals tiles to CTA pairs round-robin in list order; listing the groups with
+  // The kernel deals tiles to CTA pairs in rounds, every other one reversed; listing the groups with
   // the deepest products (the most k-blocks per tile) first spreads the long tiles over the
   // pairs before the short ones fill the gaps.
   std::vector<size_t> order(plan.groups.size());

@@ -324,6 +324,13 @@ struct Tile {
 };
 
 // Tile `tile` of the flattened list: group, matrix, first output row and column.
+// The k-th tile of CTA pair `pair`: tiles are dealt in rounds of npairs, every other round
+// in reverse pair order, so that with the deepest tiles listed first the pairs that drew
+// the deeper tiles of a round draw the shallower ones of the next.
+__device__ __forceinline__ int pair_tile(int pair, int k, int npairs) {
+  return k * npairs + ((k & 1) ? npairs - 1 - pair : pair);
+}
+
 __device__ __forceinline__ void decode_tile(const TcParams& p, int tile, Tile& t) {
   int g = 0;
   while (g + 1 < p.ngroups && p.g[g + 1].tile_begin <= tile) ++g;
@@ -796,7 +803,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads(MODE), 1)
     bool ok = true;
     bool dep_done = false;  // griddepcontrol.wait passed (before the first global access)
     uint32_t armed = 0, armed_phase = 0;  // leader: stages armed at least once, their phase
-    for (int tile = pair; ok && tile < p.total_tiles; tile += npairs) {
+    for (int k = 0, tile = pair; ok && tile < p.total_tiles; tile = pair_tile(pair, ++k, npairs)) {
       Tile t;
       decode_tile(p, tile, t);
       const TcGroup& G = p.g[t.g];
@@ -893,7 +900,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads(MODE), 1)
       int local = 0;
       bool ok = true;
       bool issued = false;
-      for (int tile = pair; ok && tile < p.total_tiles; tile += npairs, ++local) {
+      for (int tile = pair; ok && tile < p.total_tiles; tile = pair_tile(pair, ++local, npairs)) {
         Tile t;
         decode_tile(p, tile, t);
         const TcGroup& G = p.g[t.g];
@@ -990,13 +997,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads(MODE), 1)
     Tile tc, tn;
     OutEntry oc, on;
     bool hc = tile < p.total_tiles;
-    bool hn = tile + npairs < p.total_tiles;
+    bool hn = pair_tile(pair, 1, npairs) < p.total_tiles;
     if (hc) {
       decode_tile(p, tile, tc);
       oc = p.out_table[p.g[tc.g].slot0 + tc.z];
     }
     if (hn) {
-      decode_tile(p, tile + npairs, tn);
+      decode_tile(p, pair_tile(pair, 1, npairs), tn);
       on = p.out_table[p.g[tn.g].slot0 + tn.z];
     }
     if (hc) {
@@ -1005,7 +1012,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads(MODE), 1)
     }
     for (int local = 0; hc; ++local) {
       // the tile after next: its entry is loaded now and used a tile from now
-      const int tile2 = tile + 2 * npairs;
+      const int tile2 = pair_tile(pair, local + 2, npairs);
       const bool h2 = tile2 < p.total_tiles;
       Tile t2;
       OutEntry o2;
@@ -1073,7 +1080,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads(MODE), 1)
         if (warp == 2) atomicAdd(&g_tc_trace[6], 1ull);
       }
 #endif
-      tile += npairs;
+      tile = pair_tile(pair, local + 1, npairs);
       tc = tn;
       oc = on;
       hc = hn;
@@ -1093,7 +1100,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads(MODE), 1)
     const uint32_t tempty_leader[2] = {mapa_shared(smem_u32(&tempty_bar[0]), 0),
                                        mapa_shared(smem_u32(&tempty_bar[1]), 0)};
     int local = 0;
-    for (int tile = pair; tile < p.total_tiles; tile += npairs, ++local) {
+    for (int tile = pair; tile < p.total_tiles; tile = pair_tile(pair, ++local, npairs)) {
       Tile t;
       decode_tile(p, tile, t);
       const TcGroup& G = p.g[t.g];
