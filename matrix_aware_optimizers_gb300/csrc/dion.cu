@@ -139,6 +139,45 @@ __device__ __forceinline__ float round_to(float v, int32_t dt) {
   return dt == MAO_BF16 ? __bfloat162float(__float2bfloat16_rn(v)) : v;
 }
 
+// Columns j0 .. j0 + 7 of row i of the caller's Q (zeros at and past r), 16 bytes at a time
+// where the row allows it.
+__device__ __forceinline__ void load_q8(const DionSlot& e, int r, int64_t i, int j0, float (&v)[8]) {
+  const float* q = e.Q + i * e.ldq;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int j = j0 + 4 * h;
+    if (e.qvec && j + 4 <= r) {
+      const float4 x = *reinterpret_cast<const float4*>(q + j);
+      v[4 * h] = x.x;
+      v[4 * h + 1] = x.y;
+      v[4 * h + 2] = x.z;
+      v[4 * h + 3] = x.w;
+    } else {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) v[4 * h + k] = j + k < r ? q[j + k] : 0.0f;
+    }
+  }
+}
+
+__device__ __forceinline__ void store_q8(const DionSlot& e, int r, int64_t i, int j0, const float (&v)[8]) {
+  float* q = e.Q + i * e.ldq;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int j = j0 + 4 * h;
+    if (e.qvec && j + 4 <= r) {
+      *reinterpret_cast<float4*>(q + j) = make_float4(v[4 * h], v[4 * h + 1], v[4 * h + 2], v[4 * h + 3]);
+    } else {
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        if (j + k < r) q[j + k] = v[4 * h + k];
+    }
+  }
+}
+
+// Qw = bf16(Q_prev), zero-padded to ldr columns: block qb of the slot's Q units (8 columns
+// each), kStageUnits per thread.
+__device__ __forceinline__ void stage_q_block(const DionCommon& c, const DionSlot& e, uint32_t qb);
+
 // One unit of the general path: Bw(row, col0 .. col0 + 7), and M when it is fp32.
 __device__ __forceinline__ void dion_stage_unit(const DionSlot& e, int64_t row, int64_t col0) {
   float b[8];
@@ -177,6 +216,12 @@ __global__ void __launch_bounds__(256) dion_stage_kernel(const __grid_constant__
   const DionSlot& e = c.slots[blockIdx.y];
   const uint32_t upr = uint32_t(e.ldn) / 8;
   const uint32_t units = uint32_t(e.m) * upr;
+  // blocks past the slot's B units convert Q_prev
+  const uint32_t bblocks = (units + 256u * kStageUnits - 1) / (256u * kStageUnits);
+  if (blockIdx.x >= bblocks) {
+    stage_q_block(c, e, blockIdx.x - bblocks);
+    return;
+  }
   const uint32_t ub = blockIdx.x * (256u * kStageUnits) + threadIdx.x;
   if (ub >= units) return;
   if (e.vec && e.dtm == MAO_BF16 && e.dtg == MAO_BF16) {
@@ -228,51 +273,18 @@ __global__ void __launch_bounds__(256) dion_stage_kernel(const __grid_constant__
   }
 }
 
-// Columns j0 .. j0 + 7 of row i of the caller's Q (zeros at and past r), 16 bytes at a time
-// where the row allows it.
-__device__ __forceinline__ void load_q8(const DionSlot& e, int r, int64_t i, int j0, float (&v)[8]) {
-  const float* q = e.Q + i * e.ldq;
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const int j = j0 + 4 * h;
-    if (e.qvec && j + 4 <= r) {
-      const float4 x = *reinterpret_cast<const float4*>(q + j);
-      v[4 * h] = x.x;
-      v[4 * h + 1] = x.y;
-      v[4 * h + 2] = x.z;
-      v[4 * h + 3] = x.w;
-    } else {
-#pragma unroll
-      for (int k = 0; k < 4; ++k) v[4 * h + k] = j + k < r ? q[j + k] : 0.0f;
-    }
-  }
-}
-
-__device__ __forceinline__ void store_q8(const DionSlot& e, int r, int64_t i, int j0, const float (&v)[8]) {
-  float* q = e.Q + i * e.ldq;
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const int j = j0 + 4 * h;
-    if (e.qvec && j + 4 <= r) {
-      *reinterpret_cast<float4*>(q + j) = make_float4(v[4 * h], v[4 * h + 1], v[4 * h + 2], v[4 * h + 3]);
-    } else {
-#pragma unroll
-      for (int k = 0; k < 4; ++k)
-        if (j + k < r) q[j + k] = v[4 * h + k];
-    }
-  }
-}
-
-// Qw = bf16(Q_prev), zero-padded to ldr columns; blockIdx.y = slot.
-__global__ void __launch_bounds__(256) dion_stage_q_kernel(const __grid_constant__ DionCommon c) {
-  const DionSlot& e = c.slots[blockIdx.y];
+__device__ __forceinline__ void stage_q_block(const DionCommon& c, const DionSlot& e, uint32_t qb) {
   const uint32_t upr = uint32_t(c.ldr) / 8;
-  const uint32_t u = blockIdx.x * blockDim.x + threadIdx.x;
-  if (u >= uint32_t(e.n) * upr) return;
-  const uint32_t i = u / upr, j0 = (u - i * upr) * 8;
-  float v[8];
-  load_q8(e, c.r, i, int(j0), v);
-  store8(e.Qw, size_t(i) * c.ldr + j0, MAO_BF16, v);
+  const uint32_t units = uint32_t(e.n) * upr;
+#pragma unroll
+  for (int t = 0; t < kStageUnits; ++t) {
+    const uint32_t u = qb * (256u * kStageUnits) + 256u * t + threadIdx.x;
+    if (u >= units) break;
+    const uint32_t i = u / upr, j0 = (u - i * upr) * 8;
+    float v[8];
+    load_q8(e, c.r, i, int(j0), v);
+    store8(e.Qw, size_t(i) * c.ldr + j0, MAO_BF16, v);
+  }
 }
 
 // ------------------------------------------------------- Cholesky QR: S = P^T P
@@ -752,6 +764,7 @@ struct DionPlan {
   int64_t r = 0, ldr = 0;
   size_t off_slots = 0, off_tables = 0, total = 0;
   int64_t max_units = 0, max_qunits = 0, max_nchunks = 0;
+  int64_t max_stage_blocks = 0;  // B units, then Q units, of the largest slot
 };
 
 void make_dion_plan(const mao_mat* X, int32_t batch, int32_t rank, DionPlan& plan) {
@@ -804,6 +817,9 @@ void make_dion_plan(const mao_mat* X, int32_t batch, int32_t rank, DionPlan& pla
     for (int b : mem) plan.input_of.push_back(b);
     slot += g.count;
     plan.max_units = std::max<int64_t>(plan.max_units, g.m * int64_t(ldn / 8));
+    plan.max_stage_blocks = std::max<int64_t>(
+        plan.max_stage_blocks, ceil_div(g.m * int64_t(ldn / 8), 256 * kStageUnits) +
+                                   ceil_div(g.n * int64_t(ldr / 8), 256 * kStageUnits));
     plan.max_qunits = std::max<int64_t>(plan.max_qunits, g.n * int64_t(ldr / 8));
     plan.max_nchunks = std::max<int64_t>(plan.max_nchunks, int64_t(nch));
     plan.groups.push_back(g);
@@ -1026,10 +1042,7 @@ mao_status dion_run(const mao_mat* X, const mao_mat* M, const mao_mat* G, const 
   auto blocks = [](int64_t units) { return unsigned(ceil_div(units, 256)); };
   // 1. B = M + G (M <- B), Bw; Qw = bf16(Q_prev)
   profile_before_launch(stream, MAO_PROF_DION_STAGE);
-  dion_stage_kernel<<<dim3(unsigned(ceil_div(plan.max_units, 256 * kStageUnits)), nb), 256, 0, stream>>>(c);
-  if (!launched()) return MAO_ERR_CUDA;
-  profile_before_launch(stream, MAO_PROF_DION_STAGE);
-  dion_stage_q_kernel<<<dim3(blocks(plan.max_qunits), nb), 256, 0, stream>>>(c);
+  dion_stage_kernel<<<dim3(unsigned(plan.max_stage_blocks), nb), 256, 0, stream>>>(c);
   if (!launched()) return MAO_ERR_CUDA;
   // 2. P = B Q_prev, as the bf16 parts Ys
   mao_status st = dion_tc(plan, ws, nullptr, 0, 1.0f, stream);
