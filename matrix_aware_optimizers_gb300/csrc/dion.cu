@@ -867,6 +867,7 @@ mao_status dion_tc(const DionPlan& plan, uint8_t* ws, const OutEntry* table, int
     p.scale = nullptr;
     p.out_table = table;
     p.timeout_ns = wait_limit_ns();
+    p.snake = 1;  // tiles of mixed depths, deepest groups first
     int64_t tiles = 0;
     for (size_t gi = g0; gi < plan.groups.size() && p.ngroups < tc::MAX_GROUPS; ++gi) {
       const DionGroup& g = plan.groups[order[gi]];

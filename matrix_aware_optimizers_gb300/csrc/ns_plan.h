@@ -70,7 +70,15 @@ constexpr int STAGE_BYTES = 2 * HALF_BYTES;       // A half + B half
 // caller's bf16 U with 16-byte aligned rows and no signs.
 // OUT_UPDATE_STREAM: the in-place update of a short product (rank-k update), whose
 // epilogue streams the caller's rows through shared memory (below).
-enum OutMode : int { OUT_WORKSPACE = 0, OUT_CALLER = 1, OUT_CALLER_BF16 = 2, OUT_UPDATE_STREAM = 3 };
+// OUT_WORKSPACE_KIND: workspace outputs of another kind than bf16 (TcGroup::out_kind: bf16
+// parts or fp32), kept out of the Newton–Schulz instantiations.
+enum OutMode : int {
+  OUT_WORKSPACE = 0,
+  OUT_CALLER = 1,
+  OUT_CALLER_BF16 = 2,
+  OUT_UPDATE_STREAM = 3,
+  OUT_WORKSPACE_KIND = 4
+};
 // Epilogue warps: two per 32-lane TMEM quadrant (eight), each taking every other 64-column
 // block of the tile, with one staging buffer each; OUT_CALLER uses one warp per quadrant
 // (four) with two staging buffers each (its general output code needs more registers).
@@ -144,6 +152,7 @@ struct TcParams {
   const float* scale;            // first iteration: per-slot 1/(||X||_F + eps); else null
   const OutEntry* out_table;     // per-slot final outputs
   unsigned long long timeout_ns; // bound of every barrier wait
+  int32_t snake;                 // deal tiles in alternating rounds (see pair_tile)
 };
 
 // Operand map of [count][rows][ld] bf16 buffers (ld a multiple of 64); cols (a multiple of

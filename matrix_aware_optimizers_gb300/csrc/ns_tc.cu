@@ -324,11 +324,13 @@ struct Tile {
 };
 
 // Tile `tile` of the flattened list: group, matrix, first output row and column.
-// The k-th tile of CTA pair `pair`: tiles are dealt in rounds of npairs, every other round
-// in reverse pair order, so that with the deepest tiles listed first the pairs that drew
-// the deeper tiles of a round draw the shallower ones of the next.
-__device__ __forceinline__ int pair_tile(int pair, int k, int npairs) {
-  return k * npairs + ((k & 1) ? npairs - 1 - pair : pair);
+// The k-th tile of CTA pair `pair`: tiles are dealt in rounds of npairs, round-robin, or
+// with `snake` every other round in reverse pair order, so that with the deepest tiles listed
+// first the pairs that drew the deeper tiles of a round draw the shallower ones of the next
+// (products of mixed depths; the Newton–Schulz products, of even depth, keep round-robin,
+// which measured faster for them).
+__device__ __forceinline__ int pair_tile(int pair, int k, int npairs, int snake) {
+  return k * npairs + ((snake & k & 1) ? npairs - 1 - pair : pair);
 }
 
 __device__ __forceinline__ void decode_tile(const TcParams& p, int tile, Tile& t) {
@@ -711,7 +713,7 @@ __device__ __forceinline__ void update_final(const OutEntry& e, int i0, int jb, 
 template <int STAGE, int MODE>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads(MODE), 1)
     ns_tc_kernel(const __grid_constant__ TcParams p) {
-  constexpr bool FINAL = MODE != OUT_WORKSPACE;
+  constexpr bool FINAL = MODE != OUT_WORKSPACE && MODE != OUT_WORKSPACE_KIND;
   constexpr int NEPI = epi_warps(MODE);   // epilogue warps
   constexpr int SPLIT = NEPI / 4;         // epilogue warps per TMEM quadrant
   constexpr int NST = stages_of(MODE);    // operand ring stages
@@ -803,7 +805,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads(MODE), 1)
     bool ok = true;
     bool dep_done = false;  // griddepcontrol.wait passed (before the first global access)
     uint32_t armed = 0, armed_phase = 0;  // leader: stages armed at least once, their phase
-    for (int k = 0, tile = pair; ok && tile < p.total_tiles; tile = pair_tile(pair, ++k, npairs)) {
+    for (int k = 0, tile = pair; ok && tile < p.total_tiles;
+         tile = pair_tile(pair, ++k, npairs, p.snake)) {
       Tile t;
       decode_tile(p, tile, t);
       const TcGroup& G = p.g[t.g];
@@ -900,7 +903,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads(MODE), 1)
       int local = 0;
       bool ok = true;
       bool issued = false;
-      for (int tile = pair; ok && tile < p.total_tiles; tile = pair_tile(pair, ++local, npairs)) {
+      for (int tile = pair; ok && tile < p.total_tiles;
+           tile = pair_tile(pair, ++local, npairs, p.snake)) {
         Tile t;
         decode_tile(p, tile, t);
         const TcGroup& G = p.g[t.g];
@@ -997,13 +1001,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads(MODE), 1)
     Tile tc, tn;
     OutEntry oc, on;
     bool hc = tile < p.total_tiles;
-    bool hn = pair_tile(pair, 1, npairs) < p.total_tiles;
+    bool hn = pair_tile(pair, 1, npairs, p.snake) < p.total_tiles;
     if (hc) {
       decode_tile(p, tile, tc);
       oc = p.out_table[p.g[tc.g].slot0 + tc.z];
     }
     if (hn) {
-      decode_tile(p, pair_tile(pair, 1, npairs), tn);
+      decode_tile(p, pair_tile(pair, 1, npairs, p.snake), tn);
       on = p.out_table[p.g[tn.g].slot0 + tn.z];
     }
     if (hc) {
@@ -1012,7 +1016,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads(MODE), 1)
     }
     for (int local = 0; hc; ++local) {
       // the tile after next: its entry is loaded now and used a tile from now
-      const int tile2 = pair_tile(pair, local + 2, npairs);
+      const int tile2 = pair_tile(pair, local + 2, npairs, p.snake);
       const bool h2 = tile2 < p.total_tiles;
       Tile t2;
       OutEntry o2;
@@ -1080,7 +1084,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads(MODE), 1)
         if (warp == 2) atomicAdd(&g_tc_trace[6], 1ull);
       }
 #endif
-      tile = pair_tile(pair, local + 1, npairs);
+      tile = pair_tile(pair, local + 1, npairs, p.snake);
       tc = tn;
       oc = on;
       hc = hn;
@@ -1100,7 +1104,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads(MODE), 1)
     const uint32_t tempty_leader[2] = {mapa_shared(smem_u32(&tempty_bar[0]), 0),
                                        mapa_shared(smem_u32(&tempty_bar[1]), 0)};
     int local = 0;
-    for (int tile = pair; tile < p.total_tiles; tile = pair_tile(pair, ++local, npairs)) {
+    for (int tile = pair; tile < p.total_tiles;
+         tile = pair_tile(pair, ++local, npairs, p.snake)) {
       Tile t;
       decode_tile(p, tile, t);
       const TcGroup& G = p.g[t.g];
@@ -1191,7 +1196,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads(MODE), 1)
           __syncwarp();
         } else if (FINAL) {
           store_final(oe, S, i0, jb, G.M, G.N, G.orig_cols, lane, w);
-        } else if (STAGE == NS_APPLY && G.out_kind == OUTK_F32) {
+        } else if (MODE == OUT_WORKSPACE_KIND && G.out_kind == OUTK_F32) {
           // fp32: two 32-column halves, each through the staging buffer (32 rows of 128
           // bytes) and a bulk store
 #pragma unroll
@@ -1211,7 +1216,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads(MODE), 1)
             }
             __syncwarp();
           }
-        } else if (STAGE == NS_APPLY && G.out_kind == OUTK_PARTS) {
+        } else if (MODE == OUT_WORKSPACE_KIND && G.out_kind == OUTK_PARTS) {
           // the bf16 parts hi | hi | mid | lo of the fp32 values, out_ld / 4 columns apart,
           // each through the staging buffer and bulk stores (the buffer must have been read
           // by the warp's previous bulk store before it is rewritten)
@@ -1361,17 +1366,17 @@ mao_status tc_encode_store_map(CUtensorMap* map, const void* base, int64_t rows,
 mao_status tc_gemm_launch(const TcParams& p, cudaStream_t stream) {
   if (p.total_tiles <= 0) return MAO_OK;
   using Kernel = void (*)(TcParams);
-  const Kernel kernels[7] = {
+  const Kernel kernels[8] = {
       ns_tc_kernel<NS_GRAM, OUT_WORKSPACE>, ns_tc_kernel<NS_POLY, OUT_WORKSPACE>,
       ns_tc_kernel<NS_APPLY, OUT_WORKSPACE>, ns_tc_kernel<NS_APPLY, OUT_CALLER>,
       ns_tc_kernel<TC_UPDATE, OUT_CALLER_BF16>, ns_tc_kernel<NS_APPLY, OUT_CALLER_BF16>,
-      ns_tc_kernel<TC_UPDATE, OUT_UPDATE_STREAM>};
+      ns_tc_kernel<TC_UPDATE, OUT_UPDATE_STREAM>, ns_tc_kernel<NS_APPLY, OUT_WORKSPACE_KIND>};
   static std::once_flag attr_once[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return MAO_ERR_CUDA;
   cudaError_t attr_err = cudaSuccess;
   std::call_once(attr_once[dev & 63], [&] {
-    for (int i = 0; i < 7; ++i) {
+    for (int i = 0; i < 8; ++i) {
       const size_t bytes = smem_of(i == 6 ? OUT_UPDATE_STREAM : OUT_WORKSPACE);
       const cudaError_t e =
           cudaFuncSetAttribute(kernels[i], cudaFuncAttributeMaxDynamicSharedMemorySize, int(bytes));
@@ -1394,7 +1399,11 @@ mao_status tc_gemm_launch(const TcParams& p, cudaStream_t stream) {
                            (p.stage == NS_APPLY && p.out_mode == OUT_CALLER_BF16)
                        ? OUT_CALLER_BF16
                        : OUT_CALLER;
-  const Kernel k = mode == OUT_UPDATE_STREAM ? kernels[6]
+  bool kind = false;  // a workspace output other than bf16
+  for (int g = 0; g < p.ngroups; ++g) kind = kind || p.g[g].out_kind != OUTK_BF16;
+  if (kind && (final_out || p.stage != NS_APPLY)) return MAO_ERR_INVALID_ARG;
+  const Kernel k = kind ? kernels[7]
+                   : mode == OUT_UPDATE_STREAM ? kernels[6]
                    : p.stage == TC_UPDATE  ? kernels[4]
                    : mode == OUT_CALLER_BF16 ? kernels[5]
                    : kernels[final_out ? 3 : p.stage - NS_GRAM];
