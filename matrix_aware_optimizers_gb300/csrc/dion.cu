@@ -468,58 +468,142 @@ __device__ __noinline__ void chol_write_w(const float* Wr, const float* Dk, __nv
   }
 }
 
-// Rows r0 .. r0 + NR - 1 (NR a multiple of 8), column `lane`, of Out = scale Lft In
-// (+ Out with ACC), 32 x 32 blocks, eight rows at a time: In's column is read into
-// registers first and Lft's rows by 16-byte broadcast reads, eight independent sums per
-// lane. Out may be Lft with SYNC (the warp has read a group's rows before any lane writes
-// them); with LOWER, Lft is lower triangular and the products above its diagonal are
-// skipped.
-template <int NR, bool ACC, bool LOWER, bool SYNC>
-__device__ __forceinline__ void blk_rows(const float* Lft, const float* In, float* Out, int r0, float scale,
-                                         int lane) {
-  static_assert(NR % 8 == 0, "rows in groups of eight");
-  float v[32];
+// Register-tiled products of 32 x 32 blocks (row stride kLd) for one warp. Lane (ri, ck) =
+// (lane & 7, lane >> 3) holds rows r0 + ri + 8u (u < NU) of the result. Every read of the
+// operands happens before any write of C, so C may be X (each warp writes only its own rows).
+
+// C = alpha X Y^T (+ C with ACC), the product over the columns of X and Y (both row-major):
+// columns ck + 4v (v < 8) of the lane's rows. The X and Y row reads (16 bytes) and the
+// entries' reads and writes are free of bank conflicts.
+template <int NU, bool ACC>
+__device__ __forceinline__ void blk_nt(const float* X, const float* Y, float* C, int r0, float alpha,
+                                       int lane) {
+  const int ri = lane & 7, ck = lane >> 3;
+  float acc[NU][8];
 #pragma unroll
-  for (int k = 0; k < 32; ++k) v[k] = In[k * kLd + lane];
-#pragma unroll 1
-  for (int g = r0; g < r0 + NR; g += 8) {
-    float o[8] = {};
+  for (int u = 0; u < NU; ++u)
 #pragma unroll
-    for (int q = 0; q < 32; q += 4) {
-      if (LOWER && q > g + 7) break;
+    for (int v = 0; v < 8; ++v) acc[u][v] = 0.0f;
+#pragma unroll 2
+  for (int j = 0; j < 32; j += 4) {
+    float4 x[NU], y[8];
 #pragma unroll
-      for (int t = 0; t < 8; ++t) {
-        const float4 l = ld4(Lft + (g + t) * kLd + q);
-        o[t] = __fmaf_rn(l.x, v[q], o[t]);
-        o[t] = __fmaf_rn(l.y, v[q + 1], o[t]);
-        o[t] = __fmaf_rn(l.z, v[q + 2], o[t]);
-        o[t] = __fmaf_rn(l.w, v[q + 3], o[t]);
+    for (int u = 0; u < NU; ++u) x[u] = ld4(X + (r0 + ri + 8 * u) * kLd + j);
+#pragma unroll
+    for (int v = 0; v < 8; ++v) y[v] = ld4(Y + (ck + 4 * v) * kLd + j);
+#pragma unroll
+    for (int u = 0; u < NU; ++u)
+#pragma unroll
+      for (int v = 0; v < 8; ++v) {
+        float a = acc[u][v];
+        a = __fmaf_rn(x[u].x, y[v].x, a);
+        a = __fmaf_rn(x[u].y, y[v].y, a);
+        a = __fmaf_rn(x[u].z, y[v].z, a);
+        a = __fmaf_rn(x[u].w, y[v].w, a);
+        acc[u][v] = a;
       }
-    }
-    if (SYNC) __syncwarp();
-#pragma unroll
-    for (int t = 0; t < 8; ++t) {
-      float* out = Out + (g + t) * kLd + lane;
-      *out = ACC ? *out + scale * o[t] : scale * o[t];
-    }
   }
-  if (SYNC) __syncwarp();
+  __syncwarp();
+#pragma unroll
+  for (int u = 0; u < NU; ++u)
+#pragma unroll
+    for (int v = 0; v < 8; ++v) {
+      float* c = C + (r0 + ri + 8 * u) * kLd + ck + 4 * v;
+      *c = ACC ? __fmaf_rn(alpha, acc[u][v], *c) : alpha * acc[u][v];
+    }
+  __syncwarp();
 }
 
-// Inverse step K, part 1, 2 or 3 (see the kernel below), one 8-row quarter of a block per
+// C = alpha X Y (+ C with ACC), the product over X's columns and Y's rows: columns
+// 8 ck .. 8 ck + 7 of the lane's rows (16-byte reads and writes).
+template <int NU, bool ACC>
+__device__ __forceinline__ void blk_nn(const float* X, const float* Y, float* C, int r0, float alpha,
+                                       int lane) {
+  const int ri = lane & 7, ck = lane >> 3;
+  float acc[NU][8];
+#pragma unroll
+  for (int u = 0; u < NU; ++u)
+#pragma unroll
+    for (int v = 0; v < 8; ++v) acc[u][v] = 0.0f;
+#pragma unroll 2
+  for (int k = 0; k < 32; k += 4) {
+    float4 x[NU];
+#pragma unroll
+    for (int u = 0; u < NU; ++u) x[u] = ld4(X + (r0 + ri + 8 * u) * kLd + k);
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+      const float4 y0 = ld4(Y + (k + kk) * kLd + 8 * ck), y1 = ld4(Y + (k + kk) * kLd + 8 * ck + 4);
+      const float yv[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
+#pragma unroll
+      for (int u = 0; u < NU; ++u) {
+        const float xv = kk == 0 ? x[u].x : kk == 1 ? x[u].y : kk == 2 ? x[u].z : x[u].w;
+#pragma unroll
+        for (int v = 0; v < 8; ++v) acc[u][v] = __fmaf_rn(xv, yv[v], acc[u][v]);
+      }
+    }
+  }
+  __syncwarp();
+#pragma unroll
+  for (int u = 0; u < NU; ++u) {
+    float* c = C + (r0 + ri + 8 * u) * kLd + 8 * ck;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      float4 o = make_float4(alpha * acc[u][4 * h], alpha * acc[u][4 * h + 1], alpha * acc[u][4 * h + 2],
+                             alpha * acc[u][4 * h + 3]);
+      if (ACC) {
+        const float4 old = ld4(c + 4 * h);
+        o = make_float4(old.x + o.x, old.y + o.y, old.z + o.z, old.w + o.w);
+      }
+      *reinterpret_cast<float4*>(c + 4 * h) = o;
+    }
+  }
+  __syncwarp();
+}
+
+// Inverse step K, part 1, 2 or 3 (see the kernel below), one 16-row half of a block per
 // item; nb - 1 - K block rows lie below K. Not inlined: the loop over the block columns
 // and the last two steps share its code, which is then fetched from memory once.
 __device__ __noinline__ void chol_inv_item(float* A, float* Wr, int part, int K, int item, int lane) {
-  const int r0 = 8 * (item & 3), b = item >> 2;
-  if (part == 1) {  // item < 4 K: W_KJ = -D_K T_KJ into Wr
-    blk_rows<8, false, true, false>(blk(A, K, K), blk(A, K, b), Wr + b * kBlk, r0, -1.0f, lane);
-  } else if (part == 2) {  // item < 4 (nb - 1 - K) K: T_IJ += L_IK W_KJ
+  const int r0 = 16 * (item & 1), b = item >> 1;
+  if (part == 1) {  // item < 2 K: W_KJ = -D_K T_KJ into Wr
+    blk_nn<2, false>(blk(A, K, K), blk(A, K, b), Wr + b * kBlk, r0, -1.0f, lane);
+  } else if (part == 2) {  // item < 2 (nb - 1 - K) K: T_IJ += L_IK W_KJ
     const int I = K + 1 + b / K, J = b % K;
-    blk_rows<8, true, false, false>(blk(A, I, K), Wr + J * kBlk, blk(A, I, J), r0, 1.0f, lane);
-  } else {  // item < 4 (nb - 1 - K): T_IK = L_IK D_K
+    blk_nn<2, true>(blk(A, I, K), Wr + J * kBlk, blk(A, I, J), r0, 1.0f, lane);
+  } else {  // item < 2 (nb - 1 - K): T_IK = L_IK D_K (in place)
     const int I = K + 1 + b;
-    blk_rows<8, false, false, true>(blk(A, I, K), blk(A, K, K), blk(A, I, K), r0, 1.0f, lane);
+    blk_nn<2, false>(blk(A, I, K), blk(A, K, K), blk(A, I, K), r0, 1.0f, lane);
   }
+}
+
+// Trailing work of block column J, one 16-row half of a block per item: the panel
+// L_IJ = A_IJ D_J^T (I = J + 2 + b, item < 2 t), or (trailing) A_IK -= L_IJ L_KJ^T over the
+// t blocks of column J + 1 below the diagonal and then the triangle K >= J + 2
+// (item < 2 (t + t (t + 1) / 2)). Not inlined (one copy of the code).
+__device__ __noinline__ void chol_trail_item(float* A, bool panel, int J, int t, int item, int lane) {
+  const int r0 = 16 * (item & 1);
+  int b = item >> 1;
+  if (panel) {
+    const int I = J + 2 + b;
+    blk_nt<2, false>(blk(A, I, J), blk(A, J, J), blk(A, I, J), r0, 1.0f, lane);
+    return;
+  }
+  int I, K;
+  if (b < t) {
+    I = J + 2 + b;
+    K = J + 1;
+  } else {
+    b -= t;
+    I = 0;
+    K = b;
+    while (K > I) {
+      K -= I + 1;
+      ++I;
+    }
+    I += J + 2;
+    K += J + 2;
+  }
+  blk_nt<2, true>(blk(A, I, J), blk(A, K, J), blk(A, I, K), r0, -1.0f, lane);
 }
 
 // One CTA per slot: S = L L^T (blocked right-looking Cholesky, 32 x 32 blocks in shared
@@ -587,60 +671,38 @@ __global__ void __launch_bounds__(kCholThreads, 1) dion_chol_kernel(const __grid
       const int K = J - 1;       // inverse step taken in this block column
       const int t = nb - J - 2;  // block rows below J + 1
       // the rest of block column J of the panel; inverse step K part (1)
-      const int np = 4 * t, n1 = K > 0 ? 4 * K : 0;
+      const int np = 2 * t, n1 = K > 0 ? 2 * K : 0;
       for (int item = h; item < np + n1; item += kHelpers) {
-        if (item < np) {
-          const int row0 = 32 * (J + 2) + 8 * item;
-          chol_panel(A, J, row0, row0 + 8, 0, 1, lane);
-        } else {
-          inv1(K, item - np);
-        }
+        if (item < np) chol_trail_item(A, true, J, t, item, lane);
+        else inv1(K, item - np);
       }
       hsync();
       // trailing blocks: t blocks of column J + 1 below the diagonal, then the triangle
       // K' >= J + 2; inverse step K part (2); block row K of W to global memory
-      const int nu = 4 * (t + t * (t + 1) / 2), n2 = K > 0 ? 4 * (nb - 1 - K) * K : 0;
+      const int nu = 2 * (t + t * (t + 1) / 2), n2 = K > 0 ? 2 * (nb - 1 - K) * K : 0;
       for (int item = h; item < nu + n2; item += kHelpers) {
-        if (item >= nu) {
-          inv2(K, item - nu);
-          continue;
-        }
-        int b = item >> 2, I, Kc;
-        if (b < t) {
-          I = J + 2 + b;
-          Kc = J + 1;
-        } else {
-          b -= t;
-          I = 0;
-          Kc = b;
-          while (Kc > I) {
-            Kc -= I + 1;
-            ++I;
-          }
-          I += J + 2;
-          Kc += J + 2;
-        }
-        chol_update<8>(A, J, I, Kc, 8 * (item & 3), lane);
+        if (item < nu) chol_trail_item(A, false, J, t, item, lane);
+        else inv2(K, item - nu);
       }
       if (K >= 0) chol_write_w(Wr, blk(A, K, K), e.Wsp, K, nb, ldr, false, h * 32 + lane, 32 * kHelpers);
       hsync();
       if (K >= 0)
-        for (int item = h; item < 4 * (nb - 1 - K); item += kHelpers) inv3(K, item);
+        for (int item = h; item < 2 * (nb - 1 - K); item += kHelpers) inv3(K, item);
     }
     __syncthreads();
   }
   // inverse steps nb - 2 and nb - 1 on all warps
   const int K = nb - 2;
   if (K >= 0) {
-    for (int item = warp; item < 4 * K; item += kWarps) inv1(K, item);
+    for (int item = warp; item < 2 * K; item += kWarps) inv1(K, item);
     __syncthreads();
-    for (int item = warp; item < 4 * K; item += kWarps) inv2(K, item);
+    for (int item = warp; item < 2 * K; item += kWarps) inv2(K, item);
     chol_write_w(Wr, blk(A, K, K), e.Wsp, K, nb, ldr, false, threadIdx.x, kCholThreads);
     __syncthreads();
-    if (warp < 4) inv3(K, warp);
+    if (warp < 2) inv3(K, warp);
     __syncthreads();
   }
-  for (int item = warp; item < 4 * (nb - 1); item += kWarps) inv1(nb - 1, item);
+  for (int item = warp; item < 2 * (nb - 1); item += kWarps) inv1(nb - 1, item);
   __syncthreads();
   chol_write_w(Wr, blk(A, nb - 1, nb - 1), e.Wsp, nb - 1, nb, ldr, true, threadIdx.x, kCholThreads);
 }
