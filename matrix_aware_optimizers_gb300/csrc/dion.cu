@@ -560,32 +560,31 @@ __device__ __forceinline__ void blk_nn(const float* X, const float* Y, float* C,
   __syncwarp();
 }
 
-// Inverse step K, part 1, 2 or 3 (see the kernel below), one 16-row half of a block per
-// item; nb - 1 - K block rows lie below K. Not inlined: the loop over the block columns
+// Inverse step K, part 1, 2 or 3 (see the kernel below), one block per item; nb - 1 - K
+// block rows lie below K. Not inlined: the loop over the block columns
 // and the last two steps share its code, which is then fetched from memory once.
 __device__ __noinline__ void chol_inv_item(float* A, float* Wr, int part, int K, int item, int lane) {
-  const int r0 = 16 * (item & 1), b = item >> 1;
-  if (part == 1) {  // item < 2 K: W_KJ = -D_K T_KJ into Wr
-    blk_nn<2, false>(blk(A, K, K), blk(A, K, b), Wr + b * kBlk, r0, -1.0f, lane);
-  } else if (part == 2) {  // item < 2 (nb - 1 - K) K: T_IJ += L_IK W_KJ
+  const int b = item;
+  if (part == 1) {  // item < K: W_KJ = -D_K T_KJ into Wr
+    blk_nn<4, false>(blk(A, K, K), blk(A, K, b), Wr + b * kBlk, 0, -1.0f, lane);
+  } else if (part == 2) {  // item < (nb - 1 - K) K: T_IJ += L_IK W_KJ
     const int I = K + 1 + b / K, J = b % K;
-    blk_nn<2, true>(blk(A, I, K), Wr + J * kBlk, blk(A, I, J), r0, 1.0f, lane);
-  } else {  // item < 2 (nb - 1 - K): T_IK = L_IK D_K (in place)
+    blk_nn<4, true>(blk(A, I, K), Wr + J * kBlk, blk(A, I, J), 0, 1.0f, lane);
+  } else {  // item < nb - 1 - K: T_IK = L_IK D_K (in place)
     const int I = K + 1 + b;
-    blk_nn<2, false>(blk(A, I, K), blk(A, K, K), blk(A, I, K), r0, 1.0f, lane);
+    blk_nn<4, false>(blk(A, I, K), blk(A, K, K), blk(A, I, K), 0, 1.0f, lane);
   }
 }
 
-// Trailing work of block column J, one 16-row half of a block per item: the panel
-// L_IJ = A_IJ D_J^T (I = J + 2 + b, item < 2 t), or (trailing) A_IK -= L_IJ L_KJ^T over the
-// t blocks of column J + 1 below the diagonal and then the triangle K >= J + 2
-// (item < 2 (t + t (t + 1) / 2)). Not inlined (one copy of the code).
+// Trailing work of block column J, one block per item: the panel L_IJ = A_IJ D_J^T
+// (I = J + 2 + item, item < t), or (trailing) A_IK -= L_IJ L_KJ^T over the t blocks of
+// column J + 1 below the diagonal and then the triangle K >= J + 2
+// (item < t + t (t + 1) / 2). Not inlined (one copy of the code).
 __device__ __noinline__ void chol_trail_item(float* A, bool panel, int J, int t, int item, int lane) {
-  const int r0 = 16 * (item & 1);
-  int b = item >> 1;
+  int b = item;
   if (panel) {
     const int I = J + 2 + b;
-    blk_nt<2, false>(blk(A, I, J), blk(A, J, J), blk(A, I, J), r0, 1.0f, lane);
+    blk_nt<4, false>(blk(A, I, J), blk(A, J, J), blk(A, I, J), 0, 1.0f, lane);
     return;
   }
   int I, K;
@@ -603,7 +602,7 @@ __device__ __noinline__ void chol_trail_item(float* A, bool panel, int J, int t,
     I += J + 2;
     K += J + 2;
   }
-  blk_nt<2, true>(blk(A, I, J), blk(A, K, J), blk(A, I, K), r0, -1.0f, lane);
+  blk_nt<4, true>(blk(A, I, J), blk(A, K, J), blk(A, I, K), 0, -1.0f, lane);
 }
 
 // One CTA per slot: S = L L^T (blocked right-looking Cholesky, 32 x 32 blocks in shared
@@ -621,9 +620,9 @@ __device__ __noinline__ void chol_trail_item(float* A, bool panel, int J, int t,
 // For each block column J of the factorisation:
 //   critical path (all warps): block row J + 1 of the panel, L_J+1,J = A_J+1,J D_J^T, then
 //   the diagonal block A_J+1,J+1 -= L_J+1,J L_J+1,J^T; then warp 0 factors and inverts the
-//   diagonal block J + 1 (chol_inv32) while the warps off warp 0's sub-partition finish the
-//   panel (L_IJ for I >= J + 2), update the trailing blocks A_IK, J + 1 <= K <= I,
-//   I >= J + 2, and take inverse step J - 1 (all of it in items of eight rows).
+//   diagonal block J + 1 (chol_inv32) while the other warps finish the panel (L_IJ for
+//   I >= J + 2), update the trailing blocks A_IK, J + 1 <= K <= I, I >= J + 2, and take
+//   inverse step J - 1 (one block per item, register-tiled).
 // The last two inverse steps run on all warps at the end. S arrives in this block layout
 // (the assemble kernel writes it so). Rows and columns past r are the identity. A pivot
 // that is not positive sets the device error word (P had dependent columns).
@@ -638,7 +637,7 @@ __global__ void __launch_bounds__(kCholThreads, 1) dion_chol_kernel(const __grid
   float* Wr = A + nlow * kBlk;   // nb - 1 blocks: the block row of W of the current inverse step
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   constexpr int kWarps = kCholThreads / 32;
-  constexpr int kHelpers = kWarps - kWarps / 4;  // warps with warp % 4 != 0
+  constexpr int kHelpers = kWarps - 1;  // every warp but warp 0
   // the lower blocks of S (their Gram entries past r are zero), then ones on the diagonal
   // past r
   for (int q = threadIdx.x; q < nlow * kBlk / 4; q += kCholThreads)
@@ -663,15 +662,15 @@ __global__ void __launch_bounds__(kCholThreads, 1) dion_chol_kernel(const __grid
     __syncthreads();
     if (warp == 0) {
       if (chol_inv32(blk(A, J + 1, J + 1), col, lane) && lane == 0) atomicOr(&g_dion_error, 1u);
-    } else if (warp % 4 != 0) {
-      // the warps that do not share warp 0's sub-partition (warp w runs on sub-partition
-      // w % 4), numbered h = 0 .. kHelpers - 1
-      const int h = warp - warp / 4 - 1;
+    } else {
+      // the other warps, numbered h = 0 .. kHelpers - 1 (sharing warp 0's sub-partition
+      // slows the factorisation less than leaving three warps idle)
+      const int h = warp - 1;
       auto hsync = [] { asm volatile("bar.sync 1, %0;" ::"r"(32 * kHelpers) : "memory"); };
       const int K = J - 1;       // inverse step taken in this block column
       const int t = nb - J - 2;  // block rows below J + 1
       // the rest of block column J of the panel; inverse step K part (1)
-      const int np = 2 * t, n1 = K > 0 ? 2 * K : 0;
+      const int np = t, n1 = K > 0 ? K : 0;
       for (int item = h; item < np + n1; item += kHelpers) {
         if (item < np) chol_trail_item(A, true, J, t, item, lane);
         else inv1(K, item - np);
@@ -679,7 +678,7 @@ __global__ void __launch_bounds__(kCholThreads, 1) dion_chol_kernel(const __grid
       hsync();
       // trailing blocks: t blocks of column J + 1 below the diagonal, then the triangle
       // K' >= J + 2; inverse step K part (2); block row K of W to global memory
-      const int nu = 2 * (t + t * (t + 1) / 2), n2 = K > 0 ? 2 * (nb - 1 - K) * K : 0;
+      const int nu = t + t * (t + 1) / 2, n2 = K > 0 ? (nb - 1 - K) * K : 0;
       for (int item = h; item < nu + n2; item += kHelpers) {
         if (item < nu) chol_trail_item(A, false, J, t, item, lane);
         else inv2(K, item - nu);
@@ -687,22 +686,22 @@ __global__ void __launch_bounds__(kCholThreads, 1) dion_chol_kernel(const __grid
       if (K >= 0) chol_write_w(Wr, blk(A, K, K), e.Wsp, K, nb, ldr, false, h * 32 + lane, 32 * kHelpers);
       hsync();
       if (K >= 0)
-        for (int item = h; item < 2 * (nb - 1 - K); item += kHelpers) inv3(K, item);
+        for (int item = h; item < nb - 1 - K; item += kHelpers) inv3(K, item);
     }
     __syncthreads();
   }
   // inverse steps nb - 2 and nb - 1 on all warps
   const int K = nb - 2;
   if (K >= 0) {
-    for (int item = warp; item < 2 * K; item += kWarps) inv1(K, item);
+    for (int item = warp; item < K; item += kWarps) inv1(K, item);
     __syncthreads();
-    for (int item = warp; item < 2 * K; item += kWarps) inv2(K, item);
+    for (int item = warp; item < K; item += kWarps) inv2(K, item);
     chol_write_w(Wr, blk(A, K, K), e.Wsp, K, nb, ldr, false, threadIdx.x, kCholThreads);
     __syncthreads();
-    if (warp < 2) inv3(K, warp);
+    if (warp < 1) inv3(K, warp);
     __syncthreads();
   }
-  for (int item = warp; item < 2 * (nb - 1); item += kWarps) inv1(nb - 1, item);
+  for (int item = warp; item < nb - 1; item += kWarps) inv1(nb - 1, item);
   __syncthreads();
   chol_write_w(Wr, blk(A, nb - 1, nb - 1), e.Wsp, nb - 1, nb, ldr, true, threadIdx.x, kCholThreads);
 }
