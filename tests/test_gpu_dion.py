@@ -124,6 +124,32 @@ def test_dion_exact_low_rank_gives_polar_factor(cuda):
     assert rel_fro(to_np(M), 0.8 * G.double().cpu().numpy()) <= TOL
 
 
+@pytest.mark.parametrize("m,n,r", [(768, 1024, 64), (3072, 768, 192), (300, 500, 40)])
+def test_dion_basis_orthonormal_when_ill_conditioned(cuda, m, n, r):
+    # independent of the oracle: B Q_prev with singular values spread over three decades
+    # (kappa about 1e3, so one Cholesky QR pass leaves an error near kappa^2 times the
+    # Gram's): after the two passes the fp32 copy of P is orthonormal to about 2^-17 (the
+    # bf16-part products), checked at 2e-4, ten times tighter than the parity test's bound
+    gen = torch.Generator().manual_seed(85 + r)
+    U = torch.linalg.qr(torch.randn((m, r), generator=gen, dtype=torch.float64))[0]
+    V = torch.linalg.qr(torch.randn((n, r), generator=gen, dtype=torch.float64))[0]
+    S = torch.logspace(0.0, -3.0, r, dtype=torch.float64)
+    G = ((U * S) @ V.T).float().to(cuda)
+    M = torch.zeros((m, n), dtype=torch.float32, device=cuda)
+    X = torch.zeros((m, n), dtype=torch.float32, device=cuda)
+    Qp = V + 0.05 * torch.randn((n, r), generator=gen, dtype=torch.float64) / n ** 0.5
+    Q = (Qp / Qp.norm(dim=0, keepdim=True)).float().to(cuda).contiguous()
+    P = torch.empty((m, r), dtype=torch.float32, device=cuda)
+    mao.dion_step(X, M, G, Q, mu=0.9, lr=0.1, P_out=P)
+    mao.sync_status()
+    Pd = P.double().cpu()
+    assert (Pd.T @ Pd - torch.eye(r, dtype=torch.float64)).abs().max().item() <= 2e-4
+    # the basis contains the leading half of B's left singular space (the trailing
+    # directions, down to 1e-3 of the largest, are within the bf16 rounding of B Q_prev)
+    C = Pd.T @ U[:, : r // 2]
+    assert (C.T @ C - torch.eye(r // 2, dtype=torch.float64)).abs().max().item() <= 1e-2
+
+
 def test_dion_zero_buffer_reports_numeric_error(cuda):
     # B = 0: B Q has no column rank, the Cholesky pivot is zero; the step leaves X and M
     # at zero and mao_sync_status reports MAO_ERR_NUMERIC (no device fault)
