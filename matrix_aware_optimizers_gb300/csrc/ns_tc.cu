@@ -823,30 +823,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads(MODE), 1)
       // a diagonal tile of a product of a buffer with itself: the B half equals the A half
       const bool share = G.same_ab && t.row0 == t.col0;
       const uint32_t tx_bytes = (share ? 2u : 4u) * uint32_t(HALF_BYTES);  // both CTAs
-      if (STAGE == TC_UPDATE && t.nkb <= 2) {
-        // a short product (rank-r update): the epilogue, which will read this CTA's 128 rows
-        // of the caller's matrix a tile or two from now, is the bottleneck. Have L2 fetch
-        // them while the operands load. With longer products the prefetched rows displace
-        // operand panels from L2 and the prefetch does not pay.
-        if (!dep_done) {
-          asm volatile("griddepcontrol.wait;" ::: "memory");
-          dep_done = true;
-        }
-        const OutEntry oe = p.out_table[G.slot0 + t.z];
-        if (oe.flags & OUT_VEC) {
-          const int es = oe.dtype == MAO_BF16 ? 2 : 4;
-          const uint32_t bytes = uint32_t(min(BN, G.N - t.col0) * es) & ~15u;
-          const int r0 = t.row0 + HALF * int(cta);
-          // one 128-byte line per lane and step, eight lines (up to 1 KB) per row
-          const uint8_t* src = reinterpret_cast<const uint8_t*>(upd_src(oe));
-          const int64_t sld = upd_src_ld(oe);
-          for (int q = lane; q < HALF * 8; q += 32) {
-            const int64_t row = r0 + (q >> 3);
-            const uint32_t off = uint32_t(q & 7) * 128u;
-            if (row < G.M && off < bytes) prefetch_l2(src + (row * sld + t.col0) * es + off);
-          }
-        }
-      }
       for (int kb = 0; kb < t.nkb; ++kb) {
         int okw = 1;
         if (lane == 0) {
@@ -885,6 +861,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads(MODE), 1)
         if (++stage == NST) {
           stage = 0;
           phase ^= 1u;
+        }
+      }
+      if (ok && STAGE == TC_UPDATE && t.nkb <= 2) {
+        // a short product (rank-r update): the epilogue, which will read this CTA's 128 rows
+        // of the caller's matrix a tile or two from now, is the bottleneck. Have L2 fetch
+        // them while the operands load; issued after the tile's operand loads, which would
+        // otherwise queue behind them (the first tile's data came 3 to 4 us later). With
+        // longer products the prefetched rows displace operand panels from L2 and the
+        // prefetch does not pay.
+        const OutEntry oe = p.out_table[G.slot0 + t.z];
+        if (oe.flags & OUT_VEC) {
+          const int es = oe.dtype == MAO_BF16 ? 2 : 4;
+          const uint32_t bytes = uint32_t(min(BN, G.N - t.col0) * es) & ~15u;
+          const int r0 = t.row0 + HALF * int(cta);
+          // one 128-byte line per lane and step, eight lines (up to 1 KB) per row
+          const uint8_t* src = reinterpret_cast<const uint8_t*>(upd_src(oe));
+          const int64_t sld = upd_src_ld(oe);
+          for (int q = lane; q < HALF * 8; q += 32) {
+            const int64_t row = r0 + (q >> 3);
+            const uint32_t off = uint32_t(q & 7) * 128u;
+            if (row < G.M && off < bytes) prefetch_l2(src + (row * sld + t.col0) * es + off);
+          }
         }
       }
     }
