@@ -133,6 +133,13 @@ __global__ void __launch_bounds__(64) dion_setup_kernel(const __grid_constant__ 
   p.c.tX[z] = o;
 }
 
+// Lets the next launch in the stream (a tensor-core product, launched with programmatic
+// stream serialization) start its set-up on the SMs this grid leaves free; the product
+// still waits for this grid's completion (griddepcontrol.wait) before it reads any result.
+__device__ __forceinline__ void allow_dependent_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- B = M + G, Qw
 
 __device__ __forceinline__ float round_to(float v, int32_t dt) {
@@ -213,6 +220,7 @@ __device__ __forceinline__ void dion_stage_unit(const DionSlot& e, int64_t row, 
 constexpr int kStageUnits = 4;
 
 __global__ void __launch_bounds__(256) dion_stage_kernel(const __grid_constant__ DionCommon c) {
+  allow_dependent_launch();
   const DionSlot& e = c.slots[blockIdx.y];
   const uint32_t upr = uint32_t(e.ldn) / 8;
   const uint32_t units = uint32_t(e.m) * upr;
@@ -629,6 +637,7 @@ __device__ __noinline__ void chol_trail_item(float* A, bool panel, int J, int t,
 __global__ void __launch_bounds__(kCholThreads, 1) dion_chol_kernel(const __grid_constant__ DionCommon c) {
   extern __shared__ __align__(16) float sm[];
   __shared__ __align__(16) float col[128];  // chol_inv32's column broadcast (two buffers)
+  allow_dependent_launch();
   const DionSlot& e = c.slots[blockIdx.x];
   const int r = c.r, ldr = c.ldr;
   const int nb = (r + 31) / 32;
@@ -790,6 +799,7 @@ __global__ void __launch_bounds__(256) dion_norm_kernel(const __grid_constant__ 
 // Q = R / ||R_:j|| (times the reciprocal norm; a zero column stays zero) into the caller's
 // Q, and the bf16 copies Qw, Rw; 8 columns per thread, 16-byte accesses.
 __global__ void __launch_bounds__(256) dion_q_kernel(const __grid_constant__ DionCommon c) {
+  allow_dependent_launch();
   const DionSlot& e = c.slots[blockIdx.y];
   const uint32_t upr = uint32_t(c.ldr) / 8;
   const uint32_t u = blockIdx.x * blockDim.x + threadIdx.x;
