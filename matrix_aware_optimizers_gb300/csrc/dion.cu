@@ -910,17 +910,22 @@ int out_flags(const mao_mat& a) {
 // B Q_prev, R, the Gram products and the multiplies go to workspace buffers through bulk
 // stores (eight epilogue warps); only the final P with a caller's copy, and the updates, go
 // through the slots' output entries (`table`).
+// op 6: both in-place updates in one launch (M with alpha through table[slot], X with alpha2
+// through table[batch + slot]), so that their tiles share the rounds.
 mao_status dion_tc(const DionPlan& plan, uint8_t* ws, const OutEntry* table, int op, float alpha,
-                   cudaStream_t stream, int pass = 0) {
+                   cudaStream_t stream, int pass = 0, float alpha2 = 0.0f) {
   const int64_t r = plan.r, ldr = plan.ldr;
+  const int32_t batch = int32_t(plan.input_of.size());
   // The kernel deals tiles to CTA pairs in rounds, every other one reversed; listing the groups with
   // the deepest products (the most k-blocks per tile) first spreads the long tiles over the
   // pairs before the short ones fill the gaps.
-  std::vector<size_t> order(plan.groups.size());
-  for (size_t i = 0; i < order.size(); ++i) order[i] = i;
-  auto depth = [&](size_t i) {
-    const DionGroup& g = plan.groups[i];
-    switch (op) {
+  std::vector<std::pair<size_t, int>> order;  // (group, product) in launch order
+  for (size_t i = 0; i < plan.groups.size(); ++i) order.push_back({i, op == 6 ? 2 : op});
+  if (op == 6)
+    for (size_t i = 0; i < plan.groups.size(); ++i) order.push_back({i, 3});
+  auto depth = [&](const std::pair<size_t, int>& it) {
+    const DionGroup& g = plan.groups[it.first];
+    switch (it.second) {
       case 0: return g.n;
       case 1: return g.m;
       case 4: return 3 * ldr;
@@ -929,24 +934,28 @@ mao_status dion_tc(const DionPlan& plan, uint8_t* ws, const OutEntry* table, int
     }
   };
   std::stable_sort(order.begin(), order.end(),
-                   [&](size_t x, size_t y) { return depth(x) > depth(y); });
-  for (size_t g0 = 0; g0 < plan.groups.size(); g0 += tc::MAX_GROUPS) {
+                   [&](const std::pair<size_t, int>& x, const std::pair<size_t, int>& y) {
+                     return depth(x) > depth(y);
+                   });
+  const bool update = op == 2 || op == 3 || op == 6;
+  for (size_t g0 = 0; g0 < order.size(); g0 += tc::MAX_GROUPS) {
     TcParams p;
     memset(&p, 0, sizeof(p));
-    p.stage = (op == 2 || op == 3) ? TC_UPDATE : NS_APPLY;
+    p.stage = update ? TC_UPDATE : NS_APPLY;
     p.a = alpha;
     p.scale = nullptr;
     p.out_table = table;
     p.timeout_ns = wait_limit_ns();
     p.snake = 1;  // tiles of mixed depths, deepest groups first
     int64_t tiles = 0;
-    for (size_t gi = g0; gi < plan.groups.size() && p.ngroups < tc::MAX_GROUPS; ++gi) {
-      const DionGroup& g = plan.groups[order[gi]];
+    for (size_t gi = g0; gi < order.size() && p.ngroups < tc::MAX_GROUPS; ++gi) {
+      const DionGroup& g = plan.groups[order[gi].first];
+      const int gop = order[gi].second;  // this group's product
       TcGroup& G = p.g[p.ngroups++];
       const int64_t ldn = round_up(g.n, tc::LD_ALIGN);
       const void *A, *B;
       int64_t rowsA, ldA, rowsB, ldB, colsA = -1, colsB = -1;
-      switch (op) {
+      switch (gop) {
         case 0:  // (m x n)(n x ldr): Bw K-major, Qw MN-major (zeros past r)
           A = ws + g.off_bw; rowsA = g.m; ldA = ldn; G.a_mn = 0;
           B = ws + g.off_qw; rowsB = g.n; ldB = ldr; G.b_mn = 1;
@@ -971,12 +980,14 @@ mao_status dion_tc(const DionPlan& plan, uint8_t* ws, const OutEntry* table, int
           break;
         default:  // (m x r)(r x n): Pw K-major, Rw / Qw K-major
           A = ws + g.off_pw; rowsA = g.m; ldA = ldr; G.a_mn = 0;
-          B = ws + (op == 2 ? g.off_rw : g.off_qw); rowsB = g.n; ldB = ldr; G.b_mn = 0;
+          B = ws + (gop == 2 ? g.off_rw : g.off_qw); rowsB = g.n; ldB = ldr; G.b_mn = 0;
           G.M = int32_t(g.m); G.N = int32_t(g.n); G.K = int32_t(r);
           break;
       }
       G.count = g.count;
-      G.slot0 = g.slot0;
+      // the X update's entries follow the M update's in the combined launch's table
+      G.slot0 = g.slot0 + (op == 6 && gop == 3 ? batch : 0);
+      G.alpha = op == 6 && gop == 3 ? alpha2 : alpha;
       G.orig_cols = G.N;
       // workspace outputs: B Q_prev and the first pass's P W^T as the bf16 parts of the next
       // Cholesky QR pass, the final P W^T as Pw (bf16) unless the caller wants a copy of P,
@@ -1151,9 +1162,8 @@ mao_status dion_run(const mao_mat* X, const mao_mat* M, const mao_mat* G, const 
   dion_q_kernel<<<dim3(blocks(plan.max_qunits), nb), 256, 0, stream>>>(c);
   if (!launched()) return MAO_ERR_CUDA;
   // 6. M <- B - (1 - mu) P R^T ; X <- X - lr P Q^T (in place)
-  st = dion_tc(plan, ws, c.tM, 2, -(1.0f - mu), stream);
-  if (st != MAO_OK) return st;
-  return dion_tc(plan, ws, c.tX, 3, -lr, stream);
+  // (both in one launch: the X update's table entries follow the M update's)
+  return dion_tc(plan, ws, c.tM, 6, -(1.0f - mu), stream, 0, -lr);
 }
 
 mao_status dion_read_and_clear_error(cudaStream_t stream) {

@@ -562,6 +562,7 @@ mao_status run_tc_stage(const Buffers& buf, const std::vector<const NsGroupPlan*
   if (last && stage == NS_APPLY && std::isfinite(update_alpha)) {
     p.stage = TC_UPDATE;
     p.a = update_alpha;
+    for (int g = 0; g < p.ngroups; ++g) p.g[g].alpha = update_alpha;
   }
   return tc_gemm_launch(p, stream);
 }

@@ -142,6 +142,7 @@ struct TcGroup {
                             // mid = bf16(x - hi), lo = bf16(x - hi - mid)), out_ld / 4
                             // columns apart; OUTK_F32 (tmOR from tc_encode_store_map_f32)
   int32_t orig_cols;        // C of the original matrix (sign-bit indexing)
+  float alpha;              // TC_UPDATE: out <- out + alpha (A B^T) for this group's outputs
 };
 
 struct TcParams {

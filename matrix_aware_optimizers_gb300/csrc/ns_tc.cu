@@ -1061,8 +1061,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads(MODE), 1)
           for (int c = 0; c < 64; ++c) w[c] *= s;
         }
         vec[pos] = upd_block_vec(oc, jb, G.N);
-        if (vec[pos]) slot_apply(slots + ((j0 + pos) % STREAM_SLOTS) * EP_BYTES, lane, w, p.a);
-        else update_final(oc, i0, jb, G.M, G.N, lane, w, p.a);
+        if (vec[pos]) slot_apply(slots + ((j0 + pos) % STREAM_SLOTS) * EP_BYTES, lane, w, G.alpha);
+        else update_final(oc, i0, jb, G.M, G.N, lane, w, G.alpha);
       }
       tc_fence_before();
       __syncwarp();
@@ -1185,8 +1185,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads(MODE), 1)
           for (int c = 0; c < 64; ++c) w[c] *= s;
         }
         if (STAGE == TC_UPDATE) {
-          if (upd_block_vec(oe, jb, G.N)) upd_apply(S, lane, w, p.a, nth == 0 ? res0 : res1);
-          else update_final(oe, i0, jb, G.M, G.N, lane, w, p.a);
+          if (upd_block_vec(oe, jb, G.N)) upd_apply(S, lane, w, G.alpha, nth == 0 ? res0 : res1);
+          else update_final(oe, i0, jb, G.M, G.N, lane, w, G.alpha);
         } else if (MODE == OUT_CALLER_BF16) {
           stage_rows(S, lane, w);
           __syncwarp();
