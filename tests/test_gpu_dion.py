@@ -90,6 +90,21 @@ def test_dion_batch_and_mixed_shapes(cuda):
         _check(oracle.dion_step(*h, mu=0.95, lr=0.3), h, s[0], s[1], s[3], P, 0.95, 0.3)
 
 
+def test_dion_deep_and_shallow_groups(cuda):
+    # groups of 2048-row matrices next to 256- and 300-row ones: products of very different
+    # depths in each launch (tiles dealt deepest first)
+    gen = torch.Generator().manual_seed(86)
+    shapes = [(256, 512, 32), (2048, 512, 32), (2048, 512, 32), (300, 700, 32)]
+    sets = [_inputs(gen, m, n, r, "bf16", "f32", cuda) for m, n, r in shapes]
+    hosts = [[to_np(t) for t in s] for s in sets]
+    Ps = [torch.empty((m, r), dtype=torch.float32, device=cuda) for m, n, r in shapes]
+    mao.dion_step([s[0] for s in sets], [s[1] for s in sets], [s[2] for s in sets],
+                  [s[3] for s in sets], mu=0.95, lr=0.3, P_out=Ps)
+    mao.sync_status()
+    for s, h, P in zip(sets, hosts, Ps):
+        _check(oracle.dion_step(*h, mu=0.95, lr=0.3), h, s[0], s[1], s[3], P, 0.95, 0.3)
+
+
 def test_dion_two_steps_warm_start(cuda):
     gen = torch.Generator().manual_seed(83)
     X, M, G, Q = _inputs(gen, 512, 1024, 128, "f32", "f32", cuda)
