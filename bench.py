@@ -234,6 +234,8 @@ class Step:
         self.block = block
         self.fused = fused and wl.kind == "muon" and block is None and wl.compute == "bf16"
         # Sign-Muon, 1-bit variant: the four stages as one sign_muon_step call
+        self._sign_call = {}  # prepared sign_muon_step calls by stream
+        self._current_stream = torch.cuda.current_stream
         self.fused_sign = fused and wl.kind == "sign" and variant == "bits" and not post_polar \
             and dplan is None
         self.W, self.M, self.G = inputs["W"], inputs["M"], inputs["G"]
@@ -405,9 +407,17 @@ class Step:
             self.fused_call()
             return
         if self.fused_sign:
-            wl = self.wl
-            self.mao.sign_muon_step(self.W[0], self.M, self.G, self.words, self.vote, wl.mu,
-                                    wl.lr, wl.steps, wl.coeffs, wl.eps, wl.compute, ws=self.ws)
+            # the call's arguments marshalled once per stream (the tensors keep their
+            # storage), as a training loop would hold them
+            key = self._current_stream().cuda_stream
+            call = self._sign_call.get(key)
+            if call is None:
+                wl = self.wl
+                call = self.mao.sign_muon_step(
+                    self.W[0], self.M, self.G, self.words, self.vote, wl.mu, wl.lr, wl.steps,
+                    wl.coeffs, wl.eps, wl.compute, ws=self.ws, prepare=True)
+                self._sign_call[key] = call
+            call()
             return
         self.momentum()
         self.ns()

@@ -197,11 +197,29 @@ def muon_step_host(W, M, G, mu, lr, g_host, g_dev, w_host, w_dev, steps=5, coeff
     _abi.check("muon_step_host", st)
 
 
+class PreparedCall:
+    """A library call whose arguments were marshalled once: calling the object repeats the
+    call with the same tensors (which must keep their storage), scalars and stream. For
+    training loops whose step is short enough that building the arguments on the host each
+    time would cost more than the GPU work."""
+
+    def __init__(self, name, args, keep):
+        self._fn = getattr(lib(), name)
+        self._name = name
+        self._args = args
+        self._keep = keep  # the tensors and ctypes objects the arguments point into
+
+    def __call__(self):
+        _abi.check(self._name, self._fn(*self._args))
+
+
 def sign_muon_step(W, M, G, words, vote, mu, lr, steps=5, coeffs=QUINTIC, eps=1e-7,
-                   compute="bf16", ws=None, stream=None):
+                   compute="bf16", ws=None, stream=None, prepare=False):
     """One whole Sign-Muon step: momentum of every worker, Newton-Schulz with the packed
     signs into words[m] (int32 tensor [W_n][stride]), the majority vote into `vote` and
-    W <- W - lr * vote; the same results as the four separate calls."""
+    W <- W - lr * vote; the same results as the four separate calls. With prepare=True the
+    call is not made: a PreparedCall that makes it (on `stream`, or the stream current now)
+    is returned."""
     Ms, Gs = _as_list(M), _as_list(G)
     if len(Ms) != len(Gs) or words.dim() != 2 or words.shape[0] != len(Ms) or \
             words.stride(1) != 1 or words.dtype != torch.int32:
@@ -209,12 +227,14 @@ def sign_muon_step(W, M, G, words, vote, mu, lr, steps=5, coeffs=QUINTIC, eps=1e
     carr, stride = _coeff_args(coeffs, steps)
     if ws is None:
         ws = workspace(Ms, compute, Ms[0].device)
-    st = lib().sign_muon_step(ctypes.byref(_mat(W)), _mats(Ms), _mats(Gs), len(Ms),
-                              ctypes.c_void_p(words.data_ptr()), words.stride(0),
-                              ctypes.c_void_p(vote.data_ptr()), float(mu), float(lr), int(steps),
-                              carr, stride, float(eps), _COMPUTE[compute],
-                              ctypes.c_void_p(ws.data_ptr()), ws.numel(), _stream(stream))
-    _abi.check("sign_muon_step", st)
+    wm, ma, ga = _mat(W), _mats(Ms), _mats(Gs)
+    args = (ctypes.byref(wm), ma, ga, len(Ms), ctypes.c_void_p(words.data_ptr()), words.stride(0),
+            ctypes.c_void_p(vote.data_ptr()), float(mu), float(lr), int(steps), carr, stride,
+            float(eps), _COMPUTE[compute], ctypes.c_void_p(ws.data_ptr()), ws.numel(),
+            _stream(stream))
+    if prepare:
+        return PreparedCall("sign_muon_step", args, (W, Ms, Gs, words, vote, ws, wm, ma, ga, carr))
+    _abi.check("sign_muon_step", lib().sign_muon_step(*args))
 
 
 def _coeff_args(coeffs, steps):

@@ -393,6 +393,50 @@ void launch_vote(int64_t blocks, cudaStream_t stream, const uint32_t* bits, int3
                                                                      P, T);
 }
 
+// The vote and the update of W in one pass: thread w forms vote word w (as vote_kernel, one
+// word per thread) and applies it to W's entries k = 32 w .. 32 w + 31 (row-major),
+// W <- fma(-lr, v, W) with v = +1 / -1, rounded to W's dtype (the update kernel's
+// arithmetic). With vec (contiguous 16-byte-aligned rows, cols a multiple of 8) the 32
+// entries are four 8-element units of one row.
+template <int PL>
+__global__ void __launch_bounds__(256) vote_update_kernel(const uint32_t* __restrict__ bits, int32_t nw,
+                                                          int64_t stride, int64_t nbits,
+                                                          uint32_t* __restrict__ vote, int P, uint32_t T,
+                                                          void* W, int64_t cols, int64_t ld, int32_t dt,
+                                                          int32_t vec, float lr) {
+  const int64_t nwords = (nbits + 31) / 32;
+  const int64_t w = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (w >= nwords) return;
+  uint32_t plane[PL];
+#pragma unroll
+  for (int p = 0; p < PL; ++p) plane[p] = 0;
+#pragma unroll 4
+  for (int m = 0; m < nw; ++m) counter_add<PL>(plane, P, __ldg(bits + int64_t(m) * stride + w));
+  uint32_t v = counter_ge<PL>(plane, P, T);
+  if (w == nwords - 1 && (nbits & 31)) v &= (1u << (nbits & 31)) - 1u;
+  vote[w] = v;
+  const int64_t k0 = 32 * w;
+  const int cnt = int(nbits - k0 < 32 ? nbits - k0 : 32);
+  const int64_t row0 = k0 / cols, col0 = k0 - row0 * cols;
+  if (vec && cnt == 32 && col0 + 32 <= cols) {
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      float a[8];
+      const int64_t at = row0 * ld + col0 + 8 * u;
+      load8(W, at, dt, a);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) a[i] = __fmaf_rn(-lr, ((v >> (8 * u + i)) & 1u) ? 1.0f : -1.0f, a[i]);
+      store8(W, at, dt, a);
+    }
+  } else {
+    for (int b = 0; b < cnt; ++b) {
+      const int64_t k = k0 + b, row = k / cols, col = k - row * cols;
+      const float x = load_elem(W, row * ld + col, dt);
+      store_elem(W, row * ld + col, dt, __fmaf_rn(-lr, ((v >> b) & 1u) ? 1.0f : -1.0f, x));
+    }
+  }
+}
+
 }  // namespace
 
 // ---------------------------------------------------------------- entry points
@@ -463,6 +507,30 @@ mao_status vote_int8_launch(const int8_t* s, int32_t n_workers, int64_t stride, 
         sbar ? sbar + bulk : nullptr, vote ? vote + bulk / 32 : nullptr);
     count_launch();
   }
+  return cuda_status(cudaGetLastError());
+}
+
+mao_status vote_update_launch(const uint32_t* bits, int32_t n_workers, int64_t stride,
+                              int64_t nbits, uint32_t* vote, const mao_mat& W, float lr,
+                              cudaStream_t stream) {
+  const int64_t nwords = ceil_div(nbits, 32);
+  int P = 0;
+  while ((int64_t(1) << P) <= n_workers) ++P;  // n_workers < 2^P
+  const uint32_t T = uint32_t((n_workers + 1) / 2);  // count of +1 needed: 2*cnt >= W_n
+  const bool vec = W.cols % 8 == 0 && reinterpret_cast<uintptr_t>(W.data) % 16 == 0 &&
+                   (W.ld * elem_size(W.dtype)) % 16 == 0;
+  const int64_t blocks = ceil_div(nwords, 256);
+  if (blocks > 0x7FFFFFFF) return MAO_ERR_UNSUPPORTED;
+  if (P <= 4)
+    vote_update_kernel<4><<<unsigned(blocks), 256, 0, stream>>>(bits, n_workers, stride, nbits, vote, P, T,
+                                                                W.data, W.cols, W.ld, W.dtype, vec, lr);
+  else if (P <= 8)
+    vote_update_kernel<8><<<unsigned(blocks), 256, 0, stream>>>(bits, n_workers, stride, nbits, vote, P, T,
+                                                                W.data, W.cols, W.ld, W.dtype, vec, lr);
+  else
+    vote_update_kernel<kMaxPlanes><<<unsigned(blocks), 256, 0, stream>>>(
+        bits, n_workers, stride, nbits, vote, P, T, W.data, W.cols, W.ld, W.dtype, vec, lr);
+  count_launch();
   return cuda_status(cudaGetLastError());
 }
 

@@ -17,6 +17,11 @@ mao_status sign_pack_launch(const mao_mat& U, uint32_t* bits, cudaStream_t strea
 mao_status sign_int8_launch(const mao_mat& U, int8_t* s, cudaStream_t stream);
 mao_status vote_int8_launch(const int8_t* s, int32_t n_workers, int64_t stride, int64_t n,
                             int8_t* sum, int8_t* sbar, uint32_t* vote, cudaStream_t stream);
+// Vote and Sign-Muon update of W in one launch (the words of vote_launch, then
+// W <- W - lr * (+1 / -1) as update_launch with a vote).
+mao_status vote_update_launch(const uint32_t* bits, int32_t n_workers, int64_t stride,
+                              int64_t nbits, uint32_t* vote, const mao_mat& W, float lr,
+                              cudaStream_t stream);
 mao_status vote_launch(const uint32_t* bits, int32_t n_workers, int64_t stride, int64_t nbits,
                        uint32_t* vote, cudaStream_t stream);
 

@@ -39,8 +39,9 @@ struct SmallEntry {
   const void* src;
   void* out;        // U (may be null)
   uint32_t* bits;   // packed signs (may be null)
-  int64_t src_ld, out_ld;
-  int32_t R, C, src_dt, out_dt;
+  const void* g;    // with momentum: the gradient, and src (M) is updated in place
+  int64_t src_ld, out_ld, g_ld;
+  int32_t R, C, src_dt, out_dt, g_dt, pad;
 };
 
 struct SmallParams {
@@ -48,6 +49,8 @@ struct SmallParams {
   float co[3 * 64];  // (a, b, c) of every iteration
   int32_t steps;
   float eps;
+  int32_t momentum;  // M <- fma(mu, M, G), rounded to M's dtype, first; X = the new M
+  float mu;
 };
 
 struct Layout {
@@ -228,9 +231,16 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
   // squares in a fixed order (the same in every CTA of the cluster): per thread in fp32,
   // then the threads' sums in fp64
   float ss = 0.0f;
+  // with momentum the matrix read is fma(mu, M, G) rounded to M's dtype (the stored new M)
+  auto mom = [&](float mv, float gv) {
+    const float v = __fmaf_rn(p.mu, mv, gv);
+    return e.src_dt == MAO_BF16 ? __bfloat162float(__float2bfloat16_rn(v)) : v;
+  };
   if (!tall) {
     const int es = e.src_dt == MAO_BF16 ? 2 : 4;
-    const bool vec = (reinterpret_cast<uintptr_t>(e.src) % (4 * es) == 0) && (e.src_ld % 4 == 0);
+    const int gs = e.g_dt == MAO_BF16 ? 2 : 4;
+    const bool vec = (reinterpret_cast<uintptr_t>(e.src) % (4 * es) == 0) && (e.src_ld % 4 == 0) &&
+                     (!p.momentum || ((reinterpret_cast<uintptr_t>(e.g) % (4 * gs) == 0) && (e.g_ld % 4 == 0)));
     const int quads = nx / 4;  // the last quad of every row is padding
     constexpr int kU = 8;
     for (int t0 = tid; t0 < m * quads; t0 += kU * kThreads) {
@@ -241,6 +251,11 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
         const int i = t / quads, q = t - i * quads;
         v[u] = t < m * quads ? load4(e.src, int64_t(i) * e.src_ld, 4 * q, n, e.src_dt, vec)
                              : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        if (p.momentum && t < m * quads) {
+          const float4 gv = load4(e.g, int64_t(i) * e.g_ld, 4 * q, n, e.g_dt, vec);
+          // (zeros past n stay zero: fma(mu, 0, 0))
+          v[u] = make_float4(mom(v[u].x, gv.x), mom(v[u].y, gv.y), mom(v[u].z, gv.z), mom(v[u].w, gv.w));
+        }
       }
 #pragma unroll
       for (int u = 0; u < kU; ++u) {
@@ -257,7 +272,8 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
   } else {
     for (int idx = tid; idx < n * e.C; idx += kThreads) {  // source row-major: M[k][i]
       const int k = idx / e.C, i = idx - k * e.C;
-      const float v = load_elem(e.src, int64_t(k) * e.src_ld + i, e.src_dt);
+      float v = load_elem(e.src, int64_t(k) * e.src_ld + i, e.src_dt);
+      if (p.momentum) v = mom(v, load_elem(e.g, int64_t(k) * e.g_ld + i, e.g_dt));
       Xb[0][size_t(i) * nx + k] = v;
       ss = __fmaf_rn(v, v, ss);
     }
@@ -280,7 +296,16 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
   for (int w = 0; w < kThreads / 32; ++w) tot += red[w];
   const float s = float(1.0 / (sqrt(tot) + double(p.eps)));
   // every CTA of the cluster is running, its barriers initialised, before any copy to it
+  // (and with momentum, every CTA has read M before the new M is written over it)
   cluster_barrier();
+  if (p.momentum && crank == 0) {  // the new M, from X[0] (which iteration 0 only reads)
+    void* mo = const_cast<void*>(e.src);
+    for (int idx = tid; idx < m * n; idx += kThreads) {
+      const int i = idx / n, k = idx - i * n;
+      const int64_t at = tall ? int64_t(k) * e.src_ld + i : int64_t(i) * e.src_ld + k;
+      store_elem(mo, at, e.src_dt, Xb[0][size_t(i) * nx + k]);
+    }
+  }
 
   const int xq = (n + 3) / 4, aq = (m + 3) / 4;
   const int pairs = (r1 - r0 + 1) / 2;
@@ -416,7 +441,8 @@ bool ns_small_eligible(const mao_mat* in, const mao_mat* out, int32_t batch, int
 
 mao_status ns_small_run(const mao_mat* in, const mao_mat* out, int32_t batch, int32_t steps,
                         const float* coeffs, int32_t coeff_stride, float eps,
-                        uint32_t* const* sign_bits, cudaStream_t stream) {
+                        uint32_t* const* sign_bits, cudaStream_t stream, const mao_mat* G,
+                        float mu) {
   static std::once_flag attr_once[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return MAO_ERR_CUDA;
@@ -432,6 +458,8 @@ mao_status ns_small_run(const mao_mat* in, const mao_mat* out, int32_t batch, in
     memset(&p, 0, sizeof(p));
     p.steps = steps;
     p.eps = eps;
+    p.momentum = G ? 1 : 0;
+    p.mu = mu;
     for (int it = 0; it < steps; ++it)
       for (int q = 0; q < 3; ++q) p.co[3 * it + q] = coeffs[(coeff_stride ? 3 * it : 0) + q];
     size_t smem = 0;
@@ -447,6 +475,11 @@ mao_status ns_small_run(const mao_mat* in, const mao_mat* out, int32_t batch, in
       e.bits = sign_bits ? sign_bits[b0 + k] : nullptr;
       e.R = int32_t(x.rows);
       e.C = int32_t(x.cols);
+      if (G) {
+        e.g = G[b0 + k].data;
+        e.g_ld = G[b0 + k].ld;
+        e.g_dt = G[b0 + k].dtype;
+      }
       smem = std::max(smem, ns_small_smem_bytes(x.rows, x.cols));
     }
     cudaLaunchConfig_t cfg = {};

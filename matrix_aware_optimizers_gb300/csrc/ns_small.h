@@ -18,10 +18,13 @@ size_t ns_small_smem_bytes(int64_t R, int64_t C);
 // bf16 inputs and outputs, and each matrix's working set within kSmallSmemMax.
 bool ns_small_eligible(const mao_mat* in, const mao_mat* out, int32_t batch, int32_t steps,
                        int32_t compute);
-// The whole Newton–Schulz call (normalisation, every iteration, U and packed signs).
+// The whole Newton–Schulz call (normalisation, every iteration, U and packed signs). With G,
+// the momentum M <- fma(mu, M, G) (rounded to M's dtype) comes first in the same launch:
+// `in` holds M, which the call updates in place, and the iteration starts from the new M.
 mao_status ns_small_run(const mao_mat* in, const mao_mat* out, int32_t batch, int32_t steps,
                         const float* coeffs, int32_t coeff_stride, float eps,
-                        uint32_t* const* sign_bits, cudaStream_t stream);
+                        uint32_t* const* sign_bits, cudaStream_t stream,
+                        const mao_mat* G = nullptr, float mu = 0.0f);
 // Reads and clears the small kernel's error word (a row exchange that timed out).
 mao_status small_read_and_clear_error(cudaStream_t stream);
 

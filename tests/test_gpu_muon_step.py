@@ -113,6 +113,8 @@ def test_muon_step_out_of_place(cuda):
 
 
 @pytest.mark.parametrize("shape,dt,compute", [((64, 128), "f32", "f32"),
+                                              ((128, 64), "f32", "f32"),
+                                              ((96, 160), "bf16", "f32"),
                                               ((300, 500), "bf16", "bf16"),
                                               ((500, 300), "bf16", "bf16")])
 def test_sign_muon_step_equals_composed_calls(cuda, shape, dt, compute):
@@ -150,6 +152,66 @@ def test_sign_muon_step_equals_composed_calls(cuda, shape, dt, compute):
     # and the vote against the oracle's vote of these words
     w = words2[:, :nw].cpu().numpy().view(np.uint32)
     assert np.array_equal(vote1[:nw].cpu().numpy().view(np.uint32), oracle.majority_vote(w, R * C))
+
+
+def test_sign_muon_step_prepared_call(cuda):
+    """A prepared sign_muon_step (arguments marshalled once) called twice gives what two
+    direct calls give, bit for bit."""
+    g = torch.Generator()
+    g.manual_seed(23)
+    Wn, R, C = 4, 64, 128
+    W0 = (torch.randn((R, C), generator=g) * 0.02).to(cuda)
+    M0 = torch.randn((R, C), generator=g).to(cuda)
+    G1 = [torch.randn((R, C), generator=g).to(cuda) for _ in range(Wn)]
+    nw = mao.packed_words(R, C)
+    stride = (nw + 3) // 4 * 4
+    res = []
+    for prepared in (False, True):
+        W, M = W0.clone(), [M0.clone() for _ in range(Wn)]
+        words = torch.zeros((Wn, stride), dtype=torch.int32, device=cuda)
+        vote = torch.zeros(stride, dtype=torch.int32, device=cuda)
+        args = (W, M, G1, words, vote, 0.95, 1e-3, 5, mao.QUINTIC, 1e-7, "f32")
+        if prepared:
+            call = mao.sign_muon_step(*args, prepare=True)
+            call()
+            call()
+        else:
+            mao.sign_muon_step(*args)
+            mao.sign_muon_step(*args)
+        mao.sync_status()
+        res.append((W, M, words, vote))
+    for a, b in zip(res[0], res[1]):
+        for x, y in zip(a if isinstance(a, list) else [a], b if isinstance(b, list) else [b]):
+            assert torch.equal(x, y)
+
+
+def test_sign_muon_step_strided_weights(cuda):
+    """The vote-and-update pass on W rows with padding (ld > cols, 20 columns: words span
+    rows) gives the same W and words as on a contiguous W."""
+    g = torch.Generator()
+    g.manual_seed(22)
+    Wn, R, C = 3, 48, 20
+    base = (torch.randn((R, C), generator=g) * 0.02).to(cuda)
+    Wpad = torch.zeros((R, C + 12), device=cuda)
+    Wpad[:, :C] = base
+    Wv = Wpad[:, :C]
+    Wc = base.clone()
+    M0 = torch.randn((R, C), generator=g).to(cuda)
+    Gs = [torch.randn((R, C), generator=g).to(cuda) for _ in range(Wn)]
+    nw = mao.packed_words(R, C)
+    stride = (nw + 3) // 4 * 4
+    out = []
+    for W in (Wv, Wc):
+        M = [M0.clone() for _ in range(Wn)]
+        words = torch.zeros((Wn, stride), dtype=torch.int32, device=cuda)
+        vote = torch.zeros(stride, dtype=torch.int32, device=cuda)
+        mao.sign_muon_step(W, M, Gs, words, vote, 0.9, 1e-2, 5, mao.QUINTIC, 1e-7, "f32")
+        out.append((words.clone(), vote.clone()))
+    mao.sync_status()
+    assert torch.equal(Wv, Wc)
+    assert torch.equal(Wpad[:, C:], torch.zeros((R, 12), device=cuda))  # padding untouched
+    assert torch.equal(out[0][0][:, :nw], out[1][0][:, :nw])
+    assert torch.equal(out[0][1][:nw], out[1][1][:nw])
 
 
 def test_muon_step_host_equals_muon_step(cuda):
