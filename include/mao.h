@@ -206,7 +206,10 @@ mao_status muon_step_host(const mao_mat* W, const mao_mat* M, const mao_mat* G,
  *                                             signs of U^(m) into words + m*stride
  *   vote   = sign(sum_m S^(m)), ties -> +1    majority_vote_packed
  *   W     <- fmaf(-lr, vote, W)               apply_update with the vote
- * with the results of those calls bit for bit (U itself is not stored).
+ * with the results of those calls bit for bit (U itself is not stored). Launches: with fp32
+ * compute and workers small enough for the one-launch Newton–Schulz kernel, the momentum
+ * runs inside that launch; the vote and the update of W are always one pass. So two
+ * launches for such workers, otherwise the Newton–Schulz launches plus two.
  *   W          one f32 or bf16 matrix (in/out).
  *   M, G       HOST arrays of n_workers matrices of W's shape (M in/out, G read).
  *   words      device, n_workers rows of worker_stride_words >= ceil(R*C/32) uint32 words
