@@ -298,10 +298,11 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
   // every CTA of the cluster is running, its barriers initialised, before any copy to it
   // (and with momentum, every CTA has read M before the new M is written over it)
   cluster_barrier();
-  if (p.momentum && crank == 0) {  // the new M, from X[0] (which iteration 0 only reads)
+  if (p.momentum) {  // the new M from X[0] (which iteration 0 only reads): this CTA's rows
     void* mo = const_cast<void*>(e.src);
-    for (int idx = tid; idx < m * n; idx += kThreads) {
-      const int i = idx / n, k = idx - i * n;
+    const int w = r1 - r0;
+    for (int idx = tid; idx < w * n; idx += kThreads) {
+      const int i = r0 + idx / n, k = idx % n;
       const int64_t at = tall ? int64_t(k) * e.src_ld + i : int64_t(i) * e.src_ld + k;
       store_elem(mo, at, e.src_dt, Xb[0][size_t(i) * nx + k]);
     }
