@@ -431,7 +431,7 @@ enum {
   MAO_PROF_DION_STAGE = 2,     /* B = M + G and its bf16 copy; bf16 copy of Q_prev */
   MAO_PROF_DION_GRAM = 3,      /* P^T P assembled from its tensor-core parts (the products are MAO_PROF_TC) */
   MAO_PROF_DION_CHOL = 4,      /* Cholesky factor and its inverse */
-  MAO_PROF_DION_SPLIT = 5,     /* P split into bf16 parts for the Cholesky QR products (MAO_PROF_TC), and the final P to bf16 */
+  MAO_PROF_DION_SPLIT = 5,     /* unused: P's bf16 parts and the final P are written by the products (MAO_PROF_TC) */
   MAO_PROF_DION_NORM = 6,      /* column norms of R, Q = ColumnNormalize(R) */
   MAO_PROF_NS_SMALL = 7        /* the one-launch fp32 Newton–Schulz of small matrices */
 };
