@@ -251,11 +251,21 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
         const int i = t / quads, q = t - i * quads;
         v[u] = t < m * quads ? load4(e.src, int64_t(i) * e.src_ld, 4 * q, n, e.src_dt, vec)
                              : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-        if (p.momentum && t < m * quads) {
-          const float4 gv = load4(e.g, int64_t(i) * e.g_ld, 4 * q, n, e.g_dt, vec);
-          // (zeros past n stay zero: fma(mu, 0, 0))
-          v[u] = make_float4(mom(v[u].x, gv.x), mom(v[u].y, gv.y), mom(v[u].z, gv.z), mom(v[u].w, gv.w));
+      }
+      if (p.momentum) {  // every unit's G loads issued before any arithmetic
+        float4 gv[kU];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+          const int t = t0 + u * kThreads;
+          const int i = t / quads, q = t - i * quads;
+          gv[u] = t < m * quads ? load4(e.g, int64_t(i) * e.g_ld, 4 * q, n, e.g_dt, vec)
+                                : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
         }
+        // (zeros past n stay zero: fma(mu, 0, 0))
+#pragma unroll
+        for (int u = 0; u < kU; ++u)
+          v[u] = make_float4(mom(v[u].x, gv[u].x), mom(v[u].y, gv[u].y), mom(v[u].z, gv[u].z),
+                             mom(v[u].w, gv[u].w));
       }
 #pragma unroll
       for (int u = 0; u < kU; ++u) {
