@@ -720,25 +720,38 @@ __global__ void __launch_bounds__(kCholThreads, 1) dion_chol_kernel(const __grid
 //   S = hi^T hi + hi^T mid + mid^T hi + hi^T lo + lo^T hi + mid^T mid,
 // summed smallest first in a fixed order, into the lower 32 x 32 blocks the Cholesky kernel
 // reads (entries at or past r are zero). The terms left out (mid^T lo, lo^T mid, lo^T lo) are
-// below 2^-26 of |P|^2.
+// below 2^-26 of |P|^2. mid^T hi is read from its own rows of D (D[ldr + i][k]); lo^T hi,
+// which D holds only as hi^T lo, is read transposed. One block per 32 x 32 block of S
+// (blockIdx.x), four consecutive entries of one row per thread: five 16-byte loads and four
+// scalar ones for four entries.
 __global__ void __launch_bounds__(256) dion_assemble_kernel(const __grid_constant__ DionCommon c) {
   const DionSlot& e = c.slots[blockIdx.y];
-  const int r = c.r, ldr = c.ldr, ldd = 3 * ldr;
-  const int q = blockIdx.x * 256 + threadIdx.x;  // element of the lower blocks
-  const int nb = (r + 31) / 32;
-  if (q >= nb * (nb + 1) / 2 * 1024) return;
-  int b = q >> 10, I = 0;
+  const int r = c.r, ldr = c.ldr;
+  const int64_t ldd = 3 * int64_t(ldr);
+  int b = blockIdx.x, I = 0;
   while (b > I) { b -= I + 1; ++I; }
-  const int J = b, ii = (q >> 5) & 31, kk = q & 31;
-  const int i = 32 * I + ii, k = 32 * J + kk;
-  float v = 0.0f;
+  const int J = b, ii = threadIdx.x >> 3, k4 = 4 * (threadIdx.x & 7);
+  const int i = 32 * I + ii, k = 32 * J + k4;
+  float4 v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
   if (i < r && k < r) {
     const float* D = e.D;
-    const float small = D[size_t(ldr + i) * ldd + ldr + k] + D[size_t(i) * ldd + 2 * ldr + k] +
-                        D[size_t(k) * ldd + 2 * ldr + i];
-    v = (small + (D[size_t(i) * ldd + ldr + k] + D[size_t(k) * ldd + ldr + i])) + D[size_t(i) * ldd + k];
+    const float* Dh = D + i * ldd + k;           // row i (hi): hh | hm | hl
+    const float* Dm = D + (ldr + i) * ldd + k;   // row ldr + i (mid): mh | mm
+    const float4 hh = ld4(Dh), hm = ld4(Dh + ldr), hl = ld4(Dh + 2 * ldr);
+    const float4 mh = ld4(Dm), mm = ld4(Dm + ldr);
+    float lh[4];
+#pragma unroll
+    for (int t = 0; t < 4; ++t) lh[t] = k + t < r ? D[(k + t) * ldd + 2 * ldr + i] : 0.0f;
+    const float a[4] = {hh.x, hh.y, hh.z, hh.w}, bm[4] = {hm.x, hm.y, hm.z, hm.w};
+    const float cl[4] = {hl.x, hl.y, hl.z, hl.w}, dm[4] = {mh.x, mh.y, mh.z, mh.w};
+    const float em[4] = {mm.x, mm.y, mm.z, mm.w};
+    float o[4];
+#pragma unroll
+    for (int t = 0; t < 4; ++t)
+      o[t] = k + t < r ? (((em[t] + cl[t]) + lh[t]) + (bm[t] + dm[t])) + a[t] : 0.0f;
+    v = make_float4(o[0], o[1], o[2], o[3]);
   }
-  blk(e.Sf, I, J)[ii * kLd + kk] = v;
+  *reinterpret_cast<float4*>(blk(e.Sf, I, J) + ii * kLd + k4) = v;
 }
 
 // ------------------------------------------------------ R -> Q = ColumnNormalize(R)
@@ -1133,7 +1146,7 @@ mao_status dion_run(const mao_mat* X, const mao_mat* M, const mao_mat* G, const 
   // 3. Cholesky QR, twice: Ys -> Ys2 -> Pw (bf16; + the caller's fp32 P)
   const size_t chol_smem = chol_bytes(rank);
   const int nbk = int(ceil_div(rank, 32));
-  const unsigned assemble_blocks = unsigned(nbk * (nbk + 1) / 2 * 4);
+  const unsigned assemble_blocks = unsigned(nbk * (nbk + 1) / 2);
   for (int pass = 0; pass < 2; ++pass) {
     // S = P^T P on the tensor cores from P's parts, assembled in the Cholesky's block layout
     mao_status sg = dion_tc(plan, ws, nullptr, 5, 1.0f, stream, pass);
