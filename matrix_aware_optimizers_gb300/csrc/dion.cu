@@ -43,7 +43,6 @@ __device__ unsigned int g_dion_error;  // bit 0: a Cholesky pivot was not positi
 namespace {
 
 constexpr int kMaxRank = 256;
-constexpr int kNormRows = 256;    // rows of R summed by one partial column norm
 constexpr int kSetup = 96;        // table entries written per set-up launch (kernel parameters <= 32 KB)
 constexpr int kCholThreads = 512;
 
@@ -62,12 +61,13 @@ struct DionSlot {
                                     // then after the first Cholesky QR pass)
   float* D;                         // Gram work product [2 ldr][3 ldr] (fp32)
   __nv_bfloat16* Wsp;               // L^-1 split [ldr][3 ldr]: hi | lo | hi (rows j, columns k)
-  float* cn;                        // column norms of R: partials [nchunks][r], then the norms
+  float* cn;                        // column norms of R: partial sums of squares [nrb][ldr]
+                                    // (32 rows each, from the B^T P product), then r norms
   int64_t ldm, ldg, ldx, ldq, ldxo;
   int32_t m, n, ldn;
   int32_t dtm, dtg, dtx;
   int32_t flags_m, flags_x;
-  int32_t nchunks;                  // partial norm chunks of R
+  int32_t nrb;                      // 32-row blocks of R (ceil(n / 32))
   int32_t vec;                      // M and G: bf16/f32 rows that allow 16-byte accesses
   int32_t qvec;                     // Q: 16-byte aligned rows (ldq a multiple of 4)
 };
@@ -756,56 +756,26 @@ __global__ void __launch_bounds__(256) dion_assemble_kernel(const __grid_constan
 
 // ------------------------------------------------------ R -> Q = ColumnNormalize(R)
 
-// Partial column sums of squares of R over rows [chunk*kNormRows, ...); grid
-// (ceil(r / 64), row chunks, slots). Thread (phase, g) takes columns 4 g .. 4 g + 3 of the
-// block's 64 (16-byte loads) and rows phase, phase + 16, ...; the 16 phases are added in a
-// fixed order. Columns at or past r hold no data and are skipped.
-__global__ void __launch_bounds__(256) dion_colnorm_kernel(const __grid_constant__ DionCommon c) {
-  const DionSlot& e = c.slots[blockIdx.z];
-  if (int(blockIdx.y) >= e.nchunks) return;
-  const int g = threadIdx.x & 15, phase = threadIdx.x >> 4;
-  const int j = int(blockIdx.x) * 64 + 4 * g;
-  const int64_t r0 = int64_t(blockIdx.y) * kNormRows;
-  const int64_t r1 = min(int64_t(e.n), r0 + kNormRows);
-  float4 s = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-  if (j < c.r) {
-#pragma unroll 4
-    for (int64_t i = r0 + phase; i < r1; i += 16) {
-      const float4 v = *reinterpret_cast<const float4*>(e.Rf + i * c.ldr + j);
-      s.x = __fmaf_rn(v.x, v.x, s.x);
-      s.y = __fmaf_rn(v.y, v.y, s.y);
-      s.z = __fmaf_rn(v.z, v.z, s.z);
-      s.w = __fmaf_rn(v.w, v.w, s.w);
-    }
-  }
-  __shared__ float4 part[16][16];
-  part[phase][g] = s;
-  __syncthreads();
-  if (phase == 0) {
-    float4 t = part[0][g];
-#pragma unroll
-    for (int q = 1; q < 16; ++q) {
-      t.x += part[q][g].x;
-      t.y += part[q][g].y;
-      t.z += part[q][g].z;
-      t.w += part[q][g].w;
-    }
-    float* out = e.cn + size_t(blockIdx.y) * c.r;
-    const float tv[4] = {t.x, t.y, t.z, t.w};
-#pragma unroll
-    for (int k = 0; k < 4; ++k)
-      if (j + k < c.r) out[j + k] = tv[k];
-  }
-}
-
-// Reciprocal column norms: the partial sums added in chunk order, then 1 / sqrt (0 for a
-// zero column); one block per slot. They go after the partials (e.cn + nchunks * r).
+// Reciprocal column norms: the 32-row partial sums of squares (written by the B^T P
+// product's epilogue) added up, then 1 / sqrt (0 for a zero column); they go after the
+// partials (e.cn + nrb * ldr). Grid (ldr / 32, slots): 32 columns per block, the row
+// blocks dealt to 8 warps (b = warp, warp + 8, ...) and the 8 warps' sums added in a fixed
+// order.
 __global__ void __launch_bounds__(256) dion_norm_kernel(const __grid_constant__ DionCommon c) {
-  const DionSlot& e = c.slots[blockIdx.x];
-  for (int j = threadIdx.x; j < c.r; j += blockDim.x) {
-    float ss = 0.0f;
-    for (int ch = 0; ch < e.nchunks; ++ch) ss += e.cn[size_t(ch) * c.r + j];
-    e.cn[size_t(e.nchunks) * c.r + j] = ss > 0.0f ? 1.0f / sqrtf(ss) : 0.0f;
+  const DionSlot& e = c.slots[blockIdx.y];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int j = int(blockIdx.x) * 32 + lane;
+  float ss = 0.0f;
+#pragma unroll 4
+  for (int b = w; b < e.nrb; b += 8) ss += e.cn[size_t(b) * c.ldr + j];
+  __shared__ float part[8][32];
+  part[w][lane] = ss;
+  __syncthreads();
+  if (w == 0 && j < c.r) {
+    float t = part[0][lane];
+#pragma unroll
+    for (int q = 1; q < 8; ++q) t += part[q][lane];
+    e.cn[size_t(e.nrb) * c.ldr + j] = t > 0.0f ? 1.0f / sqrtf(t) : 0.0f;
   }
 }
 
@@ -818,7 +788,7 @@ __global__ void __launch_bounds__(256) dion_q_kernel(const __grid_constant__ Dio
   const uint32_t u = blockIdx.x * blockDim.x + threadIdx.x;
   if (u >= uint32_t(e.n) * upr) return;
   const uint32_t i = u / upr, j0 = (u - i * upr) * 8;
-  const float* rn = e.cn + size_t(e.nchunks) * c.r;
+  const float* rn = e.cn + size_t(e.nrb) * c.ldr;
   const float4* rp = reinterpret_cast<const float4*>(e.Rf + size_t(i) * c.ldr + j0);
   const float4 r0 = rp[0], r1 = rp[1];
   const float raw[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
@@ -847,7 +817,7 @@ struct DionPlan {
   std::vector<int> input_of;  // slot -> caller's index
   int64_t r = 0, ldr = 0;
   size_t off_slots = 0, off_tables = 0, total = 0;
-  int64_t max_units = 0, max_qunits = 0, max_nchunks = 0;
+  int64_t max_units = 0, max_qunits = 0;
   int64_t max_stage_blocks = 0;  // B units, then Q units, of the largest slot
 };
 
@@ -885,7 +855,7 @@ void make_dion_plan(const mao_mat* X, int32_t batch, int32_t rank, DionPlan& pla
     g.slot0 = slot;
     const size_t c = size_t(g.count), m = size_t(g.m), n = size_t(g.n);
     const size_t ldn = size_t(round_up(g.n, tc::LD_ALIGN));
-    const size_t nch = size_t(ceil_div(g.n, kNormRows));
+    const size_t nrb = size_t(ceil_div(g.n, 32));
     g.off_bw = take(c * m * ldn * 2);
     g.off_qw = take(c * n * ldr * 2);
     g.off_rw = take(c * n * ldr * 2);
@@ -897,7 +867,7 @@ void make_dion_plan(const mao_mat* X, int32_t batch, int32_t rank, DionPlan& pla
     g.off_ys2 = take(c * m * 4 * ldr * 2);
     g.off_d = take(c * 2 * ldr * 3 * ldr * 4);
     g.off_wsp = take(c * ldr * 3 * ldr * 2);
-    g.off_cn = take(c * (nch + 1) * r * 4);
+    g.off_cn = take(c * (nrb * ldr + r) * 4);
     for (int b : mem) plan.input_of.push_back(b);
     slot += g.count;
     plan.max_units = std::max<int64_t>(plan.max_units, g.m * int64_t(ldn / 8));
@@ -905,7 +875,6 @@ void make_dion_plan(const mao_mat* X, int32_t batch, int32_t rank, DionPlan& pla
         plan.max_stage_blocks, ceil_div(g.m * int64_t(ldn / 8), 256 * kStageUnits) +
                                    ceil_div(g.n * int64_t(ldr / 8), 256 * kStageUnits));
     plan.max_qunits = std::max<int64_t>(plan.max_qunits, g.n * int64_t(ldr / 8));
-    plan.max_nchunks = std::max<int64_t>(plan.max_nchunks, int64_t(nch));
     plan.groups.push_back(g);
   }
   plan.total = off;
@@ -1015,9 +984,16 @@ mao_status dion_tc(const DionPlan& plan, uint8_t* ws, const OutEntry* table, int
                       : pass == 0 ? g.off_ys2 : g.off_pw);
         G.out_ld = ld;
         G.out_mstride = rows * ld;
-        G.out_kind = op == 1 || op == 5 ? OUTK_F32 : (op == 0 || pass == 0) ? OUTK_PARTS : OUTK_BF16;
-        st = G.out_kind == OUTK_F32 ? tc_encode_store_map_f32(&G.tmOR, G.out, rows, ld, g.count)
-                                    : tc_encode_store_map(&G.tmOR, G.out, rows, ld, g.count);
+        G.out_kind = op == 1 ? OUTK_F32_COLSQ : op == 5 ? OUTK_F32
+                     : (op == 0 || pass == 0) ? OUTK_PARTS : OUTK_BF16;
+        if (op == 1) {  // R's 32-row column sums of squares into the norm partials
+          const int64_t nrb = ceil_div(g.n, 32);
+          G.colsq = reinterpret_cast<float*>(ws + g.off_cn);
+          G.colsq_mstride = nrb * ldr + r;
+          G.colsq_ld = int32_t(ldr);
+        }
+        st = op == 1 || op == 5 ? tc_encode_store_map_f32(&G.tmOR, G.out, rows, ld, g.count)
+                                : tc_encode_store_map(&G.tmOR, G.out, rows, ld, g.count);
       }
       if (st != MAO_OK) return st;
       G.tiles_m = int32_t(ceil_div(G.M, tc::TILE_M));
@@ -1098,14 +1074,14 @@ mao_status dion_run(const mao_mat* X, const mao_mat* M, const mao_mat* G, const 
       e.Rw = reinterpret_cast<__nv_bfloat16*>(ws + g.off_rw) + size_t(k) * g.n * plan.ldr;
       e.Pw = reinterpret_cast<__nv_bfloat16*>(ws + g.off_pw) + size_t(k) * g.m * plan.ldr;
       e.Rf = reinterpret_cast<float*>(ws + g.off_rf) + size_t(k) * g.n * plan.ldr;
-      e.nchunks = int32_t(ceil_div(g.n, kNormRows));
+      e.nrb = int32_t(ceil_div(g.n, 32));
       const size_t nsb = size_t(plan.ldr / 32) * size_t(plan.ldr / 32 + 1) / 2;
       e.Sf = reinterpret_cast<float*>(ws + g.off_sf) + size_t(k) * nsb * kBlk;
       e.Ys = reinterpret_cast<__nv_bfloat16*>(ws + g.off_ys) + size_t(k) * g.m * 4 * plan.ldr;
       e.Ys2 = reinterpret_cast<__nv_bfloat16*>(ws + g.off_ys2) + size_t(k) * g.m * 4 * plan.ldr;
       e.D = reinterpret_cast<float*>(ws + g.off_d) + size_t(k) * 2 * plan.ldr * 3 * plan.ldr;
       e.Wsp = reinterpret_cast<__nv_bfloat16*>(ws + g.off_wsp) + size_t(k) * plan.ldr * 3 * plan.ldr;
-      e.cn = reinterpret_cast<float*>(ws + g.off_cn) + size_t(k) * (e.nchunks + 1) * rank;
+      e.cn = reinterpret_cast<float*>(ws + g.off_cn) + size_t(k) * (e.nrb * plan.ldr + rank);
       e.ldm = M[b].ld;
       e.ldg = G[b].ld;
       e.ldx = X[b].ld;
@@ -1166,10 +1142,7 @@ mao_status dion_run(const mao_mat* X, const mao_mat* M, const mao_mat* G, const 
   if (st != MAO_OK) return st;
   // 5. Q = ColumnNormalize(R) (caller's Q), bf16 copies of Q and R
   profile_before_launch(stream, MAO_PROF_DION_NORM);
-  dion_colnorm_kernel<<<dim3(unsigned(plan.ldr / 64), unsigned(plan.max_nchunks), nb), 256, 0, stream>>>(c);
-  if (!launched()) return MAO_ERR_CUDA;
-  profile_before_launch(stream, MAO_PROF_DION_NORM);
-  dion_norm_kernel<<<nb, 256, 0, stream>>>(c);
+  dion_norm_kernel<<<dim3(unsigned(plan.ldr / 32), nb), 256, 0, stream>>>(c);
   if (!launched()) return MAO_ERR_CUDA;
   profile_before_launch(stream, MAO_PROF_DION_NORM);
   dion_q_kernel<<<dim3(blocks(plan.max_qunits), nb), 256, 0, stream>>>(c);

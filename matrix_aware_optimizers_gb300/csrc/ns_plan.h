@@ -113,7 +113,7 @@ static_assert(smem_of(OUT_UPDATE_STREAM) <= 232448, "shared memory budget of one
 }  // namespace tc
 
 enum NsStage : int32_t { NS_GRAM = 1, NS_POLY = 2, NS_APPLY = 3 };
-enum OutKind : int32_t { OUTK_BF16 = 0, OUTK_PARTS = 1, OUTK_F32 = 2 };
+enum OutKind : int32_t { OUTK_BF16 = 0, OUTK_PARTS = 1, OUTK_F32 = 2, OUTK_F32_COLSQ = 3 };
 // Products of the same kernel outside Newton–Schulz: an in-place rank-k update of the
 // caller's matrix, out <- out + a * (A B^T), written through the slot's OutEntry.
 constexpr int32_t TC_UPDATE = 4;
@@ -140,9 +140,16 @@ struct TcGroup {
   int32_t out_kind;         // workspace output (NS_APPLY): OUTK_BF16; OUTK_PARTS, the bf16
                             // parts hi | hi | mid | lo of the fp32 values (hi = bf16(x),
                             // mid = bf16(x - hi), lo = bf16(x - hi - mid)), out_ld / 4
-                            // columns apart; OUTK_F32 (tmOR from tc_encode_store_map_f32)
+                            // columns apart; OUTK_F32 (tmOR from tc_encode_store_map_f32);
+                            // OUTK_F32_COLSQ: fp32, and the column sums of squares of every
+                            // 32 rows into colsq (below)
   int32_t orig_cols;        // C of the original matrix (sign-bit indexing)
   float alpha;              // TC_UPDATE: out <- out + alpha (A B^T) for this group's outputs
+  float* colsq;             // OUTK_F32_COLSQ: [count] x colsq_mstride floats; the sum of
+                            // squares of column j over rows 32 b .. 32 b + 31 at
+                            // b * colsq_ld + j (j < colsq_ld)
+  int64_t colsq_mstride;
+  int32_t colsq_ld;
 };
 
 struct TcParams {

@@ -1194,9 +1194,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads(MODE), 1)
           __syncwarp();
         } else if (FINAL) {
           store_final(oe, S, i0, jb, G.M, G.N, G.orig_cols, lane, w);
-        } else if (MODE == OUT_WORKSPACE_KIND && G.out_kind == OUTK_F32) {
+        } else if (MODE == OUT_WORKSPACE_KIND &&
+                   (G.out_kind == OUTK_F32 || G.out_kind == OUTK_F32_COLSQ)) {
           // fp32: two 32-column halves, each through the staging buffer (32 rows of 128
-          // bytes) and a bulk store
+          // bytes) and a bulk store; with OUTK_F32_COLSQ lane c then sums the squares of
+          // column c of the staged rows (one row per step: conflict-free reads)
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             if (lane == 0) bulk_wait_read();
@@ -1211,6 +1213,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads(MODE), 1)
             if (lane == 0) {
               tma_store_3d(&G.tmOR, smem_u32(S), jb + 32 * h, i0, t.z);
               bulk_commit();
+            }
+            if (G.out_kind == OUTK_F32_COLSQ) {
+              const int col = jb + 32 * h + lane;
+              float sq = 0.0f;
+#pragma unroll 8
+              for (int rr = 0; rr < 32; ++rr) {
+                const float x = *reinterpret_cast<const float*>(S + srow(rr, lane >> 2) + 4 * (lane & 3));
+                sq = __fmaf_rn(x, x, sq);
+              }
+              if (col < G.colsq_ld && i0 < G.M)
+                G.colsq[int64_t(t.z) * G.colsq_mstride + int64_t(i0 >> 5) * G.colsq_ld + col] = sq;
             }
             __syncwarp();
           }
