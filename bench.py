@@ -1170,6 +1170,37 @@ def _slab(tensors, device, pin=False):
     return buf, views
 
 
+def _copy_only(K, G_host, G_dsts, W_host, W_srcs, world, scaling, max_over_ranks):
+    """The host link alone: the step's K copies each way (gradient slab in, weight slab out)
+    on two streams at once, with no compute; an e2e figure cannot exceed this rate."""
+    import torch
+    main = torch.cuda.current_stream()
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    c0 = torch.cuda.Event(enable_timing=True)
+    c1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    c0.record(main)
+    s_in.wait_stream(main)
+    s_out.wait_stream(main)
+    for k in range(K):
+        with torch.cuda.stream(s_in):
+            G_dsts[k % len(G_dsts)].copy_(G_host, non_blocking=True)
+        with torch.cuda.stream(s_out):
+            W_host.copy_(W_srcs[k % len(W_srcs)], non_blocking=True)
+    main.wait_stream(s_in)
+    main.wait_stream(s_out)
+    c1.record(main)
+    torch.cuda.synchronize()
+    ms_copy = max_over_ranks(c0.elapsed_time(c1))
+    h2d = G_host.numel() * G_host.element_size()
+    d2h = W_host.numel() * W_host.element_size()
+    return {"value": job_throughput(ms_copy, K, world, scaling),
+            "h2d_gbs": h2d * K / (ms_copy / 1000.0) / 1e9,
+            "d2h_gbs": d2h * K / (ms_copy / 1000.0) / 1e9,
+            "note": "the step's copies alone, both directions at once: the host-link bound "
+                    "of the e2e figure"}
+
+
 def run_e2e(step, K, world, dev, barrier, max_over_ranks, scaling="strong"):
     """The same step with host data: every step copies its gradients from pinned host memory
     (one copy of one contiguous slab) and reads the updated weights back (one copy).
@@ -1250,8 +1281,11 @@ def run_e2e(step, K, world, dev, barrier, max_over_ranks, scaling="strong"):
         for w, v in zip(W_orig, Ws[K % n][1]):
             w.copy_(v)
         step.G, step.W = G_orig, W_orig
+        copy_only = _copy_only(K, G_host, [g[0] for g in Gs], W_host, [w[0] for w in Ws], world,
+                               scaling, max_over_ranks)
         return {"value": job_throughput(ms, K, world, scaling), "unit": "steps/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": K,
+                "copy_only": copy_only,
                 "call": "muon_step_host (C ABI: host gradients in, host weights out)",
                 "copies": "one pinned H2D slab and one D2H slab per step inside each call; %d "
                           "streams in rotation, step k waiting on step k-1's compute event" % n}
@@ -1297,31 +1331,11 @@ def run_e2e(step, K, world, dev, barrier, max_over_ranks, scaling="strong"):
     step.G, step.W = G_orig, W_orig
     for w, v in zip(W_orig, last_views):
         w.copy_(v)
-    # the host link alone: the same K copies each way, concurrently, with no compute; the
-    # e2e figure cannot exceed this rate
-    c0 = torch.cuda.Event(enable_timing=True)
-    c1 = torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize()
-    c0.record(main)
-    s_in.wait_stream(main)
-    s_out.wait_stream(main)
-    for k in range(K):
-        with torch.cuda.stream(s_in):
-            G_dev[k % 2][0].copy_(G_host, non_blocking=True)
-        with torch.cuda.stream(s_out):
-            W_host.copy_(W_bufs[k % len(W_bufs)][0], non_blocking=True)
-    main.wait_stream(s_in)
-    main.wait_stream(s_out)
-    c1.record(main)
-    torch.cuda.synchronize()
-    ms_copy = max_over_ranks(c0.elapsed_time(c1))
+    copy_only = _copy_only(K, G_host, [g[0] for g in G_dev], W_host, [w[0] for w in W_bufs], world,
+                           scaling, max_over_ranks)
     return {"value": job_throughput(ms, K, world, scaling), "unit": "steps/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": K,
-            "copy_only": {"value": job_throughput(ms_copy, K, world, scaling),
-                          "h2d_gbs": h2d * K / (ms_copy / 1000.0) / 1e9,
-                          "d2h_gbs": d2h * K / (ms_copy / 1000.0) / 1e9,
-                          "note": "the step's copies alone, both directions at once: the "
-                                  "host-link bound of the e2e figure"},
+            "copy_only": copy_only,
             "copies": "one pinned H2D slab and one D2H slab per step, on copy streams overlapping "
                       "the neighbouring steps' compute" +
                       ("; two device weight slabs, read one, write the other (%s)"
