@@ -51,7 +51,8 @@ def _check(out, host, X, M, Q, P, mu, lr):
 
 @pytest.mark.parametrize("m,n,r", [(256, 640, 32), (768, 768, 192), (300, 1000, 48),
                                    (1000, 300, 64), (768, 3072, 192), (200, 72, 16),
-                                   (512, 768, 256), (400, 640, 200), (300, 300, 1)])
+                                   (512, 768, 256), (400, 640, 200), (300, 300, 1),
+                                   (96, 20, 8), (20, 96, 8)])
 @pytest.mark.parametrize("mdt,xdt", [("f32", "f32"), ("bf16", "f32")])
 def test_dion_step_parity(cuda, m, n, r, mdt, xdt):
     gen = torch.Generator().manual_seed(80 + m + r)
