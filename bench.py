@@ -15,9 +15,9 @@ every stage through the C ABI of libmao.so.
   python bench.py --sweep-hbm      (each HBM-bound kernel alone on L2-cold buffers)
 
 Default workload: the 12-layer d=768 transformer-shaped Muon step (48 bf16 matrices). On
-one GPU the default run also measures the other four workloads (64x128 Sign-Muon, 4096^2
-Sign-Muon with 8 workers, the 32-layer dense model, the 128-expert MoE) and reports them
-under "per_config" (--no-per-config skips them).
+one GPU the default run also measures the other five workloads (64x128 Sign-Muon, 4096^2
+Sign-Muon with 8 workers, the 32-layer dense model, the 128-expert MoE, the Dion step on the
+12-layer shapes) and reports them under "per_config" (--no-per-config skips them).
 
 Across N GPUs (torchrun) a Muon workload runs layer-wise: every matrix is owned by one rank
 (longest-first on Newton–Schulz flops) and the updated weights are all-gathered; a Sign-Muon
@@ -46,7 +46,7 @@ if ROOT not in sys.path:
 DEFAULT_STEPS = {1: 2000, 2: 400, 3: 60, 4: 10, 5: 100, 6: 400}
 DEFAULT_WARMUP = {1: 20, 2: 10, 3: 5, 4: 3, 5: 5, 6: 10}
 # workloads measured beside the default one (steps, warm-up steps), on one GPU
-PER_CONFIG = {1: (2000, 20), 3: (60, 5), 4: (10, 3), 5: (100, 5)}
+PER_CONFIG = {1: (2000, 20), 3: (60, 5), 4: (10, 3), 5: (100, 5), 6: (300, 10)}
 PARITY_TESTS = {
     1: "tests/test_gpu_steps.py::test_config1_sign_muon_64x128_f32",
     2: "tests/test_gpu_steps.py::test_config2_muon_gpt12_d768_full, "
@@ -1030,11 +1030,16 @@ def per_config_runs(args, dev, local, barrier, max_over_ranks):
         out[str(c)] = {
             "workload": wl.name, "metric": line["metric"], "value": line["value"],
             "unit": "steps/s", "steps": K, "warmup": Wu, "ms_per_step": line["ms_per_step"],
-            "ns_tflops_alg": line["ns_tflops_alg"], "ns_tflops_dense": line["ns_tflops_dense"],
+            "ns_tflops_alg": line.get("ns_tflops_alg"),
+            "ns_tflops_dense": line.get("ns_tflops_dense"),
             "roofline": {k: r.get(k) for k in ("kernel", "bound", "achieved", "peak", "unit",
                                                "frac", "frac_isolated", "peak_source",
-                                               "avg_launch_ms", "avg_launch_ms_isolated")},
+                                               "avg_launch_ms", "avg_launch_ms_isolated",
+                                               "tc_tflops", "tc_share_of_step")
+                         if k in r},
             "stages_ms": line["stages_ms"], "gpu_launches": line["gpu_launches"],
+            **({"kernels_ms_per_step": line["kernels_ms_per_step"]}
+               if "kernels_ms_per_step" in line else {}),
             "clocks": line["clocks"], "parity": PARITY_TESTS[c],
         }
         del step, line
