@@ -154,6 +154,34 @@ def test_sign_muon_step_equals_composed_calls(cuda, shape, dt, compute):
     assert np.array_equal(vote1[:nw].cpu().numpy().view(np.uint32), oracle.majority_vote(w, R * C))
 
 
+@pytest.mark.parametrize("shape,workers,compute", [((520, 264), 4, "bf16"), ((37, 104), 9, "f32"),
+                                                   ((1024, 512), 17, "bf16")])
+def test_sign_muon_step_vote_update_blocks(cuda, shape, workers, compute):
+    """The vote-and-update pass over several blocks of vote words, a partial last block, a
+    last word with padding bits, and more than 8 workers (wider counters): vote and W bit for
+    bit against majority_vote_packed and apply_update of the same words."""
+    g = torch.Generator()
+    g.manual_seed(24 + workers)
+    R, C = shape
+    W0 = (torch.randn(shape, generator=g) * 0.02).to(torch.bfloat16).to(cuda)
+    M0 = torch.randn(shape, generator=g).to(torch.bfloat16).to(cuda)
+    Gs = [torch.randn(shape, generator=g).to(torch.bfloat16).to(cuda) for _ in range(workers)]
+    nw = mao.packed_words(R, C)
+    stride = (nw + 3) // 4 * 4
+    W1, M1 = W0.clone(), [M0.clone() for _ in range(workers)]
+    words = torch.zeros((workers, stride), dtype=torch.int32, device=cuda)
+    vote1 = torch.zeros(stride, dtype=torch.int32, device=cuda)
+    mao.sign_muon_step(W1, M1, Gs, words, vote1, 0.95, 1e-3, 5, mao.QUINTIC, 1e-7, compute)
+    vote2 = mao.majority_vote_packed(words, R * C)
+    W2 = W0.clone()
+    mao.apply_update(W2, 1e-3, vote=vote2)
+    mao.sync_status()
+    assert torch.equal(vote1[:nw], vote2[:nw])
+    assert torch.equal(W1, W2)
+    w = words[:, :nw].cpu().numpy().view(np.uint32)
+    assert np.array_equal(vote1[:nw].cpu().numpy().view(np.uint32), oracle.majority_vote(w, R * C))
+
+
 def test_sign_muon_step_prepared_call(cuda):
     """A prepared sign_muon_step (arguments marshalled once) called twice gives what two
     direct calls give, bit for bit."""
