@@ -208,8 +208,10 @@ mao_status muon_step_host(const mao_mat* W, const mao_mat* M, const mao_mat* G,
  *   W     <- fmaf(-lr, vote, W)               apply_update with the vote
  * with the results of those calls bit for bit (U itself is not stored). Launches: with fp32
  * compute and workers small enough for the one-launch Newton–Schulz kernel, the momentum
- * runs inside that launch; the vote and the update of W are always one pass. So two
- * launches for such workers, otherwise the Newton–Schulz launches plus two.
+ * runs inside that launch; with bf16 compute it runs in the pass that stages the workers'
+ * M for the tensor-core products; the vote and the update of W are always one pass. So two
+ * launches for small fp32 workers, the Newton–Schulz launches plus one with bf16 compute,
+ * plus two otherwise.
  *   W          one f32 or bf16 matrix (in/out).
  *   M, G       HOST arrays of n_workers matrices of W's shape (M in/out, G read).
  *   words      device, n_workers rows of worker_stride_words >= ceil(R*C/32) uint32 words

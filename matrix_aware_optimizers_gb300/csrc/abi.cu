@@ -286,11 +286,17 @@ mao_status sign_muon_step(const mao_mat* W, const mao_mat* M, const mao_mat* G,
   if (compute == MAO_BF16 && device_cc() / 10 != 10) return MAO_ERR_UNSUPPORTED;
   if (workspace_bytes < ns_workspace_size(M, n_workers, compute)) return MAO_ERR_WORKSPACE;
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // small fp32 matrices: the momentum inside the one-launch Newton–Schulz kernel; otherwise
-  // its own launch first. Then the vote and the update of W in one launch.
+  // small fp32 matrices: the momentum inside the one-launch Newton–Schulz kernel; on the
+  // tensor-core path inside the pass that stages M for the products; otherwise its own
+  // launch first. Then the vote and the update of W in one launch.
   if (ns_small_eligible(M, out.data(), n_workers, steps, compute)) {
     st = ns_small_run(M, out.data(), n_workers, steps, coeffs, coeff_stride, eps, bits.data(), s,
                       G, mu);
+  } else if (compute == MAO_BF16) {
+    NsFuse fuse{G, nullptr, mu, 0.0f};
+    fuse.update = false;
+    st = ns_run(M, out.data(), n_workers, steps, coeffs, coeff_stride, eps, compute, bits.data(),
+                workspace, workspace_bytes, s, &fuse);
   } else {
     st = momentum_launch(M, G, n_workers, mu, s);
     if (st == MAO_OK)

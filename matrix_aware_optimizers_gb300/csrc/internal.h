@@ -28,11 +28,13 @@ mao_status vote_launch(const uint32_t* bits, int32_t n_workers, int64_t stride, 
 size_t ns_workspace_size(const mao_mat* X, int32_t batch, int32_t compute);
 // A whole Muon step around Newton–Schulz (muon_step): the staging pass first sets
 // in[b] <- fmaf(mu, in[b], G[b]) (rounded to its dtype) and orthogonalises the new values;
-// the last product then updates out[b] <- out[b] - lr * U in place instead of writing U.
+// with update set, the last product then updates out[b] <- out[b] - lr * U in place instead
+// of writing U (without it the call's outputs are as without the momentum: U or its signs).
 struct NsFuse {
   const mao_mat* G;
   const mao_mat* W_in;  // null: out[b] is updated in place; else out[b] <- W_in[b] - lr * U
   float mu, lr;
+  bool update = true;
 };
 mao_status ns_run(const mao_mat* in, const mao_mat* out, int32_t batch, int32_t steps,
                   const float* coeffs, int32_t coeff_stride, float eps, int32_t compute,

@@ -662,7 +662,8 @@ mao_status ns_run(const mao_mat* in, const mao_mat* out, int32_t batch, int32_t 
   int64_t* prange = reinterpret_cast<int64_t*>(ws + plan.off_prange);
   const bool tcpath = compute == MAO_BF16;
   const int32_t ws_dt = tcpath ? MAO_BF16 : MAO_F32;
-  if (fuse && (!tcpath || sign_bits)) return MAO_ERR_UNSUPPORTED;
+  if (fuse && (!tcpath || (fuse->update && sign_bits))) return MAO_ERR_UNSUPPORTED;
+  const bool upd = fuse && fuse->update;  // the last product updates out in place
   // small fp32 matrices: the whole call in one launch, one cluster per matrix. The choice
   // is made per matrix, so a matrix's result does not depend on the rest of the batch.
   if (!fuse && compute == MAO_F32) {
@@ -689,8 +690,8 @@ mao_status ns_run(const mao_mat* in, const mao_mat* out, int32_t batch, int32_t 
   std::vector<OutEntry> entries(batch);
   for (int b = 0; b < batch; ++b) {
     OutEntry& e = entries[b];
-    e.src = fuse && fuse->W_in ? fuse->W_in[b].data : nullptr;
-    e.src_ld = fuse && fuse->W_in ? fuse->W_in[b].ld : 0;
+    e.src = upd && fuse->W_in ? fuse->W_in[b].data : nullptr;
+    e.src_ld = upd && fuse->W_in ? fuse->W_in[b].ld : 0;
     e.out = out[b].data;
     e.bits = sign_bits ? sign_bits[b] : nullptr;
     e.ld = out[b].ld;
@@ -789,7 +790,7 @@ mao_status ns_run(const mao_mat* in, const mao_mat* out, int32_t batch, int32_t 
       for (int stage = NS_GRAM; stage <= NS_APPLY; ++stage) {
         const mao_status st =
             tcpath ? run_tc_stage(buf, round, stage, cur, first, last, co, scale, table, out_mode,
-                                  stream, fuse ? -fuse->lr : NAN)
+                                  stream, upd ? -fuse->lr : NAN)
                    : run_simt_stage(buf, round, stage, cur, first, last, co, scale, table, stream);
         if (st != MAO_OK) return st;
       }
