@@ -1143,7 +1143,8 @@ def finish_line(args, line, wl, step, K, world, rank, dev, barrier, max_over_ran
         if step.dplan is not None:
             line["e2e"] = run_e2e_dist(step, K, dev, barrier, max_over_ranks)
         else:
-            line["e2e"] = run_e2e(step, K, world, dev, barrier, max_over_ranks, line["scaling"])
+            line["e2e"] = run_e2e(step, K, world, dev, barrier, max_over_ranks, line["scaling"],
+                                  warmup=max(3, args.warmup))
 
     # ---------------- CPU baseline: the oracle on a bounded sample (rank 0, N = 1)
     if world == 1 and rank == 0 and not args.no_cpu_baseline:
@@ -1206,9 +1207,10 @@ def _copy_only(K, G_host, G_dsts, W_host, W_srcs, world, scaling, max_over_ranks
                     "of the e2e figure"}
 
 
-def run_e2e(step, K, world, dev, barrier, max_over_ranks, scaling="strong"):
+def run_e2e(step, K, world, dev, barrier, max_over_ranks, scaling="strong", warmup=3):
     """The same step with host data: every step copies its gradients from pinned host memory
-    (one copy of one contiguous slab) and reads the updated weights back (one copy).
+    (one copy of one contiguous slab) and reads the updated weights back (one copy). The
+    first `warmup` steps of the sequence are run untimed; K are timed.
 
     Copies run on their own streams and overlap other work where the data allow it: the
     gradients of step k+1 go into the second of two device slabs while step k computes, and
@@ -1267,23 +1269,30 @@ def run_e2e(step, K, world, dev, barrier, max_over_ranks, scaling="strong"):
         for st_, ev in zip(streams, done):
             ev.record(st_)
         torch.cuda.synchronize()
+
+        def host_steps(k0, k1):
+            for st_ in streams:
+                st_.wait_stream(main)
+            for k in range(k0, k1):
+                b = k % n
+                step.mao.muon_step_host(
+                    Ws[b][1], step.M, Gs[b][1], wl.mu, wl.lr, G_host, Gs[b][0], W_hosts[b],
+                    Ws[(k + 1) % n][0], wl.steps, wl.coeffs, wl.eps, wl.compute, ws=step.ws,
+                    W_out=Ws[(k + 1) % n][1], stream=streams[b],
+                    wait_event=done[(k - 1) % n] if k > 0 else None, record_event=done[b])
+            for st_ in streams:
+                main.wait_stream(st_)
+
+        host_steps(0, warmup)
+        torch.cuda.synchronize()
+        barrier()
         e0.record(main)
-        for st_ in streams:
-            st_.wait_stream(main)
-        for k in range(K):
-            b = k % n
-            step.mao.muon_step_host(
-                Ws[b][1], step.M, Gs[b][1], wl.mu, wl.lr, G_host, Gs[b][0], W_hosts[b],
-                Ws[(k + 1) % n][0], wl.steps, wl.coeffs, wl.eps, wl.compute, ws=step.ws,
-                W_out=Ws[(k + 1) % n][1], stream=streams[b],
-                wait_event=done[(k - 1) % n] if k > 0 else None, record_event=done[b])
-        for st_ in streams:
-            main.wait_stream(st_)
+        host_steps(warmup, warmup + K)
         e1.record(main)
         torch.cuda.synchronize()
         barrier()
         ms = max_over_ranks(e0.elapsed_time(e1))
-        for w, v in zip(W_orig, Ws[K % n][1]):
+        for w, v in zip(W_orig, Ws[(warmup + K) % n][1]):
             w.copy_(v)
         step.G, step.W = G_orig, W_orig
         copy_only = _copy_only(K, G_host, [g[0] for g in Gs], W_host, [w[0] for w in Ws], world,
@@ -1294,8 +1303,12 @@ def run_e2e(step, K, world, dev, barrier, max_over_ranks, scaling="strong"):
                 "call": "muon_step_host (C ABI: host gradients in, host weights out)",
                 "copies": "one pinned H2D slab and one D2H slab per step inside each call; %d "
                           "streams in rotation, step k waiting on step k-1's compute event" % n}
-    e0.record(main)
-    for k in range(K):
+    def steps(k0, k1):
+        for k in range(k0, k1):
+            one_step(k)
+
+    def one_step(k):
+        nonlocal W_src
         b = k % 2
         s_in.wait_event(g_free[b])            # step k-2 has read this slab
         with torch.cuda.stream(s_in):
@@ -1327,12 +1340,19 @@ def run_e2e(step, K, world, dev, barrier, max_over_ranks, scaling="strong"):
         w_read.record(s_out)
         if fused:
             w_read_slab[1 - k % 2].record(s_out)
+
+    steps(0, warmup)
+    main.wait_event(w_read)
+    torch.cuda.synchronize()
+    barrier()
+    e0.record(main)
+    steps(warmup, warmup + K)
     main.wait_event(w_read)
     e1.record(main)
     torch.cuda.synchronize()
     barrier()
     ms = max_over_ranks(e0.elapsed_time(e1))
-    last_views = W_bufs[K % 2][1] if fused else W_views
+    last_views = W_bufs[(warmup + K) % 2][1] if fused else W_views
     step.G, step.W = G_orig, W_orig
     for w, v in zip(W_orig, last_views):
         w.copy_(v)
