@@ -337,8 +337,8 @@ __global__ void __launch_bounds__(32) finalize_scale_kernel(const float* partial
 // ------------------------------------------------------- fp32 FFMA product path
 
 constexpr int kSimtMaxGroups = 8;
-constexpr int kSimtTile = 64;
-constexpr int kSimtK = 16;
+constexpr int kSimtTile = 128;
+constexpr int kSimtK = 8;
 
 struct SimtGroup {
   const float* a;
@@ -360,7 +360,40 @@ struct SimtParams {
   const OutEntry* out_table;
 };
 
-// D(i, j) = sum_k A(i, k) B(j, k) on a 64x64 tile, 4x4 outputs per thread, fp32 FFMA.
+// One operand's slice of a k-step: kSimtTile rows (i) x kSimtK columns (k) of
+// src(i, k) = src[i*si + k*sk], four elements per thread. When k is the contiguous index
+// (sk == 1) eight neighbouring threads read eight consecutive k of one row, otherwise 128
+// neighbouring threads read 128 consecutive rows of one k, so the loads coalesce either
+// way. Outside [0, rows) x [0, K) the values are zero.
+struct SimtSlice {
+  float v[4];
+};
+__device__ __forceinline__ void simt_load(SimtSlice& t, const float* src, int64_t si, int64_t sk,
+                                          int r0, int rows, int k0, int K) {
+  const bool kfast = sk == 1;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int e = threadIdx.x + 256 * q;
+    const int ii = kfast ? e >> 3 : e & (kSimtTile - 1);
+    const int kk = kfast ? e & 7 : e >> 7;
+    const int gi = r0 + ii, gk = k0 + kk;
+    t.v[q] = (gi < rows && gk < K) ? src[int64_t(gi) * si + int64_t(gk) * sk] : 0.0f;
+  }
+}
+__device__ __forceinline__ void simt_store(const SimtSlice& t, float (*S)[kSimtTile + 4], bool kfast) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int e = threadIdx.x + 256 * q;
+    const int ii = kfast ? e >> 3 : e & (kSimtTile - 1);
+    const int kk = kfast ? e & 7 : e >> 7;
+    S[kk][ii] = t.v[q];
+  }
+}
+
+// D(i, j) = sum_k A(i, k) B(j, k) on a 128 x 128 tile, fp32 FFMA: thread (ty, tx) of 16 x 16
+// holds rows ty*4 + {0..3} and 64 + ty*4 + {0..3}, columns tx*4 + {0..3} and
+// 64 + tx*4 + {0..3} (conflict-free 16-byte shared-memory reads); the next k-step's slices
+// are loaded into registers while the current one is multiplied.
 __global__ void __launch_bounds__(256) ns_simt_kernel(const __grid_constant__ SimtParams p) {
   int gi = 0;
   while (gi + 1 < p.ngroups && p.g[gi + 1].block_begin <= int64_t(blockIdx.x)) ++gi;
@@ -375,36 +408,38 @@ __global__ void __launch_bounds__(256) ns_simt_kernel(const __grid_constant__ Si
   const float* A = G.a + int64_t(z) * G.a_ms;
   const float* B = G.b + int64_t(z) * G.b_ms;
 
-  __shared__ float As[kSimtK][kSimtTile + 4];
-  __shared__ float Bs[kSimtK][kSimtTile + 4];
+  __shared__ __align__(16) float As[kSimtK][kSimtTile + 4];
+  __shared__ __align__(16) float Bs[kSimtK][kSimtTile + 4];
   const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
-  float acc[4][4];
+  float acc[8][8];
 #pragma unroll
-  for (int i = 0; i < 4; ++i)
+  for (int i = 0; i < 8; ++i)
 #pragma unroll
-    for (int j = 0; j < 4; ++j) acc[i][j] = 0.0f;
+    for (int j = 0; j < 8; ++j) acc[i][j] = 0.0f;
 
+  SimtSlice ta, tb;
+  simt_load(ta, A, G.a_si, G.a_sk, row0, G.M, 0, G.K);
+  simt_load(tb, B, G.b_sj, G.b_sk, col0, G.N, 0, G.K);
   for (int k0 = 0; k0 < G.K; k0 += kSimtK) {
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int idx = threadIdx.x + 256 * q;
-      const int ii = idx & 63, kk = idx >> 6;
-      const int gi_ = row0 + ii, gj = col0 + ii, gk = k0 + kk;
-      As[kk][ii] = (gi_ < G.M && gk < G.K) ? A[int64_t(gi_) * G.a_si + int64_t(gk) * G.a_sk] : 0.0f;
-      Bs[kk][ii] = (gj < G.N && gk < G.K) ? B[int64_t(gj) * G.b_sj + int64_t(gk) * G.b_sk] : 0.0f;
-    }
+    simt_store(ta, As, G.a_sk == 1);
+    simt_store(tb, Bs, G.b_sk == 1);
     __syncthreads();
+    if (k0 + kSimtK < G.K) {
+      simt_load(ta, A, G.a_si, G.a_sk, row0, G.M, k0 + kSimtK, G.K);
+      simt_load(tb, B, G.b_sj, G.b_sk, col0, G.N, k0 + kSimtK, G.K);
+    }
 #pragma unroll
     for (int kk = 0; kk < kSimtK; ++kk) {
-      float av[4], bv[4];
+      const float4 a0 = *reinterpret_cast<const float4*>(&As[kk][ty * 4]);
+      const float4 a1 = *reinterpret_cast<const float4*>(&As[kk][64 + ty * 4]);
+      const float4 b0 = *reinterpret_cast<const float4*>(&Bs[kk][tx * 4]);
+      const float4 b1 = *reinterpret_cast<const float4*>(&Bs[kk][64 + tx * 4]);
+      const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+      const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
 #pragma unroll
-      for (int i = 0; i < 4; ++i) av[i] = As[kk][ty * 4 + i];
+      for (int i = 0; i < 8; ++i)
 #pragma unroll
-      for (int j = 0; j < 4; ++j) bv[j] = Bs[kk][tx * 4 + j];
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) acc[i][j] = __fmaf_rn(av[i], bv[j], acc[i][j]);
+        for (int j = 0; j < 8; ++j) acc[i][j] = __fmaf_rn(av[i], bv[j], acc[i][j]);
     }
     __syncthreads();
   }
@@ -414,12 +449,12 @@ __global__ void __launch_bounds__(256) ns_simt_kernel(const __grid_constant__ Si
   float* out = G.out + int64_t(z) * G.out_ms;
   const float* res = G.res + int64_t(z) * G.res_ms;
 #pragma unroll
-  for (int ii = 0; ii < 4; ++ii) {
-    const int i = row0 + ty * 4 + ii;
+  for (int ii = 0; ii < 8; ++ii) {
+    const int i = row0 + (ii < 4 ? ty * 4 + ii : 64 + ty * 4 + ii - 4);
     if (i >= G.M) continue;
 #pragma unroll
-    for (int jj = 0; jj < 4; ++jj) {
-      const int j = col0 + tx * 4 + jj;
+    for (int jj = 0; jj < 8; ++jj) {
+      const int j = col0 + (jj < 4 ? tx * 4 + jj : 64 + tx * 4 + jj - 4);
       if (j >= G.N) continue;
       const float v = acc[ii][jj];
       if (p.stage == NS_GRAM || p.stage == NS_POLY) {
@@ -432,7 +467,7 @@ __global__ void __launch_bounds__(256) ns_simt_kernel(const __grid_constant__ Si
       } else {
         const float w = s * v;
         if (G.final_out) {
-          const OutEntry e = p.out_table[slot];
+          const OutEntry& e = p.out_table[slot];
           if (e.out) store_elem(e.out, int64_t(i) * e.ld + j, e.dtype, w);
           if (e.bits && !(w < 0.0f)) {
             const int64_t k = int64_t(i) * G.orig_cols + j;
