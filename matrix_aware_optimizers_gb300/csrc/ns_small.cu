@@ -3,8 +3,8 @@
 //
 // For a matrix whose working set (X twice, A, and this CTA's rows of B) fits in one SM's
 // shared memory, the per-product launches of the general path cost more than the
-// arithmetic. Here a cluster of eight CTAs owns one matrix for the whole call: every CTA
-// holds all of X and A in shared memory and computes one eighth of the rows of each
+// arithmetic. Here a cluster of sixteen CTAs owns one matrix for the whole call: every CTA
+// holds all of X and A in shared memory and computes one sixteenth of the rows of each
 // product ("分散ニュートン・シュルツ" of the Megatron Muon article: three products per
 // iteration; the iteration of the Sign-Muon summary, §2 "Mecanismo Central" item 1):
 //   A  = s^2 X X^T            rows of this CTA, sent to every other CTA
@@ -14,11 +14,11 @@
 // of the normalisation as the general path). A CTA sends its rows with one bulk
 // asynchronous copy per peer (shared memory to the peer's shared memory), whose bytes
 // complete on the peer's barrier for that exchange; each CTA waits on its own barrier for
-// the other seven CTAs' rows. No buffer is written while a peer may still read it: a CTA
+// the other fifteen CTAs' rows. No buffer is written while a peer may still read it: a CTA
 // sends its A rows of the next iteration only after it holds every CTA's X rows of that
 // iteration, which each CTA sends only after it has used the current A, and the X buffers
 // alternate. Every CTA computes the Frobenius norm itself from its full copy in the same
-// fixed order, so all eight hold the same s. At the end each CTA writes one eighth of
+// fixed order, so all sixteen hold the same s. At the end each CTA writes one sixteenth of
 // U (in the matrix's own orientation) and of the packed signs, whole words, so the sign
 // buffer needs no clearing. All arithmetic is fp32 FFMA with one accumulation chain per
 // output, in k order.
@@ -32,7 +32,7 @@
 namespace mao {
 namespace {
 
-constexpr int kCluster = 8;
+constexpr int kCluster = 16;  // a non-portable cluster size (at most 8 is portable)
 constexpr int kThreads = 256;
 
 struct SmallEntry {
@@ -380,7 +380,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
   // every CTA has received all of its rows before any CTA leaves
   cluster_barrier();
 
-  // ---- outputs from the final X (complete in every CTA): one eighth each
+  // ---- outputs from the final X (complete in every CTA): one sixteenth each
   const float* Xf = Xb[p.steps & 1];
   const int N = e.R * e.C;  // below 2^31: the working set fits one SM
   auto value = [&](int k) {  // entry k of U in its own row-major orientation
@@ -439,9 +439,46 @@ size_t ns_small_smem_bytes(int64_t R, int64_t C) {
   return smem_floats(layout_of(int(R), int(C))) * sizeof(float);
 }
 
+// The kernel's attributes, set once per device: its shared memory and the non-portable
+// cluster size; and whether a cluster of kCluster such CTAs can be placed at all (where it
+// cannot, no matrix takes this path and the general one serves them).
+bool small_kernel_ready() {
+  static std::once_flag once[64];
+  static bool ok[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  std::call_once(once[dev & 63], [&] {
+    bool good =
+        cudaFuncSetAttribute(ns_small_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
+            cudaSuccess &&
+        cudaFuncSetAttribute(ns_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             int(kSmallSmemMax)) == cudaSuccess;
+    if (good) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(unsigned(kCluster));
+      cfg.blockDim = dim3(unsigned(kThreads));
+      cfg.dynamicSmemBytes = kSmallSmemMax;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = kCluster;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      int clusters = 0;
+      good = cudaOccupancyMaxActiveClusters(&clusters, ns_small_kernel, &cfg) == cudaSuccess &&
+             clusters > 0;
+    }
+    cudaGetLastError();  // a refused query leaves no error behind for the caller
+    ok[dev & 63] = good;
+  });
+  return ok[dev & 63];
+}
+
 bool ns_small_eligible(const mao_mat* in, const mao_mat* out, int32_t batch, int32_t steps,
                        int32_t compute) {
   if (compute != MAO_F32 || steps < 1 || steps > 64) return false;
+  if (!small_kernel_ready()) return false;
   for (int b = 0; b < batch; ++b) {
     if (in[b].dtype != MAO_F32 && in[b].dtype != MAO_BF16) return false;
     if (ns_small_smem_bytes(in[b].rows, in[b].cols) > kSmallSmemMax) return false;
@@ -454,15 +491,7 @@ mao_status ns_small_run(const mao_mat* in, const mao_mat* out, int32_t batch, in
                         const float* coeffs, int32_t coeff_stride, float eps,
                         uint32_t* const* sign_bits, cudaStream_t stream, const mao_mat* G,
                         float mu) {
-  static std::once_flag attr_once[64];
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return MAO_ERR_CUDA;
-  cudaError_t attr_err = cudaSuccess;
-  std::call_once(attr_once[dev & 63], [&] {
-    attr_err = cudaFuncSetAttribute(ns_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    int(kSmallSmemMax));
-  });
-  if (attr_err != cudaSuccess) return MAO_ERR_CUDA;
+  if (!small_kernel_ready()) return MAO_ERR_UNSUPPORTED;
   for (int b0 = 0; b0 < batch; b0 += kSmallMaxPerLaunch) {
     const int nb = std::min(batch - b0, kSmallMaxPerLaunch);
     SmallParams p;
