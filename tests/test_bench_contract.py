@@ -69,3 +69,15 @@ def test_both_arms_describe_the_same_config():
     assert d["config"] == json.loads(json.dumps(bench.config_block(wl, "bits", False, None, 1)))
     assert d["step_fraction"] == 1.0
     assert abs(d["value"] * d["ms_per_step"] / 1000.0 - 1.0) < 0.05
+
+
+def test_per_config_entries_name_existing_parity_tests():
+    """Every workload the default line measures under per_config names the GPU parity tests
+    that check it, and those tests exist."""
+    sys.path.insert(0, ROOT)
+    import bench
+    src = open(os.path.join(ROOT, "tests", "test_gpu_steps.py")).read()
+    assert set(bench.PER_CONFIG) <= set(bench.PARITY_TESTS)
+    for c, names in bench.PARITY_TESTS.items():
+        for name in names.replace("tests/test_gpu_steps.py::", "").split(","):
+            assert "def %s(" % name.strip() in src, (c, name)
